@@ -1,0 +1,254 @@
+"""Seeded synthetic inputs for the MoE FFN layer with SelectedSoftmax routing.
+
+This module only draws random numbers and encodes them in the storage formats
+the layer consumes (fp32, bf16 bit patterns, Q8_0 blocks).  It holds none of
+the layer's arithmetic: no router projection, no top-k, no softmax, no expert
+FFN.  Both the CUDA path and the CPU oracle read the bytes produced here.
+
+Shapes follow the two backbones described on the source pages:
+  * ZONOS2 ("zonos2.cpp internals", §Model architecture): n_embd 2048,
+    16 experts, top-1.
+  * ZONOS3-Mini ("New Community Model: ZONOS3-Mini (Zyphra) - #1271",
+    §Summary): width 1024, top-2 of 64 experts on layers 1-10.
+Expert ffn widths (512, 2816) are not printed on the pages; they are the
+workload definitions of this library's benchmark suite.
+
+Value recipe (all seeded with numpy.random.default_rng(seed)):
+  x ~ N(0, 1); W_r, W_g, W_u ~ N(0, 1/d) (standard deviation 1/sqrt(fan_in));
+  W_d ~ N(0, 1/F); selection bias ~ N(0, bias_sd), or, for the Zipf workload,
+  b_e = ZIPF_ALPHA * log(p_rank(e)) with p_r proportional to r^-1.1 and ranks
+  assigned to experts by a seeded permutation.  Draws are made in float32 and
+  rounded to nearest-even bf16 where the workload is bf16.  Q8_0 blocks hold
+  32 consecutive values along the contiguous (reduction) axis: an fp16 scale
+  max|w|/127 followed by 32 int8 values round-half-away-from-zero(w/scale).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+F32, BF16, Q8_0 = 0, 1, 2
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0"}
+Q8_0_BLOCK = 32
+Q8_0_BLOCK_BYTES = 34
+
+# Scale on log(p_rank) for the Zipf-skewed workload.  With router logits close
+# to N(0, 1), 0.65 puts ~25% of the top-2 assignments on the busiest expert,
+# the head share of Zipf(s=1.1) over 64 ranks; the tail falls off faster than
+# Zipf.  The achieved per-expert counts are reported with every measurement.
+ZIPF_S = 1.1
+ZIPF_ALPHA = 0.65
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    d: int
+    E: int
+    k: int
+    F: int
+    act_dtype: int      # dtype of x and W_r (F32 or BF16)
+    w_dtype: int        # dtype of expert weights (F32, BF16, Q8_0)
+    bias: str           # "normal" or "zipf"
+    bias_sd: float
+    layers: int         # layers run back to back in one benchmark step
+    description: str
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload(
+        "tiny_fp32", T=8, d=64, E=8, k=2, F=128, act_dtype=F32, w_dtype=F32,
+        bias="normal", bias_sd=0.1, layers=1,
+        description="tiny fp32 MoE layer, T=8 d=64 E=8 top-2 F=128"),
+    "zonos3_mini_decode": Workload(
+        "zonos3_mini_decode", T=128, d=1024, E=64, k=2, F=512, act_dtype=BF16,
+        w_dtype=BF16, bias="normal", bias_sd=0.5, layers=10,
+        description="ZONOS3-Mini-shaped decode step: 128 rows (64 streams x "
+                    "speaker-CFG pair), d=1024, E=64, top-2, F=512, bf16, "
+                    "10 MoE layers back to back"),
+    "zonos2_decode": Workload(
+        "zonos2_decode", T=64, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=BF16, bias="normal", bias_sd=0.1, layers=28,
+        description="ZONOS2-shaped decode step: d=2048, E=16, top-1, F=2816, "
+                    "bf16, T in {1, 8, 64}, 28-layer weight rotation"),
+    "zonos3_mini_prefill": Workload(
+        "zonos3_mini_prefill", T=8192, d=1024, E=64, k=2, F=512, act_dtype=BF16,
+        w_dtype=BF16, bias="zipf", bias_sd=0.0, layers=1,
+        description="ZONOS3-Mini-shaped prefill: T=8192, d=1024, E=64, top-2, "
+                    "F=512, bf16, Zipf(1.1)-skewed expert loads"),
+    "zonos2_prefill_q8": Workload(
+        "zonos2_prefill_q8", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q8_0, bias="normal", bias_sd=0.1, layers=1,
+        description="ZONOS2-shaped prefill with Q8_0 experts: T=4096, d=2048, "
+                    "E=16, top-1, F=2816, bf16 activations and router"),
+}
+
+
+@dataclasses.dataclass
+class Layer:
+    """One MoE layer's inputs as raw storage arrays (host numpy)."""
+    T: int
+    d: int
+    E: int
+    k: int
+    F: int
+    act_dtype: int
+    w_dtype: int
+    x: np.ndarray        # [T, d] float32 or uint16 (bf16 bits)
+    w_router: np.ndarray  # [E, d] same storage as x
+    bias: np.ndarray     # [E] float32
+    w_gate: np.ndarray   # [E, F, d] (Q8_0: uint8 [E, F, d/32, 34])
+    w_up: np.ndarray     # [E, F, d]
+    w_down: np.ndarray   # [E, d, F] (Q8_0: uint8 [E, d, F/32, 34])
+
+
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); return bits."""
+    a32 = np.ascontiguousarray(a, dtype=np.float32)
+    u = a32.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def q8_0_quantize(w) -> np.ndarray:
+    """Encode w[..., K] (K % 32 == 0) as Q8_0 blocks: uint8 [..., K/32, 34].
+
+    Block layout: bytes 0-1 the fp16 scale (little endian), bytes 2-33 the
+    int8 values.  scale = max|w|/127 (float32, stored rounded to fp16);
+    q = round-half-away-from-zero(w / scale) clamped to [-127, 127]; an
+    all-zero block has scale 0 and q 0.
+    """
+    w = np.asarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    if K % Q8_0_BLOCK:
+        raise ValueError("Q8_0 needs the contiguous axis to be a multiple of 32")
+    blocks = w.reshape(w.shape[:-1] + (K // Q8_0_BLOCK, Q8_0_BLOCK))
+    amax = np.abs(blocks).max(axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    inv = np.zeros_like(scale)
+    nz = scale > 0
+    inv[nz] = np.float32(1.0) / scale[nz]
+    v = blocks * inv[..., None]
+    q = np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+    q = np.clip(q, -127, 127).astype(np.int8)
+    out = np.empty(blocks.shape[:-1] + (Q8_0_BLOCK_BYTES,), dtype=np.uint8)
+    out[..., 0:2] = scale.astype(np.float16).view(np.uint8).reshape(scale.shape + (2,))
+    out[..., 2:] = q.view(np.uint8)
+    return out
+
+
+def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
+    if dtype == F32:
+        return np.ascontiguousarray(a, dtype=np.float32)
+    if dtype == BF16:
+        return f32_to_bf16_bits(a)
+    if dtype == Q8_0:
+        return q8_0_quantize(a)
+    raise ValueError(dtype)
+
+
+def zipf_bias(E: int, rng: np.random.Generator, s: float = ZIPF_S,
+              alpha: float = ZIPF_ALPHA) -> np.ndarray:
+    """Selection bias whose log-shares follow Zipf(s) over a seeded ranking."""
+    ranks = np.arange(1, E + 1, dtype=np.float64)
+    p = ranks ** (-s)
+    p /= p.sum()
+    order = rng.permutation(E)          # order[r] = expert holding rank r+1
+    b = np.empty(E, dtype=np.float64)
+    b[order] = alpha * np.log(p)
+    return b.astype(np.float32)
+
+
+def make_layer(w: Workload, seed: int, T: Optional[int] = None,
+               d: Optional[int] = None, E: Optional[int] = None,
+               k: Optional[int] = None, F: Optional[int] = None) -> Layer:
+    """Draw one layer's inputs for workload ``w`` (sizes may be overridden)."""
+    T = w.T if T is None else T
+    d = w.d if d is None else d
+    E = w.E if E is None else E
+    k = w.k if k is None else k
+    F = w.F if F is None else F
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    x = rng.standard_normal((T, d), dtype=f32)
+    wr = rng.standard_normal((E, d), dtype=f32) * f32(1.0 / math.sqrt(d))
+    if w.bias == "zipf":
+        bias = zipf_bias(E, rng)
+    else:
+        bias = (rng.standard_normal(E, dtype=f32) * f32(w.bias_sd)).astype(f32)
+    wg = rng.standard_normal((E, F, d), dtype=f32) * f32(1.0 / math.sqrt(d))
+    wu = rng.standard_normal((E, F, d), dtype=f32) * f32(1.0 / math.sqrt(d))
+    wd = rng.standard_normal((E, d, F), dtype=f32) * f32(1.0 / math.sqrt(F))
+    return Layer(T=T, d=d, E=E, k=k, F=F, act_dtype=w.act_dtype,
+                 w_dtype=w.w_dtype, x=_encode(x, w.act_dtype),
+                 w_router=_encode(wr, w.act_dtype), bias=bias,
+                 w_gate=_encode(wg, w.w_dtype), w_up=_encode(wu, w.w_dtype),
+                 w_down=_encode(wd, w.w_dtype))
+
+
+def make_custom_layer(seed: int, T: int, d: int, E: int, k: int, F: int,
+                      act_dtype: int, w_dtype: int, bias_sd: float = 0.1,
+                      bias: str = "normal") -> Layer:
+    """A layer with arbitrary sizes (edge-case and ragged-size tests)."""
+    w = Workload("custom", T, d, E, k, F, act_dtype, w_dtype, bias, bias_sd, 1, "")
+    return make_layer(w, seed)
+
+
+def weight_bytes_per_expert(d: int, F: int, w_dtype: int) -> int:
+    """Storage bytes of one expert's W_g + W_u + W_d in ``w_dtype``."""
+    n = 3 * d * F
+    if w_dtype == F32:
+        return 4 * n
+    if w_dtype == BF16:
+        return 2 * n
+    return n // Q8_0_BLOCK * Q8_0_BLOCK_BYTES
+
+
+def act_bytes(dtype: int) -> int:
+    return 4 if dtype == F32 else 2
+
+
+# ---------------------------------------------------------------- device draws
+def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = None,
+                      device="cuda"):
+    """Draw ``layers`` independent bf16 layers directly in device memory.
+
+    Used for benchmark stacks whose weights (GBs) are too large to draw on the
+    host.  Same distributions as make_layer, drawn with torch's seeded device
+    generator; returns a list of dicts of torch tensors (bf16 stored as
+    torch.bfloat16).  Only bf16 workloads are supported here.
+    """
+    import torch
+    if w.w_dtype != BF16 or w.act_dtype != BF16:
+        raise ValueError("device stacks are bf16 only")
+    T = w.T if T is None else T
+    g = torch.Generator(device=device)
+    out = []
+    for layer in range(layers):
+        g.manual_seed(seed * 1000003 + layer)
+
+        def rn(*shape, sd=1.0):
+            t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+            return (t * sd).to(torch.bfloat16)
+        d, E, F = w.d, w.E, w.F
+        x = rn(T, d)
+        wr = rn(E, d, sd=1.0 / math.sqrt(d))
+        if w.bias == "zipf":
+            rng = np.random.default_rng(seed * 1000003 + layer)
+            b = torch.from_numpy(zipf_bias(E, rng)).to(device)
+        else:
+            b = torch.randn(E, generator=g, device=device, dtype=torch.float32) * w.bias_sd
+        wg = rn(E, F, d, sd=1.0 / math.sqrt(d))
+        wu = rn(E, F, d, sd=1.0 / math.sqrt(d))
+        wd = rn(E, d, F, sd=1.0 / math.sqrt(F))
+        out.append(dict(x=x, w_router=wr, bias=b, w_gate=wg, w_up=wu, w_down=wd))
+    return out

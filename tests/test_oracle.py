@@ -1,0 +1,302 @@
+"""Pins of the CPU oracle against what the definition and mathematics fix.
+
+Definition: SelectedSoftmax routing ("New Community Model: ZONOS3-Mini
+(Zyphra) - #1271", §Framework change) feeding SwiGLU experts ("zonos2.cpp
+internals", §Recommended: F16 spine + K-quant experts, expert stacks
+ffn_{gate,up,down}_exps).  Each test is chosen so that a plausible slip in the
+oracle -- biased logits in the softmax, a wrong tie-break, a transposed weight,
+a dropped SiLU factor, an off-by-one in the scan -- fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "selected_softmax_worked.txt")
+
+
+def _golden():
+    cases = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if parts[0] == "case":
+            cases.setdefault(parts[1], {})[parts[2]] = [float(v) for v in parts[3:]]
+        elif parts[0] == "ffn":
+            cases["ffn"] = [float(v) for v in parts[2:]]
+    return cases
+
+
+# ------------------------------------------------ independent numpy helpers
+def decode(a, dtype):
+    """Storage -> float64, written independently of the C oracle."""
+    if dtype == wl.F32:
+        return np.asarray(a, np.float32).astype(np.float64)
+    if dtype == wl.BF16:
+        return wl.bf16_bits_to_f32(a).astype(np.float64)
+    blocks = np.asarray(a, np.uint8)
+    scale = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    q = blocks[..., 2:].copy().view(np.int8).astype(np.float64)
+    w = q * scale[..., None]
+    return w.reshape(w.shape[:-2] + (w.shape[-2] * w.shape[-1],))
+
+
+def brute_force_dense(layer):
+    """All experts on every token, then a brute-force top-k mask.
+
+    The ranking uses Python's sort on (-score, expert) tuples, so ties go to
+    the lower expert index; weights are exp(l - max) over the mask.
+    """
+    x = decode(layer.x, layer.act_dtype)
+    wr = decode(layer.w_router, layer.act_dtype)
+    wg = decode(layer.w_gate, layer.w_dtype)
+    wu = decode(layer.w_up, layer.w_dtype)
+    wd = decode(layer.w_down, layer.w_dtype)
+    b = np.asarray(layer.bias, np.float64)
+    T, E, k = x.shape[0], layer.E, layer.k
+    logits = np.array([[sum(x[t, i] * wr[e, i] for i in range(x.shape[1])) for e in range(E)]
+                       for t in range(T)])
+    # dense: every expert for every token, [E, T, d]
+    g = np.einsum("efi,ti->etf", wg, x)
+    u = np.einsum("efi,ti->etf", wu, x)
+    h = g * (1.0 / (1.0 + np.exp(-g))) * u
+    y = np.einsum("eif,etf->eti", wd, h)
+    out = np.zeros_like(x)
+    sel_all = []
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-(logits[t, e] + b[e]), e))
+        sel = order[:k]
+        sel_all.append(sel)
+        m = max(logits[t, e] for e in sel)
+        z = sum(math.exp(logits[t, e] - m) for e in sel)
+        for e in sel:
+            out[t] += math.exp(logits[t, e] - m) / z * y[e, t]
+    return out, np.array(sel_all, dtype=np.int32), logits
+
+
+def tiny_layer(seed=0, act=wl.F32, wdt=wl.F32, T=8, d=64, E=8, k=2, F=128, bias_sd=0.1):
+    return wl.make_custom_layer(seed, T, d, E, k, F, act, wdt, bias_sd=bias_sd)
+
+
+# ---------------------------------------------------------------- the pins
+def test_golden_worked_routing():
+    gold = _golden()
+    x = np.array([[1.0, 0.0]], np.float32)
+    wr = np.array([[0.5, 0], [1, 0], [-1, 0], [2, 0]], np.float32)
+    logits = oracle.router_logits(x, wl.F32, wr, 4)
+    assert logits.tolist() == [[0.5, 1.0, -1.0, 2.0]]
+    bias_a = np.array([3, 0, 0, 0], np.float32)
+    for name, bias, k in (("A", bias_a, 2), ("B", None, 2), ("D", bias_a, 1)):
+        idx, w, _ = oracle.selected_softmax(logits, bias, k)
+        assert idx[0].tolist() == [int(v) for v in gold[name]["idx"]], name
+        np.testing.assert_allclose(w[0], gold[name]["w"], rtol=1e-15, atol=0)
+    tie = np.array([[1.0, 1.0, 0.0, 1.0]])
+    idx, w, margin = oracle.selected_softmax(tie, None, 2)
+    assert idx[0].tolist() == [int(v) for v in gold["C"]["idx"]]
+    assert w[0].tolist() == gold["C"]["w"]
+    assert margin[0] == 0.0
+
+
+def test_golden_worked_ffn():
+    gold = _golden()
+    x = np.array([[1.0, 2.0]], np.float32)
+    wg = np.array([[[1, 0], [0, -1]]], np.float32)
+    wu = np.array([[[2, 0], [1, 1]]], np.float32)
+    wd = np.array([[[1, 3], [5, 7]]], np.float32)
+    out = oracle.expert_combine(x, wl.F32, np.array([[0]]), np.array([[1.0]]), wg, wu, wd,
+                                wl.F32, 1, 2)
+    np.testing.assert_allclose(out[0], gold["ffn"], rtol=1e-14, atol=0)
+
+
+def test_k1_weight_is_exactly_one():
+    layer = tiny_layer(k=1, E=16)
+    logits = oracle.router_logits(layer.x, layer.act_dtype, layer.w_router, layer.E)
+    _, w, _ = oracle.selected_softmax(logits, layer.bias, 1)
+    assert np.all(w == 1.0)
+
+
+@pytest.mark.parametrize("k", [2, 3, 4, 8])
+def test_weights_sum_to_one(k):
+    rng = np.random.default_rng(k)
+    logits = rng.standard_normal((64, 16)) * 3
+    idx, w, _ = oracle.selected_softmax(logits, rng.standard_normal(16).astype(np.float32), k)
+    assert np.all(np.abs(w.sum(1) - 1.0) <= 1e-15)
+    assert np.all(w > 0)
+    # each row's slots are distinct experts, in descending ranking score
+    for t in range(64):
+        assert len(set(idx[t].tolist())) == k
+
+
+def test_bias_selects_but_never_weighs():
+    rng = np.random.default_rng(3)
+    T, E, k = 32, 12, 3
+    logits = rng.standard_normal((T, E))
+    idx0, w0, margin0 = oracle.selected_softmax(logits, None, k)
+    # a bias too small to change any selection leaves weights bit-identical
+    small = (rng.standard_normal(E) * 1e-9).astype(np.float32)
+    ok = margin0 > 1e-6
+    idx1, w1, _ = oracle.selected_softmax(logits, small, k)
+    assert np.array_equal(idx1[ok], idx0[ok])
+    assert np.array_equal(w1[ok], w0[ok])
+    # a bias forcing set S = {1, 5, 7} gives weights = softmax of the S logits
+    force = np.zeros(E, np.float32)
+    force[[1, 5, 7]] = 1e6
+    idx2, w2, _ = oracle.selected_softmax(logits, force, k)
+    for t in range(T):
+        assert sorted(idx2[t].tolist()) == [1, 5, 7]
+        l = logits[t, idx2[t]]
+        ref = np.exp(l - l.max()) / np.exp(l - l.max()).sum()
+        np.testing.assert_allclose(w2[t], ref, rtol=1e-14)
+
+
+def test_zero_bias_is_textbook_topk_softmax_renormalised():
+    """bias = 0: softmax over all E, keep the top k, renormalise."""
+    rng = np.random.default_rng(4)
+    T, E, k = 40, 10, 4
+    logits = rng.standard_normal((T, E)) * 2
+    idx, w, _ = oracle.selected_softmax(logits, None, k)
+    p = np.exp(logits - logits.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    for t in range(T):
+        top = np.argsort(-p[t], kind="stable")[:k]
+        assert idx[t].tolist() == top.tolist()
+        np.testing.assert_allclose(w[t], p[t, top] / p[t, top].sum(), rtol=1e-13)
+
+
+def test_k_equals_e_is_dense_softmax_gating():
+    layer = tiny_layer(seed=5, E=4, k=4, T=6, d=32, F=64, bias_sd=3.0)
+    out, idx, w, margin = oracle.moe_forward(layer)
+    assert np.all(np.isinf(margin))
+    x = decode(layer.x, wl.F32)
+    logits = x @ decode(layer.w_router, wl.F32).T
+    p = np.exp(logits - logits.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    wg, wu, wd = (decode(a, wl.F32) for a in (layer.w_gate, layer.w_up, layer.w_down))
+    ref = np.zeros_like(x)
+    for e in range(4):
+        g, u = x @ wg[e].T, x @ wu[e].T
+        ref += p[:, e:e + 1] * ((g / (1 + np.exp(-g)) * u) @ wd[e].T)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("act,wdt", [(wl.F32, wl.F32), (wl.BF16, wl.BF16), (wl.BF16, wl.Q8_0)])
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_matches_dense_brute_force(act, wdt, k):
+    layer = tiny_layer(seed=10 + k, act=act, wdt=wdt, T=5, d=64, E=6, k=k, F=96, bias_sd=0.3)
+    out, idx, w, margin = oracle.moe_forward(layer)
+    ref, sel, logits = brute_force_dense(layer)
+    assert np.array_equal(idx, sel)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_identical_experts_give_one_ffn():
+    layer = tiny_layer(seed=6, k=3, E=5)
+    for name in ("w_gate", "w_up", "w_down"):
+        a = getattr(layer, name)
+        a[:] = a[0:1]
+    out, idx, w, _ = oracle.moe_forward(layer)
+    ref = oracle.expert_combine(layer.x, wl.F32, np.zeros((layer.T, 1), np.int32),
+                                np.ones((layer.T, 1)), layer.w_gate, layer.w_up,
+                                layer.w_down, wl.F32, layer.E, layer.F)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_zero_up_projection_gives_zero():
+    layer = tiny_layer(seed=7)
+    layer.w_up[:] = 0
+    out, *_ = oracle.moe_forward(layer)
+    assert np.all(out == 0.0)
+
+
+def test_token_permutation_equivariance_bit_exact():
+    layer = tiny_layer(seed=8, act=wl.BF16, wdt=wl.BF16, T=12)
+    out, idx, w, _ = oracle.moe_forward(layer)
+    perm = np.random.default_rng(1).permutation(layer.T)
+    layer.x = layer.x[perm].copy()
+    out_p, idx_p, w_p, _ = oracle.moe_forward(layer)
+    assert np.array_equal(out_p, out[perm])
+    assert np.array_equal(idx_p, idx[perm])
+    assert np.array_equal(w_p, w[perm])
+
+
+def test_linear_in_down_projection():
+    layer = tiny_layer(seed=9)
+    out, *_ = oracle.moe_forward(layer)
+    layer.w_down = (layer.w_down * np.float32(2.0)).astype(np.float32)
+    out2, *_ = oracle.moe_forward(layer)
+    assert np.array_equal(out2, 2.0 * out)
+
+
+def test_q8_0_equals_its_exact_dequantisation():
+    """Q8_0 bytes and their fp32 dequantisation (exact: 11 x 8 bits) agree bit for bit."""
+    layer = tiny_layer(seed=11, act=wl.BF16, wdt=wl.Q8_0, T=6, d=64, F=96)
+    out_q, idx_q, w_q, _ = oracle.moe_forward(layer)
+    for name in ("w_gate", "w_up", "w_down"):
+        deq = decode(getattr(layer, name), wl.Q8_0)
+        assert np.array_equal(deq.astype(np.float32).astype(np.float64), deq)
+        setattr(layer, name, deq.astype(np.float32))
+    layer.w_dtype = wl.F32
+    out_f, idx_f, w_f, _ = oracle.moe_forward(layer)
+    assert np.array_equal(idx_q, idx_f)
+    assert np.array_equal(out_q, out_f)
+
+
+def test_q8_0_block_encoding():
+    w = np.zeros((2, 64), np.float32)
+    w[0, :32] = np.linspace(-1, 1, 32)
+    w[1, 32:] = 0.5
+    blocks = wl.q8_0_quantize(w)
+    assert blocks.shape == (2, 2, 34)
+    deq = decode(blocks, wl.Q8_0)
+    assert np.all(deq[0, 32:] == 0) and np.all(deq[1, :32] == 0)
+    # scale = max|w|/127 stored in fp16; extreme values map to +-127
+    s = np.float16(np.float32(1.0) / np.float32(127))
+    assert blocks[0, 0, 2:].view(np.int8)[0] == -127
+    np.testing.assert_allclose(deq[0, :32], w[0, :32], atol=float(s))
+
+
+def test_permute_brute_force_and_invariants():
+    rng = np.random.default_rng(12)
+    for T, k, E in ((0, 2, 4), (1, 1, 1), (17, 2, 5), (100, 3, 9), (64, 4, 64)):
+        idx = np.array([rng.choice(E, size=k, replace=False) for _ in range(T)],
+                       dtype=np.int32).reshape(T, k)
+        counts, offsets, perm_tok, inv = oracle.permute(idx, E)
+        assert counts.sum() == T * k
+        assert offsets[0] == 0 and np.array_equal(np.diff(offsets), counts)
+        flat = idx.ravel()
+        # brute force: stable sort of flat slots by expert
+        order = sorted(range(T * k), key=lambda i: (flat[i], i))
+        assert perm_tok.tolist() == [i // k for i in order]
+        assert sorted(inv.tolist()) == list(range(T * k))
+        for i in range(T * k):
+            assert perm_tok[inv[i]] == i // k
+            assert offsets[flat[i]] <= inv[i] < offsets[flat[i] + 1]
+
+
+def test_margin_is_kth_minus_next_score():
+    logits = np.array([[0.0, 3.0, 1.0, 2.0]])
+    bias = np.array([0.5, 0, 0, 0], np.float32)
+    idx, w, margin = oracle.selected_softmax(logits, bias, 2)
+    assert idx[0].tolist() == [1, 3]
+    assert margin[0] == 2.0 - 1.0
+
+
+def test_invalid_arguments_raise():
+    with pytest.raises(ValueError):
+        oracle.selected_softmax(np.zeros((2, 4)), None, 5)
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[7]], np.int32), 4)
+
+
+def test_multithreaded_equals_single_threaded():
+    layer = tiny_layer(seed=13, act=wl.BF16, wdt=wl.BF16, T=33)
+    a = oracle.moe_forward(layer, nthreads=1)
+    b = oracle.moe_forward(layer, nthreads=7)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
