@@ -1,0 +1,464 @@
+"""Benchmark of the GB300 MoE FFN layer with SelectedSoftmax routing.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME] [--T T] [--no-graph]
+
+A step is one pass of the whole layer (routing, grouping, expert FFN,
+combine) over every layer of the workload's stack, on synthetic inputs
+resident in HBM.  The default workload is the ZONOS3-Mini-shaped decode step:
+T=128 rows, d=1024, E=64, top-2, F=512, bf16, 10 independent MoE layers
+back to back (2.0 GB of expert weights per step, far above the 129 MB L2, so
+every step reads its weights from HBM).  value = layer-tokens per second
+(T x layers x steps / time).  One JSON line is printed by rank 0.
+
+--impl reference times the CPU fp64 oracle (the only reference this library
+has) on the machine's host cores, on bounded token samples of the same workload.
+Under torchrun each rank runs an independent replica (no collective on the
+data path); timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s and prefill TFLOPS as % of GB300 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="zonos3_mini_decode")
+    p.add_argument("--T", type=int, default=None)
+    p.add_argument("--layers", type=int, default=None)
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks, key):
+    for k, v in peaks.items():
+        if k == key and isinstance(v, (int, float)):
+            return float(v)
+    # tolerate nested layouts {"hbm_gbs": {"value": ..}}
+    v = peaks.get(key)
+    if isinstance(v, dict) and "value" in v:
+        return float(v["value"])
+    return FALLBACK_PEAKS[key]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- algorithmic
+def algorithmic(w, T, counts_per_layer):
+    """Algorithmic bytes/flops per stage for one step (sum over the stack).
+
+    Bytes: each active expert's weights once, x, W_r, bias, fp32 output.
+    Flops: 2*T*d*E (router) + 2*T*k*3*d*F (experts).
+    """
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    asz = wl.act_bytes(w.act_dtype)
+    per_w = wl.weight_bytes_per_expert(w.d, w.F, w.w_dtype)
+    gu_w, dn_w = per_w * 2 // 3, per_w // 3
+    x_b, wr_b, out_b, b_b = T * w.d * asz, w.E * w.d * asz, T * w.d * 4, w.E * 4
+    total = dict(bytes=0, flops=0, gateup_bytes=0, down_bytes=0, route_bytes=0, active=[])
+    for counts in counts_per_layer:
+        act = int((np.asarray(counts) > 0).sum())
+        total["active"].append(act)
+        total["route_bytes"] += x_b + wr_b + b_b
+        total["gateup_bytes"] += act * gu_w + x_b
+        total["down_bytes"] += act * dn_w + out_b
+        total["bytes"] += act * per_w + x_b + wr_b + out_b + b_b
+        total["flops"] += 2 * T * w.d * w.E + 2 * T * w.k * 3 * w.d * w.F
+    return total
+
+
+def profile_traffic(kernel_key):
+    """dram bytes per launch recorded from an ncu capture, if the kernel source
+    it was taken on is unchanged (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel_key:
+            rec = {"bytes": float(parts[1]), "sha": parts[2]}
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "expert_routed_ffn_selectedsoftmax_gb300", "csrc",
+                       kernel_key.split(":")[0])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes"] if sha == rec["sha"] else None
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(layers_host, w, budget_s):
+    """Time the oracle on whole-layer token samples until ~budget_s elapses."""
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    done_tokens, t_used = 0, 0.0
+    li = 0
+    while t_used < budget_s and li < len(layers_host):
+        layer = layers_host[li]
+        t0 = time.perf_counter()
+        oracle.moe_forward(layer, nthreads=threads)
+        t_used += time.perf_counter() - t0
+        done_tokens += layer.T
+        li += 1
+    return done_tokens, t_used, threads, li
+
+
+def host_layer_from_device(w, dl, T):
+    """A workloads.Layer (host storage arrays) from one device-drawn layer."""
+    import torch
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return wl.Layer(T=T, d=w.d, E=w.E, k=w.k, F=w.F, act_dtype=w.act_dtype, w_dtype=w.w_dtype,
+                    x=bits(dl["x"]), w_router=bits(dl["w_router"]),
+                    bias=dl["bias"].float().cpu().numpy(), w_gate=bits(dl["w_gate"]),
+                    w_up=bits(dl["w_up"]), w_down=bits(dl["w_down"]))
+
+
+def run_reference(args, w, T, layers):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    oracle.build()
+    threads = oracle.default_threads()
+    # host-drawn layer of the same shapes and distributions; each step runs the
+    # oracle on a bounded sample of `sample_T` tokens of that layer
+    layer = wl.make_layer(w, seed=0, T=T)
+    sample_T = min(T, max(1, threads))
+    import copy
+    subs = []
+    for s in range(4):
+        sub = copy.copy(layer)
+        rows = (np.arange(sample_T) + s * sample_T) % T
+        sub.x = np.ascontiguousarray(layer.x[rows])
+        sub.T = sample_T
+        subs.append(sub)
+    for i in range(args.warmup):
+        oracle.moe_forward(subs[i % 4], nthreads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.moe_forward(subs[i % 4], nthreads=threads)
+    dt = time.perf_counter() - t0
+    value = sample_T * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, T, layers, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{sample_T} tokens of one {w.name} layer per step "
+                                   f"(fp64 C oracle, {threads} threads)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w, T, layers, args):
+    return {"workload": w.name, "T": T, "d": w.d, "E": w.E, "k": w.k, "F": w.F,
+            "layers": layers, "act_dtype": "bf16" if w.act_dtype else "f32",
+            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[w.w_dtype],
+            "bias": w.bias, "global_batch": T * max(1, args.gpus), "parallelism": "replicas",
+            "l2": "inputs larger than L2: every step reads all layers' expert weights",
+            "graph": not args.no_graph}
+
+
+def main():
+    args = parse()
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    T = args.T if args.T is not None else w.T
+    layers = args.layers if args.layers is not None else w.layers
+    if args.impl == "reference":
+        return run_reference(args, w, T, layers)
+
+    import torch
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pkg.load_library()
+
+    # ------------------------------------------------------------ inputs
+    stack = wl.make_device_stack(w, seed=1 + rank, layers=layers, T=T, device=dev)
+    act_dt, w_dt = pkg.MOE_BF16, pkg.MOE_BF16
+    ws_bytes = pkg.moe_workspace_size(T, w.d, w.E, w.k, w.F, act_dt, w_dt)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    outs = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in range(layers)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def layer_call(i, events=None):
+        L = stack[i]
+        pkg.moe_forward(L["x"], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
+                        w.k, out=outs[i], workspace=ws, events=events)
+
+    def step():
+        for i in range(layers):
+            layer_call(i)
+
+    # counts per layer (for the algorithmic bytes): one routing pass
+    counts_per_layer = []
+    with torch.cuda.stream(stream):
+        for L in stack:
+            idx, _ = pkg.moe_route(L["x"], L["w_router"], L["bias"], w.k)
+            c, _, _, _ = pkg.moe_permute(idx, w.E)
+            counts_per_layer.append(c)
+    stream.synchronize()
+    counts_per_layer = [c.cpu().numpy() for c in counts_per_layer]
+    alg = algorithmic(w, T, counts_per_layer)
+
+    # --------------------------------------------------------- warm-up + graph
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        stream.synchronize()
+    assert pkg.moe_check(ws) == 0
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ------------------------------------------------------------ timed region
+    clocks = ClockSampler(local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+        e1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    barrier()
+    t_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    ms_per_step = t_ms / args.steps
+    tokens_per_step = T * layers
+    value = tokens_per_step * world / (ms_per_step * 1e-3)
+
+    # --------------------------------------------- per-kernel (stage) timing
+    # the same step with CUDA events at the stage boundaries, on the stream
+    # the kernels run on
+    n_prof = max(1, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(layers)]
+    # torch only reports elapsed time for events it has recorded itself once;
+    # the library re-records the same events at its stage boundaries
+    for row in evs:
+        for ev in row:
+            ev.record(stream)
+    stream.synchronize()
+    stage_ms = np.zeros(5)
+    with torch.cuda.stream(stream):
+        for _ in range(n_prof):
+            for i in range(layers):
+                layer_call(i, events=evs[i])
+            stream.synchronize()
+            for i in range(layers):
+                for s in range(5):
+                    stage_ms[s] += evs[i][s].elapsed_time(evs[i][s + 1])
+    stage_us = stage_ms / (n_prof * layers) * 1e3     # per launch, µs
+    names = ["route", "permute", "gather", "gateup", "down"]
+
+    # ------------------------------------------------------- roofline object
+    peaks, peak_src = load_peaks()
+    hbm = peak_value(peaks, "hbm_gbs")
+    gu_bytes_per_launch = alg["gateup_bytes"] / layers
+    dn_bytes_per_launch = alg["down_bytes"] / layers
+    dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
+    dom_bytes = gu_bytes_per_launch if dominant == "gateup" else dn_bytes_per_launch
+    dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    traffic = profile_traffic(f"decode.cu:{dominant}")
+    roofline = {"bound": "hbm", "kernel": f"decode_{dominant}_kernel", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                "peak_source": f"hbm_gbs of {peak_src}",
+                "bytes_per_launch": dom_bytes, "us_per_launch": dom_us}
+    layer_gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
+    layer_tflops = alg["flops"] / (ms_per_step * 1e-3) / 1e12
+
+    # ------------------------------------------------------------- e2e
+    # through the public API with host buffers: pinned x in, fp32 out back, per step
+    hx = [L["x"].cpu().pin_memory() for L in stack]
+    hout = [torch.empty((T, w.d), dtype=torch.float32).pin_memory() for _ in range(layers)]
+    dx = [torch.empty_like(L["x"]) for L in stack]
+    n_e2e = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        for i in range(layers):
+            dx[i].copy_(hx[i], non_blocking=True)
+        for i in range(layers):
+            L = stack[i]
+            pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
+                            w.k, out=outs[i], workspace=ws)
+        for i in range(layers):
+            hout[i].copy_(outs[i], non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    stream.synchronize()
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_value = tokens_per_step * world / (e2e_ms * 1e-3)
+    h2d = sum(t.numel() * t.element_size() for t in hx)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    # ------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_layers = [host_layer_from_device(w, stack[i], T) for i in range(min(layers, 3))]
+        ntok, secs, threads, nl = oracle_sample(host_layers, w, budget_s=10.0)
+        cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nl} of the {layers} layers of one step, all {T} tokens each "
+                         f"(fp64 C oracle, {threads} threads), {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(w, T, layers, args),
+        "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s",
+                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * layers * args.steps,
+        "roofline": roofline, "cpu_baseline": cpu,
+        "layer": {"algorithmic_GBps": layer_gbs, "TFLOPS": layer_tflops,
+                  "frac_hbm": layer_gbs / hbm, "bytes_per_step": alg["bytes"],
+                  "flops_per_step": alg["flops"],
+                  "active_experts_per_layer": alg["active"],
+                  "stage_us": dict(zip(names, [round(float(v), 3) for v in stage_us]))},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

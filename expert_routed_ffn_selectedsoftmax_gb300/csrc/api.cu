@@ -1,0 +1,264 @@
+// api.cu -- the C ABI declared in include/moe.h: argument checks, workspace
+// layout and kernel dispatch.  Every check happens on the host before any
+// launch; nothing here allocates, frees or synchronises (except moe_check,
+// which documents that it waits).
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_gemm.h"
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool act_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+
+bool weights_ok(int act_dt, int w_dt)
+{
+    if (act_dt == MOE_F32) return w_dt == MOE_F32;
+    return w_dt == MOE_BF16 || w_dt == MOE_Q8_0;
+}
+
+// Largest d the router kernel can stage (one token of fp32 in <= 200 KB).
+bool route_fits(int d, int E) { return route_smem_bytes(1, d, E) <= 200 * 1024; }
+
+moe_status check_route_args(const void *x, int act_dt, int T, int d, const void *w_router,
+                            const float *bias, int E, int k)
+{
+    if (T < 0 || d <= 0 || E <= 0 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+    if (!act_ok(act_dt)) return MOE_ERR_INVALID_ARG;
+    if (d % 8) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if (!route_fits(d, E)) return MOE_ERR_UNSUPPORTED;
+    if ((long long)T * k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!aligned16(x) || !aligned16(w_router))) return MOE_ERR_INVALID_ARG;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+struct WsLayout {
+    size_t status, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w, h, xp, total;
+};
+
+bool prefill_capable(int act_dt, int w_dt, int d, int F)
+{
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q8_0) && d % 256 == 0 &&
+           F % 128 == 0;
+}
+
+WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
+{
+    WsLayout L{};
+    const size_t n = (size_t)T * k;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
+    L.status = take(4);
+    L.topk_idx = take(4 * n);
+    L.topk_w = take(4 * n);
+    L.counts = take(4 * (size_t)E);
+    L.offsets = take(4 * ((size_t)E + 1));
+    L.perm_tok = take(4 * n);
+    L.inv = take(4 * n);
+    L.perm_w = take(4 * n);
+    L.h = take(4 * n * (size_t)F);            // fp32 (decode); prefill uses 2 bytes/element
+    L.xp = prefill_capable(act_dt, w_dt, d, F) ? take(2 * n * (size_t)d) : off;
+    L.total = off;
+    return L;
+}
+
+int device_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 148;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_str(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype combination";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case MOE_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "a device-side consistency check failed";
+    default: return "unknown status";
+    }
+}
+
+int moe_version(void) { return 100; }
+
+moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                     const float *sel_bias, int E, int k, int32_t *topk_idx, float *topk_w,
+                     moe_stream stream)
+{
+    moe_status st = check_route_args(x, act_dt, T, d, w_router, sel_bias, E, k);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (!topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    cudaError_t e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w,
+                                 nullptr, nullptr, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
+                       int32_t *offsets, int32_t *perm_tok, int32_t *inv, moe_stream stream)
+{
+    if (T < 0 || k < 1 || E <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if ((long long)T * k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !perm_tok || !inv)) return MOE_ERR_INVALID_ARG;
+    // T == 0 still writes zero counts and offsets
+    cudaError_t e = launch_permute(topk_idx, T, k, E, counts, offsets, perm_tok, inv, nullptr,
+                                   nullptr, nullptr, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_q8_0_packed_size(long long rows, int cols)
+{
+    if (rows < 0 || cols <= 0 || cols % 32) return 0;
+    return align_up((size_t)rows * cols, 256) + (size_t)rows * (cols / 32) * 2;
+}
+
+moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
+                         moe_stream stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    cudaError_t e = launch_pack_q8_0(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype act_dt, moe_dtype w_dt)
+{
+    if (T < 0 || d <= 0 || E <= 0 || k < 1 || k > E || F <= 0) return 0;
+    if (!act_ok(act_dt) || !weights_ok(act_dt, w_dt)) return 0;
+    return ws_layout(T, d, E, k, F, act_dt, w_dt).total;
+}
+
+moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                       const float *sel_bias, int E, int k, const void *w_gate,
+                       const void *w_up, const void *w_down, moe_dtype w_dt, int F,
+                       float *out, void *workspace, size_t ws_bytes, int path,
+                       moe_stream stream)
+{
+    return moe_forward_profiled(x, act_dt, T, d, w_router, sel_bias, E, k, w_gate, w_up, w_down,
+                                w_dt, F, out, workspace, ws_bytes, path, nullptr, stream);
+}
+
+moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
+                                const void *w_router, const float *sel_bias, int E, int k,
+                                const void *w_gate, const void *w_up, const void *w_down,
+                                moe_dtype w_dt, int F, float *out, void *workspace,
+                                size_t ws_bytes, int path, void *const *events,
+                                moe_stream stream)
+{
+    moe_status st = check_route_args(x, act_dt, T, d, w_router, sel_bias, E, k);
+    if (st != MOE_OK) return st;
+    if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
+    if (!weights_ok(act_dt, w_dt)) {
+        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0) ? MOE_ERR_UNSUPPORTED
+                                                                         : MOE_ERR_INVALID_ARG;
+    }
+    if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL)
+        return MOE_ERR_INVALID_ARG;
+    const bool can_prefill = prefill_capable(act_dt, w_dt, d, F) && tc_gemm_supports(w_dt) &&
+                             tc_gemm_available();
+    if (path == MOE_PATH_PREFILL && !can_prefill) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!w_gate || !w_up || !w_down || !out || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    if (w_dt == MOE_Q8_0) {
+        const uintptr_t m = 255u;
+        if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
+            (reinterpret_cast<uintptr_t>(w_down) & m))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, F, act_dt, w_dt);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+    char *ws = static_cast<char *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws + L.status);
+    int32_t *topk_idx = reinterpret_cast<int32_t *>(ws + L.topk_idx);
+    float *topk_w = reinterpret_cast<float *>(ws + L.topk_w);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *perm_tok = reinterpret_cast<int32_t *>(ws + L.perm_tok);
+    int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
+    float *perm_w = reinterpret_cast<float *>(ws + L.perm_w);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    bool use_prefill = false;
+    if (path == MOE_PATH_PREFILL) use_prefill = true;
+    else if (path == MOE_PATH_AUTO) use_prefill = can_prefill && tc_gemm_prefer(T, d, E, k, F);
+
+    cudaEvent_t ev[6] = {};
+    if (events)
+        for (int i = 0; i < 6; ++i) ev[i] = static_cast<cudaEvent_t>(events[i]);
+    auto mark = [&](int i) { return ev[i] ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+
+    if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w,
+                                 k > 1 ? out : nullptr, status, s);
+    if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_permute(topk_idx, T, k, E, counts, offsets, perm_tok, inv, topk_w, perm_w, status, s);
+    if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+
+    const int num_sms = device_sm_count();
+    if (use_prefill) {
+        TcArgs a{};
+        a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
+        a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down; a.w_dt = w_dt;
+        a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
+        a.xp = ws + L.xp; a.h = ws + L.h; a.out = out; a.status = status; a.num_sms = num_sms;
+        a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
+        e = launch_tc_experts(a, s);
+    } else {
+        DecodeArgs a{};
+        a.x = x; a.act_dt = act_dt; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
+        a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down; a.w_dt = w_dt;
+        a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
+        a.h = reinterpret_cast<float *>(ws + L.h); a.out = out; a.num_sms = num_sms;
+        a.ev_gateup = ev[4];
+        if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+        e = launch_decode_experts(a, s);
+    }
+    if (e != cudaSuccess || mark(5) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_check(const void *workspace, uint32_t *device_word, moe_stream stream)
+{
+    if (!workspace) return MOE_ERR_INVALID_ARG;
+    uint32_t w = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&w, workspace, sizeof w, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (device_word) *device_word = w;
+    if (w & kDevTimeout) return MOE_ERR_TIMEOUT;
+    if (w & kDevCheckFailed) return MOE_ERR_DEVICE_CHECK;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,177 @@
+// common.cuh -- small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+
+// Device status word values (first word of the workspace).
+constexpr uint32_t kDevOk = 0;
+constexpr uint32_t kDevTimeout = 1u;       // bounded mbarrier wait gave up
+constexpr uint32_t kDevCheckFailed = 2u;   // device consistency check failed
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- conversions
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Eight consecutive elements -> fp32, for each storage type.
+struct Chunk8 { float v[8]; };
+
+__device__ __forceinline__ void load8(const float *p, Chunk8 &c)
+{
+    float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    c.v[0] = a.x; c.v[1] = a.y; c.v[2] = a.z; c.v[3] = a.w;
+    c.v[4] = b.x; c.v[5] = b.y; c.v[6] = b.z; c.v[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, Chunk8 &c)
+{
+    uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    c.v[0] = bf16lo(u.x); c.v[1] = bf16hi(u.x);
+    c.v[2] = bf16lo(u.y); c.v[3] = bf16hi(u.y);
+    c.v[4] = bf16lo(u.z); c.v[5] = bf16hi(u.z);
+    c.v[6] = bf16lo(u.w); c.v[7] = bf16hi(u.w);
+}
+
+// Streaming (read-once) weight loads: do not keep the lines in L1.
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_stream_u2(const void *p)
+{
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+// Raw weight chunk of 8 elements as loaded from HBM (converted later).
+template <typename WT> struct RawW;
+template <> struct RawW<float> { uint4 a, b; };
+template <> struct RawW<__nv_bfloat16> { uint4 a; };
+struct Q8Tag {};   // Q8_0 planes: int8 q plane + fp16 scale per 32 values
+template <> struct RawW<Q8Tag> { uint2 q; float s; };
+
+// Weight matrix view: row-major [rows, cols] in one of the storage types.
+template <typename WT> struct WView {
+    const WT *p;
+    size_t cols;
+    __device__ __forceinline__ void load(size_t row, int col, RawW<WT> &r) const;
+    __device__ __forceinline__ static void cvt(const RawW<WT> &r, Chunk8 &c);
+};
+
+template <> __device__ __forceinline__ void WView<float>::load(size_t row, int col, RawW<float> &r) const
+{
+    const float *q = p + row * cols + col;
+    r.a = ld_stream_u4(q);
+    r.b = ld_stream_u4(q + 4);
+}
+template <> __device__ __forceinline__ void WView<float>::cvt(const RawW<float> &r, Chunk8 &c)
+{
+    c.v[0] = __uint_as_float(r.a.x); c.v[1] = __uint_as_float(r.a.y);
+    c.v[2] = __uint_as_float(r.a.z); c.v[3] = __uint_as_float(r.a.w);
+    c.v[4] = __uint_as_float(r.b.x); c.v[5] = __uint_as_float(r.b.y);
+    c.v[6] = __uint_as_float(r.b.z); c.v[7] = __uint_as_float(r.b.w);
+}
+template <> __device__ __forceinline__ void WView<__nv_bfloat16>::load(size_t row, int col,
+                                                                        RawW<__nv_bfloat16> &r) const
+{
+    r.a = ld_stream_u4(p + row * cols + col);
+}
+template <> __device__ __forceinline__ void WView<__nv_bfloat16>::cvt(const RawW<__nv_bfloat16> &r,
+                                                                       Chunk8 &c)
+{
+    c.v[0] = bf16lo(r.a.x); c.v[1] = bf16hi(r.a.x);
+    c.v[2] = bf16lo(r.a.y); c.v[3] = bf16hi(r.a.y);
+    c.v[4] = bf16lo(r.a.z); c.v[5] = bf16hi(r.a.z);
+    c.v[6] = bf16lo(r.a.w); c.v[7] = bf16hi(r.a.w);
+}
+
+// Q8_0 view: p points at the q plane; the fp16 scale plane follows at
+// align256(rows*cols) bytes.  `scales` is precomputed by the host.
+template <> struct WView<Q8Tag> {
+    const int8_t *q;
+    const __half *scales;
+    size_t cols;
+    __device__ __forceinline__ void load(size_t row, int col, RawW<Q8Tag> &r) const
+    {
+        r.q = ld_stream_u2(q + row * cols + col);
+        r.s = __half2float(scales[row * (cols / 32) + col / 32]);
+    }
+    __device__ __forceinline__ static void cvt(const RawW<Q8Tag> &r, Chunk8 &c)
+    {
+        const uint32_t w[2] = {r.q.x, r.q.y};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int v = (int)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+            c.v[i] = (float)v * r.s;
+        }
+    }
+};
+
+// -------------------------------------------------------------- warp helpers
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Reduce 8 per-lane values across the warp so that afterwards every lane
+// holds the full sum of value index r = ((lane>>4)&1)*4 + ((lane>>3)&1)*2 + ((lane>>2)&1).
+// Uses 9 shuffles instead of 8 x 5.
+__device__ __forceinline__ float warp_transpose_sum8(float (&v)[8], int lane)
+{
+    // stage offset 16: keep half, send half
+    {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float send = hi ? v[i] : v[i + 4];
+            float keep = hi ? v[i + 4] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+    }
+    {
+        const bool hi = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float send = hi ? v[i] : v[i + 2];
+            float keep = hi ? v[i + 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+    }
+    {
+        const bool hi = lane & 4;
+        float send = hi ? v[0] : v[1];
+        float keep = hi ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    float s = v[0];
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    return s;
+}
+
+__device__ __forceinline__ int transpose8_row(int lane)
+{
+    return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+
+}  // namespace moe

@@ -1,0 +1,48 @@
+// q8.cu -- repack Q8_0 expert weights into planes the kernels can stream.
+//
+// Q8_0 (ggml's 8-bit block format, used for the ZONOS2 experts:
+// "zonos2.cpp internals", §Quantization): each block of 32 consecutive values
+// along the contiguous axis is 34 bytes, an fp16 scale then 32 int8 values;
+// value = scale * q.  34-byte blocks are not 16-byte aligned, so the library
+// repacks once, at load time, into an int8 plane [rows, cols] and an fp16 scale
+// plane [rows, cols/32] (same bytes, aligned for 128-bit and TMA loads).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__global__ void pack_q8_0_kernel(const uint8_t *__restrict__ blocks, long long nblocks,
+                                 int8_t *__restrict__ q, __half *__restrict__ scales)
+{
+    for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
+         b += (long long)gridDim.x * blockDim.x) {
+        const uint8_t *src = blocks + b * 34;
+        uint16_t s = (uint16_t)src[0] | ((uint16_t)src[1] << 8);
+        scales[b] = __ushort_as_half(s);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = (uint32_t)src[2 + 4 * i] | ((uint32_t)src[3 + 4 * i] << 8) |
+                   ((uint32_t)src[4 + 4 * i] << 16) | ((uint32_t)src[5 + 4 * i] << 24);
+        uint4 *dst = reinterpret_cast<uint4 *>(q + b * 32);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
+                             cudaStream_t stream)
+{
+    const long long nblocks = rows * (cols / 32);
+    if (nblocks == 0) return cudaSuccess;
+    int8_t *q = static_cast<int8_t *>(packed);
+    __half *s = reinterpret_cast<__half *>(static_cast<char *>(packed) +
+                                           align_up((size_t)rows * cols, 256));
+    long long grid = (nblocks + 255) / 256;
+    if (grid > 65535LL * 16) grid = 65535LL * 16;
+    pack_q8_0_kernel<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks),
+                                                          nblocks, q, s);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,553 @@
+// tc_gemm.cu -- grouped expert GEMMs on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA) for prefill-sized batches.
+//
+// The expert FFN is SwiGLU ("zonos2.cpp internals", §Recommended: expert
+// stacks ffn_{gate,up,down}_exps; "New Community Model: ZONOS3-Mini (Zyphra) -
+// #1271", §Summary): with many rows per expert it is a set of dense
+// contractions, one group per expert, of the rows routed to that expert.
+//
+// Kernel GATEUP: C = Xp_e . [W_g[e]; W_u[e]]^T over tiles of 128 grouped rows
+//   x (128 gate + 128 up columns); the epilogue reads both halves from TMEM
+//   and writes h = SiLU(G) * U as 16-bit values, so G and U never reach HBM.
+// Kernel DOWN: C = H_e . W_d[e]^T over tiles of 128 rows x 256 model columns;
+//   the epilogue scales each row by its routing weight and adds it into
+//   out[token] (fp32; a plain store when k == 1).
+//
+// Per CTA (persistent, one per SM): warp 0 issues TMA loads of the A (rows)
+// and B (weights) tiles into a 4-stage shared-memory ring (128-byte swizzle);
+// warp 1 issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulators in TMEM,
+// two accumulator buffers of 256 columns); warps 2-5 drain the accumulators.
+// Tiles are (expert, n-tile, m-tile), m fastest, so CTAs running at the same
+// time share weight tiles through L2.  Rows of a tile past the end of the
+// expert's group are computed on neighbouring rows (or TMA zero fill) and
+// dropped in the epilogue.
+//
+// Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
+// waiting role sets the status word, raises a CTA-wide abort flag that the
+// other roles poll, waits (bounded) for its own copies or MMAs in flight, and
+// the CTA frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_gemm.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+enum Mode { GATEUP = 0, DOWN = 1 };
+
+struct Params {
+    const int32_t *offsets;   // [E+1] grouped-row offsets
+    int E;
+    int K;                    // reduction length (d for GATEUP, F for DOWN)
+    int n_tiles;              // N / BN   (GATEUP: F / 128, DOWN: d / 256)
+    int F, d, k;
+    uint16_t *h;              // GATEUP output [rows, F] (bf16 or fp16 bits)
+    const int32_t *perm_tok;  // DOWN epilogue
+    const float *perm_w;
+    float *out;
+    uint32_t *status;
+    int h_fp16;               // GATEUP: write h as fp16 (else bf16)
+};
+
+struct SmemCtl {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int n_tiles_total;
+    int tile_start[kMaxExperts + 1];
+    int mtiles[kMaxExperts];
+    int off[kMaxExperts + 1];
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of parity `parity` to complete.  Returns false
+// on timeout or when another role has raised the abort flag.
+__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (tcgen05 descriptor format:
+// start>>4 in bits 0-13, leading offset>>4 in 16-29, stride offset>>4 in
+// 32-45, version 1 in bits 46-47, swizzle mode in 61-63 with 2 = 128B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused with swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;             // descriptor version
+    d |= (uint64_t)2 << 61;             // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
+// both bf16 (ab_fp16 = 0) or both fp16, both K-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t idesc_f16(int ab_fp16)
+{
+    return (1u << 4)                                   // D format: f32
+           | ((ab_fp16 ? 0u : 1u) << 7)                // A format: f16 0 / bf16 1
+           | ((ab_fp16 ? 0u : 1u) << 10)               // B format
+           | ((uint32_t)(BN >> 3) << 17)               // N >> 3
+           | ((uint32_t)(BM >> 4) << 24);              // M >> 4
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// tile -> (expert, m-tile, n-tile); tile_start is an exclusive scan over experts
+__device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int n_tiles, int tile,
+                                            int &e, int &mt, int &nt)
+{
+    int lo = 0, hi = E - 1;   // largest e with tile_start[e] <= tile
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (c.tile_start[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    e = lo;
+    const int local = tile - c.tile_start[e];
+    const int m = c.mtiles[e];
+    nt = local / m;
+    mt = local - nt * m;
+    (void)n_tiles;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_b0,
+                    const __grid_constant__ CUtensorMap tm_b1, const Params p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(smem + STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+
+    // ---- set-up: barriers, tile table, TMEM
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
+        mbar_init(&c.drain, 1);
+        c.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b0)) : "memory");
+        if (MODE == GATEUP)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b1)) : "memory");
+    }
+    for (int e = threadIdx.x; e <= E; e += THREADS) c.off[e] = p.offsets[e];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        // exclusive scan of mtiles_e * n_tiles over experts (E <= 256: 8 per lane)
+        int local[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            int m = 0;
+            if (e < E) {
+                const int rows = c.off[e + 1] - c.off[e];
+                m = (rows + BM - 1) / BM;
+                c.mtiles[e] = m;
+            }
+            local[j] = m * p.n_tiles;
+            sum += local[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            if (e < E) c.tile_start[e] = run;
+            run += local[j];
+        }
+        if (lane == 31) { c.n_tiles_total = incl; c.tile_start[E] = incl; }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&c.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem = c.tmem_base;
+    const int total = c.n_tiles_total;
+    const int kblocks = p.K / BK;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        uint32_t it = 0;   // global k-block counter across tiles
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            int e, mt, nt;
+            decode_tile(c, E, p.n_tiles, tile, e, mt, nt);
+            const int arow = c.off[e] + mt * BM;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(&c.full[s], STAGE_BYTES);
+                tma_load_2d(sA + s * A_BYTES, &tm_a, &c.full[s], kb * BK, arow);
+                if (MODE == GATEUP) {
+                    const int brow = e * p.F + nt * (BN / 2);
+                    tma_load_2d(sB + s * B_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
+                    tma_load_2d(sB + s * B_BYTES + B_BYTES / 2, &tm_b1, &c.full[s], kb * BK, brow);
+                } else {
+                    const int brow = e * p.d + nt * BN;
+                    tma_load_2d(sB + s * B_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
+                }
+            }
+        }
+        if (!ok) {
+            atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+            // let loads already issued land before the CTA exits
+            for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j) {
+                volatile int no_abort = 0;
+                mbar_wait(&c.full[j % STAGES], (j / STAGES) & 1u, &no_abort);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_f16(0);
+        const uint32_t idesc_rt = p.h_fp16 && MODE == DOWN ? idesc_f16(1) : idesc;
+        uint32_t it = 0, local_tile = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local_tile) {
+            const uint32_t acc = local_tile & 1u;
+            const uint32_t acc_ph = (local_tile >> 1) & 1u;
+            if (!mbar_wait(&c.tempty[acc], acc_ph ^ 1u, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * BN;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + s * A_BYTES);
+                const uint32_t b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc_rt,
+                             (kb | kk) != 0);
+                }
+                umma_commit(&c.empty[s]);     // frees the stage when these MMAs finish
+            }
+            if (!ok) break;
+            umma_commit(&c.tfull[acc]);       // accumulator ready for the epilogue
+        }
+        if (!ok) {
+            atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+            umma_commit(&c.drain);            // wait for MMAs in flight before TMEM is freed
+            volatile int no_abort = 0;
+            mbar_wait(&c.drain, 0, &no_abort);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue (4 warps)
+        const int quarter = warp & 3;         // TMEM lanes this warp may access
+        const int row_in_tile = quarter * 32 + lane;
+        uint32_t local_tile = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local_tile) {
+            const uint32_t acc = local_tile & 1u;
+            const uint32_t acc_ph = (local_tile >> 1) & 1u;
+            if (!mbar_wait(&c.tfull[acc], acc_ph, abort_flag)) {
+                if (lane == 0) atomicOr(p.status, kDevTimeout);
+                c.abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            int e, mt, nt;
+            decode_tile(c, E, p.n_tiles, tile, e, mt, nt);
+            const int rows_e = c.off[e + 1] - c.off[e];
+            const bool valid = mt * BM + row_in_tile < rows_e;
+            const int grow = c.off[e] + mt * BM + row_in_tile;
+            const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+            if (MODE == GATEUP) {
+                uint16_t *hrow = p.h + (size_t)grow * p.F + nt * (BN / 2);
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 2; cc += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tbase + cc, g);
+                    tmem_ld16(tbase + BN / 2 + cc, u);
+                    tmem_ld_wait();
+                    uint32_t packed[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                        const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                        if (p.h_fp16) {
+                            __half2 v = __floats2half2_rn(h0, h1);
+                            packed[j] = *reinterpret_cast<uint32_t *>(&v);
+                        } else {
+                            __nv_bfloat162 v = __floats2bfloat162_rn(h0, h1);
+                            packed[j] = *reinterpret_cast<uint32_t *>(&v);
+                        }
+                    }
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + cc);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                }
+            } else {
+                int tok = 0;
+                float wgt = 0.f;
+                if (valid) { tok = p.perm_tok[grow]; wgt = p.perm_w[grow]; }
+                float *orow = p.out + (size_t)tok * p.d + nt * BN;
+#pragma unroll 1
+                for (int cc = 0; cc < BN; cc += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + cc, v);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float a = wgt * __uint_as_float(v[j]);
+                            const float b = wgt * __uint_as_float(v[j + 1]);
+                            const float cq = wgt * __uint_as_float(v[j + 2]);
+                            const float dq = wgt * __uint_as_float(v[j + 3]);
+                            if (p.k == 1)
+                                *reinterpret_cast<float4 *>(orow + cc + j) = make_float4(a, b, cq, dq);
+                            else
+                                red_add_v4(orow + cc + j, a, b, cq, dq);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&c.tempty[acc]);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+constexpr size_t smem_bytes()
+{
+    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load();
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// 2-D row-major [rows, cols] 16-bit tensor, box {64 cols, box_rows}, 128B swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              CUtensorMapDataType dt)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
+bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16; }
+
+bool tc_gemm_prefer(int T, int d, int E, int k, int F)
+{
+    (void)d; (void)F;
+    // grouped GEMMs pay off once experts hold whole 128-row tiles on average
+    return (long long)T * k >= 64LL * E && T >= 512;
+}
+
+cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
+{
+    using namespace tc;
+    if (a.w_dt != MOE_BF16) return cudaErrorNotSupported;   // Q8_0 mainloop: separate kernel
+    const int rows = a.T * a.k;
+    cudaError_t err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, 0, a.num_sms, stream);
+    if (err != cudaSuccess) return err;
+    if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
+
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap m_xp, m_wg, m_wu, m_h, m_wd;
+    if (!make_map(&m_xp, a.xp, rows, a.d, BM, bf) ||
+        !make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BN / 2, bf) ||
+        !make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BN / 2, bf) ||
+        !make_map(&m_h, a.h, rows, a.F, BM, bf) ||
+        !make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BN, bf))
+        return cudaErrorInvalidValue;
+
+    const size_t smem = smem_bytes();
+    static std::atomic<int> attr_done{0};
+    if (!attr_done.load()) {
+        if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+                cudaSuccess)
+            return err;
+        attr_done.store(1);
+    }
+    Params p{};
+    p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k;
+    p.h = static_cast<uint16_t *>(a.h); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
+    p.out = a.out; p.status = a.status; p.h_fp16 = 0;
+
+    // upper bound on tiles: every expert could own a ragged tile
+    const long long max_mtiles = rows / BM + (a.E < rows ? a.E : rows);
+    p.K = a.d; p.n_tiles = a.F / (BN / 2);
+    int grid = (int)(max_mtiles * p.n_tiles < a.num_sms ? max_mtiles * p.n_tiles : a.num_sms);
+    if (grid < 1) grid = 1;
+    grouped_gemm_kernel<GATEUP><<<grid, THREADS, smem, stream>>>(m_xp, m_wg, m_wu, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
+
+    p.K = a.F; p.n_tiles = a.d / BN;
+    grid = (int)(max_mtiles * p.n_tiles < a.num_sms ? max_mtiles * p.n_tiles : a.num_sms);
+    if (grid < 1) grid = 1;
+    grouped_gemm_kernel<DOWN><<<grid, THREADS, smem, stream>>>(m_h, m_wd, m_wd, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,36 @@
+// tc_gemm.h -- internal interface of the tcgen05 grouped-GEMM expert path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct TcArgs {
+    const void *x;              // [T, d] bf16
+    int T, d, E, k, F;
+    const void *w_gate, *w_up, *w_down;   // BF16 arrays, or Q8_0 packed buffers
+    moe_dtype w_dt;
+    const int32_t *offsets;     // [E+1]
+    const int32_t *perm_tok;    // [T*k]
+    const float *perm_w;        // [T*k]
+    void *xp;                   // [T*k, d] 16-bit scratch (grouped rows)
+    void *h;                    // [T*k, F] 16-bit scratch
+    float *out;                 // [T, d] fp32 (zeroed beforehand when k > 1)
+    uint32_t *status;           // device status word
+    int num_sms;
+    cudaEvent_t ev_gathered;    // optional: recorded after the row gather
+    cudaEvent_t ev_gateup;      // optional: recorded after the gate/up GEMM
+};
+
+// True when the tensor-core expert kernels are compiled into this library.
+bool tc_gemm_available();
+// True when the tensor-core expert kernels handle this weight storage type.
+bool tc_gemm_supports(moe_dtype w_dt);
+// Shape heuristic: prefer the grouped GEMMs over the decode kernels.
+bool tc_gemm_prefer(int T, int d, int E, int k, int F);
+cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream);
+
+}  // namespace moe

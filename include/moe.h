@@ -1,0 +1,174 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) mixture-of-experts FFN layer with
+ * SelectedSoftmax routing.
+ *
+ * The layer, per token t with input row x_t[d]:
+ *   1. router projection  l[t,e] = sum_i x[t,i] * W_r[e,i]
+ *   2. SelectedSoftmax    rank experts by l[t,e] + b[e], keep the top k
+ *      (equal scores: lower expert index first), weight each kept expert by
+ *      the softmax of the kept *unbiased* logits
+ *      ("New Community Model: ZONOS3-Mini (Zyphra) - #1271", §Framework change)
+ *   3. token grouping     per-expert counts, exclusive scan, stable permutation
+ *      (grouped expert compute as in ggml's mul_mat_id,
+ *       "zonos2.cpp internals", §Performance)
+ *   4. SwiGLU experts     h = SiLU(W_g[e] x) * (W_u[e] x),  y = W_d[e] h
+ *      ("zonos2.cpp internals", §Recommended: expert stacks ffn_{gate,up,down}_exps;
+ *       "... - #1271", §Summary: SwiGLU FFN)
+ *   5. combine            out[t] = sum_j w[t,j] * y_j, fp32 (residual streams
+ *      are F32, "zonos2.cpp internals", §Notes)
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers owned by the caller, row-major,
+ *    16-byte aligned.  The library never allocates, frees or synchronises on
+ *    these paths; work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and the call returns once it is enqueued.
+ *  - Argument errors are reported synchronously, before anything is
+ *    enqueued.  A kernel launch failure returns MOE_ERR_CUDA.  Nothing aborts.
+ *  - Shapes: T tokens (T >= 0; T == 0 is a no-op), d model width, E experts
+ *    (1..256), k experts per token (1..min(E, 8)), F expert ffn width.
+ *  - Activation storage (x, W_r): MOE_F32 or MOE_BF16; logits, routing
+ *    weights and the output are fp32.  Expert weights: MOE_F32 (with F32
+ *    activations), MOE_BF16 or MOE_Q8_0 (with BF16 activations).
+ *  - Calls on distinct workspaces and outputs are independent; there is no
+ *    global mutable state.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* A cudaStream_t, passed as an opaque pointer. */
+typedef void *moe_stream;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, k > E ... */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype combination, E > 256 ...) */
+    MOE_ERR_WORKSPACE = 3,     /* workspace smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (see moe_check) */
+    MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (see moe_check) */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2 } moe_dtype;
+
+/* Which expert-compute kernels moe_forward uses.  AUTO picks by shape. */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_PREFILL = 2 } moe_path;
+
+/* Static description of a status code (never NULL). */
+MOE_API const char *moe_status_str(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+MOE_API int moe_version(void);
+
+/*
+ * moe_route -- steps 1-2 (router projection + SelectedSoftmax).
+ *   x[T,d], w_router[E,d]: storage act_dt (F32 or BF16), fp32 accumulation.
+ *   sel_bias[E] fp32, or NULL for no bias; it changes which experts are kept,
+ *   never their weights.
+ *   topk_idx[T,k] int32 out: kept experts in ranking order (score descending,
+ *   then index ascending).
+ *   topk_w[T,k] fp32 out: softmax over the kept experts' unbiased logits;
+ *   with k == 1 every weight is exactly 1.0f.
+ */
+MOE_API moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                     const float *sel_bias, int E, int k, int32_t *topk_idx, float *topk_w,
+                     moe_stream stream);
+
+/*
+ * moe_permute -- step 3 (token grouping), integer-exact and atomic-free.
+ *   topk_idx[T,k] int32 in, each value in [0, E).
+ *   counts[E]      out: number of (t, j) slots routed to expert e.
+ *   offsets[E+1]   out: exclusive prefix sum of counts (offsets[E] == T*k).
+ *   perm_tok[T*k]  out: token of grouped row r; rows of expert e are
+ *                  [offsets[e], offsets[e+1]) in increasing flat slot order
+ *                  t*k + j (i.e. increasing t).
+ *   inv[T*k]       out: grouped row of flat slot t*k + j.
+ *   Out-of-range expert ids are not checked on the device; moe_forward's own
+ *   indices always come from moe_route.
+ */
+MOE_API moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
+                       int32_t *offsets, int32_t *perm_tok, int32_t *inv, moe_stream stream);
+
+/*
+ * Q8_0 expert weights.  Input format: rows of `cols` values along the
+ * contiguous (reduction) axis, stored as cols/32 blocks of 34 bytes
+ * {fp16 scale (little endian), int8 q[32]}; value = scale * q.
+ * moe_forward consumes them repacked into two planes in one buffer:
+ *   bytes [0, rows*cols)                     int8 q plane [rows, cols]
+ *   bytes [align256(rows*cols), ... + rows*cols/16)  fp16 scale plane [rows, cols/32]
+ * moe_q8_0_packed_size returns the buffer size (0 if cols % 32 != 0 or
+ * rows < 0).  moe_pack_q8_0 repacks `blocks` (device, any alignment) into
+ * `packed` (device, 256-byte aligned) on `stream`; pack W_g and W_u as
+ * rows = E*F, cols = d and W_d as rows = E*d, cols = F.
+ */
+MOE_API size_t moe_q8_0_packed_size(long long rows, int cols);
+MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
+                         moe_stream stream);
+
+/*
+ * Bytes of device workspace moe_forward needs for these sizes (any path).
+ * 0 on invalid sizes.  The workspace is scratch owned by the caller; its
+ * first 256 bytes hold the device status word read by moe_check.
+ */
+MOE_API size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype act_dt,
+                          moe_dtype w_dt);
+
+/*
+ * moe_forward -- the whole layer, steps 1-5.
+ *   x[T,d] (act_dt), w_router[E,d] (act_dt), sel_bias[E] fp32 or NULL,
+ *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0: packed by
+ *   moe_pack_q8_0), out[T,d] fp32 (overwritten).
+ *   workspace: device scratch of at least moe_workspace_size() bytes,
+ *   256-byte aligned; it must not be shared by calls that can overlap.
+ *   path: a moe_path value.  MOE_PATH_PREFILL needs bf16 activations,
+ *   bf16 or Q8_0 weights, d % 256 == 0 and F % 128 == 0, and returns
+ *   MOE_ERR_UNSUPPORTED otherwise.
+ *   Summation order: with k <= 2 the result is bitwise deterministic.
+ */
+MOE_API moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                       const float *sel_bias, int E, int k, const void *w_gate,
+                       const void *w_up, const void *w_down, moe_dtype w_dt, int F,
+                       float *out, void *workspace, size_t ws_bytes, int path,
+                       moe_stream stream);
+
+/*
+ * moe_forward_profiled -- moe_forward that also records caller-created CUDA
+ * events (cudaEvent_t, timing enabled) on `stream` at its stage boundaries,
+ * so a caller can time each kernel on the stream it runs on:
+ *   events[0] before routing          events[3] after the row gather
+ *   events[1] after routing           events[4] after gate/up + SwiGLU
+ *   events[2] after token grouping    events[5] after down + combine
+ * (on the decode path there is no gather: events[3] follows events[2]
+ * immediately).  events may be NULL, which makes this moe_forward.
+ */
+MOE_API moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
+                                        const void *w_router, const float *sel_bias, int E,
+                                        int k, const void *w_gate, const void *w_up,
+                                        const void *w_down, moe_dtype w_dt, int F, float *out,
+                                        void *workspace, size_t ws_bytes, int path,
+                                        void *const *events, moe_stream stream);
+
+/*
+ * moe_check -- wait for `stream`, then read the device status word that the
+ * most recent moe_forward on `workspace` left: MOE_OK, MOE_ERR_TIMEOUT (a
+ * bounded device wait gave up; outputs of that call are invalid) or
+ * MOE_ERR_DEVICE_CHECK.  `*device_word` (optional) receives the raw word.
+ */
+MOE_API moe_status moe_check(const void *workspace, uint32_t *device_word, moe_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

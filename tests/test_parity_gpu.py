@@ -1,0 +1,313 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bars: routing indices and token grouping bit-exact (indices wherever the
+oracle's ranking margin is >= 1e-3); routing weights within 2e-6; outputs with
+max|err| <= 1e-4 * RMS(ref) for fp32 and <= 2e-2 * RMS(ref) for bf16 / Q8_0.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+
+from helpers import (MARGIN, check_output, compare_routing, gpu_forward, sub_layer, to_dev,
+                     upload_layer)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+DECODE, PREFILL = 1, 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    pkg.load_library()
+    torch.cuda.set_device(0)
+
+
+def _route(layer):
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    x, wr, b = to_dev(layer.x, DEV), to_dev(layer.w_router, DEV), to_dev(layer.bias, DEV)
+    idx, w = pkg.moe_route(x, wr, b, layer.k)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
+def _oracle_route(layer):
+    logits = oracle.router_logits(layer.x, layer.act_dtype, layer.w_router, layer.E)
+    return oracle.selected_softmax(logits, layer.bias, layer.k)
+
+
+# ------------------------------------------------------------------ routing
+ROUTE_CASES = [
+    ("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode", 1),
+    ("zonos2_decode", 8), ("zonos2_decode", 64), ("zonos3_mini_prefill", None),
+    ("zonos2_prefill_q8", None),
+]
+
+
+@pytest.mark.parametrize("name,T", ROUTE_CASES)
+def test_route_matches_oracle(name, T):
+    w = wl.WORKLOADS[name]
+    # only x, W_r and the bias matter for routing: draw a small-F layer
+    layer = wl.make_layer(w, seed=1, T=T, F=32 if w.w_dtype != wl.Q8_0 else 32)
+    idx, wts = _route(layer)
+    idx_ref, w_ref, margin = _oracle_route(layer)
+    ok = compare_routing(idx, wts, idx_ref, w_ref, margin, layer.k)
+    assert ok.mean() > 0.95
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (5, 3, 3), (33, 2, 64), (300, 4, 256), (1000, 8, 16)])
+def test_route_edge_shapes(T, k, E):
+    layer = wl.make_custom_layer(7, T=T, d=64, E=E, k=k, F=32, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16, bias_sd=0.3)
+    idx, wts = _route(layer)
+    idx_ref, w_ref, margin = _oracle_route(layer)
+    compare_routing(idx, wts, idx_ref, w_ref, margin, k)
+    assert np.all(np.abs(wts.sum(1) - 1) < 1e-6)
+
+
+def test_route_ties_go_to_lower_index():
+    """Experts 1, 2, 3 share one router row (equal logits); 0, 4, 5 its negation."""
+    layer = wl.make_custom_layer(3, T=16, d=64, E=6, k=2, F=32, act_dtype=wl.F32,
+                                 w_dtype=wl.F32, bias_sd=0.0)
+    v = layer.w_router[0].copy()
+    layer.w_router[[1, 2, 3]] = v
+    layer.w_router[[0, 4, 5]] = -v
+    layer.x = (np.outer(np.arange(1, 17), v) * 4).astype(np.float32)   # x . v > 0
+    idx, wts = _route(layer)
+    assert np.all(idx == [1, 2])
+    assert np.all(wts == 0.5)
+
+
+# ------------------------------------------------------------------ permute
+@pytest.mark.parametrize("T,k,E", [(0, 2, 4), (1, 1, 1), (128, 2, 64), (8192, 2, 64),
+                                   (4096, 1, 16), (777, 3, 250), (40000, 8, 256)])
+def test_permute_bit_exact(T, k, E):
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    rng = np.random.default_rng(T + k + E)
+    if T:
+        # skewed choice: distinct experts per token, biased toward low ids
+        p = 1.0 / np.arange(1, E + 1)
+        p /= p.sum()
+        idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    else:
+        idx = np.zeros((0, k), np.int32)
+    counts, offsets, perm_tok, inv = pkg.moe_permute(to_dev(idx, DEV), E)
+    torch.cuda.synchronize()
+    c_ref, o_ref, p_ref, i_ref = oracle.permute(idx, E)
+    assert np.array_equal(counts.cpu().numpy(), c_ref)
+    assert np.array_equal(offsets.cpu().numpy(), o_ref)
+    assert np.array_equal(perm_tok.cpu().numpy(), p_ref)
+    assert np.array_equal(inv.cpu().numpy(), i_ref)
+
+
+# ------------------------------------------------- whole layer, small sizes
+SMALL = [
+    # (act, w, T, d, E, k, F)  -- several tiles and ragged tails
+    (wl.F32, wl.F32, 8, 64, 8, 2, 128),
+    (wl.F32, wl.F32, 37, 200, 7, 3, 72),
+    (wl.BF16, wl.BF16, 1, 256, 8, 2, 128),
+    (wl.BF16, wl.BF16, 61, 264, 12, 2, 136),
+    (wl.BF16, wl.BF16, 200, 512, 16, 1, 384),
+    (wl.BF16, wl.Q8_0, 45, 256, 8, 2, 160),
+    (wl.BF16, wl.Q8_0, 3, 2048, 16, 1, 2816),
+    (wl.BF16, wl.BF16, 96, 256, 4, 4, 128),     # k == E: dense gating
+]
+
+
+@pytest.mark.parametrize("act,wdt,T,d,E,k,F", SMALL)
+def test_forward_small_matches_oracle(act, wdt, T, d, E, k, F):
+    layer = wl.make_custom_layer(11, T=T, d=d, E=E, k=k, F=F, act_dtype=act, w_dtype=wdt,
+                                 bias_sd=0.3)
+    out = gpu_forward(layer, DEV, path=DECODE)
+    idx_g, _ = _route(layer)
+    torch.cuda.synchronize()
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
+    check_output(out.cpu().numpy(), layer, ref, idx_ref, margin, idx_gpu=idx_g)
+
+
+def test_forward_all_tokens_one_expert():
+    """A bias that sends every token to expert 3 (and 5): many row blocks in one expert."""
+    layer = wl.make_custom_layer(12, T=150, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    layer.bias[:] = 0
+    layer.bias[3] = 100.0
+    layer.bias[5] = 50.0
+    out = gpu_forward(layer, DEV, path=DECODE)
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    assert np.all(idx_ref == [3, 5])
+    check_output(out.cpu().numpy(), layer, ref, idx_ref, margin)
+
+
+def test_forward_empty_batch():
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(13, T=0, d=64, E=4, k=2, F=64, act_dtype=wl.F32,
+                                 w_dtype=wl.F32)
+    t = upload_layer(layer, DEV)
+    out = pkg.moe_forward(t["x"], t["w_router"], t["bias"], t["w_gate"], t["w_up"], t["w_down"], 2)
+    assert out.shape == (0, 64)
+
+
+def test_forward_no_bias_pointer():
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(14, T=20, d=128, E=8, k=2, F=64, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    t = upload_layer(layer, DEV)
+    out = pkg.moe_forward(t["x"], t["w_router"], None, t["w_gate"], t["w_up"], t["w_down"], 2)
+    layer.bias[:] = 0
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    check_output(out.cpu().numpy(), layer, ref, idx_ref, margin)
+
+
+# ------------------------------------------------------------- properties
+def test_deterministic_and_permutation_equivariant():
+    layer = wl.make_custom_layer(15, T=64, d=256, E=16, k=2, F=128, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    t = upload_layer(layer, DEV)
+    a = gpu_forward(layer, DEV, t=t).cpu().numpy()
+    b = gpu_forward(layer, DEV, t=t).cpu().numpy()
+    assert np.array_equal(a, b)
+    perm = np.random.default_rng(0).permutation(layer.T)
+    t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
+    c = gpu_forward(layer, DEV, t=t2).cpu().numpy()
+    assert np.array_equal(c, a[perm])
+
+
+def test_k1_weights_exactly_one_and_bias_only_selects():
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(16, T=100, d=128, E=8, k=3, F=64, act_dtype=wl.F32,
+                                 w_dtype=wl.F32)
+    x, wr = to_dev(layer.x, DEV), to_dev(layer.w_router, DEV)
+    _, w1 = pkg.moe_route(x, wr, None, 1)
+    assert torch.all(w1 == 1.0)
+    idx0, w0 = pkg.moe_route(x, wr, None, 3)
+    # bias forcing {1, 4, 6}: weights are the softmax of those unbiased logits
+    b = torch.zeros(8, device=DEV)
+    b[[1, 4, 6]] = 1e4
+    idx2, w2 = pkg.moe_route(x, wr, b, 3)
+    torch.cuda.synchronize()
+    logits = oracle.router_logits(layer.x, wl.F32, layer.w_router, 8)
+    ref = oracle.softmax_of_set(logits, idx2.cpu().numpy())
+    assert np.all(np.sort(idx2.cpu().numpy(), 1) == [1, 4, 6])
+    np.testing.assert_allclose(w2.cpu().numpy(), ref, atol=2e-6)
+
+
+def test_device_status_ok_after_forward():
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(17, T=32, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    t = upload_layer(layer, DEV)
+    ws = torch.empty(pkg.moe_workspace_size(32, 256, 8, 2, 128, 1, 1), dtype=torch.uint8,
+                     device=DEV)
+    gpu_forward(layer, DEV, t=t, workspace=ws)
+    assert pkg.moe_check(ws) == 0
+
+
+# -------------------------------------------------- workload sizes (full)
+@pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("zonos3_mini_decode", None),
+                                    ("zonos2_decode", 1), ("zonos2_decode", 8),
+                                    ("zonos2_decode", 64)])
+def test_forward_decode_workloads_full(name, T):
+    """Decode workloads at full size, in the launch configuration the benchmark
+    times (path AUTO), every output row against the oracle."""
+    layer = wl.make_layer(wl.WORKLOADS[name], seed=2, T=T)
+    out = gpu_forward(layer, DEV, path=0)
+    idx_g, w_g = _route(layer)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
+    compare_routing(idx_g, w_g, idx_ref, w_ref, margin, layer.k)
+    check_output(out.cpu().numpy(), layer, ref, idx_ref, margin, idx_gpu=idx_g)
+
+
+@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8"])
+@pytest.mark.parametrize("path", [DECODE, 0])
+def test_forward_prefill_workloads_sampled(name, path):
+    """Prefill workloads at full size; 96 sampled token rows against the oracle,
+    plus exact grouping of the GPU's own routing."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_layer(wl.WORKLOADS[name], seed=3)
+    t = upload_layer(layer, DEV)
+    out = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy()
+    idx_t, w_t = pkg.moe_route(t["x"], t["w_router"], t["bias"], layer.k)
+    counts, offsets, perm_tok, inv = pkg.moe_permute(idx_t, layer.E)
+    torch.cuda.synchronize()
+    idx_g = idx_t.cpu().numpy()
+    c_ref, o_ref, p_ref, i_ref = oracle.permute(idx_g, layer.E)
+    assert np.array_equal(counts.cpu().numpy(), c_ref)
+    assert np.array_equal(perm_tok.cpu().numpy(), p_ref)
+    rows = np.sort(np.random.default_rng(5).choice(layer.T, size=96, replace=False))
+    sub = sub_layer(layer, rows)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(sub)
+    compare_routing(idx_g[rows], w_t.cpu().numpy()[rows], idx_ref, w_ref, margin, layer.k)
+    check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g[rows])
+
+
+# ------------------------------------------- tensor-core (prefill) path
+PREFILL_SMALL = [
+    # (T, d, E, k, F): ragged groups, tiles crossing expert boundaries, empty experts
+    (130, 256, 2, 1, 128),
+    (300, 256, 4, 2, 128),
+    (1000, 512, 8, 2, 256),
+    (2048, 256, 16, 1, 384),
+    (520, 1024, 64, 2, 512),
+    (777, 2048, 16, 1, 256),
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,F", PREFILL_SMALL)
+def test_forward_prefill_small_matches_oracle(T, d, E, k, F):
+    layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16, bias_sd=0.5)
+    t = upload_layer(layer, DEV)
+    out = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
+    idx_g, _ = _route(layer)
+    rows = np.arange(T) if T <= 400 else np.sort(
+        np.random.default_rng(T).choice(T, size=400, replace=False))
+    sub = sub_layer(layer, rows)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(sub)
+    check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g[rows])
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    ws = torch.empty(pkg.moe_workspace_size(T, d, E, k, F, 1, 1), dtype=torch.uint8, device=DEV)
+    gpu_forward(layer, DEV, path=PREFILL, t=t, workspace=ws)
+    assert pkg.moe_check(ws) == 0
+
+
+def test_prefill_one_expert_many_tiles():
+    """Every token to experts 3 and 5: 1100 rows per group, a ragged last tile."""
+    layer = wl.make_custom_layer(22, T=1100, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    layer.bias[:] = 0
+    layer.bias[3] = 100.0
+    layer.bias[5] = 50.0
+    out = gpu_forward(layer, DEV, path=PREFILL).cpu().numpy()
+    rows = np.arange(0, 1100, 7)
+    sub = sub_layer(layer, rows)
+    ref, idx_ref, _, margin = oracle.moe_forward(sub)
+    check_output(out[rows], sub, ref, idx_ref, margin)
+
+
+def test_prefill_and_decode_paths_agree():
+    layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    t = upload_layer(layer, DEV)
+    a = gpu_forward(layer, DEV, path=DECODE, t=t).cpu().numpy().astype(np.float64)
+    b = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(a ** 2))
+    assert np.abs(a - b).max() <= 2e-2 * rms
+
+
+def test_prefill_deterministic_and_equivariant():
+    layer = wl.make_custom_layer(24, T=512, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    t = upload_layer(layer, DEV)
+    a = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
+    b = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
+    assert np.array_equal(a, b)
+    perm = np.random.default_rng(1).permutation(layer.T)
+    t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
+    c = gpu_forward(layer, DEV, path=PREFILL, t=t2).cpu().numpy()
+    assert np.array_equal(c, a[perm])
