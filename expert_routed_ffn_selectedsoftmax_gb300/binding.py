@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_permute",
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_workspace_size", "moe_forward",
-           "moe_forward_profiled", "moe_check")
+           "moe_forward_profiled", "moe_forward_noalloc", "moe_check")
 
 _lib = None
 
@@ -71,6 +71,8 @@ def load_library():
     L.moe_forward_profiled.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz,
                                        i, vp, vp]
     L.moe_forward_profiled.restype = i
+    L.moe_forward_noalloc.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, i, vp]
+    L.moe_forward_noalloc.restype = i
     L.moe_check.argtypes = [vp, vp, vp]
     L.moe_check.restype = i
     _lib = L
@@ -187,6 +189,31 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
                                       _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F,
                                       _ptr(out), _ptr(workspace), ws_len, path, handles,
                                       _stream(x)), "moe_forward_profiled")
+    return out
+
+
+def moe_forward_noalloc(x: torch.Tensor, w_router: torch.Tensor,
+                        sel_bias: Optional[torch.Tensor], w_gate: torch.Tensor,
+                        w_up: torch.Tensor, w_down: torch.Tensor, k: int, out: torch.Tensor,
+                        F: Optional[int] = None, w_dtype: Optional[int] = None,
+                        path: int = MOE_PATH_AUTO) -> torch.Tensor:
+    """moe_forward without a workspace: the library's static scratch is used.
+
+    For hosts that cannot allocate device memory; `out` must be supplied.
+    Layers needing more than 8 MiB of scratch raise MOE_ERR_WORKSPACE.
+    """
+    L = load_library()
+    T, d = x.shape
+    E = w_router.shape[0]
+    if w_dtype is None:
+        w_dtype = _act_dtype(w_gate)
+    if F is None:
+        if w_dtype == MOE_Q8_0:
+            raise ValueError("F is required for Q8_0 weights")
+        F = w_gate.shape[1]
+    _check(L.moe_forward_noalloc(_ptr(x), _act_dtype(x), T, d, _ptr(w_router), _ptr(sel_bias), E,
+                                 k, _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F, _ptr(out),
+                                 path, _stream(x)), "moe_forward_noalloc")
     return out
 
 

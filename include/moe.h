@@ -161,6 +161,35 @@ MOE_API moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, 
                                         void *const *events, moe_stream stream);
 
 /*
+ * moe_forward_noalloc -- moe_forward for callers that cannot allocate device
+ * memory.  (No counterpart on the source pages: an addition of this library.)
+ * Some hosts give the layer only its inputs and outputs -- serving runtimes
+ * and plugin hosts that own all device memory through their own pool and
+ * forbid cudaMalloc while serving, because it synchronises the device and can
+ * fail under a fixed memory budget.  This entry point takes the same arguments
+ * as moe_forward minus the workspace, runs the same kernels, and uses as
+ * scratch one static 8 MiB device array inside the library instead; it calls
+ * no allocator of any kind.
+ *  - Limit: layers whose moe_workspace_size() exceeds 8 MiB (8388608 bytes)
+ *    are rejected with MOE_ERR_WORKSPACE before anything is enqueued.
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the array's device address once; make that first call before any
+ *    stream capture.
+ *  - Sharing: every call, on any stream, uses the same array, which keeps the
+ *    previous call's contents (each call rewrites every scratch byte it reads,
+ *    and its first kernel clears the status word).  Calls that can overlap on
+ *    the GPU race on it: serialise them (one stream, or events).
+ *  - Memory: every GPU that loads the library holds the 8 MiB until exit.
+ *  - moe_check cannot be pointed at this scratch; launch and argument errors
+ *    come back as the return value.
+ */
+MOE_API moe_status moe_forward_noalloc(const void *x, moe_dtype act_dt, int T, int d,
+                                       const void *w_router, const float *sel_bias, int E, int k,
+                                       const void *w_gate, const void *w_up, const void *w_down,
+                                       moe_dtype w_dt, int F, float *out, int path,
+                                       moe_stream stream);
+
+/*
  * moe_check -- wait for `stream`, then read the device status word that the
  * most recent moe_forward on `workspace` left: MOE_OK, MOE_ERR_TIMEOUT (a
  * bounded device wait gave up; outputs of that call are invalid) or

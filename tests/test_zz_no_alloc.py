@@ -1,0 +1,74 @@
+"""moe_forward_noalloc: the layer for callers that cannot allocate device memory.
+
+Hosts such as serving runtimes or plugin hosts may own every byte of device
+memory and forbid cudaMalloc while serving.  The library gives them an entry
+point whose scratch lives in a static device array; these checks call it
+through the C ABI and compare it with moe_forward (same tolerance as the
+parity tests) on two consecutive calls with different inputs, so stale
+scratch from the first call would show in the second.  This file is named to
+be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+
+from helpers import TOL, upload_layer
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    torch.cuda.set_device(0)
+    return pkg.load_library()
+
+
+def _noalloc(lib, layer, t, out, path):
+    p = lambda a: ctypes.c_void_p(a.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.moe_forward_noalloc(p(t["x"]), layer.act_dtype, layer.T, layer.d, p(t["w_router"]),
+                                   p(t["bias"]), layer.E, layer.k, p(t["w_gate"]), p(t["w_up"]),
+                                   p(t["w_down"]), layer.w_dtype, layer.F, p(out), path, stream)
+
+
+@pytest.mark.parametrize("path,shape", [
+    (1, dict(T=96, d=256, E=16, k=2, F=128)),     # decode kernels
+    (2, dict(T=512, d=256, E=8, k=2, F=128)),     # tensor-core kernels
+])
+def test_noalloc_matches_moe_forward_twice(lib, path, shape):
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    for seed in (31, 32):   # two calls in a row, different inputs
+        layer = wl.make_custom_layer(seed, act_dtype=wl.BF16, w_dtype=wl.BF16, bias_sd=0.5,
+                                     **shape)
+        t = upload_layer(layer, DEV)
+        out = torch.full((layer.T, layer.d), float("nan"), dtype=torch.float32, device=DEV)
+        assert _noalloc(lib, layer, t, out, path) == 0
+        ref = pkg.moe_forward(t["x"], t["w_router"], t["bias"], t["w_gate"], t["w_up"],
+                              t["w_down"], layer.k, path=path)
+        torch.cuda.synchronize()
+        a = out.cpu().numpy().astype(np.float64)
+        b = ref.cpu().numpy().astype(np.float64)
+        rms = np.sqrt(np.mean(b ** 2))
+        assert np.all(np.isfinite(a))
+        assert np.abs(a - b).max() <= TOL[wl.BF16] * rms
+
+
+def test_noalloc_rejects_layers_beyond_the_static_scratch(lib):
+    layer_T, d, E, k, F = 8192, 1024, 64, 2, 512     # needs ~67 MB of scratch
+    assert lib.moe_workspace_size(layer_T, d, E, k, F, 1, 1) > 8 << 20
+    fake = ctypes.c_void_p(0x10000)    # rejected before any pointer is used
+    st = lib.moe_forward_noalloc(fake, 1, layer_T, d, fake, None, E, k, fake, fake, fake, 1, F,
+                                 fake, 0, None)
+    assert st == 3                     # MOE_ERR_WORKSPACE
+    # invalid arguments are still reported as such
+    assert lib.moe_forward_noalloc(fake, 1, 4, 64, fake, None, 4, 5, fake, fake, fake, 1, 64,
+                                   fake, 0, None) == 1
