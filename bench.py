@@ -157,6 +157,22 @@ def algorithmic(w, T, counts_per_layer):
     return total
 
 
+def expert_kernel_names(w, T):
+    """Which expert kernels moe_forward's AUTO path runs for this workload
+    (mirrors the library's selection: tensor-core decode for bf16 layers with
+    d, F multiples of 128 and T*k <= 8192; grouped GEMMs from 64 rows per
+    expert on average and T >= 512)."""
+    rows = T * w.k
+    bf16 = w.act_dtype == 1 and w.w_dtype == 1
+    if bf16 and w.d % 256 == 0 and w.F % 128 == 0 and rows >= 64 * w.E and T >= 512:
+        return {"file": "tc_gemm.cu", "gateup": "grouped_gemm_kernel<GATEUP>",
+                "down": "grouped_gemm_kernel<DOWN>"}
+    if bf16 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
+        return {"file": "decode_tc.cu", "gateup": "decode_tc_kernel<GATEUP>",
+                "down": "decode_tc_kernel<DOWN> + combine_kernel"}
+    return {"file": "decode.cu", "gateup": "decode_gateup_kernel", "down": "decode_down_kernel"}
+
+
 def profile_traffic(kernel_key):
     """dram bytes per launch recorded from an ncu capture, if the kernel source
     it was taken on is unchanged (else None)."""
@@ -377,19 +393,20 @@ def main():
                 for s in range(5):
                     stage_ms[s] += evs[i][s].elapsed_time(evs[i][s + 1])
     stage_us = stage_ms / (n_prof * layers) * 1e3     # per launch, µs
-    names = ["route", "permute", "gather", "gateup", "down"]
+    stage_names = ["route", "permute", "gather", "gateup", "down"]
 
     # ------------------------------------------------------- roofline object
     peaks, peak_src = load_peaks()
     hbm = peak_value(peaks, "hbm_gbs")
     gu_bytes_per_launch = alg["gateup_bytes"] / layers
     dn_bytes_per_launch = alg["down_bytes"] / layers
+    names = expert_kernel_names(w, T)
     dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
     dom_bytes = gu_bytes_per_launch if dominant == "gateup" else dn_bytes_per_launch
     dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-    traffic = profile_traffic(f"decode.cu:{dominant}")
-    roofline = {"bound": "hbm", "kernel": f"decode_{dominant}_kernel", "achieved": achieved,
+    traffic = profile_traffic(f"{names['file']}:{dominant}")
+    roofline = {"bound": "hbm", "kernel": names[dominant], "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                 "peak_source": f"hbm_gbs of {peak_src}",
                 "bytes_per_launch": dom_bytes, "us_per_launch": dom_us}
@@ -450,7 +467,7 @@ def main():
                   "frac_hbm": layer_gbs / hbm, "bytes_per_step": alg["bytes"],
                   "flops_per_step": alg["flops"],
                   "active_experts_per_layer": alg["active"],
-                  "stage_us": dict(zip(names, [round(float(v), 3) for v in stage_us]))},
+                  "stage_us": dict(zip(stage_names, [round(float(v), 3) for v in stage_us]))},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -16,7 +16,7 @@ import torch
 from . import build as _build
 
 MOE_F32, MOE_BF16, MOE_Q8_0 = 0, 1, 2
-MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
+MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_PATH_DECODE_SIMT = 0, 1, 2, 3
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
           6: "MOE_ERR_DEVICE_CHECK"}

@@ -42,7 +42,9 @@ moe_status check_route_args(const void *x, int act_dt, int T, int d, const void 
 }
 
 struct WsLayout {
-    size_t status, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w, h, xp, total;
+    size_t status, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w, h, xp, pgu, pd,
+        rank, tile_cnt, total;
+    bool dtc;   // tensor-core decode partials present
 };
 
 bool prefill_capable(int act_dt, int w_dt, int d, int F)
@@ -65,8 +67,20 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.perm_tok = take(4 * n);
     L.inv = take(4 * n);
     L.perm_w = take(4 * n);
+    L.rank = take(4 * n);
+    L.tile_cnt = take(4 * (size_t)(T > 0 ? T : 1) * (size_t)E);   // <= one tile per token
     L.h = take(4 * n * (size_t)F);            // fp32 (decode); prefill uses 2 bytes/element
-    L.xp = prefill_capable(act_dt, w_dt, d, F) ? take(2 * n * (size_t)d) : off;
+    // the decode_tc_capable() shape/dtype conditions, without the driver query
+    L.dtc = act_dt == MOE_BF16 && w_dt == MOE_BF16 && d % 128 == 0 && F % 128 == 0 &&
+            n <= (size_t)kDecodeTcMaxRows;
+    L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
+    L.pgu = L.pd = off;
+    if (L.dtc) {
+        int ks_gu = 1, ks_d = 1;
+        decode_tc_splits(T, d, E, k, F, &ks_gu, &ks_d);
+        L.pgu = take(4 * (size_t)ks_gu * 2 * n * (size_t)F);
+        L.pd = take(4 * (size_t)ks_d * n * (size_t)d);
+    }
     L.total = off;
     return L;
 }
@@ -110,8 +124,16 @@ moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *
     if (!topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
         return MOE_ERR_INVALID_ARG;
-    cudaError_t e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w,
-                                 nullptr, nullptr, static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
+        RouteTcArgs a{};
+        a.x = x; a.w_router = w_router; a.bias = sel_bias; a.T = T; a.d = d; a.E = E; a.k = k;
+        a.topk_idx = topk_idx; a.topk_w = topk_w;
+        e = launch_route_tc(a, static_cast<cudaStream_t>(stream));
+    } else {
+        e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w, nullptr,
+                         nullptr, 0, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -178,7 +200,8 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
                                                                          : MOE_ERR_INVALID_ARG;
     }
     if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
-    if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL)
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL &&
+        path != MOE_PATH_DECODE_SIMT)
         return MOE_ERR_INVALID_ARG;
     const bool can_prefill = prefill_capable(act_dt, w_dt, d, F) && tc_gemm_supports(w_dt) &&
                              tc_gemm_available();
@@ -218,11 +241,38 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     auto mark = [&](int i) { return ev[i] ? cudaEventRecord(ev[i], s) : cudaSuccess; };
 
     if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
-    cudaError_t e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w,
-                                 k > 1 ? out : nullptr, status, s);
-    if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_permute(topk_idx, T, k, E, counts, offsets, perm_tok, inv, topk_w, perm_w, status, s);
-    if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+    const bool use_dtc = !use_prefill && path != MOE_PATH_DECODE_SIMT && L.dtc &&
+                         decode_tc_capable(act_dt, w_dt, d, F, E);
+    // the combine steps that accumulate into `out` need it zeroed first
+    const bool zero_out = k > 1 && !use_dtc;
+    // routing, then the grouping scatter (which also writes the grouped x rows
+    // that the tensor-core expert kernels read)
+    RouteTcArgs ra{};
+    ra.x = x; ra.w_router = w_router; ra.bias = sel_bias; ra.T = T; ra.d = d; ra.E = E; ra.k = k;
+    ra.topk_idx = topk_idx; ra.topk_w = topk_w;
+    ra.rank = reinterpret_cast<int32_t *>(ws + L.rank);
+    ra.tile_cnt = reinterpret_cast<int32_t *>(ws + L.tile_cnt);
+    ra.counts = counts; ra.offsets = offsets; ra.perm_tok = perm_tok; ra.inv = inv; ra.perm_w = perm_w;
+    const bool act16 = act_dt == MOE_BF16;
+    ra.xp = ((use_prefill || use_dtc) && act16) ? ws + L.xp : nullptr;
+    ra.out_zero = zero_out ? out : nullptr;
+    ra.zero_words = nullptr;
+    ra.n_zero = 0;
+    ra.status = status;
+    ra.ev_routed = ev[1];
+    const bool xp_ready = ra.xp != nullptr;
+    cudaError_t e;
+    if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
+        e = launch_route_tc(ra, s);
+        if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+    } else {
+        e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w, ra.out_zero,
+                         ra.zero_words, ra.n_zero, ra.rank, ra.tile_cnt, status, s);
+        if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+        const int tpb = route_tokens_per_block(T, d, E);
+        e = launch_scatter(ra, (T + tpb - 1) / tpb, tpb, s);
+        if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+    }
 
     const int num_sms = device_sm_count();
     if (use_prefill) {
@@ -230,9 +280,23 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
         a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
         a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down; a.w_dt = w_dt;
         a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
-        a.xp = ws + L.xp; a.h = ws + L.h; a.out = out; a.status = status; a.num_sms = num_sms;
+        a.xp = ws + L.xp; a.xp_ready = xp_ready;
+        a.h = ws + L.h; a.out = out; a.status = status; a.num_sms = num_sms;
         a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
         e = launch_tc_experts(a, s);
+    } else if (use_dtc) {
+        DecodeTcArgs a{};
+        a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
+        a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down;
+        a.offsets = offsets; a.inv = inv; a.topk_w = topk_w; a.xp = ws + L.xp;
+        a.pgu = reinterpret_cast<float *>(ws + L.pgu); a.pd = reinterpret_cast<float *>(ws + L.pd);
+        a.h = reinterpret_cast<uint16_t *>(ws + L.h);
+        a.out = out; a.status = status; a.num_sms = num_sms; a.ev_gateup = ev[4];
+        if (!xp_ready &&
+            launch_gather_rows(x, d, perm_tok, T * k, ws + L.xp, 0, num_sms, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+        e = launch_decode_tc(a, s);
     } else {
         DecodeArgs a{};
         a.x = x; a.act_dt = act_dt; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;

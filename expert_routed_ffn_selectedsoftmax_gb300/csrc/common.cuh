@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -124,6 +126,43 @@ template <> struct WView<Q8Tag> {
         }
     }
 };
+
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while its predecessor in the stream finishes; it calls
+// pdl_wait() before touching global memory (this waits for the predecessor to
+// complete and its writes to be visible) and pdl_trigger() right after, which
+// lets the next kernel of the stream start launching in turn.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() { pdl_wait(); pdl_trigger(); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// True (uniformly across the CTA) when an earlier kernel of this call has
+// already recorded an error in the status word: the caller then returns
+// without touching scratch whose contents may be incomplete.
+__device__ __forceinline__ bool upstream_failed(const uint32_t *status)
+{
+    __shared__ int failed;
+    if (threadIdx.x == 0) failed = status ? (int)*(volatile const uint32_t *)status : 0;
+    __syncthreads();
+    return failed != 0;
+}
 
 // -------------------------------------------------------------- warp helpers
 __device__ __forceinline__ float warp_sum(float v)

@@ -66,6 +66,7 @@ decode_gateup_kernel(const AT *__restrict__ x, int d, WView<WT> wg, WView<WT> wu
                      const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
                      int E, float *__restrict__ h)
 {
+    pdl_enter();
     __shared__ int act[kMaxExperts];
     __shared__ int wtot[kDecWarps];
     const int n_act = build_active_list(offsets, E, act, wtot);
@@ -129,6 +130,7 @@ decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
                    const float *__restrict__ perm_w, int E, int k, float *__restrict__ out)
 {
+    pdl_enter();
     __shared__ int act[kMaxExperts];
     __shared__ int wtot[kDecWarps];
     const int n_act = build_active_list(offsets, E, act, wtot);
@@ -214,12 +216,12 @@ static cudaError_t launch_t(const DecodeArgs &a, WView<WT> wg, WView<WT> wu, WVi
     int g2 = (int)(items2 < (long long)a.num_sms * occ2 ? items2 : (long long)a.num_sms * occ2);
     if (g1 < 1) g1 = 1;
     if (g2 < 1) g2 = 1;
-    k1<<<g1, kDecThreads, 0, stream>>>(static_cast<const AT *>(a.x), a.d, wg, wu, a.F, a.offsets,
+    launch_pdl(k1, dim3(g1), dim3(kDecThreads), 0, stream, static_cast<const AT *>(a.x), a.d, wg, wu, a.F, a.offsets,
                                         a.perm_tok, a.E, a.h);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
-    k2<<<g2, kDecThreads, 0, stream>>>(a.h, a.F, wd, a.d, a.offsets, a.perm_tok, a.perm_w, a.E,
+    launch_pdl(k2, dim3(g2), dim3(kDecThreads), 0, stream, a.h, a.F, wd, a.d, a.offsets, a.perm_tok, a.perm_w, a.E,
                                         a.k, a.out);
     return cudaGetLastError();
 }

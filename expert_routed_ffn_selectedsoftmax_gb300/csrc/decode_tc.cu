@@ -1,0 +1,441 @@
+// decode_tc.cu -- expert FFN for decode-sized batches on tcgen05, weights
+// streamed by TMA.
+//
+// At decode sizes an expert holds a handful of token rows, and the layer's
+// cost is reading the active experts' weights once from HBM ("Zyphra-ZONOS2-
+// 4bit", §Performance notes: batch-1 MoE reads ~1/16 of the experts; batching
+// touches more distinct experts until the read is bandwidth bound).  The
+// contraction is still dense -- [rows x K] . [K x weight rows] per expert --
+// so it runs on the tensor cores with the operands swapped: a 128-row weight
+// tile is the M operand (TMA, 128-byte swizzle, an 8-deep ring of 16 KB
+// stages per SM), the expert's token rows (padded to 16 or 32) are the N
+// operand, and fp32 accumulators live in TMEM.  This keeps the instruction
+// count per weight byte near zero, which the CUDA-core version could not.
+//
+// Work item = (expert, chunk of <= 32 token rows, weight matrix, 128-row
+// tile, K split).  K is split so that every SM streams several items; partial
+// sums go to fp32 scratch and are always reduced in split order, so results
+// are bitwise reproducible.
+//   GATEUP: matrices W_g, W_u; B operand = grouped x rows; partials
+//           Pgu[s][m][row][f].
+//   swiglu: h = SiLU(sum_s G) * sum_s U as bf16 [rows, F] (elementwise).
+//   DOWN:   matrix W_d; B operand = h rows; partials Pd[s][row][o].
+//   combine: out[t] = sum_j w[t,j] * sum_s Pd[s][inv[t,j]]  (fp32).
+// Both operands of every ring stage arrive by TMA, so the MMA thread only
+// waits for data and the epilogue only reads TMEM and stores partials.
+//
+// CTA: warp 0 = TMA producer, warp 1 = MMA issuer (+ TMEM owner), warps 2-5
+// stage the B operand of the next item and drain the accumulator of the
+// previous one.  All mbarrier waits are bounded (see sm100.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tc_gemm.h"
+
+namespace moe {
+namespace dtc {
+
+using namespace sm100;
+
+// Tuning (compile-time): ring depth, resident CTAs per SM, target item count.
+#ifndef MOE_DTC_STAGES
+#define MOE_DTC_STAGES 4
+#endif
+#ifndef MOE_DTC_CTAS_PER_SM
+#define MOE_DTC_CTAS_PER_SM 2
+#endif
+#ifndef MOE_DTC_TARGET_ITEMS
+#define MOE_DTC_TARGET_ITEMS 608
+#endif
+
+constexpr int BM = 128, BK = 64, STAGES = MOE_DTC_STAGES;
+constexpr int CTAS_PER_SM = MOE_DTC_CTAS_PER_SM;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB weight tile
+constexpr int NTMAX = 32;                       // token rows per item
+constexpr int B_BYTES = NTMAX * BK * 2;         // 4 KB token tile (16 or 32 rows used)
+constexpr int SLOT = A_BYTES + B_BYTES;         // 20 KB per stage, 1024-aligned
+constexpr int KBMAX = 8;                        // k-blocks per item
+constexpr int THREADS = 192;
+constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
+constexpr int TMEM_COLS = 128;
+constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~4 items per SM on 152 SMs
+
+enum Mode { GATEUP = 0, DOWN = 1 };
+
+struct Params {
+    const int32_t *offsets;
+    int E;
+    int K, R, n_mats, KS, kb_total, rows_total, rtiles;
+    float *P;            // partial outputs [KS][n_mats][rows_total][R]
+    uint32_t *status;
+};
+
+struct Ctl {
+    uint64_t full[STAGES], empty[STAGES], tfull[NACC], tempty[NACC], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int n_items;
+    int unit_start[kMaxExperts + 1];
+    int off[kMaxExperts + 1];
+};
+
+struct Item {
+    int e, nc, m, rt, s;
+    int row0, nrows, nt, kb0, nkb;
+};
+
+__device__ __forceinline__ Item decode_item(const Ctl &c, const Params &p, int item)
+{
+    int lo = 0, hi = p.E - 1;   // largest e with unit_start[e] <= item
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (c.unit_start[mid] <= item) lo = mid;
+        else hi = mid - 1;
+    }
+    Item it;
+    it.e = lo;
+    const int units = p.n_mats * p.rtiles * p.KS;
+    int local = item - c.unit_start[lo];
+    it.nc = local / units;
+    local -= it.nc * units;
+    it.m = local / (p.rtiles * p.KS);
+    local -= it.m * (p.rtiles * p.KS);
+    it.rt = local / p.KS;
+    it.s = local - it.rt * p.KS;
+    const int rows_e = c.off[lo + 1] - c.off[lo];
+    it.row0 = c.off[lo] + it.nc * NTMAX;
+    it.nrows = min(NTMAX, rows_e - it.nc * NTMAX);
+    it.nt = it.nrows <= 16 ? 16 : 32;
+    it.kb0 = it.s * p.kb_total / p.KS;
+    it.nkb = (it.s + 1) * p.kb_total / p.KS - it.kb0;
+    return it;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// tm_w0/tm_w1: weight matrices (box 64 x 128 rows); tm_b16/tm_b32: the token
+// rows (grouped x for GATEUP, h for DOWN) with boxes of 16 and 32 rows.
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                 const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
+                 const Params p)
+{
+    pdl_enter();
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Ctl &c = *reinterpret_cast<Ctl *>(smem + STAGES * SLOT);
+
+    if (upstream_failed(p.status)) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
+        for (int b = 0; b < NACC; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
+        mbar_init(&c.drain, 1);
+        c.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
+        if (MODE == GATEUP)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w1)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b16)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b32)) : "memory");
+    }
+    for (int e = threadIdx.x; e <= E; e += THREADS) c.off[e] = p.offsets[e];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int units = p.n_mats * p.rtiles * p.KS;
+        int local[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            int n = 0;
+            if (e < E) n = (c.off[e + 1] - c.off[e] + NTMAX - 1) / NTMAX;
+            local[j] = n * units;
+            sum += local[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            if (e < E) c.unit_start[e] = run;
+            run += local[j];
+        }
+        if (lane == 31) { c.n_items = incl; c.unit_start[E] = incl; }
+    }
+    if (warp == 1) tmem_alloc(&c.tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem = c.tmem_base;
+    const int n_items = c.n_items;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer: weights + token rows
+        uint32_t it_k = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item it = decode_item(c, p, item);
+            const CUtensorMap *wmap = (MODE == GATEUP && it.m == 1) ? &tm_w1 : &tm_w0;
+            const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
+            const uint32_t bytes = A_BYTES + it.nt * BK * 2;
+            const int wrow = it.e * p.R + it.rt * BM;
+            for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
+                const int s = it_k % STAGES;
+                const uint32_t ph = (it_k / STAGES) & 1u;
+                if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(&c.full[s], bytes);
+                const int kx = (it.kb0 + kbl) * BK;
+                tma_load_2d(smem + s * SLOT, wmap, &c.full[s], kx, wrow);
+                tma_load_2d(smem + s * SLOT + A_BYTES, bmap, &c.full[s], kx, it.row0);
+            }
+        }
+        if (!ok) {
+            atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+            for (uint32_t j = (it_k >= STAGES ? it_k - STAGES : 0); j < it_k; ++j) {
+                volatile int no_abort = 0;
+                mbar_wait(&c.full[j % STAGES], (j / STAGES) & 1u, &no_abort);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        uint32_t it_k = 0, li = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++li) {
+            const Item it = decode_item(c, p, item);
+            const uint32_t acc = li % NACC, aph = (li / NACC) & 1u;
+            if (!mbar_wait(&c.tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * 32;
+            const uint32_t idesc = idesc_f16_mn(0, BM, it.nt);
+            for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
+                const int s = it_k % STAGES;
+                const uint32_t ph = (it_k / STAGES) & 1u;
+                if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smem + s * SLOT);
+                const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                             (kbl | kk) != 0);
+                umma_commit(&c.empty[s]);
+            }
+            if (!ok) break;
+            umma_commit(&c.tfull[acc]);
+        }
+        if (!ok) {
+            atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+            umma_commit(&c.drain);
+            volatile int no_abort = 0;
+            mbar_wait(&c.drain, 0, &no_abort);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue (4 warps)
+        const int quarter = warp & 3;
+        uint32_t li = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++li) {
+            const Item it = decode_item(c, p, item);
+            const uint32_t acc = li % NACC, aph = (li / NACC) & 1u;
+            // warp-uniform outcome: tcgen05.ld below is warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(&c.tfull[acc], aph, abort_flag))) { ok = false; break; }
+            tc_fence_after();
+            uint32_t v[32];
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 32;
+            tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            if (it.nt > 16) tmem_ld16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&c.tempty[acc]);          // accumulator is in registers now
+            const int wr = it.rt * BM + quarter * 32 + lane;   // weight row = output column
+            float *dst = p.P + ((size_t)(it.s * p.n_mats + it.m) * p.rows_total + it.row0) * p.R + wr;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < it.nrows) dst[(size_t)j * p.R] = __uint_as_float(v[j]);
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// h[row, f] = SiLU(sum_s G[s][row][f]) * sum_s U[s][row][f], bf16 (fixed order)
+__global__ void swiglu_reduce_kernel(const float *__restrict__ pgu, int KS, int rows, int F,
+                                     uint16_t *__restrict__ h, const uint32_t *status)
+{
+    pdl_enter();
+    if (upstream_failed(status)) return;
+    const int vec = F / 4;
+    const long long total = (long long)rows * vec;
+    const size_t mat = (size_t)rows * F;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const size_t o = (size_t)i * 4;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int s = 0; s < KS; ++s) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(pgu + (size_t)(2 * s) * mat + o));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(pgu + (size_t)(2 * s + 1) * mat + o));
+            g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+            u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(silu_f(g.x) * u.x, silu_f(g.y) * u.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+        uint2 packed = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+        *reinterpret_cast<uint2 *>(h + o) = packed;
+    }
+}
+
+// out[t, :] = sum_j w[t, j] * sum_s Pd[s][inv[t, j]][:]   (fixed order)
+__global__ void combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
+                               const int32_t *__restrict__ inv, const float *__restrict__ topk_w,
+                               int T, int k, float *__restrict__ out, const uint32_t *status)
+{
+    pdl_enter();
+    if (upstream_failed(status)) return;
+    const int vec = d / 4;
+    const long long total = (long long)T * vec;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / vec), o = (int)(i - (long long)t * vec) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int r = inv[t * k + j];
+            const float w = topk_w[t * k + j];
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < KS; ++s) {
+                const float4 v = *reinterpret_cast<const float4 *>(pd + ((size_t)s * rows_total + r) * d + o);
+                y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+            }
+            acc.x += w * y.x; acc.y += w * y.y; acc.z += w * y.z; acc.w += w * y.w;
+        }
+        *reinterpret_cast<float4 *>(out + (size_t)t * d + o) = acc;
+    }
+}
+
+constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * SLOT + sizeof(Ctl); }
+
+int choose_splits(int kb_total, long long units)
+{
+    long long ks = (kTargetItems + units - 1) / (units > 0 ? units : 1);
+    const int min_ks = (kb_total + KBMAX - 1) / KBMAX;   // keep each split <= KBMAX k-blocks
+    if (ks < min_ks) ks = min_ks;
+    if (ks > kb_total) ks = kb_total;
+    if (ks < 1) ks = 1;
+    return (int)ks;
+}
+
+}  // namespace dtc
+
+bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E)
+{
+    return act_dt == MOE_BF16 && w_dt == MOE_BF16 && d % 128 == 0 && F % 128 == 0 &&
+           E <= kMaxExperts && tc_gemm_available();
+}
+
+void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d)
+{
+    const long long n_exp = (long long)(E < T * k ? E : T * k);
+    *ks_gu = dtc::choose_splits(d / dtc::BK, n_exp * 2 * (F / dtc::BM));
+    *ks_d = dtc::choose_splits(F / dtc::BK, n_exp * (d / dtc::BM));
+}
+
+cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
+{
+    using namespace dtc;
+    const int rows = a.T * a.k;
+    int ks_gu, ks_d;
+    decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
+
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap m_wg, m_wu, m_wd, m_x16, m_x32, m_h16, m_h32;
+    if (!tc::make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BM, bf) ||
+        !tc::make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BM, bf) ||
+        !tc::make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BM, bf) ||
+        !tc::make_map(&m_x16, a.xp, (uint64_t)rows, a.d, 16, bf) ||
+        !tc::make_map(&m_x32, a.xp, (uint64_t)rows, a.d, 32, bf) ||
+        !tc::make_map(&m_h16, a.h, (uint64_t)rows, a.F, 16, bf) ||
+        !tc::make_map(&m_h32, a.h, (uint64_t)rows, a.F, 32, bf))
+        return cudaErrorInvalidValue;
+
+    cudaError_t err;
+    const size_t smem = smem_bytes();
+    static std::atomic<int> attr_done{0};
+    if (!attr_done.load()) {
+        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+                cudaSuccess)
+            return err;
+        attr_done.store(1);
+    }
+    const long long n_exp = a.E < rows ? a.E : rows;
+    auto grid_for = [&](long long max_items) {
+        const long long slots = (long long)a.num_sms * CTAS_PER_SM;
+        long long g = max_items < slots ? max_items : slots;
+        return (int)(g < 1 ? 1 : g);
+    };
+
+    Params p{};
+    p.offsets = a.offsets; p.E = a.E; p.rows_total = rows; p.status = a.status;
+    // upper bound on items: chunks <= n_exp + rows / NTMAX
+    const long long chunks = n_exp + rows / NTMAX;
+
+    // gate/up: matrices W_g, W_u ([E*F, d]), K = d, token rows = grouped x
+    p.K = a.d; p.R = a.F; p.n_mats = 2; p.KS = ks_gu; p.kb_total = a.d / BK; p.rtiles = a.F / BM;
+    p.P = a.pgu;
+    launch_pdl(decode_tc_kernel<GATEUP>, dim3(grid_for(chunks * 2 * p.rtiles * ks_gu)), dim3(THREADS), smem, stream, 
+        m_wg, m_wu, m_x16, m_x32, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    auto elementwise_grid = [&](long long total) {
+        long long blocks = (total + 255) / 256;
+        if (blocks > (long long)a.num_sms * 8) blocks = (long long)a.num_sms * 8;
+        return (int)(blocks < 1 ? 1 : blocks);
+    };
+    launch_pdl(swiglu_reduce_kernel, dim3(elementwise_grid((long long)rows * (a.F / 4))), dim3(256), 0, stream, 
+        a.pgu, ks_gu, rows, a.F, a.h, a.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
+
+    // down: matrix W_d ([E*d, F]), K = F, token rows = h
+    p.K = a.F; p.R = a.d; p.n_mats = 1; p.KS = ks_d; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
+    p.P = a.pd;
+    launch_pdl(decode_tc_kernel<DOWN>, dim3(grid_for(chunks * p.rtiles * ks_d)), dim3(THREADS), smem, stream, 
+        m_wd, m_wd, m_h16, m_h32, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+    launch_pdl(combine_kernel, dim3(elementwise_grid((long long)a.T * (a.d / 4))), dim3(256), 0, stream, 
+        a.pd, ks_d, rows, a.d, a.inv, a.topk_w, a.T, a.k, a.out, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

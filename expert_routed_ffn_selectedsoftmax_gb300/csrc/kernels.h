@@ -10,9 +10,43 @@ namespace moe {
 
 // route.cu
 size_t route_smem_bytes(int tpb, int d, int E);
+// out_zero: rows [T, d] to zero (or NULL); zero_words[n_zero]: scratch words
+// later kernels need zeroed (or NULL); rank/tile_cnt: grouping inputs for the
+// scatter over tiles of route_tokens_per_block() tokens (or NULL); status:
+// device status word to clear.
+int route_tokens_per_block(int T, int d, int E);
 cudaError_t launch_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                          const float *bias, int E, int k, int32_t *topk_idx, float *topk_w,
-                         float *out_zero, uint32_t *status, cudaStream_t stream);
+                         float *out_zero, uint32_t *zero_words, int n_zero, int32_t *rank,
+                         int32_t *tile_cnt, uint32_t *status, cudaStream_t stream);
+// the tensor-core router pays off from this many tokens (one 128-row tile per CTA)
+constexpr int kRouteTcMinTokens = 512;
+
+// route_tc.cu -- tensor-core router + SelectedSoftmax, then the grouping scatter
+struct RouteTcArgs {
+    const void *x;              // [T, d] bf16
+    const void *w_router;       // [E, d] bf16
+    const float *bias;          // [E] or NULL
+    int T, d, E, k;
+    int32_t *topk_idx;          // [T*k]
+    float *topk_w;              // [T*k]
+    int32_t *rank;              // [T*k] scratch, or NULL (routing only)
+    int32_t *tile_cnt;          // [route_tc_tiles(T) * E] scratch, or NULL
+    // grouping outputs (counts == NULL: routing only, no scatter launch)
+    int32_t *counts, *offsets, *perm_tok, *inv;
+    float *perm_w;
+    void *xp;                   // optional [T*k, d] bf16 grouped copy of x
+    float *out_zero;            // optional rows to zero
+    uint32_t *zero_words;       // optional scratch words to zero
+    int n_zero;
+    uint32_t *status;
+    cudaEvent_t ev_routed;      // optional: recorded between routing and scatter
+};
+bool route_tc_capable(int act_dt, int d, int E);
+int route_tc_tiles(int T);
+cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream);
+// grouping scatter over token tiles of `tile_tokens` (counts/ranks from either router)
+cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cudaStream_t stream);
 
 // permute.cu
 cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
@@ -38,6 +72,28 @@ struct DecodeArgs {
     cudaEvent_t ev_gateup;      // optional: recorded between the two kernels
 };
 cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream);
+
+// decode_tc.cu -- expert FFN for few rows per expert on tcgen05 (bf16 only)
+struct DecodeTcArgs {
+    const void *x;              // [T, d] bf16
+    const void *xp;             // [T*k, d] bf16 grouped rows of x
+    int T, d, E, k, F;
+    const void *w_gate, *w_up, *w_down;   // bf16
+    const int32_t *offsets;     // [E+1]
+    const int32_t *inv;         // [T*k]
+    const float *topk_w;        // [T*k]
+    float *pgu;                 // gate/up partials [ks_gu][2][T*k][F]
+    uint16_t *h;                // bf16 h [T*k, F] scratch
+    float *pd;                  // down partials [ks_d][T*k][d]
+    float *out;                 // [T, d] fp32 (fully written)
+    uint32_t *status;
+    int num_sms;
+    cudaEvent_t ev_gateup;
+};
+constexpr int kDecodeTcMaxRows = 8192;   // T*k above this uses the CUDA-core kernels
+bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E);
+void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d);
+cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream);
 
 // q8.cu
 cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,

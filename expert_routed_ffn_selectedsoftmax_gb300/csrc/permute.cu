@@ -7,7 +7,7 @@
 // port ("zonos2.cpp internals", §Performance); the grouping here is its
 // explicit form.
 //
-// One CTA of 32 warps.  Warp w owns the contiguous flat-slot range
+// One CTA of 8-32 warps (more for more slots).  Warp w owns the contiguous flat-slot range
 // [w*chunk, (w+1)*chunk).  Pass 1: each warp counts its range per expert
 // (__match_any_sync finds the lanes sharing an expert; the lowest of them adds
 // the group size to the warp's private counter).  Scan: counts, exclusive
@@ -20,26 +20,28 @@
 
 namespace moe {
 
-constexpr int kPermThreads = 1024;
-constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kPermMaxWarps = 32;
 
-__global__ void __launch_bounds__(kPermThreads)
+__global__ void __launch_bounds__(kPermMaxWarps * 32)
 permute_kernel(const int32_t *__restrict__ topk_idx, int n, int k, int E,
                int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                int32_t *__restrict__ perm_tok, int32_t *__restrict__ inv,
                const float *__restrict__ topk_w, float *__restrict__ perm_w,
                uint32_t *__restrict__ status)
 {
-    __shared__ int32_t wcnt[kPermWarps][kMaxExperts];
+    pdl_enter();
+    __shared__ int32_t wcnt[kPermMaxWarps][kMaxExperts];
     __shared__ int32_t cnt_s[kMaxExperts];
     __shared__ int32_t off_s[kMaxExperts + 1];
 
+    if (upstream_failed(status)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;          // >= 8, so blockDim >= E
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int chunk = (n + kPermWarps - 1) / kPermWarps;
+    const int chunk = (n + nwarps - 1) / nwarps;
     const int begin = min(n, warp * chunk), end = min(n, begin + chunk);
 
-    for (int i = threadIdx.x; i < kPermWarps * kMaxExperts; i += kPermThreads)
+    for (int i = threadIdx.x; i < nwarps * kMaxExperts; i += blockDim.x)
         (&wcnt[0][0])[i] = 0;
     __syncthreads();
 
@@ -58,7 +60,7 @@ permute_kernel(const int32_t *__restrict__ topk_idx, int n, int k, int E,
     // scan: per-expert totals, exclusive offsets, per-warp bases
     if (threadIdx.x < E) {
         int e = threadIdx.x, s = 0;
-        for (int w = 0; w < kPermWarps; ++w) s += wcnt[w][e];
+        for (int w = 0; w < nwarps; ++w) s += wcnt[w][e];
         cnt_s[e] = s;
     }
     __syncthreads();
@@ -88,7 +90,7 @@ permute_kernel(const int32_t *__restrict__ topk_idx, int n, int k, int E,
         int e = threadIdx.x, run = off_s[e];
         counts[e] = cnt_s[e];
         offsets[e] = off_s[e];
-        for (int w = 0; w < kPermWarps; ++w) {
+        for (int w = 0; w < nwarps; ++w) {
             int c = wcnt[w][e];
             wcnt[w][e] = run;
             run += c;
@@ -123,7 +125,11 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
                            const float *topk_w, float *perm_w, uint32_t *status,
                            cudaStream_t stream)
 {
-    permute_kernel<<<1, kPermThreads, 0, stream>>>(topk_idx, T * k, k, E, counts, offsets,
+    // about 64 slots per warp, between 8 and 32 warps
+    const int n = T * k;
+    int warps = (n + 63) / 64;
+    warps = warps < 8 ? 8 : (warps > kPermMaxWarps ? kPermMaxWarps : warps);
+    launch_pdl(permute_kernel, dim3(1), dim3(warps * 32), 0, stream, topk_idx, T * k, k, E, counts, offsets,
                                                    perm_tok, inv, topk_w, perm_w, status);
     return cudaGetLastError();
 }
@@ -134,6 +140,7 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, int d,
                                    const int32_t *__restrict__ perm_tok, int rows,
                                    uint16_t *__restrict__ xp, int to_fp16)
 {
+    pdl_enter();
     const int vec_per_row = d / 8;
     const long long total = (long long)rows * vec_per_row;
     for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < total;
@@ -161,7 +168,7 @@ cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, in
     long long want = (total + 255) / 256, cap = (long long)num_sms * 8;
     int blocks = (int)(want < cap ? want : cap);
     if (blocks < 1) blocks = 1;
-    gather_rows_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(x), d, perm_tok,
+    launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const uint16_t *>(x), d, perm_tok,
                                                    rows, static_cast<uint16_t *>(xp), to_fp16);
     return cudaGetLastError();
 }

@@ -39,22 +39,52 @@ __device__ __forceinline__ void load_act8<__nv_bfloat16>(const __nv_bfloat16 *p,
     dst[4] = bf16lo(u.z); dst[5] = bf16hi(u.z); dst[6] = bf16lo(u.w); dst[7] = bf16hi(u.w);
 }
 
+// 8 consecutive activations as raw storage (bf16: one 16-byte load; fp32: two)
+template <typename AT> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 a;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { a = __ldg(reinterpret_cast<const uint4 *>(p)); }
+    __device__ __forceinline__ void cvt(float *f) const
+    {
+        f[0] = bf16lo(a.x); f[1] = bf16hi(a.x); f[2] = bf16lo(a.y); f[3] = bf16hi(a.y);
+        f[4] = bf16lo(a.z); f[5] = bf16hi(a.z); f[6] = bf16lo(a.w); f[7] = bf16hi(a.w);
+    }
+};
+template <> struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float *p)
+    {
+        a = __ldg(reinterpret_cast<const float4 *>(p));
+        b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    __device__ __forceinline__ void cvt(float *f) const
+    {
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+};
+
 template <typename AT, int TPB>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const AT *__restrict__ x, int T, int d, const AT *__restrict__ w_router,
              const float *__restrict__ bias, int E, int k, int32_t *__restrict__ topk_idx,
              float *__restrict__ topk_w, float *__restrict__ out_zero,
-             uint32_t *__restrict__ status)
+             uint32_t *__restrict__ zero_words, int n_zero, int32_t *__restrict__ rank,
+             int32_t *__restrict__ tile_cnt, uint32_t *__restrict__ status)
 {
+    pdl_enter();
     extern __shared__ float4 smem_f4[];
     float *xs = reinterpret_cast<float *>(smem_f4);            // [TPB][d]
     float *logit = xs + (size_t)TPB * d;                        // [TPB][E]
+    __shared__ int sel_s[TPB][kMaxTopK];                        // this CTA's selections
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TPB;
     const int ntok = min(TPB, T - t0);
 
     if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = kDevOk;
+    // scratch words later kernels count on being zero (split-K semaphores)
+    for (int i = blockIdx.x * kRouteThreads + threadIdx.x; i < n_zero; i += gridDim.x * kRouteThreads)
+        zero_words[i] = 0u;
 
     // stage the x rows, widened to fp32
     for (int c = threadIdx.x * 8; c < ntok * d; c += kRouteThreads * 8) {
@@ -69,32 +99,58 @@ route_kernel(const AT *__restrict__ x, int T, int d, const AT *__restrict__ w_ro
     }
     __syncthreads();
 
-    // router projection: warp w owns experts w, w+8, ...
-    for (int e = warp; e < E; e += kRouteWarps) {
-        float acc[TPB];
+    // router projection: warp w owns experts in groups of EG; each group's
+    // router chunks (CG per lane) are loaded together before any use, so a
+    // warp waits for one round trip per group rather than one per expert
+    constexpr int EG = 4;
+    constexpr int CG = sizeof(AT) == 4 ? 2 : 4;
+    for (int e0 = warp * EG; e0 < E; e0 += kRouteWarps * EG) {
+        float acc[EG][TPB];
 #pragma unroll
-        for (int t = 0; t < TPB; ++t) acc[t] = 0.f;
-        const AT *wr = w_router + (size_t)e * d;
-        for (int i = lane * 8; i < d; i += 32 * 8) {
-            float wv[8];
-            load_act8<AT>(wr + i, wv);
+        for (int g = 0; g < EG; ++g)
 #pragma unroll
-            for (int t = 0; t < TPB; ++t) {
-                if (t < ntok) {
-                    const float4 *xp = reinterpret_cast<const float4 *>(xs + (size_t)t * d + i);
-                    float4 a = xp[0], b = xp[1];
-                    acc[t] = fmaf(wv[0], a.x, acc[t]); acc[t] = fmaf(wv[1], a.y, acc[t]);
-                    acc[t] = fmaf(wv[2], a.z, acc[t]); acc[t] = fmaf(wv[3], a.w, acc[t]);
-                    acc[t] = fmaf(wv[4], b.x, acc[t]); acc[t] = fmaf(wv[5], b.y, acc[t]);
-                    acc[t] = fmaf(wv[6], b.z, acc[t]); acc[t] = fmaf(wv[7], b.w, acc[t]);
+            for (int t = 0; t < TPB; ++t) acc[g][t] = 0.f;
+        for (int c0 = lane * 8; c0 < d; c0 += 256 * CG) {
+            Raw8<AT> raw[EG][CG];
+#pragma unroll
+            for (int g = 0; g < EG; ++g)
+#pragma unroll
+                for (int q = 0; q < CG; ++q) {
+                    const int i = c0 + q * 256;
+                    if (e0 + g < E && i < d) raw[g][q].load(w_router + (size_t)(e0 + g) * d + i);
+                }
+#pragma unroll
+            for (int g = 0; g < EG; ++g) {
+#pragma unroll
+                for (int q = 0; q < CG; ++q) {
+                    const int i = c0 + q * 256;
+                    if (e0 + g < E && i < d) {
+                        float wv[8];
+                        raw[g][q].cvt(wv);
+#pragma unroll
+                        for (int t = 0; t < TPB; ++t) {
+                            if (t < ntok) {
+                                const float4 *xp = reinterpret_cast<const float4 *>(xs + (size_t)t * d + i);
+                                const float4 a = xp[0], b = xp[1];
+                                float s = acc[g][t];
+                                s = fmaf(wv[0], a.x, s); s = fmaf(wv[1], a.y, s);
+                                s = fmaf(wv[2], a.z, s); s = fmaf(wv[3], a.w, s);
+                                s = fmaf(wv[4], b.x, s); s = fmaf(wv[5], b.y, s);
+                                s = fmaf(wv[6], b.z, s); s = fmaf(wv[7], b.w, s);
+                                acc[g][t] = s;
+                            }
+                        }
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int t = 0; t < TPB; ++t) {
-            float s = warp_sum(acc[t]);
-            if (lane == 0 && t < ntok) logit[t * E + e] = s;
-        }
+        for (int g = 0; g < EG; ++g)
+#pragma unroll
+            for (int t = 0; t < TPB; ++t) {
+                const float s = warp_sum(acc[g][t]);
+                if (lane == 0 && t < ntok && e0 + g < E) logit[t * E + e0 + g] = s;
+            }
     }
     __syncthreads();
 
@@ -149,8 +205,26 @@ route_kernel(const AT *__restrict__ x, int T, int d, const AT *__restrict__ w_ro
             for (int j = 0; j < k; ++j) {
                 topk_idx[base + j] = sel_e[j];
                 topk_w[base + j] = p[j] / den;
+                sel_s[t][j] = sel_e[j];
             }
         }
+    }
+    if (!rank) return;
+    // grouping inputs: per-expert count of this CTA's tokens, and each slot's
+    // stable rank among them (tokens of a CTA are consecutive)
+    __syncthreads();
+    for (int i = threadIdx.x; i < ntok * k; i += kRouteThreads) {
+        const int t = i / k, e = sel_s[t][i - t * k];
+        int rk = 0;
+        for (int u = 0; u < t; ++u)
+            for (int j = 0; j < k; ++j) rk += sel_s[u][j] == e;
+        rank[(size_t)t0 * k + i] = rk;
+    }
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+        int cnt = 0;
+        for (int u = 0; u < ntok; ++u)
+            for (int j = 0; j < k; ++j) cnt += sel_s[u][j] == e;
+        tile_cnt[(size_t)blockIdx.x * E + e] = cnt;
     }
 }
 
@@ -171,7 +245,8 @@ int route_tokens_per_block(int T, int d, int E)
 template <typename AT, int TPB>
 static cudaError_t launch_route_t(const void *x, int T, int d, const void *w_router,
                                   const float *bias, int E, int k, int32_t *topk_idx,
-                                  float *topk_w, float *out_zero, uint32_t *status,
+                                  float *topk_w, float *out_zero, uint32_t *zero_words,
+                                  int n_zero, int32_t *rank, int32_t *tile_cnt, uint32_t *status,
                                   cudaStream_t stream)
 {
     size_t smem = route_smem_bytes(TPB, d, E);
@@ -182,30 +257,32 @@ static cudaError_t launch_route_t(const void *x, int T, int d, const void *w_rou
         if (e != cudaSuccess) return e;
     }
     dim3 grid((T + TPB - 1) / TPB);
-    kern<<<grid, kRouteThreads, smem, stream>>>(static_cast<const AT *>(x), T, d,
+    launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, stream, static_cast<const AT *>(x), T, d,
                                                  static_cast<const AT *>(w_router), bias, E, k,
-                                                 topk_idx, topk_w, out_zero, status);
+                                                 topk_idx, topk_w, out_zero, zero_words, n_zero,
+                                                 rank, tile_cnt, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                          const float *bias, int E, int k, int32_t *topk_idx, float *topk_w,
-                         float *out_zero, uint32_t *status, cudaStream_t stream)
+                         float *out_zero, uint32_t *zero_words, int n_zero, int32_t *rank,
+                         int32_t *tile_cnt, uint32_t *status, cudaStream_t stream)
 {
     int tpb = route_tokens_per_block(T, d, E);
     if (act_dt == MOE_F32) {
         switch (tpb) {
-        case 8: return launch_route_t<float, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
-        case 4: return launch_route_t<float, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
-        case 2: return launch_route_t<float, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
-        default: return launch_route_t<float, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
+        case 8: return launch_route_t<float, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+        case 4: return launch_route_t<float, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+        case 2: return launch_route_t<float, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+        default: return launch_route_t<float, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
         }
     }
     switch (tpb) {
-    case 8: return launch_route_t<__nv_bfloat16, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
-    case 4: return launch_route_t<__nv_bfloat16, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
-    case 2: return launch_route_t<__nv_bfloat16, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
-    default: return launch_route_t<__nv_bfloat16, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, status, stream);
+    case 8: return launch_route_t<__nv_bfloat16, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+    case 4: return launch_route_t<__nv_bfloat16, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+    case 2: return launch_route_t<__nv_bfloat16, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+    default: return launch_route_t<__nv_bfloat16, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
     }
 }
 

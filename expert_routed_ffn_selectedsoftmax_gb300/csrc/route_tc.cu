@@ -1,0 +1,438 @@
+// route_tc.cu -- router projection + SelectedSoftmax on tcgen05, and the
+// token-grouping scatter that follows it (bf16 activations).
+//
+// SelectedSoftmax ("New Community Model: ZONOS3-Mini (Zyphra) - #1271",
+// §Framework change): rank experts by router logit plus selection bias, keep
+// the top k, weight them by the softmax of their unbiased logits; ties in the
+// ranking score go to the lower expert index.
+//
+// route_tc_kernel: one CTA per tile of 128 tokens.  Warp 0 streams the x tile
+// [128 x 64] and the router tile [EP x 64] (E rows padded to a multiple of 16,
+// TMA zero-fills the padding) through a 4-stage ring; warp 1 issues
+// tcgen05.mma M=128, N=EP, accumulating the logits [128 tokens x EP] in TMEM
+// (fp32); warps 2-5 each own 32 tokens -- thread = token: it reads its logit
+// row from TMEM, keeps a sorted top-k in registers, and writes indices and
+// softmax weights.  The same threads record, per expert, a 128-bit mask of the
+// tile's tokens that chose it: the tile's per-expert counts are the mask
+// popcounts and a token's stable rank within the tile is the popcount of the
+// mask bits below it.
+//
+// scatter_kernel: one CTA per token tile.  Exclusive scan over (expert, tile)
+// of the tile counts gives every slot its grouped row
+//   row = offset[e] + sum_{tiles b' < b} count[b'][e] + rank,
+// i.e. a stable sort by expert with tokens ascending -- the same permutation
+// as the single-CTA grouping kernel.  It writes perm_tok, inv and the
+// per-row routing weight, and optionally copies x rows into grouped order for
+// the grouped GEMMs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tc_gemm.h"
+
+namespace moe {
+namespace rtc {
+
+using namespace sm100;
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB x tile
+constexpr int B_MAX_BYTES = 256 * BK * 2;       // 32 KB router tile (EP <= 256)
+constexpr int THREADS = 192;
+
+struct Params {
+    int T, d, E, EP, k;
+    const float *bias;
+    int32_t *topk_idx;
+    float *topk_w;
+    int32_t *rank;        // [T*k] stable rank of the slot within its token tile
+    int32_t *tile_cnt;    // [ntiles][E]
+    float *out_zero;      // optional [T, d] rows to zero
+    uint32_t *zero_words;
+    int n_zero;
+    uint32_t *status;
+};
+
+struct Ctl {
+    uint64_t full[STAGES], empty[STAGES], tfull, epi;
+    uint32_t tmem_base;
+    int abort_flag;
+    float bias[kMaxExperts];
+    uint32_t mask[kMaxExperts][4];   // tokens of this tile that chose expert e
+};
+
+// KMAX: compile-time bound on k (1, 2, 4 or 8) so the top-k insertion is as
+// short as the k it serves.
+template <int KMAX>
+__global__ void __launch_bounds__(THREADS, 1)
+route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                const Params p)
+{
+    pdl_enter();
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    const int b_bytes = p.EP * BK * 2;
+    Ctl &c = *reinterpret_cast<Ctl *>(sB + STAGES * B_MAX_BYTES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E, EP = p.EP;
+    const int t0 = blockIdx.x * BM;
+    const int kblocks = p.d / BK;
+    const uint32_t ncols = EP <= 32 ? 32 : EP <= 64 ? 64 : EP <= 128 ? 128 : 256;
+
+    if (p.status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;
+    for (int i = blockIdx.x * THREADS + threadIdx.x; i < p.n_zero; i += gridDim.x * THREADS)
+        p.zero_words[i] = 0u;
+    if (p.out_zero) {
+        const int ntok = min(BM, p.T - t0);
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = threadIdx.x * 4; i < ntok * p.d; i += THREADS * 4)
+            *reinterpret_cast<float4 *>(p.out_zero + (size_t)t0 * p.d + i) = z;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
+        mbar_init(&c.tfull, 1);
+        mbar_init(&c.epi, 128);
+        c.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int e = threadIdx.x; e < kMaxExperts; e += THREADS) {
+        c.bias[e] = (e < E && p.bias) ? p.bias[e] : 0.f;
+        c.mask[e][0] = c.mask[e][1] = c.mask[e][2] = c.mask[e][3] = 0u;
+    }
+    if (warp == 1) tmem_alloc(&c.tmem_base, ncols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        bool ok = true;
+        int kb = 0;
+        for (; kb < kblocks; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1u;
+            if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+            mbar_expect_tx(&c.full[s], A_BYTES + b_bytes);
+            tma_load_2d(sA + s * A_BYTES, &tm_x, &c.full[s], kb * BK, t0);
+            tma_load_2d(sB + s * B_MAX_BYTES, &tm_w, &c.full[s], kb * BK, 0);
+        }
+        if (!ok) {
+            atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+            for (int j = (kb >= STAGES ? kb - STAGES : 0); j < kb; ++j) {
+                volatile int no_abort = 0;
+                mbar_wait(&c.full[j % STAGES], (j / STAGES) & 1u, &no_abort);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        const uint32_t idesc = idesc_f16_mn(0, BM, EP);
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1u;
+            if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * A_BYTES);
+            const uint32_t b0 = smem_u32(sB + s * B_MAX_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+                umma_f16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                         (kb | kk) != 0);
+            umma_commit(&c.empty[s]);
+        }
+        if (ok) {
+            umma_commit(&c.tfull);
+        } else {
+            atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+            umma_commit(&c.tfull);   // drains the MMAs in flight; the epilogue sees the abort
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ thread = token epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;        // token row within the tile (TMEM lane)
+        const int t = t0 + r;
+        const bool valid = t < p.T;
+        bool ok = mbar_wait(&c.tfull, 0, abort_flag);
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+        }
+        ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld below is warp-collective
+        uint32_t epi_phase = 0;
+        {
+            if (ok) tc_fence_after();
+            float bs[KMAX], bl[KMAX];
+            int be[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) { bs[j] = -INFINITY; bl[j] = 0.f; be[j] = 0x7fffffff; }
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = 0; ok && c0 < EP; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int e = c0 + q;
+                    if (e < E) {
+                        float cl = __uint_as_float(v[q]);
+                        float cs = cl + c.bias[e];
+                        if (isnan(cs)) cs = -INFINITY;   // keep the ranking a total order
+                        int ce = e;
+                        // insertion into the sorted top-k (score desc, index asc)
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) {
+                            if (j < p.k && (cs > bs[j] || (cs == bs[j] && ce < be[j]))) {
+                                const float ts = bs[j], tl = bl[j];
+                                const int te = be[j];
+                                bs[j] = cs; bl[j] = cl; be[j] = ce;
+                                cs = ts; cl = tl; ce = te;
+                            }
+                        }
+                    }
+                }
+            }
+            if (ok && valid) {
+                float m = bl[0];
+#pragma unroll
+                for (int j = 1; j < KMAX; ++j) if (j < p.k) m = fmaxf(m, bl[j]);
+                float pr[KMAX], den = 0.f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    pr[j] = j < p.k ? expf(bl[j] - m) : 0.f;
+                    den += pr[j];
+                }
+                const size_t base = (size_t)t * p.k;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < p.k) {
+                        p.topk_idx[base + j] = be[j];
+                        p.topk_w[base + j] = pr[j] / den;
+                        if (p.rank) atomicOr(&c.mask[be[j]][r >> 5], 1u << (r & 31));
+                    }
+                }
+            }
+            // wait for every token's mask bits, then ranks and tile counts
+            // (a bounded barrier: a thread that gave up above still arrives)
+            if (!bounded_bar(&c.epi, epi_phase, abort_flag)) ok = false;
+            if (ok && valid && p.rank) {
+                const size_t base = (size_t)t * p.k;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < p.k) {
+                        const uint32_t *mk = c.mask[be[j]];
+                        int rk = 0;
+                        for (int w = 0; w < (r >> 5); ++w) rk += __popc(mk[w]);
+                        rk += __popc(mk[r >> 5] & ((1u << (r & 31)) - 1u));
+                        p.rank[base + j] = rk;
+                    }
+                }
+            }
+            for (int e = threadIdx.x - 64; ok && p.tile_cnt && e < E; e += 128)
+                p.tile_cnt[(size_t)blockIdx.x * E + e] =
+                    __popc(c.mask[e][0]) + __popc(c.mask[e][1]) + __popc(c.mask[e][2]) + __popc(c.mask[e][3]);
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, ncols);
+    }
+}
+
+}  // namespace rtc
+
+// Grouped rows of the slots of token tile `blockIdx.x` (tiles of `tile_tokens`
+// tokens, as produced by either router): part blockIdx.y of gridDim.y handles
+// every gridDim.y-th slot of the tile.  See the file header.
+__global__ void __launch_bounds__(256)
+scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w,
+               const int32_t *__restrict__ rank, const int32_t *__restrict__ tile_cnt, int ntiles,
+               int tile_tokens, int T, int k, int E, int32_t *__restrict__ counts,
+               int32_t *__restrict__ offsets, int32_t *__restrict__ perm_tok,
+               int32_t *__restrict__ inv, float *__restrict__ perm_w,
+               const uint16_t *__restrict__ x, int d, uint16_t *__restrict__ xp,
+               uint32_t *__restrict__ status)
+{
+    pdl_enter();
+    __shared__ int tot[kMaxExperts], pre[kMaxExperts], off[kMaxExperts + 1];
+    __shared__ int part_tot[8][kMaxExperts], part_pre[8][kMaxExperts];
+    if (upstream_failed(status)) return;
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nslots_all = T * k;
+    // per-expert totals over all tiles and over the tiles before this one:
+    // warp w sums tiles w, w+8, ...; lane owns experts lane, lane+32, ...
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        int s_tot = 0, s_pre = 0;
+        if (e < E) {
+            int bb = warp;
+            for (; bb + 24 < ntiles; bb += 32) {   // four independent loads in flight
+                const int c0 = __ldcg(tile_cnt + (size_t)bb * E + e);
+                const int c1 = __ldcg(tile_cnt + (size_t)(bb + 8) * E + e);
+                const int c2 = __ldcg(tile_cnt + (size_t)(bb + 16) * E + e);
+                const int c3 = __ldcg(tile_cnt + (size_t)(bb + 24) * E + e);
+                s_tot += c0 + c1 + c2 + c3;
+                s_pre += (bb < b ? c0 : 0) + (bb + 8 < b ? c1 : 0) + (bb + 16 < b ? c2 : 0) +
+                         (bb + 24 < b ? c3 : 0);
+            }
+            for (; bb < ntiles; bb += 8) {
+                const int c0 = __ldcg(tile_cnt + (size_t)bb * E + e);
+                s_tot += c0;
+                s_pre += bb < b ? c0 : 0;
+            }
+        }
+        if (e < E) { part_tot[warp][e] = s_tot; part_pre[warp][e] = s_pre; }
+    }
+    __syncthreads();
+    if (threadIdx.x < E) {
+        int s_tot = 0, s_pre = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) { s_tot += part_tot[w][threadIdx.x]; s_pre += part_pre[w][threadIdx.x]; }
+        tot[threadIdx.x] = s_tot;
+        pre[threadIdx.x] = s_pre;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        int local = 0;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) local += tot[e];
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) { off[e] = run; run += tot[e]; }
+        }
+        if (lane == 31) off[E] = incl;
+    }
+    __syncthreads();
+    if (b == 0 && blockIdx.y == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) { counts[e] = tot[e]; offsets[e] = off[e]; }
+        if (threadIdx.x == 0) offsets[E] = off[E];
+    }
+    const int t0 = b * tile_tokens;
+    const int nslots = min(tile_tokens, T - t0) * k;
+    const int part = blockIdx.y, nparts = gridDim.y;
+    // one warp per slot: lane 0 resolves the row, the warp copies x[t] to xp[row]
+    for (int i = part + nparts * warp; i < nslots; i += nparts * (blockDim.x / 32)) {
+        const size_t slot = (size_t)t0 * k + i;
+        int pos = -1;
+        if (lane == 0) {
+            const int e = __ldcg(topk_idx + slot);
+            pos = (e >= 0 && e < E) ? off[e] + pre[e] + __ldcg(rank + slot) : -1;
+            if (pos < 0 || pos >= nslots_all) {   // cannot happen with consistent routing
+                if (status) atomicOr(status, kDevCheckFailed);
+                pos = -1;
+            } else {
+                perm_tok[pos] = (int)(slot / k);
+                inv[slot] = pos;
+                perm_w[pos] = __ldcg(topk_w + slot);
+            }
+        }
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        if (pos < 0 || !xp) continue;
+        const int t = (int)(slot / k);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pos * d);
+        const int vec = d / 8;
+        constexpr int U = 4;   // 4 x 16 bytes per lane in flight
+        for (int c0 = lane; c0 < vec; c0 += 32 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < vec) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < vec) dst[c0 + 32 * u] = v[u];
+        }
+    }
+}
+
+namespace rtc {
+
+constexpr size_t smem_bytes()
+{
+    return 1024 + (size_t)STAGES * (A_BYTES + B_MAX_BYTES) + sizeof(Ctl);
+}
+
+}  // namespace rtc
+
+cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cudaStream_t stream)
+{
+    // enough CTAs that every SM gets a few warps of slots
+    const int slots_per_tile = tile_tokens * a.k;
+    int parts = (2 * 152 + ntiles - 1) / ntiles;
+    const int max_parts = (slots_per_tile + 7) / 8;   // >= 1 slot per warp
+    if (parts > max_parts) parts = max_parts;
+    if (parts < 1) parts = 1;
+    launch_pdl(scatter_kernel, dim3(ntiles, parts), dim3(256), 0, stream,
+        a.topk_idx, a.topk_w, a.rank, a.tile_cnt, ntiles, tile_tokens, a.T, a.k, a.E, a.counts,
+        a.offsets, a.perm_tok, a.inv, a.perm_w, static_cast<const uint16_t *>(a.x), a.d,
+        static_cast<uint16_t *>(a.xp), a.status);
+    return cudaGetLastError();
+}
+
+bool route_tc_capable(int act_dt, int d, int E)
+{
+    return act_dt == MOE_BF16 && d % 64 == 0 && E <= kMaxExperts && tc_gemm_available();
+}
+
+int route_tc_tiles(int T) { return (T + 127) / 128; }
+
+cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream)
+{
+    using namespace rtc;
+    const int EP = (a.E + 15) / 16 * 16;
+    CUtensorMap m_x, m_w;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!tc::make_map(&m_x, a.x, (uint64_t)a.T, a.d, BM, bf) ||
+        !tc::make_map(&m_w, a.w_router, (uint64_t)a.E, a.d, EP, bf))
+        return cudaErrorInvalidValue;
+    cudaError_t err;
+    const size_t smem = smem_bytes();
+    static std::atomic<int> attr_done{0};
+    if (!attr_done.load()) {
+        if ((err = cudaFuncSetAttribute(route_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return err;
+        attr_done.store(1);
+    }
+    Params p{};
+    p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.bias = a.bias;
+    p.topk_idx = a.topk_idx; p.topk_w = a.topk_w; p.rank = a.rank; p.tile_cnt = a.tile_cnt;
+    p.out_zero = a.out_zero; p.zero_words = a.zero_words; p.n_zero = a.n_zero; p.status = a.status;
+    const int ntiles = route_tc_tiles(a.T);
+    auto kern = a.k == 1 ? route_tc_kernel<1> : a.k == 2 ? route_tc_kernel<2>
+              : a.k <= 4 ? route_tc_kernel<4> : route_tc_kernel<8>;
+    launch_pdl(kern, dim3(ntiles), dim3(THREADS), smem, stream, m_x, m_w, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (a.ev_routed && (err = cudaEventRecord(a.ev_routed, stream)) != cudaSuccess) return err;
+    if (!a.counts) return cudaSuccess;   // routing only (moe_route)
+    return launch_scatter(a, ntiles, BM, stream);
+}
+
+}  // namespace moe

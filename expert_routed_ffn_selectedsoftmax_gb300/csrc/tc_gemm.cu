@@ -33,10 +33,13 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 #include "tc_gemm.h"
 
 namespace moe {
 namespace tc {
+
+using namespace sm100;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
@@ -44,7 +47,6 @@ constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
@@ -72,129 +74,8 @@ struct SmemCtl {
     int off[kMaxExperts + 1];
 };
 
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase of parity `parity` to complete.  Returns false
-// on timeout or when another role has raised the abort flag.
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) return false;
-        }
-    }
-}
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row groups 1024 bytes apart (tcgen05 descriptor format:
-// start>>4 in bits 0-13, leading offset>>4 in 16-29, stride offset>>4 in
-// 32-45, version 1 in bits 46-47, swizzle mode in 61-63 with 2 = 128B).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;             // leading byte offset (unused with swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
-    d |= (uint64_t)1 << 46;             // descriptor version
-    d |= (uint64_t)2 << 61;             // SWIZZLE_128B
-    return d;
-}
-
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
-// both bf16 (ab_fp16 = 0) or both fp16, both K-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t idesc_f16(int ab_fp16)
-{
-    return (1u << 4)                                   // D format: f32
-           | ((ab_fp16 ? 0u : 1u) << 7)                // A format: f16 0 / bf16 1
-           | ((ab_fp16 ? 0u : 1u) << 10)               // B format
-           | ((uint32_t)(BN >> 3) << 17)               // N >> 3
-           | ((uint32_t)(BM >> 4) << 24);              // M >> 4
-}
-
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t *bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
-{
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
+// Instruction descriptor for the M = 128, N = 256 tiles of this file.
+__host__ __device__ constexpr uint32_t idesc_f16(int ab_fp16) { return idesc_f16_mn(ab_fp16, BM, BN); }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
@@ -222,6 +103,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b0,
                     const __grid_constant__ CUtensorMap tm_b1, const Params p)
 {
+    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -229,6 +111,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     uint8_t *sB = smem + STAGES * A_BYTES;
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(smem + STAGES * STAGE_BYTES);
 
+    if (upstream_failed(p.status)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
 
@@ -371,7 +254,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local_tile) {
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_ph = (local_tile >> 1) & 1u;
-            if (!mbar_wait(&c.tfull[acc], acc_ph, abort_flag)) {
+            // warp-uniform outcome: tcgen05.ld below is warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(&c.tfull[acc], acc_ph, abort_flag))) {
                 if (lane == 0) atomicOr(p.status, kDevTimeout);
                 c.abort_flag = 1;
                 break;
@@ -504,8 +388,10 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     using namespace tc;
     if (a.w_dt != MOE_BF16) return cudaErrorNotSupported;   // Q8_0 mainloop: separate kernel
     const int rows = a.T * a.k;
-    cudaError_t err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, 0, a.num_sms, stream);
-    if (err != cudaSuccess) return err;
+    cudaError_t err = cudaSuccess;
+    if (!a.xp_ready &&
+        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, 0, a.num_sms, stream)) != cudaSuccess)
+        return err;
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
 
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -539,14 +425,14 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     p.K = a.d; p.n_tiles = a.F / (BN / 2);
     int grid = (int)(max_mtiles * p.n_tiles < a.num_sms ? max_mtiles * p.n_tiles : a.num_sms);
     if (grid < 1) grid = 1;
-    grouped_gemm_kernel<GATEUP><<<grid, THREADS, smem, stream>>>(m_xp, m_wg, m_wu, p);
+    launch_pdl(grouped_gemm_kernel<GATEUP>, dim3(grid), dim3(THREADS), smem, stream, m_xp, m_wg, m_wu, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     p.K = a.F; p.n_tiles = a.d / BN;
     grid = (int)(max_mtiles * p.n_tiles < a.num_sms ? max_mtiles * p.n_tiles : a.num_sms);
     if (grid < 1) grid = 1;
-    grouped_gemm_kernel<DOWN><<<grid, THREADS, smem, stream>>>(m_h, m_wd, m_wd, p);
+    launch_pdl(grouped_gemm_kernel<DOWN>, dim3(grid), dim3(THREADS), smem, stream, m_h, m_wd, m_wd, p);
     return cudaGetLastError();
 }
 

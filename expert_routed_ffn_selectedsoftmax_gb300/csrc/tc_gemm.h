@@ -1,6 +1,7 @@
 // tc_gemm.h -- internal interface of the tcgen05 grouped-GEMM expert path.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +18,7 @@ struct TcArgs {
     const int32_t *perm_tok;    // [T*k]
     const float *perm_w;        // [T*k]
     void *xp;                   // [T*k, d] 16-bit scratch (grouped rows)
+    int xp_ready;               // xp already holds the grouped rows
     void *h;                    // [T*k, F] 16-bit scratch
     float *out;                 // [T, d] fp32 (zeroed beforehand when k > 1)
     uint32_t *status;           // device status word
@@ -24,6 +26,13 @@ struct TcArgs {
     cudaEvent_t ev_gathered;    // optional: recorded after the row gather
     cudaEvent_t ev_gateup;      // optional: recorded after the gate/up GEMM
 };
+
+namespace tc {
+// 2-D row-major [rows, cols] 16-bit tensor map, box {64 cols, box_rows},
+// 128-byte swizzle (the K-major operand tiles of the tcgen05 kernels).
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              CUtensorMapDataType dt);
+}  // namespace tc
 
 // True when the tensor-core expert kernels are compiled into this library.
 bool tc_gemm_available();

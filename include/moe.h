@@ -63,8 +63,17 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2 } moe_dtype;
 
-/* Which expert-compute kernels moe_forward uses.  AUTO picks by shape. */
-typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_PREFILL = 2 } moe_path;
+/* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
+ * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16
+ *   weights with d % 128 == 0, F % 128 == 0 and T*k <= 8192, otherwise the
+ *   CUDA-core kernels.  PREFILL: tcgen05 grouped GEMMs.  DECODE_SIMT: always
+ *   the CUDA-core decode kernels (the decode path for fp32 and Q8_0). */
+typedef enum {
+    MOE_PATH_AUTO = 0,
+    MOE_PATH_DECODE = 1,
+    MOE_PATH_PREFILL = 2,
+    MOE_PATH_DECODE_SIMT = 3
+} moe_path;
 
 /* Static description of a status code (never NULL). */
 MOE_API const char *moe_status_str(int status);
@@ -135,7 +144,8 @@ MOE_API size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype a
  *   path: a moe_path value.  MOE_PATH_PREFILL needs bf16 activations,
  *   bf16 or Q8_0 weights, d % 256 == 0 and F % 128 == 0, and returns
  *   MOE_ERR_UNSUPPORTED otherwise.
- *   Summation order: with k <= 2 the result is bitwise deterministic.
+ *   Summation order is fixed on every path except the CUDA-core decode
+ *   kernels with k > 2 (fp32 atomics): results are bitwise reproducible.
  */
 MOE_API moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                        const float *sel_bias, int E, int k, const void *w_gate,
@@ -150,7 +160,7 @@ MOE_API moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, co
  *   events[0] before routing          events[3] after the row gather
  *   events[1] after routing           events[4] after gate/up + SwiGLU
  *   events[2] after token grouping    events[5] after down + combine
- * (on the decode path there is no gather: events[3] follows events[2]
+ * (where no separate gather kernel runs, events[3] follows events[2]
  * immediately).  events may be NULL, which makes this moe_forward.
  */
 MOE_API moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,

@@ -17,7 +17,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-DECODE, PREFILL = 1, 2
+DECODE, PREFILL, SIMT = 1, 2, 3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -84,6 +84,23 @@ def test_route_ties_go_to_lower_index():
     assert np.all(wts == 0.5)
 
 
+@pytest.mark.parametrize("T", [16, 200, 600])
+def test_route_ties_go_to_lower_index_bf16(T):
+    """Same on the bf16 (tensor-core) router: identical router rows give
+    bitwise-equal logits, and the lower expert index wins."""
+    layer = wl.make_custom_layer(4, T=T, d=128, E=6, k=2, F=32, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16, bias_sd=0.0)
+    v = layer.w_router[0].copy()
+    neg = wl.f32_to_bf16_bits(-wl.bf16_bits_to_f32(v))
+    layer.w_router[[1, 2, 3]] = v
+    layer.w_router[[0, 4, 5]] = neg
+    xv = wl.bf16_bits_to_f32(v)
+    layer.x = wl.f32_to_bf16_bits(np.outer(np.linspace(1, 2, T), xv) * 4)
+    idx, wts = _route(layer)
+    assert np.all(idx == [1, 2])
+    assert np.all(wts == 0.5)
+
+
 # ------------------------------------------------------------------ permute
 @pytest.mark.parametrize("T,k,E", [(0, 2, 4), (1, 1, 1), (128, 2, 64), (8192, 2, 64),
                                    (4096, 1, 16), (777, 3, 250), (40000, 8, 256)])
@@ -120,25 +137,27 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("path", [DECODE, SIMT])
 @pytest.mark.parametrize("act,wdt,T,d,E,k,F", SMALL)
-def test_forward_small_matches_oracle(act, wdt, T, d, E, k, F):
+def test_forward_small_matches_oracle(act, wdt, T, d, E, k, F, path):
     layer = wl.make_custom_layer(11, T=T, d=d, E=E, k=k, F=F, act_dtype=act, w_dtype=wdt,
                                  bias_sd=0.3)
-    out = gpu_forward(layer, DEV, path=DECODE)
+    out = gpu_forward(layer, DEV, path=path)
     idx_g, _ = _route(layer)
     torch.cuda.synchronize()
     ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
     check_output(out.cpu().numpy(), layer, ref, idx_ref, margin, idx_gpu=idx_g)
 
 
-def test_forward_all_tokens_one_expert():
+@pytest.mark.parametrize("path", [DECODE, SIMT])
+def test_forward_all_tokens_one_expert(path):
     """A bias that sends every token to expert 3 (and 5): many row blocks in one expert."""
     layer = wl.make_custom_layer(12, T=150, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
                                  w_dtype=wl.BF16)
     layer.bias[:] = 0
     layer.bias[3] = 100.0
     layer.bias[5] = 50.0
-    out = gpu_forward(layer, DEV, path=DECODE)
+    out = gpu_forward(layer, DEV, path=path)
     ref, idx_ref, _, margin = oracle.moe_forward(layer)
     assert np.all(idx_ref == [3, 5])
     check_output(out.cpu().numpy(), layer, ref, idx_ref, margin)
@@ -294,10 +313,28 @@ def test_prefill_and_decode_paths_agree():
     layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
                                  w_dtype=wl.BF16)
     t = upload_layer(layer, DEV)
-    a = gpu_forward(layer, DEV, path=DECODE, t=t).cpu().numpy().astype(np.float64)
-    b = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy().astype(np.float64)
+    a = gpu_forward(layer, DEV, path=SIMT, t=t).cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(a ** 2))
-    assert np.abs(a - b).max() <= 2e-2 * rms
+    for path in (DECODE, PREFILL):
+        b = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy().astype(np.float64)
+        assert np.abs(a - b).max() <= 2e-2 * rms
+
+
+@pytest.mark.parametrize("T,k", [(1, 1), (8, 1), (64, 1), (33, 2), (128, 2), (300, 4)])
+def test_decode_tc_deterministic_and_equivariant(T, k):
+    layer = wl.make_custom_layer(25, T=T, d=512, E=16, k=k, F=384, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16, bias_sd=0.5)
+    t = upload_layer(layer, DEV)
+    a = gpu_forward(layer, DEV, path=DECODE, t=t).cpu().numpy()
+    b = gpu_forward(layer, DEV, path=DECODE, t=t).cpu().numpy()
+    assert np.array_equal(a, b)
+    perm = np.random.default_rng(2).permutation(layer.T)
+    t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
+    c = gpu_forward(layer, DEV, path=DECODE, t=t2).cpu().numpy()
+    assert np.array_equal(c, a[perm])
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    idx_g, _ = _route(layer)
+    check_output(a, layer, ref, idx_ref, margin, idx_gpu=idx_g)
 
 
 def test_prefill_deterministic_and_equivariant():
