@@ -255,6 +255,7 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     ra.counts = counts; ra.offsets = offsets; ra.perm_tok = perm_tok; ra.inv = inv; ra.perm_w = perm_w;
     const bool act16 = act_dt == MOE_BF16;
     ra.xp = ((use_prefill || use_dtc) && act16) ? ws + L.xp : nullptr;
+    ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows
     ra.out_zero = zero_out ? out : nullptr;
     ra.zero_words = nullptr;
     ra.n_zero = 0;

@@ -105,16 +105,17 @@ template <> __device__ __forceinline__ void WView<__nv_bfloat16>::cvt(const RawW
     c.v[6] = bf16lo(r.a.w); c.v[7] = bf16hi(r.a.w);
 }
 
-// Q8_0 view: p points at the q plane; the fp16 scale plane follows at
-// align256(rows*cols) bytes.  `scales` is precomputed by the host.
+// Q8_0 view: p points at the q plane; the fp16 scale plane [cols/32, rows]
+// follows at align256(rows*cols) bytes.  `scales` and `rows` are set by the host.
 template <> struct WView<Q8Tag> {
     const int8_t *q;
     const __half *scales;
     size_t cols;
+    size_t rows;
     __device__ __forceinline__ void load(size_t row, int col, RawW<Q8Tag> &r) const
     {
         r.q = ld_stream_u2(q + row * cols + col);
-        r.s = __half2float(scales[row * (cols / 32) + col / 32]);
+        r.s = __half2float(scales[(size_t)(col / 32) * rows + row]);
     }
     __device__ __forceinline__ static void cvt(const RawW<Q8Tag> &r, Chunk8 &c)
     {

@@ -247,6 +247,7 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
         v.scales = reinterpret_cast<const __half *>(static_cast<const char *>(p) +
                                                     align_up((size_t)rows * cols, 256));
         v.cols = (size_t)cols;
+        v.rows = (size_t)rows;
         return v;
     };
     return launch_t<__nv_bfloat16, Q8Tag>(a, view(a.w_gate, (long long)a.E * a.F, a.d),

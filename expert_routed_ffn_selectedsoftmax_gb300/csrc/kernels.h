@@ -35,7 +35,8 @@ struct RouteTcArgs {
     // grouping outputs (counts == NULL: routing only, no scatter launch)
     int32_t *counts, *offsets, *perm_tok, *inv;
     float *perm_w;
-    void *xp;                   // optional [T*k, d] bf16 grouped copy of x
+    void *xp;                   // optional [T*k, d] grouped copy of x
+    int xp_fp16;                // write xp as fp16 (else bf16)
     float *out_zero;            // optional rows to zero
     uint32_t *zero_words;       // optional scratch words to zero
     int n_zero;

@@ -5,20 +5,24 @@
 // along the contiguous axis is 34 bytes, an fp16 scale then 32 int8 values;
 // value = scale * q.  34-byte blocks are not 16-byte aligned, so the library
 // repacks once, at load time, into an int8 plane [rows, cols] and an fp16 scale
-// plane [rows, cols/32] (same bytes, aligned for 128-bit and TMA loads).
+// plane [cols/32, rows] (same bytes, aligned for 128-bit and TMA loads; the
+// scales of one 32-column block are contiguous over rows, so a weight tile's
+// scales are one TMA box).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
 __global__ void pack_q8_0_kernel(const uint8_t *__restrict__ blocks, long long nblocks,
-                                 int8_t *__restrict__ q, __half *__restrict__ scales)
+                                 long long rows, int bpr, int8_t *__restrict__ q,
+                                 __half *__restrict__ scales)
 {
     for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
          b += (long long)gridDim.x * blockDim.x) {
         const uint8_t *src = blocks + b * 34;
         uint16_t s = (uint16_t)src[0] | ((uint16_t)src[1] << 8);
-        scales[b] = __ushort_as_half(s);
+        const long long row = b / bpr, blk = b - row * bpr;   // block blk of row `row`
+        scales[blk * rows + row] = __ushort_as_half(s);
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -41,7 +45,7 @@ cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void 
     long long grid = (nblocks + 255) / 256;
     if (grid > 65535LL * 16) grid = 65535LL * 16;
     pack_q8_0_kernel<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks),
-                                                          nblocks, q, s);
+                                                          nblocks, rows, cols / 32, q, s);
     return cudaGetLastError();
 }
 

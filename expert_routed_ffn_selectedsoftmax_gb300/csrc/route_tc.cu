@@ -265,7 +265,7 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
                int tile_tokens, int T, int k, int E, int32_t *__restrict__ counts,
                int32_t *__restrict__ offsets, int32_t *__restrict__ perm_tok,
                int32_t *__restrict__ inv, float *__restrict__ perm_w,
-               const uint16_t *__restrict__ x, int d, uint16_t *__restrict__ xp,
+               const uint16_t *__restrict__ x, int d, uint16_t *__restrict__ xp, int xp_fp16,
                uint32_t *__restrict__ status)
 {
     pdl_enter();
@@ -363,6 +363,18 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (c0 + 32 * u < vec) v[u] = __ldg(src + c0 + 32 * u);
+            if (xp_fp16) {   // bf16 -> fp16 rows for the fp16 (Q8_0) tensor-core path
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __half2 hh = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
+                        w[i] = *reinterpret_cast<uint32_t *>(&hh);
+                    }
+                    v[u] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (c0 + 32 * u < vec) dst[c0 + 32 * u] = v[u];
@@ -390,7 +402,7 @@ cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cu
     launch_pdl(scatter_kernel, dim3(ntiles, parts), dim3(256), 0, stream,
         a.topk_idx, a.topk_w, a.rank, a.tile_cnt, ntiles, tile_tokens, a.T, a.k, a.E, a.counts,
         a.offsets, a.perm_tok, a.inv, a.perm_w, static_cast<const uint16_t *>(a.x), a.d,
-        static_cast<uint16_t *>(a.xp), a.status);
+        static_cast<uint16_t *>(a.xp), a.xp_fp16, a.status);
     return cudaGetLastError();
 }
 

@@ -22,6 +22,13 @@
 // expert's group are computed on neighbouring rows (or TMA zero fill) and
 // dropped in the epilogue.
 //
+// Q8_0 weights ("zonos2.cpp internals", §Quantization: 8-bit blocks of 32
+// values with one fp16 scale): the B stage holds the int8 tile as loaded by
+// TMA; four converter warps (6-9) turn it into fp16 in the 128-byte-swizzled
+// layout -- int8 -> fp16 exactly via the 1024+q bit trick, times the block's
+// fp16 scale -- in one of two converted-B buffers, and the MMA runs kind::f16
+// with fp16 operands (the grouped rows and h are fp16 on this path).
+//
 // Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
 // waiting role sets the status word, raises a CTA-wide abort flag that the
 // other roles poll, waits (bounded) for its own copies or MMAs in flight, and
@@ -43,10 +50,20 @@ using namespace sm100;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int B_BYTES = BN * BK * 2;          // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB (16-bit B tile)
+constexpr int BQ_BYTES = BN * BK;             // 16 KB (int8 B tile)
+constexpr int SC_BYTES = BN * (BK / 32) * 2;  // 1 KB (fp16 scales of the int8 tile)
 constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
+
+// Per-variant shared-memory layout: a ring of STAGES stages {A, B or Bq},
+// then (Q8 only) two converted fp16 B buffers, then the control block.
+template <bool Q8> struct Cfg {
+    static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SC_BYTES + 1023) / 1024 * 1024
+                                    : A_BYTES + B_BYTES;
+    static constexpr int CVT = Q8 ? 2 : 0;
+    static constexpr int THREADS = Q8 ? 320 : 192;
+    static constexpr size_t CTL = (size_t)STAGES * STAGE + (size_t)CVT * B_BYTES;
+};
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
@@ -65,7 +82,7 @@ struct Params {
 };
 
 struct SmemCtl {
-    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, cfull[2], cempty[2];
     uint32_t tmem_base;
     int abort_flag;
     int n_tiles_total;
@@ -97,19 +114,45 @@ __device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int n_tiles
     (void)n_tiles;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+// int8 x 16 (one uint4) -> fp16 x 16 scaled by s: (q ^ 0x80) placed in the
+// mantissa of 1024.0 gives 1024 + 128 + q exactly; subtracting 1152 leaves q.
+__device__ __forceinline__ void dequant16(const uint4 q, const __half2 s, uint4 &lo, uint4 &hi)
+{
+    const uint32_t w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u,
+                           q.w ^ 0x80808080u};
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t a = __byte_perm(w[i], 0x64646464u, 0x4140);
+        uint32_t b = __byte_perm(w[i], 0x64646464u, 0x4342);
+        __half2 ha = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&a), bias), s);
+        __half2 hb = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&b), bias), s);
+        o[2 * i] = *reinterpret_cast<uint32_t *>(&ha);
+        o[2 * i + 1] = *reinterpret_cast<uint32_t *>(&hb);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// tm_s0/tm_s1 (Q8 only): the B matrices' fp16 scale planes [cols/32, rows],
+// box {rows of the tile, 2 blocks}.
+template <int MODE, bool Q8>
+__global__ void __launch_bounds__(Cfg<Q8>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b0,
-                    const __grid_constant__ CUtensorMap tm_b1, const Params p)
+                    const __grid_constant__ CUtensorMap tm_b1,
+                    const __grid_constant__ CUtensorMap tm_s0,
+                    const __grid_constant__ CUtensorMap tm_s1, const Params p)
 {
     pdl_enter();
+    using C = Cfg<Q8>;
+    constexpr int THREADS = C::THREADS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_BYTES;
-    SmemCtl &c = *reinterpret_cast<SmemCtl *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *sCvt = smem + STAGES * C::STAGE;   // Q8: converted fp16 B buffers
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(smem + C::CTL);
 
     if (upstream_failed(p.status)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,7 +161,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     // ---- set-up: barriers, tile table, TMEM
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128);
+            mbar_init(&c.cfull[b], 128); mbar_init(&c.cempty[b], 1);
+        }
         mbar_init(&c.drain, 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -189,15 +235,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                mbar_expect_tx(&c.full[s], STAGE_BYTES);
-                tma_load_2d(sA + s * A_BYTES, &tm_a, &c.full[s], kb * BK, arow);
+                mbar_expect_tx(&c.full[s], A_BYTES + (Q8 ? BQ_BYTES + SC_BYTES : B_BYTES));
+                uint8_t *st = smem + s * C::STAGE;
+                tma_load_2d(st, &tm_a, &c.full[s], kb * BK, arow);
+                // B: 16-bit tiles are 128 B per row, int8 tiles 64 B per row
+                constexpr int half_b = (Q8 ? BQ_BYTES : B_BYTES) / 2;
+                uint8_t *sc = st + A_BYTES + BQ_BYTES;   // Q8: scales [2 blocks][rows]
                 if (MODE == GATEUP) {
                     const int brow = e * p.F + nt * (BN / 2);
-                    tma_load_2d(sB + s * B_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
-                    tma_load_2d(sB + s * B_BYTES + B_BYTES / 2, &tm_b1, &c.full[s], kb * BK, brow);
+                    tma_load_2d(st + A_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
+                    tma_load_2d(st + A_BYTES + half_b, &tm_b1, &c.full[s], kb * BK, brow);
+                    if (Q8) {
+                        tma_load_2d(sc, &tm_s0, &c.full[s], brow, kb * 2);
+                        tma_load_2d(sc + SC_BYTES / 2, &tm_s1, &c.full[s], brow, kb * 2);
+                    }
                 } else {
                     const int brow = e * p.d + nt * BN;
-                    tma_load_2d(sB + s * B_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
+                    tma_load_2d(st + A_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
+                    if (Q8) tma_load_2d(sc, &tm_s0, &c.full[s], brow, kb * 2);
                 }
             }
         }
@@ -212,8 +267,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16(0);
-        const uint32_t idesc_rt = p.h_fp16 && MODE == DOWN ? idesc_f16(1) : idesc;
+        // fp16 operands on the Q8_0 path (grouped rows and h are fp16), else
+        // bf16 -- except a bf16-weight DOWN over an fp16 h, which cannot occur
+        const uint32_t idesc_rt = idesc_f16(Q8 ? 1 : 0);
         uint32_t it = 0, local_tile = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local_tile) {
@@ -226,15 +282,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
+                const int cb = it & 1;
+                if (Q8 && !mbar_wait(&c.cfull[cb], (it >> 1) & 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + s * A_BYTES);
-                const uint32_t b0 = smem_u32(sB + s * B_BYTES);
+                const uint32_t a0 = smem_u32(smem + s * C::STAGE);
+                const uint32_t b0 = Q8 ? smem_u32(sCvt + cb * B_BYTES) : a0 + A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc_rt,
                              (kb | kk) != 0);
                 }
                 umma_commit(&c.empty[s]);     // frees the stage when these MMAs finish
+                if (Q8) umma_commit(&c.cempty[cb]);
             }
             if (!ok) break;
             umma_commit(&c.tfull[acc]);       // accumulator ready for the epilogue
@@ -246,7 +305,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             volatile int no_abort = 0;
             mbar_wait(&c.drain, 0, &no_abort);
         }
-    } else if (warp >= 2) {
+    } else if (Q8 && warp >= 6) {
+        // ------------------------------------------------ Q8_0 converters (4 warps)
+        // lane -> (row in an 8-row pass, 16-byte column chunk of the int8 row);
+        // warp w converts rows [64(w-6), 64(w-6)+64) of the 256-row B tile
+        const int cw = warp - 6;
+        const int rsub = lane >> 2, q = lane & 3;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                const int cb = it & 1;
+                if (!mbar_wait(&c.full[s], (it / STAGES) & 1u, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&c.cempty[cb], ((it >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                const uint8_t *bq = smem + s * C::STAGE + A_BYTES;
+                const __half *scl = reinterpret_cast<const __half *>(bq + BQ_BYTES);
+                uint8_t *bo = sCvt + cb * B_BYTES;
+#pragma unroll
+                for (int pass = 0; pass < 8; ++pass) {
+                    const int r = cw * 64 + pass * 8 + rsub;
+                    // scale of (row r, 32-column block q/2): GATEUP keeps the gate
+                    // rows' [2][128] scales, then the up rows'; DOWN [2][256]
+                    const int blk = q >> 1;
+                    const __half sv = MODE == GATEUP
+                        ? scl[(r >> 7) * 256 + blk * 128 + (r & 127)]
+                        : scl[blk * 256 + r];
+                    const uint4 v = *reinterpret_cast<const uint4 *>(bq + r * 64 + q * 16);
+                    uint4 lo, hi;
+                    dequant16(v, __half2half2(sv), lo, hi);
+                    *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q) ^ (r & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4)) = hi;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&c.cfull[cb]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+        }
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------ epilogue (4 warps)
         const int quarter = warp & 3;         // TMEM lanes this warp may access
         const int row_in_tile = quarter * 32 + lane;
@@ -334,9 +433,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     }
 }
 
-constexpr size_t smem_bytes()
+template <bool Q8> constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+    return 1024 + Cfg<Q8>::CTL + sizeof(SmemCtl);
 }
 
 // ------------------------------------------------------------------- host
@@ -353,6 +452,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
         fn.store(f);
     }
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// 2-D row-major [rows, cols] int8 tensor, box {64 cols, box_rows}, no swizzle
+// (the converters read it row by row).
+static bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 // 2-D row-major [rows, cols] 16-bit tensor, box {64 cols, box_rows}, 128B swizzle.
@@ -374,7 +490,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 }  // namespace tc
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
-bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16; }
+bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || w_dt == MOE_Q8_0; }
 
 bool tc_gemm_prefer(int T, int d, int E, int k, int F)
 {
@@ -383,56 +499,105 @@ bool tc_gemm_prefer(int T, int d, int E, int k, int F)
     return (long long)T * k >= 64LL * E && T >= 512;
 }
 
+template <bool Q8>
+static cudaError_t set_smem_attrs()
+{
+    using namespace tc;
+    static std::atomic<int> done{0};
+    if (done.load()) return cudaSuccess;
+    const int smem = (int)smem_bytes<Q8>();
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return err;
+    done.store(1);
+    return cudaSuccess;
+}
+
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
 {
     using namespace tc;
-    if (a.w_dt != MOE_BF16) return cudaErrorNotSupported;   // Q8_0 mainloop: separate kernel
+    const bool q8 = a.w_dt == MOE_Q8_0;
+    if (!q8 && a.w_dt != MOE_BF16) return cudaErrorNotSupported;
     const int rows = a.T * a.k;
     cudaError_t err = cudaSuccess;
     if (!a.xp_ready &&
-        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, 0, a.num_sms, stream)) != cudaSuccess)
+        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, q8 ? 1 : 0, a.num_sms, stream)) !=
+            cudaSuccess)
         return err;
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
 
-    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // activations: bf16, or fp16 on the Q8_0 path
+    const CUtensorMapDataType act = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t gu_rows = (uint64_t)a.E * a.F, d_rows = (uint64_t)a.E * a.d;
     CUtensorMap m_xp, m_wg, m_wu, m_h, m_wd;
-    if (!make_map(&m_xp, a.xp, rows, a.d, BM, bf) ||
-        !make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BN / 2, bf) ||
-        !make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BN / 2, bf) ||
-        !make_map(&m_h, a.h, rows, a.F, BM, bf) ||
-        !make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BN, bf))
-        return cudaErrorInvalidValue;
-
-    const size_t smem = smem_bytes();
-    static std::atomic<int> attr_done{0};
-    if (!attr_done.load()) {
-        if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-                cudaSuccess)
-            return err;
-        attr_done.store(1);
+    bool ok = make_map(&m_xp, a.xp, rows, a.d, BM, act) && make_map(&m_h, a.h, rows, a.F, BM, act);
+    if (q8) {
+        ok = ok && make_map_u8(&m_wg, a.w_gate, gu_rows, a.d, BN / 2) &&
+             make_map_u8(&m_wu, a.w_up, gu_rows, a.d, BN / 2) &&
+             make_map_u8(&m_wd, a.w_down, d_rows, a.F, BN);
+    } else {
+        ok = ok && make_map(&m_wg, a.w_gate, gu_rows, a.d, BN / 2, act) &&
+             make_map(&m_wu, a.w_up, gu_rows, a.d, BN / 2, act) &&
+             make_map(&m_wd, a.w_down, d_rows, a.F, BN, act);
     }
+    if (!ok) return cudaErrorInvalidValue;
+    if ((err = q8 ? set_smem_attrs<true>() : set_smem_attrs<false>()) != cudaSuccess) return err;
+
+    // Q8_0 packed buffers: int8 plane, then the fp16 scale plane [cols/32, rows]
+    // at align256(rows * cols); maps with box {tile rows, 2 blocks}
+    auto scale_map = [](CUtensorMap *m, const void *packed, uint64_t r, uint64_t cols,
+                        uint32_t box_rows) {
+        auto enc = encode_fn();
+        if (!enc) return false;
+        const void *base = static_cast<const char *>(packed) + align_up((size_t)(r * cols), 256);
+        cuuint64_t dims[2] = {r, cols / 32};
+        cuuint64_t strides[1] = {r * 2};
+        cuuint32_t box[2] = {box_rows, 2};
+        cuuint32_t estr[2] = {1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    CUtensorMap m_sg, m_su, m_sd;
+    if (q8 && !(scale_map(&m_sg, a.w_gate, gu_rows, a.d, BN / 2) &&
+                scale_map(&m_su, a.w_up, gu_rows, a.d, BN / 2) &&
+                scale_map(&m_sd, a.w_down, d_rows, a.F, BN)))
+        return cudaErrorInvalidValue;
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k;
     p.h = static_cast<uint16_t *>(a.h); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
-    p.out = a.out; p.status = a.status; p.h_fp16 = 0;
+    p.out = a.out; p.status = a.status; p.h_fp16 = q8 ? 1 : 0;
 
     // upper bound on tiles: every expert could own a ragged tile
     const long long max_mtiles = rows / BM + (a.E < rows ? a.E : rows);
+    auto grid_for = [&](long long tiles) { return (int)(tiles < a.num_sms ? (tiles < 1 ? 1 : tiles) : a.num_sms); };
+
     p.K = a.d; p.n_tiles = a.F / (BN / 2);
-    int grid = (int)(max_mtiles * p.n_tiles < a.num_sms ? max_mtiles * p.n_tiles : a.num_sms);
-    if (grid < 1) grid = 1;
-    launch_pdl(grouped_gemm_kernel<GATEUP>, dim3(grid), dim3(THREADS), smem, stream, m_xp, m_wg, m_wu, p);
+    if (q8) {
+        launch_pdl(grouped_gemm_kernel<GATEUP, true>, dim3(grid_for(max_mtiles * p.n_tiles)),
+                   dim3(Cfg<true>::THREADS), smem_bytes<true>(), stream, m_xp, m_wg, m_wu, m_sg,
+                   m_su, p);
+    } else {
+        launch_pdl(grouped_gemm_kernel<GATEUP, false>, dim3(grid_for(max_mtiles * p.n_tiles)),
+                   dim3(Cfg<false>::THREADS), smem_bytes<false>(), stream, m_xp, m_wg, m_wu, m_xp,
+                   m_xp, p);
+    }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     p.K = a.F; p.n_tiles = a.d / BN;
-    grid = (int)(max_mtiles * p.n_tiles < a.num_sms ? max_mtiles * p.n_tiles : a.num_sms);
-    if (grid < 1) grid = 1;
-    launch_pdl(grouped_gemm_kernel<DOWN>, dim3(grid), dim3(THREADS), smem, stream, m_h, m_wd, m_wd, p);
+    if (q8) {
+        launch_pdl(grouped_gemm_kernel<DOWN, true>, dim3(grid_for(max_mtiles * p.n_tiles)),
+                   dim3(Cfg<true>::THREADS), smem_bytes<true>(), stream, m_h, m_wd, m_wd, m_sd,
+                   m_sd, p);
+    } else {
+        launch_pdl(grouped_gemm_kernel<DOWN, false>, dim3(grid_for(max_mtiles * p.n_tiles)),
+                   dim3(Cfg<false>::THREADS), smem_bytes<false>(), stream, m_h, m_wd, m_wd, m_h,
+                   m_h, p);
+    }
     return cudaGetLastError();
 }
 

@@ -116,7 +116,8 @@ MOE_API moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int
  * {fp16 scale (little endian), int8 q[32]}; value = scale * q.
  * moe_forward consumes them repacked into two planes in one buffer:
  *   bytes [0, rows*cols)                     int8 q plane [rows, cols]
- *   bytes [align256(rows*cols), ... + rows*cols/16)  fp16 scale plane [rows, cols/32]
+ *   bytes [align256(rows*cols), ... + rows*cols/16)  fp16 scale plane [cols/32, rows]
+ *   (the scale of block b of row r is at index b*rows + r)
  * moe_q8_0_packed_size returns the buffer size (0 if cols % 32 != 0 or
  * rows < 0).  moe_pack_q8_0 repacks `blocks` (device, any alignment) into
  * `packed` (device, 256-byte aligned) on `stream`; pack W_g and W_u as

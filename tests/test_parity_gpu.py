@@ -277,10 +277,11 @@ PREFILL_SMALL = [
 ]
 
 
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
 @pytest.mark.parametrize("T,d,E,k,F", PREFILL_SMALL)
-def test_forward_prefill_small_matches_oracle(T, d, E, k, F):
+def test_forward_prefill_small_matches_oracle(T, d, E, k, F, wdt):
     layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
-                                 w_dtype=wl.BF16, bias_sd=0.5)
+                                 w_dtype=wdt, bias_sd=0.5)
     t = upload_layer(layer, DEV)
     out = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
     idx_g, _ = _route(layer)
@@ -290,7 +291,7 @@ def test_forward_prefill_small_matches_oracle(T, d, E, k, F):
     ref, idx_ref, w_ref, margin = oracle.moe_forward(sub)
     check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g[rows])
     import expert_routed_ffn_selectedsoftmax_gb300 as pkg
-    ws = torch.empty(pkg.moe_workspace_size(T, d, E, k, F, 1, 1), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(pkg.moe_workspace_size(T, d, E, k, F, 1, wdt), dtype=torch.uint8, device=DEV)
     gpu_forward(layer, DEV, path=PREFILL, t=t, workspace=ws)
     assert pkg.moe_check(ws) == 0
 
@@ -309,13 +310,14 @@ def test_prefill_one_expert_many_tiles():
     check_output(out[rows], sub, ref, idx_ref, margin)
 
 
-def test_prefill_and_decode_paths_agree():
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
+def test_prefill_and_decode_paths_agree(wdt):
     layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
-                                 w_dtype=wl.BF16)
+                                 w_dtype=wdt)
     t = upload_layer(layer, DEV)
     a = gpu_forward(layer, DEV, path=SIMT, t=t).cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(a ** 2))
-    for path in (DECODE, PREFILL):
+    for path in ((DECODE, PREFILL) if wdt == wl.BF16 else (PREFILL,)):
         b = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy().astype(np.float64)
         assert np.abs(a - b).max() <= 2e-2 * rms
 
@@ -337,9 +339,10 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
     check_output(a, layer, ref, idx_ref, margin, idx_gpu=idx_g)
 
 
-def test_prefill_deterministic_and_equivariant():
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
+def test_prefill_deterministic_and_equivariant(wdt):
     layer = wl.make_custom_layer(24, T=512, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
-                                 w_dtype=wl.BF16)
+                                 w_dtype=wdt)
     t = upload_layer(layer, DEV)
     a = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
     b = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
