@@ -145,32 +145,40 @@ def algorithmic(w, T, counts_per_layer):
     per_w = wl.weight_bytes_per_expert(w.d, w.F, w.w_dtype)
     gu_w, dn_w = per_w * 2 // 3, per_w // 3
     x_b, wr_b, out_b, b_b = T * w.d * asz, w.E * w.d * asz, T * w.d * 4, w.E * 4
-    total = dict(bytes=0, flops=0, gateup_bytes=0, down_bytes=0, route_bytes=0, active=[])
+    total = dict(bytes=0, flops=0, gateup_bytes=0, down_bytes=0, route_bytes=0,
+                 gateup_flops=0, down_flops=0, active=[])
     for counts in counts_per_layer:
         act = int((np.asarray(counts) > 0).sum())
         total["active"].append(act)
         total["route_bytes"] += x_b + wr_b + b_b
         total["gateup_bytes"] += act * gu_w + x_b
         total["down_bytes"] += act * dn_w + out_b
+        total["gateup_flops"] += 2 * T * w.k * 2 * w.d * w.F
+        total["down_flops"] += 2 * T * w.k * w.d * w.F
         total["bytes"] += act * per_w + x_b + wr_b + out_b + b_b
         total["flops"] += 2 * T * w.d * w.E + 2 * T * w.k * 3 * w.d * w.F
     return total
 
 
 def expert_kernel_names(w, T):
-    """Which expert kernels moe_forward's AUTO path runs for this workload
-    (mirrors the library's selection: tensor-core decode for bf16 layers with
-    d, F multiples of 128 and T*k <= 8192; grouped GEMMs from 64 rows per
-    expert on average and T >= 512)."""
+    """Which kernels moe_forward's AUTO path runs for this workload (mirrors
+    the library's selection: grouped GEMMs from 64 rows per expert on average
+    and T >= 512 for bf16 / Q8_0 weights with d % 256 == 0 and F % 128 == 0;
+    tensor-core decode for bf16 layers with d, F multiples of 128 and
+    T*k <= 8192; otherwise the CUDA-core decode kernels), and how many of the
+    library's kernels one layer launches."""
     rows = T * w.k
-    bf16 = w.act_dtype == 1 and w.w_dtype == 1
-    if bf16 and w.d % 256 == 0 and w.F % 128 == 0 and rows >= 64 * w.E and T >= 512:
-        return {"file": "tc_gemm.cu", "gateup": "grouped_gemm_kernel<GATEUP>",
-                "down": "grouped_gemm_kernel<DOWN>"}
-    if bf16 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
-        return {"file": "decode_tc.cu", "gateup": "decode_tc_kernel<GATEUP>",
-                "down": "decode_tc_kernel<DOWN> + combine_kernel"}
-    return {"file": "decode.cu", "gateup": "decode_gateup_kernel", "down": "decode_down_kernel"}
+    act16 = w.act_dtype == 1
+    if (act16 and w.w_dtype in (1, 2) and w.d % 256 == 0 and w.F % 128 == 0
+            and rows >= 64 * w.E and T >= 512):
+        q = "Q8_0" if w.w_dtype == 2 else "bf16"
+        return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
+                "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4}
+    if act16 and w.w_dtype == 1 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
+        return {"file": "decode_tc.cu", "gateup": "decode_tc_kernel<GATEUP> + swiglu_reduce_kernel",
+                "down": "decode_tc_kernel<DOWN> + combine_kernel", "launches": 6}
+    return {"file": "decode.cu", "gateup": "decode_gateup_kernel", "down": "decode_down_kernel",
+            "launches": 4}
 
 
 def profile_traffic(kernel_key):
@@ -218,11 +226,16 @@ def host_layer_from_device(w, dl, T):
     from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
 
     def bits(t):
+        if t.dtype == torch.float32:
+            return t.contiguous().cpu().numpy()
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    if w.w_dtype == wl.Q8_0:   # the oracle reads the Q8_0 blocks themselves
+        wts = {n: dl["blocks"][n].cpu().numpy() for n in ("w_gate", "w_up", "w_down")}
+    else:
+        wts = {n: bits(dl[n]) for n in ("w_gate", "w_up", "w_down")}
     return wl.Layer(T=T, d=w.d, E=w.E, k=w.k, F=w.F, act_dtype=w.act_dtype, w_dtype=w.w_dtype,
                     x=bits(dl["x"]), w_router=bits(dl["w_router"]),
-                    bias=dl["bias"].float().cpu().numpy(), w_gate=bits(dl["w_gate"]),
-                    w_up=bits(dl["w_up"]), w_down=bits(dl["w_down"]))
+                    bias=dl["bias"].float().cpu().numpy(), **wts)
 
 
 def run_reference(args, w, T, layers):
@@ -298,7 +311,16 @@ def main():
 
     # ------------------------------------------------------------ inputs
     stack = wl.make_device_stack(w, seed=1 + rank, layers=layers, T=T, device=dev)
-    act_dt, w_dt = pkg.MOE_BF16, pkg.MOE_BF16
+    act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
+    w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0}[w.w_dtype]
+    if w_dt == pkg.MOE_Q8_0:
+        # Q8_0 blocks are repacked once, at load time, into the kernels' planes
+        for L in stack:
+            L["blocks"] = {n: L[n] for n in ("w_gate", "w_up", "w_down")}
+            for n, rows, cols in (("w_gate", w.E * w.F, w.d), ("w_up", w.E * w.F, w.d),
+                                  ("w_down", w.E * w.d, w.F)):
+                L[n] = pkg.moe_pack_q8_0(L[n].reshape(-1), rows, cols)
+        torch.cuda.synchronize(dev)
     ws_bytes = pkg.moe_workspace_size(T, w.d, w.E, w.k, w.F, act_dt, w_dt)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     outs = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in range(layers)]
@@ -307,7 +329,7 @@ def main():
     def layer_call(i, events=None):
         L = stack[i]
         pkg.moe_forward(L["x"], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
-                        w.k, out=outs[i], workspace=ws, events=events)
+                        w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws, events=events)
 
     def step():
         for i in range(layers):
@@ -398,18 +420,29 @@ def main():
     # ------------------------------------------------------- roofline object
     peaks, peak_src = load_peaks()
     hbm = peak_value(peaks, "hbm_gbs")
-    gu_bytes_per_launch = alg["gateup_bytes"] / layers
-    dn_bytes_per_launch = alg["down_bytes"] / layers
+    tflops_peak = peak_value(peaks, "bf16_tflops")   # fp16 dense rate equals bf16
     names = expert_kernel_names(w, T)
     dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
-    dom_bytes = gu_bytes_per_launch if dominant == "gateup" else dn_bytes_per_launch
     dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
-    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    dom_bytes = alg[f"{dominant}_bytes"] / layers
+    dom_flops = alg[f"{dominant}_flops"] / layers
+    # the kernel's bound: tensor when its arithmetic intensity is past the ridge
+    tensor_bound = dom_flops / dom_bytes > tflops_peak * 1e12 / (hbm * 1e9)
     traffic = profile_traffic(f"{names['file']}:{dominant}")
-    roofline = {"bound": "hbm", "kernel": names[dominant], "achieved": achieved,
-                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                "peak_source": f"hbm_gbs of {peak_src}",
-                "bytes_per_launch": dom_bytes, "us_per_launch": dom_us}
+    if tensor_bound:
+        achieved = dom_flops / (dom_us * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "kernel": names[dominant], "achieved": achieved,
+                    "peak": tflops_peak, "unit": "TFLOP/s", "frac": achieved / tflops_peak,
+                    "traffic": traffic, "peak_source": f"bf16_tflops of {peak_src}",
+                    "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
+                    "us_per_launch": dom_us}
+    else:
+        achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": names[dominant], "achieved": achieved,
+                    "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                    "peak_source": f"hbm_gbs of {peak_src}",
+                    "bytes_per_launch": dom_bytes, "flops_per_launch": dom_flops,
+                    "us_per_launch": dom_us}
     layer_gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
     layer_tflops = alg["flops"] / (ms_per_step * 1e-3) / 1e12
 
@@ -426,7 +459,7 @@ def main():
         for i in range(layers):
             L = stack[i]
             pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
-                            w.k, out=outs[i], workspace=ws)
+                            w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws)
         for i in range(layers):
             hout[i].copy_(outs[i], non_blocking=True)
     with torch.cuda.stream(stream):
@@ -457,11 +490,12 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands"}[w.w_dtype],
         "data": "synthetic", "config": config_dict(w, T, layers, args),
         "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s",
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * layers * args.steps,
+        "gpu_launches": names["launches"] * layers * args.steps,
         "roofline": roofline, "cpu_baseline": cpu,
         "layer": {"algorithmic_GBps": layer_gbs, "TFLOPS": layer_tflops,
                   "frac_hbm": layer_gbs / hbm, "bytes_per_step": alg["bytes"],

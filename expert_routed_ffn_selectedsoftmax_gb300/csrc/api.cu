@@ -256,7 +256,7 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     const bool act16 = act_dt == MOE_BF16;
     ra.xp = ((use_prefill || use_dtc) && act16) ? ws + L.xp : nullptr;
     ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows
-    ra.out_zero = zero_out ? out : nullptr;
+    ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     ra.zero_words = nullptr;
     ra.n_zero = 0;
     ra.status = status;
@@ -282,7 +282,7 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
         a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down; a.w_dt = w_dt;
         a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
         a.xp = ws + L.xp; a.xp_ready = xp_ready;
-        a.h = ws + L.h; a.out = out; a.status = status; a.num_sms = num_sms;
+        a.h = ws + L.h; a.out = out; a.zero_out = zero_out; a.status = status; a.num_sms = num_sms;
         a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
         e = launch_tc_experts(a, s);
     } else if (use_dtc) {

@@ -8,7 +8,8 @@
 //
 // route_tc_kernel: one CTA per tile of 128 tokens.  Warp 0 streams the x tile
 // [128 x 64] and the router tile [EP x 64] (E rows padded to a multiple of 16,
-// TMA zero-fills the padding) through a 4-stage ring; warp 1 issues
+// TMA zero-fills the padding) through a ring of up to 8 stages (as many as fit
+// in 192 KB for this EP); warp 1 issues
 // tcgen05.mma M=128, N=EP, accumulating the logits [128 tokens x EP] in TMEM
 // (fp32); warps 2-5 each own 32 tokens -- thread = token: it reads its logit
 // row from TMEM, keeps a sorted top-k in registers, and writes indices and
@@ -39,10 +40,16 @@ namespace rtc {
 
 using namespace sm100;
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64, MAXST = 8;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB x tile
-constexpr int B_MAX_BYTES = 256 * BK * 2;       // 32 KB router tile (EP <= 256)
+constexpr int RING_BYTES = 192 * 1024;          // stages of A_BYTES + EP * 128
 constexpr int THREADS = 192;
+
+__host__ __device__ constexpr int stage_bytes(int EP) { return (A_BYTES + EP * BK * 2 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int num_stages(int EP)
+{
+    return RING_BYTES / stage_bytes(EP) < MAXST ? RING_BYTES / stage_bytes(EP) : MAXST;
+}
 
 struct Params {
     int T, d, E, EP, k;
@@ -58,7 +65,7 @@ struct Params {
 };
 
 struct Ctl {
-    uint64_t full[STAGES], empty[STAGES], tfull, epi;
+    uint64_t full[MAXST], empty[MAXST], tfull, epi;
     uint32_t tmem_base;
     int abort_flag;
     float bias[kMaxExperts];
@@ -76,10 +83,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_BYTES;
     const int b_bytes = p.EP * BK * 2;
-    Ctl &c = *reinterpret_cast<Ctl *>(sB + STAGES * B_MAX_BYTES);
+    const int SLOT = stage_bytes(p.EP), STAGES = num_stages(p.EP);
+    Ctl &c = *reinterpret_cast<Ctl *>(smem + RING_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E, EP = p.EP;
@@ -123,8 +129,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint32_t ph = (kb / STAGES) & 1u;
             if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
             mbar_expect_tx(&c.full[s], A_BYTES + b_bytes);
-            tma_load_2d(sA + s * A_BYTES, &tm_x, &c.full[s], kb * BK, t0);
-            tma_load_2d(sB + s * B_MAX_BYTES, &tm_w, &c.full[s], kb * BK, 0);
+            tma_load_2d(smem + s * SLOT, &tm_x, &c.full[s], kb * BK, t0);
+            tma_load_2d(smem + s * SLOT + A_BYTES, &tm_w, &c.full[s], kb * BK, 0);
         }
         if (!ok) {
             atomicOr(p.status, kDevTimeout);
@@ -143,8 +149,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint32_t ph = (kb / STAGES) & 1u;
             if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * A_BYTES);
-            const uint32_t b0 = smem_u32(sB + s * B_MAX_BYTES);
+            const uint32_t a0 = smem_u32(smem + s * SLOT);
+            const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
                 umma_f16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
@@ -335,49 +341,69 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
     const int t0 = b * tile_tokens;
     const int nslots = min(tile_tokens, T - t0) * k;
     const int part = blockIdx.y, nparts = gridDim.y;
-    // one warp per slot: lane 0 resolves the row, the warp copies x[t] to xp[row]
-    for (int i = part + nparts * warp; i < nslots; i += nparts * (blockDim.x / 32)) {
-        const size_t slot = (size_t)t0 * k + i;
-        int pos = -1;
-        if (lane == 0) {
+    const int nwarps = nparts * (blockDim.x / 32), gw = part * (blockDim.x / 32) + warp;
+    // warp gw owns slots gw, gw + nwarps, ...: in batches of 32, one slot per
+    // lane resolves its grouped row (all loads in parallel), then the warp
+    // copies the batch's x rows two at a time
+    for (int b0 = 0; gw + b0 * nwarps < nslots; b0 += 32) {
+        const int i = gw + (b0 + lane) * nwarps;
+        int pos = -1, tok = 0;
+        if (i < nslots) {
+            const size_t slot = (size_t)t0 * k + i;
             const int e = __ldcg(topk_idx + slot);
             pos = (e >= 0 && e < E) ? off[e] + pre[e] + __ldcg(rank + slot) : -1;
+            tok = (int)(slot / k);
             if (pos < 0 || pos >= nslots_all) {   // cannot happen with consistent routing
                 if (status) atomicOr(status, kDevCheckFailed);
                 pos = -1;
             } else {
-                perm_tok[pos] = (int)(slot / k);
+                perm_tok[pos] = tok;
                 inv[slot] = pos;
                 perm_w[pos] = __ldcg(topk_w + slot);
             }
         }
-        pos = __shfl_sync(0xffffffffu, pos, 0);
-        if (pos < 0 || !xp) continue;
-        const int t = (int)(slot / k);
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
-        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)pos * d);
+        if (!xp) continue;
         const int vec = d / 8;
-        constexpr int U = 4;   // 4 x 16 bytes per lane in flight
-        for (int c0 = lane; c0 < vec; c0 += 32 * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c0 + 32 * u < vec) v[u] = __ldg(src + c0 + 32 * u);
-            if (xp_fp16) {   // bf16 -> fp16 rows for the fp16 (Q8_0) tensor-core path
+        for (int j = 0; j < 32; j += 2) {
+            const int p0 = __shfl_sync(0xffffffffu, pos, j), q0 = __shfl_sync(0xffffffffu, tok, j);
+            const int p1 = __shfl_sync(0xffffffffu, pos, j + 1), q1 = __shfl_sync(0xffffffffu, tok, j + 1);
+            if (p0 < 0 && p1 < 0) continue;
+            const uint4 *s0 = reinterpret_cast<const uint4 *>(x + (size_t)q0 * d);
+            const uint4 *s1 = reinterpret_cast<const uint4 *>(x + (size_t)q1 * d);
+            uint4 *d0 = reinterpret_cast<uint4 *>(xp + (size_t)(p0 < 0 ? 0 : p0) * d);
+            uint4 *d1 = reinterpret_cast<uint4 *>(xp + (size_t)(p1 < 0 ? 0 : p1) * d);
+            constexpr int U = 4;   // 2 rows x 4 x 16 bytes per lane in flight
+            for (int c0 = lane; c0 < vec; c0 += 32 * U) {
+                uint4 v[2][U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        __half2 hh = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
-                        w[i] = *reinterpret_cast<uint32_t *>(&hh);
+                    const int c = c0 + 32 * u;
+                    if (c < vec) {
+                        if (p0 >= 0) v[0][u] = __ldg(s0 + c);
+                        if (p1 >= 0) v[1][u] = __ldg(s1 + c);
                     }
-                    v[u] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if ((r ? p1 : p0) < 0) continue;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + 32 * u;
+                        if (c >= vec) continue;
+                        uint4 w4 = v[r][u];
+                        if (xp_fp16) {   // bf16 -> fp16 rows for the fp16 (Q8_0) tensor-core path
+                            uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                __half2 hh = __floats2half2_rn(bf16lo(w[q]), bf16hi(w[q]));
+                                w[q] = *reinterpret_cast<uint32_t *>(&hh);
+                            }
+                            w4 = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                        (r ? d1 : d0)[c] = w4;
+                    }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c0 + 32 * u < vec) dst[c0 + 32 * u] = v[u];
         }
     }
 }
@@ -386,7 +412,7 @@ namespace rtc {
 
 constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)STAGES * (A_BYTES + B_MAX_BYTES) + sizeof(Ctl);
+    return 1024 + (size_t)RING_BYTES + sizeof(Ctl);
 }
 
 }  // namespace rtc

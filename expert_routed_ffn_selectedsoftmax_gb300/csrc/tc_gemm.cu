@@ -13,10 +13,19 @@
 //   the epilogue scales each row by its routing weight and adds it into
 //   out[token] (fp32; a plain store when k == 1).
 //
+// Clusters of CL = 2 CTAs work on the two m-tiles (same expert, same
+// n-tile) of one work unit: each CTA loads its own A tile and one half of the
+// shared B tile with a cluster-multicast TMA, so every SM pulls 2/3 of the
+// operand bytes of a lone CTA; each CTA's MMA commit is multicast to the
+// "stage empty" barriers of both CTAs, since a stage is refilled in both.
+//
 // Per CTA (persistent, one per SM): warp 0 issues TMA loads of the A (rows)
 // and B (weights) tiles into a 4-stage shared-memory ring (128-byte swizzle);
 // warp 1 issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulators in TMEM,
-// two accumulator buffers of 256 columns); warps 2-5 drain the accumulators.
+// two accumulator buffers of 256 columns); warps 2-9 drain the accumulators,
+// two warps per 32-lane TMEM quarter, each taking half of the tile's columns
+// (with one warp per scheduler the drain was latency-bound and as slow as
+// the mainloop of a tile).
 // Tiles are (expert, n-tile, m-tile), m fastest, so CTAs running at the same
 // time share weight tiles through L2.  Rows of a tile past the end of the
 // expert's group are computed on neighbouring rows (or TMA zero fill) and
@@ -24,7 +33,7 @@
 //
 // Q8_0 weights ("zonos2.cpp internals", §Quantization: 8-bit blocks of 32
 // values with one fp16 scale): the B stage holds the int8 tile as loaded by
-// TMA; four converter warps (6-9) turn it into fp16 in the 128-byte-swizzled
+// TMA; four converter warps (10-13) turn it into fp16 in the 128-byte-swizzled
 // layout -- int8 -> fp16 exactly via the 1024+q bit trick, times the block's
 // fp16 scale -- in one of two converted-B buffers, and the MMA runs kind::f16
 // with fp16 operands (the grouped rows and h are fp16 on this path).
@@ -42,6 +51,17 @@
 #include "kernels.h"
 #include "sm100.cuh"
 #include "tc_gemm.h"
+
+// Tuning (compile-time): CTAs per cluster (1 or 2) and whether units start
+// at a rotated k-block.  Measured on the ZONOS3-Mini and ZONOS2 prefill
+// layers, pairs that share the weight tile by multicast were 6-9 % slower
+// than single CTAs and the rotation made no difference, so both are off.
+#ifndef MOE_GEMM_CLUSTER
+#define MOE_GEMM_CLUSTER 1
+#endif
+#ifndef MOE_GEMM_KROTATE
+#define MOE_GEMM_KROTATE 0
+#endif
 
 namespace moe {
 namespace tc {
@@ -61,11 +81,12 @@ template <bool Q8> struct Cfg {
     static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SC_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
     static constexpr int CVT = Q8 ? 2 : 0;
-    static constexpr int THREADS = Q8 ? 320 : 192;
+    static constexpr int THREADS = Q8 ? 448 : 320;   // 2 + 8 epilogue (+ 4 converter) warps
     static constexpr size_t CTL = (size_t)STAGES * STAGE + (size_t)CVT * B_BYTES;
 };
 
 enum Mode { GATEUP = 0, DOWN = 1 };
+constexpr int kEpiThreads = 256;   // 8 epilogue warps
 
 struct Params {
     const int32_t *offsets;   // [E+1] grouped-row offsets
@@ -79,6 +100,8 @@ struct Params {
     float *out;
     uint32_t *status;
     int h_fp16;               // GATEUP: write h as fp16 (else bf16)
+    float *out_zero;          // GATEUP: `out` to zero for the down kernel's adds, or null
+    long long zero4;          // float4 elements of out_zero
 };
 
 struct SmemCtl {
@@ -94,9 +117,14 @@ struct SmemCtl {
 // Instruction descriptor for the M = 128, N = 256 tiles of this file.
 __host__ __device__ constexpr uint32_t idesc_f16(int ab_fp16) { return idesc_f16_mn(ab_fp16, BM, BN); }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// SiLU(z) = z * sigmoid(z), with the fast exponential and an approximate
+// divide (relative error ~1e-6, far below the 16-bit rounding of h that
+// follows; for z < -87, 1 + e^-z overflows and the result is the correct -0).
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // tile -> (expert, m-tile, n-tile); tile_start is an exclusive scan over experts
+// unit -> (expert, m-tile pair, n-tile); units are mt-pair fastest.  mtiles[e]
+// holds the number of CL-sized m-tile groups of expert e.
 __device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int n_tiles, int tile,
                                             int &e, int &mt, int &nt)
 {
@@ -136,8 +164,8 @@ __device__ __forceinline__ void dequant16(const uint4 q, const __half2 s, uint4 
 }
 
 // tm_s0/tm_s1 (Q8 only): the B matrices' fp16 scale planes [cols/32, rows],
-// box {rows of the tile, 2 blocks}.
-template <int MODE, bool Q8>
+// box {128 rows, 2 blocks}.  CL: CTAs per cluster (1 or 2).
+template <int MODE, bool Q8, int CL>
 __global__ void __launch_bounds__(Cfg<Q8>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b0,
@@ -145,7 +173,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_s0,
                     const __grid_constant__ CUtensorMap tm_s1, const Params p)
 {
-    pdl_enter();
     using C = Cfg<Q8>;
     constexpr int THREADS = C::THREADS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -154,15 +181,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     uint8_t *sCvt = smem + STAGES * C::STAGE;   // Q8: converted fp16 B buffers
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(smem + C::CTL);
 
-    if (upstream_failed(p.status)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
+    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / CL, nclusters = gridDim.x / CL;
+    constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1u);
 
-    // ---- set-up: barriers, tile table, TMEM
+    // ---- set-up that reads nothing the preceding kernels write (barriers,
+    // TMEM, tensor-map prefetch): under programmatic dependent launch it
+    // overlaps the tail of the kernel before
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], CL); }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128);
+            mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], kEpiThreads);
             mbar_init(&c.cfull[b], 128); mbar_init(&c.cempty[b], 1);
         }
         mbar_init(&c.drain, 1);
@@ -175,6 +206,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         if (MODE == GATEUP)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b1)) : "memory");
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&c.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    pdl_enter();
+    if (upstream_failed(p.status)) {   // (synchronises the CTA)
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(c.tmem_base, TMEM_COLS);
+        }
+        return;
+    }
+    // ---- tile table from the grouped-row offsets
     for (int e = threadIdx.x; e <= E; e += THREADS) c.off[e] = p.offsets[e];
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -186,7 +234,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             int m = 0;
             if (e < E) {
                 const int rows = c.off[e + 1] - c.off[e];
-                m = (rows + BM - 1) / BM;
+                m = (rows + BM * CL - 1) / (BM * CL);   // groups of CL m-tiles
                 c.mtiles[e] = m;
             }
             local[j] = m * p.n_tiles;
@@ -207,15 +255,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         }
         if (lane == 31) { c.n_tiles_total = incl; c.tile_start[E] = incl; }
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&c.tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
     tc_fence_before();
-    __syncthreads();
+    // the peer's multicast copies and commits target this CTA's barriers:
+    // every barrier of the cluster is initialised before anyone proceeds
+    if (CL > 1) cluster_sync_all();
+    else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem = c.tmem_base;
@@ -227,11 +271,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         // ------------------------------------------------ TMA producer
         uint32_t it = 0;   // global k-block counter across tiles
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int tile = cid; tile < total && ok; tile += nclusters) {
             int e, mt, nt;
             decode_tile(c, E, p.n_tiles, tile, e, mt, nt);
+            mt = mt * CL + rank;
             const int arow = c.off[e] + mt * BM;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+            // units start at different k-blocks, so CTAs sharing a weight tile do
+            // not all request the same lines at once (same order for both CTAs
+            // of a pair; the sum order of a tile is fixed by its unit id)
+            const int rot = MOE_GEMM_KROTATE ? (tile * 5) % kblocks : 0;
+            for (int kl = 0; kl < kblocks; ++kl, ++it) {
+                const int kb = kl + rot < kblocks ? kl + rot : kl + rot - kblocks;
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
@@ -240,19 +290,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 tma_load_2d(st, &tm_a, &c.full[s], kb * BK, arow);
                 // B: 16-bit tiles are 128 B per row, int8 tiles 64 B per row
                 constexpr int half_b = (Q8 ? BQ_BYTES : B_BYTES) / 2;
-                uint8_t *sc = st + A_BYTES + BQ_BYTES;   // Q8: scales [2 blocks][rows]
-                if (MODE == GATEUP) {
-                    const int brow = e * p.F + nt * (BN / 2);
-                    tma_load_2d(st + A_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
-                    tma_load_2d(st + A_BYTES + half_b, &tm_b1, &c.full[s], kb * BK, brow);
+                // Q8 scales: two [2 blocks][128 rows] boxes, one per B half
+                uint8_t *sc = st + A_BYTES + BQ_BYTES;
+                // B halves: GATEUP = (gate rows, up rows), DOWN = (rows 0-127, 128-255)
+                const int brow = MODE == GATEUP ? e * p.F + nt * (BN / 2) : e * p.d + nt * BN;
+                const CUtensorMap *bm[2] = {&tm_b0, MODE == GATEUP ? &tm_b1 : &tm_b0};
+                const CUtensorMap *sm[2] = {&tm_s0, MODE == GATEUP ? &tm_s1 : &tm_s0};
+                const int hrow[2] = {brow, MODE == GATEUP ? brow : brow + BN / 2};
+                if (CL == 1) {
+                    if (MODE == GATEUP) {
+                        tma_load_2d(st + A_BYTES, bm[0], &c.full[s], kb * BK, hrow[0]);
+                        tma_load_2d(st + A_BYTES + half_b, bm[1], &c.full[s], kb * BK, hrow[1]);
+                    } else {
+                        tma_load_2d(st + A_BYTES, &tm_b0, &c.full[s], kb * BK, brow);   // 256-row box
+                    }
                     if (Q8) {
-                        tma_load_2d(sc, &tm_s0, &c.full[s], brow, kb * 2);
-                        tma_load_2d(sc + SC_BYTES / 2, &tm_s1, &c.full[s], brow, kb * 2);
+                        tma_load_2d(sc, sm[0], &c.full[s], hrow[0], kb * 2);
+                        tma_load_2d(sc + SC_BYTES / 2, sm[1], &c.full[s], hrow[1], kb * 2);
                     }
                 } else {
-                    const int brow = e * p.d + nt * BN;
-                    tma_load_2d(st + A_BYTES, &tm_b0, &c.full[s], kb * BK, brow);
-                    if (Q8) tma_load_2d(sc, &tm_s0, &c.full[s], brow, kb * 2);
+                    // this CTA fetches half `rank` of B for both CTAs of the pair
+                    tma_load_2d_mc(st + A_BYTES + rank * half_b, bm[rank], &c.full[s], kb * BK,
+                                   hrow[rank], kAll);
+                    if (Q8)
+                        tma_load_2d_mc(sc + rank * (SC_BYTES / 2), sm[rank], &c.full[s], hrow[rank],
+                                       kb * 2, kAll);
                 }
             }
         }
@@ -272,7 +334,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         const uint32_t idesc_rt = idesc_f16(Q8 ? 1 : 0);
         uint32_t it = 0, local_tile = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local_tile) {
+        for (int tile = cid; tile < total && ok; tile += nclusters, ++local_tile) {
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_ph = (local_tile >> 1) & 1u;
             if (!mbar_wait(&c.tempty[acc], acc_ph ^ 1u, abort_flag)) { ok = false; break; }
@@ -292,7 +354,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc_rt,
                              (kb | kk) != 0);
                 }
-                umma_commit(&c.empty[s]);     // frees the stage when these MMAs finish
+                // frees the stage (in both CTAs of a pair) when these MMAs finish
+                if (CL > 1) umma_commit_mc(&c.empty[s], kAll);
+                else umma_commit(&c.empty[s]);
                 if (Q8) umma_commit(&c.cempty[cb]);
             }
             if (!ok) break;
@@ -305,15 +369,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             volatile int no_abort = 0;
             mbar_wait(&c.drain, 0, &no_abort);
         }
-    } else if (Q8 && warp >= 6) {
+    } else if (Q8 && warp >= 10) {
         // ------------------------------------------------ Q8_0 converters (4 warps)
         // lane -> (row in an 8-row pass, 16-byte column chunk of the int8 row);
-        // warp w converts rows [64(w-6), 64(w-6)+64) of the 256-row B tile
-        const int cw = warp - 6;
+        // warp w converts rows [64(w-10), 64(w-10)+64) of the 256-row B tile
+        const int cw = warp - 10;
         const int rsub = lane >> 2, q = lane & 3;
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int tile = cid; tile < total && ok; tile += nclusters) {
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 const int cb = it & 1;
@@ -328,9 +392,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     // scale of (row r, 32-column block q/2): GATEUP keeps the gate
                     // rows' [2][128] scales, then the up rows'; DOWN [2][256]
                     const int blk = q >> 1;
-                    const __half sv = MODE == GATEUP
-                        ? scl[(r >> 7) * 256 + blk * 128 + (r & 127)]
-                        : scl[blk * 256 + r];
+                    const __half sv = scl[(r >> 7) * 256 + blk * 128 + (r & 127)];
                     const uint4 v = *reinterpret_cast<const uint4 *>(bq + r * 64 + q * 16);
                     uint4 lo, hi;
                     dequant16(v, __half2half2(sv), lo, hi);
@@ -345,12 +407,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             if (lane == 0) atomicOr(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
-    } else if (warp >= 2 && warp < 6) {
-        // ------------------------------------------------ epilogue (4 warps)
+    } else if (warp >= 2 && warp < 10) {
+        // ------------------------------------------------ epilogue (8 warps)
         const int quarter = warp & 3;         // TMEM lanes this warp may access
         const int row_in_tile = quarter * 32 + lane;
+        const int chalf = (warp - 2) >> 2;    // which half of the tile's columns
+        if (MODE == GATEUP && p.out_zero) {
+            // the down kernel accumulates into `out`: zero this CTA's share of
+            // it while the first tile's operands stream in
+            float4 *o4 = reinterpret_cast<float4 *>(p.out_zero);
+            const long long per = (p.zero4 + gridDim.x - 1) / gridDim.x;
+            const long long lo = (long long)blockIdx.x * per;
+            const long long hi = lo + per < p.zero4 ? lo + per : p.zero4;
+            for (long long i = lo + (threadIdx.x - 64); i < hi; i += kEpiThreads)
+                o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         uint32_t local_tile = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local_tile) {
+        for (int tile = cid; tile < total; tile += nclusters, ++local_tile) {
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_ph = (local_tile >> 1) & 1u;
             // warp-uniform outcome: tcgen05.ld below is warp-collective
@@ -362,23 +435,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             tc_fence_after();
             int e, mt, nt;
             decode_tile(c, E, p.n_tiles, tile, e, mt, nt);
+            mt = mt * CL + rank;
             const int rows_e = c.off[e + 1] - c.off[e];
             const bool valid = mt * BM + row_in_tile < rows_e;
             const int grow = c.off[e] + mt * BM + row_in_tile;
             const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
             if (MODE == GATEUP) {
-                uint16_t *hrow = p.h + (size_t)grow * p.F + nt * (BN / 2);
+                // this thread: h columns [chalf*64, chalf*64 + 64) of its row
+                constexpr int HC = BN / 4;
+                uint16_t *hrow = p.h + (size_t)grow * p.F + nt * (BN / 2) + chalf * HC;
+                const uint32_t tg = tbase + chalf * HC, tu = tg + BN / 2;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 2; cc += 16) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tbase + cc, g);
-                    tmem_ld16(tbase + BN / 2 + cc, u);
+                for (int cc = 0; cc < HC; cc += 32) {
+                    uint32_t g[2][16], u[2][16];
+                    tmem_ld16(tg + cc, g[0]);
+                    tmem_ld16(tg + cc + 16, g[1]);
+                    tmem_ld16(tu + cc, u[0]);
+                    tmem_ld16(tu + cc + 16, u[1]);
                     tmem_ld_wait();
-                    uint32_t packed[8];
+                    uint32_t packed[16];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-                        const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                    for (int j = 0; j < 16; ++j) {
+                        const int hi = j >> 3, i0 = (2 * j) & 15;
+                        const float h0 = silu_f(__uint_as_float(g[hi][i0])) * __uint_as_float(u[hi][i0]);
+                        const float h1 = silu_f(__uint_as_float(g[hi][i0 + 1])) * __uint_as_float(u[hi][i0 + 1]);
                         if (p.h_fp16) {
                             __half2 v = __floats2half2_rn(h0, h1);
                             packed[j] = *reinterpret_cast<uint32_t *>(&v);
@@ -389,19 +469,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     }
                     if (valid) {
                         uint4 *dst = reinterpret_cast<uint4 *>(hrow + cc);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                                packed[4 * q + 3]);
                     }
                 }
             } else {
                 int tok = 0;
                 float wgt = 0.f;
                 if (valid) { tok = p.perm_tok[grow]; wgt = p.perm_w[grow]; }
-                float *orow = p.out + (size_t)tok * p.d + nt * BN;
+                // this thread: output columns [chalf*128, chalf*128 + 128) of its row
+                float *orow = p.out + (size_t)tok * p.d + nt * BN + chalf * (BN / 2);
+                const uint32_t tv = tbase + chalf * (BN / 2);
 #pragma unroll 1
-                for (int cc = 0; cc < BN; cc += 16) {
+                for (int cc = 0; cc < BN / 2; cc += 16) {
                     uint32_t v[16];
-                    tmem_ld16(tbase + cc, v);
+                    tmem_ld16(tv + cc, v);
                     tmem_ld_wait();
                     if (valid) {
 #pragma unroll
@@ -423,7 +507,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         }
     }
 
-    __syncthreads();
+    // no CTA leaves while its peer may still multicast into it or commit to it
+    if (CL > 1) cluster_sync_all();
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -499,7 +585,9 @@ bool tc_gemm_prefer(int T, int d, int E, int k, int F)
     return (long long)T * k >= 64LL * E && T >= 512;
 }
 
-template <bool Q8>
+constexpr int kCluster = MOE_GEMM_CLUSTER;   // CTAs per cluster of the grouped GEMMs
+
+template <bool Q8, int CL>
 static cudaError_t set_smem_attrs()
 {
     using namespace tc;
@@ -507,13 +595,88 @@ static cudaError_t set_smem_attrs()
     if (done.load()) return cudaSuccess;
     const int smem = (int)smem_bytes<Q8>();
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8>,
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8, CL>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8>,
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8, CL>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return err;
     done.store(1);
     return cudaSuccess;
+}
+
+// Clusters of CL CTAs that can be resident at once (0 if the query fails).
+template <int MODE, bool Q8, int CL>
+static int max_active_clusters()
+{
+    using namespace tc;
+    static std::atomic<int> cached{-1};
+    int n = cached.load();
+    if (n >= 0) return n;
+    // the query needs the kernel's dynamic shared-memory limit raised first
+    if (set_smem_attrs<Q8, CL>() != cudaSuccess) {
+        cudaGetLastError();
+        cached.store(0);
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL * 152);
+    cfg.blockDim = dim3(Cfg<Q8>::THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<Q8>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, Q8, CL>, &cfg) != cudaSuccess)
+        n = 0;
+    cudaGetLastError();   // clear a failed query
+    cached.store(n);
+    return n;
+}
+
+template <bool Q8, int CL>
+static cudaError_t launch_pair(const TcArgs &a, tc::Params p, const CUtensorMap &m_xp,
+                               const CUtensorMap &m_wg, const CUtensorMap &m_wu,
+                               const CUtensorMap &m_h, const CUtensorMap &m_wd,
+                               const CUtensorMap &m_sg, const CUtensorMap &m_su,
+                               const CUtensorMap &m_sd, cudaStream_t stream)
+{
+    using namespace tc;
+    cudaError_t err;
+    if ((err = set_smem_attrs<Q8, CL>()) != cudaSuccess) return err;
+    const int rows = a.T * a.k;
+    // upper bound on units: every expert could own a ragged group of CL m-tiles
+    const long long max_groups = rows / (BM * CL) + (a.E < rows ? a.E : rows);
+    auto grid_for = [&](long long units, int max_clusters) {
+        long long cl = units < max_clusters ? units : max_clusters;
+        return dim3((unsigned)((cl < 1 ? 1 : cl) * CL));
+    };
+    const size_t smem = smem_bytes<Q8>();
+    const dim3 block(Cfg<Q8>::THREADS);
+
+    p.K = a.d; p.n_tiles = a.F / (BN / 2);
+    const dim3 g1 = grid_for(max_groups * p.n_tiles, CL > 1 ? max_active_clusters<GATEUP, Q8, CL>() : a.num_sms);
+    if (CL > 1)
+        err = launch_pdl_cluster(grouped_gemm_kernel<GATEUP, Q8, CL>, g1, block, smem, stream, CL,
+                                 m_xp, m_wg, m_wu, m_sg, m_su, p);
+    else
+        err = launch_pdl(grouped_gemm_kernel<GATEUP, Q8, CL>, g1, block, smem, stream, m_xp, m_wg,
+                         m_wu, m_sg, m_su, p);
+    if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
+    if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
+
+    p.K = a.F; p.n_tiles = a.d / BN;
+    const dim3 g2 = grid_for(max_groups * p.n_tiles, CL > 1 ? max_active_clusters<DOWN, Q8, CL>() : a.num_sms);
+    if (CL > 1)
+        err = launch_pdl_cluster(grouped_gemm_kernel<DOWN, Q8, CL>, g2, block, smem, stream, CL, m_h,
+                                 m_wd, m_wd, m_sd, m_sd, p);
+    else
+        err = launch_pdl(grouped_gemm_kernel<DOWN, Q8, CL>, g2, block, smem, stream, m_h, m_wd, m_wd,
+                         m_sd, m_sd, p);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
@@ -529,76 +692,58 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
         return err;
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
 
+    // pairs of CTAs when clusters of two can be resident, else single CTAs
+    const bool pair = (q8 ? max_active_clusters<GATEUP, true, kCluster>()
+                          : max_active_clusters<GATEUP, false, kCluster>()) > 0;
+    const int CLr = pair ? kCluster : 1;
+
     // activations: bf16, or fp16 on the Q8_0 path
     const CUtensorMapDataType act = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t gu_rows = (uint64_t)a.E * a.F, d_rows = (uint64_t)a.E * a.d;
+    const uint32_t wd_box = (uint32_t)(BN / CLr);   // a pair fetches W_d in two 128-row halves
     CUtensorMap m_xp, m_wg, m_wu, m_h, m_wd;
     bool ok = make_map(&m_xp, a.xp, rows, a.d, BM, act) && make_map(&m_h, a.h, rows, a.F, BM, act);
     if (q8) {
         ok = ok && make_map_u8(&m_wg, a.w_gate, gu_rows, a.d, BN / 2) &&
              make_map_u8(&m_wu, a.w_up, gu_rows, a.d, BN / 2) &&
-             make_map_u8(&m_wd, a.w_down, d_rows, a.F, BN);
+             make_map_u8(&m_wd, a.w_down, d_rows, a.F, wd_box);
     } else {
         ok = ok && make_map(&m_wg, a.w_gate, gu_rows, a.d, BN / 2, act) &&
              make_map(&m_wu, a.w_up, gu_rows, a.d, BN / 2, act) &&
-             make_map(&m_wd, a.w_down, d_rows, a.F, BN, act);
+             make_map(&m_wd, a.w_down, d_rows, a.F, wd_box, act);
     }
     if (!ok) return cudaErrorInvalidValue;
-    if ((err = q8 ? set_smem_attrs<true>() : set_smem_attrs<false>()) != cudaSuccess) return err;
 
     // Q8_0 packed buffers: int8 plane, then the fp16 scale plane [cols/32, rows]
-    // at align256(rows * cols); maps with box {tile rows, 2 blocks}
-    auto scale_map = [](CUtensorMap *m, const void *packed, uint64_t r, uint64_t cols,
-                        uint32_t box_rows) {
+    // at align256(rows * cols); maps with box {128 rows, 2 blocks}
+    auto scale_map = [](CUtensorMap *m, const void *packed, uint64_t r, uint64_t cols) {
         auto enc = encode_fn();
         if (!enc) return false;
         const void *base = static_cast<const char *>(packed) + align_up((size_t)(r * cols), 256);
         cuuint64_t dims[2] = {r, cols / 32};
         cuuint64_t strides[1] = {r * 2};
-        cuuint32_t box[2] = {box_rows, 2};
+        cuuint32_t box[2] = {(cuuint32_t)(BN / 2), 2};
         cuuint32_t estr[2] = {1, 1};
         return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    CUtensorMap m_sg, m_su, m_sd;
-    if (q8 && !(scale_map(&m_sg, a.w_gate, gu_rows, a.d, BN / 2) &&
-                scale_map(&m_su, a.w_up, gu_rows, a.d, BN / 2) &&
-                scale_map(&m_sd, a.w_down, d_rows, a.F, BN)))
+    CUtensorMap m_sg = m_xp, m_su = m_xp, m_sd = m_xp;   // unused unless Q8_0
+    if (q8 && !(scale_map(&m_sg, a.w_gate, gu_rows, a.d) && scale_map(&m_su, a.w_up, gu_rows, a.d) &&
+                scale_map(&m_sd, a.w_down, d_rows, a.F)))
         return cudaErrorInvalidValue;
+
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k;
     p.h = static_cast<uint16_t *>(a.h); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
     p.out = a.out; p.status = a.status; p.h_fp16 = q8 ? 1 : 0;
-
-    // upper bound on tiles: every expert could own a ragged tile
-    const long long max_mtiles = rows / BM + (a.E < rows ? a.E : rows);
-    auto grid_for = [&](long long tiles) { return (int)(tiles < a.num_sms ? (tiles < 1 ? 1 : tiles) : a.num_sms); };
-
-    p.K = a.d; p.n_tiles = a.F / (BN / 2);
-    if (q8) {
-        launch_pdl(grouped_gemm_kernel<GATEUP, true>, dim3(grid_for(max_mtiles * p.n_tiles)),
-                   dim3(Cfg<true>::THREADS), smem_bytes<true>(), stream, m_xp, m_wg, m_wu, m_sg,
-                   m_su, p);
-    } else {
-        launch_pdl(grouped_gemm_kernel<GATEUP, false>, dim3(grid_for(max_mtiles * p.n_tiles)),
-                   dim3(Cfg<false>::THREADS), smem_bytes<false>(), stream, m_xp, m_wg, m_wu, m_xp,
-                   m_xp, p);
-    }
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
-
-    p.K = a.F; p.n_tiles = a.d / BN;
-    if (q8) {
-        launch_pdl(grouped_gemm_kernel<DOWN, true>, dim3(grid_for(max_mtiles * p.n_tiles)),
-                   dim3(Cfg<true>::THREADS), smem_bytes<true>(), stream, m_h, m_wd, m_wd, m_sd,
-                   m_sd, p);
-    } else {
-        launch_pdl(grouped_gemm_kernel<DOWN, false>, dim3(grid_for(max_mtiles * p.n_tiles)),
-                   dim3(Cfg<false>::THREADS), smem_bytes<false>(), stream, m_h, m_wd, m_wd, m_h,
-                   m_h, p);
-    }
-    return cudaGetLastError();
+    p.out_zero = a.zero_out ? a.out : nullptr;
+    p.zero4 = (long long)a.T * a.d / 4;
+    if (q8)
+        return pair ? launch_pair<true, kCluster>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                    : launch_pair<true, 1>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+    return pair ? launch_pair<false, kCluster>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                : launch_pair<false, 1>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
 }
 
 }  // namespace moe

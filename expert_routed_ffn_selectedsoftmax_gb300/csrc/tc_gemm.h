@@ -20,7 +20,8 @@ struct TcArgs {
     void *xp;                   // [T*k, d] 16-bit scratch (grouped rows)
     int xp_ready;               // xp already holds the grouped rows
     void *h;                    // [T*k, F] 16-bit scratch
-    float *out;                 // [T, d] fp32 (zeroed beforehand when k > 1)
+    float *out;                 // [T, d] fp32
+    int zero_out;               // zero `out` in the gate/up kernel (the down kernel adds into it)
     uint32_t *status;           // device status word
     int num_sms;
     cudaEvent_t ev_gathered;    // optional: recorded after the row gather

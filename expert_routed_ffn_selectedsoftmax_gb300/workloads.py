@@ -77,14 +77,16 @@ WORKLOADS = {
                     "bf16, T in {1, 8, 64}, 28-layer weight rotation"),
     "zonos3_mini_prefill": Workload(
         "zonos3_mini_prefill", T=8192, d=1024, E=64, k=2, F=512, act_dtype=BF16,
-        w_dtype=BF16, bias="zipf", bias_sd=0.0, layers=1,
+        w_dtype=BF16, bias="zipf", bias_sd=0.0, layers=4,
         description="ZONOS3-Mini-shaped prefill: T=8192, d=1024, E=64, top-2, "
-                    "F=512, bf16, Zipf(1.1)-skewed expert loads"),
+                    "F=512, bf16, Zipf(1.1)-skewed expert loads (4 independent "
+                    "layers per benchmark step so weights come from HBM)"),
     "zonos2_prefill_q8": Workload(
         "zonos2_prefill_q8", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
-        w_dtype=Q8_0, bias="normal", bias_sd=0.1, layers=1,
+        w_dtype=Q8_0, bias="normal", bias_sd=0.1, layers=4,
         description="ZONOS2-shaped prefill with Q8_0 experts: T=4096, d=2048, "
-                    "E=16, top-1, F=2816, bf16 activations and router"),
+                    "E=16, top-1, F=2816, bf16 activations and router (4 "
+                    "independent layers per benchmark step)"),
 }
 
 
@@ -218,27 +220,47 @@ def act_bytes(dtype: int) -> int:
 
 
 # ---------------------------------------------------------------- device draws
+def q8_0_quantize_torch(w):
+    """Device twin of q8_0_quantize for benchmark weights: float32 [..., K] ->
+    uint8 blocks [..., K/32, 34] (same block layout and rounding rule)."""
+    import torch
+    K = w.shape[-1]
+    b = w.reshape(*w.shape[:-1], K // Q8_0_BLOCK, Q8_0_BLOCK).float()
+    amax = b.abs().amax(-1)
+    scale = amax / 127.0
+    inv = torch.where(scale > 0, 1.0 / torch.where(scale > 0, scale, torch.ones_like(scale)),
+                      torch.zeros_like(scale))
+    v = b * inv[..., None]
+    q = (torch.sign(v) * torch.floor(v.abs() + 0.5)).clamp(-127, 127).to(torch.int8)
+    out = torch.empty(*b.shape[:-1], Q8_0_BLOCK_BYTES, dtype=torch.uint8, device=w.device)
+    out[..., 0:2] = scale.to(torch.float16).contiguous().view(torch.uint8).reshape(*scale.shape, 2)
+    out[..., 2:] = q.view(torch.uint8)
+    return out
+
+
 def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = None,
                       device="cuda"):
-    """Draw ``layers`` independent bf16 layers directly in device memory.
+    """Draw ``layers`` independent layers directly in device memory.
 
     Used for benchmark stacks whose weights (GBs) are too large to draw on the
     host.  Same distributions as make_layer, drawn with torch's seeded device
-    generator; returns a list of dicts of torch tensors (bf16 stored as
-    torch.bfloat16).  Only bf16 workloads are supported here.
+    generator; returns a list of dicts of torch tensors: x / W_r as
+    torch.bfloat16, expert weights as torch.bfloat16 or, for Q8_0 workloads,
+    uint8 Q8_0 blocks [E, rows, cols/32, 34].
     """
     import torch
-    if w.w_dtype != BF16 or w.act_dtype != BF16:
-        raise ValueError("device stacks are bf16 only")
+    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (F32, F32)):
+        raise ValueError("device stacks: bf16/bf16, bf16/Q8_0 or fp32/fp32 layers")
+    act = torch.float32 if w.act_dtype == F32 else torch.bfloat16
     T = w.T if T is None else T
     g = torch.Generator(device=device)
     out = []
     for layer in range(layers):
         g.manual_seed(seed * 1000003 + layer)
 
-        def rn(*shape, sd=1.0):
-            t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
-            return (t * sd).to(torch.bfloat16)
+        def rn(*shape, sd=1.0, q8=False):
+            t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * sd
+            return q8_0_quantize_torch(t) if q8 else t.to(act)
         d, E, F = w.d, w.E, w.F
         x = rn(T, d)
         wr = rn(E, d, sd=1.0 / math.sqrt(d))
@@ -247,8 +269,9 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             b = torch.from_numpy(zipf_bias(E, rng)).to(device)
         else:
             b = torch.randn(E, generator=g, device=device, dtype=torch.float32) * w.bias_sd
-        wg = rn(E, F, d, sd=1.0 / math.sqrt(d))
-        wu = rn(E, F, d, sd=1.0 / math.sqrt(d))
-        wd = rn(E, d, F, sd=1.0 / math.sqrt(F))
+        q8 = w.w_dtype == Q8_0
+        wg = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
+        wu = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
+        wd = rn(E, d, F, sd=1.0 / math.sqrt(F), q8=q8)
         out.append(dict(x=x, w_router=wr, bias=b, w_gate=wg, w_up=wu, w_down=wd))
     return out
