@@ -254,7 +254,10 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     ra.tile_cnt = reinterpret_cast<int32_t *>(ws + L.tile_cnt);
     ra.counts = counts; ra.offsets = offsets; ra.perm_tok = perm_tok; ra.inv = inv; ra.perm_w = perm_w;
     const bool act16 = act_dt == MOE_BF16;
-    ra.xp = ((use_prefill || use_dtc) && act16) ? ws + L.xp : nullptr;
+    // decode batches of up to 128 tokens: one clustered kernel routes and
+    // groups (no scatter) and the expert kernel gathers x rows itself (no xp)
+    const bool fused_small = use_dtc && route_small_capable(act_dt, T, d, E, k);
+    ra.xp = ((use_prefill || use_dtc) && act16 && !fused_small) ? ws + L.xp : nullptr;
     ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     ra.zero_words = nullptr;
@@ -263,7 +266,10 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     ra.ev_routed = ev[1];
     const bool xp_ready = ra.xp != nullptr;
     cudaError_t e;
-    if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
+    if (fused_small) {
+        e = launch_route_small(ra, s);
+        if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+    } else if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
         e = launch_route_tc(ra, s);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
     } else {
@@ -293,9 +299,13 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
         a.pgu = reinterpret_cast<float *>(ws + L.pgu); a.pd = reinterpret_cast<float *>(ws + L.pd);
         a.h = reinterpret_cast<uint16_t *>(ws + L.h);
         a.out = out; a.status = status; a.num_sms = num_sms; a.ev_gateup = ev[4];
-        if (!xp_ready &&
-            launch_gather_rows(x, d, perm_tok, T * k, ws + L.xp, 0, num_sms, s) != cudaSuccess)
+        if (fused_small) {
+            a.x_gather = x;
+            a.perm_tok = perm_tok;
+        } else if (!xp_ready &&
+                   launch_gather_rows(x, d, perm_tok, T * k, ws + L.xp, 0, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;
+        }
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
         e = launch_decode_tc(a, s);
     } else {

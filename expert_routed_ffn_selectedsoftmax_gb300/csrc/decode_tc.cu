@@ -61,6 +61,7 @@ constexpr int B_BYTES = NTMAX * BK * 2;         // 4 KB token tile (16 or 32 row
 constexpr int SLOT = A_BYTES + B_BYTES;         // 20 KB per stage, 1024-aligned
 constexpr int KBMAX = 8;                        // k-blocks per item
 constexpr int THREADS = 192;
+constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
 constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
 constexpr int TMEM_COLS = 128;
 constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~4 items per SM on 152 SMs
@@ -73,6 +74,9 @@ struct Params {
     int K, R, n_mats, KS, kb_total, rows_total, rtiles;
     float *P;            // partial outputs [KS][n_mats][rows_total][R]
     uint32_t *status;
+    // GATHER: the token rows come from x[perm_tok[row]] (no grouped copy)
+    const uint16_t *xg;  // [T, K] bf16
+    const int32_t *perm_tok;
 };
 
 struct Ctl {
@@ -120,24 +124,30 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)
 
 // tm_w0/tm_w1: weight matrices (box 64 x 128 rows); tm_b16/tm_b32: the token
 // rows (grouped x for GATEUP, h for DOWN) with boxes of 16 and 32 rows.
-template <int MODE>
-__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
+// GATHER: the token rows are not loaded by TMA but gathered from x through
+// perm_tok by warps 6-9 (stage s by warp 6 + s % 4, lane = token row), written
+// into the 128-byte-swizzled layout the MMA expects.
+template <int MODE, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, CTAS_PER_SM)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
                  const Params p)
 {
-    pdl_enter();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Ctl &c = *reinterpret_cast<Ctl *>(smem + STAGES * SLOT);
 
-    if (upstream_failed(p.status)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
 
+    // set-up that reads nothing the preceding kernels write (barriers, TMEM,
+    // tensor-map prefetch) overlaps their tail under programmatic dependent launch
+    constexpr int NTHREADS = GATHER ? THREADS_GATHER : THREADS;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
+        // GATHER: a stage is full after the weight tile's bytes and the 32
+        // arrivals of the warp that wrote its token rows
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], GATHER ? 33 : 1); mbar_init(&c.empty[s], 1); }
         for (int b = 0; b < NACC; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
         mbar_init(&c.drain, 1);
         c.abort_flag = 0;
@@ -147,10 +157,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
         if (MODE == GATEUP)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w1)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b16)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b32)) : "memory");
+        if (!GATHER) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b16)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b32)) : "memory");
+        }
     }
-    for (int e = threadIdx.x; e <= E; e += THREADS) c.off[e] = p.offsets[e];
+    if (warp == 1) tmem_alloc(&c.tmem_base, TMEM_COLS);
+    tc_fence_before();
+    pdl_enter();
+    if (upstream_failed(p.status)) {   // (synchronises the CTA)
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(c.tmem_base, TMEM_COLS);
+        }
+        return;
+    }
+    for (int e = threadIdx.x; e <= E; e += NTHREADS) c.off[e] = p.offsets[e];
     __syncthreads();
     if (threadIdx.x < 32) {
         const int units = p.n_mats * p.rtiles * p.KS;
@@ -178,7 +200,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         }
         if (lane == 31) { c.n_items = incl; c.unit_start[E] = incl; }
     }
-    if (warp == 1) tmem_alloc(&c.tmem_base, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -195,7 +216,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             const Item it = decode_item(c, p, item);
             const CUtensorMap *wmap = (MODE == GATEUP && it.m == 1) ? &tm_w1 : &tm_w0;
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
-            const uint32_t bytes = A_BYTES + it.nt * BK * 2;
+            const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
@@ -204,7 +225,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 mbar_expect_tx(&c.full[s], bytes);
                 const int kx = (it.kb0 + kbl) * BK;
                 tma_load_2d(smem + s * SLOT, wmap, &c.full[s], kx, wrow);
-                tma_load_2d(smem + s * SLOT + A_BYTES, bmap, &c.full[s], kx, it.row0);
+                if (!GATHER) tma_load_2d(smem + s * SLOT + A_BYTES, bmap, &c.full[s], kx, it.row0);
             }
         }
         if (!ok) {
@@ -249,7 +270,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             volatile int no_abort = 0;
             mbar_wait(&c.drain, 0, &no_abort);
         }
-    } else if (warp >= 2) {
+    } else if (GATHER && warp >= 6) {
+        // ------------------------------------------------ token-row gatherers (4 warps)
+        // warp 6 + w fills the ring stages s with s % 4 == w;
+        // lane j copies the 128-byte K slice of the item's j-th token row,
+        // zeros for the padding rows of a 16/32-row tile
+        const int sw = warp - 6;
+        uint32_t it_k = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item it = decode_item(c, p, item);
+            const bool has = lane < it.nrows;
+            const uint16_t *src = p.xg + (size_t)(has ? p.perm_tok[it.row0 + lane] : 0) * p.K;
+            for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
+                const int s = it_k % STAGES;
+                if ((s & 3) != sw) continue;
+                const uint32_t ph = (it_k / STAGES) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&c.empty[s], ph ^ 1u, abort_flag))) { ok = false; break; }
+                if (lane < it.nt) {
+                    const int kx = (it.kb0 + kbl) * BK;
+                    uint4 v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        v[q] = has ? __ldg(reinterpret_cast<const uint4 *>(src + kx) + q) : make_uint4(0u, 0u, 0u, 0u);
+                    uint8_t *dst = smem + s * SLOT + A_BYTES + lane * 128;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4 *>(dst + ((q ^ (lane & 7)) << 4)) = v[q];
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&c.full[s]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            c.abort_flag = 1;
+        }
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------ epilogue (4 warps)
         const int quarter = warp & 3;
         uint32_t li = 0;
@@ -375,24 +432,33 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
 
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const bool gather = a.x_gather != nullptr;   // token rows gathered from x in-kernel
     CUtensorMap m_wg, m_wu, m_wd, m_x16, m_x32, m_h16, m_h32;
     if (!tc::make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BM, bf) ||
         !tc::make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BM, bf) ||
         !tc::make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BM, bf) ||
-        !tc::make_map(&m_x16, a.xp, (uint64_t)rows, a.d, 16, bf) ||
-        !tc::make_map(&m_x32, a.xp, (uint64_t)rows, a.d, 32, bf) ||
         !tc::make_map(&m_h16, a.h, (uint64_t)rows, a.F, 16, bf) ||
         !tc::make_map(&m_h32, a.h, (uint64_t)rows, a.F, 32, bf))
         return cudaErrorInvalidValue;
+    if (gather) {
+        m_x16 = m_wg;   // unused by the gathering kernel
+        m_x32 = m_wg;
+    } else if (!tc::make_map(&m_x16, a.xp, (uint64_t)rows, a.d, 16, bf) ||
+               !tc::make_map(&m_x32, a.xp, (uint64_t)rows, a.d, 32, bf)) {
+        return cudaErrorInvalidValue;
+    }
 
     cudaError_t err;
     const size_t smem = smem_bytes();
     static std::atomic<int> attr_done{0};
     if (!attr_done.load()) {
-        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP>,
+        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
                 cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN>,
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
                 cudaSuccess)
             return err;
@@ -413,8 +479,16 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     // gate/up: matrices W_g, W_u ([E*F, d]), K = d, token rows = grouped x
     p.K = a.d; p.R = a.F; p.n_mats = 2; p.KS = ks_gu; p.kb_total = a.d / BK; p.rtiles = a.F / BM;
     p.P = a.pgu;
-    launch_pdl(decode_tc_kernel<GATEUP>, dim3(grid_for(chunks * 2 * p.rtiles * ks_gu)), dim3(THREADS), smem, stream, 
-        m_wg, m_wu, m_x16, m_x32, p);
+    const dim3 g_gu(grid_for(chunks * 2 * p.rtiles * ks_gu));
+    if (gather) {
+        p.xg = static_cast<const uint16_t *>(a.x_gather);
+        p.perm_tok = a.perm_tok;
+        launch_pdl(decode_tc_kernel<GATEUP, true>, g_gu, dim3(THREADS_GATHER), smem, stream, m_wg, m_wu,
+                   m_x16, m_x32, p);
+    } else {
+        launch_pdl(decode_tc_kernel<GATEUP, false>, g_gu, dim3(THREADS), smem, stream, m_wg, m_wu, m_x16,
+                   m_x32, p);
+    }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     auto elementwise_grid = [&](long long total) {
         long long blocks = (total + 255) / 256;
@@ -429,7 +503,9 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     // down: matrix W_d ([E*d, F]), K = F, token rows = h
     p.K = a.F; p.R = a.d; p.n_mats = 1; p.KS = ks_d; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
     p.P = a.pd;
-    launch_pdl(decode_tc_kernel<DOWN>, dim3(grid_for(chunks * p.rtiles * ks_d)), dim3(THREADS), smem, stream, 
+    p.xg = nullptr;
+    p.perm_tok = nullptr;
+    launch_pdl(decode_tc_kernel<DOWN, false>, dim3(grid_for(chunks * p.rtiles * ks_d)), dim3(THREADS), smem, stream, 
         m_wd, m_wd, m_h16, m_h32, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 

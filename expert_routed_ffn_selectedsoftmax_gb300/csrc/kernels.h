@@ -49,6 +49,12 @@ cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream);
 // grouping scatter over token tiles of `tile_tokens` (counts/ranks from either router)
 cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cudaStream_t stream);
 
+// route_small.cu -- routing and grouping in one clustered kernel for T <= 128
+// (bf16 activations): writes topk_idx/topk_w and counts, offsets, perm_tok,
+// inv, perm_w; ignores rank, tile_cnt, xp, out_zero and zero_words.
+bool route_small_capable(int act_dt, int T, int d, int E, int k);
+cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream);
+
 // permute.cu
 cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
                            int32_t *offsets, int32_t *perm_tok, int32_t *inv,
@@ -77,7 +83,9 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream);
 // decode_tc.cu -- expert FFN for few rows per expert on tcgen05 (bf16 only)
 struct DecodeTcArgs {
     const void *x;              // [T, d] bf16
-    const void *xp;             // [T*k, d] bf16 grouped rows of x
+    const void *xp;             // [T*k, d] bf16 grouped rows of x (unused when gathering)
+    const void *x_gather;       // non-null: gather token rows from this [T, d] via perm_tok
+    const int32_t *perm_tok;    // [T*k] grouped row -> token
     int T, d, E, k, F;
     const void *w_gate, *w_up, *w_down;   // bf16
     const int32_t *offsets;     // [E+1]

@@ -72,6 +72,29 @@ struct Ctl {
     uint32_t mask[kMaxExperts][4];   // tokens of this tile that chose expert e
 };
 
+// Sorted top-K insertion of (score cs, logit cl, expert ce) into slots
+// (bs, bl, be), ordered by score descending then expert ascending.  Experts
+// arrive in ascending order, so a newcomer never precedes an equal score;
+// unfilled slots (be == kNone) take anything.  Every slot's update reads only
+// the old slots, so the K updates of one expert are independent.
+constexpr int kNone = 0x7fffffff;
+template <int K>
+__device__ __forceinline__ void topk_insert(float (&bs)[K], float (&bl)[K], int (&be)[K], float cs,
+                                            float cl, int ce)
+{
+    bool gt[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) gt[j] = cs > bs[j] || be[j] == kNone;
+#pragma unroll
+    for (int j = K - 1; j > 0; --j) {
+        const bool from_prev = gt[j - 1], take = gt[j];
+        bs[j] = from_prev ? bs[j - 1] : (take ? cs : bs[j]);
+        bl[j] = from_prev ? bl[j - 1] : (take ? cl : bl[j]);
+        be[j] = from_prev ? be[j - 1] : (take ? ce : be[j]);
+    }
+    if (gt[0]) { bs[0] = cs; bl[0] = cl; be[0] = ce; }
+}
+
 // KMAX: compile-time bound on k (1, 2, 4 or 8) so the top-k insertion is as
 // short as the k it serves.
 template <int KMAX>
@@ -182,49 +205,42 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             float bs[KMAX], bl[KMAX];
             int be[KMAX];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) { bs[j] = -INFINITY; bl[j] = 0.f; be[j] = 0x7fffffff; }
+            for (int j = 0; j < KMAX; ++j) { bs[j] = -INFINITY; bl[j] = 0.f; be[j] = kNone; }
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 0; ok && c0 < EP; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(taddr + c0, v);
+            for (int c0 = 0; ok && c0 < EP; c0 += 32) {
+                uint32_t v[2][16];
+                tmem_ld16(taddr + c0, v[0]);
+                if (c0 + 16 < EP) tmem_ld16(taddr + c0 + 16, v[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
+                for (int q = 0; q < 32; ++q) {
                     const int e = c0 + q;
                     if (e < E) {
-                        float cl = __uint_as_float(v[q]);
+                        const float cl = __uint_as_float(v[q >> 4][q & 15]);
                         float cs = cl + c.bias[e];
                         if (isnan(cs)) cs = -INFINITY;   // keep the ranking a total order
-                        int ce = e;
-                        // insertion into the sorted top-k (score desc, index asc)
-#pragma unroll
-                        for (int j = 0; j < KMAX; ++j) {
-                            if (j < p.k && (cs > bs[j] || (cs == bs[j] && ce < be[j]))) {
-                                const float ts = bs[j], tl = bl[j];
-                                const int te = be[j];
-                                bs[j] = cs; bl[j] = cl; be[j] = ce;
-                                cs = ts; cl = tl; ce = te;
-                            }
-                        }
+                        topk_insert<KMAX>(bs, bl, be, cs, cl, e);
                     }
                 }
             }
+            float wsel[KMAX];
             if (ok && valid) {
                 float m = bl[0];
 #pragma unroll
                 for (int j = 1; j < KMAX; ++j) if (j < p.k) m = fmaxf(m, bl[j]);
-                float pr[KMAX], den = 0.f;
+                float den = 0.f;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
-                    pr[j] = j < p.k ? expf(bl[j] - m) : 0.f;
-                    den += pr[j];
+                    wsel[j] = j < p.k ? expf(bl[j] - m) : 0.f;
+                    den += wsel[j];
                 }
                 const size_t base = (size_t)t * p.k;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
                     if (j < p.k) {
+                        wsel[j] = wsel[j] / den;
                         p.topk_idx[base + j] = be[j];
-                        p.topk_w[base + j] = pr[j] / den;
+                        p.topk_w[base + j] = wsel[j];
                         if (p.rank) atomicOr(&c.mask[be[j]][r >> 5], 1u << (r & 31));
                     }
                 }
