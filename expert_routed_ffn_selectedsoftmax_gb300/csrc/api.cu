@@ -243,8 +243,9 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
     const bool use_dtc = !use_prefill && path != MOE_PATH_DECODE_SIMT && L.dtc &&
                          decode_tc_capable(act_dt, w_dt, d, F, E);
-    // the combine steps that accumulate into `out` need it zeroed first
-    const bool zero_out = k > 1 && !use_dtc;
+    // the expert kernels that accumulate into `out` need it zeroed first (the
+    // tensor-core decode path adds into it only when its down kernel does)
+    const bool zero_out = k > 1 && (!use_dtc || decode_tc_down_direct(T, d, E, k, F));
     // routing, then the grouping scatter (which also writes the grouped x rows
     // that the tensor-core expert kernels read)
     RouteTcArgs ra{};
@@ -299,9 +300,10 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
         a.pgu = reinterpret_cast<float *>(ws + L.pgu); a.pd = reinterpret_cast<float *>(ws + L.pd);
         a.h = reinterpret_cast<uint16_t *>(ws + L.h);
         a.out = out; a.status = status; a.num_sms = num_sms; a.ev_gateup = ev[4];
+        a.perm_tok = perm_tok;
+        a.perm_w = perm_w;
         if (fused_small) {
             a.x_gather = x;
-            a.perm_tok = perm_tok;
         } else if (!xp_ready &&
                    launch_gather_rows(x, d, perm_tok, T * k, ws + L.xp, 0, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;

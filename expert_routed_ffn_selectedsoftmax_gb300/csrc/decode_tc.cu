@@ -12,15 +12,25 @@
 // operand, and fp32 accumulators live in TMEM.  This keeps the instruction
 // count per weight byte near zero, which the CUDA-core version could not.
 //
-// Work item = (expert, chunk of <= 32 token rows, weight matrix, 128-row
-// tile, K split).  K is split so that every SM streams several items; partial
-// sums go to fp32 scratch and are always reduced in split order, so results
-// are bitwise reproducible.
-//   GATEUP: matrices W_g, W_u; B operand = grouped x rows; partials
-//           Pgu[s][m][row][f].
-//   swiglu: h = SiLU(sum_s G) * sum_s U as bf16 [rows, F] (elementwise).
-//   DOWN:   matrix W_d; B operand = h rows; partials Pd[s][row][o].
-//   combine: out[t] = sum_j w[t,j] * sum_s Pd[s][inv[t,j]]  (fp32).
+// Two schedules, chosen per kernel by how many work units the batch has:
+//  * whole K (enough units to keep every SM streaming in one wave): GATEUP
+//    item = (expert, chunk of <= 32 token rows, 128-row tile of F), its ring
+//    stages alternating between the gate and the up tile of the same rows
+//    into two accumulators; the epilogue writes h = SiLU(G) * U (bf16)
+//    directly.  DOWN item = (expert, chunk, 128-row tile of d); the epilogue
+//    adds w * y into out[token] (a plain store when k = 1; with k = 2 each
+//    element receives exactly two additions onto zero, whose fp32 result does
+//    not depend on their order).
+//  * split K (small batches, or k > 2): K is split so that every SM streams
+//    several items; partial sums go to fp32 scratch and are reduced in split
+//    order, so results are bitwise reproducible.
+//      GATEUP item = (expert, chunk, matrix, 128-row tile, K split) -> partials
+//      Pgu[s][m][row][f]; swiglu: h = SiLU(sum_s G) * sum_s U (bf16);
+//      DOWN item -> partials Pd[s][row][o]; combine: out[t] =
+//      sum_j w[t,j] * sum_s Pd[s][inv[t,j]] (fp32).
+// (An equal split of every layer's k-blocks across CTAs with a fix-up of the
+// items cut at range boundaries measured slower on these shapes: the
+// fix-ups land at the end of every CTA's range.)
 // Both operands of every ring stage arrive by TMA, so the MMA thread only
 // waits for data and the epilogue only reads TMEM and stores partials.
 //
@@ -77,6 +87,12 @@ struct Params {
     // GATHER: the token rows come from x[perm_tok[row]] (no grouped copy)
     const uint16_t *xg;  // [T, K] bf16
     const int32_t *perm_tok;
+    int fused;           // GATEUP: gate + up tiles per item, h written directly
+    uint16_t *h;         //   h [rows_total, R] bf16
+    int direct;          // DOWN: w * y added into out directly
+    float *out;          //   out [T, R] fp32 (zeroed beforehand when k > 1)
+    const float *perm_w;
+    int k;
 };
 
 struct Ctl {
@@ -117,10 +133,20 @@ __device__ __forceinline__ Item decode_item(const Ctl &c, const Params &p, int i
     it.nt = it.nrows <= 16 ? 16 : 32;
     it.kb0 = it.s * p.kb_total / p.KS;
     it.nkb = (it.s + 1) * p.kb_total / p.KS - it.kb0;
+    if (p.fused) { it.kb0 = 0; it.nkb = 2 * p.kb_total; }   // stages alternate gate / up
     return it;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// Weight matrix and k-block of stage `kbl` of an item.
+__device__ __forceinline__ void stage_of(const Params &p, const Item &it, int kbl, int &m, int &kb)
+{
+    if (p.fused) { m = kbl & 1; kb = kbl >> 1; }
+    else { m = it.m; kb = it.kb0 + kbl; }
+}
+
+// SiLU(z) = z * sigmoid(z) with the fast exponential and an approximate
+// divide (relative error ~1e-6, below the bf16 rounding of h that follows).
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // tm_w0/tm_w1: weight matrices (box 64 x 128 rows); tm_b16/tm_b32: the token
 // rows (grouped x for GATEUP, h for DOWN) with boxes of 16 and 32 rows.
@@ -214,7 +240,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item(c, p, item);
-            const CUtensorMap *wmap = (MODE == GATEUP && it.m == 1) ? &tm_w1 : &tm_w0;
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
             const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
@@ -223,7 +248,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 const uint32_t ph = (it_k / STAGES) & 1u;
                 if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
                 mbar_expect_tx(&c.full[s], bytes);
-                const int kx = (it.kb0 + kbl) * BK;
+                int m, kb;
+                stage_of(p, it, kbl, m, kb);
+                const CUtensorMap *wmap = (MODE == GATEUP && m == 1) ? &tm_w1 : &tm_w0;
+                const int kx = kb * BK;
                 tma_load_2d(smem + s * SLOT, wmap, &c.full[s], kx, wrow);
                 if (!GATHER) tma_load_2d(smem + s * SLOT + A_BYTES, bmap, &c.full[s], kx, it.row0);
             }
@@ -242,22 +270,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++li) {
             const Item it = decode_item(c, p, item);
-            const uint32_t acc = li % NACC, aph = (li / NACC) & 1u;
+            // accumulator slots: NACC of 32 columns, or (fused) NACC/2 pairs of
+            // (gate, up) accumulators
+            const uint32_t nslot = p.fused ? NACC / 2 : NACC;
+            const uint32_t acc = li % nslot, aph = (li / nslot) & 1u;
             if (!mbar_wait(&c.tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + acc * 32;
             const uint32_t idesc = idesc_f16_mn(0, BM, it.nt);
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
                 const uint32_t ph = (it_k / STAGES) & 1u;
                 if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                int m, kb;
+                stage_of(p, it, kbl, m, kb);
+                const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
                 const uint32_t a0 = smem_u32(smem + s * SLOT);
                 const uint32_t b0 = a0 + A_BYTES;
+                const int first = p.fused ? kb : kbl;   // first k-block of this accumulator
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                             (kbl | kk) != 0);
+                             (first | kk) != 0);
                 umma_commit(&c.empty[s]);
             }
             if (!ok) break;
@@ -288,7 +322,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 const uint32_t ph = (it_k / STAGES) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&c.empty[s], ph ^ 1u, abort_flag))) { ok = false; break; }
                 if (lane < it.nt) {
-                    const int kx = (it.kb0 + kbl) * BK;
+                    int m, kb;
+                    stage_of(p, it, kbl, m, kb);
+                    const int kx = kb * BK;
                     uint4 v[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
@@ -313,10 +349,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         bool ok = true;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++li) {
             const Item it = decode_item(c, p, item);
-            const uint32_t acc = li % NACC, aph = (li / NACC) & 1u;
+            const uint32_t nslot = p.fused ? NACC / 2 : NACC;
+            const uint32_t acc = li % nslot, aph = (li / nslot) & 1u;
             // warp-uniform outcome: tcgen05.ld below is warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait(&c.tfull[acc], aph, abort_flag))) { ok = false; break; }
             tc_fence_after();
+            const int wr = it.rt * BM + quarter * 32 + lane;   // weight row = output column
+            if (MODE == GATEUP && p.fused) {
+                // lane = f; column j = token row j of the chunk; two halves of
+                // 16 token columns (the second only for 32-row chunks)
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 64;
+                uint16_t *dst = p.h + (size_t)it.row0 * p.R + wr;
+                for (int half = 0; half < it.nt / 16; ++half) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(taddr + half * 16, g);
+                    tmem_ld16(taddr + 32 + half * 16, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int j = half * 16 + q;
+                        if (j < it.nrows) {
+                            const float hv = silu_f(__uint_as_float(g[q])) * __uint_as_float(u[q]);
+                            dst[(size_t)j * p.R] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&c.tempty[acc]);      // accumulators are read
+                continue;
+            }
             uint32_t v[32];
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 32;
             tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
@@ -324,7 +385,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&c.tempty[acc]);          // accumulator is in registers now
-            const int wr = it.rt * BM + quarter * 32 + lane;   // weight row = output column
+            if (MODE == DOWN && p.direct) {
+                // token and routing weight of row j, held by lane j
+                const int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
+                const float w_l = lane < it.nrows ? p.perm_w[it.row0 + lane] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int tok = __shfl_sync(0xffffffffu, tok_l, j);
+                    const float w = __shfl_sync(0xffffffffu, w_l, j);
+                    if (j < it.nrows) {
+                        float *o = p.out + (size_t)tok * p.R + wr;
+                        if (p.k == 1) *o = w * __uint_as_float(v[j]);
+                        else atomicAdd(o, w * __uint_as_float(v[j]));
+                    }
+                }
+                continue;
+            }
             float *dst = p.P + ((size_t)(it.s * p.n_mats + it.m) * p.rows_total + it.row0) * p.R + wr;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -424,6 +500,26 @@ void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d)
     *ks_d = dtc::choose_splits(F / dtc::BK, n_exp * (d / dtc::BM));
 }
 
+// Whole-K items stream at a few tens of GB/s per CTA: about 200 of them keep
+// HBM busy.  Gate/up items (both matrices, the whole of d) are large, so they
+// are used only when they also fit in one wave of the CTAs.
+constexpr long long kWholeKMinUnits = 192;
+
+bool decode_tc_gateup_fused(int T, int d, int E, int k, int F, int num_sms)
+{
+    (void)d;
+    const long long n_exp = (long long)(E < T * k ? E : T * k);
+    const long long units = n_exp * (F / dtc::BM);
+    return units >= kWholeKMinUnits && units <= (long long)num_sms * dtc::CTAS_PER_SM;
+}
+
+bool decode_tc_down_direct(int T, int d, int E, int k, int F)
+{
+    (void)F;
+    const long long n_exp = (long long)(E < T * k ? E : T * k);
+    return k <= 2 && n_exp * (d / dtc::BM) >= kWholeKMinUnits;
+}
+
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
 {
     using namespace dtc;
@@ -476,10 +572,17 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     // upper bound on items: chunks <= n_exp + rows / NTMAX
     const long long chunks = n_exp + rows / NTMAX;
 
+    const bool fused = decode_tc_gateup_fused(a.T, a.d, a.E, a.k, a.F, a.num_sms);
+    const bool direct = decode_tc_down_direct(a.T, a.d, a.E, a.k, a.F);
+
     // gate/up: matrices W_g, W_u ([E*F, d]), K = d, token rows = grouped x
-    p.K = a.d; p.R = a.F; p.n_mats = 2; p.KS = ks_gu; p.kb_total = a.d / BK; p.rtiles = a.F / BM;
-    p.P = a.pgu;
-    const dim3 g_gu(grid_for(chunks * 2 * p.rtiles * ks_gu));
+    p.K = a.d; p.R = a.F; p.kb_total = a.d / BK; p.rtiles = a.F / BM;
+    if (fused) {
+        p.n_mats = 1; p.KS = 1; p.fused = 1; p.h = a.h;   // an item covers both matrices
+    } else {
+        p.n_mats = 2; p.KS = ks_gu; p.P = a.pgu;
+    }
+    const dim3 g_gu(grid_for(chunks * p.n_mats * p.rtiles * p.KS));
     if (gather) {
         p.xg = static_cast<const uint16_t *>(a.x_gather);
         p.perm_tok = a.perm_tok;
@@ -495,21 +598,28 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
         if (blocks > (long long)a.num_sms * 8) blocks = (long long)a.num_sms * 8;
         return (int)(blocks < 1 ? 1 : blocks);
     };
-    launch_pdl(swiglu_reduce_kernel, dim3(elementwise_grid((long long)rows * (a.F / 4))), dim3(256), 0, stream, 
-        a.pgu, ks_gu, rows, a.F, a.h, a.status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (!fused) {
+        launch_pdl(swiglu_reduce_kernel, dim3(elementwise_grid((long long)rows * (a.F / 4))), dim3(256), 0,
+                   stream, a.pgu, ks_gu, rows, a.F, a.h, a.status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     // down: matrix W_d ([E*d, F]), K = F, token rows = h
-    p.K = a.F; p.R = a.d; p.n_mats = 1; p.KS = ks_d; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
-    p.P = a.pd;
+    p.K = a.F; p.R = a.d; p.n_mats = 1; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
+    p.fused = 0; p.h = nullptr;
     p.xg = nullptr;
-    p.perm_tok = nullptr;
-    launch_pdl(decode_tc_kernel<DOWN, false>, dim3(grid_for(chunks * p.rtiles * ks_d)), dim3(THREADS), smem, stream, 
-        m_wd, m_wd, m_h16, m_h32, p);
+    if (direct) {
+        p.KS = 1; p.direct = 1; p.out = a.out; p.perm_tok = a.perm_tok; p.perm_w = a.perm_w; p.k = a.k;
+    } else {
+        p.KS = ks_d; p.P = a.pd; p.perm_tok = nullptr;
+    }
+    launch_pdl(decode_tc_kernel<DOWN, false>, dim3(grid_for(chunks * p.rtiles * p.KS)), dim3(THREADS), smem,
+               stream, m_wd, m_wd, m_h16, m_h32, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (direct) return cudaSuccess;
 
-    launch_pdl(combine_kernel, dim3(elementwise_grid((long long)a.T * (a.d / 4))), dim3(256), 0, stream, 
+    launch_pdl(combine_kernel, dim3(elementwise_grid((long long)a.T * (a.d / 4))), dim3(256), 0, stream,
         a.pd, ks_d, rows, a.d, a.inv, a.topk_w, a.T, a.k, a.out, a.status);
     return cudaGetLastError();
 }

@@ -51,7 +51,8 @@ cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cu
 
 // route_small.cu -- routing and grouping in one clustered kernel for T <= 128
 // (bf16 activations): writes topk_idx/topk_w and counts, offsets, perm_tok,
-// inv, perm_w; ignores rank, tile_cnt, xp, out_zero and zero_words.
+// inv, perm_w, and zeroes out_zero and zero_words when given; ignores rank,
+// tile_cnt and xp.
 bool route_small_capable(int act_dt, int T, int d, int E, int k);
 cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream);
 
@@ -91,10 +92,11 @@ struct DecodeTcArgs {
     const int32_t *offsets;     // [E+1]
     const int32_t *inv;         // [T*k]
     const float *topk_w;        // [T*k]
+    const float *perm_w;        // [T*k] routing weight of each grouped row
     float *pgu;                 // gate/up partials [ks_gu][2][T*k][F]
     uint16_t *h;                // bf16 h [T*k, F] scratch
     float *pd;                  // down partials [ks_d][T*k][d]
-    float *out;                 // [T, d] fp32 (fully written)
+    float *out;                 // [T, d] fp32 (zeroed beforehand when the down kernel adds into it)
     uint32_t *status;
     int num_sms;
     cudaEvent_t ev_gateup;
@@ -102,6 +104,10 @@ struct DecodeTcArgs {
 constexpr int kDecodeTcMaxRows = 8192;   // T*k above this uses the CUDA-core kernels
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E);
 void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d);
+// whole-K schedules: gate/up writes h itself; down adds into out (zeroed
+// beforehand when k > 1) -- no reduction or combine kernels
+bool decode_tc_gateup_fused(int T, int d, int E, int k, int F, int num_sms);
+bool decode_tc_down_direct(int T, int d, int E, int k, int F);
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream);
 
 // q8.cu

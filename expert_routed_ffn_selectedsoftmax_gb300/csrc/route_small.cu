@@ -67,6 +67,9 @@ struct Params {
     int32_t *counts, *offsets, *perm_tok, *inv;
     float *perm_w;
     uint32_t *status;
+    float *out_zero;                     // optional [T, d] output to zero (the down kernel adds into it)
+    uint32_t *zero_words;                // optional scratch words later kernels count on being zero
+    int n_zero;
 };
 
 struct Ctl {
@@ -189,6 +192,14 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     cluster_sync_all();                       // every CTA's mbarriers exist before anyone signals them
     pdl_enter();
     if (p.status && rank == 0 && threadIdx.x == 0) *p.status = kDevOk;
+    if (p.out_zero) {   // this CTA's share of the output rows
+        float4 *o4 = reinterpret_cast<float4 *>(p.out_zero);
+        const long long n4 = (long long)p.T * p.d / 4;
+        const long long per = (n4 + R - 1) / R, lo = (long long)rank * per;
+        const long long hi = lo + per < n4 ? lo + per : n4;
+        for (long long i = lo + threadIdx.x; i < hi; i += THREADS) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int i = (int)rank * THREADS + threadIdx.x; i < p.n_zero; i += R * THREADS) p.zero_words[i] = 0u;
     for (int e = threadIdx.x; e < kMaxExperts; e += THREADS) c.bias[e] = (e < E && p.bias) ? p.bias[e] : 0.f;
     __syncthreads();
     tc_fence_after();
@@ -455,7 +466,8 @@ cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream)
     p.box_rows = box_rows; p.tpc = (a.T + R - 1) / R;
     p.bias = a.bias; p.topk_idx = a.topk_idx; p.topk_w = a.topk_w;
     p.counts = a.counts; p.offsets = a.offsets; p.perm_tok = a.perm_tok; p.inv = a.inv;
-    p.perm_w = a.perm_w; p.status = a.status;
+    p.perm_w = a.perm_w; p.status = a.status; p.out_zero = a.out_zero;
+    p.zero_words = a.zero_words; p.n_zero = a.n_zero;
     auto kern = a.k == 1 ? route_small_kernel<1> : a.k == 2 ? route_small_kernel<2>
               : a.k <= 4 ? route_small_kernel<4> : route_small_kernel<8>;
     err = launch_pdl_cluster(kern, dim3(R), dim3(THREADS), smem, stream, R, m_x, m_w, p);
