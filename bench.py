@@ -160,13 +160,16 @@ def algorithmic(w, T, counts_per_layer):
     return total
 
 
-def expert_kernel_names(w, T):
+def expert_kernel_names(w, T, num_sms):
     """Which kernels moe_forward's AUTO path runs for this workload (mirrors
     the library's selection: grouped GEMMs from 64 rows per expert on average
     and T >= 512 for bf16 / Q8_0 weights with d % 256 == 0 and F % 128 == 0;
     tensor-core decode for bf16 layers with d, F multiples of 128 and
-    T*k <= 8192; otherwise the CUDA-core decode kernels), and how many of the
-    library's kernels one layer launches."""
+    T*k <= 8192 -- one clustered routing+grouping kernel for T <= 128, whole-K
+    gate/up items when ~200 of them fit in one wave of two CTAs per SM,
+    whole-K down items when k <= 2 and ~200 of them exist; otherwise the
+    CUDA-core decode kernels), and how many of the library's kernels one
+    layer launches."""
     rows = T * w.k
     act16 = w.act_dtype == 1
     if (act16 and w.w_dtype in (1, 2) and w.d % 256 == 0 and w.F % 128 == 0
@@ -175,8 +178,16 @@ def expert_kernel_names(w, T):
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4}
     if act16 and w.w_dtype == 1 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
-        return {"file": "decode_tc.cu", "gateup": "decode_tc_kernel<GATEUP> + swiglu_reduce_kernel",
-                "down": "decode_tc_kernel<DOWN> + combine_kernel", "launches": 6}
+        n_exp = min(w.E, rows)
+        small = T <= 128 and w.d // 64 <= 64 and w.k <= w.E
+        fused = 192 <= n_exp * (w.F // 128) <= 2 * num_sms
+        direct = w.k <= 2 and n_exp * (w.d // 128) >= 192
+        launches = (1 if small else 2) + (1 if fused else 2) + (1 if direct else 2)
+        gu = "decode_tc_kernel<GATEUP> (whole K, writes h)" if fused else \
+            "decode_tc_kernel<GATEUP> + swiglu_reduce_kernel"
+        dn = "decode_tc_kernel<DOWN> (whole K, adds into out)" if direct else \
+            "decode_tc_kernel<DOWN> + combine_kernel"
+        return {"file": "decode_tc.cu", "gateup": gu, "down": dn, "launches": launches}
     return {"file": "decode.cu", "gateup": "decode_gateup_kernel", "down": "decode_down_kernel",
             "launches": 4}
 
@@ -421,7 +432,7 @@ def main():
     peaks, peak_src = load_peaks()
     hbm = peak_value(peaks, "hbm_gbs")
     tflops_peak = peak_value(peaks, "bf16_tflops")   # fp16 dense rate equals bf16
-    names = expert_kernel_names(w, T)
+    names = expert_kernel_names(w, T, torch.cuda.get_device_properties(dev).multi_processor_count)
     dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
     dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
     dom_bytes = alg[f"{dominant}_bytes"] / layers
