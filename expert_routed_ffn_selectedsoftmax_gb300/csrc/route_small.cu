@@ -133,10 +133,13 @@ __device__ __forceinline__ void insert(float (&bs)[K], float (&bl)[K], int (&be)
 // partial logits: 128 x EP fp32][receive buffer: MAXR slots x TPC rows x EP
 // fp32][Ctl]
 __host__ __device__ inline size_t stage_offset(int kbpc, int EP) { return (size_t)kbpc * (A_TILE + b_tile_bytes(EP)); }
-__host__ __device__ inline size_t recv_offset(int kbpc, int EP) { return stage_offset(kbpc, EP) + (size_t)128 * EP * 4; }
+// staged and received rows are EP + 4 floats apart: rows land 4 banks apart,
+// so per-row 16-byte stores and per-expert reads of 8 rows do not conflict
+__host__ __device__ constexpr int row_stride(int EP) { return EP + 4; }
+__host__ __device__ inline size_t recv_offset(int kbpc, int EP) { return stage_offset(kbpc, EP) + (size_t)128 * row_stride(EP) * 4; }
 __host__ __device__ inline size_t ctl_offset(int kbpc, int EP)
 {
-    return recv_offset(kbpc, EP) + (size_t)MAXR * TPC * EP * 4;
+    return recv_offset(kbpc, EP) + (size_t)MAXR * TPC * row_stride(EP) * 4;
 }
 // token rows owned by CTA q
 __host__ __device__ inline int owned_rows(int q, int tpc, int T)
@@ -176,7 +179,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         mbar_init(&c.mx, 1);
         // the bytes the peers will send: R slots of this CTA's token rows, and
         // R mask rows
-        if (mine_rows > 0) mbar_expect_tx(&c.rx, (uint32_t)(R * mine_rows * EP * 4));
+        if (mine_rows > 0) mbar_expect_tx(&c.rx, (uint32_t)(R * mine_rows * row_stride(EP) * 4));
         mbar_expect_tx(&c.mx, (uint32_t)(R * EP * 4));
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -244,14 +247,18 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
             tc_fence_after();
             const int row = quarter * 32 + lane;   // token row
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 0; c0 < EP; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(taddr + c0, v);   // warp-collective
+            for (int c0 = 0; c0 < EP; c0 += 32) {  // two TMEM loads per wait
+                uint32_t v[2][16];
+                tmem_ld16(taddr + c0, v[0]);   // warp-collective
+                if (c0 + 16 < EP) tmem_ld16(taddr + c0 + 16, v[1]);
                 tmem_ld_wait();
                 if (row < p.T) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(stage + (size_t)row * EP + c0);
+                    uint4 *dst = reinterpret_cast<uint4 *>(stage + (size_t)row * row_stride(EP) + c0);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int q = 0; q < 8; ++q)
+                        if (c0 + 4 * q < EP)
+                            dst[q] = make_uint4(v[q >> 2][(4 * q) & 15], v[q >> 2][(4 * q + 1) & 15],
+                                                v[q >> 2][(4 * q + 2) & 15], v[q >> 2][(4 * q + 3) & 15]);
                 }
             }
             fence_proxy_async_smem();          // the bulk copies read these rows
@@ -260,15 +267,13 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     }
     __syncwarp();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // owner q receives its token rows of this CTA's partials in slot `rank`
-        for (int q = 0; q < R; ++q) {
-            const int n = owned_rows(q, p.tpc, p.T);
-            if (n > 0)
-                bulk_to_peer(peer_addr(recv + (size_t)rank * TPC * EP, (uint32_t)q),
-                             stage + (size_t)q * p.tpc * EP, (uint32_t)(n * EP * 4),
-                             peer_addr(&c.rx, (uint32_t)q));
-        }
+    if (threadIdx.x < R) {
+        // owner q = lane receives its token rows of this CTA's partials in slot `rank`
+        const int q = threadIdx.x, n = owned_rows(q, p.tpc, p.T);
+        if (n > 0)
+            bulk_to_peer(peer_addr(recv + (size_t)rank * TPC * row_stride(EP), (uint32_t)q),
+                         stage + (size_t)q * p.tpc * row_stride(EP), (uint32_t)(n * row_stride(EP) * 4),
+                         peer_addr(&c.rx, (uint32_t)q));
         bulk_commit();
     }
 
@@ -294,7 +299,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
                 float cl = 0.f;
 #pragma unroll
                 for (int q = 0; q < MAXR; ++q)
-                    if (q < R) cl += recv[((size_t)q * TPC + tok) * EP + e];
+                    if (q < R) cl += recv[((size_t)q * TPC + tok) * row_stride(EP) + e];
                 float cs = cl + c.bias[e];
                 if (isnan(cs)) cs = -INFINITY;        // keep the ranking a total order
                 insert<KMAX>(bs, bl, be, cs, cl, e);
@@ -341,11 +346,11 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     fence_proxy_async_smem();                 // the bulk copies read the masks
     __syncwarp();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // this CTA's masks into slot `rank` of every CTA's table
-        for (int q = 0; q < R; ++q)
-            bulk_to_peer(peer_addr(&c.all_mask[rank][0], (uint32_t)q), c.mask, (uint32_t)(EP * 4),
-                         peer_addr(&c.mx, (uint32_t)q));
+    if (threadIdx.x < R) {
+        // this CTA's masks into slot `rank` of CTA q = lane's table
+        const int q = threadIdx.x;
+        bulk_to_peer(peer_addr(&c.all_mask[rank][0], (uint32_t)q), c.mask, (uint32_t)(EP * 4),
+                     peer_addr(&c.mx, (uint32_t)q));
         bulk_commit();
     }
     if (!mbar_wait(&c.mx, 0, abort_flag)) {
@@ -406,8 +411,10 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         p.inv[(size_t)t * p.k + j] = pos;
         p.perm_w[pos] = c.sel_w[i][j];
     }
-    if (threadIdx.x == 0) bulk_wait_read();   // this CTA's outgoing copies have read their sources
-    cluster_sync_all();                       // no CTA leaves while a peer may still copy into it
+    if (threadIdx.x < R) bulk_wait_read();    // this CTA's outgoing copies have read their sources
+    // no CTA leaves while a peer may still copy into it (no memory ordering needed)
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
