@@ -87,6 +87,11 @@ template <bool Q8> struct Cfg {
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 constexpr int kEpiThreads = 256;   // 8 epilogue warps
+// down-epilogue staging: per epilogue warp 32 rows x 16 fp32 columns, rows
+// padded to 20 floats (80 B: 16-byte aligned, and 8 consecutive rows fall in
+// distinct banks)
+constexpr int kStgRow = 20;
+constexpr size_t kStgBytes = (size_t)8 * 32 * kStgRow * 4;
 
 struct Params {
     const int32_t *offsets;   // [E+1] grouped-row offsets
@@ -479,27 +484,39 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 int tok = 0;
                 float wgt = 0.f;
                 if (valid) { tok = p.perm_tok[grow]; wgt = p.perm_w[grow]; }
-                // this thread: output columns [chalf*128, chalf*128 + 128) of its row
-                float *orow = p.out + (size_t)tok * p.d + nt * BN + chalf * (BN / 2);
+                // this warp: output columns [chalf*128, chalf*128 + 128) of its 32
+                // rows, in chunks of 16 columns.  A chunk is transposed through
+                // shared memory so that each store / reduction instruction of the
+                // warp covers 8 rows x 64 contiguous bytes (lane l: row l/4 + 8i,
+                // columns 4(l%4)..+3) instead of 32 rows x 16 bytes.
+                float *stg = reinterpret_cast<float *>(smem + C::CTL + sizeof(SmemCtl)) +
+                             (warp - 2) * 32 * kStgRow;
+                const float *obase = p.out + nt * BN + chalf * (BN / 2);
                 const uint32_t tv = tbase + chalf * (BN / 2);
 #pragma unroll 1
                 for (int cc = 0; cc < BN / 2; cc += 16) {
                     uint32_t v[16];
                     tmem_ld16(tv + cc, v);
                     tmem_ld_wait();
-                    if (valid) {
+                    float4 *srow = reinterpret_cast<float4 *>(stg + lane * kStgRow);
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float a = wgt * __uint_as_float(v[j]);
-                            const float b = wgt * __uint_as_float(v[j + 1]);
-                            const float cq = wgt * __uint_as_float(v[j + 2]);
-                            const float dq = wgt * __uint_as_float(v[j + 3]);
-                            if (p.k == 1)
-                                *reinterpret_cast<float4 *>(orow + cc + j) = make_float4(a, b, cq, dq);
-                            else
-                                red_add_v4(orow + cc + j, a, b, cq, dq);
+                    for (int j = 0; j < 4; ++j)
+                        srow[j] = make_float4(wgt * __uint_as_float(v[4 * j]), wgt * __uint_as_float(v[4 * j + 1]),
+                                              wgt * __uint_as_float(v[4 * j + 2]), wgt * __uint_as_float(v[4 * j + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = (lane >> 2) + 8 * i;          // row within the warp's 32
+                        const int rt = __shfl_sync(0xffffffffu, tok, r);
+                        const bool rv = __shfl_sync(0xffffffffu, valid ? 1 : 0, r) != 0;
+                        const float4 val = *reinterpret_cast<const float4 *>(stg + r * kStgRow + (lane & 3) * 4);
+                        if (rv) {
+                            float *o = const_cast<float *>(obase) + (size_t)rt * p.d + cc + (lane & 3) * 4;
+                            if (p.k == 1) *reinterpret_cast<float4 *>(o) = val;
+                            else red_add_v4(o, val.x, val.y, val.z, val.w);
                         }
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -521,7 +538,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 
 template <bool Q8> constexpr size_t smem_bytes()
 {
-    return 1024 + Cfg<Q8>::CTL + sizeof(SmemCtl);
+    // ring (+ converted B buffers), control block, down-epilogue staging
+    return 1024 + Cfg<Q8>::CTL + sizeof(SmemCtl) + kStgBytes;
 }
 
 // ------------------------------------------------------------------- host
