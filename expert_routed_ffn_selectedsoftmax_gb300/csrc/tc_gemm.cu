@@ -33,7 +33,7 @@
 //
 // Q8_0 weights ("zonos2.cpp internals", §Quantization: 8-bit blocks of 32
 // values with one fp16 scale): the B stage holds the int8 tile as loaded by
-// TMA; four converter warps (10-13) turn it into fp16 in the 128-byte-swizzled
+// TMA; eight converter warps (10-17) turn it into fp16 in the 128-byte-swizzled
 // layout -- int8 -> fp16 exactly via the 1024+q bit trick, times the block's
 // fp16 scale -- in one of two converted-B buffers, and the MMA runs kind::f16
 // with fp16 operands (the grouped rows and h are fp16 on this path).
@@ -75,13 +75,18 @@ constexpr int BQ_BYTES = BN * BK;             // 16 KB (int8 B tile)
 constexpr int SC_BYTES = BN * (BK / 32) * 2;  // 1 KB (fp16 scales of the int8 tile)
 constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
 
+#ifndef MOE_GEMM_CONV_WARPS
+#define MOE_GEMM_CONV_WARPS 8
+#endif
+constexpr int kConvWarps = MOE_GEMM_CONV_WARPS;   // Q8_0 converter warps (4 or 8)
+
 // Per-variant shared-memory layout: a ring of STAGES stages {A, B or Bq},
 // then (Q8 only) two converted fp16 B buffers, then the control block.
 template <bool Q8> struct Cfg {
     static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SC_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
     static constexpr int CVT = Q8 ? 2 : 0;
-    static constexpr int THREADS = Q8 ? 448 : 320;   // 2 + 8 epilogue (+ 4 converter) warps
+    static constexpr int THREADS = Q8 ? 320 + 32 * kConvWarps : 320;   // 2 + 8 epilogue (+ converter) warps
     static constexpr size_t CTL = (size_t)STAGES * STAGE + (size_t)CVT * B_BYTES;
 };
 
@@ -199,7 +204,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], CL); }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], kEpiThreads);
-            mbar_init(&c.cfull[b], 128); mbar_init(&c.cempty[b], 1);
+            mbar_init(&c.cfull[b], 32 * kConvWarps); mbar_init(&c.cempty[b], 1);
         }
         mbar_init(&c.drain, 1);
         c.abort_flag = 0;
@@ -375,9 +380,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             mbar_wait(&c.drain, 0, &no_abort);
         }
     } else if (Q8 && warp >= 10) {
-        // ------------------------------------------------ Q8_0 converters (4 warps)
+        // ------------------------------------------------ Q8_0 converters (kConvWarps warps)
         // lane -> (row in an 8-row pass, 16-byte column chunk of the int8 row);
-        // warp w converts rows [64(w-10), 64(w-10)+64) of the 256-row B tile
+        // converter warp cw converts rows [cw*256/kConvWarps, (cw+1)*256/kConvWarps)
+        // of the 256-row B tile
         const int cw = warp - 10;
         const int rsub = lane >> 2, q = lane & 3;
         uint32_t it = 0;
@@ -392,8 +398,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 const __half *scl = reinterpret_cast<const __half *>(bq + BQ_BYTES);
                 uint8_t *bo = sCvt + cb * B_BYTES;
 #pragma unroll
-                for (int pass = 0; pass < 8; ++pass) {
-                    const int r = cw * 64 + pass * 8 + rsub;
+                for (int pass = 0; pass < BN / 8 / kConvWarps; ++pass) {
+                    const int r = cw * (BN / kConvWarps) + pass * 8 + rsub;
                     // scale of (row r, 32-column block q/2): GATEUP keeps the gate
                     // rows' [2][128] scales, then the up rows'; DOWN [2][256]
                     const int blk = q >> 1;
