@@ -174,7 +174,7 @@ def expert_kernel_names(w, T, num_sms):
     act16 = w.act_dtype == 1
     if (act16 and w.w_dtype in (1, 2) and w.d % 256 == 0 and w.F % 128 == 0
             and rows >= 64 * w.E and T >= 512):
-        q = "Q8_0" if w.w_dtype == 2 else "bf16"
+        q = "Q8_0, CTA pairs" if w.w_dtype == 2 else "bf16"
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4}
     if act16 and w.w_dtype == 1 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:

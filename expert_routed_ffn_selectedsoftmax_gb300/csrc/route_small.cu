@@ -84,12 +84,6 @@ struct Ctl {
     float sel_w[TPC][kMaxTopK];
 };
 
-__device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    return remote;
-}
 // bulk copy of `bytes` from this CTA's shared memory to a CTA of the
 // cluster; completion is counted on that CTA's mbarrier (cluster addresses)
 __device__ __forceinline__ void bulk_to_peer(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)

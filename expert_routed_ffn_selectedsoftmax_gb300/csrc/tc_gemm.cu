@@ -13,19 +13,15 @@
 //   the epilogue scales each row by its routing weight and adds it into
 //   out[token] (fp32; a plain store when k == 1).
 //
-// Clusters of CL = 2 CTAs work on the two m-tiles (same expert, same
-// n-tile) of one work unit: each CTA loads its own A tile and one half of the
-// shared B tile with a cluster-multicast TMA, so every SM pulls 2/3 of the
-// operand bytes of a lone CTA; each CTA's MMA commit is multicast to the
-// "stage empty" barriers of both CTAs, since a stage is refilled in both.
-//
 // Per CTA (persistent, one per SM): warp 0 issues TMA loads of the A (rows)
-// and B (weights) tiles into a 4-stage shared-memory ring (128-byte swizzle);
-// warp 1 issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulators in TMEM,
-// two accumulator buffers of 256 columns); warps 2-9 drain the accumulators,
-// two warps per 32-lane TMEM quarter, each taking half of the tile's columns
+// and B (weights) tiles into a shared-memory ring (128-byte swizzle); warp 1
+// issues tcgen05.mma (M=128, N=256, K=16, fp32 accumulators in TMEM, two
+// accumulator buffers of 256 columns); warps 2-9 drain the accumulators, two
+// warps per 32-lane TMEM quarter, each taking half of the tile's columns
 // (with one warp per scheduler the drain was latency-bound and as slow as
-// the mainloop of a tile).
+// the mainloop of a tile).  In steady state a 16-bit k-block takes about as
+// long as its four MMAs at the tensor pipe's sustained rate (~0.36 us per
+// 128x256x64 on every SM at once).
 // Tiles are (expert, n-tile, m-tile), m fastest, so CTAs running at the same
 // time share weight tiles through L2.  Rows of a tile past the end of the
 // expert's group are computed on neighbouring rows (or TMA zero fill) and
@@ -35,8 +31,22 @@
 // values with one fp16 scale): the B stage holds the int8 tile as loaded by
 // TMA; eight converter warps (10-17) turn it into fp16 in the 128-byte-swizzled
 // layout -- int8 -> fp16 exactly via the 1024+q bit trick, times the block's
-// fp16 scale -- in one of two converted-B buffers, and the MMA runs kind::f16
+// fp16 scale -- in one of CVT converted-B buffers, and the MMA runs kind::f16
 // with fp16 operands (the grouped rows and h are fp16 on this path).
+//
+// CTA pairs (PAIR, used for Q8_0): two CTAs of a cluster share one tile of
+// 256 grouped rows x 256 columns through tcgen05.mma.cta_group::2 (M = 256):
+// each CTA loads its own 128 rows of A and one half of B (GATEUP: the gate
+// rows in the even CTA, the up rows in the odd one; DOWN: columns 0-127 /
+// 128-255) and converts only that half, and the even CTA's MMA thread
+// multiplies the whole tile, reading both CTAs' shared memory; each CTA's
+// TMEM receives its own 128 rows.  Halving the per-CTA B part halves the
+// converters' work per k-block and leaves room for four converted buffers.
+// The odd CTA's loads count their bytes on the even CTA's "stage full"
+// barrier (16-bit B) or its converter warps arrive there once its part of B
+// is converted (Q8_0); the MMA commits are multicast to the "stage empty" /
+// "accumulator full" barriers of both CTAs, and both CTAs' epilogue warps
+// arrive on the even CTA's "accumulator empty" barrier.
 //
 // Every wait on an mbarrier is bounded (2 s of %globaltimer); on timeout the
 // waiting role sets the status word, raises a CTA-wide abort flag that the
@@ -52,15 +62,14 @@
 #include "sm100.cuh"
 #include "tc_gemm.h"
 
-// Tuning (compile-time): CTAs per cluster (1 or 2) and whether units start
-// at a rotated k-block.  Measured on the ZONOS3-Mini and ZONOS2 prefill
-// layers, pairs that share the weight tile by multicast were 6-9 % slower
-// than single CTAs and the rotation made no difference, so both are off.
-#ifndef MOE_GEMM_CLUSTER
-#define MOE_GEMM_CLUSTER 1
-#endif
-#ifndef MOE_GEMM_KROTATE
-#define MOE_GEMM_KROTATE 0
+// Tuning (compile-time): which grouped GEMMs run as CTA pairs (when clusters
+// of two fit on the device): 0 none, 1 Q8_0 weights only, 2 all.  Measured on
+// the ZONOS2 Q8_0 prefill layer, pairs with 4 converted buffers took 238 us
+// per layer against 249 us for single CTAs; on the ZONOS3-Mini bf16 prefill
+// layer (Zipf-skewed experts) single CTAs took 111 us against 114 us, since
+// 256-row units pad more rows of small experts.
+#ifndef MOE_GEMM_PAIR
+#define MOE_GEMM_PAIR 1
 #endif
 
 namespace moe {
@@ -68,35 +77,57 @@ namespace tc {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int B_BYTES = BN * BK * 2;          // 32 KB (16-bit B tile)
-constexpr int BQ_BYTES = BN * BK;             // 16 KB (int8 B tile)
-constexpr int SC_BYTES = BN * (BK / 32) * 2;  // 1 KB (fp16 scales of the int8 tile)
+constexpr int SC_BYTES = BN * (BK / 32) * 2;  // 1 KB (fp16 scales of a 256-row int8 tile)
 constexpr int TMEM_COLS = 512;                // 2 accumulators x 256 fp32 columns
+constexpr int kMaxStages = 6;
 
 #ifndef MOE_GEMM_CONV_WARPS
 #define MOE_GEMM_CONV_WARPS 8
 #endif
 constexpr int kConvWarps = MOE_GEMM_CONV_WARPS;   // Q8_0 converter warps (4 or 8)
+// Q8_0: converted fp16 B buffers and ring stages, pair and single-CTA kernels
+#ifndef MOE_GEMM_PAIR_Q8_CVT
+#define MOE_GEMM_PAIR_Q8_CVT 4
+#endif
+#ifndef MOE_GEMM_Q8_CVT
+#define MOE_GEMM_Q8_CVT 2
+#endif
+#ifndef MOE_GEMM_PAIR_Q8_STAGES
+#define MOE_GEMM_PAIR_Q8_STAGES 5
+#endif
+#ifndef MOE_GEMM_Q8_STAGES
+#define MOE_GEMM_Q8_STAGES 4
+#endif
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 
-// Per-variant shared-memory layout: a ring of STAGES stages {A, B or Bq},
-// then (Q8 only) two converted fp16 B buffers, then the control block.
-template <bool Q8> struct Cfg {
-    static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SC_BYTES + 1023) / 1024 * 1024
+// Per-variant shared-memory layout: a ring of STAGES stages {A, this CTA's
+// part of B (16-bit) or of Bq (int8) + its scales}, then (Q8 only) two
+// converted fp16 B buffers, then the control block.
+template <bool Q8, bool PAIR> struct Cfg {
+    static constexpr int CL = PAIR ? 2 : 1;
+    static constexpr int BNL = BN / CL;             // B rows held by this CTA
+    static constexpr int B_BYTES = BNL * BK * 2;    // 16-bit B (this CTA's rows)
+    static constexpr int BQ_BYTES = BNL * BK;       // int8 B
+    static constexpr int SCL_BYTES = SC_BYTES / CL; // its scales
+    static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SCL_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
-    static constexpr int CVT = Q8 ? 2 : 0;
-    static constexpr int THREADS = Q8 ? 320 + 32 * kConvWarps : 320;   // 2 + 8 epilogue (+ converter) warps
+    static constexpr int STAGES = Q8 ? (PAIR ? MOE_GEMM_PAIR_Q8_STAGES : MOE_GEMM_Q8_STAGES) : (PAIR ? 6 : 4);
+    static constexpr int CVT = Q8 ? (PAIR ? MOE_GEMM_PAIR_Q8_CVT : MOE_GEMM_Q8_CVT) : 0;
+    static constexpr int NCVT = CVT > 0 ? CVT : 1;   // (index arithmetic of the 16-bit variants)
+    static constexpr int THREADS = Q8 ? 64 + kEpiThreads + 32 * kConvWarps : 64 + kEpiThreads;
     static constexpr size_t CTL = (size_t)STAGES * STAGE + (size_t)CVT * B_BYTES;
+    static_assert(STAGES <= kMaxStages && CVT <= 4, "ring deeper than the control block");
 };
 
 enum Mode { GATEUP = 0, DOWN = 1 };
-constexpr int kEpiThreads = 256;   // 8 epilogue warps
 // down-epilogue staging: per epilogue warp 32 rows x 16 fp32 columns, rows
 // padded to 20 floats (80 B: 16-byte aligned, and 8 consecutive rows fall in
 // distinct banks)
 constexpr int kStgRow = 20;
-constexpr size_t kStgBytes = (size_t)8 * 32 * kStgRow * 4;
+constexpr size_t kStgBytes = (size_t)kEpiWarps * 32 * kStgRow * 4;
 
 struct Params {
     const int32_t *offsets;   // [E+1] grouped-row offsets
@@ -115,28 +146,26 @@ struct Params {
 };
 
 struct SmemCtl {
-    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, cfull[2], cempty[2];
+    uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain, cfull[4], cempty[4];
     uint32_t tmem_base;
     int abort_flag;
+    uint32_t fail;
     int n_tiles_total;
     int tile_start[kMaxExperts + 1];
     int mtiles[kMaxExperts];
     int off[kMaxExperts + 1];
 };
 
-// Instruction descriptor for the M = 128, N = 256 tiles of this file.
-__host__ __device__ constexpr uint32_t idesc_f16(int ab_fp16) { return idesc_f16_mn(ab_fp16, BM, BN); }
-
 // SiLU(z) = z * sigmoid(z), with the fast exponential and an approximate
 // divide (relative error ~1e-6, far below the 16-bit rounding of h that
 // follows; for z < -87, 1 + e^-z overflows and the result is the correct -0).
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-// tile -> (expert, m-tile, n-tile); tile_start is an exclusive scan over experts
-// unit -> (expert, m-tile pair, n-tile); units are mt-pair fastest.  mtiles[e]
-// holds the number of CL-sized m-tile groups of expert e.
-__device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int n_tiles, int tile,
-                                            int &e, int &mt, int &nt)
+// unit -> (expert, m-group, n-tile); tile_start is an exclusive scan over
+// experts of mtiles[e] * n_tiles, mtiles[e] the number of CL-row-tile groups
+// of expert e; units are m-group fastest, so CTAs running at the same time
+// share weight tiles through L2.
+__device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int tile, int &e, int &mt, int &nt)
 {
     int lo = 0, hi = E - 1;   // largest e with tile_start[e] <= tile
     while (lo < hi) {
@@ -149,7 +178,6 @@ __device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int n_tiles
     const int m = c.mtiles[e];
     nt = local / m;
     mt = local - nt * m;
-    (void)n_tiles;
 }
 
 // int8 x 16 (one uint4) -> fp16 x 16 scaled by s: (q ^ 0x80) placed in the
@@ -173,18 +201,36 @@ __device__ __forceinline__ void dequant16(const uint4 q, const __half2 s, uint4 
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Bounded wait of a whole warp for a barrier phase (warp-uniform result).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+}
+
+// Arrival of one warp (lane 0, after the warp's prior work) on the barrier
+// `bar` of cluster CTA 0 (PAIR) or of this CTA.
+template <bool PAIR>
+__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane)
+{
+    __syncwarp();
+    if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(peer_addr(bar, 0));
+        else mbar_arrive(bar);
+    }
+}
+
 // tm_s0/tm_s1 (Q8 only): the B matrices' fp16 scale planes [cols/32, rows],
-// box {128 rows, 2 blocks}.  CL: CTAs per cluster (1 or 2).
-template <int MODE, bool Q8, int CL>
-__global__ void __launch_bounds__(Cfg<Q8>::THREADS, 1)
+// box {128 rows, 2 blocks}.
+template <int MODE, bool Q8, bool PAIR>
+__global__ void __launch_bounds__(Cfg<Q8, PAIR>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b0,
                     const __grid_constant__ CUtensorMap tm_b1,
                     const __grid_constant__ CUtensorMap tm_s0,
                     const __grid_constant__ CUtensorMap tm_s1, const Params p)
 {
-    using C = Cfg<Q8>;
-    constexpr int THREADS = C::THREADS;
+    using C = Cfg<Q8, PAIR>;
+    constexpr int CL = C::CL, STAGES = C::STAGES, BNL = C::BNL;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -193,19 +239,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
-    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
     const int cid = blockIdx.x / CL, nclusters = gridDim.x / CL;
-    constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1u);
 
     // ---- set-up that reads nothing the preceding kernels write (barriers,
     // TMEM, tensor-map prefetch): under programmatic dependent launch it
     // overlaps the tail of the kernel before
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], CL); }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], kEpiThreads);
-            mbar_init(&c.cfull[b], 32 * kConvWarps); mbar_init(&c.cempty[b], 1);
-        }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], CL * kEpiWarps); }
+        for (int b = 0; b < 4; ++b) { mbar_init(&c.cfull[b], CL * kConvWarps); mbar_init(&c.cempty[b], 1); }
         mbar_init(&c.drain, 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -217,23 +260,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b1)) : "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&c.tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
+        else tmem_alloc(&c.tmem_base, TMEM_COLS);
     }
     tc_fence_before();
     pdl_enter();
-    if (upstream_failed(p.status)) {   // (synchronises the CTA)
-        if (warp == 1) {
-            tc_fence_after();
-            tmem_dealloc(c.tmem_base, TMEM_COLS);
-        }
-        return;
-    }
-    // ---- tile table from the grouped-row offsets
-    for (int e = threadIdx.x; e <= E; e += THREADS) c.off[e] = p.offsets[e];
+    // ---- status of the kernels before, and the tile table from the
+    // grouped-row offsets (harmless arithmetic when the status says failed)
+    if (threadIdx.x == 0) c.fail = p.status ? *(volatile const uint32_t *)p.status : 0u;
+    for (int e = threadIdx.x; e <= E; e += C::THREADS) c.off[e] = p.offsets[e];
     __syncthreads();
     if (threadIdx.x < 32) {
         // exclusive scan of mtiles_e * n_tiles over experts (E <= 256: 8 per lane)
@@ -266,14 +301,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         if (lane == 31) { c.n_tiles_total = incl; c.tile_start[E] = incl; }
     }
     tc_fence_before();
-    // the peer's multicast copies and commits target this CTA's barriers:
-    // every barrier of the cluster is initialised before anyone proceeds
-    if (CL > 1) cluster_sync_all();
+    // the peer's arrivals and commits target this CTA's barriers: every
+    // barrier of the cluster is initialised before anyone proceeds
+    if (PAIR) cluster_sync_all();
     else __syncthreads();
     tc_fence_after();
+    // both CTAs of a pair take the same decision (the peer's flag is read
+    // before the final cluster barrier, so it is still resident)
+    const bool run = (c.fail | (PAIR ? ld_cluster_u32(peer_addr(&c.fail, rank ^ 1u)) : 0u)) == 0u;
 
     const uint32_t tmem = c.tmem_base;
-    const int total = c.n_tiles_total;
+    const int total = run ? c.n_tiles_total : 0;
     const int kblocks = p.K / BK;
     volatile int *abort_flag = &c.abort_flag;
 
@@ -283,48 +321,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += nclusters) {
             int e, mt, nt;
-            decode_tile(c, E, p.n_tiles, tile, e, mt, nt);
-            mt = mt * CL + rank;
+            decode_tile(c, E, tile, e, mt, nt);
+            mt = mt * CL + (int)rank;
             const int arow = c.off[e] + mt * BM;
-            // units start at different k-blocks, so CTAs sharing a weight tile do
-            // not all request the same lines at once (same order for both CTAs
-            // of a pair; the sum order of a tile is fixed by its unit id)
-            const int rot = MOE_GEMM_KROTATE ? (tile * 5) % kblocks : 0;
-            for (int kl = 0; kl < kblocks; ++kl, ++it) {
-                const int kb = kl + rot < kblocks ? kl + rot : kl + rot - kblocks;
+            // this CTA's B rows: GATEUP (non-pair: gate then up; pair: gate in
+            // CTA 0, up in CTA 1), DOWN 256 (non-pair) or 128 rows of W_d
+            const int grow = e * p.F + nt * (BN / 2);
+            const int drow = e * p.d + nt * BN + (int)rank * BNL;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                mbar_expect_tx(&c.full[s], A_BYTES + (Q8 ? BQ_BYTES + SC_BYTES : B_BYTES));
                 uint8_t *st = smem + s * C::STAGE;
+                uint8_t *sb = st + A_BYTES;
+                uint8_t *sc = st + A_BYTES + C::BQ_BYTES;   // Q8 scales
+                if (PAIR && !Q8) {
+                    // both CTAs' A and B parts count on CTA 0's stage barrier
+                    if (rank == 0) mbar_expect_tx(&c.full[s], 2 * (A_BYTES + C::B_BYTES));
+                    const uint32_t bar0 = peer_addr(&c.full[s], 0);
+                    tma_load_2d_pair(st, &tm_a, bar0, kb * BK, arow);
+                    if (MODE == GATEUP) tma_load_2d_pair(sb, rank ? &tm_b1 : &tm_b0, bar0, kb * BK, grow);
+                    else tma_load_2d_pair(sb, &tm_b0, bar0, kb * BK, drow);
+                    continue;
+                }
+                mbar_expect_tx(&c.full[s], A_BYTES + (Q8 ? C::BQ_BYTES + C::SCL_BYTES : C::B_BYTES));
                 tma_load_2d(st, &tm_a, &c.full[s], kb * BK, arow);
-                // B: 16-bit tiles are 128 B per row, int8 tiles 64 B per row
-                constexpr int half_b = (Q8 ? BQ_BYTES : B_BYTES) / 2;
-                // Q8 scales: two [2 blocks][128 rows] boxes, one per B half
-                uint8_t *sc = st + A_BYTES + BQ_BYTES;
-                // B halves: GATEUP = (gate rows, up rows), DOWN = (rows 0-127, 128-255)
-                const int brow = MODE == GATEUP ? e * p.F + nt * (BN / 2) : e * p.d + nt * BN;
-                const CUtensorMap *bm[2] = {&tm_b0, MODE == GATEUP ? &tm_b1 : &tm_b0};
-                const CUtensorMap *sm[2] = {&tm_s0, MODE == GATEUP ? &tm_s1 : &tm_s0};
-                const int hrow[2] = {brow, MODE == GATEUP ? brow : brow + BN / 2};
-                if (CL == 1) {
-                    if (MODE == GATEUP) {
-                        tma_load_2d(st + A_BYTES, bm[0], &c.full[s], kb * BK, hrow[0]);
-                        tma_load_2d(st + A_BYTES + half_b, bm[1], &c.full[s], kb * BK, hrow[1]);
+                if (MODE == GATEUP) {
+                    if (PAIR) {
+                        const CUtensorMap *bm = rank ? &tm_b1 : &tm_b0;
+                        tma_load_2d(sb, bm, &c.full[s], kb * BK, grow);
+                        if (Q8) tma_load_2d(sc, rank ? &tm_s1 : &tm_s0, &c.full[s], grow, kb * 2);
                     } else {
-                        tma_load_2d(st + A_BYTES, &tm_b0, &c.full[s], kb * BK, brow);   // 256-row box
-                    }
-                    if (Q8) {
-                        tma_load_2d(sc, sm[0], &c.full[s], hrow[0], kb * 2);
-                        tma_load_2d(sc + SC_BYTES / 2, sm[1], &c.full[s], hrow[1], kb * 2);
+                        constexpr int half_b = (Q8 ? C::BQ_BYTES : C::B_BYTES) / 2;
+                        tma_load_2d(sb, &tm_b0, &c.full[s], kb * BK, grow);
+                        tma_load_2d(sb + half_b, &tm_b1, &c.full[s], kb * BK, grow);
+                        if (Q8) {
+                            tma_load_2d(sc, &tm_s0, &c.full[s], grow, kb * 2);
+                            tma_load_2d(sc + SC_BYTES / 2, &tm_s1, &c.full[s], grow, kb * 2);
+                        }
                     }
                 } else {
-                    // this CTA fetches half `rank` of B for both CTAs of the pair
-                    tma_load_2d_mc(st + A_BYTES + rank * half_b, bm[rank], &c.full[s], kb * BK,
-                                   hrow[rank], kAll);
-                    if (Q8)
-                        tma_load_2d_mc(sc + rank * (SC_BYTES / 2), sm[rank], &c.full[s], hrow[rank],
-                                       kb * 2, kAll);
+                    tma_load_2d(sb, &tm_b0, &c.full[s], kb * BK, drow);   // BNL-row box
+                    if (Q8) {
+                        tma_load_2d(sc, &tm_s0, &c.full[s], drow, kb * 2);
+                        if (!PAIR) tma_load_2d(sc + SC_BYTES / 2, &tm_s0, &c.full[s], drow + BN / 2, kb * 2);
+                    }
                 }
             }
         }
@@ -332,16 +373,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             atomicOr(p.status, kDevTimeout);
             c.abort_flag = 1;
             // let loads already issued land before the CTA exits
-            for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j) {
-                volatile int no_abort = 0;
-                mbar_wait(&c.full[j % STAGES], (j / STAGES) & 1u, &no_abort);
+            if (PAIR && !Q8 && rank != 0) {
+                // their bytes count on CTA 0's barriers: give them time
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 200000ull) {}
+            } else {
+                for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&c.full[j % STAGES], (j / STAGES) & 1u, &no_abort, 1000000ull);
+                }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        // fp16 operands on the Q8_0 path (grouped rows and h are fp16), else
-        // bf16 -- except a bf16-weight DOWN over an fp16 h, which cannot occur
-        const uint32_t idesc_rt = idesc_f16(Q8 ? 1 : 0);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (CTA 0 of a pair)
+        // fp16 operands on the Q8_0 path (grouped rows and h are fp16), else bf16
+        const uint32_t idesc = idesc_f16_mn(Q8 ? 1 : 0, BM * CL, BN);
         uint32_t it = 0, local_tile = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += nclusters, ++local_tile) {
@@ -354,54 +400,66 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
-                const int cb = it & 1;
-                if (Q8 && !mbar_wait(&c.cfull[cb], (it >> 1) & 1u, abort_flag)) { ok = false; break; }
+                const int cb = Q8 ? it % C::NCVT : 0;
+                if (Q8 && !mbar_wait(&c.cfull[cb], (it / C::NCVT) & 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(smem + s * C::STAGE);
-                const uint32_t b0 = Q8 ? smem_u32(sCvt + cb * B_BYTES) : a0 + A_BYTES;
+                const uint32_t b0 = Q8 ? smem_u32(sCvt + cb * C::B_BYTES) : a0 + A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
-                    umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc_rt,
-                             (kb | kk) != 0);
+                    if (PAIR)
+                        umma_f16_pair(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                                      (kb | kk) != 0);
+                    else
+                        umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                                 (kb | kk) != 0);
                 }
-                // frees the stage (in both CTAs of a pair) when these MMAs finish
-                if (CL > 1) umma_commit_mc(&c.empty[s], kAll);
-                else umma_commit(&c.empty[s]);
-                if (Q8) umma_commit(&c.cempty[cb]);
+                // frees the stage (and the converted buffer) in both CTAs of a
+                // pair once these MMAs have read them
+                if (PAIR) {
+                    umma_commit_pair_mc(&c.empty[s], 3);
+                    if (Q8) umma_commit_pair_mc(&c.cempty[cb], 3);
+                } else {
+                    umma_commit(&c.empty[s]);
+                    if (Q8) umma_commit(&c.cempty[cb]);
+                }
             }
             if (!ok) break;
-            umma_commit(&c.tfull[acc]);       // accumulator ready for the epilogue
+            // accumulator ready for the epilogue warps of both CTAs
+            if (PAIR) umma_commit_pair_mc(&c.tfull[acc], 3);
+            else umma_commit(&c.tfull[acc]);
         }
         if (!ok) {
             atomicOr(p.status, kDevTimeout);
             c.abort_flag = 1;
-            umma_commit(&c.drain);            // wait for MMAs in flight before TMEM is freed
+            // wait for MMAs in flight before TMEM is freed
+            if (PAIR) umma_commit_pair(&c.drain);
+            else umma_commit(&c.drain);
             volatile int no_abort = 0;
             mbar_wait(&c.drain, 0, &no_abort);
         }
-    } else if (Q8 && warp >= 10) {
+    } else if (Q8 && warp >= 2 + kEpiWarps) {
         // ------------------------------------------------ Q8_0 converters (kConvWarps warps)
         // lane -> (row in an 8-row pass, 16-byte column chunk of the int8 row);
-        // converter warp cw converts rows [cw*256/kConvWarps, (cw+1)*256/kConvWarps)
-        // of the 256-row B tile
-        const int cw = warp - 10;
+        // converter warp cw converts rows [cw*BNL/kConvWarps, (cw+1)*BNL/kConvWarps)
+        // of this CTA's B rows
+        const int cw = warp - 2 - kEpiWarps;
         const int rsub = lane >> 2, q = lane & 3;
         uint32_t it = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += nclusters) {
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 const int s = it % STAGES;
-                const int cb = it & 1;
-                if (!mbar_wait(&c.full[s], (it / STAGES) & 1u, abort_flag)) { ok = false; break; }
-                if (!mbar_wait(&c.cempty[cb], ((it >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                const int cb = it % C::NCVT;
+                if (!warp_wait(&c.full[s], (it / STAGES) & 1u, abort_flag)) { ok = false; break; }
+                if (!warp_wait(&c.cempty[cb], ((it / C::NCVT) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 const uint8_t *bq = smem + s * C::STAGE + A_BYTES;
-                const __half *scl = reinterpret_cast<const __half *>(bq + BQ_BYTES);
-                uint8_t *bo = sCvt + cb * B_BYTES;
+                const __half *scl = reinterpret_cast<const __half *>(bq + C::BQ_BYTES);
+                uint8_t *bo = sCvt + cb * C::B_BYTES;
 #pragma unroll
-                for (int pass = 0; pass < BN / 8 / kConvWarps; ++pass) {
-                    const int r = cw * (BN / kConvWarps) + pass * 8 + rsub;
-                    // scale of (row r, 32-column block q/2): GATEUP keeps the gate
-                    // rows' [2][128] scales, then the up rows'; DOWN [2][256]
+                for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
+                    const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
+                    // scale of (row r, 32-column block q/2): boxes of [2 blocks][128 rows]
                     const int blk = q >> 1;
                     const __half sv = scl[(r >> 7) * 256 + blk * 128 + (r & 127)];
                     const uint4 v = *reinterpret_cast<const uint4 *>(bq + r * 64 + q * 16);
@@ -411,19 +469,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4)) = hi;
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&c.cfull[cb]);
+                warp_arrive<PAIR>(&c.cfull[cb], lane);
             }
         }
         if (!ok) {
             if (lane == 0) atomicOr(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
-    } else if (warp >= 2 && warp < 10) {
+    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
         // ------------------------------------------------ epilogue (8 warps)
         const int quarter = warp & 3;         // TMEM lanes this warp may access
         const int row_in_tile = quarter * 32 + lane;
         const int chalf = (warp - 2) >> 2;    // which half of the tile's columns
-        if (MODE == GATEUP && p.out_zero) {
+        if (MODE == GATEUP && p.out_zero && run) {
             // the down kernel accumulates into `out`: zero this CTA's share of
             // it while the first tile's operands stream in
             float4 *o4 = reinterpret_cast<float4 *>(p.out_zero);
@@ -438,15 +496,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_ph = (local_tile >> 1) & 1u;
             // warp-uniform outcome: tcgen05.ld below is warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(&c.tfull[acc], acc_ph, abort_flag))) {
+            if (!warp_wait(&c.tfull[acc], acc_ph, abort_flag)) {
                 if (lane == 0) atomicOr(p.status, kDevTimeout);
                 c.abort_flag = 1;
                 break;
             }
             tc_fence_after();
             int e, mt, nt;
-            decode_tile(c, E, p.n_tiles, tile, e, mt, nt);
-            mt = mt * CL + rank;
+            decode_tile(c, E, tile, e, mt, nt);
+            mt = mt * CL + (int)rank;
             const int rows_e = c.off[e + 1] - c.off[e];
             const bool valid = mt * BM + row_in_tile < rows_e;
             const int grow = c.off[e] + mt * BM + row_in_tile;
@@ -526,27 +584,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 }
             }
             tc_fence_before();
-            mbar_arrive(&c.tempty[acc]);
+            warp_arrive<PAIR>(&c.tempty[acc], lane);
         }
     }
 
-    // no CTA leaves while its peer may still multicast into it or commit to it
-    if (CL > 1) cluster_sync_all();
+    // no CTA leaves while its peer may still read its shared memory, arrive
+    // on its barriers or (CTA 0) have MMAs writing its TMEM
+    if (PAIR) cluster_sync_all();
     else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        if (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
+        else tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
-template <bool Q8> constexpr size_t smem_bytes()
+template <bool Q8, bool PAIR> constexpr size_t smem_bytes()
 {
     // ring (+ converted B buffers), control block, down-epilogue staging
-    return 1024 + Cfg<Q8>::CTL + sizeof(SmemCtl) + kStgBytes;
+    return 1024 + Cfg<Q8, PAIR>::CTL + sizeof(SmemCtl) + kStgBytes;
 }
+static_assert(smem_bytes<false, true>() <= 232448 && smem_bytes<true, true>() <= 232448 &&
+                  smem_bytes<false, false>() <= 232448 && smem_bytes<true, false>() <= 232448,
+              "shared memory per CTA");
 
 // ------------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -609,67 +670,77 @@ bool tc_gemm_prefer(int T, int d, int E, int k, int F)
     return (long long)T * k >= 64LL * E && T >= 512;
 }
 
-constexpr int kCluster = MOE_GEMM_CLUSTER;   // CTAs per cluster of the grouped GEMMs
-
-template <bool Q8, int CL>
+template <bool Q8, bool PAIR>
 static cudaError_t set_smem_attrs()
 {
     using namespace tc;
     static std::atomic<int> done{0};
     if (done.load()) return cudaSuccess;
-    const int smem = (int)smem_bytes<Q8>();
+    const int smem = (int)smem_bytes<Q8, PAIR>();
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8, CL>,
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8, CL>,
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return err;
     done.store(1);
     return cudaSuccess;
 }
 
-// Clusters of CL CTAs that can be resident at once (0 if the query fails).
-template <int MODE, bool Q8, int CL>
-static int max_active_clusters()
+// Clusters of two CTAs (pair kernels) that can be resident at once (0 if the
+// query fails).
+template <int MODE, bool Q8>
+static int max_active_pairs()
 {
     using namespace tc;
     static std::atomic<int> cached{-1};
     int n = cached.load();
     if (n >= 0) return n;
     // the query needs the kernel's dynamic shared-memory limit raised first
-    if (set_smem_attrs<Q8, CL>() != cudaSuccess) {
+    if (set_smem_attrs<Q8, true>() != cudaSuccess) {
         cudaGetLastError();
         cached.store(0);
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL * 152);
-    cfg.blockDim = dim3(Cfg<Q8>::THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<Q8>();
+    cfg.gridDim = dim3(2 * 152);
+    cfg.blockDim = dim3(Cfg<Q8, true>::THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<Q8, true>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, Q8, CL>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, Q8, true>, &cfg) != cudaSuccess)
         n = 0;
     cudaGetLastError();   // clear a failed query
     cached.store(n);
     return n;
 }
 
-template <bool Q8, int CL>
-static cudaError_t launch_pair(const TcArgs &a, tc::Params p, const CUtensorMap &m_xp,
-                               const CUtensorMap &m_wg, const CUtensorMap &m_wu,
-                               const CUtensorMap &m_h, const CUtensorMap &m_wd,
-                               const CUtensorMap &m_sg, const CUtensorMap &m_su,
-                               const CUtensorMap &m_sd, cudaStream_t stream)
+bool tc_gemm_pairs(moe_dtype w_dt)
+{
+    const bool q8 = w_dt == MOE_Q8_0;
+    if (MOE_GEMM_PAIR == 0 || (MOE_GEMM_PAIR == 1 && !q8)) return false;
+    if constexpr (MOE_GEMM_PAIR >= 2) {
+        if (!q8) return max_active_pairs<tc::GATEUP, false>() > 0 && max_active_pairs<tc::DOWN, false>() > 0;
+    }
+    return q8 && max_active_pairs<tc::GATEUP, true>() > 0 && max_active_pairs<tc::DOWN, true>() > 0;
+}
+
+template <bool Q8, bool PAIR>
+static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap &m_xp,
+                                const CUtensorMap &m_wg, const CUtensorMap &m_wu,
+                                const CUtensorMap &m_h, const CUtensorMap &m_wd,
+                                const CUtensorMap &m_sg, const CUtensorMap &m_su,
+                                const CUtensorMap &m_sd, cudaStream_t stream)
 {
     using namespace tc;
+    constexpr int CL = Cfg<Q8, PAIR>::CL;
     cudaError_t err;
-    if ((err = set_smem_attrs<Q8, CL>()) != cudaSuccess) return err;
+    if ((err = set_smem_attrs<Q8, PAIR>()) != cudaSuccess) return err;
     const int rows = a.T * a.k;
     // upper bound on units: every expert could own a ragged group of CL m-tiles
     const long long max_groups = rows / (BM * CL) + (a.E < rows ? a.E : rows);
@@ -677,27 +748,27 @@ static cudaError_t launch_pair(const TcArgs &a, tc::Params p, const CUtensorMap 
         long long cl = units < max_clusters ? units : max_clusters;
         return dim3((unsigned)((cl < 1 ? 1 : cl) * CL));
     };
-    const size_t smem = smem_bytes<Q8>();
-    const dim3 block(Cfg<Q8>::THREADS);
+    const size_t smem = smem_bytes<Q8, PAIR>();
+    const dim3 block(Cfg<Q8, PAIR>::THREADS);
 
     p.K = a.d; p.n_tiles = a.F / (BN / 2);
-    const dim3 g1 = grid_for(max_groups * p.n_tiles, CL > 1 ? max_active_clusters<GATEUP, Q8, CL>() : a.num_sms);
-    if (CL > 1)
-        err = launch_pdl_cluster(grouped_gemm_kernel<GATEUP, Q8, CL>, g1, block, smem, stream, CL,
+    const dim3 g1 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<GATEUP, Q8>() : a.num_sms);
+    if (PAIR)
+        err = launch_pdl_cluster(grouped_gemm_kernel<GATEUP, Q8, PAIR>, g1, block, smem, stream, CL,
                                  m_xp, m_wg, m_wu, m_sg, m_su, p);
     else
-        err = launch_pdl(grouped_gemm_kernel<GATEUP, Q8, CL>, g1, block, smem, stream, m_xp, m_wg,
+        err = launch_pdl(grouped_gemm_kernel<GATEUP, Q8, PAIR>, g1, block, smem, stream, m_xp, m_wg,
                          m_wu, m_sg, m_su, p);
     if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     p.K = a.F; p.n_tiles = a.d / BN;
-    const dim3 g2 = grid_for(max_groups * p.n_tiles, CL > 1 ? max_active_clusters<DOWN, Q8, CL>() : a.num_sms);
-    if (CL > 1)
-        err = launch_pdl_cluster(grouped_gemm_kernel<DOWN, Q8, CL>, g2, block, smem, stream, CL, m_h,
+    const dim3 g2 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<DOWN, Q8>() : a.num_sms);
+    if (PAIR)
+        err = launch_pdl_cluster(grouped_gemm_kernel<DOWN, Q8, PAIR>, g2, block, smem, stream, CL, m_h,
                                  m_wd, m_wd, m_sd, m_sd, p);
     else
-        err = launch_pdl(grouped_gemm_kernel<DOWN, Q8, CL>, g2, block, smem, stream, m_h, m_wd, m_wd,
+        err = launch_pdl(grouped_gemm_kernel<DOWN, Q8, PAIR>, g2, block, smem, stream, m_h, m_wd, m_wd,
                          m_sd, m_sd, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
@@ -717,14 +788,12 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
 
     // pairs of CTAs when clusters of two can be resident, else single CTAs
-    const bool pair = (q8 ? max_active_clusters<GATEUP, true, kCluster>()
-                          : max_active_clusters<GATEUP, false, kCluster>()) > 0;
-    const int CLr = pair ? kCluster : 1;
+    const bool pair = tc_gemm_pairs(a.w_dt);
 
     // activations: bf16, or fp16 on the Q8_0 path
     const CUtensorMapDataType act = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t gu_rows = (uint64_t)a.E * a.F, d_rows = (uint64_t)a.E * a.d;
-    const uint32_t wd_box = (uint32_t)(BN / CLr);   // a pair fetches W_d in two 128-row halves
+    const uint32_t wd_box = (uint32_t)(pair ? BN / 2 : BN);   // each CTA of a pair: 128 rows of W_d
     CUtensorMap m_xp, m_wg, m_wu, m_h, m_wd;
     bool ok = make_map(&m_xp, a.xp, rows, a.d, BM, act) && make_map(&m_h, a.h, rows, a.F, BM, act);
     if (q8) {
@@ -764,10 +833,13 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     p.out_zero = a.zero_out ? a.out : nullptr;
     p.zero4 = (long long)a.T * a.d / 4;
     if (q8)
-        return pair ? launch_pair<true, kCluster>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
-                    : launch_pair<true, 1>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
-    return pair ? launch_pair<false, kCluster>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
-                : launch_pair<false, 1>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+        return pair ? launch_gemms<true, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                    : launch_gemms<true, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+    if constexpr (MOE_GEMM_PAIR >= 2) {
+        if (pair)
+            return launch_gemms<false, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+    }
+    return launch_gemms<false, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
 }
 
 }  // namespace moe

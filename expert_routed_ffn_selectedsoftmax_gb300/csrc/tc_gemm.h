@@ -41,6 +41,8 @@ bool tc_gemm_available();
 bool tc_gemm_supports(moe_dtype w_dt);
 // Shape heuristic: prefer the grouped GEMMs over the decode kernels.
 bool tc_gemm_prefer(int T, int d, int E, int k, int F);
+// True when the grouped GEMMs for weights of type w_dt run as CTA pairs.
+bool tc_gemm_pairs(moe_dtype w_dt);
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream);
 
 }  // namespace moe
