@@ -60,7 +60,7 @@ using namespace sm100;
 #define MOE_DTC_CTAS_PER_SM 2
 #endif
 #ifndef MOE_DTC_TARGET_ITEMS
-#define MOE_DTC_TARGET_ITEMS 608
+#define MOE_DTC_TARGET_ITEMS 304
 #endif
 
 constexpr int BM = 128, BK = 64, STAGES = MOE_DTC_STAGES;
@@ -74,7 +74,7 @@ constexpr int THREADS = 192;
 constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
 constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
 constexpr int TMEM_COLS = 128;
-constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~4 items per SM on 152 SMs
+constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~1 item per CTA: 2 CTAs per SM on 152 SMs
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
@@ -420,56 +420,97 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
     }
 }
 
-// h[row, f] = SiLU(sum_s G[s][row][f]) * sum_s U[s][row][f], bf16 (fixed order)
-__global__ void swiglu_reduce_kernel(const float *__restrict__ pgu, int KS, int rows, int F,
-                                     uint16_t *__restrict__ h, const uint32_t *status)
+// The split-K reductions below give each group of 32 float4 columns a block
+// of 32 x SL threads: warp sl sums splits sl, sl + SL, ... (loads unrolled so
+// several are in flight), and the block adds the SL warps' sums in warp
+// order.  The order depends only on (KS, SL), never on which tokens a row
+// holds, so results are deterministic and permutation-equivariant.
+constexpr int kSplitLanes = 8;
+
+// h[row, f] = SiLU(sum_s G[s][row][f]) * sum_s U[s][row][f], bf16
+__global__ void __launch_bounds__(32 * kSplitLanes)
+swiglu_reduce_kernel(const float *__restrict__ pgu, int KS, int rows, int F,
+                     uint16_t *__restrict__ h, const uint32_t *status)
 {
     pdl_enter();
     if (upstream_failed(status)) return;
-    const int vec = F / 4;
-    const long long total = (long long)rows * vec;
+    __shared__ float4 sg[kSplitLanes][32], su[kSplitLanes][32];
+    const int lane = threadIdx.x, sl = threadIdx.y, SL = blockDim.y;
+    const long long total = (long long)rows * (F / 4);
     const size_t mat = (size_t)rows * F;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const size_t o = (size_t)i * 4;
+    for (long long base = blockIdx.x * 32LL; base < total; base += gridDim.x * 32LL) {
+        const long long i = base + lane;
         float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-        for (int s = 0; s < KS; ++s) {
-            const float4 a = __ldcg(reinterpret_cast<const float4 *>(pgu + (size_t)(2 * s) * mat + o));
-            const float4 b = __ldcg(reinterpret_cast<const float4 *>(pgu + (size_t)(2 * s + 1) * mat + o));
-            g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
-            u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+        if (i < total) {
+            const size_t o = (size_t)i * 4;
+#pragma unroll 4
+            for (int s = sl; s < KS; s += SL) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(pgu + (size_t)(2 * s) * mat + o));
+                const float4 b = __ldcg(reinterpret_cast<const float4 *>(pgu + (size_t)(2 * s + 1) * mat + o));
+                g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+                u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+            }
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(silu_f(g.x) * u.x, silu_f(g.y) * u.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(silu_f(g.z) * u.z, silu_f(g.w) * u.w);
-        uint2 packed = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-        *reinterpret_cast<uint2 *>(h + o) = packed;
+        sg[sl][lane] = g;
+        su[sl][lane] = u;
+        __syncthreads();
+        if (sl == 0 && i < total) {
+            for (int w = 1; w < SL; ++w) {
+                const float4 a = sg[w][lane], b = su[w][lane];
+                g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+                u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+            }
+            __nv_bfloat162 lo = __floats2bfloat162_rn(silu_f(g.x) * u.x, silu_f(g.y) * u.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+            uint2 packed = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            *reinterpret_cast<uint2 *>(h + (size_t)i * 4) = packed;
+        }
+        __syncthreads();
     }
 }
 
-// out[t, :] = sum_j w[t, j] * sum_s Pd[s][inv[t, j]][:]   (fixed order)
-__global__ void combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
-                               const int32_t *__restrict__ inv, const float *__restrict__ topk_w,
-                               int T, int k, float *__restrict__ out, const uint32_t *status)
+// out[t, :] = sum_j w[t, j] * sum_s Pd[s][inv[t, j]][:]   (fixed order: see above)
+__global__ void __launch_bounds__(32 * kSplitLanes)
+combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
+               const int32_t *__restrict__ inv, const float *__restrict__ topk_w,
+               int T, int k, float *__restrict__ out, const uint32_t *status)
 {
     pdl_enter();
     if (upstream_failed(status)) return;
+    __shared__ float4 sy[kSplitLanes][kMaxTopK][32];
+    const int lane = threadIdx.x, sl = threadIdx.y, SL = blockDim.y;
     const int vec = d / 4;
     const long long total = (long long)T * vec;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+    for (long long base = blockIdx.x * 32LL; base < total; base += gridDim.x * 32LL) {
+        const long long i = base + lane;
         const int t = (int)(i / vec), o = (int)(i - (long long)t * vec) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int r = inv[t * k + j];
-            const float w = topk_w[t * k + j];
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < KS; ++s) {
-                const float4 v = *reinterpret_cast<const float4 *>(pd + ((size_t)s * rows_total + r) * d + o);
-                y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+        if (i < total) {
+            for (int j = 0; j < k; ++j) {
+                const int r = inv[t * k + j];
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                for (int s = sl; s < KS; s += SL) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(pd + ((size_t)s * rows_total + r) * d + o));
+                    y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+                }
+                sy[sl][j][lane] = y;
             }
-            acc.x += w * y.x; acc.y += w * y.y; acc.z += w * y.z; acc.w += w * y.w;
         }
-        *reinterpret_cast<float4 *>(out + (size_t)t * d + o) = acc;
+        __syncthreads();
+        if (sl == 0 && i < total) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < k; ++j) {
+                float4 y = sy[0][j][lane];
+                for (int w = 1; w < SL; ++w) {
+                    const float4 v = sy[w][j][lane];
+                    y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+                }
+                const float wt = topk_w[t * k + j];
+                acc.x += wt * y.x; acc.y += wt * y.y; acc.z += wt * y.z; acc.w += wt * y.w;
+            }
+            *reinterpret_cast<float4 *>(out + (size_t)t * d + o) = acc;
+        }
+        __syncthreads();
     }
 }
 
@@ -593,14 +634,17 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
                    m_x32, p);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    auto elementwise_grid = [&](long long total) {
-        long long blocks = (total + 255) / 256;
-        if (blocks > (long long)a.num_sms * 8) blocks = (long long)a.num_sms * 8;
+    // split-K reductions: blocks of 32 float4 columns x min(KS, 8) split lanes
+    auto reduce_block = [](int ks) { return dim3(32, ks < kSplitLanes ? (ks < 1 ? 1 : ks) : kSplitLanes); };
+    auto reduce_grid = [&](long long total, int ks) {
+        long long blocks = (total + 31) / 32;
+        const long long cap = (long long)a.num_sms * (64 / reduce_block(ks).y) * 4;
+        if (blocks > cap) blocks = cap;
         return (int)(blocks < 1 ? 1 : blocks);
     };
     if (!fused) {
-        launch_pdl(swiglu_reduce_kernel, dim3(elementwise_grid((long long)rows * (a.F / 4))), dim3(256), 0,
-                   stream, a.pgu, ks_gu, rows, a.F, a.h, a.status);
+        launch_pdl(swiglu_reduce_kernel, dim3(reduce_grid((long long)rows * (a.F / 4), ks_gu)), reduce_block(ks_gu),
+                   0, stream, a.pgu, ks_gu, rows, a.F, a.h, a.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
@@ -619,7 +663,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (direct) return cudaSuccess;
 
-    launch_pdl(combine_kernel, dim3(elementwise_grid((long long)a.T * (a.d / 4))), dim3(256), 0, stream,
+    launch_pdl(combine_kernel, dim3(reduce_grid((long long)a.T * (a.d / 4), ks_d)), reduce_block(ks_d), 0, stream,
         a.pd, ks_d, rows, a.d, a.inv, a.topk_w, a.T, a.k, a.out, a.status);
     return cudaGetLastError();
 }
