@@ -134,6 +134,8 @@ SMALL = [
     (wl.BF16, wl.Q8_0, 45, 256, 8, 2, 160),
     (wl.BF16, wl.Q8_0, 3, 2048, 16, 1, 2816),
     (wl.BF16, wl.BF16, 96, 256, 4, 4, 128),     # k == E: dense gating
+    (wl.BF16, wl.BF16, 5, 512, 64, 8, 128),     # few tokens: largest E and k of the small-batch router
+    (wl.BF16, wl.BF16, 8, 2048, 33, 3, 128),    # few tokens: ragged E, longest rows
 ]
 
 
