@@ -54,8 +54,12 @@ def _load():
         lib.oracle_expert_combine.argtypes = [vp, i, i, i, vp, dp, i, vp, vp, vp, i, i, i, dp, i]
         lib.oracle_moe_forward.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, dp,
                                            vp, dp, dp, i]
+        lib.oracle_route_scored.argtypes = [dp, vp, i, i, i, i, vp, dp, dp]
+        lib.oracle_moe_forward_scored.argtypes = [vp, i, i, i, vp, vp, i, i, i, vp, vp, vp, i, i,
+                                                  dp, vp, dp, dp, i]
         for name in ("oracle_router_logits", "oracle_selected_softmax", "oracle_softmax_of_set",
-                     "oracle_permute", "oracle_expert_combine", "oracle_moe_forward"):
+                     "oracle_permute", "oracle_expert_combine", "oracle_moe_forward",
+                     "oracle_route_scored", "oracle_moe_forward_scored"):
             getattr(lib, name).restype = i
         _lib = lib
     return _lib
@@ -100,6 +104,24 @@ def selected_softmax(logits, bias, k: int):
     return idx, w, margin
 
 
+# scoring modes (oracle_route_scored): SelectedSoftmax, softmax before rank,
+# sigmoid before rank
+SELECTED_SOFTMAX, SOFTMAX, SIGMOID = 0, 1, 2
+
+
+def route_scored(logits, bias, k: int, mode: int):
+    """Routing in scoring mode `mode`: (topk_idx [T,k], topk_w [T,k], margin [T])."""
+    logits = _c(logits, np.float64)
+    T, E = logits.shape
+    b = _c(bias, np.float32)
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    margin = np.empty(T, dtype=np.float64)
+    _check(_load().oracle_route_scored(_p(logits), _p(b), T, E, k, mode, _p(idx), _p(w),
+                                       _p(margin)), "route_scored")
+    return idx, w, margin
+
+
 def softmax_of_set(logits, topk_idx) -> np.ndarray:
     logits = _c(logits, np.float64)
     idx = _c(topk_idx, np.int32)
@@ -137,8 +159,9 @@ def expert_combine(x, act_dtype: int, topk_idx, topk_w, w_gate, w_up, w_down, w_
     return out
 
 
-def moe_forward(layer, nthreads: int = 0):
-    """Whole layer on a workloads.Layer.  Returns (out, topk_idx, topk_w, margin)."""
+def moe_forward(layer, nthreads: int = 0, mode: int = SELECTED_SOFTMAX):
+    """Whole layer on a workloads.Layer in scoring mode `mode`.  Returns (out,
+    topk_idx, topk_w, margin)."""
     x = _c(layer.x)
     T, d = x.shape
     E, k, F = layer.E, layer.k, layer.F
@@ -148,7 +171,8 @@ def moe_forward(layer, nthreads: int = 0):
     margin = np.empty(T, dtype=np.float64)
     wr, b = _c(layer.w_router), _c(layer.bias, np.float32)
     wg, wu, wd = _c(layer.w_gate), _c(layer.w_up), _c(layer.w_down)
-    _check(_load().oracle_moe_forward(_p(x), layer.act_dtype, T, d, _p(wr), _p(b), E, k,
-                                      _p(wg), _p(wu), _p(wd), layer.w_dtype, F, _p(out),
-                                      _p(idx), _p(w), _p(margin), nthreads), "moe_forward")
+    _check(_load().oracle_moe_forward_scored(_p(x), layer.act_dtype, T, d, _p(wr), _p(b), E, k,
+                                             mode, _p(wg), _p(wu), _p(wd), layer.w_dtype, F,
+                                             _p(out), _p(idx), _p(w), _p(margin), nthreads),
+           "moe_forward")
     return out, idx, w, margin

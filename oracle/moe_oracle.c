@@ -211,6 +211,66 @@ int oracle_selected_softmax(const double *logits, const float *bias, int T, int 
     return 0;
 }
 
+/* ------------------------------ other scoring modes: activation before rank
+ * "New Community Model: ZONOS3-Mini (Zyphra) - #1271", §Framework change: the
+ * framework's older modes apply a softmax or a sigmoid to the router logits
+ * before ranking, and so weigh the experts differently from SelectedSoftmax.
+ * The pages give no formulas; the reading taken here:
+ *   p = softmax over all E logits (mode 1) or p = sigmoid(logit) (mode 2);
+ *   ranking score = p + selection bias; top k, higher first, lower index on ties;
+ *   weights = p of the selected experts, not renormalised (renormalised
+ *   softmax-before-rank weights would equal SelectedSoftmax's).
+ * Mode 0 is SelectedSoftmax. */
+int oracle_route_scored(const double *logits, const float *bias, int T, int E, int k, int mode,
+                        int32_t *topk_idx, double *topk_w, double *margin)
+{
+    if (mode == 0) return oracle_selected_softmax(logits, bias, T, E, k, topk_idx, topk_w, margin);
+    if (T < 0 || E <= 0 || k < 1 || k > E || (mode != 1 && mode != 2)) return -1;
+    double *prob = (double *)malloc(sizeof(double) * (size_t)E);
+    double *score = (double *)malloc(sizeof(double) * (size_t)E);
+    char *taken = (char *)malloc((size_t)E);
+    for (int t = 0; t < T; ++t) {
+        const double *l = logits + (size_t)t * E;
+        if (mode == 1) {
+            double m = -INFINITY;
+            for (int e = 0; e < E; ++e) if (l[e] > m) m = l[e];
+            double den = 0.0;
+            for (int e = 0; e < E; ++e) den += exp(l[e] - m);
+            for (int e = 0; e < E; ++e) prob[e] = exp(l[e] - m) / den;
+        } else {
+            for (int e = 0; e < E; ++e) prob[e] = 1.0 / (1.0 + exp(-l[e]));
+        }
+        for (int e = 0; e < E; ++e) score[e] = prob[e] + (bias ? (double)bias[e] : 0.0);
+        memset(taken, 0, (size_t)E);
+        double kth = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || score[e] > score[best]) best = e;
+            }
+            taken[best] = 1;
+            topk_idx[(size_t)t * k + j] = best;
+            topk_w[(size_t)t * k + j] = prob[best];
+            kth = score[best];
+        }
+        if (margin) {
+            if (k == E) {
+                margin[t] = INFINITY;
+            } else {
+                double next = -INFINITY;
+                for (int e = 0; e < E; ++e)
+                    if (!taken[e] && score[e] > next) next = score[e];
+                margin[t] = kth - next;
+            }
+        }
+    }
+    free(taken);
+    free(score);
+    free(prob);
+    return 0;
+}
+
 int oracle_softmax_of_set(const double *logits, int T, int E, int k, const int32_t *topk_idx,
                           double *topk_w)
 {
@@ -324,11 +384,20 @@ int oracle_moe_forward(const void *x, int x_dt, int T, int d, const void *w_rout
                        const void *w_down, int w_dt, int F, double *out, int32_t *topk_idx,
                        double *topk_w, double *margin, int nthreads)
 {
+    return oracle_moe_forward_scored(x, x_dt, T, d, w_router, bias, E, k, 0, w_gate, w_up,
+                                     w_down, w_dt, F, out, topk_idx, topk_w, margin, nthreads);
+}
+
+int oracle_moe_forward_scored(const void *x, int x_dt, int T, int d, const void *w_router,
+                              const float *bias, int E, int k, int mode, const void *w_gate,
+                              const void *w_up, const void *w_down, int w_dt, int F, double *out,
+                              int32_t *topk_idx, double *topk_w, double *margin, int nthreads)
+{
     if (T < 0 || k < 1 || k > E) return -1;
     if (T == 0) return 0;
     double *logits = (double *)malloc(sizeof(double) * (size_t)T * E);
     int rc = oracle_router_logits(x, x_dt, T, d, w_router, E, logits, nthreads);
-    if (rc == 0) rc = oracle_selected_softmax(logits, bias, T, E, k, topk_idx, topk_w, margin);
+    if (rc == 0) rc = oracle_route_scored(logits, bias, T, E, k, mode, topk_idx, topk_w, margin);
     if (rc == 0)
         rc = oracle_expert_combine(x, x_dt, T, d, topk_idx, topk_w, k, w_gate, w_up, w_down,
                                    w_dt, E, F, out, nthreads);

@@ -34,6 +34,13 @@ int oracle_router_logits(const void *x, int x_dt, int T, int d, const void *w_ro
 int oracle_selected_softmax(const double *logits, const float *bias, int T, int E, int k,
                             int32_t *topk_idx, double *topk_w, double *margin);
 
+/* Scoring mode 0: SelectedSoftmax (as above).  Mode 1 / 2: p = softmax over
+ * all E logits / sigmoid of each logit; top-k of p + bias (ties -> lower
+ * index); weights = p of the selected experts (not renormalised); margin on
+ * p + bias. */
+int oracle_route_scored(const double *logits, const float *bias, int T, int E, int k, int mode,
+                        int32_t *topk_idx, double *topk_w, double *margin);
+
 /* Weights for a given selected set: softmax of logits over topk_idx[t,:]. */
 int oracle_softmax_of_set(const double *logits, int T, int E, int k, const int32_t *topk_idx,
                           double *topk_w);
@@ -55,6 +62,12 @@ int oracle_moe_forward(const void *x, int x_dt, int T, int d, const void *w_rout
                        const float *bias, int E, int k, const void *w_gate, const void *w_up,
                        const void *w_down, int w_dt, int F, double *out, int32_t *topk_idx,
                        double *topk_w, double *margin, int nthreads);
+
+/* Whole layer with scoring mode `mode` (see oracle_route_scored). */
+int oracle_moe_forward_scored(const void *x, int x_dt, int T, int d, const void *w_router,
+                              const float *bias, int E, int k, int mode, const void *w_gate,
+                              const void *w_up, const void *w_down, int w_dt, int F, double *out,
+                              int32_t *topk_idx, double *topk_w, double *margin, int nthreads);
 
 #ifdef __cplusplus
 }

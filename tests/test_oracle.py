@@ -300,3 +300,117 @@ def test_multithreaded_equals_single_threaded():
     b = oracle.moe_forward(layer, nthreads=7)
     for u, v in zip(a, b):
         assert np.array_equal(u, v)
+
+
+# ---------------------------------------------- other scoring modes (next row f1)
+# "New Community Model: ZONOS3-Mini (Zyphra) - #1271", §Framework change: the
+# older modes apply a softmax or a sigmoid before ranking.  Reading (the pages
+# give no formulas): p = softmax over all experts / sigmoid per expert, rank by
+# p + bias, weigh by p of the selected experts, no renormalisation.
+
+def _softmax_rows(l):
+    from scipy.special import softmax
+    return softmax(l, axis=1)
+
+
+def _sigmoid(l):
+    from scipy.special import expit
+    return expit(l)
+
+
+@pytest.mark.parametrize("k", [1, 2, 5])
+def test_softmax_mode_weights_are_library_softmax_of_selected(k):
+    rng = np.random.default_rng(40 + k)
+    lg = rng.standard_normal((64, 12)) * 2.0
+    b = (rng.standard_normal(12) * 0.05).astype(np.float32)
+    idx, w, _ = oracle.route_scored(lg, b, k, oracle.SOFTMAX)
+    p = _softmax_rows(lg)
+    assert np.allclose(w, np.take_along_axis(p, idx, axis=1), rtol=0, atol=1e-15)
+    # ranking: top-k of p + bias (library sort, ties to the lower index)
+    s = p + b.astype(np.float64)
+    ref = np.array([sorted(range(12), key=lambda e: (-s[t, e], e))[:k] for t in range(64)])
+    assert np.array_equal(idx, ref)
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_sigmoid_mode_weights_are_library_sigmoid(k):
+    rng = np.random.default_rng(50 + k)
+    lg = rng.standard_normal((64, 10)) * 3.0
+    b = (rng.standard_normal(10) * 0.1).astype(np.float32)
+    idx, w, _ = oracle.route_scored(lg, b, k, oracle.SIGMOID)
+    sel = np.take_along_axis(lg, idx, axis=1)
+    assert np.allclose(w, _sigmoid(sel), rtol=1e-15, atol=0)
+    s = _sigmoid(lg) + b.astype(np.float64)
+    ref = np.array([sorted(range(10), key=lambda e: (-s[t, e], e))[:k] for t in range(64)])
+    assert np.array_equal(idx, ref)
+
+
+def test_scoring_modes_zero_bias_same_set_as_selected_softmax():
+    """Softmax and sigmoid are increasing, so with no bias every mode picks the
+    same experts; softmax-mode weights are SelectedSoftmax's scaled by the
+    selected experts' share of the full softmax."""
+    rng = np.random.default_rng(60)
+    lg = rng.standard_normal((100, 16))
+    z = np.zeros(16, np.float32)
+    i0, w0, _ = oracle.route_scored(lg, z, 3, oracle.SELECTED_SOFTMAX)
+    i1, w1, _ = oracle.route_scored(lg, z, 3, oracle.SOFTMAX)
+    i2, _, _ = oracle.route_scored(lg, z, 3, oracle.SIGMOID)
+    assert np.array_equal(i0, i1) and np.array_equal(i0, i2)
+    share = np.take_along_axis(_softmax_rows(lg), i0, axis=1).sum(axis=1, keepdims=True)
+    assert np.allclose(w1, w0 * share, rtol=1e-13, atol=0)
+    assert np.all(w1.sum(axis=1) < 1.0)   # not renormalised
+
+
+def test_scoring_modes_rank_probabilities_plus_bias_worked_example():
+    """Hand-derived: logits (0, 2, 3), bias (0.8, 0, 0), k = 1.  SelectedSoftmax
+    ranks 0.8 < 2 < 3 and picks expert 2 (weight 1).  Softmax before rank:
+    p = (1, e^2, e^3) / (1 + e^2 + e^3) = (0.03512, 0.25950, 0.70538), plus bias
+    (0.83512, 0.25950, 0.70538): expert 0, weight 0.03512.  Sigmoid before rank:
+    p = (0.5, 0.88080, 0.95257), plus bias (1.3, ...): expert 0, weight 1/2."""
+    lg = np.array([[0.0, 2.0, 3.0]])
+    b = np.array([0.8, 0.0, 0.0], np.float32)
+    i0, w0, _ = oracle.route_scored(lg, b, 1, oracle.SELECTED_SOFTMAX)
+    assert i0[0, 0] == 2 and w0[0, 0] == 1.0
+    i1, w1, m1 = oracle.route_scored(lg, b, 1, oracle.SOFTMAX)
+    assert i1[0, 0] == 0 and abs(w1[0, 0] - 0.0351190) < 1e-6
+    assert abs(m1[0] - (0.8 + 0.0351190 - 0.7053845)) < 1e-6   # margin on p + bias
+    i2, w2, _ = oracle.route_scored(lg, b, 1, oracle.SIGMOID)
+    assert i2[0, 0] == 0 and w2[0, 0] == 0.5
+
+
+def test_softmax_mode_k_equals_e_is_dense_softmax_and_bias_only_selects():
+    rng = np.random.default_rng(70)
+    lg = rng.standard_normal((20, 6))
+    b = (rng.standard_normal(6) * 5).astype(np.float32)
+    idx, w, margin = oracle.route_scored(lg, b, 6, oracle.SOFTMAX)
+    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-15) and np.all(np.isinf(margin))
+    # two different biases forcing the same set {1, 4}: identical weights
+    f1 = np.array([0, 9, 0, 0, 8, 0], np.float32)
+    f2 = np.array([0, 50, 0, 0, 40, 0], np.float32)
+    for mode in (oracle.SOFTMAX, oracle.SIGMOID):
+        ia, wa, _ = oracle.route_scored(lg, f1, 2, mode)
+        ib, wb, _ = oracle.route_scored(lg, f2, 2, mode)
+        assert np.array_equal(ia, ib) and np.all(ia == [1, 4]) and np.array_equal(wa, wb)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("k", [1, 2])
+def test_scoring_modes_layer_matches_dense_brute_force(mode, k):
+    layer = tiny_layer(seed=80 + k, k=k, bias_sd=0.2)
+    out, idx, w, _ = oracle.moe_forward(layer, mode=mode)
+    x = decode(layer.x, layer.act_dtype)
+    wr = decode(layer.w_router, layer.act_dtype)
+    lg = x @ wr.T
+    p = _softmax_rows(lg) if mode == 1 else _sigmoid(lg)
+    s = p + np.asarray(layer.bias, np.float64)
+    wg = decode(layer.w_gate, layer.w_dtype)
+    wu = decode(layer.w_up, layer.w_dtype)
+    wd = decode(layer.w_down, layer.w_dtype)
+    g = np.einsum("efi,ti->etf", wg, x)
+    u = np.einsum("efi,ti->etf", wu, x)
+    y = np.einsum("eif,etf->eti", wd, g / (1.0 + np.exp(-g)) * u)
+    ref = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        for e in sorted(range(layer.E), key=lambda e: (-s[t, e], e))[:k]:
+            ref[t] += p[t, e] * y[e, t]
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
