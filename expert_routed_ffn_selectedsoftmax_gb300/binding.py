@@ -17,14 +17,15 @@ from . import build as _build
 
 MOE_F32, MOE_BF16, MOE_Q8_0 = 0, 1, 2
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_PATH_DECODE_SIMT = 0, 1, 2, 3
+MOE_SCORE_SELECTED_SOFTMAX, MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
           6: "MOE_ERR_DEVICE_CHECK"}
 
 # Every symbol include/moe.h declares.
-EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_permute",
+EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "moe_permute",
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_workspace_size", "moe_forward",
-           "moe_forward_profiled", "moe_forward_noalloc", "moe_check")
+           "moe_forward_profiled", "moe_forward_scored", "moe_forward_noalloc", "moe_check")
 
 _lib = None
 
@@ -58,6 +59,8 @@ def load_library():
     L.moe_version.restype = i
     L.moe_route.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp]
     L.moe_route.restype = i
+    L.moe_route_scored.argtypes = [vp, i, i, i, vp, vp, i, i, i, vp, vp, vp]
+    L.moe_route_scored.restype = i
     L.moe_permute.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp]
     L.moe_permute.restype = i
     L.moe_q8_0_packed_size.argtypes = [ll, i]
@@ -71,6 +74,9 @@ def load_library():
     L.moe_forward_profiled.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz,
                                        i, vp, vp]
     L.moe_forward_profiled.restype = i
+    L.moe_forward_scored.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz,
+                                     i, i, vp, vp]
+    L.moe_forward_scored.restype = i
     L.moe_forward_noalloc.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, i, vp]
     L.moe_forward_noalloc.restype = i
     L.moe_check.argtypes = [vp, vp, vp]
@@ -101,8 +107,10 @@ def _check(status: int, where: str):
 
 
 def moe_route(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torch.Tensor], k: int,
-              topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None):
-    """Router projection + SelectedSoftmax -> (topk_idx int32 [T,k], topk_w fp32 [T,k])."""
+              topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
+              scoring: int = MOE_SCORE_SELECTED_SOFTMAX):
+    """Router projection + scoring (SelectedSoftmax by default) -> (topk_idx int32
+    [T,k], topk_w fp32 [T,k])."""
     L = load_library()
     T, d = x.shape
     E = w_router.shape[0]
@@ -110,8 +118,13 @@ def moe_route(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torch.
         topk_idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
     if topk_w is None:
         topk_w = torch.empty((T, k), dtype=torch.float32, device=x.device)
-    _check(L.moe_route(_ptr(x), _act_dtype(x), T, d, _ptr(w_router), _ptr(sel_bias), E, k,
-                       _ptr(topk_idx), _ptr(topk_w), _stream(x)), "moe_route")
+    if scoring == MOE_SCORE_SELECTED_SOFTMAX:
+        _check(L.moe_route(_ptr(x), _act_dtype(x), T, d, _ptr(w_router), _ptr(sel_bias), E, k,
+                           _ptr(topk_idx), _ptr(topk_w), _stream(x)), "moe_route")
+    else:
+        _check(L.moe_route_scored(_ptr(x), _act_dtype(x), T, d, _ptr(w_router), _ptr(sel_bias),
+                                  E, k, scoring, _ptr(topk_idx), _ptr(topk_w), _stream(x)),
+               "moe_route_scored")
     return topk_idx, topk_w
 
 
@@ -153,13 +166,15 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
                 w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor, k: int,
                 F: Optional[int] = None, w_dtype: Optional[int] = None,
                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                path: int = MOE_PATH_AUTO, events=None) -> torch.Tensor:
+                path: int = MOE_PATH_AUTO, events=None,
+                scoring: int = MOE_SCORE_SELECTED_SOFTMAX) -> torch.Tensor:
     """The whole MoE layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [E,F,d], [E,F,d], [E,d,F]; or, with
     w_dtype=MOE_Q8_0, uint8 buffers from moe_pack_q8_0 (then F is required).
     events: optional sequence of 6 torch.cuda.Event(enable_timing=True), recorded
     at the stage boundaries (moe_forward_profiled).
+    scoring: a MOE_SCORE_* mode (moe_forward_scored when not SelectedSoftmax).
     """
     L = load_library()
     T, d = x.shape
@@ -177,7 +192,17 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
     ws_len = workspace.numel() * workspace.element_size()
-    if events is None:
+    if scoring != MOE_SCORE_SELECTED_SOFTMAX:
+        handles = None
+        if events is not None:
+            if len(events) != 6:
+                raise ValueError("events: 6 CUDA events expected")
+            handles = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
+        _check(L.moe_forward_scored(_ptr(x), act, T, d, _ptr(w_router), _ptr(sel_bias), E, k,
+                                    _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F,
+                                    _ptr(out), _ptr(workspace), ws_len, path, scoring, handles,
+                                    _stream(x)), "moe_forward_scored")
+    elif events is None:
         _check(L.moe_forward(_ptr(x), act, T, d, _ptr(w_router), _ptr(sel_bias), E, k,
                              _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F, _ptr(out),
                              _ptr(workspace), ws_len, path, _stream(x)), "moe_forward")

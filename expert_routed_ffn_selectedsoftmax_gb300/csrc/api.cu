@@ -17,6 +17,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool act_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
 
+bool scoring_ok(int scoring)
+{
+    return scoring == MOE_SCORE_SELECTED_SOFTMAX || scoring == MOE_SCORE_SOFTMAX ||
+           scoring == MOE_SCORE_SIGMOID;
+}
+
 bool weights_ok(int act_dt, int w_dt)
 {
     if (act_dt == MOE_F32) return w_dt == MOE_F32;
@@ -118,6 +124,15 @@ moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *
                      const float *sel_bias, int E, int k, int32_t *topk_idx, float *topk_w,
                      moe_stream stream)
 {
+    return moe_route_scored(x, act_dt, T, d, w_router, sel_bias, E, k, MOE_SCORE_SELECTED_SOFTMAX,
+                            topk_idx, topk_w, stream);
+}
+
+moe_status moe_route_scored(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                            const float *sel_bias, int E, int k, int scoring, int32_t *topk_idx,
+                            float *topk_w, moe_stream stream)
+{
+    if (!scoring_ok(scoring)) return MOE_ERR_INVALID_ARG;
     moe_status st = check_route_args(x, act_dt, T, d, w_router, sel_bias, E, k);
     if (st != MOE_OK) return st;
     if (T == 0) return MOE_OK;
@@ -128,11 +143,13 @@ moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *
     if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
         RouteTcArgs a{};
         a.x = x; a.w_router = w_router; a.bias = sel_bias; a.T = T; a.d = d; a.E = E; a.k = k;
+        a.mode = scoring;
         a.topk_idx = topk_idx; a.topk_w = topk_w;
         e = launch_route_tc(a, static_cast<cudaStream_t>(stream));
     } else {
         e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w, nullptr,
-                         nullptr, 0, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+                         nullptr, 0, nullptr, nullptr, nullptr, scoring,
+                         static_cast<cudaStream_t>(stream));
     }
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -192,6 +209,19 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
                                 size_t ws_bytes, int path, void *const *events,
                                 moe_stream stream)
 {
+    return moe_forward_scored(x, act_dt, T, d, w_router, sel_bias, E, k, w_gate, w_up, w_down,
+                              w_dt, F, out, workspace, ws_bytes, path, MOE_SCORE_SELECTED_SOFTMAX,
+                              events, stream);
+}
+
+moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
+                              const void *w_router, const float *sel_bias, int E, int k,
+                              const void *w_gate, const void *w_up, const void *w_down,
+                              moe_dtype w_dt, int F, float *out, void *workspace,
+                              size_t ws_bytes, int path, int scoring, void *const *events,
+                              moe_stream stream)
+{
+    if (!scoring_ok(scoring)) return MOE_ERR_INVALID_ARG;
     moe_status st = check_route_args(x, act_dt, T, d, w_router, sel_bias, E, k);
     if (st != MOE_OK) return st;
     if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
@@ -250,6 +280,7 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
     // that the tensor-core expert kernels read)
     RouteTcArgs ra{};
     ra.x = x; ra.w_router = w_router; ra.bias = sel_bias; ra.T = T; ra.d = d; ra.E = E; ra.k = k;
+    ra.mode = scoring;
     ra.topk_idx = topk_idx; ra.topk_w = topk_w;
     ra.rank = reinterpret_cast<int32_t *>(ws + L.rank);
     ra.tile_cnt = reinterpret_cast<int32_t *>(ws + L.tile_cnt);
@@ -275,7 +306,7 @@ moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, int d,
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
     } else {
         e = launch_route(x, act_dt, T, d, w_router, sel_bias, E, k, topk_idx, topk_w, ra.out_zero,
-                         ra.zero_words, ra.n_zero, ra.rank, ra.tile_cnt, status, s);
+                         ra.zero_words, ra.n_zero, ra.rank, ra.tile_cnt, status, scoring, s);
         if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
         const int tpb = route_tokens_per_block(T, d, E);
         e = launch_scatter(ra, (T + tpb - 1) / tpb, tpb, s);

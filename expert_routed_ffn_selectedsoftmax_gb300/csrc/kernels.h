@@ -18,7 +18,7 @@ int route_tokens_per_block(int T, int d, int E);
 cudaError_t launch_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                          const float *bias, int E, int k, int32_t *topk_idx, float *topk_w,
                          float *out_zero, uint32_t *zero_words, int n_zero, int32_t *rank,
-                         int32_t *tile_cnt, uint32_t *status, cudaStream_t stream);
+                         int32_t *tile_cnt, uint32_t *status, int mode, cudaStream_t stream);
 // the tensor-core router pays off from this many tokens (one 128-row tile per CTA)
 constexpr int kRouteTcMinTokens = 512;
 
@@ -28,6 +28,7 @@ struct RouteTcArgs {
     const void *w_router;       // [E, d] bf16
     const float *bias;          // [E] or NULL
     int T, d, E, k;
+    int mode;                   // scoring: 0 SelectedSoftmax, 1 softmax / 2 sigmoid before rank
     int32_t *topk_idx;          // [T*k]
     float *topk_w;              // [T*k]
     int32_t *rank;              // [T*k] scratch, or NULL (routing only)

@@ -1,5 +1,10 @@
 // route.cu -- router projection + SelectedSoftmax (steps 1-2 of the layer).
 //
+// Scoring modes (same section): mode 0 is SelectedSoftmax; modes 1 and 2
+// apply a softmax over all experts / a sigmoid to the logits first, rank by
+// that probability plus the bias and weigh by the probability (no
+// renormalisation).
+//
 // SelectedSoftmax ("New Community Model: ZONOS3-Mini (Zyphra) - #1271",
 // §Framework change): experts are ranked by raw router logit plus a
 // per-expert selection bias; the top k are kept; the kept experts are weighted
@@ -69,7 +74,7 @@ route_kernel(const AT *__restrict__ x, int T, int d, const AT *__restrict__ w_ro
              const float *__restrict__ bias, int E, int k, int32_t *__restrict__ topk_idx,
              float *__restrict__ topk_w, float *__restrict__ out_zero,
              uint32_t *__restrict__ zero_words, int n_zero, int32_t *__restrict__ rank,
-             int32_t *__restrict__ tile_cnt, uint32_t *__restrict__ status)
+             int32_t *__restrict__ tile_cnt, uint32_t *__restrict__ status, int mode)
 {
     pdl_enter();
     extern __shared__ float4 smem_f4[];
@@ -154,18 +159,41 @@ route_kernel(const AT *__restrict__ x, int T, int d, const AT *__restrict__ w_ro
     }
     __syncthreads();
 
-    // SelectedSoftmax: one warp per token
+    // ranking and weights: one warp per token.  lg holds what the weights are
+    // made of: the logit (mode 0, softmax over the selected later) or the
+    // probability (modes 1, 2)
     for (int t = warp; t < ntok; t += kRouteWarps) {
         float sc[8], lg[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             int e = lane + 32 * s;
+            lg[s] = e < E ? logit[t * E + e] : 0.f;
+        }
+        if (mode == 1) {   // softmax over all E: lane partials, xor-shuffle trees
+            float m = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (lane + 32 * s < E) m = fmaxf(m, lg[s]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float den = 0.f;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (lane + 32 * s < E) den += expf(lg[s] - m);
+            den = warp_sum(den);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) lg[s] = expf(lg[s] - m) / den;
+        } else if (mode == 2) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) lg[s] = 1.0f / (1.0f + expf(-lg[s]));
+        }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            int e = lane + 32 * s;
             if (e < E) {
-                lg[s] = logit[t * E + e];
                 sc[s] = lg[s] + (bias ? bias[e] : 0.f);
                 if (isnan(sc[s])) sc[s] = -INFINITY;   // keep the ranking a total order
             } else {
-                lg[s] = 0.f;
                 sc[s] = -INFINITY;
             }
         }
@@ -197,14 +225,19 @@ route_kernel(const AT *__restrict__ x, int T, int d, const AT *__restrict__ w_ro
             sel_l[j] = bl;
         }
         if (lane == 0) {
-            float m = sel_l[0];
-            for (int j = 1; j < k; ++j) m = fmaxf(m, sel_l[j]);
-            float p[kMaxTopK], den = 0.f;
-            for (int j = 0; j < k; ++j) { p[j] = expf(sel_l[j] - m); den += p[j]; }
+            float p[kMaxTopK], den = 1.f;
+            if (mode == 0) {   // softmax over the selected logits
+                float m = sel_l[0];
+                for (int j = 1; j < k; ++j) m = fmaxf(m, sel_l[j]);
+                den = 0.f;
+                for (int j = 0; j < k; ++j) { p[j] = expf(sel_l[j] - m); den += p[j]; }
+            } else {
+                for (int j = 0; j < k; ++j) p[j] = sel_l[j];
+            }
             const size_t base = (size_t)(t0 + t) * k;
             for (int j = 0; j < k; ++j) {
                 topk_idx[base + j] = sel_e[j];
-                topk_w[base + j] = p[j] / den;
+                topk_w[base + j] = mode == 0 ? p[j] / den : p[j];
                 sel_s[t][j] = sel_e[j];
             }
         }
@@ -247,7 +280,7 @@ static cudaError_t launch_route_t(const void *x, int T, int d, const void *w_rou
                                   const float *bias, int E, int k, int32_t *topk_idx,
                                   float *topk_w, float *out_zero, uint32_t *zero_words,
                                   int n_zero, int32_t *rank, int32_t *tile_cnt, uint32_t *status,
-                                  cudaStream_t stream)
+                                  int mode, cudaStream_t stream)
 {
     size_t smem = route_smem_bytes(TPB, d, E);
     auto kern = route_kernel<AT, TPB>;
@@ -260,29 +293,29 @@ static cudaError_t launch_route_t(const void *x, int T, int d, const void *w_rou
     launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, stream, static_cast<const AT *>(x), T, d,
                                                  static_cast<const AT *>(w_router), bias, E, k,
                                                  topk_idx, topk_w, out_zero, zero_words, n_zero,
-                                                 rank, tile_cnt, status);
+                                                 rank, tile_cnt, status, mode);
     return cudaGetLastError();
 }
 
 cudaError_t launch_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                          const float *bias, int E, int k, int32_t *topk_idx, float *topk_w,
                          float *out_zero, uint32_t *zero_words, int n_zero, int32_t *rank,
-                         int32_t *tile_cnt, uint32_t *status, cudaStream_t stream)
+                         int32_t *tile_cnt, uint32_t *status, int mode, cudaStream_t stream)
 {
     int tpb = route_tokens_per_block(T, d, E);
     if (act_dt == MOE_F32) {
         switch (tpb) {
-        case 8: return launch_route_t<float, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
-        case 4: return launch_route_t<float, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
-        case 2: return launch_route_t<float, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
-        default: return launch_route_t<float, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+        case 8: return launch_route_t<float, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
+        case 4: return launch_route_t<float, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
+        case 2: return launch_route_t<float, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
+        default: return launch_route_t<float, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
         }
     }
     switch (tpb) {
-    case 8: return launch_route_t<__nv_bfloat16, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
-    case 4: return launch_route_t<__nv_bfloat16, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
-    case 2: return launch_route_t<__nv_bfloat16, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
-    default: return launch_route_t<__nv_bfloat16, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, stream);
+    case 8: return launch_route_t<__nv_bfloat16, 8>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
+    case 4: return launch_route_t<__nv_bfloat16, 4>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
+    case 2: return launch_route_t<__nv_bfloat16, 2>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
+    default: return launch_route_t<__nv_bfloat16, 1>(x, T, d, w_router, bias, E, k, topk_idx, topk_w, out_zero, zero_words, n_zero, rank, tile_cnt, status, mode, stream);
     }
 }
 

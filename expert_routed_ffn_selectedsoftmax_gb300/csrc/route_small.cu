@@ -4,7 +4,9 @@
 // SelectedSoftmax ("New Community Model: ZONOS3-Mini (Zyphra) - #1271",
 // §Framework change): rank experts by router logit plus selection bias, keep
 // the top k, weight them by the softmax of their unbiased logits; ties in the
-// ranking score go to the lower expert index.  Grouping: the slots of each
+// ranking score go to the lower expert index.  Scoring modes 1 and 2 (same
+// section): rank by softmax-over-all-experts / sigmoid probability plus the
+// bias and weigh by that probability (no renormalisation).  Grouping: the slots of each
 // expert in increasing token order (stable), rows offset by the exclusive
 // scan of the per-expert counts.
 //
@@ -61,6 +63,7 @@ __host__ __device__ constexpr int b_tile_bytes(int EP) { return (EP * BK * 2 + 1
 
 struct Params {
     int T, d, E, EP, k, R, kblocks, box_rows, tpc;
+    int mode;                            // scoring: 0 SelectedSoftmax, 1 softmax / 2 sigmoid before rank
     const float *bias;
     int32_t *topk_idx;
     float *topk_w;
@@ -288,12 +291,33 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         int be[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) { bs[j] = -INFINITY; bl[j] = 0.f; be[j] = kNone; }
-        if (mine) {
-            for (int e = sub; e < E; e += SUBS) {
-                float cl = 0.f;
+        auto logit_of = [&](int e) {
+            float cl = 0.f;
 #pragma unroll
-                for (int q = 0; q < MAXR; ++q)
-                    if (q < R) cl += recv[((size_t)q * TPC + tok) * row_stride(EP) + e];
+            for (int q = 0; q < MAXR; ++q)
+                if (q < R) cl += recv[((size_t)q * TPC + tok) * row_stride(EP) + e];
+            return cl;
+        };
+        // softmax before rank: the token's max and denominator over all E,
+        // each of its 8 threads over every 8th expert, combined by xor shuffles
+        float lmax = -INFINITY, lden = 1.f;
+        if (p.mode == 1) {
+            if (mine)
+                for (int e = sub; e < E; e += SUBS) lmax = fmaxf(lmax, logit_of(e));
+#pragma unroll
+            for (int o = 1; o < SUBS; o <<= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            lden = 0.f;
+            if (mine)
+                for (int e = sub; e < E; e += SUBS) lden += expf(logit_of(e) - lmax);
+#pragma unroll
+            for (int o = 1; o < SUBS; o <<= 1) lden += __shfl_xor_sync(0xffffffffu, lden, o);
+        }
+        if (mine) {
+            // bl: the selected experts' logits (mode 0) or probabilities
+            for (int e = sub; e < E; e += SUBS) {
+                float cl = logit_of(e);
+                if (p.mode == 1) cl = expf(cl - lmax) / lden;
+                else if (p.mode == 2) cl = 1.0f / (1.0f + expf(-cl));
                 float cs = cl + c.bias[e];
                 if (isnan(cs)) cs = -INFINITY;        // keep the ranking a total order
                 insert<KMAX>(bs, bl, be, cs, cl, e);
@@ -320,9 +344,10 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
             float w[KMAX], den = 0.f;
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
-                w[j] = j < p.k ? expf(bl[j] - m) : 0.f;
+                w[j] = j < p.k ? (p.mode == 0 ? expf(bl[j] - m) : bl[j]) : 0.f;
                 den += w[j];
             }
+            if (p.mode != 0) den = 1.f;   // probabilities as they are
             const size_t ob = (size_t)t * p.k;
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
@@ -464,6 +489,7 @@ cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream)
     }
     Params p{};
     p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.R = R; p.kblocks = kblocks;
+    p.mode = a.mode;
     p.box_rows = box_rows; p.tpc = (a.T + R - 1) / R;
     p.bias = a.bias; p.topk_idx = a.topk_idx; p.topk_w = a.topk_w;
     p.counts = a.counts; p.offsets = a.offsets; p.perm_tok = a.perm_tok; p.inv = a.inv;

@@ -4,7 +4,9 @@
 // SelectedSoftmax ("New Community Model: ZONOS3-Mini (Zyphra) - #1271",
 // §Framework change): rank experts by router logit plus selection bias, keep
 // the top k, weight them by the softmax of their unbiased logits; ties in the
-// ranking score go to the lower expert index.
+// ranking score go to the lower expert index.  Scoring modes 1 and 2 (same
+// section): rank by softmax-over-all-experts / sigmoid probability plus the
+// bias and weigh by that probability (no renormalisation).
 //
 // route_tc_kernel: one CTA per tile of 128 tokens.  Warp 0 streams the x tile
 // [128 x 64] and the router tile [EP x 64] (E rows padded to a multiple of 16,
@@ -53,6 +55,7 @@ __host__ __device__ constexpr int num_stages(int EP)
 
 struct Params {
     int T, d, E, EP, k;
+    int mode;             // scoring: 0 SelectedSoftmax, 1 softmax before rank, 2 sigmoid before rank
     const float *bias;
     int32_t *topk_idx;
     float *topk_w;
@@ -207,22 +210,35 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) { bs[j] = -INFINITY; bl[j] = 0.f; be[j] = kNone; }
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 0; ok && c0 < EP; c0 += 32) {
-                uint32_t v[2][16];
-                tmem_ld16(taddr + c0, v[0]);
-                if (c0 + 16 < EP) tmem_ld16(taddr + c0 + 16, v[1]);
-                tmem_ld_wait();
+            // this token's logits, 32 TMEM columns at a time: f(e, logit)
+            auto for_each_logit = [&](auto &&f) {
+                for (int c0 = 0; ok && c0 < EP; c0 += 32) {
+                    uint32_t v[2][16];
+                    tmem_ld16(taddr + c0, v[0]);
+                    if (c0 + 16 < EP) tmem_ld16(taddr + c0 + 16, v[1]);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int e = c0 + q;
-                    if (e < E) {
-                        const float cl = __uint_as_float(v[q >> 4][q & 15]);
-                        float cs = cl + c.bias[e];
-                        if (isnan(cs)) cs = -INFINITY;   // keep the ranking a total order
-                        topk_insert<KMAX>(bs, bl, be, cs, cl, e);
+                    for (int q = 0; q < 32; ++q) {
+                        const int e = c0 + q;
+                        if (e < E) f(e, __uint_as_float(v[q >> 4][q & 15]));
                     }
                 }
+            };
+            // softmax before rank: max, then the denominator in expert order
+            float lmax = -INFINITY, lden = 1.f;
+            if (p.mode == 1) {
+                for_each_logit([&](int, float l) { lmax = fmaxf(lmax, l); });
+                lden = 0.f;
+                for_each_logit([&](int, float l) { lden += expf(l - lmax); });
             }
+            // bl: the selected experts' logits (mode 0) or probabilities
+            for_each_logit([&](int e, float cl) {
+                if (p.mode == 1) cl = expf(cl - lmax) / lden;
+                else if (p.mode == 2) cl = 1.0f / (1.0f + expf(-cl));
+                float cs = cl + c.bias[e];
+                if (isnan(cs)) cs = -INFINITY;   // keep the ranking a total order
+                topk_insert<KMAX>(bs, bl, be, cs, cl, e);
+            });
             float wsel[KMAX];
             if (ok && valid) {
                 float m = bl[0];
@@ -231,14 +247,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 float den = 0.f;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
-                    wsel[j] = j < p.k ? expf(bl[j] - m) : 0.f;
+                    wsel[j] = j < p.k ? (p.mode == 0 ? expf(bl[j] - m) : bl[j]) : 0.f;
                     den += wsel[j];
                 }
                 const size_t base = (size_t)t * p.k;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
                     if (j < p.k) {
-                        wsel[j] = wsel[j] / den;
+                        wsel[j] = p.mode == 0 ? wsel[j] / den : wsel[j];
                         p.topk_idx[base + j] = be[j];
                         p.topk_w[base + j] = wsel[j];
                         if (p.rank) atomicOr(&c.mask[be[j]][r >> 5], 1u << (r & 31));
@@ -476,7 +492,7 @@ cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream)
         attr_done.store(1);
     }
     Params p{};
-    p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.bias = a.bias;
+    p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.bias = a.bias; p.mode = a.mode;
     p.topk_idx = a.topk_idx; p.topk_w = a.topk_w; p.rank = a.rank; p.tile_cnt = a.tile_cnt;
     p.out_zero = a.out_zero; p.zero_words = a.zero_words; p.n_zero = a.n_zero; p.status = a.status;
     const int ntiles = route_tc_tiles(a.T);

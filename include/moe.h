@@ -96,6 +96,35 @@ MOE_API moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, cons
                      moe_stream stream);
 
 /*
+ * Scoring modes of the router ("New Community Model: ZONOS3-Mini (Zyphra) -
+ * #1271", §Framework change: SelectedSoftmax is added beside the older modes,
+ * which apply a softmax or a sigmoid before ranking and so weigh experts
+ * differently; the pages give no formulas, the reading taken here is):
+ *   MOE_SCORE_SELECTED_SOFTMAX  rank by logit + bias, weights = softmax of the
+ *                               kept experts' logits (moe_route, moe_forward);
+ *   MOE_SCORE_SOFTMAX           p = softmax of the logits over all E experts,
+ *                               rank by p + bias, weights = p of the kept
+ *                               experts (not renormalised);
+ *   MOE_SCORE_SIGMOID           p = sigmoid(logit), rank by p + bias,
+ *                               weights = p of the kept experts.
+ * Ties in the ranking score go to the lower expert index in every mode.
+ */
+typedef enum {
+    MOE_SCORE_SELECTED_SOFTMAX = 0,
+    MOE_SCORE_SOFTMAX = 1,
+    MOE_SCORE_SIGMOID = 2
+} moe_scoring;
+
+/*
+ * moe_route_scored -- moe_route with scoring mode `scoring` (a moe_scoring
+ *   value; anything else is MOE_ERR_INVALID_ARG).
+ */
+MOE_API moe_status moe_route_scored(const void *x, moe_dtype act_dt, int T, int d,
+                                    const void *w_router, const float *sel_bias, int E, int k,
+                                    int scoring, int32_t *topk_idx, float *topk_w,
+                                    moe_stream stream);
+
+/*
  * moe_permute -- step 3 (token grouping), integer-exact and atomic-free.
  *   topk_idx[T,k] int32 in, each value in [0, E).
  *   counts[E]      out: number of (t, j) slots routed to expert e.
@@ -170,6 +199,18 @@ MOE_API moe_status moe_forward_profiled(const void *x, moe_dtype act_dt, int T, 
                                         const void *w_down, moe_dtype w_dt, int F, float *out,
                                         void *workspace, size_t ws_bytes, int path,
                                         void *const *events, moe_stream stream);
+
+/*
+ * moe_forward_scored -- moe_forward_profiled with scoring mode `scoring` (a
+ *   moe_scoring value; anything else is MOE_ERR_INVALID_ARG).  events may be
+ *   NULL.
+ */
+MOE_API moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
+                                      const void *w_router, const float *sel_bias, int E, int k,
+                                      const void *w_gate, const void *w_up, const void *w_down,
+                                      moe_dtype w_dt, int F, float *out, void *workspace,
+                                      size_t ws_bytes, int path, int scoring,
+                                      void *const *events, moe_stream stream);
 
 /*
  * moe_forward_noalloc -- moe_forward for callers that cannot allocate device

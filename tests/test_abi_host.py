@@ -105,3 +105,19 @@ def test_argument_errors_are_synchronous(lib):
     # T == 0 is a successful no-op that touches nothing
     assert fwd(T=0, wg=None, out=None, ws=None) == 0
     assert lib.moe_route(None, 1, 0, 64, None, None, 4, 2, None, None, None) == 0
+
+
+def test_scoring_mode_is_checked_before_any_cuda_call(lib):
+    """moe_route_scored / moe_forward_scored reject an unknown scoring mode
+    (MOE_ERR_INVALID_ARG = 1) and accept the three defined ones on an empty
+    batch (T = 0 returns before any launch)."""
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    for bad in (-1, 3, 99):
+        assert lib.moe_route_scored(fake, 1, 4, 64, fake, None, 4, 2, bad, fake, fake, None) == 1
+        assert lib.moe_forward_scored(fake, 1, 4, 64, fake, None, 4, 2, fake, fake, fake, 1, 128,
+                                      fake, fake, 1 << 20, 0, bad, None, None) == 1
+    for mode in (0, 1, 2):
+        assert lib.moe_route_scored(None, 1, 0, 64, None, None, 4, 2, mode, None, None, None) == 0
+        assert lib.moe_forward_scored(None, 1, 0, 64, None, None, 4, 2, None, None, None, 1, 128,
+                                      None, None, 0, 0, mode, None, None) == 0

@@ -355,3 +355,42 @@ def test_prefill_deterministic_and_equivariant(wdt, k, F):
     t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
     c = gpu_forward(layer, DEV, path=PREFILL, t=t2).cpu().numpy()
     assert np.array_equal(c, a[perm])
+
+
+# ---------------------------------------- other scoring modes (next row f1)
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("act,T", [(wl.F32, 37), (wl.BF16, 200), (wl.BF16, 700)])
+def test_route_scored_matches_oracle(mode, act, T):
+    """CUDA-core router (fp32, bf16 below 512 tokens) and tensor-core router
+    (bf16, 512 tokens and more) in softmax / sigmoid-before-rank mode."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(31, T=T, d=256, E=24, k=3, F=128, act_dtype=act, w_dtype=act,
+                                 bias_sd=0.05)
+    x, wr, b = to_dev(layer.x, DEV), to_dev(layer.w_router, DEV), to_dev(layer.bias, DEV)
+    idx, w = pkg.moe_route(x, wr, b, layer.k, scoring=mode)
+    torch.cuda.synchronize()
+    logits = oracle.router_logits(layer.x, layer.act_dtype, layer.w_router, layer.E)
+    idx_ref, w_ref, margin = oracle.route_scored(logits, layer.bias, layer.k, mode)
+    ok = compare_routing(idx.cpu().numpy(), w.cpu().numpy(), idx_ref, w_ref, margin, layer.k, mode)
+    assert ok.mean() > 0.5
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("path,T,wdt", [(DECODE, 40, wl.BF16), (SIMT, 40, wl.BF16),
+                                        (PREFILL, 600, wl.BF16), (PREFILL, 600, wl.Q8_0)])
+def test_forward_scored_matches_oracle(mode, path, T, wdt):
+    """Whole layer in softmax / sigmoid-before-rank mode on the clustered
+    decode router, the CUDA-core router and the tensor-core prefill router."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(32, T=T, d=256, E=16, k=2, F=256, act_dtype=wl.BF16,
+                                 w_dtype=wdt, bias_sd=0.05)
+    t = upload_layer(layer, DEV)
+    out = gpu_forward(layer, DEV, path=path, t=t, scoring=mode).cpu().numpy()
+    idx_g, _ = pkg.moe_route(t["x"], t["w_router"], t["bias"], layer.k, scoring=mode)
+    torch.cuda.synchronize()
+    rows = np.arange(T) if T <= 300 else np.sort(
+        np.random.default_rng(T).choice(T, size=300, replace=False))
+    sub = sub_layer(layer, rows)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(sub, mode=mode)
+    check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g.cpu().numpy()[rows],
+                 mode=mode)
