@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--layers", type=int, default=None)
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--scoring", default="selected_softmax",
+                   choices=["selected_softmax", "softmax", "sigmoid"],
+                   help="router scoring mode (SelectedSoftmax, or softmax / sigmoid before rank)")
     return p.parse_args()
 
 
@@ -214,7 +217,7 @@ def profile_traffic(kernel_key):
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(layers_host, w, budget_s):
+def oracle_sample(layers_host, w, budget_s, mode=0):
     """Time the oracle on whole-layer token samples until ~budget_s elapses."""
     import oracle
     oracle.build()
@@ -224,7 +227,7 @@ def oracle_sample(layers_host, w, budget_s):
     while t_used < budget_s and li < len(layers_host):
         layer = layers_host[li]
         t0 = time.perf_counter()
-        oracle.moe_forward(layer, nthreads=threads)
+        oracle.moe_forward(layer, nthreads=threads, mode=mode)
         t_used += time.perf_counter() - t0
         done_tokens += layer.T
         li += 1
@@ -270,10 +273,10 @@ def run_reference(args, w, T, layers):
         sub.T = sample_T
         subs.append(sub)
     for i in range(args.warmup):
-        oracle.moe_forward(subs[i % 4], nthreads=threads)
+        oracle.moe_forward(subs[i % 4], nthreads=threads, mode=scoring_mode(args))
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.moe_forward(subs[i % 4], nthreads=threads)
+        oracle.moe_forward(subs[i % 4], nthreads=threads, mode=scoring_mode(args))
     dt = time.perf_counter() - t0
     value = sample_T * args.steps / dt
     line = {
@@ -298,7 +301,12 @@ def config_dict(w, T, layers, args):
             "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[w.w_dtype],
             "bias": w.bias, "global_batch": T * max(1, args.gpus), "parallelism": "replicas",
             "l2": "inputs larger than L2: every step reads all layers' expert weights",
-            "graph": not args.no_graph}
+            "graph": not args.no_graph, "scoring": args.scoring}
+
+
+def scoring_mode(args):
+    """moe_forward scoring argument (and the oracle's mode) for --scoring."""
+    return {"selected_softmax": 0, "softmax": 1, "sigmoid": 2}[args.scoring]
 
 
 def main():
@@ -340,7 +348,8 @@ def main():
     def layer_call(i, events=None):
         L = stack[i]
         pkg.moe_forward(L["x"], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
-                        w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws, events=events)
+                        w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws, events=events,
+                        scoring=scoring_mode(args))
 
     def step():
         for i in range(layers):
@@ -470,7 +479,8 @@ def main():
         for i in range(layers):
             L = stack[i]
             pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
-                            w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws)
+                            w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws,
+                            scoring=scoring_mode(args))
         for i in range(layers):
             hout[i].copy_(outs[i], non_blocking=True)
     with torch.cuda.stream(stream):
@@ -493,7 +503,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host_layers = [host_layer_from_device(w, stack[i], T) for i in range(min(layers, 3))]
-        ntok, secs, threads, nl = oracle_sample(host_layers, w, budget_s=10.0)
+        ntok, secs, threads, nl = oracle_sample(host_layers, w, budget_s=10.0,
+                                                mode=scoring_mode(args))
         cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{nl} of the {layers} layers of one step, all {T} tokens each "
                          f"(fp64 C oracle, {threads} threads), {secs:.1f} s"}
