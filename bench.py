@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--layers", type=int, default=None)
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--dense", action="store_true",
+                   help="a dense SwiGLU layer of the workload's d and F (one expert, k = 1) "
+                        "through moe_ffn_dense")
     p.add_argument("--scoring", default="selected_softmax",
                    choices=["selected_softmax", "softmax", "sigmoid"],
                    help="router scoring mode (SelectedSoftmax, or softmax / sigmoid before rank)")
@@ -301,7 +304,8 @@ def config_dict(w, T, layers, args):
             "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[w.w_dtype],
             "bias": w.bias, "global_batch": T * max(1, args.gpus), "parallelism": "replicas",
             "l2": "inputs larger than L2: every step reads all layers' expert weights",
-            "graph": not args.no_graph, "scoring": args.scoring}
+            "graph": not args.no_graph, "scoring": args.scoring,
+            "dense": bool(args.dense)}
 
 
 def scoring_mode(args):
@@ -313,6 +317,9 @@ def main():
     args = parse()
     from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
+    if args.dense:   # one expert of the workload's shape, no router
+        import dataclasses
+        w = dataclasses.replace(w, E=1, k=1)
     T = args.T if args.T is not None else w.T
     layers = args.layers if args.layers is not None else w.layers
     if args.impl == "reference":
@@ -347,6 +354,12 @@ def main():
 
     def layer_call(i, events=None):
         L = stack[i]
+        if args.dense and events is None:
+            pkg.moe_ffn_dense(L["x"], L["w_gate"], L["w_up"], L["w_down"], F=w.F, w_dtype=w_dt,
+                              out=outs[i], workspace=ws)
+            return
+        # (dense layers: the per-stage timings come from the same one-expert
+        # layer through moe_forward_profiled -- same expert kernels)
         pkg.moe_forward(L["x"], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
                         w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws, events=events,
                         scoring=scoring_mode(args))
@@ -478,9 +491,13 @@ def main():
             dx[i].copy_(hx[i], non_blocking=True)
         for i in range(layers):
             L = stack[i]
-            pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
-                            w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws,
-                            scoring=scoring_mode(args))
+            if args.dense:
+                pkg.moe_ffn_dense(dx[i], L["w_gate"], L["w_up"], L["w_down"], F=w.F,
+                                  w_dtype=w_dt, out=outs[i], workspace=ws)
+            else:
+                pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"],
+                                L["w_down"], w.k, F=w.F, w_dtype=w_dt, out=outs[i],
+                                workspace=ws, scoring=scoring_mode(args))
         for i in range(layers):
             hout[i].copy_(outs[i], non_blocking=True)
     with torch.cuda.stream(stream):

@@ -8,5 +8,6 @@ tensors to it.  Importing this package loads no CUDA code.
 from .binding import (EXPORTS, MOE_BF16, MOE_F32, MOE_PATH_AUTO, MOE_PATH_DECODE,  # noqa: F401
                       MOE_PATH_PREFILL, MOE_PATH_DECODE_SIMT, MOE_Q8_0, MoeError, library_path, load_library,
                       MOE_SCORE_SELECTED_SOFTMAX, MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX,
-                      moe_check, moe_forward, moe_pack_q8_0, moe_permute, moe_q8_0_packed_size,
+                      moe_check, moe_ffn_dense, moe_forward, moe_pack_q8_0, moe_permute,
+                      moe_q8_0_packed_size,
                       moe_route, moe_workspace_size)

@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "moe_permute",
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_workspace_size", "moe_forward",
-           "moe_forward_profiled", "moe_forward_scored", "moe_forward_noalloc", "moe_check")
+           "moe_forward_profiled", "moe_forward_scored", "moe_ffn_dense", "moe_forward_noalloc",
+           "moe_check")
 
 _lib = None
 
@@ -77,6 +78,8 @@ def load_library():
     L.moe_forward_scored.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz,
                                      i, i, vp, vp]
     L.moe_forward_scored.restype = i
+    L.moe_ffn_dense.argtypes = [vp, i, i, i, vp, vp, vp, i, i, vp, vp, sz, i, vp]
+    L.moe_ffn_dense.restype = i
     L.moe_forward_noalloc.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, i, vp]
     L.moe_forward_noalloc.restype = i
     L.moe_check.argtypes = [vp, vp, vp]
@@ -214,6 +217,35 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
                                       _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F,
                                       _ptr(out), _ptr(workspace), ws_len, path, handles,
                                       _stream(x)), "moe_forward_profiled")
+    return out
+
+
+def moe_ffn_dense(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor,
+                  w_down: torch.Tensor, F: Optional[int] = None, w_dtype: Optional[int] = None,
+                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  path: int = MOE_PATH_AUTO) -> torch.Tensor:
+    """A dense SwiGLU FFN layer -> out fp32 [T, d].
+
+    Weights: float32/bfloat16 tensors [F,d], [F,d], [d,F] (or [1,F,d] ...); or,
+    with w_dtype=MOE_Q8_0, uint8 buffers from moe_pack_q8_0 (then F is required).
+    """
+    L = load_library()
+    T, d = x.shape
+    act = _act_dtype(x)
+    if w_dtype is None:
+        w_dtype = _act_dtype(w_gate)
+    if F is None:
+        if w_dtype == MOE_Q8_0:
+            raise ValueError("F is required for Q8_0 weights")
+        F = w_gate.shape[-2]
+    if out is None:
+        out = torch.empty((T, d), dtype=torch.float32, device=x.device)
+    ws_bytes = moe_workspace_size(T, d, 1, 1, F, act, w_dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
+    ws_len = workspace.numel() * workspace.element_size()
+    _check(L.moe_ffn_dense(_ptr(x), act, T, d, _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F,
+                           _ptr(out), _ptr(workspace), ws_len, path, _stream(x)), "moe_ffn_dense")
     return out
 
 

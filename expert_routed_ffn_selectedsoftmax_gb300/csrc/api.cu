@@ -100,6 +100,13 @@ int device_sm_count()
     return n;
 }
 
+// the layer (defined below; `dense`: see there)
+moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                        const float *sel_bias, int E, int k, const void *w_gate, const void *w_up,
+                        const void *w_down, moe_dtype w_dt, int F, float *out, void *workspace,
+                        size_t ws_bytes, int path, int scoring, bool dense, void *const *events,
+                        moe_stream stream);
+
 }  // namespace
 
 extern "C" {
@@ -221,8 +228,36 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
                               size_t ws_bytes, int path, int scoring, void *const *events,
                               moe_stream stream)
 {
+    return forward_impl(x, act_dt, T, d, w_router, sel_bias, E, k, w_gate, w_up, w_down, w_dt, F,
+                        out, workspace, ws_bytes, path, scoring, false, events, stream);
+}
+
+moe_status moe_ffn_dense(const void *x, moe_dtype act_dt, int T, int d, const void *w_gate,
+                         const void *w_up, const void *w_down, moe_dtype w_dt, int F, float *out,
+                         void *workspace, size_t ws_bytes, int path, moe_stream stream)
+{
+    return forward_impl(x, act_dt, T, d, nullptr, nullptr, 1, 1, w_gate, w_up, w_down, w_dt, F,
+                        out, workspace, ws_bytes, path, MOE_SCORE_SELECTED_SOFTMAX, true, nullptr,
+                        stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The layer; `dense`: one expert and k = 1 with no router (every token to
+// expert 0 with weight 1), the rows read in place where the expert kernels
+// take the activation dtype as it is.
+moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                        const float *sel_bias, int E, int k, const void *w_gate, const void *w_up,
+                        const void *w_down, moe_dtype w_dt, int F, float *out, void *workspace,
+                        size_t ws_bytes, int path, int scoring, bool dense, void *const *events,
+                        moe_stream stream)
+{
     if (!scoring_ok(scoring)) return MOE_ERR_INVALID_ARG;
-    moe_status st = check_route_args(x, act_dt, T, d, w_router, sel_bias, E, k);
+    // (dense: no router; the router checks then cover x alone)
+    moe_status st = check_route_args(x, act_dt, T, d, dense ? x : w_router, dense ? nullptr : sel_bias,
+                                     E, k);
     if (st != MOE_OK) return st;
     if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
     if (!weights_ok(act_dt, w_dt)) {
@@ -288,7 +323,7 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
     const bool act16 = act_dt == MOE_BF16;
     // decode batches of up to 128 tokens: one clustered kernel routes and
     // groups (no scatter) and the expert kernel gathers x rows itself (no xp)
-    const bool fused_small = use_dtc && route_small_capable(act_dt, T, d, E, k);
+    const bool fused_small = !dense && use_dtc && route_small_capable(act_dt, T, d, E, k);
     ra.xp = ((use_prefill || use_dtc) && act16 && !fused_small) ? ws + L.xp : nullptr;
     ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
@@ -296,9 +331,19 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
     ra.n_zero = 0;
     ra.status = status;
     ra.ev_routed = ev[1];
-    const bool xp_ready = ra.xp != nullptr;
+    bool xp_ready = ra.xp != nullptr;
+    // grouped 16-bit rows for the tensor-core kernels: a dense layer's are x
+    // itself unless the Q8_0 GEMMs need them converted to fp16
+    void *xp_rows = ws + L.xp;
     cudaError_t e;
-    if (fused_small) {
+    if (dense) {
+        e = launch_identity_grouping(T, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w,
+                                     status, device_sm_count(), s);
+        if (e != cudaSuccess || mark(1) != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+        const bool in_place = act16 && w_dt != MOE_Q8_0;
+        if (in_place) xp_rows = const_cast<void *>(x);
+        xp_ready = in_place;
+    } else if (fused_small) {
         e = launch_route_small(ra, s);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
     } else if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
@@ -319,7 +364,7 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
         a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
         a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down; a.w_dt = w_dt;
         a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
-        a.xp = ws + L.xp; a.xp_ready = xp_ready;
+        a.xp = xp_rows; a.xp_ready = xp_ready;
         a.h = ws + L.h; a.out = out; a.zero_out = zero_out; a.status = status; a.num_sms = num_sms;
         a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
         e = launch_tc_experts(a, s);
@@ -327,7 +372,7 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
         DecodeTcArgs a{};
         a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
         a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down;
-        a.offsets = offsets; a.inv = inv; a.topk_w = topk_w; a.xp = ws + L.xp;
+        a.offsets = offsets; a.inv = inv; a.topk_w = topk_w; a.xp = xp_rows;
         a.pgu = reinterpret_cast<float *>(ws + L.pgu); a.pd = reinterpret_cast<float *>(ws + L.pd);
         a.h = reinterpret_cast<uint16_t *>(ws + L.h);
         a.out = out; a.status = status; a.num_sms = num_sms; a.ev_gateup = ev[4];
@@ -336,7 +381,7 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
         if (fused_small) {
             a.x_gather = x;
         } else if (!xp_ready &&
-                   launch_gather_rows(x, d, perm_tok, T * k, ws + L.xp, 0, num_sms, s) != cudaSuccess) {
+                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, 0, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;
         }
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
@@ -354,6 +399,10 @@ moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, int d,
     if (e != cudaSuccess || mark(5) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 moe_status moe_check(const void *workspace, uint32_t *device_word, moe_stream stream)
 {

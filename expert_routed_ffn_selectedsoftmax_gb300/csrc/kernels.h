@@ -64,6 +64,11 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
                            cudaStream_t stream);
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
                                void *xp, int to_fp16, int num_sms, cudaStream_t stream);
+// dense layer (E = 1, k = 1): expert 0, weight 1, identity grouping; clears status
+cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, int32_t *counts,
+                                     int32_t *offsets, int32_t *perm_tok, int32_t *inv,
+                                     float *perm_w, uint32_t *status, int num_sms,
+                                     cudaStream_t stream);
 
 // decode.cu -- expert FFN for few rows per expert (CUDA-core, weight streaming)
 struct DecodeArgs {

@@ -161,6 +161,45 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, int d,
     }
 }
 
+// Routing and grouping of a dense layer (one expert, k = 1): every token to
+// expert 0 with weight 1 -- the softmax of a single logit -- and grouped row
+// r = token r.  Written directly instead of running a router whose answer is
+// fixed.
+__global__ void identity_grouping_kernel(int T, int32_t *__restrict__ topk_idx,
+                                         float *__restrict__ topk_w, int32_t *__restrict__ counts,
+                                         int32_t *__restrict__ offsets, int32_t *__restrict__ perm_tok,
+                                         int32_t *__restrict__ inv, float *__restrict__ perm_w,
+                                         uint32_t *__restrict__ status)
+{
+    pdl_enter();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (status) *status = kDevOk;
+        counts[0] = T;
+        offsets[0] = 0;
+        offsets[1] = T;
+    }
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < T; r += gridDim.x * blockDim.x) {
+        topk_idx[r] = 0;
+        topk_w[r] = 1.0f;
+        perm_tok[r] = r;
+        inv[r] = r;
+        perm_w[r] = 1.0f;
+    }
+}
+
+cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, int32_t *counts,
+                                     int32_t *offsets, int32_t *perm_tok, int32_t *inv,
+                                     float *perm_w, uint32_t *status, int num_sms,
+                                     cudaStream_t stream)
+{
+    long long want = ((long long)T + 255) / 256, cap = (long long)num_sms * 4;
+    int blocks = (int)(want < cap ? want : cap);
+    if (blocks < 1) blocks = 1;
+    launch_pdl(identity_grouping_kernel, dim3(blocks), dim3(256), 0, stream, T, topk_idx, topk_w,
+               counts, offsets, perm_tok, inv, perm_w, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
                                void *xp, int to_fp16, int num_sms, cudaStream_t stream)
 {

@@ -213,6 +213,21 @@ MOE_API moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, in
                                       void *const *events, moe_stream stream);
 
 /*
+ * moe_ffn_dense -- a dense SwiGLU FFN layer: out = W_d (SiLU(W_g x) * (W_u x))
+ *   per token, the E = 1, k = 1 case of the layer ("zonos2.cpp internals",
+ *   §Model architecture: dense FFN layers beside the MoE ones; "New Community
+ *   Model: ZONOS3-Mini (Zyphra) - #1271", §Summary: layer 0 has a dense SwiGLU
+ *   FFN).  No router: every token goes to the one expert with weight 1.
+ *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0: packed by
+ *   moe_pack_q8_0 with rows = F or d); other arguments as moe_forward, with a
+ *   workspace of moe_workspace_size(T, d, 1, 1, F, act_dt, w_dt) bytes.
+ */
+MOE_API moe_status moe_ffn_dense(const void *x, moe_dtype act_dt, int T, int d,
+                                 const void *w_gate, const void *w_up, const void *w_down,
+                                 moe_dtype w_dt, int F, float *out, void *workspace,
+                                 size_t ws_bytes, int path, moe_stream stream);
+
+/*
  * moe_forward_noalloc -- moe_forward for callers that cannot allocate device
  * memory.  (No counterpart on the source pages: an addition of this library.)
  * Some hosts give the layer only its inputs and outputs -- serving runtimes

@@ -121,3 +121,17 @@ def test_scoring_mode_is_checked_before_any_cuda_call(lib):
         assert lib.moe_route_scored(None, 1, 0, 64, None, None, 4, 2, mode, None, None, None) == 0
         assert lib.moe_forward_scored(None, 1, 0, 64, None, None, 4, 2, None, None, None, 1, 128,
                                       None, None, 0, 0, mode, None, None) == 0
+
+
+def test_ffn_dense_argument_checks(lib):
+    """moe_ffn_dense: empty batch is a no-op; bad path / F / dtype rejected
+    (MOE_ERR_INVALID_ARG = 1, MOE_ERR_UNSUPPORTED = 2) before any CUDA call."""
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    assert lib.moe_ffn_dense(None, 1, 0, 64, None, None, None, 1, 128, None, None, 0, 0, None) == 0
+    assert lib.moe_ffn_dense(fake, 1, 4, 64, fake, fake, fake, 1, 128, fake, fake, 1 << 20, 9,
+                             None) == 1
+    assert lib.moe_ffn_dense(fake, 1, 4, 64, fake, fake, fake, 1, 100, fake, fake, 1 << 20, 0,
+                             None) == 1
+    assert lib.moe_ffn_dense(fake, 0, 4, 64, fake, fake, fake, 1, 128, fake, fake, 1 << 20, 0,
+                             None) == 2

@@ -414,3 +414,20 @@ def test_scoring_modes_layer_matches_dense_brute_force(mode, k):
         for e in sorted(range(layer.E), key=lambda e: (-s[t, e], e))[:k]:
             ref[t] += p[t, e] * y[e, t]
     assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+# ------------------------------------- dense SwiGLU layer (next row f2)
+@pytest.mark.parametrize("act,wdt", [(wl.F32, wl.F32), (wl.BF16, wl.Q8_0)])
+def test_one_expert_layer_is_the_dense_swiglu_ffn(act, wdt):
+    """E = 1, k = 1: the weight is the softmax of one logit, exactly 1, so the
+    layer is W_d (SiLU(W_g x) * (W_u x)) whatever the router holds."""
+    layer = tiny_layer(seed=90, act=act, wdt=wdt, T=6, d=64, E=1, k=1, F=96)
+    out, idx, w, _ = oracle.moe_forward(layer)
+    assert np.all(idx == 0) and np.all(w == 1.0)
+    x = decode(layer.x, act)
+    wg = decode(layer.w_gate, wdt)[0]
+    wu = decode(layer.w_up, wdt)[0]
+    wd = decode(layer.w_down, wdt)[0]
+    g, u = x @ wg.T, x @ wu.T
+    ref = (g / (1.0 + np.exp(-g)) * u) @ wd.T
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())

@@ -394,3 +394,26 @@ def test_forward_scored_matches_oracle(mode, path, T, wdt):
     ref, idx_ref, w_ref, margin = oracle.moe_forward(sub, mode=mode)
     check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g.cpu().numpy()[rows],
                  mode=mode)
+
+
+# ---------------------------------------- dense SwiGLU layer (next row f2)
+@pytest.mark.parametrize("act,wdt,T,path", [
+    (wl.BF16, wl.BF16, 5, DECODE), (wl.BF16, wl.BF16, 5, SIMT), (wl.F32, wl.F32, 37, SIMT),
+    (wl.BF16, wl.Q8_0, 9, SIMT), (wl.BF16, wl.BF16, 600, PREFILL), (wl.BF16, wl.Q8_0, 600, PREFILL),
+    (wl.BF16, wl.BF16, 700, 0)])
+def test_ffn_dense_matches_oracle(act, wdt, T, path):
+    """moe_ffn_dense against the oracle's one-expert layer, and bit for bit
+    against moe_forward with E = 1, k = 1 (same expert kernels; only the
+    routing step differs)."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_custom_layer(33, T=T, d=256, E=1, k=1, F=256, act_dtype=act, w_dtype=wdt)
+    t = upload_layer(layer, DEV)
+    out = pkg.moe_ffn_dense(t["x"], t["w_gate"], t["w_up"], t["w_down"], F=layer.F,
+                            w_dtype=layer.w_dtype, path=path).cpu().numpy()
+    via_moe = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy()
+    assert np.array_equal(out, via_moe)
+    rows = np.arange(T) if T <= 300 else np.sort(
+        np.random.default_rng(T).choice(T, size=300, replace=False))
+    sub = sub_layer(layer, rows)
+    ref, idx_ref, _, margin = oracle.moe_forward(sub)
+    check_output(out[rows], sub, ref, idx_ref, margin)
