@@ -30,8 +30,10 @@ from typing import Optional
 
 import numpy as np
 
-F32, BF16, Q8_0 = 0, 1, 2
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0"}
+F32, BF16, Q8_0, Q4_A64 = 0, 1, 2, 3
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64"}
+Q4_A64_GROUP = 64
+Q4_A64_BLOCK_BYTES = 36
 Q8_0_BLOCK = 32
 Q8_0_BLOCK_BYTES = 34
 
@@ -52,7 +54,7 @@ class Workload:
     k: int
     F: int
     act_dtype: int      # dtype of x and W_r (F32 or BF16)
-    w_dtype: int        # dtype of expert weights (F32, BF16, Q8_0)
+    w_dtype: int        # dtype of expert weights (F32, BF16, Q8_0, Q4_A64)
     bias: str           # "normal" or "zipf"
     bias_sd: float
     layers: int         # layers run back to back in one benchmark step
@@ -87,6 +89,12 @@ WORKLOADS = {
         description="ZONOS2-shaped prefill with Q8_0 experts: T=4096, d=2048, "
                     "E=16, top-1, F=2816, bf16 activations and router (4 "
                     "independent layers per benchmark step)"),
+    "zonos2_decode_q4": Workload(
+        "zonos2_decode_q4", T=8, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q4_A64, bias="normal", bias_sd=0.1, layers=28,
+        description="ZONOS2-shaped decode step with affine 4-bit group-64 experts "
+                    "(the format of the pages' MLX figures): d=2048, E=16, top-1, "
+                    "F=2816, T in {1, 8, 64}, 28-layer weight rotation"),
 }
 
 
@@ -148,6 +156,37 @@ def q8_0_quantize(w) -> np.ndarray:
     return out
 
 
+def q4_a64_quantize(w) -> np.ndarray:
+    """Encode w[..., K] (K % 64 == 0) as affine 4-bit blocks: uint8 [..., K/64, 36].
+
+    Block layout: bytes 0-1 the fp16 scale, bytes 2-3 the fp16 bias (little
+    endian), bytes 4-35 the 64 codes, value 2j in the low nibble of byte 4+j and
+    2j+1 in the high nibble; value = scale * q + bias.  Per group of 64:
+    scale = (max - min) / 15, bias = min (both stored rounded to fp16);
+    q = round-half-away-from-zero((w - bias) / scale) with the stored fp16
+    scale and bias, clamped to [0, 15]; a constant group has scale 0, q 0.
+    """
+    w = np.asarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    if K % Q4_A64_GROUP:
+        raise ValueError("affine 4-bit needs the contiguous axis to be a multiple of 64")
+    g = w.reshape(w.shape[:-1] + (K // Q4_A64_GROUP, Q4_A64_GROUP))
+    mn, mx = g.min(axis=-1), g.max(axis=-1)
+    scale16 = ((mx - mn) / np.float32(15.0)).astype(np.float16)
+    bias16 = mn.astype(np.float16)
+    sc, bi = scale16.astype(np.float32), bias16.astype(np.float32)
+    inv = np.zeros_like(sc)
+    nz = sc > 0
+    inv[nz] = np.float32(1.0) / sc[nz]
+    v = (g - bi[..., None]) * inv[..., None]
+    q = np.clip(np.sign(v) * np.floor(np.abs(v) + np.float32(0.5)), 0, 15).astype(np.uint8)
+    out = np.empty(g.shape[:-1] + (Q4_A64_BLOCK_BYTES,), dtype=np.uint8)
+    out[..., 0:2] = scale16.view(np.uint8).reshape(scale16.shape + (2,))
+    out[..., 2:4] = bias16.view(np.uint8).reshape(bias16.shape + (2,))
+    out[..., 4:] = q[..., 0::2] | (q[..., 1::2] << 4)
+    return out
+
+
 def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == F32:
         return np.ascontiguousarray(a, dtype=np.float32)
@@ -155,6 +194,8 @@ def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
         return f32_to_bf16_bits(a)
     if dtype == Q8_0:
         return q8_0_quantize(a)
+    if dtype == Q4_A64:
+        return q4_a64_quantize(a)
     raise ValueError(dtype)
 
 
@@ -212,6 +253,8 @@ def weight_bytes_per_expert(d: int, F: int, w_dtype: int) -> int:
         return 4 * n
     if w_dtype == BF16:
         return 2 * n
+    if w_dtype == Q4_A64:
+        return n // Q4_A64_GROUP * Q4_A64_BLOCK_BYTES
     return n // Q8_0_BLOCK * Q8_0_BLOCK_BYTES
 
 
@@ -238,6 +281,26 @@ def q8_0_quantize_torch(w):
     return out
 
 
+def q4_a64_quantize_torch(w):
+    """Device twin of q4_a64_quantize: float32 [..., K] -> uint8 blocks
+    [..., K/64, 36] (same layout and rounding rule)."""
+    import torch
+    K = w.shape[-1]
+    g = w.reshape(*w.shape[:-1], K // Q4_A64_GROUP, Q4_A64_GROUP).float()
+    mn, mx = g.amin(-1), g.amax(-1)
+    scale16 = ((mx - mn) / 15.0).to(torch.float16)
+    bias16 = mn.to(torch.float16)
+    sc, bi = scale16.float(), bias16.float()
+    inv = torch.where(sc > 0, 1.0 / torch.where(sc > 0, sc, torch.ones_like(sc)), torch.zeros_like(sc))
+    v = (g - bi[..., None]) * inv[..., None]
+    q = (torch.sign(v) * torch.floor(v.abs() + 0.5)).clamp(0, 15).to(torch.uint8)
+    out = torch.empty(*g.shape[:-1], Q4_A64_BLOCK_BYTES, dtype=torch.uint8, device=w.device)
+    out[..., 0:2] = scale16.contiguous().view(torch.uint8).reshape(*scale16.shape, 2)
+    out[..., 2:4] = bias16.contiguous().view(torch.uint8).reshape(*bias16.shape, 2)
+    out[..., 4:] = q[..., 0::2] | (q[..., 1::2] << 4)
+    return out
+
+
 def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = None,
                       device="cuda"):
     """Draw ``layers`` independent layers directly in device memory.
@@ -249,8 +312,8 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
     uint8 Q8_0 blocks [E, rows, cols/32, 34].
     """
     import torch
-    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (F32, F32)):
-        raise ValueError("device stacks: bf16/bf16, bf16/Q8_0 or fp32/fp32 layers")
+    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (F32, F32)):
+        raise ValueError("device stacks: bf16/bf16, bf16/Q8_0, bf16/Q4_A64 or fp32/fp32 layers")
     act = torch.float32 if w.act_dtype == F32 else torch.bfloat16
     T = w.T if T is None else T
     g = torch.Generator(device=device)
@@ -260,7 +323,9 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
 
         def rn(*shape, sd=1.0, q8=False):
             t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * sd
-            return q8_0_quantize_torch(t) if q8 else t.to(act)
+            if q8:
+                return q4_a64_quantize_torch(t) if w.w_dtype == Q4_A64 else q8_0_quantize_torch(t)
+            return t.to(act)
         d, E, F = w.d, w.E, w.F
         x = rn(T, d)
         wr = rn(E, d, sd=1.0 / math.sqrt(d))
@@ -269,7 +334,7 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             b = torch.from_numpy(zipf_bias(E, rng)).to(device)
         else:
             b = torch.randn(E, generator=g, device=device, dtype=torch.float32) * w.bias_sd
-        q8 = w.w_dtype == Q8_0
+        q8 = w.w_dtype in (Q8_0, Q4_A64)   # block-quantised expert weights
         wg = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wu = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wd = rn(E, d, F, sd=1.0 / math.sqrt(F), q8=q8)

@@ -67,7 +67,7 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
     } else if (dt == ORACLE_BF16) {
         const uint16_t *p = (const uint16_t *)base + row * (size_t)cols;
         for (int c = 0; c < cols; ++c) out[c] = bf16_bits_to_double(p[c]);
-    } else { /* ORACLE_Q8_0: per row cols/32 blocks of {fp16 scale, int8 q[32]} */
+    } else if (dt == ORACLE_Q8_0) { /* per row cols/32 blocks of {fp16 scale, int8 q[32]} */
         const uint8_t *p = (const uint8_t *)base + row * (size_t)(cols / 32) * 34;
         for (int b = 0; b < cols / 32; ++b) {
             const uint8_t *blk = p + (size_t)b * 34;
@@ -75,11 +75,26 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
             for (int i = 0; i < 32; ++i)
                 out[b * 32 + i] = scale * (double)(int8_t)blk[2 + i];
         }
+    } else { /* ORACLE_Q4_A64: per row cols/64 blocks of {fp16 scale, fp16 bias,
+              * 32 bytes: value 2j in the low nibble of byte j, 2j+1 in the high} */
+        const uint8_t *p = (const uint8_t *)base + row * (size_t)(cols / 64) * 36;
+        for (int b = 0; b < cols / 64; ++b) {
+            const uint8_t *blk = p + (size_t)b * 36;
+            double scale = f16_bits_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+            double bias = f16_bits_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+            for (int j = 0; j < 32; ++j) {
+                out[b * 64 + 2 * j] = scale * (double)(blk[4 + j] & 15) + bias;
+                out[b * 64 + 2 * j + 1] = scale * (double)(blk[4 + j] >> 4) + bias;
+            }
+        }
     }
 }
 
 static int valid_act(int dt) { return dt == ORACLE_F32 || dt == ORACLE_BF16; }
-static int valid_w(int dt) { return dt == ORACLE_F32 || dt == ORACLE_BF16 || dt == ORACLE_Q8_0; }
+static int valid_w(int dt)
+{
+    return dt == ORACLE_F32 || dt == ORACLE_BF16 || dt == ORACLE_Q8_0 || dt == ORACLE_Q4_A64;
+}
 
 /* ------------------------------------------------------------ thread helper */
 typedef void (*range_fn)(void *ctx, int begin, int end);
@@ -370,6 +385,7 @@ int oracle_expert_combine(const void *x, int x_dt, int T, int d, const int32_t *
     if (T < 0 || d <= 0 || F <= 0 || E <= 0 || k < 1 || !valid_act(x_dt) || !valid_w(w_dt))
         return -1;
     if (w_dt == ORACLE_Q8_0 && (d % 32 || F % 32)) return -1;
+    if (w_dt == ORACLE_Q4_A64 && (d % 64 || F % 64)) return -1;
     for (size_t i = 0; i < (size_t)T * k; ++i)
         if (topk_idx[i] < 0 || topk_idx[i] >= E) return -1;
     if (T == 0) return 0;

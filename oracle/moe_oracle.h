@@ -4,7 +4,9 @@
  * the benchmark).  Independent of the CUDA library: no shared code or headers.
  *
  * Storage dtypes: 0 = fp32, 1 = bf16 bit patterns (uint16), 2 = Q8_0 rows of
- * 34-byte blocks {fp16 scale, int8 q[32]} along the contiguous axis.
+ * 34-byte blocks {fp16 scale, int8 q[32]} along the contiguous axis, 3 = affine
+ * 4-bit rows of 36-byte blocks of 64 values {fp16 scale, fp16 bias, 32 bytes:
+ * value 2j in the low nibble of byte j, 2j+1 in the high}, value = scale*q + bias.
  * Activations (x, W_r) are fp32 or bf16; expert weights may also be Q8_0.
  * Layouts (row-major): x[T,d], W_r[E,d], W_g[E,F,d], W_u[E,F,d], W_d[E,d,F].
  * All functions return 0 on success, -1 on invalid arguments.
@@ -19,7 +21,7 @@
 extern "C" {
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3 };
 
 int oracle_default_threads(void);
 

@@ -42,6 +42,14 @@ def decode(a, dtype):
         return wl.bf16_bits_to_f32(a).astype(np.float64)
     blocks = np.asarray(a, np.uint8)
     scale = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    if dtype == wl.Q4_A64:   # {scale, bias, 32 bytes: value 2j low nibble, 2j+1 high}
+        bias = blocks[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+        codes = blocks[..., 4:]
+        q = np.empty(codes.shape[:-1] + (64,), np.float64)
+        q[..., 0::2] = codes & 15
+        q[..., 1::2] = codes >> 4
+        w = q * scale[..., None] + bias[..., None]
+        return w.reshape(w.shape[:-2] + (w.shape[-2] * w.shape[-1],))
     q = blocks[..., 2:].copy().view(np.int8).astype(np.float64)
     w = q * scale[..., None]
     return w.reshape(w.shape[:-2] + (w.shape[-2] * w.shape[-1],))
@@ -431,3 +439,47 @@ def test_one_expert_layer_is_the_dense_swiglu_ffn(act, wdt):
     g, u = x @ wg.T, x @ wu.T
     ref = (g / (1.0 + np.exp(-g)) * u) @ wd.T
     assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+
+# ------------------------------- affine 4-bit group-64 experts (next row f3)
+def test_q4_a64_block_encoding_worked_example():
+    """Hand-built group: w_i = (i mod 16) / 4 - 1 spans [-1, 2.75], so
+    scale = 3.75 / 15 = 0.25 and bias = -1 (both exact in fp16), q_i = i mod 16
+    exactly, byte j = q_2j | q_2j+1 << 4, and decoding gives w back exactly.
+    A constant group has scale 0, bias = the value, codes 0."""
+    w = np.array([(i % 16) / 4.0 - 1.0 for i in range(64)], np.float32)
+    b = wl.q4_a64_quantize(w[None])[0, 0]
+    assert b[0:2].view(np.float16)[0] == 0.25 and b[2:4].view(np.float16)[0] == -1.0
+    assert np.array_equal(b[4:], np.array([(2 * j % 16) | ((2 * j + 1) % 16) << 4
+                                           for j in range(32)], np.uint8))
+    assert np.array_equal(decode(b[None, None], wl.Q4_A64)[0], w.astype(np.float64))
+    c = wl.q4_a64_quantize(np.full((1, 64), 0.375, np.float32))[0, 0]
+    assert c[0:2].view(np.float16)[0] == 0 and c[2:4].view(np.float16)[0] == 0.375
+    assert not c[4:].any()
+
+
+def test_q4_a64_error_within_half_a_step():
+    rng = np.random.default_rng(91)
+    w = rng.standard_normal((16, 256)).astype(np.float32)
+    b = wl.q4_a64_quantize(w)
+    deq = decode(b, wl.Q4_A64)
+    step = np.repeat(b[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64), 64, axis=-1)
+    # half a step, plus the fp16 rounding of scale and bias (a few ulps of the range)
+    assert np.all(np.abs(deq - w) <= 0.5 * step + 2e-3 * np.abs(w).max())
+
+
+def test_q4_a64_layer_equals_its_exact_dequantisation():
+    """The oracle on 4-bit bytes equals the oracle on fp32 weights holding the
+    decoded values (exactly representable: fp16 scale x 4-bit code + fp16 bias)."""
+    layer = tiny_layer(seed=92, act=wl.BF16, wdt=wl.Q4_A64, T=6, d=128, E=4, k=2, F=64)
+    out_q, idx_q, _, _ = oracle.moe_forward(layer)
+    import copy
+    f = copy.copy(layer)
+    f.w_dtype = wl.F32
+    for n in ("w_gate", "w_up", "w_down"):
+        v = decode(getattr(layer, n), wl.Q4_A64)
+        assert np.array_equal(v.astype(np.float32).astype(np.float64), v)
+        setattr(f, n, v.astype(np.float32))
+    out_f, idx_f, _, _ = oracle.moe_forward(f)
+    assert np.array_equal(idx_q, idx_f) and np.array_equal(out_q, out_f)
