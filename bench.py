@@ -246,7 +246,7 @@ def host_layer_from_device(w, dl, T):
         if t.dtype == torch.float32:
             return t.contiguous().cpu().numpy()
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    if w.w_dtype == wl.Q8_0:   # the oracle reads the Q8_0 blocks themselves
+    if w.w_dtype in (wl.Q8_0, wl.Q4_A64):   # the oracle reads the blocks themselves
         wts = {n: dl["blocks"][n].cpu().numpy() for n in ("w_gate", "w_up", "w_down")}
     else:
         wts = {n: bits(dl[n]) for n in ("w_gate", "w_up", "w_down")}
@@ -301,7 +301,7 @@ def run_reference(args, w, T, layers):
 def config_dict(w, T, layers, args):
     return {"workload": w.name, "T": T, "d": w.d, "E": w.E, "k": w.k, "F": w.F,
             "layers": layers, "act_dtype": "bf16" if w.act_dtype else "f32",
-            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[w.w_dtype],
+            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_a64"}[w.w_dtype],
             "bias": w.bias, "global_batch": T * max(1, args.gpus), "parallelism": "replicas",
             "l2": "inputs larger than L2: every step reads all layers' expert weights",
             "graph": not args.no_graph, "scoring": args.scoring,
@@ -338,14 +338,16 @@ def main():
     # ------------------------------------------------------------ inputs
     stack = wl.make_device_stack(w, seed=1 + rank, layers=layers, T=T, device=dev)
     act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
-    w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0}[w.w_dtype]
-    if w_dt == pkg.MOE_Q8_0:
-        # Q8_0 blocks are repacked once, at load time, into the kernels' planes
+    w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0,
+            wl.Q4_A64: pkg.MOE_Q4_A64}[w.w_dtype]
+    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64):
+        # block-quantised weights are repacked once, at load time, into the kernels' planes
+        pack = pkg.moe_pack_q8_0 if w_dt == pkg.MOE_Q8_0 else pkg.moe_pack_q4_a64
         for L in stack:
             L["blocks"] = {n: L[n] for n in ("w_gate", "w_up", "w_down")}
             for n, rows, cols in (("w_gate", w.E * w.F, w.d), ("w_up", w.E * w.F, w.d),
                                   ("w_down", w.E * w.d, w.F)):
-                L[n] = pkg.moe_pack_q8_0(L[n].reshape(-1), rows, cols)
+                L[n] = pack(L[n].reshape(-1), rows, cols)
         torch.cuda.synchronize(dev)
     ws_bytes = pkg.moe_workspace_size(T, w.d, w.E, w.k, w.F, act_dt, w_dt)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -530,7 +532,8 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands"}[w.w_dtype],
+        "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands",
+                  wl.Q4_A64: "affine 4-bit weights, f32 CUDA-core arithmetic"}[w.w_dtype],
         "data": "synthetic", "config": config_dict(w, T, layers, args),
         "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s",
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-MOE_F32, MOE_BF16, MOE_Q8_0 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_A64 = 0, 1, 2, 3
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_PATH_DECODE_SIMT = 0, 1, 2, 3
 MOE_SCORE_SELECTED_SOFTMAX, MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -24,7 +24,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "moe_permute",
-           "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_workspace_size", "moe_forward",
+           "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_q4_a64_packed_size", "moe_pack_q4_a64",
+           "moe_workspace_size", "moe_forward",
            "moe_forward_profiled", "moe_forward_scored", "moe_ffn_dense", "moe_forward_noalloc",
            "moe_check")
 
@@ -68,6 +69,10 @@ def load_library():
     L.moe_q8_0_packed_size.restype = sz
     L.moe_pack_q8_0.argtypes = [vp, ll, i, vp, vp]
     L.moe_pack_q8_0.restype = i
+    L.moe_q4_a64_packed_size.argtypes = [ll, i]
+    L.moe_q4_a64_packed_size.restype = sz
+    L.moe_pack_q4_a64.argtypes = [vp, ll, i, vp, vp]
+    L.moe_pack_q4_a64.restype = i
     L.moe_workspace_size.argtypes = [i, i, i, i, i, i, i]
     L.moe_workspace_size.restype = sz
     L.moe_forward.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz, i, vp]
@@ -161,6 +166,23 @@ def moe_pack_q8_0(blocks: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
     return packed
 
 
+def moe_q4_a64_packed_size(rows: int, cols: int) -> int:
+    return int(load_library().moe_q4_a64_packed_size(rows, cols))
+
+
+def moe_pack_q4_a64(blocks: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
+    """Repack affine 4-bit group-64 blocks (uint8 device tensor, rows*cols/64*36
+    bytes) into planes."""
+    L = load_library()
+    n = moe_q4_a64_packed_size(rows, cols)
+    if n == 0 and rows != 0:
+        raise MoeError(1, "moe_q4_a64_packed_size")
+    packed = torch.empty(max(n, 256), dtype=torch.uint8, device=blocks.device)
+    _check(L.moe_pack_q4_a64(_ptr(blocks), rows, cols, _ptr(packed), _stream(blocks)),
+           "moe_pack_q4_a64")
+    return packed
+
+
 def moe_workspace_size(T: int, d: int, E: int, k: int, F: int, act_dt: int, w_dt: int) -> int:
     return int(load_library().moe_workspace_size(T, d, E, k, F, act_dt, w_dt))
 
@@ -186,8 +208,8 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
     if w_dtype is None:
         w_dtype = _act_dtype(w_gate)
     if F is None:
-        if w_dtype == MOE_Q8_0:
-            raise ValueError("F is required for Q8_0 weights")
+        if w_dtype in (MOE_Q8_0, MOE_Q4_A64):
+            raise ValueError("F is required for block-quantised weights")
         F = w_gate.shape[1]
     if out is None:
         out = torch.empty((T, d), dtype=torch.float32, device=x.device)
@@ -235,8 +257,8 @@ def moe_ffn_dense(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor,
     if w_dtype is None:
         w_dtype = _act_dtype(w_gate)
     if F is None:
-        if w_dtype == MOE_Q8_0:
-            raise ValueError("F is required for Q8_0 weights")
+        if w_dtype in (MOE_Q8_0, MOE_Q4_A64):
+            raise ValueError("F is required for block-quantised weights")
         F = w_gate.shape[-2]
     if out is None:
         out = torch.empty((T, d), dtype=torch.float32, device=x.device)
@@ -265,8 +287,8 @@ def moe_forward_noalloc(x: torch.Tensor, w_router: torch.Tensor,
     if w_dtype is None:
         w_dtype = _act_dtype(w_gate)
     if F is None:
-        if w_dtype == MOE_Q8_0:
-            raise ValueError("F is required for Q8_0 weights")
+        if w_dtype in (MOE_Q8_0, MOE_Q4_A64):
+            raise ValueError("F is required for block-quantised weights")
         F = w_gate.shape[1]
     _check(L.moe_forward_noalloc(_ptr(x), _act_dtype(x), T, d, _ptr(w_router), _ptr(sel_bias), E,
                                  k, _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F, _ptr(out),

@@ -26,7 +26,7 @@ bool scoring_ok(int scoring)
 bool weights_ok(int act_dt, int w_dt)
 {
     if (act_dt == MOE_F32) return w_dt == MOE_F32;
-    return w_dt == MOE_BF16 || w_dt == MOE_Q8_0;
+    return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64;
 }
 
 // Largest d the router kernel can stage (one token of fp32 in <= 200 KB).
@@ -192,6 +192,23 @@ moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *pac
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+size_t moe_q4_a64_packed_size(long long rows, int cols)
+{
+    if (rows < 0 || cols <= 0 || cols % 64) return 0;
+    return q4_a64_bias_offset(rows, cols) + (size_t)rows * (cols / 64) * 2;
+}
+
+moe_status moe_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
+                           moe_stream stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 64) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    cudaError_t e = launch_pack_q4_a64(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype act_dt, moe_dtype w_dt)
 {
     if (T < 0 || d <= 0 || E <= 0 || k < 1 || k > E || F <= 0) return 0;
@@ -261,10 +278,12 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     if (st != MOE_OK) return st;
     if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
     if (!weights_ok(act_dt, w_dt)) {
-        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0) ? MOE_ERR_UNSUPPORTED
-                                                                         : MOE_ERR_INVALID_ARG;
+        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64)
+                   ? MOE_ERR_UNSUPPORTED
+                   : MOE_ERR_INVALID_ARG;
     }
     if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
+    if (w_dt == MOE_Q4_A64 && (d % 64 || F % 64)) return MOE_ERR_INVALID_ARG;
     if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL &&
         path != MOE_PATH_DECODE_SIMT)
         return MOE_ERR_INVALID_ARG;
@@ -275,7 +294,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     if (!w_gate || !w_up || !w_down || !out || !workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
         return MOE_ERR_INVALID_ARG;
-    if (w_dt == MOE_Q8_0) {
+    if (w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64) {
         const uintptr_t m = 255u;
         if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
             (reinterpret_cast<uintptr_t>(w_down) & m))

@@ -69,6 +69,8 @@ template <> struct RawW<float> { uint4 a, b; };
 template <> struct RawW<__nv_bfloat16> { uint4 a; };
 struct Q8Tag {};   // Q8_0 planes: int8 q plane + fp16 scale per 32 values
 template <> struct RawW<Q8Tag> { uint2 q; float s; };
+struct Q4Tag {};   // affine 4-bit planes: codes + fp16 scale and bias per 64 values
+template <> struct RawW<Q4Tag> { uint32_t q; float s, b; };
 
 // Weight matrix view: row-major [rows, cols] in one of the storage types.
 template <typename WT> struct WView {
@@ -125,6 +127,31 @@ template <> struct WView<Q8Tag> {
             int v = (int)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
             c.v[i] = (float)v * r.s;
         }
+    }
+};
+
+// Affine 4-bit view: q points at the code plane [rows, cols/2] (value 2j in the
+// low nibble of byte j); fp16 scale and bias planes [cols/64, rows].  Set by
+// the host.
+template <> struct WView<Q4Tag> {
+    const uint8_t *q;
+    const __half *scales, *biases;
+    size_t cols;
+    size_t rows;
+    __device__ __forceinline__ void load(size_t row, int col, RawW<Q4Tag> &r) const
+    {
+        uint32_t v;
+        asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
+                     : "=r"(v) : "l"(q + (row * cols + col) / 2));
+        r.q = v;
+        const size_t g = (size_t)(col / 64) * rows + row;
+        r.s = __half2float(scales[g]);
+        r.b = __half2float(biases[g]);
+    }
+    __device__ __forceinline__ static void cvt(const RawW<Q4Tag> &r, Chunk8 &c)
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c.v[i] = fmaf(r.s, (float)((r.q >> (4 * i)) & 15u), r.b);
     }
 };
 

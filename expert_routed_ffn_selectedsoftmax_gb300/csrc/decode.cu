@@ -240,6 +240,22 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
         WView<__nv_bfloat16> wd{static_cast<const __nv_bfloat16 *>(a.w_down), (size_t)a.F};
         return launch_t<__nv_bfloat16, __nv_bfloat16>(a, wg, wu, wd, stream);
     }
+    if (a.w_dt == MOE_Q4_A64) {
+        // affine 4-bit packed planes: codes, fp16 scales, fp16 biases
+        auto view4 = [](const void *p, long long rows, int cols) {
+            WView<Q4Tag> v;
+            const char *b = static_cast<const char *>(p);
+            v.q = reinterpret_cast<const uint8_t *>(b);
+            v.scales = reinterpret_cast<const __half *>(b + q4_a64_scale_offset(rows, cols));
+            v.biases = reinterpret_cast<const __half *>(b + q4_a64_bias_offset(rows, cols));
+            v.cols = (size_t)cols;
+            v.rows = (size_t)rows;
+            return v;
+        };
+        return launch_t<__nv_bfloat16, Q4Tag>(a, view4(a.w_gate, (long long)a.E * a.F, a.d),
+                                              view4(a.w_up, (long long)a.E * a.F, a.d),
+                                              view4(a.w_down, (long long)a.E * a.d, a.F), stream);
+    }
     // Q8_0 packed planes: q plane, then the fp16 scales at align256(rows*cols)
     auto view = [](const void *p, long long rows, int cols) {
         WView<Q8Tag> v;

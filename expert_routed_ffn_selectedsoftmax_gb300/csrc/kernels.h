@@ -119,5 +119,10 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream);
 // q8.cu
 cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
                              cudaStream_t stream);
+// q8.cu -- affine 4-bit group-64 planes (codes, fp16 scales, fp16 biases)
+size_t q4_a64_scale_offset(long long rows, int cols);
+size_t q4_a64_bias_offset(long long rows, int cols);
+cudaError_t launch_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
+                               cudaStream_t stream);
 
 }  // namespace moe

@@ -28,7 +28,7 @@
  *    (1..256), k experts per token (1..min(E, 8)), F expert ffn width.
  *  - Activation storage (x, W_r): MOE_F32 or MOE_BF16; logits, routing
  *    weights and the output are fp32.  Expert weights: MOE_F32 (with F32
- *    activations), MOE_BF16 or MOE_Q8_0 (with BF16 activations).
+ *    activations), MOE_BF16, MOE_Q8_0 or MOE_Q4_A64 (with BF16 activations).
  *  - Calls on distinct workspaces and outputs are independent; there is no
  *    global mutable state.
  */
@@ -61,7 +61,7 @@ typedef enum {
     MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (see moe_check) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3 } moe_dtype;
 
 /* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
  * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16
@@ -155,6 +155,28 @@ MOE_API moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int
 MOE_API size_t moe_q8_0_packed_size(long long rows, int cols);
 MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
                          moe_stream stream);
+
+/*
+ * Affine 4-bit expert weights, groups of 64 (MOE_Q4_A64; the expert format of
+ * the pages' MLX figures: "ZONOS2 (Zyphra) -- MLX runtime", 4-bit group-64
+ * affine experts; the pages give no byte layout, this is the library's).
+ * Input format: rows of `cols` values along the contiguous axis, stored as
+ * cols/64 blocks of 36 bytes {fp16 scale, fp16 bias (little endian), 32 bytes
+ * of codes: value 2j in the low nibble of byte j, 2j+1 in the high nibble};
+ * value = scale * q + bias.  Used with BF16 activations on the CUDA-core
+ * decode kernels (MOE_PATH_PREFILL returns MOE_ERR_UNSUPPORTED).  moe_forward
+ * consumes them repacked into three planes in one buffer:
+ *   bytes [0, rows*cols/2)                 codes [rows, cols/2], as above
+ *   at align256(rows*cols/2)               fp16 scale plane [cols/64, rows]
+ *   at align256(end of the scale plane)    fp16 bias plane [cols/64, rows]
+ * moe_q4_a64_packed_size returns the buffer size (0 if cols % 64 != 0 or
+ * rows < 0); moe_pack_q4_a64 repacks `blocks` (device, any alignment) into
+ * `packed` (device, 256-byte aligned) on `stream`, with the same rows/cols as
+ * moe_pack_q8_0.
+ */
+MOE_API size_t moe_q4_a64_packed_size(long long rows, int cols);
+MOE_API moe_status moe_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
+                                   moe_stream stream);
 
 /*
  * Bytes of device workspace moe_forward needs for these sizes (any path).

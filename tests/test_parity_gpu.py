@@ -134,6 +134,8 @@ SMALL = [
     (wl.BF16, wl.Q8_0, 45, 256, 8, 2, 160),
     (wl.BF16, wl.Q8_0, 3, 2048, 16, 1, 2816),
     (wl.BF16, wl.BF16, 96, 256, 4, 4, 128),     # k == E: dense gating
+    (wl.BF16, wl.Q4_A64, 5, 256, 8, 2, 128),    # affine 4-bit experts (CUDA-core decode)
+    (wl.BF16, wl.Q4_A64, 70, 512, 16, 1, 192),
     (wl.BF16, wl.BF16, 5, 512, 64, 8, 128),     # few tokens: largest E and k of the small-batch router
     (wl.BF16, wl.BF16, 8, 2048, 33, 3, 128),    # few tokens: ragged E, longest rows
 ]
@@ -232,7 +234,8 @@ def test_device_status_ok_after_forward():
 # -------------------------------------------------- workload sizes (full)
 @pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("zonos3_mini_decode", None),
                                     ("zonos2_decode", 1), ("zonos2_decode", 8),
-                                    ("zonos2_decode", 64)])
+                                    ("zonos2_decode", 64), ("zonos2_decode_q4", 1),
+                                    ("zonos2_decode_q4", 8)])
 def test_forward_decode_workloads_full(name, T):
     """Decode workloads at full size, in the launch configuration the benchmark
     times (path AUTO), every output row against the oracle."""
