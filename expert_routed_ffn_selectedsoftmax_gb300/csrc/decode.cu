@@ -21,6 +21,7 @@
 // received rows, built per CTA from the device offsets, so the grid never
 // depends on the routing.
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -60,7 +61,11 @@ __device__ __forceinline__ float dot8(const Chunk8 &a, const Chunk8 &b, float ac
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
-template <typename AT, typename WT, int NCH>
+// RPW: weight rows per warp.  Each token chunk loaded into registers is used
+// for all RPW rows, and a lane has RPW x NCH weight chunks in flight: for
+// narrow weight encodings (4-bit codes, 4 bytes per 8 values) one row per warp
+// leaves the loads dominated by re-reads of the token rows.
+template <typename AT, typename WT, int NCH, int RPW>
 __global__ void __launch_bounds__(kDecThreads)
 decode_gateup_kernel(const AT *__restrict__ x, int d, WView<WT> wg, WView<WT> wu, int F,
                      const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
@@ -71,60 +76,73 @@ decode_gateup_kernel(const AT *__restrict__ x, int d, WView<WT> wg, WView<WT> wu
     __shared__ int wtot[kDecWarps];
     const int n_act = build_active_list(offsets, E, act, wtot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ftiles = (F + kDecWarps - 1) / kDecWarps;
+    constexpr int ROWS = kDecWarps * RPW;     // ffn rows per work item
+    const int ftiles = (F + ROWS - 1) / ROWS;
     const int items = n_act * ftiles;
 
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int ai = item / ftiles, ft = item - ai * ftiles;
         const int e = act[ai];
         const int row0 = offsets[e], M = offsets[e + 1] - row0;
-        const int f = ft * kDecWarps + warp;
-        if (f >= F) continue;   // warp-uniform
-        const size_t wrow = (size_t)e * F + f;
+        const int f0 = ft * ROWS + warp * RPW;  // this warp's rows f0 .. f0 + RPW - 1
+        if (f0 >= F) continue;   // warp-uniform
+        const size_t wrow = (size_t)e * F + f0;
         for (int rb = 0; rb < M; rb += kRowBlock) {
-            float ag[kRowBlock], au[kRowBlock];
+            float ag[RPW][kRowBlock], au[RPW][kRowBlock];
             int tok[kRowBlock];
 #pragma unroll
             for (int r = 0; r < kRowBlock; ++r) {
-                ag[r] = 0.f; au[r] = 0.f;
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) { ag[i][r] = 0.f; au[i][r] = 0.f; }
                 tok[r] = rb + r < M ? perm_tok[row0 + rb + r] : -1;
             }
             for (int c0 = lane * 8; c0 < d; c0 += 32 * 8 * NCH) {
-                RawW<WT> rg[NCH], ru[NCH];
+                RawW<WT> rg[RPW][NCH], ru[RPW][NCH];
 #pragma unroll
                 for (int j = 0; j < NCH; ++j) {
                     const int c = c0 + j * 256;
-                    if (c < d) { wg.load(wrow, c, rg[j]); wu.load(wrow, c, ru[j]); }
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i)
+                        if (c < d && f0 + i < F) { wg.load(wrow + i, c, rg[i][j]); wu.load(wrow + i, c, ru[i][j]); }
                 }
 #pragma unroll
                 for (int j = 0; j < NCH; ++j) {
                     const int c = c0 + j * 256;
                     if (c < d) {
-                        Chunk8 g8, u8;
-                        WView<WT>::cvt(rg[j], g8);
-                        WView<WT>::cvt(ru[j], u8);
+                        Chunk8 g8[RPW], u8[RPW];
+#pragma unroll
+                        for (int i = 0; i < RPW; ++i) {
+                            WView<WT>::cvt(rg[i][j], g8[i]);
+                            WView<WT>::cvt(ru[i][j], u8[i]);
+                        }
 #pragma unroll
                         for (int r = 0; r < kRowBlock; ++r) {
                             if (tok[r] >= 0) {
                                 Chunk8 xv;
                                 load8(x + (size_t)tok[r] * d + c, xv);
-                                ag[r] = dot8(g8, xv, ag[r]);
-                                au[r] = dot8(u8, xv, au[r]);
+#pragma unroll
+                                for (int i = 0; i < RPW; ++i) {
+                                    ag[i][r] = dot8(g8[i], xv, ag[i][r]);
+                                    au[i][r] = dot8(u8[i], xv, au[i][r]);
+                                }
                             }
                         }
                     }
                 }
             }
-            const float gs = warp_transpose_sum8(ag, lane);
-            const float us = warp_transpose_sum8(au, lane);
-            const int r = transpose8_row(lane);
-            if ((lane & 3) == 0 && rb + r < M)
-                h[(size_t)(row0 + rb + r) * F + f] = silu(gs) * us;
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float gs = warp_transpose_sum8(ag[i], lane);
+                const float us = warp_transpose_sum8(au[i], lane);
+                const int r = transpose8_row(lane);
+                if ((lane & 3) == 0 && rb + r < M && f0 + i < F)
+                    h[(size_t)(row0 + rb + r) * F + f0 + i] = silu(gs) * us;
+            }
         }
     }
 }
 
-template <typename WT, int NCH>
+template <typename WT, int NCH, int RPW>
 __global__ void __launch_bounds__(kDecThreads)
 decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
@@ -135,54 +153,64 @@ decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
     __shared__ int wtot[kDecWarps];
     const int n_act = build_active_list(offsets, E, act, wtot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int dtiles = (d + kDecWarps - 1) / kDecWarps;
+    constexpr int COLS = kDecWarps * RPW;     // output columns per work item
+    const int dtiles = (d + COLS - 1) / COLS;
     const int items = n_act * dtiles;
 
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int ai = item / dtiles, dt = item - ai * dtiles;
         const int e = act[ai];
         const int row0 = offsets[e], M = offsets[e + 1] - row0;
-        const int o = dt * kDecWarps + warp;
-        if (o >= d) continue;
-        const size_t wrow = (size_t)e * d + o;
+        const int o0 = dt * COLS + warp * RPW;  // this warp's columns o0 .. o0 + RPW - 1
+        if (o0 >= d) continue;
+        const size_t wrow = (size_t)e * d + o0;
         for (int rb = 0; rb < M; rb += kRowBlock) {
-            float acc[kRowBlock];
+            float acc[RPW][kRowBlock];
 #pragma unroll
-            for (int r = 0; r < kRowBlock; ++r) acc[r] = 0.f;
+            for (int i = 0; i < RPW; ++i)
+#pragma unroll
+                for (int r = 0; r < kRowBlock; ++r) acc[i][r] = 0.f;
             const int nr = min(kRowBlock, M - rb);
             for (int c0 = lane * 8; c0 < F; c0 += 32 * 8 * NCH) {
-                RawW<WT> rw[NCH];
+                RawW<WT> rw[RPW][NCH];
 #pragma unroll
                 for (int j = 0; j < NCH; ++j) {
                     const int c = c0 + j * 256;
-                    if (c < F) wd.load(wrow, c, rw[j]);
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i)
+                        if (c < F && o0 + i < d) wd.load(wrow + i, c, rw[i][j]);
                 }
 #pragma unroll
                 for (int j = 0; j < NCH; ++j) {
                     const int c = c0 + j * 256;
                     if (c < F) {
-                        Chunk8 w8;
-                        WView<WT>::cvt(rw[j], w8);
+                        Chunk8 w8[RPW];
+#pragma unroll
+                        for (int i = 0; i < RPW; ++i) WView<WT>::cvt(rw[i][j], w8[i]);
 #pragma unroll
                         for (int r = 0; r < kRowBlock; ++r) {
                             if (r < nr) {
                                 Chunk8 hv;
                                 load8(h + (size_t)(row0 + rb + r) * F + c, hv);
-                                acc[r] = dot8(w8, hv, acc[r]);
+#pragma unroll
+                                for (int i = 0; i < RPW; ++i) acc[i][r] = dot8(w8[i], hv, acc[i][r]);
                             }
                         }
                     }
                 }
             }
-            const float s = warp_transpose_sum8(acc, lane);
-            const int r = transpose8_row(lane);
-            if ((lane & 3) == 0 && r < nr) {
-                const int row = row0 + rb + r;
-                const int t = perm_tok[row];
-                const float v = perm_w[row] * s;
-                float *dst = out + (size_t)t * d + o;
-                if (k == 1) *dst = v;
-                else atomicAdd(dst, v);
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float s = warp_transpose_sum8(acc[i], lane);
+                const int r = transpose8_row(lane);
+                if ((lane & 3) == 0 && r < nr && o0 + i < d) {
+                    const int row = row0 + rb + r;
+                    const int t = perm_tok[row];
+                    const float v = perm_w[row] * s;
+                    float *dst = out + (size_t)t * d + o0 + i;
+                    if (k == 1) *dst = v;
+                    else atomicAdd(dst, v);
+                }
             }
         }
     }
@@ -198,32 +226,60 @@ static int blocks_per_sm(K kern)
     return n;
 }
 
+template <typename AT, typename WT, int NCH, int RPW>
+static cudaError_t launch_gateup(const DecodeArgs &a, WView<WT> wg, WView<WT> wu, cudaStream_t stream)
+{
+    auto k1 = decode_gateup_kernel<AT, WT, NCH, RPW>;
+    static std::atomic<int> occ{0};
+    if (occ.load() == 0) occ.store(blocks_per_sm(k1));
+    const int n_exp = a.E < a.T * a.k ? a.E : a.T * a.k;   // experts that can be active
+    const long long items = (long long)n_exp * ((a.F + kDecWarps * RPW - 1) / (kDecWarps * RPW));
+    int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);
+    if (g < 1) g = 1;
+    launch_pdl(k1, dim3(g), dim3(kDecThreads), 0, stream, static_cast<const AT *>(a.x), a.d, wg, wu,
+               a.F, a.offsets, a.perm_tok, a.E, a.h);
+    return cudaGetLastError();
+}
+
+template <typename WT, int NCH, int RPW>
+static cudaError_t launch_down(const DecodeArgs &a, WView<WT> wd, cudaStream_t stream)
+{
+    auto k2 = decode_down_kernel<WT, NCH, RPW>;
+    static std::atomic<int> occ{0};
+    if (occ.load() == 0) occ.store(blocks_per_sm(k2));
+    const int n_exp = a.E < a.T * a.k ? a.E : a.T * a.k;
+    const long long items = (long long)n_exp * ((a.d + kDecWarps * RPW - 1) / (kDecWarps * RPW));
+    int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);
+    if (g < 1) g = 1;
+    launch_pdl(k2, dim3(g), dim3(kDecThreads), 0, stream, a.h, a.F, wd, a.d, a.offsets, a.perm_tok,
+               a.perm_w, a.E, a.k, a.out);
+    return cudaGetLastError();
+}
+
 template <typename AT, typename WT>
 static cudaError_t launch_t(const DecodeArgs &a, WView<WT> wg, WView<WT> wu, WView<WT> wd,
                             cudaStream_t stream)
 {
-    constexpr int NCH_GU = 4, NCH_D = 8;
-    auto k1 = decode_gateup_kernel<AT, WT, NCH_GU>;
-    auto k2 = decode_down_kernel<WT, NCH_D>;
-    static std::atomic<int> occ1{0}, occ2{0};
-    if (occ1.load() == 0) occ1.store(blocks_per_sm(k1));
-    if (occ2.load() == 0) occ2.store(blocks_per_sm(k2));
-
-    const int n_exp = a.E < a.T * a.k ? a.E : a.T * a.k;   // experts that can be active
-    long long items1 = (long long)n_exp * ((a.F + kDecWarps - 1) / kDecWarps);
-    long long items2 = (long long)n_exp * ((a.d + kDecWarps - 1) / kDecWarps);
-    int g1 = (int)(items1 < (long long)a.num_sms * occ1 ? items1 : (long long)a.num_sms * occ1);
-    int g2 = (int)(items2 < (long long)a.num_sms * occ2 ? items2 : (long long)a.num_sms * occ2);
-    if (g1 < 1) g1 = 1;
-    if (g2 < 1) g2 = 1;
-    launch_pdl(k1, dim3(g1), dim3(kDecThreads), 0, stream, static_cast<const AT *>(a.x), a.d, wg, wu, a.F, a.offsets,
-                                        a.perm_tok, a.E, a.h);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err;
+    // 4-bit codes: several rows per warp (see decode_gateup_kernel) when the
+    // wider items still give every SM two of them; wider types: one row
+    const int n_exp = a.E < a.T * a.k ? a.E : a.T * a.k;
+    const long long two_per_sm = 2LL * a.num_sms;
+    if constexpr (std::is_same<WT, Q4Tag>::value) {
+        err = (long long)n_exp * ((a.F + 2 * kDecWarps - 1) / (2 * kDecWarps)) >= two_per_sm
+                  ? launch_gateup<AT, WT, 2, 2>(a, wg, wu, stream)
+                  : launch_gateup<AT, WT, 4, 1>(a, wg, wu, stream);
+    } else {
+        err = launch_gateup<AT, WT, 4, 1>(a, wg, wu, stream);
+    }
     if (err != cudaSuccess) return err;
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
-    launch_pdl(k2, dim3(g2), dim3(kDecThreads), 0, stream, a.h, a.F, wd, a.d, a.offsets, a.perm_tok, a.perm_w, a.E,
-                                        a.k, a.out);
-    return cudaGetLastError();
+    if constexpr (std::is_same<WT, Q4Tag>::value) {
+        return (long long)n_exp * ((a.d + 4 * kDecWarps - 1) / (4 * kDecWarps)) >= two_per_sm
+                   ? launch_down<WT, 4, 4>(a, wd, stream)
+                   : launch_down<WT, 8, 1>(a, wd, stream);
+    }
+    return launch_down<WT, 8, 1>(a, wd, stream);
 }
 
 cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
