@@ -199,8 +199,9 @@ def expert_kernel_names(w, T, num_sms):
 
 
 def profile_traffic(kernel_key):
-    """dram bytes per launch recorded from an ncu capture, if the kernel source
-    it was taken on is unchanged (else None)."""
+    """dram bytes per launch recorded from an ncu capture of this kernel on this
+    workload (key "file:stage:workload:T<tokens>"), if the kernel source it was
+    taken on is unchanged (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -463,7 +464,8 @@ def main():
     dom_flops = alg[f"{dominant}_flops"] / layers
     # the kernel's bound: tensor when its arithmetic intensity is past the ridge
     tensor_bound = dom_flops / dom_bytes > tflops_peak * 1e12 / (hbm * 1e9)
-    traffic = profile_traffic(f"{names['file']}:{dominant}")
+    traffic = profile_traffic(f"{names['file']}:{dominant}:{w.name}"
+                              f"{'-dense' if args.dense else ''}:T{T}")
     if tensor_bound:
         achieved = dom_flops / (dom_us * 1e-6) / 1e12
         roofline = {"bound": "tensor", "kernel": names[dominant], "achieved": achieved,
