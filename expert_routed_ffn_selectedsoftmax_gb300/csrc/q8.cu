@@ -49,7 +49,8 @@ cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void 
     return cudaGetLastError();
 }
 
-// Affine 4-bit, groups of 64 (the expert format of the pages' MLX figures):
+// Affine 4-bit, groups of 64 (the experts of the MLX build, "Zyphra-ZONOS2-4bit",
+// §How this was quantized):
 // 36-byte blocks {fp16 scale, fp16 bias, 32 bytes of codes, value 2j in the low
 // nibble of byte j} -> a code plane [rows, cols/2] (the blocks' code bytes in
 // order) and fp16 scale and bias planes [cols/64, rows].

@@ -158,8 +158,9 @@ MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, v
 
 /*
  * Affine 4-bit expert weights, groups of 64 (MOE_Q4_A64; the expert format of
- * the pages' MLX figures: "ZONOS2 (Zyphra) -- MLX runtime", 4-bit group-64
- * affine experts; the pages give no byte layout, this is the library's).
+ * the MLX build, "Zyphra-ZONOS2-4bit", §How this was quantized: experts at
+ * 4 bits, group size 64, affine mode; the page gives no byte layout, this is
+ * the library's).
  * Input format: rows of `cols` values along the contiguous axis, stored as
  * cols/64 blocks of 36 bytes {fp16 scale, fp16 bias (little endian), 32 bytes
  * of codes: value 2j in the low nibble of byte j, 2j+1 in the high nibble};
