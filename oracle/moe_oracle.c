@@ -75,8 +75,11 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
             for (int i = 0; i < 32; ++i)
                 out[b * 32 + i] = scale * (double)(int8_t)blk[2 + i];
         }
-    } else { /* ORACLE_Q4_A64: per row cols/64 blocks of {fp16 scale, fp16 bias,
-              * 32 bytes: value 2j in the low nibble of byte j, 2j+1 in the high} */
+    } else { /* ORACLE_Q4_A64 ("Zyphra-ZONOS2-4bit", §How this was quantized:
+              * experts at 4 bits, groups of 64, affine; the byte layout is this
+              * library's): per row cols/64 blocks of {fp16 scale, fp16 bias,
+              * 32 bytes: value 2j in the low nibble of byte j, 2j+1 in the high},
+              * value = scale * q + bias */
         const uint8_t *p = (const uint8_t *)base + row * (size_t)(cols / 64) * 36;
         for (int b = 0; b < cols / 64; ++b) {
             const uint8_t *blk = p + (size_t)b * 36;
