@@ -57,6 +57,23 @@ def parse():
     return p.parse_args()
 
 
+def max_over_ranks(t_ms, world, device):
+    """The slowest rank's time: the whole job ends when it does (world > 1:
+    an all-reduce over the initialised process group)."""
+    if world <= 1:
+        return float(t_ms)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(t_ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(tokens_per_step_per_rank, world, ms_per_step):
+    """Whole-job tokens/s: every rank processes its own tokens each step."""
+    return tokens_per_step_per_rank * world / (ms_per_step * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -420,15 +437,10 @@ def main():
     stream.synchronize()
     clk = clocks.stop()
     barrier()
-    t_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = t_ms / args.steps
     tokens_per_step = T * layers
-    value = tokens_per_step * world / (ms_per_step * 1e-3)
+    value = job_throughput(tokens_per_step, world, ms_per_step)
 
     # --------------------------------------------- per-kernel (stage) timing
     # the same step with CUDA events at the stage boundaries, on the stream

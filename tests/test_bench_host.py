@@ -1,0 +1,78 @@
+"""Host-side checks of the benchmark's multi-rank logic and of its reference
+arm (no GPU): two gloo ranks on CPU take the slowest rank's time, whole-job
+throughput counts every rank's tokens, and `bench.py --impl reference` prints
+one JSON line with the contract's keys on rank 0 and nothing on other ranks."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, times, out_dir):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        t = bench.max_over_ranks(times[rank], world, torch.device("cpu"))
+        with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+            f.write(repr(t))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks(tmp_path):
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    times = [3.25, 5.5]
+    mp.start_processes(_rank_main, args=(2, _free_port(), times, str(tmp_path)), nprocs=2,
+                       join=True, start_method="spawn")
+    got = [float(open(tmp_path / f"rank{r}.txt").read()) for r in range(2)]
+    assert got == [5.5, 5.5]
+
+
+def test_single_rank_and_throughput():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(2.5, 1, None) == 2.5
+    # 128 tokens x 10 layers per rank per step, 2 ranks, 0.5 ms per step
+    assert bench.job_throughput(1280, 2, 0.5) == pytest.approx(5.12e6)
+
+
+def _reference(env_extra):
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_fp32", "--steps", "2", "--warmup", "1"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_reference_arm_prints_the_contract_line_on_rank_zero_only():
+    lines = _reference({"RANK": "0", "WORLD_SIZE": "1"})
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["impl"] == "reference" and j["value"] > 0 and j["higher_is_better"] is True
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
+    assert j["config"]["workload"] == "tiny_fp32"
+    assert _reference({"RANK": "1", "WORLD_SIZE": "2"}) == []
