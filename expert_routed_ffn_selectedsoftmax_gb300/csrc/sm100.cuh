@@ -118,18 +118,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cl)
         : "memory");
 }
-// Same as tma_load_2d, but the tile lands at the same shared-memory offset in
-// every CTA of the cluster selected by `mask`, and each of them gets the
-// transaction bytes on its own mbarrier at the offset of `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                               int x, int y, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank()
 {
     uint32_t r;
@@ -177,15 +165,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-// tcgen05.commit whose mbarrier arrival goes to the barrier at the same offset
-// in every CTA of the cluster selected by `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
-        : "memory");
 }
 // CTA-pair forms (cta_group::2).  One thread of the even CTA of a pair issues
 // the MMA for both: A has M = 256 rows, rows 0-127 in the issuing CTA's shared
