@@ -255,6 +255,33 @@ def test_q8_0_equals_its_exact_dequantisation():
     assert np.array_equal(out_q, out_f)
 
 
+def test_q8_0_fp16_scales_of_every_class_decode_exactly():
+    """Block scales are IEEE binary16 (ggml's Q8_0, named in "zonos2.cpp
+    internals", §Quantization: 32 int8 codes and one fp16 scale).  Scales set to subnormals (both
+    signs, smallest and largest), the smallest normal, +-1 and zero must decode
+    as numpy's float16 does: the layer on the Q8_0 bytes equals the layer on the
+    fp32 values numpy decodes (each fp16 x int8 product is exact in fp32)."""
+    layer = tiny_layer(seed=13, act=wl.BF16, wdt=wl.Q8_0, T=6, d=64, F=96)
+    bits = np.array([0x0001, 0x0155, 0x03FF, 0x8200, 0x0400, 0x3C00, 0xBC00, 0x0000, 0x2E66],
+                    np.uint16)
+    for n, name in enumerate(("w_gate", "w_up", "w_down")):
+        blocks = getattr(layer, name).copy()
+        flat = blocks.reshape(-1, 34)
+        pick = bits[(np.arange(flat.shape[0]) + n) % bits.size]
+        flat[:, 0:2] = pick.view(np.uint8).reshape(-1, 2)
+        setattr(layer, name, blocks)
+    out_q, idx_q, _, _ = oracle.moe_forward(layer)
+    assert np.abs(out_q).max() > 0
+    for name in ("w_gate", "w_up", "w_down"):
+        deq = decode(getattr(layer, name), wl.Q8_0)
+        assert np.array_equal(deq.astype(np.float32).astype(np.float64), deq)
+        setattr(layer, name, deq.astype(np.float32))
+    layer.w_dtype = wl.F32
+    out_f, idx_f, _, _ = oracle.moe_forward(layer)
+    assert np.array_equal(idx_q, idx_f)
+    assert np.array_equal(out_q, out_f)
+
+
 def test_q8_0_block_encoding():
     w = np.zeros((2, 64), np.float32)
     w[0, :32] = np.linspace(-1, 1, 32)
