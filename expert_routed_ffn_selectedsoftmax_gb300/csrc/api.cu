@@ -94,9 +94,10 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
 int device_sm_count()
 {
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    // (a failed query falls back to the GB300's 152 SMs; the launch then reports the error)
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-        return 148;
+        return 152;
     return n;
 }
 
@@ -169,6 +170,9 @@ moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *co
     if ((long long)T * k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
     if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !perm_tok || !inv)) return MOE_ERR_INVALID_ARG;
+    for (const void *p : {(const void *)topk_idx, (const void *)counts, (const void *)offsets,
+                          (const void *)perm_tok, (const void *)inv})
+        if (reinterpret_cast<uintptr_t>(p) & 3u) return MOE_ERR_INVALID_ARG;
     // T == 0 still writes zero counts and offsets
     cudaError_t e = launch_permute(topk_idx, T, k, E, counts, offsets, perm_tok, inv, nullptr,
                                    nullptr, nullptr, static_cast<cudaStream_t>(stream));

@@ -133,8 +133,10 @@ MOE_API moe_status moe_route_scored(const void *x, moe_dtype act_dt, int T, int 
  *                  [offsets[e], offsets[e+1]) in increasing flat slot order
  *                  t*k + j (i.e. increasing t).
  *   inv[T*k]       out: grouped row of flat slot t*k + j.
- *   Out-of-range expert ids are not checked on the device; moe_forward's own
- *   indices always come from moe_route.
+ *   All five buffers are device memory, 4-byte aligned, owned by the caller.
+ *   An expert id outside [0, E) is left out of counts and of the permutation
+ *   (its inv entry is not written, no other memory is touched); moe_forward's
+ *   own indices always come from its router.
  */
 MOE_API moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,
                        int32_t *offsets, int32_t *perm_tok, int32_t *inv, moe_stream stream);

@@ -82,6 +82,7 @@ def test_argument_errors_are_synchronous(lib):
     # permute: k > E, null outputs
     assert lib.moe_permute(fake, 4, 3, 2, fake, fake, fake, fake, None) == I
     assert lib.moe_permute(fake, 4, 1, 2, None, fake, fake, fake, None) == I
+    assert lib.moe_permute(fake, 4, 1, 2, vp(0x10002), fake, fake, fake, None) == I   # misaligned
     # pack: cols not a multiple of 32, misaligned destination
     assert lib.moe_pack_q8_0(fake, 4, 48, fake, None) == I
     assert lib.moe_pack_q8_0(fake, 4, 64, vp(0x10010), None) == I
