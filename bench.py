@@ -273,6 +273,33 @@ def host_layer_from_device(w, dl, T):
                     bias=dl["bias"].float().cpu().numpy(), **wts)
 
 
+def host_cpu_model():
+    """The host CPU's model name (x86: /proc/cpuinfo; Arm: lscpu), for the CPU baseline."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+def percentiles(samples_ms):
+    """p10 / median / p90 of per-step times (nearest rank)."""
+    v = sorted(samples_ms)
+    at = lambda q: v[min(len(v) - 1, max(0, int(math.ceil(q * len(v))) - 1))]
+    return {"p10": at(0.10), "median": statistics.median(v), "p90": at(0.90), "n": len(v)}
+
+
 def run_reference(args, w, T, layers):
     rank, world, local = dist_env()
     if rank != 0:
@@ -307,6 +334,7 @@ def run_reference(args, w, T, layers):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w, T, layers, args),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "cpu_model": host_cpu_model(),
                          "sample": f"{sample_T} tokens of one {w.name} layer per step "
                                    f"(fp64 C oracle, {threads} threads)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -442,6 +470,22 @@ def main():
     tokens_per_step = T * layers
     value = job_throughput(tokens_per_step, world, ms_per_step)
 
+    # -------------------------------- per-step distribution (separate pass)
+    # one event between consecutive steps; the contract's number above is
+    # the bracketed total, this only adds its spread
+    n_dist = max(1, min(args.steps, 200))
+    step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_dist + 1)]
+    with torch.cuda.stream(stream):
+        step_evs[0].record(stream)
+        for i in range(n_dist):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+            step_evs[i + 1].record(stream)
+    stream.synchronize()
+    step_dist = percentiles([step_evs[i].elapsed_time(step_evs[i + 1]) for i in range(n_dist)])
+
     # --------------------------------------------- per-kernel (stage) timing
     # the same step with CUDA events at the stage boundaries, on the stream
     # the kernels run on
@@ -539,6 +583,7 @@ def main():
         ntok, secs, threads, nl = oracle_sample(host_layers, w, budget_s=10.0,
                                                 mode=scoring_mode(args))
         cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "cpu_model": host_cpu_model(),
                "sample": f"{nl} of the {layers} layers of one step, all {T} tokens each "
                          f"(fp64 C oracle, {threads} threads), {secs:.1f} s"}
 
@@ -552,7 +597,7 @@ def main():
         "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s",
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": names["launches"] * layers * args.steps,
-        "roofline": roofline, "cpu_baseline": cpu,
+        "roofline": roofline, "cpu_baseline": cpu, "step_ms": step_dist,
         "layer": {"algorithmic_GBps": layer_gbs, "TFLOPS": layer_tflops,
                   "frac_hbm": layer_gbs / hbm, "bytes_per_step": alg["bytes"],
                   "flops_per_step": alg["flops"],

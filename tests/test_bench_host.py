@@ -54,6 +54,14 @@ def test_single_rank_and_throughput():
     assert bench.job_throughput(1280, 2, 0.5) == pytest.approx(5.12e6)
 
 
+def test_step_percentiles_nearest_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    p = bench.percentiles([float(v) for v in range(10, 0, -1)])   # 1..10, unsorted
+    assert p == {"p10": 1.0, "median": 5.5, "p90": 9.0, "n": 10}
+    assert bench.percentiles([2.0]) == {"p10": 2.0, "median": 2.0, "p90": 2.0, "n": 1}
+
+
 def _reference(env_extra):
     env = dict(os.environ, **env_extra)
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
@@ -73,6 +81,7 @@ def test_reference_arm_prints_the_contract_line_on_rank_zero_only():
         assert key in j, key
     assert j["impl"] == "reference" and j["value"] > 0 and j["higher_is_better"] is True
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert isinstance(j["cpu_baseline"]["cpu_model"], str) and j["cpu_baseline"]["cpu_model"]
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
     assert j["config"]["workload"] == "tiny_fp32"
     assert _reference({"RANK": "1", "WORLD_SIZE": "2"}) == []
