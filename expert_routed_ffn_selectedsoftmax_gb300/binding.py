@@ -196,7 +196,8 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
     """The whole MoE layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [E,F,d], [E,F,d], [E,d,F]; or, with
-    w_dtype=MOE_Q8_0, uint8 buffers from moe_pack_q8_0 (then F is required).
+    w_dtype=MOE_Q8_0 / MOE_Q4_A64, uint8 buffers from moe_pack_q8_0 /
+    moe_pack_q4_a64 (then F is required).
     events: optional sequence of 6 torch.cuda.Event(enable_timing=True), recorded
     at the stage boundaries (moe_forward_profiled).
     scoring: a MOE_SCORE_* mode (moe_forward_scored when not SelectedSoftmax).
@@ -249,7 +250,8 @@ def moe_ffn_dense(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor,
     """A dense SwiGLU FFN layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [F,d], [F,d], [d,F] (or [1,F,d] ...); or,
-    with w_dtype=MOE_Q8_0, uint8 buffers from moe_pack_q8_0 (then F is required).
+    with w_dtype=MOE_Q8_0 / MOE_Q4_A64, uint8 buffers from moe_pack_q8_0 /
+    moe_pack_q4_a64 (then F is required).
     """
     L = load_library()
     T, d = x.shape
