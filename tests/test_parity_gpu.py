@@ -138,6 +138,8 @@ SMALL = [
     (wl.BF16, wl.Q4_A64, 70, 512, 16, 1, 192),
     (wl.BF16, wl.BF16, 5, 512, 64, 8, 128),     # few tokens: largest E and k of the small-batch router
     (wl.BF16, wl.BF16, 8, 2048, 33, 3, 128),    # few tokens: ragged E, longest rows
+    (wl.BF16, wl.BF16, 40, 256, 256, 8, 128),   # the largest E and k the library takes
+    (wl.F32, wl.F32, 20, 64, 256, 8, 64),
 ]
 
 
@@ -280,6 +282,7 @@ PREFILL_SMALL = [
     (520, 1024, 64, 2, 512),
     (777, 2048, 16, 1, 256),
     (600, 256, 4, 1, 1024),     # k == 1, long F: the down GEMM splits K in two halves
+    (700, 256, 256, 8, 128),    # the largest E and k: 5600 rows over 256 small groups
 ]
 
 
