@@ -233,8 +233,33 @@ def profile_traffic(kernel_key):
                        kernel_key.split(":")[0])
     if not os.path.exists(src):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["bytes"] if sha == rec["sha"] else None
+    return rec["bytes"] if code_sha(open(src).read()) == rec["sha"] else None
+
+
+def code_sha(text):
+    """sha256[:16] of a C/CUDA source with comments and whitespace removed, so
+    that a recorded capture stays valid across comment-only edits (string
+    literals, e.g. inline PTX, are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch == '"':                               # string literal: copy through
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    code = "".join(out).split()
+    return hashlib.sha256(" ".join(code).encode()).hexdigest()[:16]
 
 
 # ------------------------------------------------------------- CPU oracle

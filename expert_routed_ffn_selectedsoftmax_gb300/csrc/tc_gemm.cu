@@ -104,7 +104,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 
 // Per-variant shared-memory layout: a ring of STAGES stages {A, this CTA's
-// part of B (16-bit) or of Bq (int8) + its scales}, then (Q8 only) two
+// part of B (16-bit) or of Bq (int8) + its scales}, then (Q8 only) CVT
 // converted fp16 B buffers, then the control block.
 template <bool Q8, bool PAIR> struct Cfg {
     static constexpr int CL = PAIR ? 2 : 1;

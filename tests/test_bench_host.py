@@ -62,6 +62,17 @@ def test_step_percentiles_nearest_rank():
     assert bench.percentiles([2.0]) == {"p10": 2.0, "median": 2.0, "p90": 2.0, "n": 1}
 
 
+def test_traffic_record_survives_comment_edits_only():
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int f(int a) { // one\n  return a + 1; /* two */ }\nconst char *s = "a // b";\n'
+    same = 'int f(int a) {\n  /* other words */ return a + 1; }  const char *s = "a // b";'
+    assert bench.code_sha(src) == bench.code_sha(same)
+    assert bench.code_sha(src) != bench.code_sha(src.replace("a + 1", "a + 2"))
+    assert bench.code_sha(src) != bench.code_sha(src.replace('"a // b"', '"a // c"'))
+    assert bench.profile_traffic("decode_tc.cu:down:no_such_workload:T1") is None
+
+
 def _reference(env_extra):
     env = dict(os.environ, **env_extra)
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
