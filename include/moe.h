@@ -192,8 +192,9 @@ MOE_API size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype a
 /*
  * moe_forward -- the whole layer, steps 1-5.
  *   x[T,d] (act_dt), w_router[E,d] (act_dt), sel_bias[E] fp32 or NULL,
- *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0: packed by
- *   moe_pack_q8_0), out[T,d] fp32 (overwritten).
+ *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64: the
+ *   buffers written by moe_pack_q8_0 / moe_pack_q4_a64, 256-byte aligned),
+ *   out[T,d] fp32 (overwritten).
  *   workspace: device scratch of at least moe_workspace_size() bytes,
  *   256-byte aligned; it must not be shared by calls that can overlap.
  *   path: a moe_path value.  MOE_PATH_PREFILL needs bf16 activations,
@@ -243,9 +244,10 @@ MOE_API moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, in
  *   §Model architecture: dense FFN layers beside the MoE ones; "New Community
  *   Model: ZONOS3-Mini (Zyphra) - #1271", §Summary: layer 0 has a dense SwiGLU
  *   FFN).  No router: every token goes to the one expert with weight 1.
- *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0: packed by
- *   moe_pack_q8_0 with rows = F or d); other arguments as moe_forward, with a
- *   workspace of moe_workspace_size(T, d, 1, 1, F, act_dt, w_dt) bytes.
+ *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64: packed by
+ *   moe_pack_q8_0 / moe_pack_q4_a64 with rows = F or d); other arguments as
+ *   moe_forward, with a workspace of moe_workspace_size(T, d, 1, 1, F, act_dt,
+ *   w_dt) bytes.
  */
 MOE_API moe_status moe_ffn_dense(const void *x, moe_dtype act_dt, int T, int d,
                                  const void *w_gate, const void *w_up, const void *w_down,
