@@ -249,6 +249,38 @@ def test_forward_decode_workloads_full(name, T):
     check_output(out.cpu().numpy(), layer, ref, idx_ref, margin, idx_gpu=idx_g)
 
 
+@pytest.mark.parametrize("name", ["zonos3_mini_decode", "zonos2_decode", "zonos3_mini_prefill",
+                                  "zonos2_prefill_q8"])
+def test_graph_replay_equals_direct_launch(name):
+    """The benchmark times CUDA-graph replays of the layer (warm-up launches on a
+    side stream, capture on that stream, replay): at full size, a replay writes
+    the same bits as a direct launch of the same layer."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    layer = wl.make_layer(wl.WORKLOADS[name], seed=4)
+    t = upload_layer(layer, DEV)
+    ws = torch.empty(pkg.moe_workspace_size(layer.T, layer.d, layer.E, layer.k, layer.F,
+                                            layer.act_dtype, layer.w_dtype),
+                     dtype=torch.uint8, device=DEV)
+    direct = torch.empty((layer.T, layer.d), dtype=torch.float32, device=DEV)
+    replay = torch.empty_like(direct)
+    s = torch.cuda.Stream(device=DEV)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            gpu_forward(layer, DEV, t=t, out=direct, workspace=ws)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gpu_forward(layer, DEV, t=t, out=replay, workspace=ws)
+    replay.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()
+    s.synchronize()
+    assert torch.equal(direct, replay)
+    assert pkg.moe_check(ws) == 0
+
+
 @pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8"])
 @pytest.mark.parametrize("path", [DECODE, 0])
 def test_forward_prefill_workloads_sampled(name, path):
