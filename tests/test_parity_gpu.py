@@ -313,7 +313,7 @@ PREFILL_SMALL = [
     (2048, 256, 16, 1, 384),
     (520, 1024, 64, 2, 512),
     (777, 2048, 16, 1, 256),
-    (600, 256, 4, 1, 1024),     # k == 1, long F: the down GEMM splits K in two halves
+    (600, 256, 4, 1, 1024),     # k == 1 (plain stores), long F: 16 k-blocks per down tile
     (700, 256, 256, 8, 128),    # the largest E and k: 5600 rows over 256 small groups
 ]
 
@@ -381,7 +381,7 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
 
 
 @pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
-@pytest.mark.parametrize("k,F", [(2, 128), (1, 1024)])   # (1, 1024): K split in the down GEMM
+@pytest.mark.parametrize("k,F", [(2, 128), (1, 1024)])   # (1, 1024): long K in the down GEMM
 def test_prefill_deterministic_and_equivariant(wdt, k, F):
     layer = wl.make_custom_layer(24, T=512, d=256, E=8, k=k, F=F, act_dtype=wl.BF16,
                                  w_dtype=wdt)
