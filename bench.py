@@ -571,32 +571,89 @@ def main():
     dx = [torch.empty_like(L["x"]) for L in stack]
     n_e2e = max(1, min(args.steps, 200))
 
-    def e2e_step():
-        for i in range(layers):
-            dx[i].copy_(hx[i], non_blocking=True)
-        for i in range(layers):
-            L = stack[i]
-            if args.dense:
-                pkg.moe_ffn_dense(dx[i], L["w_gate"], L["w_up"], L["w_down"], F=w.F,
-                                  w_dtype=w_dt, out=outs[i], workspace=ws)
-            else:
-                pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"],
-                                L["w_down"], w.k, F=w.F, w_dtype=w_dt, out=outs[i],
-                                workspace=ws, scoring=scoring_mode(args))
-        for i in range(layers):
-            hout[i].copy_(outs[i], non_blocking=True)
-    with torch.cuda.stream(stream):
+    def e2e_layer(i):
+        L = stack[i]
+        if args.dense:
+            pkg.moe_ffn_dense(dx[i], L["w_gate"], L["w_up"], L["w_down"], F=w.F,
+                              w_dtype=w_dt, out=outs[i], workspace=ws)
+        else:
+            pkg.moe_forward(dx[i], L["w_router"], L["bias"], L["w_gate"], L["w_up"],
+                            L["w_down"], w.k, F=w.F, w_dtype=w_dt, out=outs[i],
+                            workspace=ws, scoring=scoring_mode(args))
+
+    def e2e_serial():
+        """Every copy and layer in order on one stream."""
+        def one_step():
+            for i in range(layers):
+                dx[i].copy_(hx[i], non_blocking=True)
+            for i in range(layers):
+                e2e_layer(i)
+            for i in range(layers):
+                hout[i].copy_(outs[i], non_blocking=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                one_step()
+        stream.synchronize()
+        barrier()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n_e2e):
+                one_step()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / n_e2e
+
+    def e2e_pipelined():
+        """Copies on two copy streams: the host-to-device copy of layer i+1 and
+        the device-to-host copy of layer i-1 run while layer i computes.  Layer
+        i waits for its input copy and for the previous step's read-back of
+        out[i]; the input copy of the next step waits for layer i to finish
+        reading x[i].  The timed region ends after the last read-back."""
+        h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(layers)]     # x[i] on the device
+        ev_done = [torch.cuda.Event() for _ in range(layers)]   # layer i computed
+        ev_back = [torch.cuda.Event() for _ in range(layers)]   # out[i] read back
+        state = {"first": True}
+
+        def one_step():
+            first = state["first"]
+            for i in range(layers):
+                with torch.cuda.stream(h2d_s):
+                    if not first:
+                        h2d_s.wait_event(ev_done[i])
+                    dx[i].copy_(hx[i], non_blocking=True)
+                    ev_in[i].record(h2d_s)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(ev_in[i])
+                    if not first:
+                        stream.wait_event(ev_back[i])
+                    e2e_layer(i)
+                    ev_done[i].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(ev_done[i])
+                    hout[i].copy_(outs[i], non_blocking=True)
+                    ev_back[i].record(d2h_s)
+            state["first"] = False
+
         for _ in range(3):
-            e2e_step()
-    stream.synchronize()
-    barrier()
-    with torch.cuda.stream(stream):
+            one_step()
+        torch.cuda.synchronize(dev)
+        barrier()
         e0.record(stream)
+        h2d_s.wait_event(e0)
         for _ in range(n_e2e):
-            e2e_step()
+            one_step()
+        for i in range(layers):
+            stream.wait_event(ev_back[i])
         e1.record(stream)
-    stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n_e2e
+
+    try:
+        e2e_ms, e2e_mode = e2e_pipelined(), "copies overlapped with compute"
+    except Exception as exc:   # keep the serial measurement if stream pipelining fails
+        torch.cuda.synchronize(dev)
+        e2e_ms, e2e_mode = e2e_serial(), f"serial (overlap failed: {str(exc)[:120]})"
     e2e_value = tokens_per_step * world / (e2e_ms * 1e-3)
     h2d = sum(t.numel() * t.element_size() for t in hx)
     d2h = sum(t.numel() * t.element_size() for t in hout)
@@ -619,7 +676,7 @@ def main():
         "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands",
                   wl.Q4_A64: "affine 4-bit weights, f32 CUDA-core arithmetic"}[w.w_dtype],
         "data": "synthetic", "config": config_dict(w, T, layers, args),
-        "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s",
+        "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s", "mode": e2e_mode,
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": names["launches"] * layers * args.steps,
         "roofline": roofline, "cpu_baseline": cpu, "step_ms": step_dist,
