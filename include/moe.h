@@ -200,8 +200,12 @@ MOE_API size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype a
  *   path: a moe_path value.  MOE_PATH_PREFILL needs bf16 activations,
  *   bf16 or Q8_0 weights, d % 256 == 0 and F % 128 == 0, and returns
  *   MOE_ERR_UNSUPPORTED otherwise.
- *   Summation order is fixed on every path except the CUDA-core decode
- *   kernels with k > 2 (fp32 atomics): results are bitwise reproducible.
+ *   Reproducibility: with k <= 2 every path gives bitwise identical results
+ *   from run to run, and so do the tensor-core decode kernels (bf16 weights,
+ *   d and F multiples of 128, T*k <= 8192) for every k.  With k > 2 the
+ *   CUDA-core decode kernels and the prefill GEMMs add each token's k expert
+ *   outputs into out with fp32 atomics in arrival order, so the last bits can
+ *   differ between runs.
  */
 MOE_API moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                        const float *sel_bias, int E, int k, const void *w_gate,
