@@ -74,6 +74,13 @@ def job_throughput(tokens_per_step_per_rank, world, ms_per_step):
     return tokens_per_step_per_rank * world / (ms_per_step * 1e-3)
 
 
+def layer_roofline_frac(bytes_, flops, seconds, hbm_gbs, tflops):
+    """Achieved fraction of the layer's roofline: the slower of its bytes at HBM
+    bandwidth and its flops at the tensor peak, over the measured time."""
+    bound = max(bytes_ / (hbm_gbs * 1e9), flops / (tflops * 1e12))
+    return bound / seconds
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -694,7 +701,10 @@ def main():
         "gpu_launches": names["launches"] * layers * args.steps,
         "roofline": roofline, "cpu_baseline": cpu, "step_ms": step_dist,
         "layer": {"algorithmic_GBps": layer_gbs, "TFLOPS": layer_tflops,
-                  "frac_hbm": layer_gbs / hbm, "bytes_per_step": alg["bytes"],
+                  "frac_hbm": layer_gbs / hbm,
+                  "roofline_frac": layer_roofline_frac(alg["bytes"], alg["flops"], ms_per_step * 1e-3,
+                                                       hbm, tflops_peak),
+                  "bytes_per_step": alg["bytes"],
                   "flops_per_step": alg["flops"],
                   "active_experts_per_layer": alg["active"],
                   "stage_us": dict(zip(stage_names, [round(float(v), 3) for v in stage_us]))},

@@ -54,6 +54,17 @@ def test_single_rank_and_throughput():
     assert bench.job_throughput(1280, 2, 0.5) == pytest.approx(5.12e6)
 
 
+def test_layer_roofline_fraction_takes_the_slower_bound():
+    sys.path.insert(0, ROOT)
+    import bench
+    # 6.8 GB at 6.8 TB/s = 1 ms; 1.9 TFLOP at 1.9 PF = 1 ms; measured 2 ms -> 0.5
+    assert bench.layer_roofline_frac(6.8e9, 1.9e12, 2e-3, 6800.0, 1900.0) == pytest.approx(0.5)
+    # bytes-bound: flops negligible
+    assert bench.layer_roofline_frac(6.8e9, 1.0, 4e-3, 6800.0, 1900.0) == pytest.approx(0.25)
+    # flops-bound: 3.8 TFLOP = 2 ms at peak, measured 2.5 ms
+    assert bench.layer_roofline_frac(1.0, 3.8e12, 2.5e-3, 6800.0, 1900.0) == pytest.approx(0.8)
+
+
 def test_step_percentiles_nearest_rank():
     sys.path.insert(0, ROOT)
     import bench
