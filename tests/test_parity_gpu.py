@@ -50,11 +50,12 @@ ROUTE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("seed", [1, 7, 13])
 @pytest.mark.parametrize("name,T", ROUTE_CASES)
-def test_route_matches_oracle(name, T):
+def test_route_matches_oracle(name, T, seed):
     w = wl.WORKLOADS[name]
     # only x, W_r and the bias matter for routing: draw a small-F layer
-    layer = wl.make_layer(w, seed=1, T=T, F=32 if w.w_dtype != wl.Q8_0 else 32)
+    layer = wl.make_layer(w, seed=seed, T=T, F=32)
     idx, wts = _route(layer)
     idx_ref, w_ref, margin = _oracle_route(layer)
     ok = compare_routing(idx, wts, idx_ref, w_ref, margin, layer.k)
