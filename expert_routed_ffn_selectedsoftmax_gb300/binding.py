@@ -11,6 +11,7 @@ import ctypes
 import os
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -27,7 +28,7 @@ EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "mo
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_q4_a64_packed_size", "moe_pack_q4_a64",
            "moe_workspace_size", "moe_forward",
            "moe_forward_profiled", "moe_forward_scored", "moe_ffn_dense", "moe_forward_noalloc",
-           "moe_check")
+           "moe_workspace_views", "moe_check", "moe_check_noalloc")
 
 _lib = None
 
@@ -87,8 +88,12 @@ def load_library():
     L.moe_ffn_dense.restype = i
     L.moe_forward_noalloc.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, i, vp]
     L.moe_forward_noalloc.restype = i
+    L.moe_workspace_views.argtypes = [i, i, i, i, i, i, i, vp]
+    L.moe_workspace_views.restype = i
     L.moe_check.argtypes = [vp, vp, vp]
     L.moe_check.restype = i
+    L.moe_check_noalloc.argtypes = [vp, vp]
+    L.moe_check_noalloc.restype = i
     _lib = L
     return L
 
@@ -296,6 +301,49 @@ def moe_forward_noalloc(x: torch.Tensor, w_router: torch.Tensor,
                                  k, _ptr(w_gate), _ptr(w_up), _ptr(w_down), w_dtype, F, _ptr(out),
                                  path, _stream(x)), "moe_forward_noalloc")
     return out
+
+
+VIEW_NAMES = ("topk_idx", "topk_w", "counts", "offsets", "perm_tok", "inv", "perm_w")
+
+
+def moe_workspace_views(T: int, d: int, E: int, k: int, F: int, act_dt: int, w_dt: int) -> dict:
+    """Byte offsets of the routing / grouping arrays a layer call leaves in its
+    workspace: {name: offset} for VIEW_NAMES."""
+    L = load_library()
+    views = (ctypes.c_size_t * 7)()
+    _check(L.moe_workspace_views(T, d, E, k, F, act_dt, w_dt, views), "moe_workspace_views")
+    return dict(zip(VIEW_NAMES, [int(v) for v in views]))
+
+
+def read_routing(workspace: torch.Tensor, T: int, d: int, E: int, k: int, F: int, act_dt: int,
+                 w_dt: int) -> dict:
+    """The routing and grouping a layer call wrote into `workspace` (read after
+    the call's stream work completed): views of the workspace bytes, as
+    torch tensors on its device."""
+    off = moe_workspace_views(T, d, E, k, F, act_dt, w_dt)
+    n = T * k
+    shapes = {"topk_idx": ((T, k), torch.int32), "topk_w": ((T, k), torch.float32),
+              "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32),
+              "perm_tok": ((n,), torch.int32), "inv": ((n,), torch.int32),
+              "perm_w": ((n,), torch.float32)}
+    out = {}
+    for name, (shape, dt) in shapes.items():
+        count = int(np.prod(shape))
+        raw = workspace[off[name]:off[name] + 4 * count]
+        out[name] = raw.view(dt).reshape(shape)
+    return out
+
+
+def moe_check_noalloc() -> int:
+    """moe_check for moe_forward_noalloc's static scratch on the current device."""
+    L = load_library()
+    word = ctypes.c_uint32(0)
+    _check(L.moe_check_noalloc(ctypes.byref(word), _stream_current()), "moe_check_noalloc")
+    return word.value
+
+
+def _stream_current():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def moe_check(workspace: torch.Tensor) -> int:

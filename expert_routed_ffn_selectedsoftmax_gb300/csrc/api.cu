@@ -91,15 +91,50 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     return L;
 }
 
-int device_sm_count()
+}  // namespace
+
+namespace moe {
+
+moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                              const float *sel_bias, int E, int k, const void *w_gate,
+                              const void *w_up, const void *w_down, moe_dtype w_dt, int F,
+                              const float *out, int path, int scoring, bool dense)
 {
-    int dev = 0, n = 0;
-    // (a failed query falls back to the GB300's 152 SMs; the launch then reports the error)
-    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-        return 152;
-    return n;
+    if (!scoring_ok(scoring)) return MOE_ERR_INVALID_ARG;
+    // (dense: no router; the router checks then cover x alone)
+    moe_status st = check_route_args(x, act_dt, T, d, dense ? x : w_router, dense ? nullptr : sel_bias,
+                                     E, k);
+    if (st != MOE_OK) return st;
+    if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
+    if (!weights_ok(act_dt, w_dt)) {
+        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64)
+                   ? MOE_ERR_UNSUPPORTED
+                   : MOE_ERR_INVALID_ARG;
+    }
+    if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
+    if (w_dt == MOE_Q4_A64 && (d % 64 || F % 64)) return MOE_ERR_INVALID_ARG;
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL &&
+        path != MOE_PATH_DECODE_SIMT)
+        return MOE_ERR_INVALID_ARG;
+    const bool can_prefill = prefill_capable(act_dt, w_dt, d, F) && tc_gemm_supports(w_dt) &&
+                             tc_gemm_available();
+    if (path == MOE_PATH_PREFILL && !can_prefill) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    if (w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64) {
+        const uintptr_t m = 255u;
+        if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
+            (reinterpret_cast<uintptr_t>(w_down) & m))
+            return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
 }
+
+}  // namespace moe
+
+namespace {
 
 // the layer (defined below; `dense`: see there)
 moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
@@ -126,7 +161,7 @@ const char *moe_status_str(int status)
     }
 }
 
-int moe_version(void) { return 100; }
+int moe_version(void) { return 101; }
 
 moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                      const float *sel_bias, int E, int k, int32_t *topk_idx, float *topk_w,
@@ -148,7 +183,14 @@ moe_status moe_route_scored(const void *x, moe_dtype act_dt, int T, int d, const
     if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
         return MOE_ERR_INVALID_ARG;
     cudaError_t e;
-    if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
+    if (route_small_capable(act_dt, T, d, E, k)) {
+        // the clustered router moe_forward runs on bf16 decode batches (routing only)
+        RouteTcArgs a{};
+        a.x = x; a.w_router = w_router; a.bias = sel_bias; a.T = T; a.d = d; a.E = E; a.k = k;
+        a.mode = scoring;
+        a.topk_idx = topk_idx; a.topk_w = topk_w;
+        e = launch_route_small(a, static_cast<cudaStream_t>(stream));
+    } else if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
         RouteTcArgs a{};
         a.x = x; a.w_router = w_router; a.bias = sel_bias; a.T = T; a.d = d; a.E = E; a.k = k;
         a.mode = scoring;
@@ -220,6 +262,16 @@ size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype act_dt, m
     return ws_layout(T, d, E, k, F, act_dt, w_dt).total;
 }
 
+moe_status moe_workspace_views(int T, int d, int E, int k, int F, moe_dtype act_dt,
+                               moe_dtype w_dt, size_t *views)
+{
+    if (!views || moe_workspace_size(T, d, E, k, F, act_dt, w_dt) == 0) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, F, act_dt, w_dt);
+    views[0] = L.topk_idx; views[1] = L.topk_w; views[2] = L.counts; views[3] = L.offsets;
+    views[4] = L.perm_tok; views[5] = L.inv; views[6] = L.perm_w;
+    return MOE_OK;
+}
+
 moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                        const float *sel_bias, int E, int k, const void *w_gate,
                        const void *w_up, const void *w_down, moe_dtype w_dt, int F,
@@ -275,36 +327,12 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
                         size_t ws_bytes, int path, int scoring, bool dense, void *const *events,
                         moe_stream stream)
 {
-    if (!scoring_ok(scoring)) return MOE_ERR_INVALID_ARG;
-    // (dense: no router; the router checks then cover x alone)
-    moe_status st = check_route_args(x, act_dt, T, d, dense ? x : w_router, dense ? nullptr : sel_bias,
-                                     E, k);
-    if (st != MOE_OK) return st;
-    if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
-    if (!weights_ok(act_dt, w_dt)) {
-        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64)
-                   ? MOE_ERR_UNSUPPORTED
-                   : MOE_ERR_INVALID_ARG;
-    }
-    if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
-    if (w_dt == MOE_Q4_A64 && (d % 64 || F % 64)) return MOE_ERR_INVALID_ARG;
-    if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL &&
-        path != MOE_PATH_DECODE_SIMT)
-        return MOE_ERR_INVALID_ARG;
+    moe_status st = forward_args_check(x, act_dt, T, d, w_router, sel_bias, E, k, w_gate, w_up,
+                                       w_down, w_dt, F, out, path, scoring, dense);
+    if (st != MOE_OK || T == 0) return st;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MOE_ERR_INVALID_ARG;
     const bool can_prefill = prefill_capable(act_dt, w_dt, d, F) && tc_gemm_supports(w_dt) &&
                              tc_gemm_available();
-    if (path == MOE_PATH_PREFILL && !can_prefill) return MOE_ERR_UNSUPPORTED;
-    if (T == 0) return MOE_OK;
-    if (!w_gate || !w_up || !w_down || !out || !workspace) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
-        return MOE_ERR_INVALID_ARG;
-    if (w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64) {
-        const uintptr_t m = 255u;
-        if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
-            (reinterpret_cast<uintptr_t>(w_down) & m))
-            return MOE_ERR_INVALID_ARG;
-    }
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, d, E, k, F, act_dt, w_dt);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 

@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/moe.h"
@@ -203,6 +204,13 @@ inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 bl
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Record a device-detected error in the status word (calls without a status
+// word -- moe_route, moe_route_scored -- have none to report to).
+__device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bits)
+{
+    if (status) atomicOr(status, bits);
+}
+
 // True (uniformly across the CTA) when an earlier kernel of this call has
 // already recorded an error in the status word: the caller then returns
 // without touching scratch whose contents may be incomplete.
@@ -213,6 +221,41 @@ __device__ __forceinline__ bool upstream_failed(const uint32_t *status)
     __syncthreads();
     return failed != 0;
 }
+
+// ------------------------------------------------------ host: per-device state
+// Index of the current device (0 when the query fails; the launch that
+// follows then reports the error).
+inline int current_device()
+{
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 ? dev : 0;
+}
+// Streaming multiprocessors of the current device (read per call, so grids
+// follow the part the process runs on; a failed query gives 1 and the launch
+// reports the error).
+inline int device_sm_count()
+{
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, current_device()) !=
+            cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+// Set-up that every device needs once (kernel attributes, occupancy
+// queries), remembered per device: devices 0-63 are cached, any further
+// device repeats the set-up on each call.
+constexpr int kCachedDevices = 64;
+struct PerDeviceFlag {
+    std::atomic<uint64_t> bits{0};
+    bool done(int dev) const { return dev < kCachedDevices && ((bits.load() >> dev) & 1u); }
+    void mark(int dev) { if (dev < kCachedDevices) bits.fetch_or(uint64_t(1) << dev); }
+};
+struct PerDeviceInt {   // -1 = not cached yet
+    std::atomic<int> v[kCachedDevices];
+    PerDeviceInt() { for (auto &x : v) x.store(-1); }
+    int get(int dev) const { return dev < kCachedDevices ? v[dev].load() : -1; }
+    void put(int dev, int value) { if (dev < kCachedDevices) v[dev].store(value); }
+};
 
 // -------------------------------------------------------------- warp helpers
 __device__ __forceinline__ float warp_sum(float v)

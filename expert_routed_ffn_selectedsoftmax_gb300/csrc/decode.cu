@@ -230,8 +230,10 @@ template <typename AT, typename WT, int NCH, int RPW>
 static cudaError_t launch_gateup(const DecodeArgs &a, WView<WT> wg, WView<WT> wu, cudaStream_t stream)
 {
     auto k1 = decode_gateup_kernel<AT, WT, NCH, RPW>;
-    static std::atomic<int> occ{0};
-    if (occ.load() == 0) occ.store(blocks_per_sm(k1));
+    static PerDeviceInt occ_cache;
+    const int dev = current_device();
+    int occ = occ_cache.get(dev);
+    if (occ <= 0) { occ = blocks_per_sm(k1); occ_cache.put(dev, occ); }
     const int n_exp = a.E < a.T * a.k ? a.E : a.T * a.k;   // experts that can be active
     const long long items = (long long)n_exp * ((a.F + kDecWarps * RPW - 1) / (kDecWarps * RPW));
     int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);
@@ -245,8 +247,10 @@ template <typename WT, int NCH, int RPW>
 static cudaError_t launch_down(const DecodeArgs &a, WView<WT> wd, cudaStream_t stream)
 {
     auto k2 = decode_down_kernel<WT, NCH, RPW>;
-    static std::atomic<int> occ{0};
-    if (occ.load() == 0) occ.store(blocks_per_sm(k2));
+    static PerDeviceInt occ_cache;
+    const int dev = current_device();
+    int occ = occ_cache.get(dev);
+    if (occ <= 0) { occ = blocks_per_sm(k2); occ_cache.put(dev, occ); }
     const int n_exp = a.E < a.T * a.k ? a.E : a.T * a.k;
     const long long items = (long long)n_exp * ((a.d + kDecWarps * RPW - 1) / (kDecWarps * RPW));
     int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);

@@ -74,7 +74,7 @@ constexpr int THREADS = 192;
 constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
 constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
 constexpr int TMEM_COLS = 128;
-constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~1 item per CTA: 2 CTAs per SM on 152 SMs
+constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~1 item per CTA: 2 CTAs per SM on a 152-SM GB300
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
@@ -257,7 +257,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             }
         }
         if (!ok) {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             for (uint32_t j = (it_k >= STAGES ? it_k - STAGES : 0); j < it_k; ++j) {
                 volatile int no_abort = 0;
@@ -298,7 +298,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             umma_commit(&c.tfull[acc]);
         }
         if (!ok) {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             umma_commit(&c.drain);
             volatile int no_abort = 0;
@@ -339,7 +339,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             }
         }
         if (!ok) {
-            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            if (lane == 0) flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
     } else if (warp >= 2 && warp < 6) {
@@ -407,7 +407,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 if (j < it.nrows) dst[(size_t)j * p.R] = __uint_as_float(v[j]);
         }
         if (!ok) {
-            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            if (lane == 0) flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
     }
@@ -587,8 +587,9 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
 
     cudaError_t err;
     const size_t smem = smem_bytes();
-    static std::atomic<int> attr_done{0};
-    if (!attr_done.load()) {
+    static PerDeviceFlag attr_done;
+    const int dev = current_device();
+    if (!attr_done.done(dev)) {
         if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
                 cudaSuccess ||
@@ -599,7 +600,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
                 cudaSuccess)
             return err;
-        attr_done.store(1);
+        attr_done.mark(dev);
     }
     const long long n_exp = a.E < rows ? a.E : rows;
     auto grid_for = [&](long long max_items) {

@@ -8,6 +8,14 @@
 
 namespace moe {
 
+// api.cu -- moe_forward's argument checks that do not involve the workspace
+// (in moe_forward's order); MOE_OK when they pass.  `dense`: moe_ffn_dense
+// (no router; w_router and sel_bias are ignored).
+moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
+                              const float *sel_bias, int E, int k, const void *w_gate,
+                              const void *w_up, const void *w_down, moe_dtype w_dt, int F,
+                              const float *out, int path, int scoring, bool dense);
+
 // route.cu
 size_t route_smem_bytes(int tpb, int d, int E);
 // out_zero: rows [T, d] to zero (or NULL); zero_words[n_zero]: scratch words
@@ -52,8 +60,8 @@ cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cu
 
 // route_small.cu -- routing and grouping in one clustered kernel for T <= 128
 // (bf16 activations): writes topk_idx/topk_w and counts, offsets, perm_tok,
-// inv, perm_w, and zeroes out_zero and zero_words when given; ignores rank,
-// tile_cnt and xp.
+// inv, perm_w (counts == NULL: routing only), and zeroes out_zero and
+// zero_words when given; ignores rank, tile_cnt and xp.
 bool route_small_capable(int act_dt, int T, int d, int E, int k);
 cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream);
 

@@ -117,7 +117,7 @@ permute_kernel(const int32_t *__restrict__ topk_idx, int n, int k, int E,
         }
         __syncwarp();
     }
-    if (bad && status) atomicOr(status, kDevCheckFailed);
+    if (bad) flag_status(status, kDevCheckFailed);
 }
 
 cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *counts,

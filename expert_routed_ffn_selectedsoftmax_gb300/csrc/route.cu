@@ -271,7 +271,8 @@ int route_tokens_per_block(int T, int d, int E)
     // keep the staged rows within ~96 KB; small T favours many CTAs
     int tpb = kRouteMaxTpb;
     while (tpb > 1 && route_smem_bytes(tpb, d, E) > 96 * 1024) tpb >>= 1;
-    while (tpb > 1 && (T + tpb - 1) / tpb < 2 * 152) tpb >>= 1;
+    const int sms = device_sm_count();
+    while (tpb > 1 && (T + tpb - 1) / tpb < 2 * sms) tpb >>= 1;
     return tpb;
 }
 

@@ -227,7 +227,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
                     umma_f16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (j | kk) != 0);
             }
         } else {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             volatile int no_abort = 0;   // let the loads land before the CTA moves on
             mbar_wait(&c.full, 0, &no_abort);
@@ -238,7 +238,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         const int quarter = warp & 3;
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&c.tfull, 0, abort_flag));
         if (!ok) {
-            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            if (lane == 0) flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
         } else if (quarter * 32 < p.T) {
             tc_fence_after();
@@ -283,7 +283,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         bool got = true;
         if (mine_rows > 0 && !mbar_wait(&c.rx, 0, abort_flag)) {
             got = false;
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
         const bool mine = got && tok < p.tpc && t < p.T && !c.abort_flag;
@@ -373,7 +373,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         bulk_commit();
     }
     if (!mbar_wait(&c.mx, 0, abort_flag)) {
-        atomicOr(p.status, kDevTimeout);
+        flag_status(p.status, kDevTimeout);
         c.abort_flag = 1;
     }
 
@@ -412,18 +412,18 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         if (lane == 31) c.off[E] = incl;
     }
     __syncthreads();
-    if (rank == 0) {
+    if (rank == 0 && p.counts) {
         for (int e = threadIdx.x; e < E; e += THREADS) { p.counts[e] = c.tot[e]; p.offsets[e] = c.off[e]; }
         if (threadIdx.x == 0) p.offsets[E] = c.off[E];
     }
-    // slot (owned token i, choice j) -> grouped row
-    for (int s = threadIdx.x; s < p.tpc * p.k; s += THREADS) {
+    // slot (owned token i, choice j) -> grouped row (routing only: no grouping outputs)
+    for (int s = threadIdx.x; p.counts && s < p.tpc * p.k; s += THREADS) {
         const int i = s / p.k, j = s - i * p.k, t = tbase + i;
         if (t >= p.T || c.abort_flag) continue;
         const int e = c.sel_e[i][j];
         const int pos = c.off[e] + c.pre[e] + __popc(c.mask[e] & ((1u << i) - 1u));
         if (pos < 0 || pos >= p.T * p.k) {   // cannot happen with consistent masks
-            if (p.status) atomicOr(p.status, kDevCheckFailed);
+            flag_status(p.status, kDevCheckFailed);
             continue;
         }
         p.perm_tok[pos] = t;
@@ -477,15 +477,16 @@ cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream)
         !tc::make_map(&m_w, a.w_router, (uint64_t)a.E, a.d, EP, bf))
         return cudaErrorInvalidValue;
     cudaError_t err;
-    static std::atomic<int> attr_done{0};
-    if (!attr_done.load()) {
+    static PerDeviceFlag attr_done;
+    const int dev = current_device();
+    if (!attr_done.done(dev)) {
         const int mx = (int)kSmemCap;
         if ((err = cudaFuncSetAttribute(route_small_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(route_small_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(route_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(route_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess)
             return err;
-        attr_done.store(1);
+        attr_done.mark(dev);
     }
     Params p{};
     p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.R = R; p.kblocks = kblocks;

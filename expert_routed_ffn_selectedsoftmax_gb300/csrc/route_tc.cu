@@ -159,7 +159,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tma_load_2d(smem + s * SLOT + A_BYTES, &tm_w, &c.full[s], kb * BK, 0);
         }
         if (!ok) {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             for (int j = (kb >= STAGES ? kb - STAGES : 0); j < kb; ++j) {
                 volatile int no_abort = 0;
@@ -186,7 +186,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if (ok) {
             umma_commit(&c.tfull);
         } else {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             umma_commit(&c.tfull);   // drains the MMAs in flight; the epilogue sees the abort
         }
@@ -198,7 +198,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const bool valid = t < p.T;
         bool ok = mbar_wait(&c.tfull, 0, abort_flag);
         if (!ok) {
-            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            if (lane == 0) flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
         ok = __all_sync(0xffffffffu, ok);   // tcgen05.ld below is warp-collective
@@ -386,7 +386,7 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
             pos = (e >= 0 && e < E) ? off[e] + pre[e] + __ldcg(rank + slot) : -1;
             tok = (int)(slot / k);
             if (pos < 0 || pos >= nslots_all) {   // cannot happen with consistent routing
-                if (status) atomicOr(status, kDevCheckFailed);
+                flag_status(status, kDevCheckFailed);
                 pos = -1;
             } else {
                 perm_tok[pos] = tok;
@@ -453,7 +453,7 @@ cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cu
 {
     // enough CTAs that every SM gets a few warps of slots
     const int slots_per_tile = tile_tokens * a.k;
-    int parts = (2 * 152 + ntiles - 1) / ntiles;
+    int parts = (2 * device_sm_count() + ntiles - 1) / ntiles;
     const int max_parts = (slots_per_tile + 7) / 8;   // >= 1 slot per warp
     if (parts > max_parts) parts = max_parts;
     if (parts < 1) parts = 1;
@@ -482,14 +482,15 @@ cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream)
         return cudaErrorInvalidValue;
     cudaError_t err;
     const size_t smem = smem_bytes();
-    static std::atomic<int> attr_done{0};
-    if (!attr_done.load()) {
+    static PerDeviceFlag attr_done;
+    const int dev = current_device();
+    if (!attr_done.done(dev)) {
         if ((err = cudaFuncSetAttribute(route_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(route_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(route_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(route_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return err;
-        attr_done.store(1);
+        attr_done.mark(dev);
     }
     Params p{};
     p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.bias = a.bias; p.mode = a.mode;

@@ -370,7 +370,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             }
         }
         if (!ok) {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             // let loads already issued land before the CTA exits
             if (PAIR && !Q8 && rank != 0) {
@@ -430,7 +430,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             else umma_commit(&c.tfull[acc]);
         }
         if (!ok) {
-            atomicOr(p.status, kDevTimeout);
+            flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
             // wait for MMAs in flight before TMEM is freed
             if (PAIR) umma_commit_pair(&c.drain);
@@ -473,7 +473,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             }
         }
         if (!ok) {
-            if (lane == 0) atomicOr(p.status, kDevTimeout);
+            if (lane == 0) flag_status(p.status, kDevTimeout);
             c.abort_flag = 1;
         }
     } else if (warp >= 2 && warp < 2 + kEpiWarps) {
@@ -497,7 +497,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             const uint32_t acc_ph = (local_tile >> 1) & 1u;
             // warp-uniform outcome: tcgen05.ld below is warp-collective
             if (!warp_wait(&c.tfull[acc], acc_ph, abort_flag)) {
-                if (lane == 0) atomicOr(p.status, kDevTimeout);
+                if (lane == 0) flag_status(p.status, kDevTimeout);
                 c.abort_flag = 1;
                 break;
             }
@@ -674,8 +674,9 @@ template <bool Q8, bool PAIR>
 static cudaError_t set_smem_attrs()
 {
     using namespace tc;
-    static std::atomic<int> done{0};
-    if (done.load()) return cudaSuccess;
+    static PerDeviceFlag done;
+    const int dev = current_device();
+    if (done.done(dev)) return cudaSuccess;
     const int smem = (int)smem_bytes<Q8, PAIR>();
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8, PAIR>,
@@ -683,7 +684,7 @@ static cudaError_t set_smem_attrs()
         (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return err;
-    done.store(1);
+    done.mark(dev);
     return cudaSuccess;
 }
 
@@ -693,17 +694,18 @@ template <int MODE, bool Q8>
 static int max_active_pairs()
 {
     using namespace tc;
-    static std::atomic<int> cached{-1};
-    int n = cached.load();
+    static PerDeviceInt cached;
+    const int dev = current_device();
+    int n = cached.get(dev);
     if (n >= 0) return n;
     // the query needs the kernel's dynamic shared-memory limit raised first
     if (set_smem_attrs<Q8, true>() != cudaSuccess) {
         cudaGetLastError();
-        cached.store(0);
+        cached.put(dev, 0);
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 152);
+    cfg.gridDim = dim3(2 * device_sm_count());
     cfg.blockDim = dim3(Cfg<Q8, true>::THREADS);
     cfg.dynamicSmemBytes = smem_bytes<Q8, true>();
     cudaLaunchAttribute attr[1];
@@ -716,7 +718,7 @@ static int max_active_pairs()
     if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, Q8, true>, &cfg) != cudaSuccess)
         n = 0;
     cudaGetLastError();   // clear a failed query
-    cached.store(n);
+    cached.put(dev, n);
     return n;
 }
 

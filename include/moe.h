@@ -90,6 +90,10 @@ MOE_API int moe_version(void);
  *   then index ascending).
  *   topk_w[T,k] fp32 out: softmax over the kept experts' unbiased logits;
  *   with k == 1 every weight is exactly 1.0f.
+ *   Kernel: the router moe_forward runs for the same x -- the clustered
+ *   tensor-core router for bf16 batches of T <= 128 (moe_forward's bf16
+ *   decode path), the tensor-core router for bf16 batches of T >= 512, the
+ *   CUDA-core router otherwise.
  */
 MOE_API moe_status moe_route(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                      const float *sel_bias, int E, int k, int32_t *topk_idx, float *topk_w,
@@ -190,6 +194,29 @@ MOE_API size_t moe_workspace_size(int T, int d, int E, int k, int F, moe_dtype a
                           moe_dtype w_dt);
 
 /*
+ * moe_workspace_views -- where a layer call leaves its routing and token
+ * grouping (steps 2-3) inside its workspace, so that a caller can read back
+ * exactly what the layer's own kernels computed (for checking, or to reuse
+ * the grouping).  For a moe_forward / moe_forward_profiled /
+ * moe_forward_scored / moe_ffn_dense call with these sizes (moe_ffn_dense:
+ * E = 1, k = 1), `views[i]` receives the byte offset from the workspace
+ * pointer of:
+ *   views[0] topk_idx  int32 [T, k]   kept experts, ranking order
+ *   views[1] topk_w    fp32  [T, k]   their routing weights
+ *   views[2] counts    int32 [E]      rows per expert
+ *   views[3] offsets   int32 [E + 1]  exclusive prefix sum of counts
+ *   views[4] perm_tok  int32 [T*k]    token of grouped row r
+ *   views[5] inv       int32 [T*k]    grouped row of slot t*k + j
+ *   views[6] perm_w    fp32  [T*k]    routing weight of grouped row r
+ * (the same conventions as moe_route and moe_permute).  The arrays hold the
+ * call's values once its work on its stream has completed, until the next
+ * call on the same workspace.  Returns MOE_ERR_INVALID_ARG for sizes that
+ * moe_workspace_size rejects or a NULL `views`.
+ */
+MOE_API moe_status moe_workspace_views(int T, int d, int E, int k, int F, moe_dtype act_dt,
+                                       moe_dtype w_dt, size_t *views);
+
+/*
  * moe_forward -- the whole layer, steps 1-5.
  *   x[T,d] (act_dt), w_router[E,d] (act_dt), sel_bias[E] fp32 or NULL,
  *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64: the
@@ -268,24 +295,36 @@ MOE_API moe_status moe_ffn_dense(const void *x, moe_dtype act_dt, int T, int d,
  * as moe_forward minus the workspace, runs the same kernels, and uses as
  * scratch one static 8 MiB device array inside the library instead; it calls
  * no allocator of any kind.
- *  - Limit: layers whose moe_workspace_size() exceeds 8 MiB (8388608 bytes)
- *    are rejected with MOE_ERR_WORKSPACE before anything is enqueued.
+ *  - Errors: moe_forward's argument checks come first, with its return
+ *    codes; then layers whose moe_workspace_size() exceeds 8 MiB (8388608
+ *    bytes) are rejected with MOE_ERR_WORKSPACE.  Nothing is enqueued on an
+ *    error.
  *  - Set-up: the first call on each device (with that device current) looks
- *    up the array's device address once; make that first call before any
+ *    up the array's device address (again after the device's context is
+ *    re-created, e.g. by cudaDeviceReset); make that first call before any
  *    stream capture.
  *  - Sharing: every call, on any stream, uses the same array, which keeps the
  *    previous call's contents (each call rewrites every scratch byte it reads,
  *    and its first kernel clears the status word).  Calls that can overlap on
  *    the GPU race on it: serialise them (one stream, or events).
  *  - Memory: every GPU that loads the library holds the 8 MiB until exit.
- *  - moe_check cannot be pointed at this scratch; launch and argument errors
- *    come back as the return value.
+ *  - Device-side errors (a bounded wait that gave up, a failed consistency
+ *    check) are read with moe_check_noalloc.
  */
 MOE_API moe_status moe_forward_noalloc(const void *x, moe_dtype act_dt, int T, int d,
                                        const void *w_router, const float *sel_bias, int E, int k,
                                        const void *w_gate, const void *w_up, const void *w_down,
                                        moe_dtype w_dt, int F, float *out, int path,
                                        moe_stream stream);
+
+/*
+ * moe_check_noalloc -- moe_check for moe_forward_noalloc: wait for `stream`,
+ * then read the status word the most recent moe_forward_noalloc on the
+ * current device left in the library's static scratch (MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK; `*device_word` optional).  It
+ * synchronises, so it cannot be captured into a CUDA graph.
+ */
+MOE_API moe_status moe_check_noalloc(uint32_t *device_word, moe_stream stream);
 
 /*
  * moe_check -- wait for `stream`, then read the device status word that the

@@ -111,3 +111,68 @@ def test_near_tie_accepts_either_set_but_only_with_its_own_output():
     # ... but claiming the runner-up while returning the original set's output fails
     with pytest.raises(AssertionError, match="max\\|err\\|"):
         check_output(out, layer, out, idx, margin, idx_gpu=idx_alt)
+
+
+def _near_tie_case(seed=6, k=2, E=8):
+    layer = _layer(seed=seed, k=k, E=E)
+    kth, nxt = _with_near_tie(layer, t=0)
+    out, idx, w, margin = oracle.moe_forward(layer)
+    logits = oracle.router_logits(layer.x, layer.act_dtype, layer.w_router, layer.E)
+    return layer, out, idx, w, margin, logits, kth, nxt
+
+
+def test_near_tie_swap_outside_the_tie_band_fails():
+    """A near-tie token may trade its k-th expert for the runner-up, not for an
+    expert that scores well below the tie."""
+    layer, out, idx, w, margin, logits, kth, nxt = _near_tie_case()
+    score = logits[0] + layer.bias.astype(np.float64)
+    s_k = score[kth]
+    far = [e for e in range(layer.E) if e not in idx[0] and score[e] < s_k - 10 * MARGIN]
+    assert far
+    idx_bad = idx.copy()
+    idx_bad[0, -1] = far[0]
+    w_bad = w.astype(np.float32).copy()
+    w_bad[:1] = oracle.softmax_of_set(logits[:1], idx_bad[:1])
+    with pytest.raises(AssertionError, match="below the tie band"):
+        compare_routing(idx_bad, w_bad, idx, w, margin, layer.k, logits=logits, bias=layer.bias)
+    out_bad = out.copy()
+    out_bad[0] = oracle.expert_combine(layer.x[:1], layer.act_dtype, idx_bad[:1], w_bad[:1],
+                                       layer.w_gate, layer.w_up, layer.w_down, layer.w_dtype,
+                                       layer.E, layer.F)[0]
+    with pytest.raises(AssertionError, match="below the tie band"):
+        check_output(out_bad, layer, out, idx, margin, idx_gpu=idx_bad)
+
+
+def test_near_tie_dropping_an_expert_above_the_band_fails():
+    """Swapping out the top expert (well above the tie) for the runner-up fails."""
+    layer, out, idx, w, margin, logits, kth, nxt = _near_tie_case(k=2)
+    idx_bad = idx.copy()
+    idx_bad[0, 0] = nxt            # drops the first-ranked expert, keeps the k-th
+    w_bad = w.astype(np.float32).copy()
+    w_bad[:1] = oracle.softmax_of_set(logits[:1], idx_bad[:1])
+    with pytest.raises(AssertionError, match="above the tie band dropped"):
+        compare_routing(idx_bad, w_bad, idx, w, margin, layer.k, logits=logits, bias=layer.bias)
+
+
+def test_near_tie_set_with_wrong_weights_fails():
+    """The runner-up set is valid, but only with its own softmax weights."""
+    layer, out, idx, w, margin, logits, kth, nxt = _near_tie_case()
+    idx_alt = idx.copy()
+    idx_alt[0, -1] = nxt
+    w_alt = w.astype(np.float32).copy()
+    w_alt[:1] = oracle.softmax_of_set(logits[:1], idx_alt[:1])
+    compare_routing(idx_alt, w_alt, idx, w, margin, layer.k, logits=logits, bias=layer.bias)
+    # the original set's weights on the runner-up set are wrong (the logits differ by far more
+    # than 2e-6)
+    with pytest.raises(AssertionError):
+        compare_routing(idx_alt, w.astype(np.float32), idx, w, margin, layer.k, logits=logits,
+                        bias=layer.bias)
+
+
+def test_near_tie_repeated_expert_fails():
+    layer, out, idx, w, margin, logits, kth, nxt = _near_tie_case(k=3, E=8)
+    idx_bad = idx.copy()
+    idx_bad[0, -1] = idx_bad[0, 0]
+    with pytest.raises(AssertionError, match="repeated expert"):
+        compare_routing(idx_bad, w.astype(np.float32), idx, w, margin, layer.k, logits=logits,
+                        bias=layer.bias)

@@ -163,6 +163,38 @@ def test_bias_selects_but_never_weighs():
         np.testing.assert_allclose(w2[t], ref, rtol=1e-14)
 
 
+def test_softmax_of_set_pinned():
+    """The set-weights helper (the weights of a fixed expert set, used to
+    re-evaluate near-tie tokens with another set) against a library softmax
+    (scipy) of the set's logits, bit for bit against the router's own weights
+    for the set the router keeps, the two-expert closed form 1/(1+e^-delta),
+    and exactly 1 for a single expert ("New Community Model: ZONOS3-Mini
+    (Zyphra) - #1271", §Framework change: the kept experts are weighed by the
+    softmax of their logits)."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(44)
+    T, E = 50, 16
+    logits = rng.standard_normal((T, E)) * 3
+    for k in (1, 2, 3, 8):
+        # arbitrary sets in arbitrary slot order, not the router's
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        w = oracle.softmax_of_set(logits, idx)
+        ref = softmax(np.take_along_axis(logits, idx, axis=1), axis=1)
+        np.testing.assert_allclose(w, ref, rtol=1e-14, atol=0)
+        if k == 1:
+            assert np.all(w == 1.0)
+        # for the router's own set: the router's weights, bit for bit
+        bias = (rng.standard_normal(E) * 0.5).astype(np.float32)
+        idx_r, w_r, _ = oracle.selected_softmax(logits, bias, k)
+        assert np.array_equal(oracle.softmax_of_set(logits, idx_r), w_r)
+    # two experts: w0 = 1 / (1 + exp(-(l0 - l1)))
+    idx2 = np.tile(np.array([[3, 9]], np.int32), (T, 1))
+    w2 = oracle.softmax_of_set(logits, idx2)
+    delta = logits[:, 3] - logits[:, 9]
+    np.testing.assert_allclose(w2[:, 0], 1.0 / (1.0 + np.exp(-delta)), rtol=1e-14)
+    np.testing.assert_allclose(w2[:, 1], 1.0 / (1.0 + np.exp(delta)), rtol=1e-14)
+
+
 def test_zero_bias_is_textbook_topk_softmax_renormalised():
     """bias = 0: softmax over all E, keep the top k, renormalise."""
     rng = np.random.default_rng(4)

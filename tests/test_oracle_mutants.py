@@ -32,6 +32,13 @@ MUTANTS = {
     "softmax_denominator_skips_first": (
         "for (int j = 0; j < k; ++j) den += exp(", "for (int j = 1; j < k; ++j) den += exp(", 0),
     "margin_sign_flipped": ("margin[t] = kth - next;", "margin[t] = next - kth;", 0),
+    # the set-weights helper (softmax of a given set's logits), a second copy
+    # of step 4 that the near-tie re-evaluation uses
+    "set_weights_denominator_skips_first": (
+        "for (int j = 0; j < k; ++j) den += exp(", "for (int j = 1; j < k; ++j) den += exp(", 1),
+    "set_weights_all_from_first_slot": (
+        "topk_w[(size_t)t * k + j] = exp(l[topk_idx[(size_t)t * k + j]] - m) / den;\n    }\n    return 0;",
+        "topk_w[(size_t)t * k + j] = exp(l[topk_idx[(size_t)t * k]] - m) / den;\n    }\n    return 0;", 0),
     # router projection
     "router_row_off_by_one": (
         "decode_row(c->w_r, c->x_dt, (size_t)e, c->d, wr);",

@@ -10,8 +10,8 @@ import pytest
 import oracle
 from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
 
-from helpers import (MARGIN, check_output, compare_routing, gpu_forward, sub_layer, to_dev,
-                     upload_layer)
+from helpers import (MARGIN, check_output, check_routing_views, compare_routing, gpu_forward,
+                     gpu_forward_views, to_dev, upload_layer)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -57,8 +57,10 @@ def test_route_matches_oracle(name, T, seed):
     # only x, W_r and the bias matter for routing: draw a small-F layer
     layer = wl.make_layer(w, seed=seed, T=T, F=32)
     idx, wts = _route(layer)
-    idx_ref, w_ref, margin = _oracle_route(layer)
-    ok = compare_routing(idx, wts, idx_ref, w_ref, margin, layer.k)
+    logits = oracle.router_logits(layer.x, layer.act_dtype, layer.w_router, layer.E)
+    idx_ref, w_ref, margin = oracle.selected_softmax(logits, layer.bias, layer.k)
+    ok = compare_routing(idx, wts, idx_ref, w_ref, margin, layer.k, logits=logits,
+                         bias=layer.bias)
     assert ok.mean() > 0.95
 
 
@@ -149,11 +151,10 @@ SMALL = [
 def test_forward_small_matches_oracle(act, wdt, T, d, E, k, F, path):
     layer = wl.make_custom_layer(11, T=T, d=d, E=E, k=k, F=F, act_dtype=act, w_dtype=wdt,
                                  bias_sd=0.3)
-    out = gpu_forward(layer, DEV, path=path)
-    idx_g, _ = _route(layer)
-    torch.cuda.synchronize()
+    out, r = gpu_forward_views(layer, DEV, path=path)
+    check_routing_views(r, layer)
     ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
-    check_output(out.cpu().numpy(), layer, ref, idx_ref, margin, idx_gpu=idx_g)
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
 @pytest.mark.parametrize("path", [DECODE, SIMT])
@@ -235,19 +236,38 @@ def test_device_status_ok_after_forward():
 
 
 # -------------------------------------------------- workload sizes (full)
-@pytest.mark.parametrize("name,T", [("tiny_fp32", None), ("zonos3_mini_decode", None),
-                                    ("zonos2_decode", 1), ("zonos2_decode", 8),
-                                    ("zonos2_decode", 64), ("zonos2_decode_q4", 1),
-                                    ("zonos2_decode_q4", 8)])
-def test_forward_decode_workloads_full(name, T):
-    """Decode workloads at full size, in the launch configuration the benchmark
-    times (path AUTO), every output row against the oracle."""
-    layer = wl.make_layer(wl.WORKLOADS[name], seed=2, T=T)
-    out = gpu_forward(layer, DEV, path=0)
-    idx_g, w_g = _route(layer)
+FULL_CASES = [("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode", 1),
+              ("zonos2_decode", 8), ("zonos2_decode", 64), ("zonos3_mini_prefill", None),
+              ("zonos2_prefill_q8", None), ("zonos2_decode_q4", 1), ("zonos2_decode_q4", 8)]
+
+
+@pytest.mark.parametrize("seed", [2, 7, 13])
+@pytest.mark.parametrize("name,T", FULL_CASES)
+def test_forward_workloads_full(name, T, seed):
+    """Every workload at full size, in the launch configuration the benchmark
+    times (path AUTO): the routing and grouping the layer's own kernels wrote
+    (read back from its workspace) against the oracle -- indices exact beyond
+    the 1e-3 margin, near ties resolved validly, weights within 2e-6, counts,
+    offsets, permutation and inverse bit-exact -- and every output row within
+    the tolerance."""
+    if name.startswith("zonos2_decode_q4") and seed != 2:
+        pytest.skip("the 4-bit decode workload runs with one seed (CUDA-core path)")
+    layer = wl.make_layer(wl.WORKLOADS[name], seed=seed, T=T)
+    out, r = gpu_forward_views(layer, DEV, path=0)
+    check_routing_views(r, layer)
     ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
-    compare_routing(idx_g, w_g, idx_ref, w_ref, margin, layer.k)
-    check_output(out.cpu().numpy(), layer, ref, idx_ref, margin, idx_gpu=idx_g)
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
+
+
+@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8"])
+def test_forward_prefill_workloads_on_decode_path(name):
+    """The prefill workloads at full size through the decode path (CUDA-core
+    kernels at these row counts): grouping and every output row."""
+    layer = wl.make_layer(wl.WORKLOADS[name], seed=3)
+    out, r = gpu_forward_views(layer, DEV, path=DECODE)
+    check_routing_views(r, layer)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
 @pytest.mark.parametrize("name", ["zonos3_mini_decode", "zonos2_decode", "zonos3_mini_prefill",
@@ -282,29 +302,6 @@ def test_graph_replay_equals_direct_launch(name):
     assert pkg.moe_check(ws) == 0
 
 
-@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8"])
-@pytest.mark.parametrize("path", [DECODE, 0])
-def test_forward_prefill_workloads_sampled(name, path):
-    """Prefill workloads at full size; 96 sampled token rows against the oracle,
-    plus exact grouping of the GPU's own routing."""
-    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
-    layer = wl.make_layer(wl.WORKLOADS[name], seed=3)
-    t = upload_layer(layer, DEV)
-    out = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy()
-    idx_t, w_t = pkg.moe_route(t["x"], t["w_router"], t["bias"], layer.k)
-    counts, offsets, perm_tok, inv = pkg.moe_permute(idx_t, layer.E)
-    torch.cuda.synchronize()
-    idx_g = idx_t.cpu().numpy()
-    c_ref, o_ref, p_ref, i_ref = oracle.permute(idx_g, layer.E)
-    assert np.array_equal(counts.cpu().numpy(), c_ref)
-    assert np.array_equal(perm_tok.cpu().numpy(), p_ref)
-    rows = np.sort(np.random.default_rng(5).choice(layer.T, size=96, replace=False))
-    sub = sub_layer(layer, rows)
-    ref, idx_ref, w_ref, margin = oracle.moe_forward(sub)
-    compare_routing(idx_g[rows], w_t.cpu().numpy()[rows], idx_ref, w_ref, margin, layer.k)
-    check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g[rows])
-
-
 # ------------------------------------------- tensor-core (prefill) path
 PREFILL_SMALL = [
     # (T, d, E, k, F): ragged groups, tiles crossing expert boundaries, empty experts
@@ -324,18 +321,10 @@ PREFILL_SMALL = [
 def test_forward_prefill_small_matches_oracle(T, d, E, k, F, wdt):
     layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
                                  w_dtype=wdt, bias_sd=0.5)
-    t = upload_layer(layer, DEV)
-    out = gpu_forward(layer, DEV, path=PREFILL, t=t).cpu().numpy()
-    idx_g, _ = _route(layer)
-    rows = np.arange(T) if T <= 400 else np.sort(
-        np.random.default_rng(T).choice(T, size=400, replace=False))
-    sub = sub_layer(layer, rows)
-    ref, idx_ref, w_ref, margin = oracle.moe_forward(sub)
-    check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g[rows])
-    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
-    ws = torch.empty(pkg.moe_workspace_size(T, d, E, k, F, 1, wdt), dtype=torch.uint8, device=DEV)
-    gpu_forward(layer, DEV, path=PREFILL, t=t, workspace=ws)
-    assert pkg.moe_check(ws) == 0
+    out, r = gpu_forward_views(layer, DEV, path=PREFILL)
+    check_routing_views(r, layer)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
 def test_prefill_one_expert_many_tiles():
@@ -345,11 +334,11 @@ def test_prefill_one_expert_many_tiles():
     layer.bias[:] = 0
     layer.bias[3] = 100.0
     layer.bias[5] = 50.0
-    out = gpu_forward(layer, DEV, path=PREFILL).cpu().numpy()
-    rows = np.arange(0, 1100, 7)
-    sub = sub_layer(layer, rows)
-    ref, idx_ref, _, margin = oracle.moe_forward(sub)
-    check_output(out[rows], sub, ref, idx_ref, margin)
+    out, r = gpu_forward_views(layer, DEV, path=PREFILL)
+    check_routing_views(r, layer)
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    assert np.all(idx_ref == [3, 5])
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
 @pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
@@ -376,9 +365,10 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
     t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
     c = gpu_forward(layer, DEV, path=DECODE, t=t2).cpu().numpy()
     assert np.array_equal(c, a[perm])
+    _, r = gpu_forward_views(layer, DEV, path=DECODE, t=t)
+    check_routing_views(r, layer)
     ref, idx_ref, _, margin = oracle.moe_forward(layer)
-    idx_g, _ = _route(layer)
-    check_output(a, layer, ref, idx_ref, margin, idx_gpu=idx_g)
+    check_output(a, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
 @pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
@@ -423,16 +413,10 @@ def test_forward_scored_matches_oracle(mode, path, T, wdt):
     import expert_routed_ffn_selectedsoftmax_gb300 as pkg
     layer = wl.make_custom_layer(32, T=T, d=256, E=16, k=2, F=256, act_dtype=wl.BF16,
                                  w_dtype=wdt, bias_sd=0.05)
-    t = upload_layer(layer, DEV)
-    out = gpu_forward(layer, DEV, path=path, t=t, scoring=mode).cpu().numpy()
-    idx_g, _ = pkg.moe_route(t["x"], t["w_router"], t["bias"], layer.k, scoring=mode)
-    torch.cuda.synchronize()
-    rows = np.arange(T) if T <= 300 else np.sort(
-        np.random.default_rng(T).choice(T, size=300, replace=False))
-    sub = sub_layer(layer, rows)
-    ref, idx_ref, w_ref, margin = oracle.moe_forward(sub, mode=mode)
-    check_output(out[rows], sub, ref, idx_ref, margin, idx_gpu=idx_g.cpu().numpy()[rows],
-                 mode=mode)
+    out, r = gpu_forward_views(layer, DEV, path=path, scoring=mode)
+    check_routing_views(r, layer, mode=mode)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(layer, mode=mode)
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"], mode=mode)
 
 
 # ---------------------------------------- dense SwiGLU layer (next row f2)
@@ -451,8 +435,15 @@ def test_ffn_dense_matches_oracle(act, wdt, T, path):
                             w_dtype=layer.w_dtype, path=path).cpu().numpy()
     via_moe = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy()
     assert np.array_equal(out, via_moe)
-    rows = np.arange(T) if T <= 300 else np.sort(
-        np.random.default_rng(T).choice(T, size=300, replace=False))
-    sub = sub_layer(layer, rows)
-    ref, idx_ref, _, margin = oracle.moe_forward(sub)
-    check_output(out[rows], sub, ref, idx_ref, margin)
+    # the dense call's own grouping: every token to expert 0 with weight 1, identity order
+    ws = torch.empty(max(pkg.moe_workspace_size(T, 256, 1, 1, 256, act, wdt), 256),
+                     dtype=torch.uint8, device=DEV)
+    pkg.moe_ffn_dense(t["x"], t["w_gate"], t["w_up"], t["w_down"], F=layer.F,
+                      w_dtype=layer.w_dtype, path=path, workspace=ws)
+    torch.cuda.synchronize()
+    r = {n: v.cpu().numpy() for n, v in pkg.read_routing(ws, T, 256, 1, 1, 256, act, wdt).items()}
+    assert np.all(r["topk_idx"] == 0) and np.all(r["topk_w"] == 1.0) and np.all(r["perm_w"] == 1.0)
+    assert r["counts"].tolist() == [T] and r["offsets"].tolist() == [0, T]
+    assert np.array_equal(r["perm_tok"], np.arange(T)) and np.array_equal(r["inv"], np.arange(T))
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    check_output(out, layer, ref, idx_ref, margin)
