@@ -11,6 +11,13 @@ back to back (2.0 GB of expert weights per step, far above the 129 MB L2, so
 every step reads its weights from HBM).  value = layer-tokens per second
 (T x layers x steps / time).  One JSON line is printed by rank 0.
 
+With the default workload the line also carries a "workloads" list: every
+other configuration (tiny fp32; ZONOS2-shaped decode at T = 1, 8 and 64; the
+ZONOS3-Mini-shaped prefill; the ZONOS2-shaped Q8_0 prefill), each measured
+alone on rank 0's GPU -- µs per layer, tokens/s, the layer's roofline
+fraction, the dominant kernel's fraction -- with the oracle's tokens/s on the
+host cores beside it (median of 3 passes over a token sample).
+
 --impl reference times the CPU fp64 oracle (the only reference this library
 has) on the machine's host cores, on bounded token samples of the same workload.
 Under torchrun each rank runs an independent replica (no collective on the
@@ -48,6 +55,9 @@ def parse():
     p.add_argument("--layers", type=int, default=None)
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--side", default=None, help=argparse.SUPPRESS)   # NAME[:T], one side config
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the per-configuration block (the other workloads, measured alone)")
     p.add_argument("--dense", action="store_true",
                    help="a dense SwiGLU layer of the workload's d and F (one expert, k = 1) "
                         "through moe_ffn_dense")
@@ -270,21 +280,42 @@ def code_sha(text):
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(layers_host, w, budget_s, mode=0):
-    """Time the oracle on whole-layer token samples until ~budget_s elapses."""
+def oracle_runs(layer, rows, runs=3, mode=0):
+    """Time the oracle `runs` times on token rows `rows` of a host layer (all
+    host cores); returns (tokens/s of each run, threads)."""
+    import copy
     import oracle
     oracle.build()
     threads = oracle.default_threads()
-    done_tokens, t_used = 0, 0.0
-    li = 0
-    while t_used < budget_s and li < len(layers_host):
-        layer = layers_host[li]
+    sub = copy.copy(layer)
+    sub.x = np.ascontiguousarray(layer.x[rows])
+    sub.T = len(rows)
+    rates = []
+    for _ in range(runs):
         t0 = time.perf_counter()
-        oracle.moe_forward(layer, nthreads=threads, mode=mode)
-        t_used += time.perf_counter() - t0
-        done_tokens += layer.T
-        li += 1
-    return done_tokens, t_used, threads, li
+        oracle.moe_forward(sub, nthreads=threads, mode=mode)
+        rates.append(sub.T / (time.perf_counter() - t0))
+    return rates, threads
+
+
+def oracle_baseline(layers_host, sample_rows, mode=0, runs=3):
+    """The oracle's tokens/s on the host cores: the median of `runs` timed
+    passes, each over the first `sample_rows` token rows of every given host
+    layer (whole layers when sample_rows >= T)."""
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    per_run = []
+    for _ in range(runs):
+        tok, secs = 0, 0.0
+        for layer in layers_host:
+            rates, _ = oracle_runs(layer, np.arange(min(sample_rows, layer.T)), runs=1, mode=mode)
+            n = min(sample_rows, layer.T)
+            tok += n
+            secs += n / rates[0]
+        per_run.append(tok / secs)
+    return {"value": statistics.median(per_run), "runs": per_run, "unit": "tokens/s",
+            "cores": threads, "kind": "oracle", "cpu_model": host_cpu_model()}
 
 
 def host_layer_from_device(w, dl, T):
@@ -391,8 +422,281 @@ def scoring_mode(args):
     return {"selected_softmax": 0, "softmax": 1, "sigmoid": 2}[args.scoring]
 
 
+def compute_peak(w, peaks, dev_props):
+    """The compute roofline of a workload's expert arithmetic: the measured
+    dense bf16 tensor peak for bf16 weights and for Q8_0 (fp16 operands, the
+    same dense rate); for fp32 and affine 4-bit weights, which run as fp32 FMAs
+    on the CUDA cores, 128 FMA lanes x 2 flops per SM per clock at the
+    device's maximum SM clock ("alu")."""
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    if w.w_dtype in (wl.F32, wl.Q4_A64):
+        mhz = float(peaks.get("sm_max_mhz") or 0) or dev_props.clock_rate / 1e3
+        return dev_props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12, "alu", \
+            "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock"
+    return peak_value(peaks, "bf16_tflops"), "tensor", "bf16_tflops"
+
+
+def setup_stack(pkg, wl, w, T, layers, seed, dev):
+    """Device stack of `layers` layers of workload w (block-quantised weights
+    repacked once), plus the dtypes moe_forward takes."""
+    import torch
+    stack = wl.make_device_stack(w, seed=seed, layers=layers, T=T, device=dev)
+    act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
+    w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0,
+            wl.Q4_A64: pkg.MOE_Q4_A64}[w.w_dtype]
+    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64):
+        pack = pkg.moe_pack_q8_0 if w_dt == pkg.MOE_Q8_0 else pkg.moe_pack_q4_a64
+        for L in stack:
+            L["blocks"] = {n: L[n] for n in ("w_gate", "w_up", "w_down")}
+            for n, rows, cols in (("w_gate", w.E * w.F, w.d), ("w_up", w.E * w.F, w.d),
+                                  ("w_down", w.E * w.d, w.F)):
+                L[n] = pack(L[n].reshape(-1), rows, cols)
+    # the stack was drawn on the current stream; the layer calls run on the
+    # runner's own stream
+    torch.cuda.synchronize(dev)
+    return stack, act_dt, w_dt
+
+
+class Runner:
+    """One workload's stack on the device and the layer calls a step makes."""
+
+    def __init__(self, pkg, wl, w, T, layers, seed, dev, scoring=0, dense=False):
+        import torch
+        self.pkg, self.w, self.T, self.layers, self.dev = pkg, w, T, layers, dev
+        self.scoring, self.dense = scoring, dense
+        self.stack, self.act_dt, self.w_dt = setup_stack(pkg, wl, w, T, layers, seed, dev)
+        self.ws_bytes = pkg.moe_workspace_size(T, w.d, w.E, w.k, w.F, self.act_dt, self.w_dt)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.outs = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in range(layers)]
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graph = None
+
+    def layer_call(self, i, events=None, x=None):
+        L, w, pkg = self.stack[i], self.w, self.pkg
+        x = L["x"] if x is None else x
+        if self.dense and events is None:
+            pkg.moe_ffn_dense(x, L["w_gate"], L["w_up"], L["w_down"], F=w.F, w_dtype=self.w_dt,
+                              out=self.outs[i], workspace=self.ws)
+            return
+        # (dense layers: the per-stage timings come from the same one-expert
+        # layer through moe_forward_profiled -- same expert kernels)
+        pkg.moe_forward(x, L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
+                        w.k, F=w.F, w_dtype=self.w_dt, out=self.outs[i], workspace=self.ws,
+                        events=events, scoring=self.scoring)
+
+    def step(self):
+        for i in range(self.layers):
+            self.layer_call(i)
+
+    def counts_per_layer(self):
+        """Per-expert row counts each layer's own routing produced (read back
+        from the workspace after the layer ran)."""
+        import torch
+        out = []
+        with torch.cuda.stream(self.stream):
+            for i in range(self.layers):
+                self.layer_call(i)
+                self.stream.synchronize()
+                r = self.pkg.read_routing(self.ws, self.T, self.w.d, self.w.E, self.w.k, self.w.F,
+                                          self.act_dt, self.w_dt)
+                out.append(r["counts"].cpu().numpy().copy())
+        return out
+
+    def capture(self, warmup, graph=True):
+        import torch
+        with torch.cuda.stream(self.stream):
+            for _ in range(max(3, warmup)):
+                self.step()
+        self.stream.synchronize()
+        if graph:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=self.stream):
+                self.step()
+            with torch.cuda.stream(self.stream):
+                for _ in range(3):
+                    self.graph.replay()
+            self.stream.synchronize()
+        assert self.pkg.moe_check(self.ws) == 0
+
+    def replay(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.step()
+
+    def time_steps(self, steps):
+        """Device time of `steps` back-to-back steps (ms), CUDA events on the
+        launching stream."""
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(steps):
+                self.replay()
+            e1.record(self.stream)
+        self.stream.synchronize()
+        return e0.elapsed_time(e1)
+
+    def stage_us(self, n_prof):
+        """Per-launch µs of each stage (route, permute, gather, gate/up, down):
+        the same layers with caller events at the stage boundaries."""
+        import torch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
+               for _ in range(self.layers)]
+        # torch only reports elapsed time for events it has recorded itself once;
+        # the library re-records the same events at its stage boundaries
+        for row in evs:
+            for ev in row:
+                ev.record(self.stream)
+        self.stream.synchronize()
+        stage_ms = np.zeros(5)
+        with torch.cuda.stream(self.stream):
+            for _ in range(n_prof):
+                for i in range(self.layers):
+                    self.layer_call(i, events=evs[i])
+                self.stream.synchronize()
+                for i in range(self.layers):
+                    for s in range(5):
+                        stage_ms[s] += evs[i][s].elapsed_time(evs[i][s + 1])
+        return stage_ms / (n_prof * self.layers) * 1e3
+
+    def free(self):
+        self.stack = self.outs = self.ws = self.graph = None
+
+
+STAGES = ["route", "permute", "gather", "gateup", "down"]
+
+
+def roofline_of(w, T, layers, alg, stage_us, names, peaks, peak_src, dev_props, dense=False):
+    """Roofline object of the dominant expert kernel (the slower of gate/up and
+    down by live stage events): its algorithmic bytes (or flops, past the
+    ridge) per launch over its measured duration."""
+    hbm = peak_value(peaks, "hbm_gbs")
+    cpeak, cbound, csrc = compute_peak(w, peaks, dev_props)
+    dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
+    dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
+    dom_bytes = alg[f"{dominant}_bytes"] / layers
+    dom_flops = alg[f"{dominant}_flops"] / layers
+    compute_bound = dom_flops / dom_bytes > cpeak * 1e12 / (hbm * 1e9)
+    traffic = profile_traffic(f"{names['file']}:{dominant}:{w.name}{'-dense' if dense else ''}:T{T}")
+    if compute_bound:
+        achieved = dom_flops / (dom_us * 1e-6) / 1e12
+        return {"bound": cbound, "kernel": names[dominant], "achieved": achieved,
+                "peak": cpeak, "unit": "TFLOP/s", "frac": achieved / cpeak, "traffic": traffic,
+                "peak_source": f"{csrc} of {peak_src}" if cbound == "tensor" else csrc,
+                "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
+                "us_per_launch": dom_us}
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    return {"bound": "hbm", "kernel": names[dominant], "achieved": achieved, "peak": hbm,
+            "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+            "peak_source": f"hbm_gbs of {peak_src}", "bytes_per_launch": dom_bytes,
+            "flops_per_launch": dom_flops, "us_per_launch": dom_us}
+
+
+def layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us):
+    hbm = peak_value(peaks, "hbm_gbs")
+    cpeak, cbound, _ = compute_peak(w, peaks, dev_props)
+    gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
+    return {"us_per_layer": ms_per_step * 1e3 / layers, "algorithmic_GBps": gbs,
+            "TFLOPS": alg["flops"] / (ms_per_step * 1e-3) / 1e12, "frac_hbm": gbs / hbm,
+            "roofline_frac": layer_roofline_frac(alg["bytes"], alg["flops"], ms_per_step * 1e-3,
+                                                 hbm, cpeak),
+            "compute_peak": {"value": cpeak, "unit": "TFLOP/s", "kind": cbound},
+            "bytes_per_step": alg["bytes"], "flops_per_step": alg["flops"],
+            "active_experts_per_layer": alg["active"],
+            "stage_us": dict(zip(STAGES, [round(float(v), 3) for v in stage_us]))}
+
+
+# The configurations every default run measures beside the headline workload
+# (each at N = 1 on rank 0's GPU, the oracle beside it): (workload, T,
+# layers, oracle token sample per layer).
+SIDE_WORKLOADS = [("tiny_fp32", None, None, 8), ("zonos2_decode", 1, None, 1),
+                  ("zonos2_decode", 8, None, 8), ("zonos2_decode", 64, None, 64),
+                  ("zonos3_mini_prefill", None, None, 512), ("zonos2_prefill_q8", None, None, 192)]
+
+
+def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, peak_src,
+                          dev_props, target_s=0.3, with_oracle=True):
+    """One configuration measured on its own: graph replays of its stack timed
+    with events, stage events, the layer and dominant-kernel roofline
+    fractions, and the oracle's tokens/s on the host cores (median of 3)."""
+    import torch
+    w = wl.WORKLOADS[name]
+    T = w.T if T is None else T
+    layers = w.layers if layers is None else layers
+    def note(what):
+        print(f"[side {name} T={T}] {what}", file=sys.stderr, flush=True)
+    r = Runner(pkg, wl, w, T, layers, seed=11, dev=dev)
+    note("stack ready")
+    counts = r.counts_per_layer()
+    note("routing read back")
+    alg = algorithmic(w, T, counts)
+    r.capture(3)
+    note("warm-up and graph done")
+    est = r.time_steps(3) / 3
+    steps = int(min(2000, max(20, math.ceil(target_s * 1e3 / max(est, 1e-3)))))
+    t_ms = r.time_steps(steps)
+    ms = t_ms / steps
+    stage = r.stage_us(max(5, min(50, steps // 4)))
+    names = expert_kernel_names(w, T, dev_props.multi_processor_count)
+    res = {"workload": name, "T": T, "d": w.d, "E": w.E, "k": w.k, "F": w.F,
+           "w_dtype": wl.DTYPE_NAMES[w.w_dtype], "layers": layers, "steps": steps,
+           "ms_per_step": ms, "tokens_per_s": T * layers / (ms * 1e-3),
+           "layer": layer_stats(w, alg, ms, layers, peaks, dev_props, stage),
+           "roofline": roofline_of(w, T, layers, alg, stage, names, peaks, peak_src, dev_props),
+           "gpu_launches_per_layer": names["launches"]}
+    if with_oracle:
+        host = host_layer_from_device(w, r.stack[0], T)
+        res["cpu_baseline"] = oracle_baseline([host], sample_rows)
+        res["cpu_baseline"]["sample"] = (f"median of 3 passes over {min(sample_rows, T)} of the "
+                                         f"{T} tokens of one layer (fp64 C oracle)")
+    r.free()
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_side_child(name, T, no_cpu_baseline):
+    """Measure one configuration in a child process (bench.py --side NAME[:T]);
+    its JSON result, or a record of the failure."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--side", f"{name}:{T if T else ''}"]
+    if no_cpu_baseline:
+        cmd.append("--no-cpu-baseline")
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env)
+    except subprocess.TimeoutExpired:
+        return {"workload": name, "T": T, "error": "timed out after 600 s"}
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    if r.returncode != 0 or not lines:
+        tail = (r.stderr or r.stdout)[-400:]
+        return {"workload": name, "T": T, "error": f"exit {r.returncode}: {tail}"}
+    return json.loads(lines[-1])
+
+
+def side_main(args):
+    """bench.py --side NAME[:T]: one configuration of SIDE_WORKLOADS, alone."""
+    import torch
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    name, _, t = args.side.partition(":")
+    T = int(t) if t else None
+    rows = next((r for n, sT, _, r in SIDE_WORKLOADS if n == name and sT == T), 64)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    pkg.load_library()
+    peaks, peak_src = load_peaks()
+    res = measure_side_workload(pkg, wl, name, T, None, rows, dev, peaks, peak_src,
+                                torch.cuda.get_device_properties(dev),
+                                with_oracle=not args.no_cpu_baseline)
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.side:
+        return side_main(args)
     from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
     if args.dense:   # one expert of the workload's shape, no router
@@ -412,68 +716,18 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     pkg.load_library()
+    dev_props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
 
     # ------------------------------------------------------------ inputs
-    stack = wl.make_device_stack(w, seed=1 + rank, layers=layers, T=T, device=dev)
-    act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
-    w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0,
-            wl.Q4_A64: pkg.MOE_Q4_A64}[w.w_dtype]
-    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64):
-        # block-quantised weights are repacked once, at load time, into the kernels' planes
-        pack = pkg.moe_pack_q8_0 if w_dt == pkg.MOE_Q8_0 else pkg.moe_pack_q4_a64
-        for L in stack:
-            L["blocks"] = {n: L[n] for n in ("w_gate", "w_up", "w_down")}
-            for n, rows, cols in (("w_gate", w.E * w.F, w.d), ("w_up", w.E * w.F, w.d),
-                                  ("w_down", w.E * w.d, w.F)):
-                L[n] = pack(L[n].reshape(-1), rows, cols)
-        torch.cuda.synchronize(dev)
-    ws_bytes = pkg.moe_workspace_size(T, w.d, w.E, w.k, w.F, act_dt, w_dt)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    outs = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in range(layers)]
-    stream = torch.cuda.Stream(device=dev)
-
-    def layer_call(i, events=None):
-        L = stack[i]
-        if args.dense and events is None:
-            pkg.moe_ffn_dense(L["x"], L["w_gate"], L["w_up"], L["w_down"], F=w.F, w_dtype=w_dt,
-                              out=outs[i], workspace=ws)
-            return
-        # (dense layers: the per-stage timings come from the same one-expert
-        # layer through moe_forward_profiled -- same expert kernels)
-        pkg.moe_forward(L["x"], L["w_router"], L["bias"], L["w_gate"], L["w_up"], L["w_down"],
-                        w.k, F=w.F, w_dtype=w_dt, out=outs[i], workspace=ws, events=events,
-                        scoring=scoring_mode(args))
-
-    def step():
-        for i in range(layers):
-            layer_call(i)
-
-    # counts per layer (for the algorithmic bytes): one routing pass
-    counts_per_layer = []
-    with torch.cuda.stream(stream):
-        for L in stack:
-            idx, _ = pkg.moe_route(L["x"], L["w_router"], L["bias"], w.k)
-            c, _, _, _ = pkg.moe_permute(idx, w.E)
-            counts_per_layer.append(c)
-    stream.synchronize()
-    counts_per_layer = [c.cpu().numpy() for c in counts_per_layer]
+    run = Runner(pkg, wl, w, T, layers, seed=1 + rank, dev=dev, scoring=scoring_mode(args),
+                 dense=args.dense)
+    stack, w_dt, stream = run.stack, run.w_dt, run.stream
+    counts_per_layer = run.counts_per_layer()
     alg = algorithmic(w, T, counts_per_layer)
 
     # --------------------------------------------------------- warm-up + graph
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-    stream.synchronize()
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                graph.replay()
-        stream.synchronize()
-    assert pkg.moe_check(ws) == 0
+    run.capture(args.warmup, graph=not args.no_graph)
 
     def barrier():
         if world > 1:
@@ -483,21 +737,12 @@ def main():
 
     # ------------------------------------------------------------ timed region
     clocks = ClockSampler(local)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     clocks.start()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
-                step()
-        e1.record(stream)
-    stream.synchronize()
+    t_ms = run.time_steps(args.steps)
     clk = clocks.stop()
     barrier()
-    t_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    t_ms = max_over_ranks(t_ms, world, dev)
     ms_per_step = t_ms / args.steps
     tokens_per_step = T * layers
     value = job_throughput(tokens_per_step, world, ms_per_step)
@@ -510,73 +755,25 @@ def main():
     with torch.cuda.stream(stream):
         step_evs[0].record(stream)
         for i in range(n_dist):
-            if graph is not None:
-                graph.replay()
-            else:
-                step()
+            run.replay()
             step_evs[i + 1].record(stream)
     stream.synchronize()
     step_dist = percentiles([step_evs[i].elapsed_time(step_evs[i + 1]) for i in range(n_dist)])
 
     # --------------------------------------------- per-kernel (stage) timing
-    # the same step with CUDA events at the stage boundaries, on the stream
-    # the kernels run on
-    n_prof = max(1, min(args.steps, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(layers)]
-    # torch only reports elapsed time for events it has recorded itself once;
-    # the library re-records the same events at its stage boundaries
-    for row in evs:
-        for ev in row:
-            ev.record(stream)
-    stream.synchronize()
-    stage_ms = np.zeros(5)
-    with torch.cuda.stream(stream):
-        for _ in range(n_prof):
-            for i in range(layers):
-                layer_call(i, events=evs[i])
-            stream.synchronize()
-            for i in range(layers):
-                for s in range(5):
-                    stage_ms[s] += evs[i][s].elapsed_time(evs[i][s + 1])
-    stage_us = stage_ms / (n_prof * layers) * 1e3     # per launch, µs
-    stage_names = ["route", "permute", "gather", "gateup", "down"]
-
-    # ------------------------------------------------------- roofline object
-    peaks, peak_src = load_peaks()
-    hbm = peak_value(peaks, "hbm_gbs")
-    tflops_peak = peak_value(peaks, "bf16_tflops")   # fp16 dense rate equals bf16
-    names = expert_kernel_names(w, T, torch.cuda.get_device_properties(dev).multi_processor_count)
-    dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
-    dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
-    dom_bytes = alg[f"{dominant}_bytes"] / layers
-    dom_flops = alg[f"{dominant}_flops"] / layers
-    # the kernel's bound: tensor when its arithmetic intensity is past the ridge
-    tensor_bound = dom_flops / dom_bytes > tflops_peak * 1e12 / (hbm * 1e9)
-    traffic = profile_traffic(f"{names['file']}:{dominant}:{w.name}"
-                              f"{'-dense' if args.dense else ''}:T{T}")
-    if tensor_bound:
-        achieved = dom_flops / (dom_us * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "kernel": names[dominant], "achieved": achieved,
-                    "peak": tflops_peak, "unit": "TFLOP/s", "frac": achieved / tflops_peak,
-                    "traffic": traffic, "peak_source": f"bf16_tflops of {peak_src}",
-                    "flops_per_launch": dom_flops, "bytes_per_launch": dom_bytes,
-                    "us_per_launch": dom_us}
-    else:
-        achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-        roofline = {"bound": "hbm", "kernel": names[dominant], "achieved": achieved,
-                    "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                    "peak_source": f"hbm_gbs of {peak_src}",
-                    "bytes_per_launch": dom_bytes, "flops_per_launch": dom_flops,
-                    "us_per_launch": dom_us}
-    layer_gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
-    layer_tflops = alg["flops"] / (ms_per_step * 1e-3) / 1e12
+    stage_us = run.stage_us(max(1, min(args.steps, 200)))
+    names = expert_kernel_names(w, T, dev_props.multi_processor_count)
+    roofline = roofline_of(w, T, layers, alg, stage_us, names, peaks, peak_src, dev_props,
+                           dense=args.dense)
 
     # ------------------------------------------------------------- e2e
     # through the public API with host buffers: pinned x in, fp32 out back, per step
+    outs, ws = run.outs, run.ws
     hx = [L["x"].cpu().pin_memory() for L in stack]
     hout = [torch.empty((T, w.d), dtype=torch.float32).pin_memory() for _ in range(layers)]
     dx = [torch.empty_like(L["x"]) for L in stack]
     n_e2e = max(1, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def e2e_layer(i):
         L = stack[i]
@@ -680,14 +877,27 @@ def main():
 
     # ------------------------------------------------------- CPU baseline
     cpu = None
+    host_layers = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host_layers = [host_layer_from_device(w, stack[i], T) for i in range(min(layers, 3))]
-        ntok, secs, threads, nl = oracle_sample(host_layers, w, budget_s=10.0,
-                                                mode=scoring_mode(args))
-        cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "cpu_model": host_cpu_model(),
-               "sample": f"{nl} of the {layers} layers of one step, all {T} tokens each "
-                         f"(fp64 C oracle, {threads} threads), {secs:.1f} s"}
+        host_layers = [host_layer_from_device(w, stack[i], T) for i in range(layers)]
+    run.free()
+    del stack, outs, ws, hx, hout, dx
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    if host_layers is not None:
+        cpu = oracle_baseline(host_layers, T, mode=scoring_mode(args))
+        cpu["sample"] = (f"median of 3 passes over all {layers} layers of one step, all {T} "
+                         f"tokens each (fp64 C oracle, {cpu['cores']} threads)")
+
+    # ------------------------------- every other configuration, measured alone
+    # (each in a process of its own on this GPU, after this process's own
+    # measurement is complete: its stacks get the device to themselves, and a
+    # failure there cannot take the headline line with it)
+    side = None
+    if world == 1 and not args.no_workloads and args.workload == "zonos3_mini_decode" and \
+            not args.dense and args.T is None and args.layers is None and args.scoring == \
+            "selected_softmax":
+        side = [run_side_child(name, sT, args.no_cpu_baseline) for name, sT, _, _ in SIDE_WORKLOADS]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -700,14 +910,8 @@ def main():
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": names["launches"] * layers * args.steps,
         "roofline": roofline, "cpu_baseline": cpu, "step_ms": step_dist,
-        "layer": {"algorithmic_GBps": layer_gbs, "TFLOPS": layer_tflops,
-                  "frac_hbm": layer_gbs / hbm,
-                  "roofline_frac": layer_roofline_frac(alg["bytes"], alg["flops"], ms_per_step * 1e-3,
-                                                       hbm, tflops_peak),
-                  "bytes_per_step": alg["bytes"],
-                  "flops_per_step": alg["flops"],
-                  "active_experts_per_layer": alg["active"],
-                  "stage_us": dict(zip(stage_names, [round(float(v), 3) for v in stage_us]))},
+        "layer": layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us),
+        "workloads": side,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
