@@ -205,21 +205,27 @@ def expert_kernel_names(w, T, num_sms):
     the library's selection: grouped GEMMs from 64 rows per expert on average
     and T >= 512 for bf16 / Q8_0 weights with d % 256 == 0 and F % 128 == 0;
     tensor-core decode for bf16 layers with d, F multiples of 128 and
-    T*k <= 8192 -- one clustered routing+grouping kernel for T <= 128, whole-K
-    gate/up items when ~200 of them fit in one wave of two CTAs per SM,
-    whole-K down items when k <= 2 and ~200 of them exist; otherwise the
-    CUDA-core decode kernels), and how many of the library's kernels one
-    layer launches."""
+    T*k <= 8192 -- one clustered routing+grouping kernel for T <= 128, then
+    one persistent kernel for gate/up, SwiGLU, down and the combine when k <= 2
+    and the batch has half a wave of whole-K gate/up items of at most 512 KB,
+    else the gate/up and down kernels with their split-K reductions; otherwise
+    the CUDA-core decode kernels), and how many of the library's kernels one
+    layer launches.  "fused": the gate/up and down GEMMs run in one kernel,
+    timed as one stage."""
     rows = T * w.k
     act16 = w.act_dtype == 1
     if (act16 and w.w_dtype in (1, 2) and w.d % 256 == 0 and w.F % 128 == 0
             and rows >= 64 * w.E and T >= 512):
         q = "Q8_0, CTA pairs" if w.w_dtype == 2 else "bf16"
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
-                "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4}
+                "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4, "fused": False}
     if act16 and w.w_dtype == 1 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
         n_exp = min(w.E, rows)
         small = T <= 128 and w.d // 64 <= 64 and w.k <= w.E
+        if w.k <= 2 and n_exp * (w.F // 128) * 2 >= 2 * num_sms and 2 * 128 * w.d * 2 <= 512 << 10:
+            name = "decode_fused_kernel (gate/up + SwiGLU + down + combine, one launch)"
+            return {"file": "decode_fused.cu", "gateup": name, "down": name, "fused": True,
+                    "launches": (1 if small else 2) + 1}
         fused = 192 <= n_exp * (w.F // 128) <= 2 * num_sms
         direct = w.k <= 2 and n_exp * (w.d // 128) >= 192
         launches = (1 if small else 2) + (1 if fused else 2) + (1 if direct else 2)
@@ -227,9 +233,10 @@ def expert_kernel_names(w, T, num_sms):
             "decode_tc_kernel<GATEUP> + swiglu_reduce_kernel"
         dn = "decode_tc_kernel<DOWN> (whole K, adds into out)" if direct else \
             "decode_tc_kernel<DOWN> + combine_kernel"
-        return {"file": "decode_tc.cu", "gateup": gu, "down": dn, "launches": launches}
+        return {"file": "decode_tc.cu", "gateup": gu, "down": dn, "launches": launches,
+                "fused": False}
     return {"file": "decode.cu", "gateup": "decode_gateup_kernel", "down": "decode_down_kernel",
-            "launches": 4}
+            "launches": 4, "fused": False}
 
 
 def profile_traffic(kernel_key):
@@ -573,10 +580,17 @@ def roofline_of(w, T, layers, alg, stage_us, names, peaks, peak_src, dev_props, 
     ridge) per launch over its measured duration."""
     hbm = peak_value(peaks, "hbm_gbs")
     cpeak, cbound, csrc = compute_peak(w, peaks, dev_props)
-    dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
-    dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
-    dom_bytes = alg[f"{dominant}_bytes"] / layers
-    dom_flops = alg[f"{dominant}_flops"] / layers
+    if names.get("fused"):
+        # one kernel streams both GEMMs' weights: its stage is the gate/up one
+        dominant, dom_us = "fused", stage_us[3]
+        names = dict(names, fused=names["gateup"])
+        dom_bytes = (alg["gateup_bytes"] + alg["down_bytes"]) / layers
+        dom_flops = (alg["gateup_flops"] + alg["down_flops"]) / layers
+    else:
+        dominant = "gateup" if stage_us[3] >= stage_us[4] else "down"
+        dom_us = stage_us[3] if dominant == "gateup" else stage_us[4]
+        dom_bytes = alg[f"{dominant}_bytes"] / layers
+        dom_flops = alg[f"{dominant}_flops"] / layers
     compute_bound = dom_flops / dom_bytes > cpeak * 1e12 / (hbm * 1e9)
     traffic = profile_traffic(f"{names['file']}:{dominant}:{w.name}{'-dense' if dense else ''}:T{T}")
     if compute_bound:

@@ -49,8 +49,9 @@ moe_status check_route_args(const void *x, int act_dt, int T, int d, const void 
 
 struct WsLayout {
     size_t status, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w, h, xp, pgu, pd,
-        rank, tile_cnt, total;
-    bool dtc;   // tensor-core decode partials present
+        flags, rank, tile_cnt, total;
+    bool dtc;   // tensor-core decode scratch present
+    int n_flags;
 };
 
 bool prefill_capable(int act_dt, int w_dt, int d, int F)
@@ -80,12 +81,16 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.dtc = act_dt == MOE_BF16 && w_dt == MOE_BF16 && d % 128 == 0 && F % 128 == 0 &&
             n <= (size_t)kDecodeTcMaxRows;
     L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
-    L.pgu = L.pd = off;
+    L.pgu = L.pd = L.flags = off;
+    L.n_flags = 0;
     if (L.dtc) {
         int ks_gu = 1, ks_d = 1;
         decode_tc_splits(T, d, E, k, F, &ks_gu, &ks_d);
         L.pgu = take(4 * (size_t)ks_gu * 2 * n * (size_t)F);
         L.pd = take(4 * (size_t)ks_d * n * (size_t)d);
+        // the fused decode kernel's flags (whichever decode kernels run)
+        L.n_flags = decode_fused_flag_words(T, E, k, F);
+        L.flags = take(4 * (size_t)L.n_flags);
     }
     L.total = off;
     return L;
@@ -359,9 +364,15 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
     const bool use_dtc = !use_prefill && path != MOE_PATH_DECODE_SIMT && L.dtc &&
                          decode_tc_capable(act_dt, w_dt, d, F, E);
+    const int num_sms = device_sm_count();
+    // bf16 decode batches with enough (expert, tile) units: gate/up, down and
+    // combine in one persistent kernel
+    const bool use_fused = use_dtc && decode_fused_fits(T, d, E, k, F, num_sms);
     // the expert kernels that accumulate into `out` need it zeroed first (the
-    // tensor-core decode path adds into it only when its down kernel does)
-    const bool zero_out = k > 1 && (!use_dtc || decode_tc_down_direct(T, d, E, k, F));
+    // fused kernel adds into it for k = 2 and stores for k = 1; the other
+    // tensor-core decode kernels add into it only when their down kernel does)
+    const bool zero_out = use_fused ? k == 2
+                          : k > 1 && (!use_dtc || decode_tc_down_direct(T, d, E, k, F));
     // routing, then the grouping scatter (which also writes the grouped x rows
     // that the tensor-core expert kernels read)
     RouteTcArgs ra{};
@@ -373,13 +384,14 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     ra.counts = counts; ra.offsets = offsets; ra.perm_tok = perm_tok; ra.inv = inv; ra.perm_w = perm_w;
     const bool act16 = act_dt == MOE_BF16;
     // decode batches of up to 128 tokens: one clustered kernel routes and
-    // groups (no scatter) and the expert kernel gathers x rows itself (no xp)
+    // groups (no scatter); the tensor-core decode kernel gathers x rows itself
     const bool fused_small = !dense && use_dtc && route_small_capable(act_dt, T, d, E, k);
-    ra.xp = ((use_prefill || use_dtc) && act16 && !fused_small) ? ws + L.xp : nullptr;
+    ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && !fused_small) ? ws + L.xp : nullptr;
     ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
-    ra.zero_words = nullptr;
-    ra.n_zero = 0;
+    // the fused decode kernel's flags and ticket start at zero
+    ra.zero_words = use_fused ? reinterpret_cast<uint32_t *>(ws + L.flags) : nullptr;
+    ra.n_zero = use_fused ? L.n_flags : 0;
     ra.status = status;
     ra.ev_routed = ev[1];
     bool xp_ready = ra.xp != nullptr;
@@ -389,7 +401,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     cudaError_t e;
     if (dense) {
         e = launch_identity_grouping(T, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w,
-                                     status, device_sm_count(), s);
+                                     status, ra.zero_words, ra.n_zero, device_sm_count(), s);
         if (e != cudaSuccess || mark(1) != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
         const bool in_place = act16 && w_dt != MOE_Q8_0;
         if (in_place) xp_rows = const_cast<void *>(x);
@@ -409,7 +421,6 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
     }
 
-    const int num_sms = device_sm_count();
     if (use_prefill) {
         TcArgs a{};
         a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
@@ -419,6 +430,16 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.h = ws + L.h; a.out = out; a.zero_out = zero_out; a.status = status; a.num_sms = num_sms;
         a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
         e = launch_tc_experts(a, s);
+    } else if (use_fused) {
+        DecodeFusedArgs a{};
+        a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
+        a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down;
+        a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
+        a.h = reinterpret_cast<uint16_t *>(ws + L.h);
+        a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
+        a.out = out; a.status = status; a.num_sms = num_sms; a.ev_done = ev[4];
+        if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+        e = launch_decode_fused(a, s);
     } else if (use_dtc) {
         DecodeTcArgs a{};
         a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;

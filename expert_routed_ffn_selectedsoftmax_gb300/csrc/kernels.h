@@ -72,11 +72,12 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
                            cudaStream_t stream);
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
                                void *xp, int to_fp16, int num_sms, cudaStream_t stream);
-// dense layer (E = 1, k = 1): expert 0, weight 1, identity grouping; clears status
+// dense layer (E = 1, k = 1): expert 0, weight 1, identity grouping; clears
+// status and zero_words[n_zero]
 cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, int32_t *counts,
                                      int32_t *offsets, int32_t *perm_tok, int32_t *inv,
-                                     float *perm_w, uint32_t *status, int num_sms,
-                                     cudaStream_t stream);
+                                     float *perm_w, uint32_t *status, uint32_t *zero_words,
+                                     int n_zero, int num_sms, cudaStream_t stream);
 
 // decode.cu -- expert FFN for few rows per expert (CUDA-core, weight streaming)
 struct DecodeArgs {
@@ -123,6 +124,28 @@ void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d);
 bool decode_tc_gateup_fused(int T, int d, int E, int k, int F, int num_sms);
 bool decode_tc_down_direct(int T, int d, int E, int k, int F);
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream);
+
+// decode_fused.cu -- the decode expert FFN in one persistent launch (bf16,
+// k <= 2, whole-K items): gate/up, SwiGLU, down and combine
+struct DecodeFusedArgs {
+    const void *x;              // [T, d] bf16 (token rows gathered through perm_tok)
+    const int32_t *perm_tok;    // [T*k] grouped row -> token
+    int T, d, E, k, F;
+    const void *w_gate, *w_up, *w_down;   // bf16
+    const int32_t *offsets;     // [E+1]
+    const float *perm_w;        // [T*k] routing weight of each grouped row
+    uint16_t *h;                // bf16 h [T*k, F] scratch
+    uint32_t *flags;            // decode_fused_flag_words() words, zero at launch
+    float *out;                 // [T, d] fp32 (zeroed beforehand when k == 2)
+    uint32_t *status;
+    int num_sms;
+    cudaEvent_t ev_done;        // optional: recorded after the launch
+};
+// the shapes the fused kernel takes (beside decode_tc_capable's dtype rules)
+bool decode_fused_fits(int T, int d, int E, int k, int F, int num_sms);
+// scratch words it needs zeroed before it starts (h-ready flags, ticket counter)
+int decode_fused_flag_words(int T, int E, int k, int F);
+cudaError_t launch_decode_fused(const DecodeFusedArgs &a, cudaStream_t stream);
 
 // q8.cu
 cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,

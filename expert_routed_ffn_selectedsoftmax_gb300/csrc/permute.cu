@@ -169,9 +169,12 @@ __global__ void identity_grouping_kernel(int T, int32_t *__restrict__ topk_idx,
                                          float *__restrict__ topk_w, int32_t *__restrict__ counts,
                                          int32_t *__restrict__ offsets, int32_t *__restrict__ perm_tok,
                                          int32_t *__restrict__ inv, float *__restrict__ perm_w,
-                                         uint32_t *__restrict__ status)
+                                         uint32_t *__restrict__ status, uint32_t *__restrict__ zero_words,
+                                         int n_zero)
 {
     pdl_enter();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x)
+        zero_words[i] = 0u;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (status) *status = kDevOk;
         counts[0] = T;
@@ -189,14 +192,14 @@ __global__ void identity_grouping_kernel(int T, int32_t *__restrict__ topk_idx,
 
 cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, int32_t *counts,
                                      int32_t *offsets, int32_t *perm_tok, int32_t *inv,
-                                     float *perm_w, uint32_t *status, int num_sms,
-                                     cudaStream_t stream)
+                                     float *perm_w, uint32_t *status, uint32_t *zero_words,
+                                     int n_zero, int num_sms, cudaStream_t stream)
 {
     long long want = ((long long)T + 255) / 256, cap = (long long)num_sms * 4;
     int blocks = (int)(want < cap ? want : cap);
     if (blocks < 1) blocks = 1;
     launch_pdl(identity_grouping_kernel, dim3(blocks), dim3(256), 0, stream, T, topk_idx, topk_w,
-               counts, offsets, perm_tok, inv, perm_w, status);
+               counts, offsets, perm_tok, inv, perm_w, status, zero_words, n_zero);
     return cudaGetLastError();
 }
 

@@ -190,7 +190,16 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();                       // every CTA's mbarriers exist before anyone signals them
-    pdl_enter();
+    pdl_wait();   // (the next kernel is released once this CTA's operands are in: see below)
+    if (threadIdx.x == 0) {
+        // ------------------------------------------------ TMA: every operand tile at once,
+        // first, so that the zeroing below overlaps the round trip from HBM
+        mbar_expect_tx(&c.full, (uint32_t)(nkb * (p.box_rows + EP) * BK * 2));
+        for (int j = 0; j < nkb; ++j) {
+            tma_load_2d(a_tiles + (size_t)j * A_TILE, &tm_x, &c.full, (kb0 + j) * BK, 0);
+            tma_load_2d(b_tiles + (size_t)j * BT, &tm_w, &c.full, (kb0 + j) * BK, 0);
+        }
+    }
     if (p.status && rank == 0 && threadIdx.x == 0) *p.status = kDevOk;
     if (p.out_zero) {   // this CTA's share of the output rows
         float4 *o4 = reinterpret_cast<float4 *>(p.out_zero);
@@ -206,14 +215,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     const uint32_t tmem = c.tmem_base;
     volatile int *abort_flag = &c.abort_flag;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ TMA: every operand tile at once
-        mbar_expect_tx(&c.full, (uint32_t)(nkb * (p.box_rows + EP) * BK * 2));
-        for (int j = 0; j < nkb; ++j) {
-            tma_load_2d(a_tiles + (size_t)j * A_TILE, &tm_x, &c.full, (kb0 + j) * BK, 0);
-            tma_load_2d(b_tiles + (size_t)j * BT, &tm_w, &c.full, (kb0 + j) * BK, 0);
-        }
-    } else if (warp == 1 && lane == 0) {
+    if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         const uint32_t idesc = idesc_f16_mn(0, 128, EP);
         const bool ok = mbar_wait(&c.full, 0, abort_flag);
@@ -264,6 +266,10 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     }
     __syncwarp();
     __syncthreads();
+    // the operands are in and the logits computed: the next kernel of the
+    // stream may start launching now (its reads from HBM no longer compete
+    // with this kernel's)
+    pdl_trigger();
     if (threadIdx.x < R) {
         // owner q = lane receives its token rows of this CTA's partials in slot `rank`
         const int q = threadIdx.x, n = owned_rows(q, p.tpc, p.T);

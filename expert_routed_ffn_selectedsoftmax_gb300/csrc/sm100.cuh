@@ -106,6 +106,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// Prefetch of one tile into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+                 : "memory");
+}
 // Tile load of one CTA of a CTA pair (cta_group::2): the tile lands in this
 // CTA's shared memory and its bytes are counted on the mbarrier at
 // shared::cluster address `bar_cl`, which may belong to either CTA of the pair.
