@@ -28,7 +28,7 @@ EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "mo
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_q4_a64_packed_size", "moe_pack_q4_a64",
            "moe_workspace_size", "moe_forward",
            "moe_forward_profiled", "moe_forward_scored", "moe_ffn_dense", "moe_forward_noalloc",
-           "moe_workspace_views", "moe_check", "moe_check_noalloc")
+           "moe_workspace_views", "moe_forward_expire_wait", "moe_check", "moe_check_noalloc")
 
 _lib = None
 
@@ -88,6 +88,9 @@ def load_library():
     L.moe_ffn_dense.restype = i
     L.moe_forward_noalloc.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, i, vp]
     L.moe_forward_noalloc.restype = i
+    L.moe_forward_expire_wait.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz,
+                                          i, i, ctypes.c_uint32, vp]
+    L.moe_forward_expire_wait.restype = i
     L.moe_workspace_views.argtypes = [i, i, i, i, i, i, i, vp]
     L.moe_workspace_views.restype = i
     L.moe_check.argtypes = [vp, vp, vp]

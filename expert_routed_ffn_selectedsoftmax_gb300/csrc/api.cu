@@ -146,7 +146,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
                         const float *sel_bias, int E, int k, const void *w_gate, const void *w_up,
                         const void *w_down, moe_dtype w_dt, int F, float *out, void *workspace,
                         size_t ws_bytes, int path, int scoring, bool dense, void *const *events,
-                        moe_stream stream);
+                        moe_stream stream, int expire_family = 0, uint32_t expire_ns = 0);
 
 }  // namespace
 
@@ -319,6 +319,21 @@ moe_status moe_ffn_dense(const void *x, moe_dtype act_dt, int T, int d, const vo
                         stream);
 }
 
+moe_status moe_forward_expire_wait(const void *x, moe_dtype act_dt, int T, int d,
+                                   const void *w_router, const float *sel_bias, int E, int k,
+                                   const void *w_gate, const void *w_up, const void *w_down,
+                                   moe_dtype w_dt, int F, float *out, void *workspace,
+                                   size_t ws_bytes, int path, int kernel_family, uint32_t wait_ns,
+                                   moe_stream stream)
+{
+    if (kernel_family < MOE_KERNEL_ROUTER_CLUSTER || kernel_family > MOE_KERNEL_GEMM ||
+        wait_ns == 0 || wait_ns > 100000000u)
+        return MOE_ERR_INVALID_ARG;
+    return forward_impl(x, act_dt, T, d, w_router, sel_bias, E, k, w_gate, w_up, w_down, w_dt, F,
+                        out, workspace, ws_bytes, path, MOE_SCORE_SELECTED_SOFTMAX, false, nullptr,
+                        stream, kernel_family, wait_ns);
+}
+
 }  // extern "C"
 
 namespace {
@@ -330,7 +345,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
                         const float *sel_bias, int E, int k, const void *w_gate, const void *w_up,
                         const void *w_down, moe_dtype w_dt, int F, float *out, void *workspace,
                         size_t ws_bytes, int path, int scoring, bool dense, void *const *events,
-                        moe_stream stream)
+                        moe_stream stream, int expire_family, uint32_t expire_ns)
 {
     moe_status st = forward_args_check(x, act_dt, T, d, w_router, sel_bias, E, k, w_gate, w_up,
                                        w_down, w_dt, F, out, path, scoring, dense);
@@ -392,6 +407,23 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // the fused decode kernel's flags and ticket start at zero
     ra.zero_words = use_fused ? reinterpret_cast<uint32_t *>(ws + L.flags) : nullptr;
     ra.n_zero = use_fused ? L.n_flags : 0;
+    // the wait-expiry test hook: the kernel family named must run on this call
+    const bool route_tc_path = !dense && !fused_small && route_tc_capable(act_dt, d, E) &&
+                               T >= kRouteTcMinTokens;
+    uint32_t x_route = 0, x_dtc = 0, x_fused = 0, x_gemm = 0;
+    if (expire_family) {
+        bool runs = false;
+        switch (expire_family) {
+        case MOE_KERNEL_ROUTER_CLUSTER: runs = fused_small; x_route = expire_ns; break;
+        case MOE_KERNEL_ROUTER_TC: runs = route_tc_path; x_route = expire_ns; break;
+        case MOE_KERNEL_DECODE_SPLIT: runs = use_dtc && !use_fused; x_dtc = expire_ns; break;
+        case MOE_KERNEL_DECODE_FUSED: runs = use_fused; x_fused = expire_ns; break;
+        case MOE_KERNEL_GEMM: runs = use_prefill; x_gemm = expire_ns; break;
+        default: break;
+        }
+        if (!runs) return MOE_ERR_UNSUPPORTED;
+    }
+    ra.expire_ns = x_route;
     ra.status = status;
     ra.ev_routed = ev[1];
     bool xp_ready = ra.xp != nullptr;
@@ -409,7 +441,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     } else if (fused_small) {
         e = launch_route_small(ra, s);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
-    } else if (route_tc_capable(act_dt, d, E) && T >= kRouteTcMinTokens) {
+    } else if (route_tc_path) {
         e = launch_route_tc(ra, s);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
     } else {
@@ -428,6 +460,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
         a.xp = xp_rows; a.xp_ready = xp_ready;
         a.h = ws + L.h; a.out = out; a.zero_out = zero_out; a.status = status; a.num_sms = num_sms;
+        a.expire_ns = x_gemm;
         a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
         e = launch_tc_experts(a, s);
     } else if (use_fused) {
@@ -438,6 +471,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.h = reinterpret_cast<uint16_t *>(ws + L.h);
         a.flags = reinterpret_cast<uint32_t *>(ws + L.flags);
         a.out = out; a.status = status; a.num_sms = num_sms; a.ev_done = ev[4];
+        a.expire_ns = x_fused;
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
         e = launch_decode_fused(a, s);
     } else if (use_dtc) {
@@ -448,6 +482,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.pgu = reinterpret_cast<float *>(ws + L.pgu); a.pd = reinterpret_cast<float *>(ws + L.pd);
         a.h = reinterpret_cast<uint16_t *>(ws + L.h);
         a.out = out; a.status = status; a.num_sms = num_sms; a.ev_gateup = ev[4];
+        a.expire_ns = x_dtc;
         a.perm_tok = perm_tok;
         a.perm_w = perm_w;
         if (fused_small) {

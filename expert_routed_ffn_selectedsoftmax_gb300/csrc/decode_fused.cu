@@ -95,6 +95,7 @@ struct Params {
     float *out;               // [T, d] fp32 (zeroed beforehand when k == 2)
     uint32_t *flags;          // zeroed by the router: see flag_layout()
     uint32_t *status;
+    uint32_t expire_ns;       // > 0: the producer's first wait gives up after this long (test hook)
 };
 
 // Flag words (all zero at launch): h ready per (chunk, F tile), then the
@@ -118,6 +119,7 @@ struct Item {
 struct Ctl {
     uint64_t full_w[STAGES], full_x[STAGES], empty[STAGES];
     uint64_t tfull[NPAIR], tempty[NPAIR], qfull[QN], qempty[QN], drain;
+    uint64_t never;                     // nothing arrives here (test hook)
     uint32_t tmem_base;
     int abort_flag;
     int n_gu, n_all;
@@ -253,6 +255,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
         for (int b = 0; b < NPAIR; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
         for (int q = 0; q < QN; ++q) { mbar_init(&c.qfull[q], 1); mbar_init(&c.qempty[q], kQueueConsumers); }
         mbar_init(&c.drain, 1);
+        mbar_init(&c.never, 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -330,9 +333,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ tickets + TMA producer (weights)
         uint32_t it_k = 0, qi = 0;
-        bool ok = true;
+        bool ok = p.expire_ns == 0 || mbar_wait(&c.never, 0, abort_flag, p.expire_ns);
         int t = first_ticket;
-        for (;;) {
+        while (ok) {
             const Item it = decode_ticket(c, p, t);
             const uint32_t qs = qi % QN, qph = (qi / QN) & 1u;
             if (!mbar_wait(&c.qempty[qs], qph ^ 1u, abort_flag)) { ok = false; break; }
@@ -611,6 +614,7 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs &a, cudaStream_t stream)
     p.spec_kb = decode_fused_spec_kb(a.T, a.d, a.E, a.k, a.F);
     p.x = static_cast<const uint16_t *>(a.x); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
     p.h = a.h; p.out = a.out; p.flags = a.flags; p.status = a.status;
+    p.expire_ns = a.expire_ns;
 
     // grid: every CTA slot, or the items there can be at most
     const long long max_items = (long long)p.nc_max * (a.F / BM + a.d / BM);

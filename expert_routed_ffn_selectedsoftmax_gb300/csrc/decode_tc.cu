@@ -93,10 +93,12 @@ struct Params {
     float *out;          //   out [T, R] fp32 (zeroed beforehand when k > 1)
     const float *perm_w;
     int k;
+    uint32_t expire_ns;  // > 0: the producer's first wait gives up after this long (test hook)
 };
 
 struct Ctl {
     uint64_t full[STAGES], empty[STAGES], tfull[NACC], tempty[NACC], drain;
+    uint64_t never;      // nothing arrives here (test hook)
     uint32_t tmem_base;
     int abort_flag;
     int n_items;
@@ -176,6 +178,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], GATHER ? 33 : 1); mbar_init(&c.empty[s], 1); }
         for (int b = 0; b < NACC; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
         mbar_init(&c.drain, 1);
+        mbar_init(&c.never, 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -237,7 +240,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer: weights + token rows
         uint32_t it_k = 0;
-        bool ok = true;
+        bool ok = p.expire_ns == 0 || mbar_wait(&c.never, 0, abort_flag, p.expire_ns);
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item(c, p, item);
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
@@ -625,6 +628,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
         p.n_mats = 2; p.KS = ks_gu; p.P = a.pgu;
     }
     const dim3 g_gu(grid_for(chunks * p.n_mats * p.rtiles * p.KS));
+    p.expire_ns = a.expire_ns;   // (the gate/up kernel only)
     if (gather) {
         p.xg = static_cast<const uint16_t *>(a.x_gather);
         p.perm_tok = a.perm_tok;
@@ -654,6 +658,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     p.K = a.F; p.R = a.d; p.n_mats = 1; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
     p.fused = 0; p.h = nullptr;
     p.xg = nullptr;
+    p.expire_ns = 0;
     if (direct) {
         p.KS = 1; p.direct = 1; p.out = a.out; p.perm_tok = a.perm_tok; p.perm_w = a.perm_w; p.k = a.k;
     } else {

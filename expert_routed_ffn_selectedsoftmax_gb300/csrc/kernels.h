@@ -51,6 +51,7 @@ struct RouteTcArgs {
     int n_zero;
     uint32_t *status;
     cudaEvent_t ev_routed;      // optional: recorded between routing and scatter
+    uint32_t expire_ns;         // > 0: one bounded wait gives up after this long (test hook)
 };
 bool route_tc_capable(int act_dt, int d, int E);
 int route_tc_tiles(int T);
@@ -115,6 +116,7 @@ struct DecodeTcArgs {
     uint32_t *status;
     int num_sms;
     cudaEvent_t ev_gateup;
+    uint32_t expire_ns;         // > 0: one bounded wait gives up after this long (test hook)
 };
 constexpr int kDecodeTcMaxRows = 8192;   // T*k above this uses the CUDA-core kernels
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E);
@@ -140,6 +142,7 @@ struct DecodeFusedArgs {
     uint32_t *status;
     int num_sms;
     cudaEvent_t ev_done;        // optional: recorded after the launch
+    uint32_t expire_ns;         // > 0: one bounded wait gives up after this long (test hook)
 };
 // the shapes the fused kernel takes (beside decode_tc_capable's dtype rules)
 bool decode_fused_fits(int T, int d, int E, int k, int F, int num_sms);

@@ -73,10 +73,12 @@ struct Params {
     float *out_zero;                     // optional [T, d] output to zero (the down kernel adds into it)
     uint32_t *zero_words;                // optional scratch words later kernels count on being zero
     int n_zero;
+    uint32_t expire_ns;                  // > 0: the MMA thread's operand wait gives up after this long (test hook)
 };
 
 struct Ctl {
     uint64_t full, tfull, rx, mx;        // operands, MMAs, partials received, masks received
+    uint64_t never;                      // nothing arrives here (test hook)
     uint32_t tmem_base;
     int abort_flag;
     float bias[kMaxExperts];
@@ -172,6 +174,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     if (threadIdx.x == 0) {
         mbar_init(&c.full, 1);
         mbar_init(&c.tfull, 1);
+        mbar_init(&c.never, 1);
         mbar_init(&c.rx, 1);
         mbar_init(&c.mx, 1);
         // the bytes the peers will send: R slots of this CTA's token rows, and
@@ -218,7 +221,8 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         const uint32_t idesc = idesc_f16_mn(0, 128, EP);
-        const bool ok = mbar_wait(&c.full, 0, abort_flag);
+        const bool ok = (p.expire_ns == 0 || mbar_wait(&c.never, 0, abort_flag, p.expire_ns)) &&
+                        mbar_wait(&c.full, 0, abort_flag);
         if (ok) {
             tc_fence_after();
             for (int j = 0; j < nkb; ++j) {
@@ -436,6 +440,14 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         p.inv[(size_t)t * p.k + j] = pos;
         p.perm_w[pos] = c.sel_w[i][j];
     }
+    if (threadIdx.x == 0 && *abort_flag) {
+        // a wait above gave up early: the peers' copies into this CTA (sent
+        // by every CTA on every path) land before it leaves (bounded)
+        volatile int no_abort = 0;
+        if (mine_rows > 0) mbar_wait(&c.rx, 0, &no_abort);
+        mbar_wait(&c.mx, 0, &no_abort);
+    }
+    __syncthreads();
     if (threadIdx.x < R) bulk_wait_read();    // this CTA's outgoing copies have read their sources
     // no CTA leaves while a peer may still copy into it (no memory ordering needed)
     __syncwarp();
@@ -502,6 +514,7 @@ cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream)
     p.counts = a.counts; p.offsets = a.offsets; p.perm_tok = a.perm_tok; p.inv = a.inv;
     p.perm_w = a.perm_w; p.status = a.status; p.out_zero = a.out_zero;
     p.zero_words = a.zero_words; p.n_zero = a.n_zero;
+    p.expire_ns = a.expire_ns;
     auto kern = a.k == 1 ? route_small_kernel<1> : a.k == 2 ? route_small_kernel<2>
               : a.k <= 4 ? route_small_kernel<4> : route_small_kernel<8>;
     err = launch_pdl_cluster(kern, dim3(R), dim3(THREADS), smem, stream, R, m_x, m_w, p);

@@ -65,10 +65,12 @@ struct Params {
     uint32_t *zero_words;
     int n_zero;
     uint32_t *status;
+    uint32_t expire_ns;   // > 0: the producer's first wait gives up after this long (test hook)
 };
 
 struct Ctl {
     uint64_t full[MAXST], empty[MAXST], tfull, epi;
+    uint64_t never;                  // nothing arrives here (test hook)
     uint32_t tmem_base;
     int abort_flag;
     float bias[kMaxExperts];
@@ -132,6 +134,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], 1); mbar_init(&c.empty[s], 1); }
         mbar_init(&c.tfull, 1);
         mbar_init(&c.epi, 128);
+        mbar_init(&c.never, 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -148,9 +151,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
-        bool ok = true;
+        bool ok = p.expire_ns == 0 || mbar_wait(&c.never, 0, abort_flag, p.expire_ns);
         int kb = 0;
-        for (; kb < kblocks; ++kb) {
+        for (; ok && kb < kblocks; ++kb) {
             const int s = kb % STAGES;
             const uint32_t ph = (kb / STAGES) & 1u;
             if (!mbar_wait(&c.empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
@@ -496,6 +499,7 @@ cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream)
     p.T = a.T; p.d = a.d; p.E = a.E; p.EP = EP; p.k = a.k; p.bias = a.bias; p.mode = a.mode;
     p.topk_idx = a.topk_idx; p.topk_w = a.topk_w; p.rank = a.rank; p.tile_cnt = a.tile_cnt;
     p.out_zero = a.out_zero; p.zero_words = a.zero_words; p.n_zero = a.n_zero; p.status = a.status;
+    p.expire_ns = a.expire_ns;
     const int ntiles = route_tc_tiles(a.T);
     auto kern = a.k == 1 ? route_tc_kernel<1> : a.k == 2 ? route_tc_kernel<2>
               : a.k <= 4 ? route_tc_kernel<4> : route_tc_kernel<8>;

@@ -143,10 +143,13 @@ struct Params {
     int h_fp16;               // GATEUP: write h as fp16 (else bf16)
     float *out_zero;          // GATEUP: `out` to zero for the down kernel's adds, or null
     long long zero4;          // float4 elements of out_zero
+    uint32_t expire_ns;       // > 0: the producer's first wait gives up after this long (test hook)
 };
 
-struct SmemCtl {
+// (16-byte aligned size: the down epilogue's float4 staging rows follow it)
+struct alignas(16) SmemCtl {
     uint64_t full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain, cfull[4], cempty[4];
+    uint64_t never;   // nothing arrives here (test hook)
     uint32_t tmem_base;
     int abort_flag;
     uint32_t fail;
@@ -250,6 +253,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         for (int b = 0; b < 2; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], CL * kEpiWarps); }
         for (int b = 0; b < 4; ++b) { mbar_init(&c.cfull[b], CL * kConvWarps); mbar_init(&c.cempty[b], 1); }
         mbar_init(&c.drain, 1);
+        mbar_init(&c.never, 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -318,7 +322,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         uint32_t it = 0;   // global k-block counter across tiles
-        bool ok = true;
+        bool ok = p.expire_ns == 0 || mbar_wait(&c.never, 0, abort_flag, p.expire_ns);
         for (int tile = cid; tile < total && ok; tile += nclusters) {
             int e, mt, nt;
             decode_tile(c, E, tile, e, mt, nt);
@@ -605,6 +609,7 @@ template <bool Q8, bool PAIR> constexpr size_t smem_bytes()
     // ring (+ converted B buffers), control block, down-epilogue staging
     return 1024 + Cfg<Q8, PAIR>::CTL + sizeof(SmemCtl) + kStgBytes;
 }
+static_assert(sizeof(SmemCtl) % 16 == 0, "the staging rows after the control block take float4 stores");
 static_assert(smem_bytes<false, true>() <= 232448 && smem_bytes<true, true>() <= 232448 &&
                   smem_bytes<false, false>() <= 232448 && smem_bytes<true, false>() <= 232448,
               "shared memory per CTA");
@@ -765,6 +770,7 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     p.K = a.F; p.n_tiles = a.d / BN;
+    p.expire_ns = 0;   // (the hook acts on the gate/up kernel only)
     const dim3 g2 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<DOWN, Q8>() : a.num_sms);
     if (PAIR)
         err = launch_pdl_cluster(grouped_gemm_kernel<DOWN, Q8, PAIR>, g2, block, smem, stream, CL, m_h,
@@ -834,6 +840,7 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     p.out = a.out; p.status = a.status; p.h_fp16 = q8 ? 1 : 0;
     p.out_zero = a.zero_out ? a.out : nullptr;
     p.zero4 = (long long)a.T * a.d / 4;
+    p.expire_ns = a.expire_ns;
     if (q8)
         return pair ? launch_gemms<true, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
                     : launch_gemms<true, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);

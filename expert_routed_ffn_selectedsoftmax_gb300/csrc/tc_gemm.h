@@ -26,6 +26,7 @@ struct TcArgs {
     int num_sms;
     cudaEvent_t ev_gathered;    // optional: recorded after the row gather
     cudaEvent_t ev_gateup;      // optional: recorded after the gate/up GEMM
+    uint32_t expire_ns;         // > 0: one bounded wait gives up after this long (test hook)
 };
 
 namespace tc {

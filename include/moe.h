@@ -318,6 +318,40 @@ MOE_API moe_status moe_forward_noalloc(const void *x, moe_dtype act_dt, int T, i
                                        moe_stream stream);
 
 /*
+ * Test hook of the failure handling.  Every wait of the library's
+ * tensor-core kernels is bounded (2 s); a wait that gives up records
+ * MOE_ERR_TIMEOUT in the status word, the kernel's other roles stop, its
+ * copies and MMAs in flight land, its TMEM is freed and it returns, and the
+ * call's later kernels return without work.  moe_forward_expire_wait runs
+ * moe_forward with one wait of one kernel family -- at its start, on a
+ * barrier that nothing ever arrives on and that no copy or MMA targets --
+ * limited to `wait_ns` (1 ns .. 100 ms) in every CTA of that kernel, so that
+ * this path runs without any fault: moe_check then reports MOE_ERR_TIMEOUT
+ * and the outputs of the call are invalid.  It returns MOE_ERR_UNSUPPORTED
+ * (nothing enqueued) when the named family does not run for these arguments:
+ *   MOE_KERNEL_ROUTER_CLUSTER  the clustered router (bf16 decode, T <= 128),
+ *                              the MMA thread's operand wait
+ *   MOE_KERNEL_ROUTER_TC       the tensor-core router (bf16, T >= 512)
+ *   MOE_KERNEL_DECODE_SPLIT    the split-K tensor-core decode kernels (gate/up)
+ *   MOE_KERNEL_DECODE_FUSED    the one-launch tensor-core decode kernel
+ *   MOE_KERNEL_GEMM            the grouped GEMMs (gate/up; CTA pairs for Q8_0)
+ * (the producer's first wait unless stated).  Not for production use.
+ */
+typedef enum {
+    MOE_KERNEL_ROUTER_CLUSTER = 1,
+    MOE_KERNEL_ROUTER_TC = 2,
+    MOE_KERNEL_DECODE_SPLIT = 3,
+    MOE_KERNEL_DECODE_FUSED = 4,
+    MOE_KERNEL_GEMM = 5
+} moe_kernel_family;
+MOE_API moe_status moe_forward_expire_wait(const void *x, moe_dtype act_dt, int T, int d,
+                                           const void *w_router, const float *sel_bias, int E,
+                                           int k, const void *w_gate, const void *w_up,
+                                           const void *w_down, moe_dtype w_dt, int F, float *out,
+                                           void *workspace, size_t ws_bytes, int path,
+                                           int kernel_family, uint32_t wait_ns, moe_stream stream);
+
+/*
  * moe_check_noalloc -- moe_check for moe_forward_noalloc: wait for `stream`,
  * then read the status word the most recent moe_forward_noalloc on the
  * current device left in the library's static scratch (MOE_OK,
