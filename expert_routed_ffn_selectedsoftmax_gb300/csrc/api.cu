@@ -49,7 +49,7 @@ moe_status check_route_args(const void *x, int act_dt, int T, int d, const void 
 
 struct WsLayout {
     size_t status, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w, h, xp, pgu, pd,
-        flags, rank, tile_cnt, total;
+        flags, y, xexp, rank, tile_cnt, total;
     bool dtc;   // tensor-core decode scratch present
     int n_flags;
 };
@@ -82,6 +82,11 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
             n <= (size_t)kDecodeTcMaxRows;
     L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
     L.pgu = L.pd = L.flags = off;
+    // k > 2: weighted expert outputs per grouped row, combined in slot order
+    // (the CUDA-core decode kernels and the grouped GEMMs)
+    L.y = k > 2 ? take(4 * n * (size_t)d) : off;
+    // Q8_0 grouped GEMMs: exponent of each fp16 grouped row's scale
+    L.xexp = (prefill_capable(act_dt, w_dt, d, F) && w_dt == MOE_Q8_0) ? take(4 * n) : off;
     L.n_flags = 0;
     if (L.dtc) {
         int ks_gu = 1, ks_d = 1;
@@ -387,7 +392,8 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // fused kernel adds into it for k = 2 and stores for k = 1; the other
     // tensor-core decode kernels add into it only when their down kernel does)
     const bool zero_out = use_fused ? k == 2
-                          : k > 1 && (!use_dtc || decode_tc_down_direct(T, d, E, k, F));
+                          : use_dtc ? k > 1 && decode_tc_down_direct(T, d, E, k, F)
+                                    : k == 2;   // k > 2: combined from per-row outputs
     // routing, then the grouping scatter (which also writes the grouped x rows
     // that the tensor-core expert kernels read)
     RouteTcArgs ra{};
@@ -402,7 +408,8 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // groups (no scatter); the tensor-core decode kernel gathers x rows itself
     const bool fused_small = !dense && use_dtc && route_small_capable(act_dt, T, d, E, k);
     ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && !fused_small) ? ws + L.xp : nullptr;
-    ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows
+    ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows (scaled)
+    ra.xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     // the fused decode kernel's flags and ticket start at zero
     ra.zero_words = use_fused ? reinterpret_cast<uint32_t *>(ws + L.flags) : nullptr;
@@ -460,6 +467,8 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
         a.xp = xp_rows; a.xp_ready = xp_ready;
         a.h = ws + L.h; a.out = out; a.zero_out = zero_out; a.status = status; a.num_sms = num_sms;
+        a.y = reinterpret_cast<float *>(ws + L.y); a.inv = inv;
+        a.xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
         a.expire_ns = x_gemm;
         a.ev_gathered = ev[3]; a.ev_gateup = ev[4];
         e = launch_tc_experts(a, s);
@@ -488,7 +497,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         if (fused_small) {
             a.x_gather = x;
         } else if (!xp_ready &&
-                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, 0, num_sms, s) != cudaSuccess) {
+                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, 0, nullptr, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;
         }
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
@@ -499,6 +508,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down; a.w_dt = w_dt;
         a.offsets = offsets; a.perm_tok = perm_tok; a.perm_w = perm_w;
         a.h = reinterpret_cast<float *>(ws + L.h); a.out = out; a.num_sms = num_sms;
+        a.y = reinterpret_cast<float *>(ws + L.y); a.inv = inv; a.status = status;
         a.ev_gateup = ev[4];
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
         e = launch_decode_experts(a, s);

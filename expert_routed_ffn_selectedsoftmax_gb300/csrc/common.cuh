@@ -156,6 +156,41 @@ template <> struct WView<Q4Tag> {
     }
 };
 
+// fp16 rows of the Q8_0 tensor-core path: each bf16 row is scaled by a power
+// of two, 2^-e, so that its largest magnitude is at most 1 (e = 0 for an
+// all-zero or non-finite row).  The scaling is exact, so fp16 keeps the
+// bf16 values' digits while no row can leave fp16's range; the epilogues undo
+// it exactly.  e is the exponent of the row maximum (warp-collective: every
+// lane gets the same e).
+__device__ __forceinline__ int fp16_row_exponent(const uint16_t *row, int d, int lane)
+{
+    float m = 0.f;
+    for (int c = lane; c < d / 8; c += 32) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(row) + c);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[q])), fabsf(bf16hi(w[q]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (!(m > 0.f) || !isfinite(m)) return 0;
+    int e;
+    frexpf(m, &e);   // m = f * 2^e, f in [0.5, 1): m <= 2^e
+    return e;
+}
+// Eight bf16 values (one uint4) times 2^-e, as fp16.
+__device__ __forceinline__ uint4 bf16x8_to_fp16_scaled(uint4 u, int e)
+{
+    const float sc = ldexpf(1.f, -e);
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __half2 hh = __floats2half2_rn(bf16lo(w[q]) * sc, bf16hi(w[q]) * sc);
+        w[q] = *reinterpret_cast<uint32_t *>(&hh);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Programmatic dependent launch.  Every kernel of the library is launched so
 // that it may start while its predecessor in the stream finishes; it calls
 // pdl_wait() before touching global memory (this waits for the predecessor to

@@ -146,7 +146,8 @@ template <typename WT, int NCH, int RPW>
 __global__ void __launch_bounds__(kDecThreads)
 decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
-                   const float *__restrict__ perm_w, int E, int k, float *__restrict__ out)
+                   const float *__restrict__ perm_w, int E, int k, float *__restrict__ out,
+                   float *__restrict__ y)
 {
     pdl_enter();
     __shared__ int act[kMaxExperts];
@@ -205,15 +206,56 @@ decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
                 const int r = transpose8_row(lane);
                 if ((lane & 3) == 0 && r < nr && o0 + i < d) {
                     const int row = row0 + rb + r;
-                    const int t = perm_tok[row];
                     const float v = perm_w[row] * s;
-                    float *dst = out + (size_t)t * d + o0 + i;
-                    if (k == 1) *dst = v;
-                    else atomicAdd(dst, v);
+                    if (k > 2) {
+                        // the grouped row's weighted output; combine_rows_kernel adds
+                        // each token's k rows in slot order
+                        y[(size_t)row * d + o0 + i] = v;
+                    } else {
+                        // k = 1: the only contribution; k = 2: two additions onto
+                        // zero, whose result does not depend on their order
+                        float *dst = out + (size_t)perm_tok[row] * d + o0 + i;
+                        if (k == 1) *dst = v;
+                        else atomicAdd(dst, v);
+                    }
                 }
             }
         }
     }
+}
+
+// out[t, :] = sum_j y[inv[t, j], :] over the k slots of token t in slot order
+// (y holds each grouped row's routing-weighted expert output): the combine of
+// k > 2 experts without atomics, so results do not depend on timing.
+__global__ void __launch_bounds__(256)
+combine_rows_kernel(const float *__restrict__ y, int d, const int32_t *__restrict__ inv, int T,
+                    int k, float *__restrict__ out, const uint32_t *status)
+{
+    pdl_enter();
+    if (upstream_failed(status)) return;
+    const int vec = d / 4;
+    const long long total = (long long)T * vec;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / vec), o = (int)(i - (long long)t * vec) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(y + (size_t)inv[t * k + j] * d + o));
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        *reinterpret_cast<float4 *>(out + (size_t)t * d + o) = acc;
+    }
+}
+
+cudaError_t launch_combine_rows(const float *y, int d, const int32_t *inv, int T, int k, float *out,
+                                const uint32_t *status, int num_sms, cudaStream_t stream)
+{
+    long long blocks = ((long long)T * (d / 4) + 255) / 256;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    launch_pdl(combine_rows_kernel, dim3((unsigned)(blocks < 1 ? 1 : blocks)), dim3(256), 0, stream, y,
+               d, inv, T, k, out, status);
+    return cudaGetLastError();
 }
 
 template <typename K>
@@ -256,8 +298,10 @@ static cudaError_t launch_down(const DecodeArgs &a, WView<WT> wd, cudaStream_t s
     int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);
     if (g < 1) g = 1;
     launch_pdl(k2, dim3(g), dim3(kDecThreads), 0, stream, a.h, a.F, wd, a.d, a.offsets, a.perm_tok,
-               a.perm_w, a.E, a.k, a.out);
-    return cudaGetLastError();
+               a.perm_w, a.E, a.k, a.out, a.y);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || a.k <= 2) return err;
+    return launch_combine_rows(a.y, a.d, a.inv, a.T, a.k, a.out, a.status, a.num_sms, stream);
 }
 
 template <typename AT, typename WT>

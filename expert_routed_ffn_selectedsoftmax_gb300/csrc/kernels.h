@@ -45,7 +45,8 @@ struct RouteTcArgs {
     int32_t *counts, *offsets, *perm_tok, *inv;
     float *perm_w;
     void *xp;                   // optional [T*k, d] grouped copy of x
-    int xp_fp16;                // write xp as fp16 (else bf16)
+    int xp_fp16;                // write xp as fp16 (else bf16), row r scaled by 2^-xexp[r]
+    int32_t *xexp;              // [T*k] (xp_fp16): exponent of each grouped row's scale
     float *out_zero;            // optional rows to zero
     uint32_t *zero_words;       // optional scratch words to zero
     int n_zero;
@@ -71,8 +72,10 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
                            int32_t *offsets, int32_t *perm_tok, int32_t *inv,
                            const float *topk_w, float *perm_w, uint32_t *status,
                            cudaStream_t stream);
+// to_fp16: rows scaled by 2^-xexp[r] (fp16_row_exponent), xexp written
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
-                               void *xp, int to_fp16, int num_sms, cudaStream_t stream);
+                               void *xp, int to_fp16, int32_t *xexp, int num_sms,
+                               cudaStream_t stream);
 // dense layer (E = 1, k = 1): expert 0, weight 1, identity grouping; clears
 // status and zero_words[n_zero]
 cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, int32_t *counts,
@@ -91,11 +94,17 @@ struct DecodeArgs {
     const int32_t *perm_tok;    // [T*k]
     const float *perm_w;        // [T*k]
     float *h;                   // [T*k, F] fp32 scratch
-    float *out;                 // [T, d] fp32 (zeroed beforehand when k > 1)
+    float *out;                 // [T, d] fp32 (zeroed beforehand when k == 2)
+    float *y;                   // k > 2: [T*k, d] weighted expert outputs (then combined)
+    const int32_t *inv;         // [T*k] grouped row of each slot (k > 2)
+    const uint32_t *status;
     int num_sms;
     cudaEvent_t ev_gateup;      // optional: recorded between the two kernels
 };
 cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream);
+// out[t] = sum_j y[inv[t*k+j]] in slot order (k > 2 combine, no atomics)
+cudaError_t launch_combine_rows(const float *y, int d, const int32_t *inv, int T, int k, float *out,
+                                const uint32_t *status, int num_sms, cudaStream_t stream);
 
 // decode_tc.cu -- expert FFN for few rows per expert on tcgen05 (bf16 only)
 struct DecodeTcArgs {

@@ -135,28 +135,33 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
 }
 
 // xp[r, :] = x[perm_tok[r], :] (bf16 rows); with to_fp16 the rows are
-// re-encoded as fp16 for the fp16 tensor-core path of Q8_0 experts.
+// re-encoded as fp16 for the fp16 tensor-core path of Q8_0 experts, each
+// scaled by 2^-xexp[r] (fp16_row_exponent), one warp per row.
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, int d,
                                    const int32_t *__restrict__ perm_tok, int rows,
-                                   uint16_t *__restrict__ xp, int to_fp16)
+                                   uint16_t *__restrict__ xp, int to_fp16, int32_t *__restrict__ xexp)
 {
     pdl_enter();
     const int vec_per_row = d / 8;
+    if (to_fp16) {
+        const int lane = threadIdx.x & 31;
+        const int wpb = blockDim.x / 32;
+        for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
+            const uint16_t *src = x + (size_t)perm_tok[r] * d;
+            const int e = fp16_row_exponent(src, d, lane);
+            if (lane == 0) xexp[r] = e;
+            for (int c = lane; c < vec_per_row; c += 32)
+                reinterpret_cast<uint4 *>(xp + (size_t)r * d)[c] =
+                    bf16x8_to_fp16_scaled(__ldg(reinterpret_cast<const uint4 *>(src) + c), e);
+        }
+        return;
+    }
     const long long total = (long long)rows * vec_per_row;
     for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < total;
          v += (long long)gridDim.x * blockDim.x) {
         int r = (int)(v / vec_per_row), c = (int)(v - (long long)r * vec_per_row);
         int t = perm_tok[r];
         uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * d) + c);
-        if (to_fp16) {
-            uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                __half2 h = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
-                w[i] = *reinterpret_cast<uint32_t *>(&h);
-            }
-            u = make_uint4(w[0], w[1], w[2], w[3]);
-        }
         reinterpret_cast<uint4 *>(xp + (size_t)r * d)[c] = u;
     }
 }
@@ -204,14 +209,14 @@ cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, in
 }
 
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
-                               void *xp, int to_fp16, int num_sms, cudaStream_t stream)
+                               void *xp, int to_fp16, int32_t *xexp, int num_sms, cudaStream_t stream)
 {
     long long total = (long long)rows * (d / 8);
     long long want = (total + 255) / 256, cap = (long long)num_sms * 8;
     int blocks = (int)(want < cap ? want : cap);
     if (blocks < 1) blocks = 1;
     launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const uint16_t *>(x), d, perm_tok,
-                                                   rows, static_cast<uint16_t *>(xp), to_fp16);
+                                                   rows, static_cast<uint16_t *>(xp), to_fp16, xexp);
     return cudaGetLastError();
 }
 

@@ -307,7 +307,7 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
                int32_t *__restrict__ offsets, int32_t *__restrict__ perm_tok,
                int32_t *__restrict__ inv, float *__restrict__ perm_w,
                const uint16_t *__restrict__ x, int d, uint16_t *__restrict__ xp, int xp_fp16,
-               uint32_t *__restrict__ status)
+               int32_t *__restrict__ xexp, uint32_t *__restrict__ status)
 {
     pdl_enter();
     __shared__ int tot[kMaxExperts], pre[kMaxExperts], off[kMaxExperts + 1];
@@ -407,6 +407,16 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
             const uint4 *s1 = reinterpret_cast<const uint4 *>(x + (size_t)q1 * d);
             uint4 *d0 = reinterpret_cast<uint4 *>(xp + (size_t)(p0 < 0 ? 0 : p0) * d);
             uint4 *d1 = reinterpret_cast<uint4 *>(xp + (size_t)(p1 < 0 ? 0 : p1) * d);
+            // fp16 rows: each row scaled by 2^-e (see fp16_row_exponent), e kept per grouped row
+            int e0 = 0, e1 = 0;
+            if (xp_fp16) {
+                if (p0 >= 0) e0 = fp16_row_exponent(x + (size_t)q0 * d, d, lane);
+                if (p1 >= 0) e1 = fp16_row_exponent(x + (size_t)q1 * d, d, lane);
+                if (lane == 0) {
+                    if (p0 >= 0) xexp[p0] = e0;
+                    if (p1 >= 0) xexp[p1] = e1;
+                }
+            }
             constexpr int U = 4;   // 2 rows x 4 x 16 bytes per lane in flight
             for (int c0 = lane; c0 < vec; c0 += 32 * U) {
                 uint4 v[2][U];
@@ -426,15 +436,8 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ t
                         const int c = c0 + 32 * u;
                         if (c >= vec) continue;
                         uint4 w4 = v[r][u];
-                        if (xp_fp16) {   // bf16 -> fp16 rows for the fp16 (Q8_0) tensor-core path
-                            uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                __half2 hh = __floats2half2_rn(bf16lo(w[q]), bf16hi(w[q]));
-                                w[q] = *reinterpret_cast<uint32_t *>(&hh);
-                            }
-                            w4 = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        if (xp_fp16)   // bf16 -> fp16 rows for the fp16 (Q8_0) tensor-core path
+                            w4 = bf16x8_to_fp16_scaled(w4, r ? e1 : e0);
                         (r ? d1 : d0)[c] = w4;
                     }
                 }
@@ -463,7 +466,7 @@ cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cu
     launch_pdl(scatter_kernel, dim3(ntiles, parts), dim3(256), 0, stream,
         a.topk_idx, a.topk_w, a.rank, a.tile_cnt, ntiles, tile_tokens, a.T, a.k, a.E, a.counts,
         a.offsets, a.perm_tok, a.inv, a.perm_w, static_cast<const uint16_t *>(a.x), a.d,
-        static_cast<uint16_t *>(a.xp), a.xp_fp16, a.status);
+        static_cast<uint16_t *>(a.xp), a.xp_fp16, a.xexp, a.status);
     return cudaGetLastError();
 }
 

@@ -11,7 +11,8 @@
 //   and writes h = SiLU(G) * U as 16-bit values, so G and U never reach HBM.
 // Kernel DOWN: C = H_e . W_d[e]^T over tiles of 128 rows x 256 model columns;
 //   the epilogue scales each row by its routing weight and adds it into
-//   out[token] (fp32; a plain store when k == 1).
+//   out[token] (fp32; a plain store when k == 1; with k > 2 it stores the row
+//   and a combine kernel adds each token's k rows in slot order).
 //
 // Per CTA (persistent, one per SM): warp 0 issues TMA loads of the A (rows)
 // and B (weights) tiles into a shared-memory ring (128-byte swizzle); warp 1
@@ -139,8 +140,11 @@ struct Params {
     const int32_t *perm_tok;  // DOWN epilogue
     const float *perm_w;
     float *out;
+    float *y;                 // DOWN, k > 2: [rows, d] weighted outputs per grouped row
     uint32_t *status;
     int h_fp16;               // GATEUP: write h as fp16 (else bf16)
+    const int32_t *xexp;      // fp16 rows (Q8_0): row r of the grouped x is scaled by 2^-xexp[r];
+                              // h is written scaled by 2^-2 xexp[r], undone in the down epilogue
     float *out_zero;          // GATEUP: `out` to zero for the down kernel's adds, or null
     long long zero4;          // float4 elements of out_zero
     uint32_t expire_ns;       // > 0: the producer's first wait gives up after this long (test hook)
@@ -518,6 +522,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 constexpr int HC = BN / 4;
                 uint16_t *hrow = p.h + (size_t)grow * p.F + nt * (BN / 2) + chalf * HC;
                 const uint32_t tg = tbase + chalf * HC, tu = tg + BN / 2;
+                // fp16 rows (Q8_0): the accumulators are G / s and U / s for this
+                // row's scale s; h / s^2 = (G/s) * sigmoid(G) * (U/s) is what fp16
+                // holds (its magnitude is bounded by the weights, whatever x is)
+                const float sx = (p.xexp && valid) ? ldexpf(1.f, p.xexp[grow]) : 1.f;
+                bool out_of_range = false;
 #pragma unroll 1
                 for (int cc = 0; cc < HC; cc += 32) {
                     uint32_t g[2][16], u[2][16];
@@ -530,12 +539,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int hi = j >> 3, i0 = (2 * j) & 15;
-                        const float h0 = silu_f(__uint_as_float(g[hi][i0])) * __uint_as_float(u[hi][i0]);
-                        const float h1 = silu_f(__uint_as_float(g[hi][i0 + 1])) * __uint_as_float(u[hi][i0 + 1]);
+                        const float g0 = __uint_as_float(g[hi][i0]), g1 = __uint_as_float(g[hi][i0 + 1]);
+                        const float u0 = __uint_as_float(u[hi][i0]), u1 = __uint_as_float(u[hi][i0 + 1]);
                         if (p.h_fp16) {
+                            const float h0 = __fdividef(g0 * u0, 1.0f + __expf(-sx * g0));
+                            const float h1 = __fdividef(g1 * u1, 1.0f + __expf(-sx * g1));
+                            out_of_range |= !(fabsf(h0) <= 65504.f) || !(fabsf(h1) <= 65504.f);
                             __half2 v = __floats2half2_rn(h0, h1);
                             packed[j] = *reinterpret_cast<uint32_t *>(&v);
                         } else {
+                            const float h0 = silu_f(g0) * u0, h1 = silu_f(g1) * u1;
                             __nv_bfloat162 v = __floats2bfloat162_rn(h0, h1);
                             packed[j] = *reinterpret_cast<uint32_t *>(&v);
                         }
@@ -548,10 +561,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                                                 packed[4 * q + 3]);
                     }
                 }
+                // an h beyond fp16's range (weights too large for it) is not silent
+                if (__any_sync(0xffffffffu, out_of_range && valid) && lane == 0)
+                    flag_status(p.status, kDevCheckFailed);
             } else {
                 int tok = 0;
                 float wgt = 0.f;
-                if (valid) { tok = p.perm_tok[grow]; wgt = p.perm_w[grow]; }
+                if (valid) {
+                    tok = p.perm_tok[grow];
+                    wgt = p.perm_w[grow];
+                    // fp16 rows (Q8_0): h was held as h / s^2
+                    if (p.xexp) wgt *= ldexpf(1.f, 2 * p.xexp[grow]);
+                }
                 // this warp: output columns [chalf*128, chalf*128 + 128) of its 32
                 // rows, in chunks of 16 columns.  A chunk is transposed through
                 // shared memory so that each store / reduction instruction of the
@@ -559,7 +580,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 // columns 4(l%4)..+3) instead of 32 rows x 16 bytes.
                 float *stg = reinterpret_cast<float *>(smem + C::CTL + sizeof(SmemCtl)) +
                              (warp - 2) * 32 * kStgRow;
-                const float *obase = p.out + nt * BN + chalf * (BN / 2);
                 const uint32_t tv = tbase + chalf * (BN / 2);
 #pragma unroll 1
                 for (int cc = 0; cc < BN / 2; cc += 16) {
@@ -576,12 +596,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     for (int i = 0; i < 4; ++i) {
                         const int r = (lane >> 2) + 8 * i;          // row within the warp's 32
                         const int rt = __shfl_sync(0xffffffffu, tok, r);
+                        const int rg = __shfl_sync(0xffffffffu, grow, r);
                         const bool rv = __shfl_sync(0xffffffffu, valid ? 1 : 0, r) != 0;
                         const float4 val = *reinterpret_cast<const float4 *>(stg + r * kStgRow + (lane & 3) * 4);
                         if (rv) {
-                            float *o = const_cast<float *>(obase) + (size_t)rt * p.d + cc + (lane & 3) * 4;
-                            if (p.k == 1) *reinterpret_cast<float4 *>(o) = val;
-                            else red_add_v4(o, val.x, val.y, val.z, val.w);
+                            const size_t col = (size_t)(nt * BN + chalf * (BN / 2) + cc + (lane & 3) * 4);
+                            if (p.k > 2) {
+                                // the grouped row's weighted output; the combine kernel
+                                // adds each token's k rows in slot order
+                                *reinterpret_cast<float4 *>(p.y + (size_t)rg * p.d + col) = val;
+                            } else {
+                                // k = 1: the only contribution; k = 2: two additions
+                                // onto zero, whose result does not depend on their order
+                                float *o = p.out + (size_t)rt * p.d + col;
+                                if (p.k == 1) *reinterpret_cast<float4 *>(o) = val;
+                                else red_add_v4(o, val.x, val.y, val.z, val.w);
+                            }
                         }
                     }
                     __syncwarp();
@@ -778,8 +808,8 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
     else
         err = launch_pdl(grouped_gemm_kernel<DOWN, Q8, PAIR>, g2, block, smem, stream, m_h, m_wd, m_wd,
                          m_sd, m_sd, p);
-    if (err != cudaSuccess) return err;
-    return cudaGetLastError();
+    if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess || a.k <= 2) return err;
+    return launch_combine_rows(a.y, a.d, a.inv, a.T, a.k, a.out, a.status, a.num_sms, stream);
 }
 
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
@@ -790,7 +820,7 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     const int rows = a.T * a.k;
     cudaError_t err = cudaSuccess;
     if (!a.xp_ready &&
-        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, q8 ? 1 : 0, a.num_sms, stream)) !=
+        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, q8 ? 1 : 0, a.xexp, a.num_sms, stream)) !=
             cudaSuccess)
         return err;
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
@@ -837,7 +867,8 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k;
     p.h = static_cast<uint16_t *>(a.h); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
-    p.out = a.out; p.status = a.status; p.h_fp16 = q8 ? 1 : 0;
+    p.out = a.out; p.y = a.y; p.status = a.status; p.h_fp16 = q8 ? 1 : 0;
+    p.xexp = q8 ? a.xexp : nullptr;
     p.out_zero = a.zero_out ? a.out : nullptr;
     p.zero4 = (long long)a.T * a.d / 4;
     p.expire_ns = a.expire_ns;

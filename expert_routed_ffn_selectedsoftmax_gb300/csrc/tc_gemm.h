@@ -18,9 +18,12 @@ struct TcArgs {
     const int32_t *perm_tok;    // [T*k]
     const float *perm_w;        // [T*k]
     void *xp;                   // [T*k, d] 16-bit scratch (grouped rows)
+    int32_t *xexp;              // [T*k] Q8_0: fp16 row r of xp is x * 2^-xexp[r]
     int xp_ready;               // xp already holds the grouped rows
     void *h;                    // [T*k, F] 16-bit scratch
     float *out;                 // [T, d] fp32
+    float *y;                   // k > 2: [T*k, d] weighted outputs per grouped row (then combined)
+    const int32_t *inv;         // [T*k] grouped row of each slot (k > 2)
     int zero_out;               // zero `out` in the gate/up kernel (the down kernel adds into it)
     uint32_t *status;           // device status word
     int num_sms;

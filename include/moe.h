@@ -157,6 +157,14 @@ MOE_API moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int
  * rows < 0).  moe_pack_q8_0 repacks `blocks` (device, any alignment) into
  * `packed` (device, 256-byte aligned) on `stream`; pack W_g and W_u as
  * rows = E*F, cols = d and W_d as rows = E*d, cols = F.
+ * Range: the Q8_0 grouped GEMMs (MOE_PATH_PREFILL) multiply fp16 operands.
+ * Each token row enters them scaled by an exact power of two so that its
+ * largest magnitude is at most 1, and h is held scaled by the square of that
+ * factor; both are undone exactly in the epilogues, so any finite bf16
+ * activations are taken.  An h that still leaves fp16's range (|h| > 65504
+ * after the scaling: expert weights with dot products above ~256 against a
+ * unit row) makes moe_check report MOE_ERR_DEVICE_CHECK.  The CUDA-core Q8_0
+ * decode kernels compute in fp32.
  */
 MOE_API size_t moe_q8_0_packed_size(long long rows, int cols);
 MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
@@ -227,12 +235,12 @@ MOE_API moe_status moe_workspace_views(int T, int d, int E, int k, int F, moe_dt
  *   path: a moe_path value.  MOE_PATH_PREFILL needs bf16 activations,
  *   bf16 or Q8_0 weights, d % 256 == 0 and F % 128 == 0, and returns
  *   MOE_ERR_UNSUPPORTED otherwise.
- *   Reproducibility: with k <= 2 every path gives bitwise identical results
- *   from run to run, and so do the tensor-core decode kernels (bf16 weights,
- *   d and F multiples of 128, T*k <= 8192) for every k.  With k > 2 the
- *   CUDA-core decode kernels and the prefill GEMMs add each token's k expert
- *   outputs into out with fp32 atomics in arrival order, so the last bits can
- *   differ between runs.
+ *   Reproducibility: every path gives bitwise identical results from run to
+ *   run, for every k, and permuting the tokens permutes the output rows bit
+ *   for bit: sums of split-K partials are added in split order, k = 2 outputs
+ *   are two additions onto zero (whose result does not depend on their
+ *   order), and with k > 2 each token's k expert outputs are added in slot
+ *   order by a combine kernel.
  */
 MOE_API moe_status moe_forward(const void *x, moe_dtype act_dt, int T, int d, const void *w_router,
                        const float *sel_bias, int E, int k, const void *w_gate,

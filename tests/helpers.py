@@ -99,15 +99,16 @@ def assert_near_tie_sets_valid(scores, idx_gpu, idx_ref, margin, k):
     return diff
 
 
-def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, margin, k, mode=0, logits=None, bias=None):
-    """Indices exact where the margin is safe; weights close there.  With the
-    oracle's logits (and the bias), tokens under the margin whose set differs
-    are checked too: a valid resolution of the tie, weighted as the scoring
-    mode weighs that set."""
+def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, margin, k, mode=0, logits=None, bias=None,
+                    w_atol=2e-6):
+    """Indices exact where the margin is safe; weights close there (w_atol).
+    With the oracle's logits (and the bias), tokens under the margin whose set
+    differs are checked too: a valid resolution of the tie, weighted as the
+    scoring mode weighs that set."""
     ok = margin >= MARGIN
     assert np.array_equal(idx_gpu[ok], idx_ref[ok]), \
         f"{int((idx_gpu[ok] != idx_ref[ok]).any(1).sum())} tokens routed differently"
-    np.testing.assert_allclose(w_gpu[ok], w_ref[ok], rtol=0, atol=2e-6)
+    np.testing.assert_allclose(w_gpu[ok], w_ref[ok], rtol=0, atol=w_atol)
     if k == 1 and mode == 0:
         assert np.all(w_gpu == 1.0)
     if logits is not None:
@@ -115,9 +116,9 @@ def compare_routing(idx_gpu, w_gpu, idx_ref, w_ref, margin, k, mode=0, logits=No
         diff = assert_near_tie_sets_valid(scores, idx_gpu, idx_ref, margin, k)
         if len(diff):
             w_set = weights_of_set(logits[diff], idx_gpu[diff], mode)
-            np.testing.assert_allclose(w_gpu[diff], w_set, rtol=0, atol=2e-6)
+            np.testing.assert_allclose(w_gpu[diff], w_set, rtol=0, atol=w_atol)
         same = ~ok & ~(idx_gpu != idx_ref).any(1)
-        np.testing.assert_allclose(w_gpu[same], w_ref[same], rtol=0, atol=2e-6)
+        np.testing.assert_allclose(w_gpu[same], w_ref[same], rtol=0, atol=w_atol)
     return ok
 
 
@@ -168,7 +169,7 @@ def gpu_forward_views(layer, dev, path=0, t=None, scoring=0, out=None):
     return o.cpu().numpy(), {n: v.cpu().numpy() for n, v in r.items()}
 
 
-def check_routing_views(r, layer, mode=0, logits=None):
+def check_routing_views(r, layer, mode=0, logits=None, w_atol=2e-6):
     """The routing and grouping a layer call wrote, against the oracle:
     indices exact beyond the margin (near ties: a valid resolution), weights
     within 2e-6, counts / offsets / perm_tok / inv bit-exact against the
@@ -181,7 +182,7 @@ def check_routing_views(r, layer, mode=0, logits=None):
     idx_ref, w_ref, margin = oracle.route_scored(logits, layer.bias, layer.k, mode)
     idx = r["topk_idx"]
     compare_routing(idx, r["topk_w"], idx_ref, w_ref, margin, layer.k, mode, logits=logits,
-                    bias=layer.bias)
+                    bias=layer.bias, w_atol=w_atol)
     c, o, p, i = oracle.permute(idx, layer.E)
     assert np.array_equal(r["counts"], c), "counts differ from the grouping of the call's routing"
     assert np.array_equal(r["offsets"], o), "offsets differ"

@@ -447,3 +447,93 @@ def test_ffn_dense_matches_oracle(act, wdt, T, path):
     assert np.array_equal(r["perm_tok"], np.arange(T)) and np.array_equal(r["inv"], np.arange(T))
     ref, idx_ref, _, margin = oracle.moe_forward(layer)
     check_output(out, layer, ref, idx_ref, margin)
+
+
+# ------------------------------------------------ k > 2: reproducible everywhere
+@pytest.mark.parametrize("k", [4, 8])
+@pytest.mark.parametrize("path,T,act,wdt", [
+    (DECODE, 64, wl.BF16, wl.BF16),     # tensor-core decode kernels (split-K + combine)
+    (SIMT, 64, wl.BF16, wl.BF16),       # CUDA-core decode kernels
+    (SIMT, 40, wl.F32, wl.F32),
+    (SIMT, 40, wl.BF16, wl.Q8_0),
+    (PREFILL, 600, wl.BF16, wl.BF16),   # grouped GEMMs
+    (PREFILL, 600, wl.BF16, wl.Q8_0),
+])
+def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
+    """With k > 2 every path adds a token's k expert outputs in slot order (no
+    atomics): two runs give the same bits, permuting the tokens permutes the
+    output rows bit for bit, and the result matches the oracle."""
+    layer = wl.make_custom_layer(26, T=T, d=256, E=16, k=k, F=128, act_dtype=act, w_dtype=wdt,
+                                 bias_sd=0.5)
+    t = upload_layer(layer, DEV)
+    a, r = gpu_forward_views(layer, DEV, path=path, t=t)
+    b, _ = gpu_forward_views(layer, DEV, path=path, t=t)
+    assert np.array_equal(a, b)
+    perm = np.random.default_rng(3).permutation(layer.T)
+    t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
+    c = gpu_forward(layer, DEV, path=path, t=t2).cpu().numpy()
+    assert np.array_equal(c, a[perm])
+    check_routing_views(r, layer)
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    check_output(a, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
+
+
+# ------------------------------------------- fp16 operands of the Q8_0 GEMMs
+@pytest.mark.parametrize("path,T", [(PREFILL, 300), (SIMT, 40), (0, 600)])
+def test_q8_0_large_activations(path, T):
+    """The Q8_0 grouped GEMMs multiply fp16 operands.  Token rows whose
+    magnitudes span 1e-2 .. 1e5 (h far beyond fp16's 65504 for the large
+    ones) match the oracle: each fp16 row is the bf16 row times an exact power
+    of two, undone exactly in the epilogues."""
+    layer = wl.make_custom_layer(27, T=T, d=256, E=8, k=2, F=256, act_dtype=wl.BF16,
+                                 w_dtype=wl.Q8_0, bias_sd=0.3)
+    mag = 10.0 ** np.random.default_rng(5).uniform(-2, 5, size=T)
+    mag[:4] = [1e5, 2e-2, 1.0, 7e4]
+    x = wl.bf16_bits_to_f32(layer.x) * mag[:, None].astype(np.float32)
+    layer.x = wl.f32_to_bf16_bits(x)
+    out, r = gpu_forward_views(layer, DEV, path=path)
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    assert np.abs(ref).max() > 65504.0 ** 2 * 1e-3     # h and out far beyond fp16's range
+    # logits of 1e5-magnitude rows carry the router's fp32 accumulation error
+    # (~1e-7 of |logit| ~ 1e4): their weights agree to ~1e-5, not 2e-6
+    check_routing_views(r, layer, w_atol=5e-5)
+    # per row: the large rows dominate any global RMS, so each row is held to
+    # the tolerance of its own magnitude
+    for rows in (mag >= 1e3, (mag >= 1) & (mag < 1e3), mag < 1):
+        if rows.any():
+            sub_rows = np.where(rows)[0]
+            from helpers import sub_layer
+            sub = sub_layer(layer, sub_rows)
+            check_output(out[sub_rows], sub, ref[sub_rows], idx_ref[sub_rows], margin[sub_rows],
+                         idx_gpu=r["topk_idx"][sub_rows])
+
+
+def test_q8_0_h_beyond_fp16_is_reported():
+    """Expert weights large enough that h leaves fp16's range even for
+    normalised rows: the call reports MOE_ERR_DEVICE_CHECK instead of
+    returning infinities silently."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    T, d, E, k, F = 256, 256, 4, 1, 128
+    layer = wl.make_custom_layer(28, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
+                                 w_dtype=wl.BF16)
+    rng = np.random.default_rng(6)
+    big = lambda *s: (rng.standard_normal(s) * 4e3).astype(np.float32)
+    layer.w_dtype = wl.Q8_0
+    layer.w_gate = wl.q8_0_quantize(big(E, F, d))
+    layer.w_up = wl.q8_0_quantize(big(E, F, d))
+    layer.w_down = wl.q8_0_quantize(big(E, d, F) * 1e-3)
+    t = upload_layer(layer, DEV)
+    ws = torch.empty(pkg.moe_workspace_size(T, d, E, k, F, 1, wl.Q8_0), dtype=torch.uint8,
+                     device=DEV)
+    gpu_forward(layer, DEV, path=PREFILL, t=t, workspace=ws)
+    torch.cuda.synchronize()
+    word = ctypes_check(pkg, ws)
+    assert word == 6, word            # MOE_ERR_DEVICE_CHECK
+
+
+def ctypes_check(pkg, ws):
+    import ctypes
+    L = pkg.load_library()
+    w = ctypes.c_uint32(0)
+    return L.moe_check(ctypes.c_void_p(ws.data_ptr()), ctypes.byref(w),
+                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
