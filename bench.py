@@ -204,8 +204,9 @@ def expert_kernel_names(w, T, num_sms):
     """Which kernels moe_forward's AUTO path runs for this workload (mirrors
     the library's selection: grouped GEMMs from 64 rows per expert on average
     and T >= 512 for bf16 / Q8_0 weights with d % 256 == 0 and F % 128 == 0;
-    tensor-core decode for bf16 layers with d, F multiples of 128 and
-    T*k <= 8192 -- one clustered routing+grouping kernel for T <= 128, then
+    tensor-core decode for bf16 and affine 4-bit layers with d, F multiples of
+    128 and T*k <= 8192 -- one clustered routing+grouping kernel for T <= 128
+    (4-bit: plus the kernel that writes the grouped fp16 rows), then for bf16
     one persistent kernel for gate/up, SwiGLU, down and the combine when k <= 2
     and the batch has half a wave of whole-K gate/up items of at most 512 KB,
     else the gate/up and down kernels with their split-K reductions; otherwise
@@ -219,20 +220,23 @@ def expert_kernel_names(w, T, num_sms):
         q = "Q8_0, CTA pairs" if w.w_dtype == 2 else "bf16"
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4, "fused": False}
-    if act16 and w.w_dtype == 1 and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
+    if act16 and w.w_dtype in (1, 3) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
         n_exp = min(w.E, rows)
         small = T <= 128 and w.d // 64 <= 64 and w.k <= w.E
-        if w.k <= 2 and n_exp * (w.F // 128) * 2 >= 2 * num_sms and 2 * 128 * w.d * 2 <= 512 << 10:
+        q4 = w.w_dtype == 3
+        if (not q4 and w.k <= 2 and n_exp * (w.F // 128) * 2 >= 2 * num_sms
+                and 2 * 128 * w.d * 2 <= 512 << 10):
             name = "decode_fused_kernel (gate/up + SwiGLU + down + combine, one launch)"
             return {"file": "decode_fused.cu", "gateup": name, "down": name, "fused": True,
                     "launches": (1 if small else 2) + 1}
         fused = 192 <= n_exp * (w.F // 128) <= 2 * num_sms
         direct = w.k <= 2 and n_exp * (w.d // 128) >= 192
-        launches = (1 if small else 2) + (1 if fused else 2) + (1 if direct else 2)
-        gu = "decode_tc_kernel<GATEUP> (whole K, writes h)" if fused else \
-            "decode_tc_kernel<GATEUP> + swiglu_reduce_kernel"
-        dn = "decode_tc_kernel<DOWN> (whole K, adds into out)" if direct else \
-            "decode_tc_kernel<DOWN> + combine_kernel"
+        launches = (1 if small and not q4 else 2) + (1 if fused else 2) + (1 if direct else 2)
+        tag = ", 4-bit" if q4 else ""
+        gu = f"decode_tc_kernel<GATEUP{tag}> (whole K, writes h)" if fused else \
+            f"decode_tc_kernel<GATEUP{tag}> + swiglu_reduce_kernel"
+        dn = f"decode_tc_kernel<DOWN{tag}> (whole K, adds into out)" if direct else \
+            f"decode_tc_kernel<DOWN{tag}> + combine_kernel"
         return {"file": "decode_tc.cu", "gateup": gu, "down": dn, "launches": launches,
                 "fused": False}
     return {"file": "decode.cu", "gateup": "decode_gateup_kernel", "down": "decode_down_kernel",
@@ -429,14 +433,16 @@ def scoring_mode(args):
     return {"selected_softmax": 0, "softmax": 1, "sigmoid": 2}[args.scoring]
 
 
-def compute_peak(w, peaks, dev_props):
+def compute_peak(w, peaks, dev_props, kernels=None):
     """The compute roofline of a workload's expert arithmetic: the measured
-    dense bf16 tensor peak for bf16 weights and for Q8_0 (fp16 operands, the
-    same dense rate); for fp32 and affine 4-bit weights, which run as fp32 FMAs
-    on the CUDA cores, 128 FMA lanes x 2 flops per SM per clock at the
-    device's maximum SM clock ("alu")."""
+    dense bf16 tensor peak for bf16 weights and for Q8_0 and affine 4-bit
+    weights on the tensor-core kernels (fp16 operands, the same dense rate);
+    for fp32 weights and 4-bit weights on the CUDA-core kernels, which run as
+    fp32 FMAs, 128 FMA lanes x 2 flops per SM per clock at the device's
+    maximum SM clock ("alu")."""
     from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
-    if w.w_dtype in (wl.F32, wl.Q4_A64):
+    simt = kernels is None or kernels["file"] == "decode.cu"
+    if w.w_dtype == wl.F32 or (w.w_dtype == wl.Q4_A64 and simt):
         mhz = float(peaks.get("sm_max_mhz") or 0) or dev_props.clock_rate / 1e3
         return dev_props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12, "alu", \
             "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock"
@@ -579,7 +585,7 @@ def roofline_of(w, T, layers, alg, stage_us, names, peaks, peak_src, dev_props, 
     down by live stage events): its algorithmic bytes (or flops, past the
     ridge) per launch over its measured duration."""
     hbm = peak_value(peaks, "hbm_gbs")
-    cpeak, cbound, csrc = compute_peak(w, peaks, dev_props)
+    cpeak, cbound, csrc = compute_peak(w, peaks, dev_props, names)
     if names.get("fused"):
         # one kernel streams both GEMMs' weights: its stage is the gate/up one
         dominant, dom_us = "fused", stage_us[3]
@@ -607,9 +613,9 @@ def roofline_of(w, T, layers, alg, stage_us, names, peaks, peak_src, dev_props, 
             "flops_per_launch": dom_flops, "us_per_launch": dom_us}
 
 
-def layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us):
+def layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us, names=None):
     hbm = peak_value(peaks, "hbm_gbs")
-    cpeak, cbound, _ = compute_peak(w, peaks, dev_props)
+    cpeak, cbound, _ = compute_peak(w, peaks, dev_props, names)
     gbs = alg["bytes"] / (ms_per_step * 1e-3) / 1e9
     return {"us_per_layer": ms_per_step * 1e3 / layers, "algorithmic_GBps": gbs,
             "TFLOPS": alg["flops"] / (ms_per_step * 1e-3) / 1e12, "frac_hbm": gbs / hbm,
@@ -656,7 +662,7 @@ def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, pea
     res = {"workload": name, "T": T, "d": w.d, "E": w.E, "k": w.k, "F": w.F,
            "w_dtype": wl.DTYPE_NAMES[w.w_dtype], "layers": layers, "steps": steps,
            "ms_per_step": ms, "tokens_per_s": T * layers / (ms * 1e-3),
-           "layer": layer_stats(w, alg, ms, layers, peaks, dev_props, stage),
+           "layer": layer_stats(w, alg, ms, layers, peaks, dev_props, stage, names),
            "roofline": roofline_of(w, T, layers, alg, stage, names, peaks, peak_src, dev_props),
            "gpu_launches_per_layer": names["launches"]}
     if with_oracle:
@@ -918,13 +924,14 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands",
-                  wl.Q4_A64: "affine 4-bit weights, f32 CUDA-core arithmetic"}[w.w_dtype],
+                  wl.Q4_A64: ("affine 4-bit weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
+                              else "affine 4-bit weights, f16 tensor-core operands")}[w.w_dtype],
         "data": "synthetic", "config": config_dict(w, T, layers, args),
         "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s", "mode": e2e_mode, **e2e_alt,
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": names["launches"] * layers * args.steps,
         "roofline": roofline, "cpu_baseline": cpu, "step_ms": step_dist,
-        "layer": layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us),
+        "layer": layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us, names),
         "workloads": side,
     }
     if rank == 0:

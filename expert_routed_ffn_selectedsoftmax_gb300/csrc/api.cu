@@ -78,15 +78,17 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.tile_cnt = take(4 * (size_t)(T > 0 ? T : 1) * (size_t)E);   // <= one tile per token
     L.h = take(4 * n * (size_t)F);            // fp32 (decode); prefill uses 2 bytes/element
     // the decode_tc_capable() shape/dtype conditions, without the driver query
-    L.dtc = act_dt == MOE_BF16 && w_dt == MOE_BF16 && d % 128 == 0 && F % 128 == 0 &&
-            n <= (size_t)kDecodeTcMaxRows;
+    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q4_A64) && d % 128 == 0 &&
+            F % 128 == 0 && n <= (size_t)kDecodeTcMaxRows;
     L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
     L.pgu = L.pd = L.flags = off;
     // k > 2: weighted expert outputs per grouped row, combined in slot order
     // (the CUDA-core decode kernels and the grouped GEMMs)
     L.y = k > 2 ? take(4 * n * (size_t)d) : off;
-    // Q8_0 grouped GEMMs: exponent of each fp16 grouped row's scale
-    L.xexp = (prefill_capable(act_dt, w_dt, d, F) && w_dt == MOE_Q8_0) ? take(4 * n) : off;
+    // Q8_0 grouped GEMMs and 4-bit tensor-core decode: exponent of each fp16
+    // grouped row's scale
+    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt == MOE_Q8_0) || (L.dtc && w_dt == MOE_Q4_A64))
+                 ? take(4 * n) : off;
     L.n_flags = 0;
     if (L.dtc) {
         int ks_gu = 1, ks_d = 1;
@@ -251,7 +253,7 @@ moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *pac
 size_t moe_q4_a64_packed_size(long long rows, int cols)
 {
     if (rows < 0 || cols <= 0 || cols % 64) return 0;
-    return q4_a64_bias_offset(rows, cols) + (size_t)rows * (cols / 64) * 2;
+    return q4_a64_packed_bytes(rows, cols);
 }
 
 moe_status moe_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
@@ -387,7 +389,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     const int num_sms = device_sm_count();
     // bf16 decode batches with enough (expert, tile) units: gate/up, down and
     // combine in one persistent kernel
-    const bool use_fused = use_dtc && decode_fused_fits(T, d, E, k, F, num_sms);
+    const bool use_fused = use_dtc && w_dt == MOE_BF16 && decode_fused_fits(T, d, E, k, F, num_sms);
     // the expert kernels that accumulate into `out` need it zeroed first (the
     // fused kernel adds into it for k = 2 and stores for k = 1; the other
     // tensor-core decode kernels add into it only when their down kernel does)
@@ -408,7 +410,9 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // groups (no scatter); the tensor-core decode kernel gathers x rows itself
     const bool fused_small = !dense && use_dtc && route_small_capable(act_dt, T, d, E, k);
     ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && !fused_small) ? ws + L.xp : nullptr;
-    ra.xp_fp16 = w_dt == MOE_Q8_0;   // the Q8_0 grouped GEMMs take fp16 rows (scaled)
+    // the Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels take fp16
+    // rows (scaled)
+    ra.xp_fp16 = w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64;
     ra.xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     // the fused decode kernel's flags and ticket start at zero
@@ -435,14 +439,14 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     ra.ev_routed = ev[1];
     bool xp_ready = ra.xp != nullptr;
     // grouped 16-bit rows for the tensor-core kernels: a dense layer's are x
-    // itself unless the Q8_0 GEMMs need them converted to fp16
+    // itself unless the Q8_0 GEMMs or the 4-bit decode kernels need fp16 rows
     void *xp_rows = ws + L.xp;
     cudaError_t e;
     if (dense) {
         e = launch_identity_grouping(T, topk_idx, topk_w, counts, offsets, perm_tok, inv, perm_w,
                                      status, ra.zero_words, ra.n_zero, device_sm_count(), s);
         if (e != cudaSuccess || mark(1) != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
-        const bool in_place = act16 && w_dt != MOE_Q8_0;
+        const bool in_place = act16 && w_dt == MOE_BF16;   // Q8_0 / 4-bit: fp16 rows
         if (in_place) xp_rows = const_cast<void *>(x);
         xp_ready = in_place;
     } else if (fused_small) {
@@ -485,6 +489,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         e = launch_decode_fused(a, s);
     } else if (use_dtc) {
         DecodeTcArgs a{};
+        a.w_dt = w_dt;
         a.x = x; a.T = T; a.d = d; a.E = E; a.k = k; a.F = F;
         a.w_gate = w_gate; a.w_up = w_up; a.w_down = w_down;
         a.offsets = offsets; a.inv = inv; a.topk_w = topk_w; a.xp = xp_rows;
@@ -494,10 +499,13 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.expire_ns = x_dtc;
         a.perm_tok = perm_tok;
         a.perm_w = perm_w;
-        if (fused_small) {
-            a.x_gather = x;
+        int32_t *xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
+        a.xexp = xexp;
+        const int q4 = w_dt == MOE_Q4_A64;
+        if (fused_small && !q4) {
+            a.x_gather = x;   // (the 4-bit kernels take fp16 token rows by TMA from xp)
         } else if (!xp_ready &&
-                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, 0, nullptr, num_sms, s) != cudaSuccess) {
+                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, q4, xexp, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;
         }
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;

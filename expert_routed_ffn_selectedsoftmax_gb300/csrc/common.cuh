@@ -134,20 +134,30 @@ template <> struct WView<Q8Tag> {
 // Affine 4-bit view: q points at the code plane [rows, cols/2] (value 2j in the
 // low nibble of byte j); fp16 scale and bias planes [cols/64, rows].  Set by
 // the host.
+// Packed affine 4-bit weights (moe_pack_q4_a64) are tiles of 128 rows x 64
+// columns (one group), 4608 bytes each, in row-tile-major order: tile (rt, g)
+// at ((rt * groups) + g) * 4608; inside, the 128 rows' 32 code bytes (value
+// 2j in the low nibble of byte j), then the 128 fp16 scales, then the 128
+// fp16 biases.  A k-block of one row tile is one contiguous copy.
+constexpr int kQ4TileRows = 128, kQ4TileBytes = 4608, kQ4ScaleOff = 4096, kQ4BiasOff = 4352;
+__host__ __device__ __forceinline__ size_t q4_tile_offset(long long row, int g, int groups)
+{
+    return ((size_t)(row / kQ4TileRows) * (size_t)groups + (size_t)g) * kQ4TileBytes;
+}
+
 template <> struct WView<Q4Tag> {
-    const uint8_t *q;
-    const __half *scales, *biases;
-    size_t cols;
-    size_t rows;
+    const uint8_t *q;     // packed tiles
+    int groups;           // cols / 64
     __device__ __forceinline__ void load(size_t row, int col, RawW<Q4Tag> &r) const
     {
+        const uint8_t *t = q + q4_tile_offset((long long)row, col / 64, groups);
+        const int rr = (int)(row % kQ4TileRows);
         uint32_t v;
         asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
-                     : "=r"(v) : "l"(q + (row * cols + col) / 2));
+                     : "=r"(v) : "l"(t + rr * 32 + (col % 64) / 2));
         r.q = v;
-        const size_t g = (size_t)(col / 64) * rows + row;
-        r.s = __half2float(scales[g]);
-        r.b = __half2float(biases[g]);
+        r.s = __half2float(reinterpret_cast<const __half *>(t + kQ4ScaleOff)[rr]);
+        r.b = __half2float(reinterpret_cast<const __half *>(t + kQ4BiasOff)[rr]);
     }
     __device__ __forceinline__ static void cvt(const RawW<Q4Tag> &r, Chunk8 &c)
     {

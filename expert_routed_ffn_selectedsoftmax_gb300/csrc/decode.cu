@@ -345,15 +345,12 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
         return launch_t<__nv_bfloat16, __nv_bfloat16>(a, wg, wu, wd, stream);
     }
     if (a.w_dt == MOE_Q4_A64) {
-        // affine 4-bit packed planes: codes, fp16 scales, fp16 biases
+        // affine 4-bit packed tiles of 128 rows x 64 columns
         auto view4 = [](const void *p, long long rows, int cols) {
+            (void)rows;
             WView<Q4Tag> v;
-            const char *b = static_cast<const char *>(p);
-            v.q = reinterpret_cast<const uint8_t *>(b);
-            v.scales = reinterpret_cast<const __half *>(b + q4_a64_scale_offset(rows, cols));
-            v.biases = reinterpret_cast<const __half *>(b + q4_a64_bias_offset(rows, cols));
-            v.cols = (size_t)cols;
-            v.rows = (size_t)rows;
+            v.q = static_cast<const uint8_t *>(p);
+            v.groups = cols / 64;
             return v;
         };
         return launch_t<__nv_bfloat16, Q4Tag>(a, view4(a.w_gate, (long long)a.E * a.F, a.d),

@@ -403,9 +403,10 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
                 const uint32_t a0 = smem_u32(smem + s * SLOT);
                 const uint32_t b0 = a0 + A_BYTES;
                 const bool first = kb == it.kb0;   // first k-block of this accumulator
+                const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                    umma_f16(d_tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc,
                              (!first || kk > 0) ? 1u : 0u);
                 umma_commit(&c.empty[s]);
             }

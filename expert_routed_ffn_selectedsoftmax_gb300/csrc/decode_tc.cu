@@ -72,6 +72,39 @@ constexpr int SLOT = A_BYTES + B_BYTES;         // 20 KB per stage, 1024-aligned
 constexpr int KBMAX = 8;                        // k-blocks per item
 constexpr int THREADS = 192;
 constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
+// Affine 4-bit weights (W4): a stage holds the token tile (4 KB, first, for the
+// swizzle) and one packed weight tile (q4_tile_offset: the 128 x 64 codes,
+// 4 KB, then their fp16 scales and biases, 256 B each), fetched by a single
+// contiguous copy; four converter warps turn it into the 16 KB fp16 tile the MMA
+// reads and copy the token tile beside it, in one of NCVT4 converted buffers
+// after the ring, then release the ring stage themselves: the MMA issuer waits
+// on one barrier and commits one per k-block.  The MMAs then run
+// on fp16 operands: each weight is scale * q + bias rounded once to fp16
+// (relative error 2^-11, a quarter of a bf16 rounding), the token rows are
+// fp16 rows of x scaled by 2^-xexp[r] (exact for bf16 digits), and h is kept
+// in fp16 as h * 2^-2 xexp[r], undone in the down epilogue or the combine.
+#ifndef MOE_DTC_STAGES4
+#define MOE_DTC_STAGES4 7
+#endif
+#ifndef MOE_DTC_NCVT4
+#define MOE_DTC_NCVT4 2
+#endif
+constexpr int STAGES4 = MOE_DTC_STAGES4;
+constexpr int SLOT4 = 9216;                     // 4096 + 4608, 1024-aligned
+constexpr int CODE_OFF4 = 4096, SC_OFF4 = CODE_OFF4 + kQ4ScaleOff, BI_OFF4 = CODE_OFF4 + kQ4BiasOff;
+constexpr int W4_TX = kQ4TileBytes;             // weight bytes of a W4 stage
+static_assert(CODE_OFF4 + kQ4TileBytes <= SLOT4, "a W4 stage holds the token tile and one weight tile");
+constexpr int NCVT4 = MOE_DTC_NCVT4;
+constexpr int THREADS_W4 = 320;                 // + 4 converter warps
+constexpr int kStagesMax = STAGES4 > STAGES ? STAGES4 : STAGES;
+template <bool W4> struct Ring {
+    static constexpr int NST = W4 ? STAGES4 : STAGES;
+    static constexpr int SLOTB = W4 ? SLOT4 : SLOT;
+    static constexpr int B_OFF = W4 ? 0 : A_BYTES;      // token tile
+    static constexpr int CVT = W4 ? NST * SLOT4 : 0;    // converted buffers: weights, token tile
+    static constexpr int CVTB = A_BYTES + B_BYTES;
+    static constexpr int CTL = NST * SLOTB + (W4 ? NCVT4 * CVTB : 0);
+};
 constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
 constexpr int TMEM_COLS = 128;
 constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~1 item per CTA: 2 CTAs per SM on a 152-SM GB300
@@ -94,10 +127,14 @@ struct Params {
     const float *perm_w;
     int k;
     uint32_t expire_ns;  // > 0: the producer's first wait gives up after this long (test hook)
+    const int32_t *xexp; // W4: token row r holds x * 2^-xexp[r] (fp16); h is h * 2^-2 xexp[r]
+    const uint8_t *w4[2];  // W4: packed tiles of the matrix (GATEUP: gate, up; DOWN: down)
+    int groups;            // W4: K / 64, tiles per row tile
 };
 
 struct Ctl {
-    uint64_t full[STAGES], empty[STAGES], tfull[NACC], tempty[NACC], drain;
+    uint64_t full[kStagesMax], empty[kStagesMax], tfull[NACC], tempty[NACC], drain;
+    uint64_t cfull[NCVT4], cempty[NCVT4];   // W4: converted buffers
     uint64_t never;      // nothing arrives here (test hook)
     uint32_t tmem_base;
     int abort_flag;
@@ -150,32 +187,46 @@ __device__ __forceinline__ void stage_of(const Params &p, const Item &it, int kb
 // divide (relative error ~1e-6, below the bf16 rounding of h that follows).
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// The scaled SwiGLU of the fp16 (W4) path: with g = g' 2^e and u = u' 2^e,
+// h * 2^-2e = g' * sigmoid(g' 2^e) * u' -- no 2^-e factor that could overflow.
+__device__ __forceinline__ float swiglu_scaled(float g, float u, int e)
+{
+    return __fdividef(g, 1.0f + __expf(-ldexpf(g, e))) * u;
+}
+
 // tm_w0/tm_w1: weight matrices (box 64 x 128 rows); tm_b16/tm_b32: the token
 // rows (grouped x for GATEUP, h for DOWN) with boxes of 16 and 32 rows.
 // GATHER: the token rows are not loaded by TMA but gathered from x through
 // perm_tok by warps 6-9 (stage s by warp 6 + s % 4, lane = token row), written
 // into the 128-byte-swizzled layout the MMA expects.
-template <int MODE, bool GATHER>
-__global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, CTAS_PER_SM)
+// W4 (affine 4-bit weights): tm_w0/tm_w1 are unused; each stage's weight tile
+// is one contiguous copy from p.w4[m], converted to fp16 by warps 6-9.
+template <int MODE, bool GATHER, bool W4>
+__global__ void __launch_bounds__(GATHER || W4 ? THREADS_GATHER : THREADS, CTAS_PER_SM)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
                  const Params p)
 {
+    static_assert(!(GATHER && W4), "4-bit weights take the token rows by TMA");
+    using RG = Ring<W4>;
+    constexpr int STAGES = RG::NST, SLOT = RG::SLOTB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Ctl &c = *reinterpret_cast<Ctl *>(smem + STAGES * SLOT);
+    Ctl &c = *reinterpret_cast<Ctl *>(smem + RG::CTL);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
 
     // set-up that reads nothing the preceding kernels write (barriers, TMEM,
     // tensor-map prefetch) overlaps their tail under programmatic dependent launch
-    constexpr int NTHREADS = GATHER ? THREADS_GATHER : THREADS;
+    constexpr int NTHREADS = GATHER || W4 ? THREADS_GATHER : THREADS;
     if (threadIdx.x == 0) {
         // GATHER: a stage is full after the weight tile's bytes and the 32
         // arrivals of the warp that wrote its token rows
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], GATHER ? 33 : 1); mbar_init(&c.empty[s], 1); }
+        // W4: the four converter warps release a stage
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], GATHER ? 33 : 1); mbar_init(&c.empty[s], W4 ? 4 : 1); }
+        for (int b = 0; b < NCVT4; ++b) { mbar_init(&c.cfull[b], 4); mbar_init(&c.cempty[b], 1); }
         for (int b = 0; b < NACC; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
         mbar_init(&c.drain, 1);
         mbar_init(&c.never, 1);
@@ -183,8 +234,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
-        if (MODE == GATEUP)
+        if (!W4)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
+        if (MODE == GATEUP && !W4)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w1)) : "memory");
         if (!GATHER) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b16)) : "memory");
@@ -244,7 +296,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item(c, p, item);
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
-            const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
+            const uint32_t bytes = (W4 ? W4_TX : A_BYTES) + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
@@ -255,8 +307,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 stage_of(p, it, kbl, m, kb);
                 const CUtensorMap *wmap = (MODE == GATEUP && m == 1) ? &tm_w1 : &tm_w0;
                 const int kx = kb * BK;
-                tma_load_2d(smem + s * SLOT, wmap, &c.full[s], kx, wrow);
-                if (!GATHER) tma_load_2d(smem + s * SLOT + A_BYTES, bmap, &c.full[s], kx, it.row0);
+                uint8_t *st = smem + s * SLOT;
+                if (W4) {
+                    // the packed tile of (row tile, k-block): codes, scales, biases
+                    bulk_load(st + CODE_OFF4, p.w4[MODE == GATEUP ? m : 0] + q4_tile_offset(wrow, kb, p.groups),
+                              kQ4TileBytes, &c.full[s]);
+                } else {
+                    tma_load_2d(st, wmap, &c.full[s], kx, wrow);
+                }
+                if (!GATHER) tma_load_2d(st + RG::B_OFF, bmap, &c.full[s], kx, it.row0);
             }
         }
         if (!ok) {
@@ -279,23 +338,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             const uint32_t acc = li % nslot, aph = (li / nslot) & 1u;
             if (!mbar_wait(&c.tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t idesc = idesc_f16_mn(0, BM, it.nt);
+            const uint32_t idesc = idesc_f16_mn(W4 ? 1 : 0, BM, it.nt);
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
                 const uint32_t ph = (it_k / STAGES) & 1u;
-                if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
+                const int cb = it_k % NCVT4;
+                // W4: the converted buffer holds both operands
+                if (W4 ? !mbar_wait(&c.cfull[cb], (it_k / NCVT4) & 1u, abort_flag)
+                       : !mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 int m, kb;
                 stage_of(p, it, kbl, m, kb);
                 const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
-                const uint32_t a0 = smem_u32(smem + s * SLOT);
-                const uint32_t b0 = a0 + A_BYTES;
+                const uint32_t a0 = W4 ? smem_u32(smem + RG::CVT + cb * RG::CVTB) : smem_u32(smem + s * SLOT);
+                const uint32_t b0 = W4 ? a0 + A_BYTES : smem_u32(smem + s * SLOT + RG::B_OFF);
                 const int first = p.fused ? kb : kbl;   // first k-block of this accumulator
+                const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                    umma_f16(d_tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc,
                              (first | kk) != 0);
-                umma_commit(&c.empty[s]);
+                umma_commit(W4 ? &c.cempty[cb] : &c.empty[s]);
             }
             if (!ok) break;
             umma_commit(&c.tfull[acc]);
@@ -306,6 +369,70 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             umma_commit(&c.drain);
             volatile int no_abort = 0;
             mbar_wait(&c.drain, 0, &no_abort);
+        }
+    } else if (W4 && warp >= 6) {
+        // ------------------------------------------------ 4-bit converters (4 warps)
+        // warp 6 + w converts rows 32w .. 32w+31 of every stage's tile, lane = row:
+        // 64 codes -> scale * q + bias in fp16, in the 128-byte-swizzled layout.
+        // Byte j of a row holds q_2j (low nibble) and q_2j+1 (high nibble).  Placed
+        // in the low byte of both halves of a word under the fp16 exponent of
+        // 1024 (ulp 1), the low half keeps the low nibble (1024 + q_2j) and the
+        // high half the high one in bits 4-7 (1024 + 16 q_2j+1); one exact fma
+        // by (1, 1/16) and (-1024, -64) leaves (q_2j, q_2j+1), a second one
+        // gives scale * q + bias with a single rounding.
+        const int row = (warp - 6) * 32 + lane;
+        const __half2 unit = __halves2half2(__float2half_rn(1.0f), __float2half_rn(0.0625f));
+        const __half2 unbias = __halves2half2(__float2half_rn(-1024.0f), __float2half_rn(-64.0f));
+        uint32_t it_k = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item it = decode_item(c, p, item);
+            for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
+                const int s = it_k % STAGES, cb = it_k % NCVT4;
+                if (!__all_sync(0xffffffffu, mbar_wait(&c.full[s], (it_k / STAGES) & 1u, abort_flag)) ||
+                    !__all_sync(0xffffffffu, mbar_wait(&c.cempty[cb], ((it_k / NCVT4) & 1u) ^ 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *st = smem + s * SLOT;
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(st + CODE_OFF4 + row * 32);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(st + CODE_OFF4 + row * 32 + 16);
+                const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(st + SC_OFF4)[row]);
+                const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(st + BI_OFF4)[row]);
+                const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                uint8_t *const cvt = smem + RG::CVT + cb * RG::CVTB;
+                uint8_t *dst = cvt + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk ch: values 8ch .. 8ch+7
+                    uint32_t o[4];
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        // values 8ch+2pr, 8ch+2pr+1: the nibbles of byte pr
+                        const uint32_t t = (__byte_perm(w[ch], 0u, (uint32_t)(pr | (pr << 8))) & 0x00F0000Fu) |
+                                           0x64006400u;
+                        const __half2 q = __hfma2(*reinterpret_cast<const __half2 *>(&t), unit, unbias);
+                        const __half2 v = __hfma2(q, sc2, bi2);
+                        o[pr] = *reinterpret_cast<const uint32_t *>(&v);
+                    }
+                    *reinterpret_cast<uint4 *>(dst + ((ch ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                // the token tile (same offset mod 1024, so the same swizzle)
+                const int tid = (warp - 6) * 32 + lane;
+                const uint4 x0 = reinterpret_cast<const uint4 *>(st + RG::B_OFF)[tid];
+                const uint4 x1 = reinterpret_cast<const uint4 *>(st + RG::B_OFF)[tid + 128];
+                reinterpret_cast<uint4 *>(cvt + A_BYTES)[tid] = x0;
+                reinterpret_cast<uint4 *>(cvt + A_BYTES)[tid + 128] = x1;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&c.cfull[cb]);
+                    mbar_arrive(&c.empty[s]);   // the ring stage is read
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) flag_status(p.status, kDevTimeout);
+            c.abort_flag = 1;
         }
     } else if (GATHER && warp >= 6) {
         // ------------------------------------------------ token-row gatherers (4 warps)
@@ -332,7 +459,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         v[q] = has ? __ldg(reinterpret_cast<const uint4 *>(src + kx) + q) : make_uint4(0u, 0u, 0u, 0u);
-                    uint8_t *dst = smem + s * SLOT + A_BYTES + lane * 128;
+                    uint8_t *dst = smem + s * SLOT + RG::B_OFF + lane * 128;
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         *reinterpret_cast<uint4 *>(dst + ((q ^ (lane & 7)) << 4)) = v[q];
@@ -363,6 +490,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 // 16 token columns (the second only for 32-row chunks)
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 64;
                 uint16_t *dst = p.h + (size_t)it.row0 * p.R + wr;
+                // W4: lane j holds the scale exponent of token row j (fp16 h, scaled)
+                const int e_l = (W4 && lane < it.nrows) ? p.xexp[it.row0 + lane] : 0;
+                bool out_of_range = false;
                 for (int half = 0; half < it.nt / 16; ++half) {
                     uint32_t g[16], u[16];
                     tmem_ld16(taddr + half * 16, g);
@@ -371,12 +501,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int j = half * 16 + q;
-                        if (j < it.nrows) {
+                        if (W4) {
+                            const int ej = __shfl_sync(0xffffffffu, e_l, j);
+                            if (j < it.nrows) {
+                                const float hv = swiglu_scaled(__uint_as_float(g[q]), __uint_as_float(u[q]), ej);
+                                out_of_range |= !(fabsf(hv) <= 65504.f);
+                                dst[(size_t)j * p.R] = __half_as_ushort(__float2half_rn(hv));
+                            }
+                        } else if (j < it.nrows) {
                             const float hv = silu_f(__uint_as_float(g[q])) * __uint_as_float(u[q]);
                             dst[(size_t)j * p.R] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
                         }
                     }
                 }
+                if (W4 && out_of_range) flag_status(p.status, kDevCheckFailed);   // h beyond fp16
                 tc_fence_before();
                 mbar_arrive(&c.tempty[acc]);      // accumulators are read
                 continue;
@@ -391,7 +529,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             if (MODE == DOWN && p.direct) {
                 // token and routing weight of row j, held by lane j
                 const int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
-                const float w_l = lane < it.nrows ? p.perm_w[it.row0 + lane] : 0.f;
+                float w_l = lane < it.nrows ? p.perm_w[it.row0 + lane] : 0.f;
+                if (W4 && lane < it.nrows) w_l *= ldexpf(1.f, 2 * p.xexp[it.row0 + lane]);   // undo h's scale
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int tok = __shfl_sync(0xffffffffu, tok_l, j);
@@ -430,10 +569,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
 // holds, so results are deterministic and permutation-equivariant.
 constexpr int kSplitLanes = 8;
 
-// h[row, f] = SiLU(sum_s G[s][row][f]) * sum_s U[s][row][f], bf16
+// h[row, f] = SiLU(sum_s G[s][row][f]) * sum_s U[s][row][f], bf16; with xexp
+// (the fp16 rows of the 4-bit path) h * 2^-2 xexp[row] in fp16 instead
 __global__ void __launch_bounds__(32 * kSplitLanes)
 swiglu_reduce_kernel(const float *__restrict__ pgu, int KS, int rows, int F,
-                     uint16_t *__restrict__ h, const uint32_t *status)
+                     uint16_t *__restrict__ h, const int32_t *__restrict__ xexp, uint32_t *status)
 {
     pdl_enter();
     if (upstream_failed(status)) return;
@@ -463,20 +603,33 @@ swiglu_reduce_kernel(const float *__restrict__ pgu, int KS, int rows, int F,
                 g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
                 u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
             }
-            __nv_bfloat162 lo = __floats2bfloat162_rn(silu_f(g.x) * u.x, silu_f(g.y) * u.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(silu_f(g.z) * u.z, silu_f(g.w) * u.w);
-            uint2 packed = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            uint2 packed;
+            if (xexp) {
+                const int e = xexp[(size_t)i * 4 / F];
+                const float h0 = swiglu_scaled(g.x, u.x, e), h1 = swiglu_scaled(g.y, u.y, e);
+                const float h2 = swiglu_scaled(g.z, u.z, e), h3 = swiglu_scaled(g.w, u.w, e);
+                if (!(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3))) <= 65504.f))
+                    flag_status(status, kDevCheckFailed);   // h beyond fp16
+                __half2 lo = __floats2half2_rn(h0, h1), hi = __floats2half2_rn(h2, h3);
+                packed = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            } else {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(silu_f(g.x) * u.x, silu_f(g.y) * u.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+                packed = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            }
             *reinterpret_cast<uint2 *>(h + (size_t)i * 4) = packed;
         }
         __syncthreads();
     }
 }
 
-// out[t, :] = sum_j w[t, j] * sum_s Pd[s][inv[t, j]][:]   (fixed order: see above)
+// out[t, :] = sum_j w[t, j] * sum_s Pd[s][inv[t, j]][:]   (fixed order: see above);
+// with xexp each weight also carries 2^2 xexp[row] (the scaled fp16 h)
 __global__ void __launch_bounds__(32 * kSplitLanes)
 combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
                const int32_t *__restrict__ inv, const float *__restrict__ topk_w,
-               int T, int k, float *__restrict__ out, const uint32_t *status)
+               const int32_t *__restrict__ xexp, int T, int k, float *__restrict__ out,
+               const uint32_t *status)
 {
     pdl_enter();
     if (upstream_failed(status)) return;
@@ -508,7 +661,8 @@ combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
                     const float4 v = sy[w][j][lane];
                     y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
                 }
-                const float wt = topk_w[t * k + j];
+                float wt = topk_w[t * k + j];
+                if (xexp) wt *= ldexpf(1.f, 2 * xexp[inv[t * k + j]]);
                 acc.x += wt * y.x; acc.y += wt * y.y; acc.z += wt * y.z; acc.w += wt * y.w;
             }
             *reinterpret_cast<float4 *>(out + (size_t)t * d + o) = acc;
@@ -517,7 +671,7 @@ combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
     }
 }
 
-constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * SLOT + sizeof(Ctl); }
+template <bool W4> constexpr size_t smem_bytes() { return 1024 + (size_t)Ring<W4>::CTL + sizeof(Ctl); }
 
 int choose_splits(int kb_total, long long units)
 {
@@ -533,8 +687,8 @@ int choose_splits(int kb_total, long long units)
 
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E)
 {
-    return act_dt == MOE_BF16 && w_dt == MOE_BF16 && d % 128 == 0 && F % 128 == 0 &&
-           E <= kMaxExperts && tc_gemm_available();
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q4_A64) && d % 128 == 0 &&
+           F % 128 == 0 && E <= kMaxExperts && tc_gemm_available();
 }
 
 void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d)
@@ -571,37 +725,46 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     int ks_gu, ks_d;
     decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
 
+    const bool w4 = a.w_dt == MOE_Q4_A64;
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const bool gather = a.x_gather != nullptr;   // token rows gathered from x in-kernel
+    // token rows and h: fp16 on the 4-bit path
+    const CUtensorMapDataType rowt = w4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
+    const bool gather = a.x_gather != nullptr && !w4;   // token rows gathered from x in-kernel
     CUtensorMap m_wg, m_wu, m_wd, m_x16, m_x32, m_h16, m_h32;
-    if (!tc::make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BM, bf) ||
-        !tc::make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BM, bf) ||
-        !tc::make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BM, bf) ||
-        !tc::make_map(&m_h16, a.h, (uint64_t)rows, a.F, 16, bf) ||
-        !tc::make_map(&m_h32, a.h, (uint64_t)rows, a.F, 32, bf))
+    if (!tc::make_map(&m_h16, a.h, (uint64_t)rows, a.F, 16, rowt) ||
+        !tc::make_map(&m_h32, a.h, (uint64_t)rows, a.F, 32, rowt))
         return cudaErrorInvalidValue;
+    if (w4) {
+        m_wg = m_wu = m_wd = m_h16;   // unused: the 4-bit tiles are contiguous copies
+    } else if (!tc::make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BM, bf) ||
+               !tc::make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BM, bf) ||
+               !tc::make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BM, bf)) {
+        return cudaErrorInvalidValue;
+    }
     if (gather) {
         m_x16 = m_wg;   // unused by the gathering kernel
         m_x32 = m_wg;
-    } else if (!tc::make_map(&m_x16, a.xp, (uint64_t)rows, a.d, 16, bf) ||
-               !tc::make_map(&m_x32, a.xp, (uint64_t)rows, a.d, 32, bf)) {
+    } else if (!tc::make_map(&m_x16, a.xp, (uint64_t)rows, a.d, 16, rowt) ||
+               !tc::make_map(&m_x32, a.xp, (uint64_t)rows, a.d, 32, rowt)) {
         return cudaErrorInvalidValue;
     }
 
     cudaError_t err;
-    const size_t smem = smem_bytes();
+    const size_t smem = w4 ? smem_bytes<true>() : smem_bytes<false>();
     static PerDeviceFlag attr_done;
     const int dev = current_device();
     if (!attr_done.done(dev)) {
-        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-                cudaSuccess)
+        const int s16 = (int)smem_bytes<false>(), s4 = (int)smem_bytes<true>();
+        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess)
             return err;
         attr_done.mark(dev);
     }
@@ -614,6 +777,10 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
 
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.rows_total = rows; p.status = a.status;
+    p.xexp = w4 ? a.xexp : nullptr;
+    p.w4[0] = static_cast<const uint8_t *>(a.w_gate);
+    p.w4[1] = static_cast<const uint8_t *>(a.w_up);
+    p.groups = a.d / 64;
     // upper bound on items: chunks <= n_exp + rows / NTMAX
     const long long chunks = n_exp + rows / NTMAX;
 
@@ -632,11 +799,14 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     if (gather) {
         p.xg = static_cast<const uint16_t *>(a.x_gather);
         p.perm_tok = a.perm_tok;
-        launch_pdl(decode_tc_kernel<GATEUP, true>, g_gu, dim3(THREADS_GATHER), smem, stream, m_wg, m_wu,
+        launch_pdl(decode_tc_kernel<GATEUP, true, false>, g_gu, dim3(THREADS_GATHER), smem, stream, m_wg,
+                   m_wu, m_x16, m_x32, p);
+    } else if (w4) {
+        launch_pdl(decode_tc_kernel<GATEUP, false, true>, g_gu, dim3(THREADS_W4), smem, stream, m_wg, m_wu,
                    m_x16, m_x32, p);
     } else {
-        launch_pdl(decode_tc_kernel<GATEUP, false>, g_gu, dim3(THREADS), smem, stream, m_wg, m_wu, m_x16,
-                   m_x32, p);
+        launch_pdl(decode_tc_kernel<GATEUP, false, false>, g_gu, dim3(THREADS), smem, stream, m_wg, m_wu,
+                   m_x16, m_x32, p);
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     // split-K reductions: blocks of 32 float4 columns x min(KS, 8) split lanes
@@ -649,13 +819,15 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     };
     if (!fused) {
         launch_pdl(swiglu_reduce_kernel, dim3(reduce_grid((long long)rows * (a.F / 4), ks_gu)), reduce_block(ks_gu),
-                   0, stream, a.pgu, ks_gu, rows, a.F, a.h, a.status);
+                   0, stream, a.pgu, ks_gu, rows, a.F, a.h, p.xexp, a.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     // down: matrix W_d ([E*d, F]), K = F, token rows = h
     p.K = a.F; p.R = a.d; p.n_mats = 1; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
+    p.w4[0] = p.w4[1] = static_cast<const uint8_t *>(a.w_down);
+    p.groups = a.F / 64;
     p.fused = 0; p.h = nullptr;
     p.xg = nullptr;
     p.expire_ns = 0;
@@ -664,13 +836,17 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     } else {
         p.KS = ks_d; p.P = a.pd; p.perm_tok = nullptr;
     }
-    launch_pdl(decode_tc_kernel<DOWN, false>, dim3(grid_for(chunks * p.rtiles * p.KS)), dim3(THREADS), smem,
-               stream, m_wd, m_wd, m_h16, m_h32, p);
+    if (w4)
+        launch_pdl(decode_tc_kernel<DOWN, false, true>, dim3(grid_for(chunks * p.rtiles * p.KS)),
+                   dim3(THREADS_W4), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
+    else
+        launch_pdl(decode_tc_kernel<DOWN, false, false>, dim3(grid_for(chunks * p.rtiles * p.KS)),
+                   dim3(THREADS), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (direct) return cudaSuccess;
 
     launch_pdl(combine_kernel, dim3(reduce_grid((long long)a.T * (a.d / 4), ks_d)), reduce_block(ks_d), 0, stream,
-        a.pd, ks_d, rows, a.d, a.inv, a.topk_w, a.T, a.k, a.out, a.status);
+        a.pd, ks_d, rows, a.d, a.inv, a.topk_w, p.xexp, a.T, a.k, a.out, a.status);
     return cudaGetLastError();
 }
 

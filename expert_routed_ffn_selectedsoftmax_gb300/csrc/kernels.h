@@ -108,8 +108,11 @@ cudaError_t launch_combine_rows(const float *y, int d, const int32_t *inv, int T
 
 // decode_tc.cu -- expert FFN for few rows per expert on tcgen05 (bf16 only)
 struct DecodeTcArgs {
+    moe_dtype w_dt;             // MOE_BF16 or MOE_Q4_A64 (packed planes, 4-bit converter warps)
     const void *x;              // [T, d] bf16
-    const void *xp;             // [T*k, d] bf16 grouped rows of x (unused when gathering)
+    const void *xp;             // [T*k, d] grouped rows of x (unused when gathering): bf16, or
+                                //   for 4-bit weights fp16 rows scaled by 2^-xexp[r]
+    const int32_t *xexp;        // [T*k] 4-bit weights: exponent of each grouped row's scale
     const void *x_gather;       // non-null: gather token rows from this [T, d] via perm_tok
     const int32_t *perm_tok;    // [T*k] grouped row -> token
     int T, d, E, k, F;
@@ -119,7 +122,7 @@ struct DecodeTcArgs {
     const float *topk_w;        // [T*k]
     const float *perm_w;        // [T*k] routing weight of each grouped row
     float *pgu;                 // gate/up partials [ks_gu][2][T*k][F]
-    uint16_t *h;                // bf16 h [T*k, F] scratch
+    uint16_t *h;                // h [T*k, F] scratch: bf16, or fp16 h * 2^-2 xexp[r] (4-bit)
     float *pd;                  // down partials [ks_d][T*k][d]
     float *out;                 // [T, d] fp32 (zeroed beforehand when the down kernel adds into it)
     uint32_t *status;
@@ -162,9 +165,8 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs &a, cudaStream_t stream);
 // q8.cu
 cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
                              cudaStream_t stream);
-// q8.cu -- affine 4-bit group-64 planes (codes, fp16 scales, fp16 biases)
-size_t q4_a64_scale_offset(long long rows, int cols);
-size_t q4_a64_bias_offset(long long rows, int cols);
+// q8.cu -- affine 4-bit group-64 weights repacked into tiles (codes, fp16 scales, biases)
+size_t q4_a64_packed_bytes(long long rows, int cols);   // tiles of 128 rows x 64 columns
 cudaError_t launch_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
                                cudaStream_t stream);
 

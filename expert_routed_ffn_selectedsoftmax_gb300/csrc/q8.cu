@@ -50,50 +50,56 @@ cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void 
 }
 
 // Affine 4-bit, groups of 64 (the experts of the MLX build, "Zyphra-ZONOS2-4bit",
-// §How this was quantized):
-// 36-byte blocks {fp16 scale, fp16 bias, 32 bytes of codes, value 2j in the low
-// nibble of byte j} -> a code plane [rows, cols/2] (the blocks' code bytes in
-// order) and fp16 scale and bias planes [cols/64, rows].
-__global__ void pack_q4_a64_kernel(const uint8_t *__restrict__ blocks, long long nblocks,
-                                   long long rows, int bpr, uint8_t *__restrict__ codes,
-                                   __half *__restrict__ scales, __half *__restrict__ biases)
+// §How this was quantized): 36-byte blocks {fp16 scale, fp16 bias, 32 bytes of
+// codes, value 2j in the low nibble of byte j} -> tiles of 128 rows x one group
+// (q4_tile_offset): the rows' code bytes in order, their scales, their biases.
+// One thread per (tile, row); rows past the last one are written as zeros.
+__global__ void pack_q4_a64_kernel(const uint8_t *__restrict__ blocks, long long rows, int groups,
+                                   long long n, uint8_t *__restrict__ packed)
 {
-    for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
-         b += (long long)gridDim.x * blockDim.x) {
-        const uint8_t *src = blocks + b * 36;
-        const long long row = b / bpr, blk = b - row * bpr;   // block blk of row `row`
-        scales[blk * rows + row] = __ushort_as_half((uint16_t)src[0] | ((uint16_t)src[1] << 8));
-        biases[blk * rows + row] = __ushort_as_half((uint16_t)src[2] | ((uint16_t)src[3] << 8));
-        uint32_t w[8];
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long tile = t / kQ4TileRows;
+        const int rr = (int)(t - tile * kQ4TileRows);
+        const long long rt = tile / groups;
+        const int g = (int)(tile - rt * groups);
+        const long long row = rt * kQ4TileRows + rr;
+        uint8_t *dst = packed + (size_t)tile * kQ4TileBytes;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint16_t sc = 0, bi = 0;
+        if (row < rows) {
+            const uint8_t *src = blocks + ((size_t)row * groups + g) * 36;
+            sc = (uint16_t)src[0] | ((uint16_t)src[1] << 8);
+            bi = (uint16_t)src[2] | ((uint16_t)src[3] << 8);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = (uint32_t)src[4 + 4 * i] | ((uint32_t)src[5 + 4 * i] << 8) |
-                   ((uint32_t)src[6 + 4 * i] << 16) | ((uint32_t)src[7 + 4 * i] << 24);
-        uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int i = 0; i < 8; ++i)
+                w[i] = (uint32_t)src[4 + 4 * i] | ((uint32_t)src[5 + 4 * i] << 8) |
+                       ((uint32_t)src[6 + 4 * i] << 16) | ((uint32_t)src[7 + 4 * i] << 24);
+        }
+        uint4 *c = reinterpret_cast<uint4 *>(dst + rr * 32);
+        c[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        c[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        reinterpret_cast<uint16_t *>(dst + kQ4ScaleOff)[rr] = sc;
+        reinterpret_cast<uint16_t *>(dst + kQ4BiasOff)[rr] = bi;
     }
 }
 
-size_t q4_a64_scale_offset(long long rows, int cols) { return align_up((size_t)rows * cols / 2, 256); }
-size_t q4_a64_bias_offset(long long rows, int cols)
+size_t q4_a64_packed_bytes(long long rows, int cols)
 {
-    return align_up(q4_a64_scale_offset(rows, cols) + (size_t)rows * (cols / 64) * 2, 256);
+    const long long tiles_r = (rows + kQ4TileRows - 1) / kQ4TileRows;
+    return (size_t)tiles_r * (size_t)(cols / 64) * kQ4TileBytes;
 }
 
 cudaError_t launch_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
                                cudaStream_t stream)
 {
-    const long long nblocks = rows * (cols / 64);
-    if (nblocks == 0) return cudaSuccess;
-    char *base = static_cast<char *>(packed);
-    long long grid = (nblocks + 255) / 256;
+    const int groups = cols / 64;
+    const long long n = (rows + kQ4TileRows - 1) / kQ4TileRows * groups * kQ4TileRows;
+    if (n == 0) return cudaSuccess;
+    long long grid = (n + 255) / 256;
     if (grid > 65535LL * 16) grid = 65535LL * 16;
-    pack_q4_a64_kernel<<<(unsigned)grid, 256, 0, stream>>>(
-        static_cast<const uint8_t *>(blocks), nblocks, rows, cols / 64,
-        reinterpret_cast<uint8_t *>(base),
-        reinterpret_cast<__half *>(base + q4_a64_scale_offset(rows, cols)),
-        reinterpret_cast<__half *>(base + q4_a64_bias_offset(rows, cols)));
+    pack_q4_a64_kernel<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), rows,
+                                                           groups, n, static_cast<uint8_t *>(packed));
     return cudaGetLastError();
 }
 

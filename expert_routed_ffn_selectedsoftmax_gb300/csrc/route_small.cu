@@ -228,9 +228,10 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
             for (int j = 0; j < nkb; ++j) {
                 const uint32_t a0 = smem_u32(a_tiles + (size_t)j * A_TILE);
                 const uint32_t b0 = smem_u32(b_tiles + (size_t)j * BT);
+                const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_f16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (j | kk) != 0);
+                    umma_f16(tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc, (j | kk) != 0);
             }
         } else {
             flag_status(p.status, kDevTimeout);

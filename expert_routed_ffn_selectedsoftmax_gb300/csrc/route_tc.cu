@@ -180,9 +180,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc_fence_after();
             const uint32_t a0 = smem_u32(smem + s * SLOT);
             const uint32_t b0 = a0 + A_BYTES;
+            const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-                umma_f16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                umma_f16(tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc,
                          (kb | kk) != 0);
             umma_commit(&c.empty[s]);
         }

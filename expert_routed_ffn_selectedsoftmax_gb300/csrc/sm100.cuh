@@ -62,10 +62,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     }
     return ok != 0;
 }
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // on timeout (`timeout_ns`) or when another role has raised the abort flag.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                              unsigned long long timeout_ns = kTimeoutNs)
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                   unsigned long long timeout_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -76,6 +89,13 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, vo
             if (globaltimer() - t0 > timeout_ns) return false;
         }
     }
+}
+// The same wait with an inline test first: a phase that has already completed
+// costs a few instructions instead of a call.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned long long timeout_ns = kTimeoutNs)
+{
+    return mbar_test_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, timeout_ns);
 }
 // Address of `local` (this CTA's shared memory) in the shared memory of
 // cluster CTA `rank`, as a shared::cluster address.
@@ -105,6 +125,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global into this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 // Prefetch of one tile into L2 (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
@@ -156,6 +184,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     d |= (uint64_t)2 << 61;             // SWIZZLE_128B
     return d;
 }
+
+// sw128_desc(saddr + bytes) from sw128_desc(saddr), for a shift that keeps the
+// address inside the descriptor's 18-bit field (the start address is in
+// 16-byte units in the low bits)
+__device__ __forceinline__ uint64_t desc_step(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate)

@@ -413,13 +413,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(smem + s * C::STAGE);
                 const uint32_t b0 = Q8 ? smem_u32(sCvt + cb * C::B_BYTES) : a0 + A_BYTES;
+                const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     if (PAIR)
-                        umma_f16_pair(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                        umma_f16_pair(d_tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc,
                                       (kb | kk) != 0);
                     else
-                        umma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                        umma_f16(d_tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc,
                                  (kb | kk) != 0);
                 }
                 // frees the stage (and the converted buffer) in both CTAs of a

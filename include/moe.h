@@ -64,10 +64,11 @@ typedef enum {
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3 } moe_dtype;
 
 /* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
- * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16
- *   weights with d % 128 == 0, F % 128 == 0 and T*k <= 8192, otherwise the
- *   CUDA-core kernels.  PREFILL: tcgen05 grouped GEMMs.  DECODE_SIMT: always
- *   the CUDA-core decode kernels (the decode path for fp32 and Q8_0). */
+ * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16 or
+ *   affine 4-bit weights (4-bit tiles converted to fp16 in shared memory) with
+ *   d % 128 == 0, F % 128 == 0 and T*k <= 8192, otherwise the CUDA-core
+ *   kernels.  PREFILL: tcgen05 grouped GEMMs.  DECODE_SIMT: always the
+ *   CUDA-core decode kernels (the decode path for fp32 and Q8_0). */
 typedef enum {
     MOE_PATH_AUTO = 0,
     MOE_PATH_DECODE = 1,
@@ -178,13 +179,21 @@ MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, v
  * Input format: rows of `cols` values along the contiguous axis, stored as
  * cols/64 blocks of 36 bytes {fp16 scale, fp16 bias (little endian), 32 bytes
  * of codes: value 2j in the low nibble of byte j, 2j+1 in the high nibble};
- * value = scale * q + bias.  Used with BF16 activations on the CUDA-core
- * decode kernels (MOE_PATH_PREFILL returns MOE_ERR_UNSUPPORTED).  moe_forward
- * consumes them repacked into three planes in one buffer:
- *   bytes [0, rows*cols/2)                 codes [rows, cols/2], as above
- *   at align256(rows*cols/2)               fp16 scale plane [cols/64, rows]
- *   at align256(end of the scale plane)    fp16 bias plane [cols/64, rows]
- * moe_q4_a64_packed_size returns the buffer size (0 if cols % 64 != 0 or
+ * value = scale * q + bias.  Used with BF16 activations on the tensor-core
+ * decode kernels (d and F multiples of 128) or the CUDA-core decode kernels
+ * (MOE_PATH_PREFILL returns MOE_ERR_UNSUPPORTED).  The tensor-core kernels
+ * multiply fp16 operands: each weight is scale * q + bias rounded once to
+ * fp16, each token row is x times a power of two (exact), and h is held in
+ * fp16 scaled by the square of that power, as on the Q8_0 path; an h beyond
+ * fp16's range there is reported as MOE_ERR_DEVICE_CHECK.  moe_forward
+ * consumes them repacked into tiles of 128 rows x 64 columns (one group),
+ * 4608 bytes each, so that one k-block of one row tile is one contiguous copy:
+ *   tile (rt, g), rt = row / 128, g = col / 64, at byte ((rt * cols/64) + g) * 4608
+ *   bytes [0, 4096)       the tile's 128 rows of 32 code bytes, in row order, as above
+ *   bytes [4096, 4352)    their 128 fp16 scales
+ *   bytes [4352, 4608)    their 128 fp16 biases
+ * Rows past `rows` in the last row tile are zero.  moe_q4_a64_packed_size
+ * returns ceil(rows / 128) * (cols / 64) * 4608 (0 if cols % 64 != 0 or
  * rows < 0); moe_pack_q4_a64 repacks `blocks` (device, any alignment) into
  * `packed` (device, 256-byte aligned) on `stream`, with the same rows/cols as
  * moe_pack_q8_0.

@@ -104,8 +104,9 @@ def test_argument_errors_are_synchronous(lib):
     assert lib.moe_pack_q4_a64(fake, 4, 96, fake, None) == I      # cols % 64
     assert lib.moe_pack_q4_a64(fake, 4, 128, vp(0x10010), None) == I
     assert lib.moe_q4_a64_packed_size(4, 96) == 0
-    # codes 4*128/2 = 256 B, scales at 256 (16 B), biases at 512 (16 B)
-    assert lib.moe_q4_a64_packed_size(4, 128) == 512 + 16
+    # one row tile (rows padded to 128) x 2 groups, 4608 bytes per tile
+    assert lib.moe_q4_a64_packed_size(4, 128) == 2 * 4608
+    assert lib.moe_q4_a64_packed_size(129, 64) == 2 * 4608
     assert fwd(path=9) == I
     assert fwd(wg=None) == I
     assert fwd(ws=vp(0x10010)) == I              # workspace not 256-byte aligned
