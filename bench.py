@@ -206,7 +206,8 @@ def expert_kernel_names(w, T, num_sms):
     and T >= 512 for bf16 / Q8_0 weights with d % 256 == 0 and F % 128 == 0;
     tensor-core decode for bf16 and affine 4-bit layers with d, F multiples of
     128 and T*k <= 8192 -- one clustered routing+grouping kernel for T <= 128
-    (4-bit: plus the kernel that writes the grouped fp16 rows), then for bf16
+    (which also writes the grouped fp16 rows of 4-bit layers of up to 16
+    tokens; beyond that a gather kernel does), then for bf16
     one persistent kernel for gate/up, SwiGLU, down and the combine when k <= 2
     and the batch has half a wave of whole-K gate/up items of at most 512 KB,
     else the gate/up and down kernels with their split-K reductions; otherwise
@@ -231,7 +232,10 @@ def expert_kernel_names(w, T, num_sms):
                     "launches": (1 if small else 2) + 1}
         fused = 192 <= n_exp * (w.F // 128) <= 2 * num_sms
         direct = w.k <= 2 and n_exp * (w.d // 128) >= 192
-        launches = (1 if small and not q4 else 2) + (1 if fused else 2) + (1 if direct else 2)
+        # 4-bit: the grouped fp16 rows come from the clustered router up to 16
+        # tokens, else from a gather kernel
+        launches = (1 if small else 2) + (1 if q4 and small and T > 16 else 0) + \
+            (1 if fused else 2) + (1 if direct else 2)
         tag = ", 4-bit" if q4 else ""
         gu = f"decode_tc_kernel<GATEUP{tag}> (whole K, writes h)" if fused else \
             f"decode_tc_kernel<GATEUP{tag}> + swiglu_reduce_kernel"

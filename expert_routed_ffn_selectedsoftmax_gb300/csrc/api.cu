@@ -409,7 +409,12 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // decode batches of up to 128 tokens: one clustered kernel routes and
     // groups (no scatter); the tensor-core decode kernel gathers x rows itself
     const bool fused_small = !dense && use_dtc && route_small_capable(act_dt, T, d, E, k);
-    ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && !fused_small) ? ws + L.xp : nullptr;
+    // the clustered router writes grouped rows only as fp16, for the 4-bit
+    // tensor-core decode kernels, and only for up to 16 tokens: beyond that a
+    // separate gather kernel writes them sooner than the router's owners do
+    const bool router_rows = w_dt == MOE_Q4_A64 && T <= kRouteSmallRowsMaxT;
+    ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && (!fused_small || router_rows)) ? ws + L.xp
+                                                                                                : nullptr;
     // the Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels take fp16
     // rows (scaled)
     ra.xp_fp16 = w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64;

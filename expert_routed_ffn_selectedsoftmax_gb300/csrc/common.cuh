@@ -136,10 +136,14 @@ template <> struct WView<Q8Tag> {
 // the host.
 // Packed affine 4-bit weights (moe_pack_q4_a64) are tiles of 128 rows x 64
 // columns (one group), 4608 bytes each, in row-tile-major order: tile (rt, g)
-// at ((rt * groups) + g) * 4608; inside, the 128 rows' 32 code bytes (value
-// 2j in the low nibble of byte j), then the 128 fp16 scales, then the 128
-// fp16 biases.  A k-block of one row tile is one contiguous copy.
+// at ((rt * groups) + g) * 4608; inside, the 128 rows' 32 code bytes, then the
+// 128 fp16 scales, then the 128 fp16 biases.  A k-block of one row tile is one
+// contiguous copy.  Each 32-bit word of a row's codes holds 8 consecutive
+// values, the even ones in nibbles 0-3 and the odd ones in nibbles 4-7
+// (value i in nibble q4_nibble(i)), so that one mask of the word yields two
+// neighbouring values, one per 16-bit half.
 constexpr int kQ4TileRows = 128, kQ4TileBytes = 4608, kQ4ScaleOff = 4096, kQ4BiasOff = 4352;
+__host__ __device__ __forceinline__ constexpr int q4_nibble(int i) { return (i >> 1) + 4 * (i & 1); }
 __host__ __device__ __forceinline__ size_t q4_tile_offset(long long row, int g, int groups)
 {
     return ((size_t)(row / kQ4TileRows) * (size_t)groups + (size_t)g) * kQ4TileBytes;
@@ -162,7 +166,7 @@ template <> struct WView<Q4Tag> {
     __device__ __forceinline__ static void cvt(const RawW<Q4Tag> &r, Chunk8 &c)
     {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c.v[i] = fmaf(r.s, (float)((r.q >> (4 * i)) & 15u), r.b);
+        for (int i = 0; i < 8; ++i) c.v[i] = fmaf(r.s, (float)((r.q >> (4 * q4_nibble(i))) & 15u), r.b);
     }
 };
 
@@ -175,11 +179,19 @@ template <> struct WView<Q4Tag> {
 __device__ __forceinline__ int fp16_row_exponent(const uint16_t *row, int d, int lane)
 {
     float m = 0.f;
-    for (int c = lane; c < d / 8; c += 32) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(row) + c);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    constexpr int U = 8;   // loads in flight per lane
+    for (int c0 = lane; c0 < d / 8; c0 += 32 * U) {
+        uint4 u[U];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[q])), fabsf(bf16hi(w[q]))));
+        for (int q = 0; q < U; ++q)
+            u[q] = c0 + 32 * q < d / 8 ? __ldg(reinterpret_cast<const uint4 *>(row) + c0 + 32 * q)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[r])), fabsf(bf16hi(w[r]))));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));

@@ -72,28 +72,32 @@ constexpr int SLOT = A_BYTES + B_BYTES;         // 20 KB per stage, 1024-aligned
 constexpr int KBMAX = 8;                        // k-blocks per item
 constexpr int THREADS = 192;
 constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
-// Affine 4-bit weights (W4): a stage holds the token tile (4 KB, first, for the
-// swizzle) and one packed weight tile (q4_tile_offset: the 128 x 64 codes,
-// 4 KB, then their fp16 scales and biases, 256 B each), fetched by a single
-// contiguous copy; four converter warps turn it into the 16 KB fp16 tile the MMA
-// reads and copy the token tile beside it, in one of NCVT4 converted buffers
-// after the ring, then release the ring stage themselves: the MMA issuer waits
-// on one barrier and commits one per k-block.  The MMAs then run
+// Affine 4-bit weights (W4): a stage holds two parts -- k-blocks kb and kb+1 of
+// the item's matrix, or (whole-K gate/up items) the gate and the up tile of one
+// k-block -- so the waits, commits and loop overheads of the MMA issuer and the
+// converters are paid once per two weight tiles.  Layout: two token tiles of 4 KB
+// (only one for a gate/up pair, which shares it) and two packed weight tiles
+// (q4_tile_offset: 128 x 64 codes, then their fp16 scales and biases; the two
+// k-blocks of one row tile are adjacent, one contiguous copy).  Four converter
+// warps turn each weight tile into the fp16 A operand of the MMA and store it in
+// tensor memory (row i in TMEM lane i, 32 columns per tile, NCVT4 buffers of two
+// tiles after the accumulators), so the converted weights never pass through
+// shared memory; the MMA issuer waits only for the converters, which have seen
+// the stage's copies land.  The MMAs then run
 // on fp16 operands: each weight is scale * q + bias rounded once to fp16
 // (relative error 2^-11, a quarter of a bf16 rounding), the token rows are
 // fp16 rows of x scaled by 2^-xexp[r] (exact for bf16 digits), and h is kept
 // in fp16 as h * 2^-2 xexp[r], undone in the down epilogue or the combine.
 #ifndef MOE_DTC_STAGES4
-#define MOE_DTC_STAGES4 7
+#define MOE_DTC_STAGES4 6
 #endif
 #ifndef MOE_DTC_NCVT4
 #define MOE_DTC_NCVT4 2
 #endif
 constexpr int STAGES4 = MOE_DTC_STAGES4;
-constexpr int SLOT4 = 9216;                     // 4096 + 4608, 1024-aligned
-constexpr int CODE_OFF4 = 4096, SC_OFF4 = CODE_OFF4 + kQ4ScaleOff, BI_OFF4 = CODE_OFF4 + kQ4BiasOff;
-constexpr int W4_TX = kQ4TileBytes;             // weight bytes of a W4 stage
-static_assert(CODE_OFF4 + kQ4TileBytes <= SLOT4, "a W4 stage holds the token tile and one weight tile");
+constexpr int SLOT4 = 17408;                    // 2 x 4096 + 2 x 4608, 1024-aligned
+constexpr int WT_OFF4 = 2 * 4096;               // the two weight tiles
+static_assert(WT_OFF4 + 2 * kQ4TileBytes <= SLOT4 && SLOT4 % 1024 == 0, "W4 stage layout");
 constexpr int NCVT4 = MOE_DTC_NCVT4;
 constexpr int THREADS_W4 = 320;                 // + 4 converter warps
 constexpr int kStagesMax = STAGES4 > STAGES ? STAGES4 : STAGES;
@@ -101,12 +105,13 @@ template <bool W4> struct Ring {
     static constexpr int NST = W4 ? STAGES4 : STAGES;
     static constexpr int SLOTB = W4 ? SLOT4 : SLOT;
     static constexpr int B_OFF = W4 ? 0 : A_BYTES;      // token tile
-    static constexpr int CVT = W4 ? NST * SLOT4 : 0;    // converted buffers: weights, token tile
-    static constexpr int CVTB = A_BYTES + B_BYTES;
-    static constexpr int CTL = NST * SLOTB + (W4 ? NCVT4 * CVTB : 0);
+    static constexpr int CTL = NST * SLOTB;
+    // TMEM: NACC accumulators of 32 columns, then (W4) NCVT4 A buffers of 32
+    static constexpr uint32_t TMEM_COLS = W4 ? 256 : 128;
 };
 constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
-constexpr int TMEM_COLS = 128;
+constexpr uint32_t A_COL4 = NACC * 32;          // W4: first column of the converted A buffers
+static_assert(A_COL4 + NCVT4 * 64 <= 256, "W4 accumulators and A buffers fit in 256 TMEM columns");
 constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~1 item per CTA: 2 CTAs per SM on a 152-SM GB300
 
 enum Mode { GATEUP = 0, DOWN = 1 };
@@ -183,6 +188,22 @@ __device__ __forceinline__ void stage_of(const Params &p, const Item &it, int kb
     else { m = it.m; kb = it.kb0 + kbl; }
 }
 
+// W4 stages of an item, the parts (1 or 2) of stage st, and part j's matrix,
+// k-block and token tile.
+__device__ __forceinline__ int w4_stages(const Params &p, const Item &it)
+{
+    return p.fused ? p.kb_total : (it.nkb + 1) / 2;
+}
+__device__ __forceinline__ int w4_parts(const Params &p, const Item &it, int st)
+{
+    return p.fused ? 2 : min(2, it.nkb - 2 * st);
+}
+__device__ __forceinline__ void w4_part(const Params &p, const Item &it, int st, int j, int &m, int &kb, int &tt)
+{
+    if (p.fused) { m = j; kb = st; tt = 0; }
+    else { m = it.m; kb = it.kb0 + 2 * st + j; tt = j; }
+}
+
 // SiLU(z) = z * sigmoid(z) with the fast exponential and an approximate
 // divide (relative error ~1e-6, below the bf16 rounding of h that follows).
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
@@ -225,7 +246,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         // GATHER: a stage is full after the weight tile's bytes and the 32
         // arrivals of the warp that wrote its token rows
         // W4: the four converter warps release a stage
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], GATHER ? 33 : 1); mbar_init(&c.empty[s], W4 ? 4 : 1); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&c.full[s], GATHER ? 33 : 1); mbar_init(&c.empty[s], 1); }
         for (int b = 0; b < NCVT4; ++b) { mbar_init(&c.cfull[b], 4); mbar_init(&c.cempty[b], 1); }
         for (int b = 0; b < NACC; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
         mbar_init(&c.drain, 1);
@@ -243,13 +264,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b32)) : "memory");
         }
     }
-    if (warp == 1) tmem_alloc(&c.tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_alloc(&c.tmem_base, RG::TMEM_COLS);
     tc_fence_before();
     pdl_enter();
     if (upstream_failed(p.status)) {   // (synchronises the CTA)
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc(c.tmem_base, TMEM_COLS);
+            tmem_dealloc(c.tmem_base, RG::TMEM_COLS);
         }
         return;
     }
@@ -296,8 +317,32 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item(c, p, item);
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
-            const uint32_t bytes = (W4 ? W4_TX : A_BYTES) + (GATHER ? 0 : it.nt * BK * 2);
+            const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
+            if constexpr (W4) {
+                const int nst = w4_stages(p, it);
+                for (int st = 0; st < nst; ++st, ++it_k) {
+                    const int s = it_k % STAGES;
+                    if (!mbar_wait(&c.empty[s], ((it_k / STAGES) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                    const int np = w4_parts(p, it, st), ntok = p.fused ? 1 : np;
+                    mbar_expect_tx(&c.full[s], (uint32_t)(np * kQ4TileBytes + ntok * it.nt * BK * 2));
+                    uint8_t *sp = smem + s * SLOT;
+                    if (p.fused) {   // gate and up tiles of k-block st
+                        bulk_load(sp + WT_OFF4, p.w4[0] + q4_tile_offset(wrow, st, p.groups), kQ4TileBytes, &c.full[s]);
+                        bulk_load(sp + WT_OFF4 + kQ4TileBytes, p.w4[1] + q4_tile_offset(wrow, st, p.groups),
+                                  kQ4TileBytes, &c.full[s]);
+                    } else {         // k-blocks kb, kb + 1: adjacent tiles
+                        bulk_load(sp + WT_OFF4, p.w4[it.m] + q4_tile_offset(wrow, it.kb0 + 2 * st, p.groups),
+                                  (uint32_t)(np * kQ4TileBytes), &c.full[s]);
+                    }
+                    for (int j = 0; j < ntok; ++j) {
+                        int m, kb, tt;
+                        w4_part(p, it, st, j, m, kb, tt);
+                        tma_load_2d(sp + tt * B_BYTES, bmap, &c.full[s], kb * BK, it.row0);
+                    }
+                }
+                continue;
+            }
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
                 const uint32_t ph = (it_k / STAGES) & 1u;
@@ -308,13 +353,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 const CUtensorMap *wmap = (MODE == GATEUP && m == 1) ? &tm_w1 : &tm_w0;
                 const int kx = kb * BK;
                 uint8_t *st = smem + s * SLOT;
-                if (W4) {
-                    // the packed tile of (row tile, k-block): codes, scales, biases
-                    bulk_load(st + CODE_OFF4, p.w4[MODE == GATEUP ? m : 0] + q4_tile_offset(wrow, kb, p.groups),
-                              kQ4TileBytes, &c.full[s]);
-                } else {
-                    tma_load_2d(st, wmap, &c.full[s], kx, wrow);
-                }
+                tma_load_2d(st, wmap, &c.full[s], kx, wrow);
                 if (!GATHER) tma_load_2d(st + RG::B_OFF, bmap, &c.full[s], kx, it.row0);
             }
         }
@@ -339,26 +378,50 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             if (!mbar_wait(&c.tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t idesc = idesc_f16_mn(W4 ? 1 : 0, BM, it.nt);
+            if constexpr (W4) {
+                const int nst = w4_stages(p, it);
+                for (int st = 0; st < nst; ++st, ++it_k) {
+                    const int s = it_k % STAGES, cb = it_k % NCVT4;
+                    // the converters arrive after they have seen the stage land
+                    if (!mbar_wait(&c.cfull[cb], (it_k / NCVT4) & 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const int np = w4_parts(p, it, st);
+                    const uint32_t sp = smem_u32(smem + s * SLOT);
+                    const uint32_t a_tm = tmem + A_COL4 + cb * 64;   // A in TMEM: K = 16 is 8 columns
+                    for (int j = 0; j < np; ++j) {
+                        int m, kb, tt;
+                        w4_part(p, it, st, j, m, kb, tt);
+                        const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
+                        const uint64_t db = sw128_desc(sp + tt * B_BYTES);
+                        const int first = p.fused ? kb : 2 * st + j;   // first k-block of this accumulator
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_f16_ts(d_tmem, a_tm + j * 32 + kk * 8, desc_step(db, kk * 32), idesc,
+                                        (first | kk) != 0);
+                    }
+                    umma_commit(&c.empty[s]);
+                    umma_commit(&c.cempty[cb]);
+                }
+                if (!ok) break;
+                umma_commit(&c.tfull[acc]);
+                continue;
+            }
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
                 const uint32_t ph = (it_k / STAGES) & 1u;
-                const int cb = it_k % NCVT4;
-                // W4: the converted buffer holds both operands
-                if (W4 ? !mbar_wait(&c.cfull[cb], (it_k / NCVT4) & 1u, abort_flag)
-                       : !mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&c.full[s], ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 int m, kb;
                 stage_of(p, it, kbl, m, kb);
                 const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
-                const uint32_t a0 = W4 ? smem_u32(smem + RG::CVT + cb * RG::CVTB) : smem_u32(smem + s * SLOT);
-                const uint32_t b0 = W4 ? a0 + A_BYTES : smem_u32(smem + s * SLOT + RG::B_OFF);
+                const uint32_t a0 = smem_u32(smem + s * SLOT);
+                const uint32_t b0 = smem_u32(smem + s * SLOT + RG::B_OFF);
                 const int first = p.fused ? kb : kbl;   // first k-block of this accumulator
                 const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_f16(d_tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc,
-                             (first | kk) != 0);
-                umma_commit(W4 ? &c.cempty[cb] : &c.empty[s]);
+                    umma_f16(d_tmem, desc_step(da, kk * 32), desc_step(db, kk * 32), idesc, (first | kk) != 0);
+                umma_commit(&c.empty[s]);
             }
             if (!ok) break;
             umma_commit(&c.tfull[acc]);
@@ -372,62 +435,62 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         }
     } else if (W4 && warp >= 6) {
         // ------------------------------------------------ 4-bit converters (4 warps)
-        // warp 6 + w converts rows 32w .. 32w+31 of every stage's tile, lane = row:
-        // 64 codes -> scale * q + bias in fp16, in the 128-byte-swizzled layout.
-        // Byte j of a row holds q_2j (low nibble) and q_2j+1 (high nibble).  Placed
-        // in the low byte of both halves of a word under the fp16 exponent of
-        // 1024 (ulp 1), the low half keeps the low nibble (1024 + q_2j) and the
-        // high half the high one in bits 4-7 (1024 + 16 q_2j+1); one exact fma
-        // by (1, 1/16) and (-1024, -64) leaves (q_2j, q_2j+1), a second one
-        // gives scale * q + bias with a single rounding.
-        const int row = (warp - 6) * 32 + lane;
-        const __half2 unit = __halves2half2(__float2half_rn(1.0f), __float2half_rn(0.0625f));
-        const __half2 unbias = __halves2half2(__float2half_rn(-1024.0f), __float2half_rn(-64.0f));
+        // a warp may access only the TMEM lanes of its quadrant (warp % 4): warp w
+        // converts rows 32 (w % 4) .. +31 of every weight tile, lane = row:
+        // 64 codes -> scale * q + bias in fp16 -> 32 columns of its TMEM lane.
+        // A 32-bit word of codes holds values 0, 2, 4, 6 of its 8 in nibbles 0-3
+        // and values 1, 3, 5, 7 in nibbles 4-7 (q4_nibble).  Masked under the
+        // fp16 exponent of 1024 (ulp 1), nibbles 0 and 4 give the pair (1024 +
+        // q_0, 1024 + q_1) and nibbles 1 and 5, left in bits 4-7 of each half,
+        // (1024 + 16 q_2, 1024 + 16 q_3); the word shifted by 8 gives values 4-7
+        // the same way.  One exact fma by (1, 1) or (1/16, 1/16) and the matching
+        // offset leaves the codes, a second one gives scale * q + bias with a
+        // single rounding.
+        const int quad = warp & 3, row = quad * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + A_COL4;
+        const __half2 one2 = __float2half2_rn(1.0f), m1024 = __float2half2_rn(-1024.0f);
+        const __half2 sixteenth2 = __float2half2_rn(0.0625f), m64 = __float2half2_rn(-64.0f);
+        auto pair = [](uint32_t t, __half2 mul, __half2 add, __half2 sc2, __half2 bi2) {
+            t |= 0x64006400u;
+            const __half2 v = __hfma2(__hfma2(*reinterpret_cast<const __half2 *>(&t), mul, add), sc2, bi2);
+            return *reinterpret_cast<const uint32_t *>(&v);
+        };
         uint32_t it_k = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item(c, p, item);
-            for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
+            const int nst = w4_stages(p, it);
+            for (int st = 0; st < nst; ++st, ++it_k) {
                 const int s = it_k % STAGES, cb = it_k % NCVT4;
                 if (!__all_sync(0xffffffffu, mbar_wait(&c.full[s], (it_k / STAGES) & 1u, abort_flag)) ||
                     !__all_sync(0xffffffffu, mbar_wait(&c.cempty[cb], ((it_k / NCVT4) & 1u) ^ 1u, abort_flag))) {
                     ok = false;
                     break;
                 }
-                const uint8_t *st = smem + s * SLOT;
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(st + CODE_OFF4 + row * 32);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(st + CODE_OFF4 + row * 32 + 16);
-                const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(st + SC_OFF4)[row]);
-                const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(st + BI_OFF4)[row]);
-                const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                uint8_t *const cvt = smem + RG::CVT + cb * RG::CVTB;
-                uint8_t *dst = cvt + row * 128;
+                const int np = w4_parts(p, it, st);
+                for (int j = 0; j < np; ++j) {
+                    const uint8_t *wt = smem + s * SLOT + WT_OFF4 + j * kQ4TileBytes;
+                    const uint4 q0 = *reinterpret_cast<const uint4 *>(wt + row * 32);
+                    const uint4 q1 = *reinterpret_cast<const uint4 *>(wt + row * 32 + 16);
+                    const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(wt + kQ4ScaleOff)[row]);
+                    const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(wt + kQ4BiasOff)[row]);
+                    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    uint32_t o[32];   // column c: values 2c, 2c+1
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk ch: values 8ch .. 8ch+7
-                    uint32_t o[4];
-#pragma unroll
-                    for (int pr = 0; pr < 4; ++pr) {
-                        // values 8ch+2pr, 8ch+2pr+1: the nibbles of byte pr
-                        const uint32_t t = (__byte_perm(w[ch], 0u, (uint32_t)(pr | (pr << 8))) & 0x00F0000Fu) |
-                                           0x64006400u;
-                        const __half2 q = __hfma2(*reinterpret_cast<const __half2 *>(&t), unit, unbias);
-                        const __half2 v = __hfma2(q, sc2, bi2);
-                        o[pr] = *reinterpret_cast<const uint32_t *>(&v);
+                    for (int ch = 0; ch < 8; ++ch) {   // values 8ch .. 8ch+7
+                        const uint32_t w8 = w[ch] >> 8;
+                        o[4 * ch + 0] = pair(w[ch] & 0x000F000Fu, one2, m1024, sc2, bi2);
+                        o[4 * ch + 1] = pair(w[ch] & 0x00F000F0u, sixteenth2, m64, sc2, bi2);
+                        o[4 * ch + 2] = pair(w8 & 0x000F000Fu, one2, m1024, sc2, bi2);
+                        o[4 * ch + 3] = pair(w8 & 0x00F000F0u, sixteenth2, m64, sc2, bi2);
                     }
-                    *reinterpret_cast<uint4 *>(dst + ((ch ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    tmem_st16(t_lane + cb * 64 + j * 32, *reinterpret_cast<const uint32_t(*)[16]>(&o[0]));
+                    tmem_st16(t_lane + cb * 64 + j * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o[16]));
                 }
-                // the token tile (same offset mod 1024, so the same swizzle)
-                const int tid = (warp - 6) * 32 + lane;
-                const uint4 x0 = reinterpret_cast<const uint4 *>(st + RG::B_OFF)[tid];
-                const uint4 x1 = reinterpret_cast<const uint4 *>(st + RG::B_OFF)[tid + 128];
-                reinterpret_cast<uint4 *>(cvt + A_BYTES)[tid] = x0;
-                reinterpret_cast<uint4 *>(cvt + A_BYTES)[tid + 128] = x1;
-                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&c.cfull[cb]);
-                    mbar_arrive(&c.empty[s]);   // the ring stage is read
-                }
+                if (lane == 0) mbar_arrive(&c.cfull[cb]);
             }
         }
         if (!ok) {
@@ -558,7 +621,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, RG::TMEM_COLS);
     }
 }
 

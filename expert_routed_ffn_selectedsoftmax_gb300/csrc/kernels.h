@@ -60,6 +60,7 @@ cudaError_t launch_route_tc(const RouteTcArgs &a, cudaStream_t stream);
 // grouping scatter over token tiles of `tile_tokens` (counts/ranks from either router)
 cudaError_t launch_scatter(const RouteTcArgs &a, int ntiles, int tile_tokens, cudaStream_t stream);
 
+constexpr int kRouteSmallRowsMaxT = 16;   // batches the clustered router also writes fp16 rows for
 // route_small.cu -- routing and grouping in one clustered kernel for T <= 128
 // (bf16 activations): writes topk_idx/topk_w and counts, offsets, perm_tok,
 // inv, perm_w (counts == NULL: routing only), and zeroes out_zero and

@@ -52,8 +52,10 @@ cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void 
 // Affine 4-bit, groups of 64 (the experts of the MLX build, "Zyphra-ZONOS2-4bit",
 // §How this was quantized): 36-byte blocks {fp16 scale, fp16 bias, 32 bytes of
 // codes, value 2j in the low nibble of byte j} -> tiles of 128 rows x one group
-// (q4_tile_offset): the rows' code bytes in order, their scales, their biases.
-// One thread per (tile, row); rows past the last one are written as zeros.
+// (q4_tile_offset): the rows' codes (each 4 bytes regrouped so that the even
+// values fill the low 16 bits and the odd ones the high 16 bits, q4_nibble),
+// their scales, their biases.  One thread per (tile, row); rows past the last
+// one are written as zeros.
 __global__ void pack_q4_a64_kernel(const uint8_t *__restrict__ blocks, long long rows, int groups,
                                    long long n, uint8_t *__restrict__ packed)
 {
@@ -72,9 +74,15 @@ __global__ void pack_q4_a64_kernel(const uint8_t *__restrict__ blocks, long long
             sc = (uint16_t)src[0] | ((uint16_t)src[1] << 8);
             bi = (uint16_t)src[2] | ((uint16_t)src[3] << 8);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = (uint32_t)src[4 + 4 * i] | ((uint32_t)src[5 + 4 * i] << 8) |
-                       ((uint32_t)src[6 + 4 * i] << 16) | ((uint32_t)src[7 + 4 * i] << 24);
+            for (int i = 0; i < 8; ++i) {
+                uint32_t lo = 0, hi = 0;   // even values (low nibbles), odd values (high nibbles)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    lo |= (uint32_t)(src[4 + 4 * i + b] & 15u) << (4 * b);
+                    hi |= (uint32_t)(src[4 + 4 * i + b] >> 4) << (4 * b);
+                }
+                w[i] = lo | (hi << 16);
+            }
         }
         uint4 *c = reinterpret_cast<uint4 *>(dst + rr * 32);
         c[0] = make_uint4(w[0], w[1], w[2], w[3]);

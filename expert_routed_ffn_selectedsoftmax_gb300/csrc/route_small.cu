@@ -31,6 +31,10 @@
 //     prefix over lower CTAs (which own lower tokens) give each slot its
 //     grouped row = offset[e] + (e's tokens in lower CTAs) + (e's tokens
 //     before it here).
+//   - Optionally (the fp16 operands of the 4-bit tensor-core decode kernels)
+//     each CTA also writes the grouped rows of its own tokens as fp16, scaled
+//     by 2^-xexp (fp16_row_exponent): the exponents are taken from x while
+//     the operands load, the rows once the grouped positions are known.
 //   Cluster barriers: one after the mbarriers are initialised (before any
 //   peer may signal them; it overlaps the wait for the preceding kernel) and
 //   one before exit (no CTA leaves while a peer may still copy into it).
@@ -74,6 +78,9 @@ struct Params {
     uint32_t *zero_words;                // optional scratch words later kernels count on being zero
     int n_zero;
     uint32_t expire_ns;                  // > 0: the MMA thread's operand wait gives up after this long (test hook)
+    const uint16_t *x;                   // [T, d] bf16 (the rows below)
+    uint16_t *xp;                        // optional [T*k, d] fp16 grouped rows, row r = x * 2^-xexp[r]
+    int32_t *xexp;                       //   and their exponents
 };
 
 struct Ctl {
@@ -87,6 +94,8 @@ struct Ctl {
     int tot[kMaxExperts], pre[kMaxExperts], off[kMaxExperts + 1];
     int sel_e[TPC][kMaxTopK];
     float sel_w[TPC][kMaxTopK];
+    int xe[TPC];                         // xp: exponent of each owned token row
+    int pos[TPC][kMaxTopK];              // xp: grouped row of each owned slot (-1: none)
 };
 
 // bulk copy of `bytes` from this CTA's shared memory to a CTA of the
@@ -147,7 +156,9 @@ __host__ __device__ inline int owned_rows(int q, int tpc, int T)
     return hi > lo ? hi - lo : 0;
 }
 
-template <int KMAX>
+// XP: also write the grouped fp16 rows (a separate instantiation, so that the
+// routing-only code is not touched by it)
+template <int KMAX, bool XP>
 __global__ void __launch_bounds__(THREADS, 1)
 route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const Params p)
@@ -243,6 +254,14 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     } else if (warp >= 2) {
         // ------------------------------------------------ partial logits -> shared memory
         const int quarter = warp & 3;
+        if constexpr (XP) {
+            // the exponents of this CTA's own token rows, while the operands
+            // load and the MMAs run
+            for (int i = warp - 2; i < mine_rows; i += 4) {
+                const int e = fp16_row_exponent(p.x + (size_t)((int)rank * p.tpc + i) * p.d, p.d, lane);
+                if (lane == 0) c.xe[i] = e;
+            }
+        }
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&c.tfull, 0, abort_flag));
         if (!ok) {
             if (lane == 0) flag_status(p.status, kDevTimeout);
@@ -430,6 +449,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     // slot (owned token i, choice j) -> grouped row (routing only: no grouping outputs)
     for (int s = threadIdx.x; p.counts && s < p.tpc * p.k; s += THREADS) {
         const int i = s / p.k, j = s - i * p.k, t = tbase + i;
+        if (XP) c.pos[i][j] = -1;
         if (t >= p.T || c.abort_flag) continue;
         const int e = c.sel_e[i][j];
         const int pos = c.off[e] + c.pre[e] + __popc(c.mask[e] & ((1u << i) - 1u));
@@ -437,6 +457,7 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
             flag_status(p.status, kDevCheckFailed);
             continue;
         }
+        if (XP) c.pos[i][j] = pos;
         p.perm_tok[pos] = t;
         p.inv[(size_t)t * p.k + j] = pos;
         p.perm_w[pos] = c.sel_w[i][j];
@@ -449,6 +470,36 @@ route_small_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         mbar_wait(&c.mx, 0, &no_abort);
     }
     __syncthreads();
+    if (XP && p.counts && !*abort_flag) {
+        // the grouped fp16 rows of this CTA's tokens and their exponents; each
+        // thread issues U loads before it converts and stores any
+        constexpr int U = 8;
+        const int vec = p.d / 8, n = mine_rows * p.k * vec;
+        for (int w0 = threadIdx.x; w0 < n; w0 += THREADS * U) {
+            uint4 u[U];
+            int dst[U], ex[U];
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const int w = w0 + q * THREADS;
+                dst[q] = -1;
+                if (w < n) {
+                    const int sj = w / vec, ch = w - sj * vec;
+                    const int i = sj / p.k, j = sj - i * p.k, pos = c.pos[i][j];
+                    if (pos >= 0) {
+                        u[q] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)(tbase + i) * p.d) + ch);
+                        dst[q] = pos * vec + ch;
+                        ex[q] = c.xe[i];
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                if (dst[q] < 0) continue;
+                reinterpret_cast<uint4 *>(p.xp)[dst[q]] = bf16x8_to_fp16_scaled(u[q], ex[q]);
+                if (dst[q] % vec == 0) p.xexp[dst[q] / vec] = ex[q];
+            }
+        }
+    }
     if (threadIdx.x < R) bulk_wait_read();    // this CTA's outgoing copies have read their sources
     // no CTA leaves while a peer may still copy into it (no memory ordering needed)
     __syncwarp();
@@ -500,10 +551,14 @@ cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream)
     const int dev = current_device();
     if (!attr_done.done(dev)) {
         const int mx = (int)kSmemCap;
-        if ((err = cudaFuncSetAttribute(route_small_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(route_small_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(route_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(route_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess)
+        if ((err = cudaFuncSetAttribute(route_small_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(route_small_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess)
             return err;
         attr_done.mark(dev);
     }
@@ -516,8 +571,15 @@ cudaError_t launch_route_small(const RouteTcArgs &a, cudaStream_t stream)
     p.perm_w = a.perm_w; p.status = a.status; p.out_zero = a.out_zero;
     p.zero_words = a.zero_words; p.n_zero = a.n_zero;
     p.expire_ns = a.expire_ns;
-    auto kern = a.k == 1 ? route_small_kernel<1> : a.k == 2 ? route_small_kernel<2>
-              : a.k <= 4 ? route_small_kernel<4> : route_small_kernel<8>;
+    p.x = static_cast<const uint16_t *>(a.x);
+    // grouped rows: fp16 only (the bf16 decode kernels gather x themselves)
+    if (a.xp && (!a.xp_fp16 || !a.counts || !a.xexp)) return cudaErrorInvalidValue;
+    p.xp = static_cast<uint16_t *>(a.xp);
+    p.xexp = a.xexp;
+    auto kern = p.xp ? (a.k == 1 ? route_small_kernel<1, true> : a.k == 2 ? route_small_kernel<2, true>
+                        : a.k <= 4 ? route_small_kernel<4, true> : route_small_kernel<8, true>)
+                     : (a.k == 1 ? route_small_kernel<1, false> : a.k == 2 ? route_small_kernel<2, false>
+                        : a.k <= 4 ? route_small_kernel<4, false> : route_small_kernel<8, false>);
     err = launch_pdl_cluster(kern, dim3(R), dim3(THREADS), smem, stream, R, m_x, m_w, p);
     if (err != cudaSuccess) return err;
     if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -189,7 +189,10 @@ MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, v
  * consumes them repacked into tiles of 128 rows x 64 columns (one group),
  * 4608 bytes each, so that one k-block of one row tile is one contiguous copy:
  *   tile (rt, g), rt = row / 128, g = col / 64, at byte ((rt * cols/64) + g) * 4608
- *   bytes [0, 4096)       the tile's 128 rows of 32 code bytes, in row order, as above
+ *   bytes [0, 4096)       the tile's 128 rows of 32 code bytes, in row order; each
+ *                         little-endian 32-bit word holds 8 consecutive values,
+ *                         value 2i in bits 4i..4i+3 and value 2i+1 in bits
+ *                         16+4i..19+4i (i = 0..3)
  *   bytes [4096, 4352)    their 128 fp16 scales
  *   bytes [4352, 4608)    their 128 fp16 biases
  * Rows past `rows` in the last row tile are zero.  moe_q4_a64_packed_size

@@ -581,8 +581,9 @@ def test_q4_pack_tile_layout(rows, cols):
     """moe_pack_q4_a64's output, byte for byte, against the tile layout its
     header states, built here from the 36-byte blocks with numpy: tile
     (row // 128, group) at ((row // 128) * groups + group) * 4608 holds the
-    128 rows' 32 code bytes, then their fp16 scales, then their biases; rows
-    past the last are zero."""
+    128 rows' 32 code bytes (each 32-bit word: values 0, 2, 4, 6 in nibbles
+    0-3, values 1, 3, 5, 7 in nibbles 4-7), then their fp16 scales, then their
+    biases; rows past the last are zero."""
     import expert_routed_ffn_selectedsoftmax_gb300 as pkg
     rng = np.random.default_rng(rows + cols)
     w = rng.standard_normal((rows, cols)).astype(np.float32)
@@ -595,7 +596,12 @@ def test_q4_pack_tile_layout(rows, cols):
         for g in range(G):
             t = ((r // 128) * G + g) * 4608
             rr = r % 128
-            want[t + rr * 32:t + rr * 32 + 32] = blocks[r, g, 4:]
+            codes = blocks[r, g, 4:].astype(np.uint32).reshape(8, 4)   # 4 bytes per word
+            lo = codes & 15                                           # values 0, 2, 4, 6
+            hi = codes >> 4                                           # values 1, 3, 5, 7
+            words = (lo << np.array([0, 4, 8, 12], dtype=np.uint32)).sum(1) | \
+                ((hi << np.array([16, 20, 24, 28], dtype=np.uint32)).sum(1))
+            want[t + rr * 32:t + rr * 32 + 32] = words.astype("<u4").view(np.uint8)
             want[t + 4096 + 2 * rr:t + 4098 + 2 * rr] = blocks[r, g, 0:2]
             want[t + 4352 + 2 * rr:t + 4354 + 2 * rr] = blocks[r, g, 2:4]
     assert got.shape == want.shape and np.array_equal(got, want)
