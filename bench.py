@@ -453,11 +453,50 @@ def compute_peak(w, peaks, dev_props, kernels=None):
     return peak_value(peaks, "bf16_tflops"), "tensor", "bf16_tflops"
 
 
+ZIPF_FIXTURE = os.path.join(ROOT, "tests", "golden", "zipf_bias_zonos3_mini_prefill.txt")
+
+
+def zipf_fit(w, T, layers):
+    """The fitted selection biases and Zipf targets of a full-size Zipf
+    workload (tests/golden/zipf_bias_zonos3_mini_prefill.txt, written with
+    the oracle's routing on the layers' host-drawn inputs), or None."""
+    if w.bias != "zipf" or w.name != "zonos3_mini_prefill" or (T is not None and T != w.T) \
+            or not os.path.exists(ZIPF_FIXTURE):
+        return None
+    rec = {}
+    for line in open(ZIPF_FIXTURE):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, layer, *vals = line.split()
+        rec.setdefault(int(layer), {})[key] = np.array([float(v) for v in vals])
+    if any(i not in rec for i in range(layers)):
+        return None
+    return [rec[i]["bias"].astype(np.float32) for i in range(layers)], \
+        [rec[i]["target"] for i in range(layers)]
+
+
+def zipf_report(targets, counts_per_layer):
+    """Achieved loads (the layer's own routing, read back) against the Zipf
+    targets: head share, tail, and the fraction of assignments off target."""
+    out = []
+    for tgt, cnt in zip(targets, counts_per_layer):
+        cnt = np.asarray(cnt, dtype=np.float64)
+        order = np.argsort(-tgt)
+        out.append({"top_share": float(cnt[order[0]] / cnt.sum()),
+                    "top_share_target": float(tgt[order[0]] / tgt.sum()),
+                    "bottom_rows": int(cnt[order[-1]]), "bottom_rows_target": float(tgt[order[-1]]),
+                    "off_target_frac": float(np.abs(cnt - tgt).sum() / cnt.sum())})
+    return out
+
+
 def setup_stack(pkg, wl, w, T, layers, seed, dev):
     """Device stack of `layers` layers of workload w (block-quantised weights
-    repacked once), plus the dtypes moe_forward takes."""
+    repacked once), plus the dtypes moe_forward takes.  A full-size Zipf
+    workload takes its fitted biases and the inputs they were fitted on."""
     import torch
-    stack = wl.make_device_stack(w, seed=seed, layers=layers, T=T, device=dev)
+    fit = zipf_fit(w, T, layers)
+    stack = wl.make_device_stack(w, seed=seed, layers=layers, T=T, device=dev,
+                                 zipf_biases=fit[0] if fit else None)
     act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
     w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0,
             wl.Q4_A64: pkg.MOE_Q4_A64}[w.w_dtype]
@@ -669,6 +708,9 @@ def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, pea
            "layer": layer_stats(w, alg, ms, layers, peaks, dev_props, stage, names),
            "roofline": roofline_of(w, T, layers, alg, stage, names, peaks, peak_src, dev_props),
            "gpu_launches_per_layer": names["launches"]}
+    fit = zipf_fit(w, T, layers)
+    if fit:   # the fitted Zipf loads, as this run's own routing produced them
+        res["zipf_loads"] = zipf_report(fit[1], counts)
     if with_oracle:
         host = host_layer_from_device(w, r.stack[0], T)
         res["cpu_baseline"] = oracle_baseline([host], sample_rows)
@@ -937,6 +979,8 @@ def main():
         "roofline": roofline, "cpu_baseline": cpu, "step_ms": step_dist,
         "layer": layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us, names),
         "workloads": side,
+        "zipf_loads": (zipf_report(zipf_fit(w, T, layers)[1], counts_per_layer)
+                       if zipf_fit(w, T, layers) else None),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

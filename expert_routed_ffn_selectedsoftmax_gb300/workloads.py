@@ -37,12 +37,17 @@ Q4_A64_BLOCK_BYTES = 36
 Q8_0_BLOCK = 32
 Q8_0_BLOCK_BYTES = 34
 
-# Scale on log(p_rank) for the Zipf-skewed workload.  With router logits close
-# to N(0, 1), 0.65 puts ~25% of the top-2 assignments on the busiest expert,
-# the head share of Zipf(s=1.1) over 64 ranks; the tail falls off faster than
-# Zipf.  The achieved per-expert counts are reported with every measurement.
+# Scale on log(p_rank) for the Zipf-skewed workload's analytic bias (used
+# where no fitted bias exists: other sizes and seeds).  With router logits
+# close to N(0, 1), 0.65 puts ~25% of the top-2 assignments on the busiest
+# expert, the head share of Zipf(s=1.1) over 64 ranks; the tail falls off
+# faster than Zipf.  The benchmark's full-size Zipf layers instead use a bias
+# fitted to their own inputs (zipf_host_inputs; fitted with the oracle's
+# routing by tests/golden/fit_zipf_bias.py) so that the loads follow
+# Zipf(s=1.1) over all ranks.
 ZIPF_S = 1.1
 ZIPF_ALPHA = 0.65
+ZIPF_HOST_SEED = 7100   # host seed of layer i's x and W_r: ZIPF_HOST_SEED + i
 
 
 @dataclasses.dataclass(frozen=True)
@@ -211,6 +216,24 @@ def zipf_bias(E: int, rng: np.random.Generator, s: float = ZIPF_S,
     return b.astype(np.float32)
 
 
+def zipf_targets(E: int, T: int, k: int, s: float = ZIPF_S) -> np.ndarray:
+    """Target assignments per rank: T*k * r^-s / sum_r r^-s, r = 1..E."""
+    p = np.arange(1, E + 1, dtype=np.float64) ** (-s)
+    return T * k * p / p.sum()
+
+
+def zipf_host_inputs(w: Workload, layer: int):
+    """Layer `layer` of a full-size Zipf workload, drawn on the host: x [T, d]
+    and W_r [E, d] as float32 (same distributions as make_layer) and the
+    seeded permutation order[r] = expert holding rank r + 1."""
+    rng = np.random.default_rng(ZIPF_HOST_SEED + layer)
+    f32 = np.float32
+    x = rng.standard_normal((w.T, w.d), dtype=f32)
+    wr = rng.standard_normal((w.E, w.d), dtype=f32) * f32(1.0 / math.sqrt(w.d))
+    order = rng.permutation(w.E)
+    return x, wr, order
+
+
 def make_layer(w: Workload, seed: int, T: Optional[int] = None,
                d: Optional[int] = None, E: Optional[int] = None,
                k: Optional[int] = None, F: Optional[int] = None) -> Layer:
@@ -302,14 +325,16 @@ def q4_a64_quantize_torch(w):
 
 
 def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = None,
-                      device="cuda"):
+                      device="cuda", zipf_biases=None):
     """Draw ``layers`` independent layers directly in device memory.
 
     Used for benchmark stacks whose weights (GBs) are too large to draw on the
     host.  Same distributions as make_layer, drawn with torch's seeded device
     generator; returns a list of dicts of torch tensors: x / W_r as
     torch.bfloat16, expert weights as torch.bfloat16 or, for Q8_0 workloads,
-    uint8 Q8_0 blocks [E, rows, cols/32, 34].
+    uint8 Q8_0 blocks [E, rows, cols/32, 34].  ``zipf_biases`` (a Zipf
+    workload at its full size): per layer, a selection bias fitted to the
+    layer's host-drawn x and W_r (zipf_host_inputs), which are used then.
     """
     import torch
     if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (F32, F32)):
@@ -329,7 +354,12 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
         d, E, F = w.d, w.E, w.F
         x = rn(T, d)
         wr = rn(E, d, sd=1.0 / math.sqrt(d))
-        if w.bias == "zipf":
+        if zipf_biases is not None and w.bias == "zipf" and T == w.T:
+            hx, hwr, _ = zipf_host_inputs(w, layer)
+            x = torch.from_numpy(hx).to(device).to(act)
+            wr = torch.from_numpy(hwr).to(device).to(act)
+            b = torch.from_numpy(np.asarray(zipf_biases[layer], dtype=np.float32)).to(device)
+        elif w.bias == "zipf":
             rng = np.random.default_rng(seed * 1000003 + layer)
             b = torch.from_numpy(zipf_bias(E, rng)).to(device)
         else:
