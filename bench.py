@@ -216,9 +216,9 @@ def expert_kernel_names(w, T, num_sms):
     timed as one stage."""
     rows = T * w.k
     act16 = w.act_dtype == 1
-    if (act16 and w.w_dtype in (1, 2) and w.d % 256 == 0 and w.F % 128 == 0
+    if (act16 and w.w_dtype in (1, 2, 3) and w.d % 256 == 0 and w.F % 128 == 0
             and rows >= 64 * w.E and T >= 512):
-        q = "Q8_0, CTA pairs" if w.w_dtype == 2 else "bf16"
+        q = {1: "bf16", 2: "Q8_0, CTA pairs", 3: "4-bit, CTA pairs"}[w.w_dtype]
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4, "fused": False}
     if act16 and w.w_dtype in (1, 3) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
@@ -675,7 +675,9 @@ def layer_stats(w, alg, ms_per_step, layers, peaks, dev_props, stage_us, names=N
 # layers, oracle token sample per layer).
 SIDE_WORKLOADS = [("tiny_fp32", None, None, 8), ("zonos2_decode", 1, None, 1),
                   ("zonos2_decode", 8, None, 8), ("zonos2_decode", 64, None, 64),
-                  ("zonos3_mini_prefill", None, None, 512), ("zonos2_prefill_q8", None, None, 192)]
+                  ("zonos3_mini_prefill", None, None, 512), ("zonos2_prefill_q8", None, None, 192),
+                  ("zonos2_decode_q4", 1, None, 1), ("zonos2_decode_q4", 8, None, 8),
+                  ("zonos2_decode_q4", 64, None, 64), ("zonos2_prefill_q4", None, None, 192)]
 
 
 def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, peak_src,

@@ -56,8 +56,8 @@ struct WsLayout {
 
 bool prefill_capable(int act_dt, int w_dt, int d, int F)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q8_0) && d % 256 == 0 &&
-           F % 128 == 0;
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64) &&
+           d % 256 == 0 && F % 128 == 0;
 }
 
 WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
@@ -85,9 +85,9 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     // k > 2: weighted expert outputs per grouped row, combined in slot order
     // (the CUDA-core decode kernels and the grouped GEMMs)
     L.y = k > 2 ? take(4 * n * (size_t)d) : off;
-    // Q8_0 grouped GEMMs and 4-bit tensor-core decode: exponent of each fp16
-    // grouped row's scale
-    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt == MOE_Q8_0) || (L.dtc && w_dt == MOE_Q4_A64))
+    // Q8_0 / 4-bit grouped GEMMs and 4-bit tensor-core decode: exponent of
+    // each fp16 grouped row's scale
+    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt != MOE_BF16) || (L.dtc && w_dt == MOE_Q4_A64))
                  ? take(4 * n) : off;
     L.n_flags = 0;
     if (L.dtc) {

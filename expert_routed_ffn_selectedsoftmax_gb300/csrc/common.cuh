@@ -149,6 +149,30 @@ __host__ __device__ __forceinline__ size_t q4_tile_offset(long long row, int g, 
     return ((size_t)(row / kQ4TileRows) * (size_t)groups + (size_t)g) * kQ4TileBytes;
 }
 
+// One 32-bit word of packed codes (8 consecutive values, q4_nibble order) ->
+// 8 fp16 values scale * q + bias in K order.  Masked under the fp16 exponent
+// of 1024 (ulp 1), nibbles 0 and 4 give the pair (1024 + q_0, 1024 + q_1) and
+// nibbles 1 and 5, left in bits 4-7 of each half, (1024 + 16 q_2, 1024 + 16
+// q_3); the word shifted by 8 gives values 4-7 the same way.  One exact fma by
+// (1, 1) or (1/16, 1/16) and the matching offset leaves the codes, a second
+// one gives scale * q + bias with a single rounding.
+__device__ __forceinline__ uint32_t q4_pair_fp16(uint32_t t, __half2 mul, __half2 add, __half2 sc2, __half2 bi2)
+{
+    t |= 0x64006400u;
+    const __half2 v = __hfma2(__hfma2(*reinterpret_cast<const __half2 *>(&t), mul, add), sc2, bi2);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ uint4 q4_word_fp16x8(uint32_t w, __half2 sc2, __half2 bi2)
+{
+    const __half2 one2 = __float2half2_rn(1.0f), m1024 = __float2half2_rn(-1024.0f);
+    const __half2 sixteenth2 = __float2half2_rn(0.0625f), m64 = __float2half2_rn(-64.0f);
+    const uint32_t w8 = w >> 8;
+    return make_uint4(q4_pair_fp16(w & 0x000F000Fu, one2, m1024, sc2, bi2),
+                      q4_pair_fp16(w & 0x00F000F0u, sixteenth2, m64, sc2, bi2),
+                      q4_pair_fp16(w8 & 0x000F000Fu, one2, m1024, sc2, bi2),
+                      q4_pair_fp16(w8 & 0x00F000F0u, sixteenth2, m64, sc2, bi2));
+}
+
 template <> struct WView<Q4Tag> {
     const uint8_t *q;     // packed tiles
     int groups;           // cols / 64

@@ -438,23 +438,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         // a warp may access only the TMEM lanes of its quadrant (warp % 4): warp w
         // converts rows 32 (w % 4) .. +31 of every weight tile, lane = row:
         // 64 codes -> scale * q + bias in fp16 -> 32 columns of its TMEM lane.
-        // A 32-bit word of codes holds values 0, 2, 4, 6 of its 8 in nibbles 0-3
-        // and values 1, 3, 5, 7 in nibbles 4-7 (q4_nibble).  Masked under the
-        // fp16 exponent of 1024 (ulp 1), nibbles 0 and 4 give the pair (1024 +
-        // q_0, 1024 + q_1) and nibbles 1 and 5, left in bits 4-7 of each half,
-        // (1024 + 16 q_2, 1024 + 16 q_3); the word shifted by 8 gives values 4-7
-        // the same way.  One exact fma by (1, 1) or (1/16, 1/16) and the matching
-        // offset leaves the codes, a second one gives scale * q + bias with a
-        // single rounding.
+        // (q4_word_fp16x8: one packed word -> 8 fp16 weights, two exact fma steps)
         const int quad = warp & 3, row = quad * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + A_COL4;
-        const __half2 one2 = __float2half2_rn(1.0f), m1024 = __float2half2_rn(-1024.0f);
-        const __half2 sixteenth2 = __float2half2_rn(0.0625f), m64 = __float2half2_rn(-64.0f);
-        auto pair = [](uint32_t t, __half2 mul, __half2 add, __half2 sc2, __half2 bi2) {
-            t |= 0x64006400u;
-            const __half2 v = __hfma2(__hfma2(*reinterpret_cast<const __half2 *>(&t), mul, add), sc2, bi2);
-            return *reinterpret_cast<const uint32_t *>(&v);
-        };
         uint32_t it_k = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -478,11 +464,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     uint32_t o[32];   // column c: values 2c, 2c+1
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {   // values 8ch .. 8ch+7
-                        const uint32_t w8 = w[ch] >> 8;
-                        o[4 * ch + 0] = pair(w[ch] & 0x000F000Fu, one2, m1024, sc2, bi2);
-                        o[4 * ch + 1] = pair(w[ch] & 0x00F000F0u, sixteenth2, m64, sc2, bi2);
-                        o[4 * ch + 2] = pair(w8 & 0x000F000Fu, one2, m1024, sc2, bi2);
-                        o[4 * ch + 3] = pair(w8 & 0x00F000F0u, sixteenth2, m64, sc2, bi2);
+                        const uint4 v = q4_word_fp16x8(w[ch], sc2, bi2);
+                        o[4 * ch + 0] = v.x; o[4 * ch + 1] = v.y; o[4 * ch + 2] = v.z; o[4 * ch + 3] = v.w;
                     }
                     tmem_st16(t_lane + cb * 64 + j * 32, *reinterpret_cast<const uint32_t(*)[16]>(&o[0]));
                     tmem_st16(t_lane + cb * 64 + j * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o[16]));

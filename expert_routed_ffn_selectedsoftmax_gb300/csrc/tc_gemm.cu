@@ -35,7 +35,14 @@
 // fp16 scale -- in one of CVT converted-B buffers, and the MMA runs kind::f16
 // with fp16 operands (the grouped rows and h are fp16 on this path).
 //
-// CTA pairs (PAIR, used for Q8_0): two CTAs of a cluster share one tile of
+// Affine 4-bit weights (the experts of the MLX build, "Zyphra-ZONOS2-4bit",
+// §How this was quantized: 4 bits, groups of 64, affine): the B stage holds
+// this CTA's packed 128-row tiles (codes, fp16 scales and biases; one
+// contiguous copy each) and the same converter warps turn them into fp16,
+// scale * q + bias rounded once (q4_word_fp16x8), on the Q8_0 path's fp16
+// operands and pairs.
+//
+// CTA pairs (PAIR, used for Q8_0 and 4-bit): two CTAs of a cluster share one tile of
 // 256 grouped rows x 256 columns through tcgen05.mma.cta_group::2 (M = 256):
 // each CTA loads its own 128 rows of A and one half of B (GATEUP: the gate
 // rows in the even CTA, the up rows in the odd one; DOWN: columns 0-127 /
@@ -104,15 +111,20 @@ constexpr int kConvWarps = MOE_GEMM_CONV_WARPS;   // Q8_0 converter warps (4 or 
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 
+// Weight storage of a variant: 16-bit, Q8_0 or affine 4-bit (the last two
+// through converter warps).
+enum WKind { W16 = 0, WQ8 = 1, WQ4 = 2 };
+
 // Per-variant shared-memory layout: a ring of STAGES stages {A, this CTA's
-// part of B (16-bit) or of Bq (int8) + its scales}, then (Q8 only) CVT
-// converted fp16 B buffers, then the control block.
-template <bool Q8, bool PAIR> struct Cfg {
+// part of B (16-bit), of Bq (int8) + its scales, or its packed 4-bit tiles},
+// then (converted kinds) CVT converted fp16 B buffers, then the control block.
+template <int WQ, bool PAIR> struct Cfg {
+    static constexpr bool Q8 = WQ != W16;           // converted weights (Q8_0 or 4-bit)
     static constexpr int CL = PAIR ? 2 : 1;
     static constexpr int BNL = BN / CL;             // B rows held by this CTA
     static constexpr int B_BYTES = BNL * BK * 2;    // 16-bit B (this CTA's rows)
-    static constexpr int BQ_BYTES = BNL * BK;       // int8 B
-    static constexpr int SCL_BYTES = SC_BYTES / CL; // its scales
+    static constexpr int BQ_BYTES = WQ == WQ4 ? (BNL / kQ4TileRows) * kQ4TileBytes : BNL * BK;   // packed B
+    static constexpr int SCL_BYTES = WQ == WQ4 ? 0 : SC_BYTES / CL;   // Q8_0 scales
     static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SCL_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
     static constexpr int STAGES = Q8 ? (PAIR ? MOE_GEMM_PAIR_Q8_STAGES : MOE_GEMM_Q8_STAGES) : (PAIR ? 6 : 4);
@@ -143,7 +155,8 @@ struct Params {
     float *y;                 // DOWN, k > 2: [rows, d] weighted outputs per grouped row
     uint32_t *status;
     int h_fp16;               // GATEUP: write h as fp16 (else bf16)
-    const int32_t *xexp;      // fp16 rows (Q8_0): row r of the grouped x is scaled by 2^-xexp[r];
+    const uint8_t *q4[3];     // 4-bit: packed tiles of W_g, W_u, W_d
+    const int32_t *xexp;      // fp16 rows (Q8_0, 4-bit): row r of the grouped x is scaled by 2^-xexp[r];
                               // h is written scaled by 2^-2 xexp[r], undone in the down epilogue
     float *out_zero;          // GATEUP: `out` to zero for the down kernel's adds, or null
     long long zero4;          // float4 elements of out_zero
@@ -228,15 +241,16 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane)
 
 // tm_s0/tm_s1 (Q8 only): the B matrices' fp16 scale planes [cols/32, rows],
 // box {128 rows, 2 blocks}.
-template <int MODE, bool Q8, bool PAIR>
-__global__ void __launch_bounds__(Cfg<Q8, PAIR>::THREADS, 1)
+template <int MODE, int WQ, bool PAIR>
+__global__ void __launch_bounds__(Cfg<WQ, PAIR>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b0,
                     const __grid_constant__ CUtensorMap tm_b1,
                     const __grid_constant__ CUtensorMap tm_s0,
                     const __grid_constant__ CUtensorMap tm_s1, const Params p)
 {
-    using C = Cfg<Q8, PAIR>;
+    using C = Cfg<WQ, PAIR>;
+    constexpr bool Q8 = C::Q8;   // converted weights (Q8_0 or 4-bit)
     constexpr int CL = C::CL, STAGES = C::STAGES, BNL = C::BNL;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -354,6 +368,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 }
                 mbar_expect_tx(&c.full[s], A_BYTES + (Q8 ? C::BQ_BYTES + C::SCL_BYTES : C::B_BYTES));
                 tma_load_2d(st, &tm_a, &c.full[s], kb * BK, arow);
+                if constexpr (WQ == WQ4) {
+                    // this CTA's packed 128-row tiles of k-block kb, one copy each
+                    const int groups = p.K / 64;
+                    if (MODE == GATEUP) {
+                        if (PAIR) {
+                            bulk_load(sb, p.q4[rank] + q4_tile_offset(grow, kb, groups), kQ4TileBytes, &c.full[s]);
+                        } else {
+                            bulk_load(sb, p.q4[0] + q4_tile_offset(grow, kb, groups), kQ4TileBytes, &c.full[s]);
+                            bulk_load(sb + kQ4TileBytes, p.q4[1] + q4_tile_offset(grow, kb, groups), kQ4TileBytes,
+                                      &c.full[s]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < BNL / kQ4TileRows; ++t)
+                            bulk_load(sb + t * kQ4TileBytes, p.q4[2] + q4_tile_offset(drow + t * kQ4TileRows, kb, groups),
+                                      kQ4TileBytes, &c.full[s]);
+                    }
+                    continue;
+                }
                 if (MODE == GATEUP) {
                     if (PAIR) {
                         const CUtensorMap *bm = rank ? &tm_b1 : &tm_b0;
@@ -394,7 +427,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         }
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ------------------------------------------------ MMA issuer (CTA 0 of a pair)
-        // fp16 operands on the Q8_0 path (grouped rows and h are fp16), else bf16
+        // fp16 operands on the Q8_0 and 4-bit paths (grouped rows and h are fp16), else bf16
         const uint32_t idesc = idesc_f16_mn(Q8 ? 1 : 0, BM * CL, BN);
         uint32_t it = 0, local_tile = 0;
         bool ok = true;
@@ -465,6 +498,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 const uint8_t *bq = smem + s * C::STAGE + A_BYTES;
                 const __half *scl = reinterpret_cast<const __half *>(bq + C::BQ_BYTES);
                 uint8_t *bo = sCvt + cb * C::B_BYTES;
+                if constexpr (WQ == WQ4) {
+                    // lane: row rsub of an 8-row pass, values 16q .. 16q+15 (two words)
+#pragma unroll
+                    for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
+                        const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
+                        const uint8_t *t = bq + (r / kQ4TileRows) * kQ4TileBytes;
+                        const int rr = r % kQ4TileRows;
+                        const uint2 v = *reinterpret_cast<const uint2 *>(t + rr * 32 + q * 8);
+                        const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(t + kQ4ScaleOff)[rr]);
+                        const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(t + kQ4BiasOff)[rr]);
+                        *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q) ^ (r & 7)) << 4)) =
+                            q4_word_fp16x8(v.x, sc2, bi2);
+                        *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4)) =
+                            q4_word_fp16x8(v.y, sc2, bi2);
+                    }
+                    fence_proxy_async_smem();
+                    warp_arrive<PAIR>(&c.cfull[cb], lane);
+                    continue;
+                }
 #pragma unroll
                 for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
                     const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
@@ -635,14 +687,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     }
 }
 
-template <bool Q8, bool PAIR> constexpr size_t smem_bytes()
+template <int WQ, bool PAIR> constexpr size_t smem_bytes()
 {
     // ring (+ converted B buffers), control block, down-epilogue staging
-    return 1024 + Cfg<Q8, PAIR>::CTL + sizeof(SmemCtl) + kStgBytes;
+    return 1024 + Cfg<WQ, PAIR>::CTL + sizeof(SmemCtl) + kStgBytes;
 }
 static_assert(sizeof(SmemCtl) % 16 == 0, "the staging rows after the control block take float4 stores");
-static_assert(smem_bytes<false, true>() <= 232448 && smem_bytes<true, true>() <= 232448 &&
-                  smem_bytes<false, false>() <= 232448 && smem_bytes<true, false>() <= 232448,
+static_assert(smem_bytes<W16, true>() <= 232448 && smem_bytes<WQ8, true>() <= 232448 &&
+                  smem_bytes<W16, false>() <= 232448 && smem_bytes<WQ8, false>() <= 232448 &&
+                  smem_bytes<WQ4, true>() <= 232448 && smem_bytes<WQ4, false>() <= 232448,
               "shared memory per CTA");
 
 // ------------------------------------------------------------------- host
@@ -697,7 +750,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 }  // namespace tc
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
-bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || w_dt == MOE_Q8_0; }
+bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64; }
 
 bool tc_gemm_prefer(int T, int d, int E, int k, int F)
 {
@@ -706,18 +759,18 @@ bool tc_gemm_prefer(int T, int d, int E, int k, int F)
     return (long long)T * k >= 64LL * E && T >= 512;
 }
 
-template <bool Q8, bool PAIR>
+template <int WQ, bool PAIR>
 static cudaError_t set_smem_attrs()
 {
     using namespace tc;
     static PerDeviceFlag done;
     const int dev = current_device();
     if (done.done(dev)) return cudaSuccess;
-    const int smem = (int)smem_bytes<Q8, PAIR>();
+    const int smem = (int)smem_bytes<WQ, PAIR>();
     cudaError_t err;
-    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, Q8, PAIR>,
+    if ((err = cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP, WQ, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, Q8, PAIR>,
+        (err = cudaFuncSetAttribute(grouped_gemm_kernel<DOWN, WQ, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return err;
     done.mark(dev);
@@ -726,7 +779,7 @@ static cudaError_t set_smem_attrs()
 
 // Clusters of two CTAs (pair kernels) that can be resident at once (0 if the
 // query fails).
-template <int MODE, bool Q8>
+template <int MODE, int WQ>
 static int max_active_pairs()
 {
     using namespace tc;
@@ -735,15 +788,15 @@ static int max_active_pairs()
     int n = cached.get(dev);
     if (n >= 0) return n;
     // the query needs the kernel's dynamic shared-memory limit raised first
-    if (set_smem_attrs<Q8, true>() != cudaSuccess) {
+    if (set_smem_attrs<WQ, true>() != cudaSuccess) {
         cudaGetLastError();
         cached.put(dev, 0);
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * device_sm_count());
-    cfg.blockDim = dim3(Cfg<Q8, true>::THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<Q8, true>();
+    cfg.blockDim = dim3(Cfg<WQ, true>::THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<WQ, true>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -751,7 +804,7 @@ static int max_active_pairs()
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, Q8, true>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, WQ, true>, &cfg) != cudaSuccess)
         n = 0;
     cudaGetLastError();   // clear a failed query
     cached.put(dev, n);
@@ -760,15 +813,17 @@ static int max_active_pairs()
 
 bool tc_gemm_pairs(moe_dtype w_dt)
 {
-    const bool q8 = w_dt == MOE_Q8_0;
-    if (MOE_GEMM_PAIR == 0 || (MOE_GEMM_PAIR == 1 && !q8)) return false;
+    const bool q8 = w_dt == MOE_Q8_0, q4 = w_dt == MOE_Q4_A64;
+    if (MOE_GEMM_PAIR == 0 || (MOE_GEMM_PAIR == 1 && !q8 && !q4)) return false;
     if constexpr (MOE_GEMM_PAIR >= 2) {
-        if (!q8) return max_active_pairs<tc::GATEUP, false>() > 0 && max_active_pairs<tc::DOWN, false>() > 0;
+        if (!q8 && !q4)
+            return max_active_pairs<tc::GATEUP, tc::W16>() > 0 && max_active_pairs<tc::DOWN, tc::W16>() > 0;
     }
-    return q8 && max_active_pairs<tc::GATEUP, true>() > 0 && max_active_pairs<tc::DOWN, true>() > 0;
+    if (q4) return max_active_pairs<tc::GATEUP, tc::WQ4>() > 0 && max_active_pairs<tc::DOWN, tc::WQ4>() > 0;
+    return q8 && max_active_pairs<tc::GATEUP, tc::WQ8>() > 0 && max_active_pairs<tc::DOWN, tc::WQ8>() > 0;
 }
 
-template <bool Q8, bool PAIR>
+template <int WQ, bool PAIR>
 static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap &m_xp,
                                 const CUtensorMap &m_wg, const CUtensorMap &m_wu,
                                 const CUtensorMap &m_h, const CUtensorMap &m_wd,
@@ -776,9 +831,9 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
                                 const CUtensorMap &m_sd, cudaStream_t stream)
 {
     using namespace tc;
-    constexpr int CL = Cfg<Q8, PAIR>::CL;
+    constexpr int CL = Cfg<WQ, PAIR>::CL;
     cudaError_t err;
-    if ((err = set_smem_attrs<Q8, PAIR>()) != cudaSuccess) return err;
+    if ((err = set_smem_attrs<WQ, PAIR>()) != cudaSuccess) return err;
     const int rows = a.T * a.k;
     // upper bound on units: every expert could own a ragged group of CL m-tiles
     const long long max_groups = rows / (BM * CL) + (a.E < rows ? a.E : rows);
@@ -786,28 +841,28 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
         long long cl = units < max_clusters ? units : max_clusters;
         return dim3((unsigned)((cl < 1 ? 1 : cl) * CL));
     };
-    const size_t smem = smem_bytes<Q8, PAIR>();
-    const dim3 block(Cfg<Q8, PAIR>::THREADS);
+    const size_t smem = smem_bytes<WQ, PAIR>();
+    const dim3 block(Cfg<WQ, PAIR>::THREADS);
 
     p.K = a.d; p.n_tiles = a.F / (BN / 2);
-    const dim3 g1 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<GATEUP, Q8>() : a.num_sms);
+    const dim3 g1 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<GATEUP, WQ>() : a.num_sms);
     if (PAIR)
-        err = launch_pdl_cluster(grouped_gemm_kernel<GATEUP, Q8, PAIR>, g1, block, smem, stream, CL,
+        err = launch_pdl_cluster(grouped_gemm_kernel<GATEUP, WQ, PAIR>, g1, block, smem, stream, CL,
                                  m_xp, m_wg, m_wu, m_sg, m_su, p);
     else
-        err = launch_pdl(grouped_gemm_kernel<GATEUP, Q8, PAIR>, g1, block, smem, stream, m_xp, m_wg,
+        err = launch_pdl(grouped_gemm_kernel<GATEUP, WQ, PAIR>, g1, block, smem, stream, m_xp, m_wg,
                          m_wu, m_sg, m_su, p);
     if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess) return err;
     if (a.ev_gateup && (err = cudaEventRecord(a.ev_gateup, stream)) != cudaSuccess) return err;
 
     p.K = a.F; p.n_tiles = a.d / BN;
     p.expire_ns = 0;   // (the hook acts on the gate/up kernel only)
-    const dim3 g2 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<DOWN, Q8>() : a.num_sms);
+    const dim3 g2 = grid_for(max_groups * p.n_tiles, PAIR ? max_active_pairs<DOWN, WQ>() : a.num_sms);
     if (PAIR)
-        err = launch_pdl_cluster(grouped_gemm_kernel<DOWN, Q8, PAIR>, g2, block, smem, stream, CL, m_h,
+        err = launch_pdl_cluster(grouped_gemm_kernel<DOWN, WQ, PAIR>, g2, block, smem, stream, CL, m_h,
                                  m_wd, m_wd, m_sd, m_sd, p);
     else
-        err = launch_pdl(grouped_gemm_kernel<DOWN, Q8, PAIR>, g2, block, smem, stream, m_h, m_wd, m_wd,
+        err = launch_pdl(grouped_gemm_kernel<DOWN, WQ, PAIR>, g2, block, smem, stream, m_h, m_wd, m_wd,
                          m_sd, m_sd, p);
     if (err != cudaSuccess || (err = cudaGetLastError()) != cudaSuccess || a.k <= 2) return err;
     return launch_combine_rows(a.y, a.d, a.inv, a.T, a.k, a.out, a.status, a.num_sms, stream);
@@ -816,12 +871,13 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
 {
     using namespace tc;
-    const bool q8 = a.w_dt == MOE_Q8_0;
-    if (!q8 && a.w_dt != MOE_BF16) return cudaErrorNotSupported;
+    const bool q8 = a.w_dt == MOE_Q8_0, q4 = a.w_dt == MOE_Q4_A64;
+    const bool f16 = q8 || q4;   // fp16 operands (converted weights)
+    if (!f16 && a.w_dt != MOE_BF16) return cudaErrorNotSupported;
     const int rows = a.T * a.k;
     cudaError_t err = cudaSuccess;
     if (!a.xp_ready &&
-        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, q8 ? 1 : 0, a.xexp, a.num_sms, stream)) !=
+        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, f16 ? 1 : 0, a.xexp, a.num_sms, stream)) !=
             cudaSuccess)
         return err;
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
@@ -829,13 +885,15 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     // pairs of CTAs when clusters of two can be resident, else single CTAs
     const bool pair = tc_gemm_pairs(a.w_dt);
 
-    // activations: bf16, or fp16 on the Q8_0 path
-    const CUtensorMapDataType act = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // activations: bf16, or fp16 on the Q8_0 and 4-bit paths
+    const CUtensorMapDataType act = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t gu_rows = (uint64_t)a.E * a.F, d_rows = (uint64_t)a.E * a.d;
     const uint32_t wd_box = (uint32_t)(pair ? BN / 2 : BN);   // each CTA of a pair: 128 rows of W_d
     CUtensorMap m_xp, m_wg, m_wu, m_h, m_wd;
     bool ok = make_map(&m_xp, a.xp, rows, a.d, BM, act) && make_map(&m_h, a.h, rows, a.F, BM, act);
-    if (q8) {
+    if (q4) {
+        m_wg = m_wu = m_wd = m_xp;   // unused: the 4-bit tiles are contiguous copies
+    } else if (q8) {
         ok = ok && make_map_u8(&m_wg, a.w_gate, gu_rows, a.d, BN / 2) &&
              make_map_u8(&m_wu, a.w_up, gu_rows, a.d, BN / 2) &&
              make_map_u8(&m_wd, a.w_down, d_rows, a.F, wd_box);
@@ -868,19 +926,25 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k;
     p.h = static_cast<uint16_t *>(a.h); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
-    p.out = a.out; p.y = a.y; p.status = a.status; p.h_fp16 = q8 ? 1 : 0;
-    p.xexp = q8 ? a.xexp : nullptr;
+    p.out = a.out; p.y = a.y; p.status = a.status; p.h_fp16 = f16 ? 1 : 0;
+    p.xexp = f16 ? a.xexp : nullptr;
+    p.q4[0] = static_cast<const uint8_t *>(a.w_gate);
+    p.q4[1] = static_cast<const uint8_t *>(a.w_up);
+    p.q4[2] = static_cast<const uint8_t *>(a.w_down);
     p.out_zero = a.zero_out ? a.out : nullptr;
     p.zero4 = (long long)a.T * a.d / 4;
     p.expire_ns = a.expire_ns;
+    if (q4)
+        return pair ? launch_gemms<WQ4, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                    : launch_gemms<WQ4, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
     if (q8)
-        return pair ? launch_gemms<true, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
-                    : launch_gemms<true, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+        return pair ? launch_gemms<WQ8, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                    : launch_gemms<WQ8, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
     if constexpr (MOE_GEMM_PAIR >= 2) {
         if (pair)
-            return launch_gemms<false, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+            return launch_gemms<W16, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
     }
-    return launch_gemms<false, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+    return launch_gemms<W16, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
 }
 
 }  // namespace moe

@@ -100,6 +100,13 @@ WORKLOADS = {
         description="ZONOS2-shaped decode step with affine 4-bit group-64 experts "
                     "(the format of the pages' MLX figures): d=2048, E=16, top-1, "
                     "F=2816, T in {1, 8, 64}, 28-layer weight rotation"),
+    "zonos2_prefill_q4": Workload(
+        "zonos2_prefill_q4", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q4_A64, bias="normal", bias_sd=0.1, layers=4,
+        description="ZONOS2-shaped prefill with affine 4-bit group-64 experts (the "
+                    "MLX build's expert format): T=4096, d=2048, E=16, top-1, "
+                    "F=2816, bf16 activations and router (4 independent layers "
+                    "per benchmark step)"),
 }
 
 

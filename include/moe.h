@@ -180,9 +180,9 @@ MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, v
  * cols/64 blocks of 36 bytes {fp16 scale, fp16 bias (little endian), 32 bytes
  * of codes: value 2j in the low nibble of byte j, 2j+1 in the high nibble};
  * value = scale * q + bias.  Used with BF16 activations on the tensor-core
- * decode kernels (d and F multiples of 128) or the CUDA-core decode kernels
- * (MOE_PATH_PREFILL returns MOE_ERR_UNSUPPORTED).  The tensor-core kernels
- * multiply fp16 operands: each weight is scale * q + bias rounded once to
+ * decode kernels (d and F multiples of 128), the grouped GEMMs of
+ * MOE_PATH_PREFILL (d % 256 == 0, F % 128 == 0) or the CUDA-core decode
+ * kernels.  The tensor-core kernels multiply fp16 operands: each weight is scale * q + bias rounded once to
  * fp16, each token row is x times a power of two (exact), and h is held in
  * fp16 scaled by the square of that power, as on the Q8_0 path; an h beyond
  * fp16's range there is reported as MOE_ERR_DEVICE_CHECK.  moe_forward

@@ -99,7 +99,7 @@ def test_argument_errors_are_synchronous(lib):
     assert fwd(act=0, wdt=1) == U                # f32 activations with bf16 weights
     assert fwd(wdt=2, F=136) == I                # Q8_0 needs F % 32
     assert fwd(wdt=3, F=160) == I                # affine 4-bit needs F % 64
-    assert fwd(wdt=3, path=2) == U               # no prefill GEMMs for affine 4-bit
+    assert fwd(wdt=3, d=192, path=2) == U        # affine 4-bit prefill GEMMs need d % 256
     assert fwd(act=0, wdt=3) == U                # affine 4-bit takes bf16 activations
     assert lib.moe_pack_q4_a64(fake, 4, 96, fake, None) == I      # cols % 64
     assert lib.moe_pack_q4_a64(fake, 4, 128, vp(0x10010), None) == I

@@ -242,7 +242,7 @@ def test_device_status_ok_after_forward():
 FULL_CASES = [("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode", 1),
               ("zonos2_decode", 8), ("zonos2_decode", 64), ("zonos3_mini_prefill", None),
               ("zonos2_prefill_q8", None), ("zonos2_decode_q4", 1), ("zonos2_decode_q4", 8),
-              ("zonos2_decode_q4", 64)]
+              ("zonos2_decode_q4", 64), ("zonos2_prefill_q4", None)]
 
 
 @pytest.mark.parametrize("seed", [2, 7, 13])
@@ -254,8 +254,8 @@ def test_forward_workloads_full(name, T, seed):
     the 1e-3 margin, near ties resolved validly, weights within 2e-6, counts,
     offsets, permutation and inverse bit-exact -- and every output row within
     the tolerance."""
-    if name.startswith("zonos2_decode_q4") and seed == 13:
-        pytest.skip("the 4-bit decode workload runs with two seeds")
+    if "_q4" in name and seed == 13:
+        pytest.skip("the 4-bit workloads run with two seeds")
     layer = wl.make_layer(wl.WORKLOADS[name], seed=seed, T=T)
     out, r = gpu_forward_views(layer, DEV, path=0)
     check_routing_views(r, layer)
@@ -263,7 +263,7 @@ def test_forward_workloads_full(name, T, seed):
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8"])
+@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8", "zonos2_prefill_q4"])
 def test_forward_prefill_workloads_on_decode_path(name):
     """The prefill workloads at full size through the decode path (CUDA-core
     kernels at these row counts): grouping and every output row."""
@@ -275,7 +275,7 @@ def test_forward_prefill_workloads_on_decode_path(name):
 
 
 @pytest.mark.parametrize("name", ["zonos3_mini_decode", "zonos2_decode", "zonos3_mini_prefill",
-                                  "zonos2_prefill_q8"])
+                                  "zonos2_prefill_q8", "zonos2_decode_q4", "zonos2_prefill_q4"])
 def test_graph_replay_equals_direct_launch(name):
     """The benchmark times CUDA-graph replays of the layer (warm-up launches on a
     side stream, capture on that stream, replay): at full size, a replay writes
@@ -320,7 +320,7 @@ PREFILL_SMALL = [
 ]
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64])
 @pytest.mark.parametrize("T,d,E,k,F", PREFILL_SMALL)
 def test_forward_prefill_small_matches_oracle(T, d, E, k, F, wdt):
     layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
@@ -345,14 +345,14 @@ def test_prefill_one_expert_many_tiles():
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64])
 def test_prefill_and_decode_paths_agree(wdt):
     layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
                                  w_dtype=wdt)
     t = upload_layer(layer, DEV)
     a = gpu_forward(layer, DEV, path=SIMT, t=t).cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(a ** 2))
-    for path in ((DECODE, PREFILL) if wdt == wl.BF16 else (PREFILL,)):
+    for path in ((PREFILL,) if wdt == wl.Q8_0 else (DECODE, PREFILL)):
         b = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy().astype(np.float64)
         assert np.abs(a - b).max() <= 2e-2 * rms
 
@@ -375,7 +375,7 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
     check_output(a, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64])
 @pytest.mark.parametrize("k,F", [(2, 128), (1, 1024)])   # (1, 1024): long K in the down GEMM
 def test_prefill_deterministic_and_equivariant(wdt, k, F):
     layer = wl.make_custom_layer(24, T=512, d=256, E=8, k=k, F=F, act_dtype=wl.BF16,
@@ -487,7 +487,8 @@ def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
     (PREFILL, 300, wl.Q8_0, 8, 256), (SIMT, 40, wl.Q8_0, 8, 256), (0, 600, wl.Q8_0, 8, 256),
     (DECODE, 40, wl.Q4_A64, 8, 256),      # split-K gate/up + SwiGLU reduction
     (DECODE, 128, wl.Q4_A64, 64, 512),    # whole-K gate/up writing h itself
-    (DECODE, 300, wl.Q4_A64, 8, 256)])    # rows grouped by the scatter kernel
+    (DECODE, 300, wl.Q4_A64, 8, 256),     # rows grouped by the scatter kernel
+    (PREFILL, 600, wl.Q4_A64, 8, 256)])   # 4-bit grouped GEMMs
 def test_fp16_operands_large_activations(path, T, wdt, E, F):
     """The Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels
     multiply fp16 operands.  Token rows whose magnitudes span 1e-2 .. 1e5 (h
@@ -520,7 +521,8 @@ def test_fp16_operands_large_activations(path, T, wdt, E, F):
 @pytest.mark.parametrize("wdt,path,T,E,k,F", [
     (wl.Q8_0, PREFILL, 256, 4, 1, 128),
     (wl.Q4_A64, DECODE, 256, 4, 1, 128),     # 4-bit: SwiGLU reduction kernel
-    (wl.Q4_A64, DECODE, 128, 64, 2, 512)])   # 4-bit: whole-K gate/up epilogue
+    (wl.Q4_A64, DECODE, 128, 64, 2, 512),    # 4-bit: whole-K gate/up epilogue
+    (wl.Q4_A64, PREFILL, 256, 4, 1, 128)])   # 4-bit grouped GEMMs
 def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     """Expert weights large enough that h leaves fp16's range even for
     normalised rows: the call reports MOE_ERR_DEVICE_CHECK instead of
