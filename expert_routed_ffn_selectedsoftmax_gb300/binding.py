@@ -31,6 +31,7 @@ EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "mo
            "moe_workspace_views", "moe_forward_expire_wait", "moe_check", "moe_check_noalloc")
 
 _lib = None
+_debug_lib = None
 
 
 class MoeError(RuntimeError):
@@ -54,7 +55,26 @@ def load_library():
         raise RuntimeError(
             f"{path} is missing: build the CUDA library first "
             "(python -m expert_routed_ffn_selectedsoftmax_gb300.build)")
-    L = ctypes.CDLL(path)
+    _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def load_debug_library():
+    """The debug build (libmoe_gb300_debug.so, MOE_DEBUG=1: device-side checks
+    of the grouping the expert kernels are given; include/moe_debug.h),
+    compiled first if it is missing or stale.  A separate ctypes handle with
+    the same signatures plus moe_debug_corrupt_next_offsets; the functions of
+    this module keep using the release library."""
+    global _debug_lib
+    if _debug_lib is None:
+        L = _declare(ctypes.CDLL(_build.build(debug=True)))
+        L.moe_debug_corrupt_next_offsets.argtypes = []
+        L.moe_debug_corrupt_next_offsets.restype = ctypes.c_int
+        _debug_lib = L
+    return _debug_lib
+
+
+def _declare(L):
     vp, i, sz, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
     L.moe_status_str.argtypes = [i]
     L.moe_status_str.restype = ctypes.c_char_p
@@ -97,7 +117,6 @@ def load_library():
     L.moe_check.restype = i
     L.moe_check_noalloc.argtypes = [vp, vp]
     L.moe_check_noalloc.restype = i
-    _lib = L
     return L
 
 

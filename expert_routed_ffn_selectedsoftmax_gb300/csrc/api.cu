@@ -8,6 +8,22 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_gemm.h"
+#if MOE_DEBUG
+#include <atomic>
+
+#include "moe_debug.h"
+
+namespace {
+std::atomic<bool> g_corrupt_offsets{false};   // moe_debug_corrupt_next_offsets
+__global__ void corrupt_offsets_kernel(int32_t *offsets, int E) { offsets[E] += 1; }
+}  // namespace
+
+moe_status moe_debug_corrupt_next_offsets(void)
+{
+    g_corrupt_offsets.store(true);
+    return MOE_OK;
+}
+#endif
 
 using namespace moe;
 
@@ -468,6 +484,12 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         e = launch_scatter(ra, (T + tpb - 1) / tpb, tpb, s);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
     }
+#if MOE_DEBUG
+    if (g_corrupt_offsets.exchange(false)) {   // test hook (moe_debug.h)
+        corrupt_offsets_kernel<<<1, 1, 0, s>>>(offsets, E);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+#endif
 
     if (use_prefill) {
         TcArgs a{};
@@ -510,7 +532,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         if (fused_small && !q4) {
             a.x_gather = x;   // (the 4-bit kernels take fp16 token rows by TMA from xp)
         } else if (!xp_ready &&
-                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, q4, xexp, num_sms, s) != cudaSuccess) {
+                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, q4, xexp, T, status, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;
         }
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;

@@ -292,6 +292,43 @@ __device__ __forceinline__ void flag_status(uint32_t *status, uint32_t bits)
     if (status) atomicOr(status, bits);
 }
 
+// Debug builds (MOE_DEBUG=1, libmoe_gb300_debug.so) check the grouped-row
+// offsets every expert kernel is given before it uses them -- offsets[0] = 0,
+// non-decreasing, offsets[E] = the number of grouped rows -- and the token
+// indices the row gathers read; a kernel given inconsistent offsets does no
+// work and records kDevCheckFailed, and a token index out of range is recorded
+// and its row skipped.  Release builds compile the checks away.
+#ifndef MOE_DEBUG
+#define MOE_DEBUG 0
+#endif
+// CTA-collective (every thread calls it): the offsets as above.
+__device__ __forceinline__ bool debug_offsets_ok(const int32_t *off, int E, int rows, uint32_t *status)
+{
+#if MOE_DEBUG
+    bool bad = false;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) bad |= off[e] > off[e + 1];
+    if (threadIdx.x == 0) bad |= off[0] != 0 || off[E] != rows;
+    bad = __syncthreads_or(bad) != 0;
+    if (bad && threadIdx.x == 0) flag_status(status, kDevCheckFailed);
+    return !bad;
+#else
+    (void)off; (void)E; (void)rows; (void)status;
+    return true;
+#endif
+}
+// A token index v in [0, n) (debug builds; release: always true).
+__device__ __forceinline__ bool debug_index_ok(int v, int n, uint32_t *status)
+{
+#if MOE_DEBUG
+    if (v >= 0 && v < n) return true;
+    flag_status(status, kDevCheckFailed);
+    return false;
+#else
+    (void)v; (void)n; (void)status;
+    return true;
+#endif
+}
+
 // True (uniformly across the CTA) when an earlier kernel of this call has
 // already recorded an error in the status word: the caller then returns
 // without touching scratch whose contents may be incomplete.

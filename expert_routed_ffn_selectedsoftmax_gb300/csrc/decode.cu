@@ -33,9 +33,11 @@ constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kRowBlock = 8;
 
 // List of experts with at least one row, in expert order.  blockDim >= E.
+// (Debug builds: none when the offsets are inconsistent, see debug_offsets_ok.)
 __device__ __forceinline__ int build_active_list(const int32_t *__restrict__ offsets, int E,
-                                                 int *act, int *wtot)
+                                                 int *act, int *wtot, int rows, uint32_t *status)
 {
+    if (!debug_offsets_ok(offsets, E, rows, status)) return 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = threadIdx.x;
     const bool a = e < E && offsets[e + 1] > offsets[e];
@@ -69,12 +71,12 @@ template <typename AT, typename WT, int NCH, int RPW>
 __global__ void __launch_bounds__(kDecThreads)
 decode_gateup_kernel(const AT *__restrict__ x, int d, WView<WT> wg, WView<WT> wu, int F,
                      const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
-                     int E, float *__restrict__ h)
+                     int E, float *__restrict__ h, int rows, int T, uint32_t *status)
 {
     pdl_enter();
     __shared__ int act[kMaxExperts];
     __shared__ int wtot[kDecWarps];
-    const int n_act = build_active_list(offsets, E, act, wtot);
+    const int n_act = build_active_list(offsets, E, act, wtot, rows, status);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int ROWS = kDecWarps * RPW;     // ffn rows per work item
     const int ftiles = (F + ROWS - 1) / ROWS;
@@ -94,7 +96,12 @@ decode_gateup_kernel(const AT *__restrict__ x, int d, WView<WT> wg, WView<WT> wu
             for (int r = 0; r < kRowBlock; ++r) {
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) { ag[i][r] = 0.f; au[i][r] = 0.f; }
-                tok[r] = rb + r < M ? perm_tok[row0 + rb + r] : -1;
+                int t = -1;
+                if (rb + r < M) {
+                    t = perm_tok[row0 + rb + r];
+                    if (!debug_index_ok(t, T, status)) t = -1;   // (debug builds)
+                }
+                tok[r] = t;
             }
             for (int c0 = lane * 8; c0 < d; c0 += 32 * 8 * NCH) {
                 RawW<WT> rg[RPW][NCH], ru[RPW][NCH];
@@ -147,12 +154,12 @@ __global__ void __launch_bounds__(kDecThreads)
 decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
                    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm_tok,
                    const float *__restrict__ perm_w, int E, int k, float *__restrict__ out,
-                   float *__restrict__ y)
+                   float *__restrict__ y, int rows, int T, uint32_t *status)
 {
     pdl_enter();
     __shared__ int act[kMaxExperts];
     __shared__ int wtot[kDecWarps];
-    const int n_act = build_active_list(offsets, E, act, wtot);
+    const int n_act = build_active_list(offsets, E, act, wtot, rows, status);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int COLS = kDecWarps * RPW;     // output columns per work item
     const int dtiles = (d + COLS - 1) / COLS;
@@ -214,9 +221,12 @@ decode_down_kernel(const float *__restrict__ h, int F, WView<WT> wd, int d,
                     } else {
                         // k = 1: the only contribution; k = 2: two additions onto
                         // zero, whose result does not depend on their order
-                        float *dst = out + (size_t)perm_tok[row] * d + o0 + i;
-                        if (k == 1) *dst = v;
-                        else atomicAdd(dst, v);
+                        const int t = perm_tok[row];
+                        if (debug_index_ok(t, T, status)) {   // (debug builds)
+                            float *dst = out + (size_t)t * d + o0 + i;
+                            if (k == 1) *dst = v;
+                            else atomicAdd(dst, v);
+                        }
                     }
                 }
             }
@@ -281,7 +291,7 @@ static cudaError_t launch_gateup(const DecodeArgs &a, WView<WT> wg, WView<WT> wu
     int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);
     if (g < 1) g = 1;
     launch_pdl(k1, dim3(g), dim3(kDecThreads), 0, stream, static_cast<const AT *>(a.x), a.d, wg, wu,
-               a.F, a.offsets, a.perm_tok, a.E, a.h);
+               a.F, a.offsets, a.perm_tok, a.E, a.h, a.T * a.k, a.T, a.status);
     return cudaGetLastError();
 }
 
@@ -298,7 +308,7 @@ static cudaError_t launch_down(const DecodeArgs &a, WView<WT> wd, cudaStream_t s
     int g = (int)(items < (long long)a.num_sms * occ ? items : (long long)a.num_sms * occ);
     if (g < 1) g = 1;
     launch_pdl(k2, dim3(g), dim3(kDecThreads), 0, stream, a.h, a.F, wd, a.d, a.offsets, a.perm_tok,
-               a.perm_w, a.E, a.k, a.out, a.y);
+               a.perm_w, a.E, a.k, a.out, a.y, a.T * a.k, a.T, a.status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || a.k <= 2) return err;
     return launch_combine_rows(a.y, a.d, a.inv, a.T, a.k, a.out, a.status, a.num_sms, stream);

@@ -293,6 +293,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
     // per-expert chunks of <= 32 rows, numbered across experts
     for (int e = threadIdx.x; e <= E; e += THREADS) c.off[e] = p.offsets[e];
     __syncthreads();
+    const bool offsets_ok = debug_offsets_ok(c.off, E, p.rows, p.status);
     if (warp == 0) {
         constexpr int PER = kMaxExperts / 32;
         int local[PER], sum = 0;
@@ -318,8 +319,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
         if (lane == 31) {
             const int nc = incl < p.nc_max ? incl : p.nc_max;   // (consistent routing: incl <= nc_max)
             c.chunk_start[E] = nc;
-            c.n_gu = nc * (p.F / BM);
-            c.n_all = c.n_gu + nc * (p.d / BM);
+            c.n_gu = offsets_ok ? nc * (p.F / BM) : 0;
+            c.n_all = offsets_ok ? c.n_gu + nc * (p.d / BM) : 0;
         }
     }
     tc_fence_before();
@@ -438,8 +439,11 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
             if (it.kind == END) break;
             const bool has = lane < it.nrows;
             const uint16_t *src;
-            if (it.kind == GATEUP)
-                src = p.x + (size_t)(has ? p.perm_tok[it.row0 + lane] : 0) * p.d;
+            if (it.kind == GATEUP) {
+                int tok = has ? p.perm_tok[it.row0 + lane] : 0;
+                if (has && !debug_index_ok(tok, p.rows / p.k, p.status)) tok = 0;   // (debug builds)
+                src = p.x + (size_t)tok * p.d;
+            }
             else
                 src = p.h + (size_t)(has ? it.row0 + lane : 0) * p.F;
             int ready_tile = -1;   // down: last F tile of h seen complete
@@ -524,8 +528,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_cons
                 continue;
             }
             // down: token and routing weight of row j, held by lane j
-            const int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
-            const float w_l = lane < it.nrows ? p.perm_w[it.row0 + lane] : 0.f;
+            int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
+            float w_l = lane < it.nrows ? p.perm_w[it.row0 + lane] : 0.f;
+            if (lane < it.nrows && !debug_index_ok(tok_l, p.rows / p.k, p.status)) { tok_l = 0; w_l = 0.f; }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int tok = __shfl_sync(0xffffffffu, tok_l, j);

@@ -133,6 +133,7 @@ struct Params {
     int k;
     uint32_t expire_ns;  // > 0: the producer's first wait gives up after this long (test hook)
     const int32_t *xexp; // W4: token row r holds x * 2^-xexp[r] (fp16); h is h * 2^-2 xexp[r]
+    int T;               // tokens (debug builds: range of perm_tok)
     const uint8_t *w4[2];  // W4: packed tiles of the matrix (GATEUP: gate, up; DOWN: down)
     int groups;            // W4: K / 64, tiles per row tile
 };
@@ -276,6 +277,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
     }
     for (int e = threadIdx.x; e <= E; e += NTHREADS) c.off[e] = p.offsets[e];
     __syncthreads();
+    const bool offsets_ok = debug_offsets_ok(c.off, E, p.rows_total, p.status);
     if (threadIdx.x < 32) {
         const int units = p.n_mats * p.rtiles * p.KS;
         int local[8], sum = 0;
@@ -300,7 +302,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             if (e < E) c.unit_start[e] = run;
             run += local[j];
         }
-        if (lane == 31) { c.n_items = incl; c.unit_start[E] = incl; }
+        if (lane == 31) { c.n_items = offsets_ok ? incl : 0; c.unit_start[E] = incl; }
     }
     tc_fence_before();
     __syncthreads();
@@ -491,7 +493,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item(c, p, item);
             const bool has = lane < it.nrows;
-            const uint16_t *src = p.xg + (size_t)(has ? p.perm_tok[it.row0 + lane] : 0) * p.K;
+            int tok = has ? p.perm_tok[it.row0 + lane] : 0;
+            if (has && !debug_index_ok(tok, p.T, p.status)) tok = 0;   // (debug builds)
+            const uint16_t *src = p.xg + (size_t)tok * p.K;
             for (int kbl = 0; kbl < it.nkb; ++kbl, ++it_k) {
                 const int s = it_k % STAGES;
                 if ((s & 3) != sw) continue;
@@ -574,8 +578,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             mbar_arrive(&c.tempty[acc]);          // accumulator is in registers now
             if (MODE == DOWN && p.direct) {
                 // token and routing weight of row j, held by lane j
-                const int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
+                int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
                 float w_l = lane < it.nrows ? p.perm_w[it.row0 + lane] : 0.f;
+                if (lane < it.nrows && !debug_index_ok(tok_l, p.T, p.status)) { tok_l = 0; w_l = 0.f; }
                 if (W4 && lane < it.nrows) w_l *= ldexpf(1.f, 2 * p.xexp[it.row0 + lane]);   // undo h's scale
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -824,6 +829,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.rows_total = rows; p.status = a.status;
     p.xexp = w4 ? a.xexp : nullptr;
+    p.T = a.T;
     p.w4[0] = static_cast<const uint8_t *>(a.w_gate);
     p.w4[1] = static_cast<const uint8_t *>(a.w_up);
     p.groups = a.d / 64;

@@ -75,8 +75,8 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
                            cudaStream_t stream);
 // to_fp16: rows scaled by 2^-xexp[r] (fp16_row_exponent), xexp written
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
-                               void *xp, int to_fp16, int32_t *xexp, int num_sms,
-                               cudaStream_t stream);
+                               void *xp, int to_fp16, int32_t *xexp, int T, uint32_t *status,
+                               int num_sms, cudaStream_t stream);
 // dense layer (E = 1, k = 1): expert 0, weight 1, identity grouping; clears
 // status and zero_words[n_zero]
 cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, int32_t *counts,
@@ -98,7 +98,7 @@ struct DecodeArgs {
     float *out;                 // [T, d] fp32 (zeroed beforehand when k == 2)
     float *y;                   // k > 2: [T*k, d] weighted expert outputs (then combined)
     const int32_t *inv;         // [T*k] grouped row of each slot (k > 2)
-    const uint32_t *status;
+    uint32_t *status;
     int num_sms;
     cudaEvent_t ev_gateup;      // optional: recorded between the two kernels
 };

@@ -139,7 +139,8 @@ cudaError_t launch_permute(const int32_t *topk_idx, int T, int k, int E, int32_t
 // scaled by 2^-xexp[r] (fp16_row_exponent), one warp per row.
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, int d,
                                    const int32_t *__restrict__ perm_tok, int rows,
-                                   uint16_t *__restrict__ xp, int to_fp16, int32_t *__restrict__ xexp)
+                                   uint16_t *__restrict__ xp, int to_fp16, int32_t *__restrict__ xexp,
+                                   int T, uint32_t *__restrict__ status)
 {
     pdl_enter();
     const int vec_per_row = d / 8;
@@ -147,7 +148,9 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, int d,
         const int lane = threadIdx.x & 31;
         const int wpb = blockDim.x / 32;
         for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
-            const uint16_t *src = x + (size_t)perm_tok[r] * d;
+            int t = perm_tok[r];
+            if (!debug_index_ok(t, T, status)) t = 0;   // (debug builds)
+            const uint16_t *src = x + (size_t)t * d;
             const int e = fp16_row_exponent(src, d, lane);
             if (lane == 0) xexp[r] = e;
             for (int c = lane; c < vec_per_row; c += 32)
@@ -161,6 +164,7 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, int d,
          v += (long long)gridDim.x * blockDim.x) {
         int r = (int)(v / vec_per_row), c = (int)(v - (long long)r * vec_per_row);
         int t = perm_tok[r];
+        if (!debug_index_ok(t, T, status)) t = 0;   // (debug builds)
         uint4 u = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * d) + c);
         reinterpret_cast<uint4 *>(xp + (size_t)r * d)[c] = u;
     }
@@ -209,14 +213,15 @@ cudaError_t launch_identity_grouping(int T, int32_t *topk_idx, float *topk_w, in
 }
 
 cudaError_t launch_gather_rows(const void *x, int d, const int32_t *perm_tok, int rows,
-                               void *xp, int to_fp16, int32_t *xexp, int num_sms, cudaStream_t stream)
+                               void *xp, int to_fp16, int32_t *xexp, int T, uint32_t *status,
+                               int num_sms, cudaStream_t stream)
 {
     long long total = (long long)rows * (d / 8);
     long long want = (total + 255) / 256, cap = (long long)num_sms * 8;
     int blocks = (int)(want < cap ? want : cap);
     if (blocks < 1) blocks = 1;
     launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const uint16_t *>(x), d, perm_tok,
-                                                   rows, static_cast<uint16_t *>(xp), to_fp16, xexp);
+                                                   rows, static_cast<uint16_t *>(xp), to_fp16, xexp, T, status);
     return cudaGetLastError();
 }
 

@@ -148,6 +148,7 @@ struct Params {
     int K;                    // reduction length (d for GATEUP, F for DOWN)
     int n_tiles;              // N / BN   (GATEUP: F / 128, DOWN: d / 256)
     int F, d, k;
+    int rows;                 // grouped rows (T * k)
     uint16_t *h;              // GATEUP output [rows, F] (bf16 or fp16 bits)
     const int32_t *perm_tok;  // DOWN epilogue
     const float *perm_w;
@@ -292,6 +293,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     if (threadIdx.x == 0) c.fail = p.status ? *(volatile const uint32_t *)p.status : 0u;
     for (int e = threadIdx.x; e <= E; e += C::THREADS) c.off[e] = p.offsets[e];
     __syncthreads();
+    if (!debug_offsets_ok(c.off, E, p.rows, p.status) && threadIdx.x == 0) c.fail = 1u;   // no tiles run
     if (threadIdx.x < 32) {
         // exclusive scan of mtiles_e * n_tiles over experts (E <= 256: 8 per lane)
         int local[8], sum = 0;
@@ -623,6 +625,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 if (valid) {
                     tok = p.perm_tok[grow];
                     wgt = p.perm_w[grow];
+                    if (!debug_index_ok(tok, p.rows / p.k, p.status)) { tok = 0; wgt = 0.f; }   // (debug builds)
                     // fp16 rows (Q8_0): h was held as h / s^2
                     if (p.xexp) wgt *= ldexpf(1.f, 2 * p.xexp[grow]);
                 }
@@ -877,7 +880,8 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     const int rows = a.T * a.k;
     cudaError_t err = cudaSuccess;
     if (!a.xp_ready &&
-        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, f16 ? 1 : 0, a.xexp, a.num_sms, stream)) !=
+        (err = launch_gather_rows(a.x, a.d, a.perm_tok, rows, a.xp, f16 ? 1 : 0, a.xexp, a.T, a.status,
+                                   a.num_sms, stream)) !=
             cudaSuccess)
         return err;
     if (a.ev_gathered && (err = cudaEventRecord(a.ev_gathered, stream)) != cudaSuccess) return err;
@@ -924,7 +928,7 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
         return cudaErrorInvalidValue;
 
     Params p{};
-    p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k;
+    p.offsets = a.offsets; p.E = a.E; p.F = a.F; p.d = a.d; p.k = a.k; p.rows = a.T * a.k;
     p.h = static_cast<uint16_t *>(a.h); p.perm_tok = a.perm_tok; p.perm_w = a.perm_w;
     p.out = a.out; p.y = a.y; p.status = a.status; p.h_fp16 = f16 ? 1 : 0;
     p.xexp = f16 ? a.xexp : nullptr;

@@ -145,3 +145,22 @@ def test_ffn_dense_argument_checks(lib):
                              None) == 1
     assert lib.moe_ffn_dense(fake, 0, 4, 64, fake, fake, fake, 1, 128, fake, fake, 1 << 20, 0,
                              None) == 2
+
+
+def test_debug_build_exports_the_debug_header_too():
+    """libmoe_gb300_debug.so (MOE_DEBUG=1) exports the moe.h ABI plus the
+    entry points of include/moe_debug.h; the release library does not export
+    the latter."""
+    import subprocess
+    from expert_routed_ffn_selectedsoftmax_gb300 import build, binding
+    dbg_header = os.path.join(ROOT, "include", "moe_debug.h")
+    debug_names = sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", open(dbg_header).read())))
+    assert debug_names == ["moe_debug_corrupt_next_offsets"]
+
+    def exported(path):
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+        return sorted({ln.split()[-1] for ln in out.splitlines() if ln.split() and ln.split()[-1].startswith("moe_")})
+
+    assert exported(build.build(debug=True)) == sorted(declared_symbols() + debug_names)
+    assert exported(build.build()) == declared_symbols()
+
