@@ -30,8 +30,10 @@ from typing import Optional
 
 import numpy as np
 
-F32, BF16, Q8_0, Q4_A64 = 0, 1, 2, 3
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64"}
+F32, BF16, Q8_0, Q4_A64, Q4_K = 0, 1, 2, 3, 4
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64", Q4_K: "q4_k"}
+Q4_K_BLOCK = 256
+Q4_K_BLOCK_BYTES = 144
 Q4_A64_GROUP = 64
 Q4_A64_BLOCK_BYTES = 36
 Q8_0_BLOCK = 32
@@ -199,6 +201,59 @@ def q4_a64_quantize(w) -> np.ndarray:
     return out
 
 
+def q4_k_pack_scales(sc, m) -> np.ndarray:
+    """Six-bit sub-block scales sc[..., 8] and mins m[..., 8] -> the 12 bytes of
+    a Q4_K super-block: bytes 0-3 hold sc[0..3] in their low 6 bits and the top
+    2 bits of sc[4..7]; bytes 4-7 likewise m[0..3] and the top bits of m[4..7];
+    bytes 8-11 hold the low nibbles of sc[4..7] (low) and m[4..7] (high)."""
+    sc = np.asarray(sc, np.uint8)
+    m = np.asarray(m, np.uint8)
+    out = np.empty(sc.shape[:-1] + (12,), np.uint8)
+    out[..., 0:4] = (sc[..., 0:4] & 63) | ((sc[..., 4:8] >> 4) << 6)
+    out[..., 4:8] = (m[..., 0:4] & 63) | ((m[..., 4:8] >> 4) << 6)
+    out[..., 8:12] = (sc[..., 4:8] & 15) | ((m[..., 4:8] & 15) << 4)
+    return out
+
+
+def q4_k_quantize(w) -> np.ndarray:
+    """Encode w[..., K] (K % 256 == 0) as Q4_K super-blocks: uint8 [..., K/256, 144].
+
+    Block: fp16 d, fp16 dmin, 12 bytes of six-bit sub-block scales and mins
+    (q4_k_pack_scales), 128 bytes of codes (the 32-byte run c holds sub-block
+    2c in its low nibbles and 2c+1 in its high nibbles); sub-block j (values
+    32j .. 32j+31) decodes as d * sc[j] * q - dmin * m[j].  This encoder: per
+    sub-block min' = max(0, -min w) and step s = (max w + min') / 15; d =
+    max s / 63 and dmin = max min' / 63 rounded to fp16; sc = round(s / d),
+    m = round(min' / dmin) clamped to [0, 63]; q = round-half-away((w + dmin
+    m) / (d sc)) clamped to [0, 15] with the stored d and dmin (0 where d sc = 0).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    if K % Q4_K_BLOCK:
+        raise ValueError("Q4_K needs the contiguous axis to be a multiple of 256")
+    g = w.reshape(w.shape[:-1] + (K // Q4_K_BLOCK, 8, 32)).astype(np.float64)
+    mn = np.maximum(0.0, -g.min(axis=-1))
+    step = (g.max(axis=-1) + mn) / 15.0
+    d16 = (step.max(axis=-1) / 63.0).astype(np.float16)
+    dmin16 = (mn.max(axis=-1) / 63.0).astype(np.float16)
+    d, dmin = d16.astype(np.float64), dmin16.astype(np.float64)
+    safe = lambda a: np.where(a > 0, a, 1.0)
+    sc = np.where(d[..., None] > 0, np.clip(np.floor(step / safe(d)[..., None] + 0.5), 0, 63), 0)
+    m = np.where(dmin[..., None] > 0, np.clip(np.floor(mn / safe(dmin)[..., None] + 0.5), 0, 63), 0)
+    a = d[..., None] * sc                    # effective step per sub-block
+    b = dmin[..., None] * m                  # effective offset per sub-block
+    v = (g + b[..., None]) / safe(a)[..., None]
+    q = np.where(a[..., None] > 0, np.clip(np.sign(v) * np.floor(np.abs(v) + 0.5), 0, 15), 0)
+    q = q.astype(np.uint8)
+    out = np.empty(g.shape[:-2] + (Q4_K_BLOCK_BYTES,), dtype=np.uint8)
+    out[..., 0:2] = d16.view(np.uint8).reshape(d16.shape + (2,))
+    out[..., 2:4] = dmin16.view(np.uint8).reshape(dmin16.shape + (2,))
+    out[..., 4:16] = q4_k_pack_scales(sc.astype(np.uint8), m.astype(np.uint8))
+    runs = q.reshape(q.shape[:-2] + (4, 2, 32))       # [..., run c, sub-block 2c / 2c+1, value]
+    out[..., 16:] = (runs[..., 0, :] | (runs[..., 1, :] << 4)).reshape(q.shape[:-2] + (128,))
+    return out
+
+
 def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == F32:
         return np.ascontiguousarray(a, dtype=np.float32)
@@ -208,6 +263,8 @@ def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
         return q8_0_quantize(a)
     if dtype == Q4_A64:
         return q4_a64_quantize(a)
+    if dtype == Q4_K:
+        return q4_k_quantize(a)
     raise ValueError(dtype)
 
 
@@ -285,6 +342,8 @@ def weight_bytes_per_expert(d: int, F: int, w_dtype: int) -> int:
         return 2 * n
     if w_dtype == Q4_A64:
         return n // Q4_A64_GROUP * Q4_A64_BLOCK_BYTES
+    if w_dtype == Q4_K:
+        return n // Q4_K_BLOCK * Q4_K_BLOCK_BYTES
     return n // Q8_0_BLOCK * Q8_0_BLOCK_BYTES
 
 

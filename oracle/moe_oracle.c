@@ -5,7 +5,8 @@
  * no code, header or table with the CUDA library.
  *
  * Plain C, fp64 throughout.  It reads the same storage bytes as the GPU path
- * (fp32, bf16 bit patterns, or 34-byte Q8_0 blocks) and widens them exactly.
+ * (fp32, bf16 bit patterns, 34-byte Q8_0 blocks, 36-byte affine 4-bit blocks
+ * or 144-byte Q4_K super-blocks) and widens them exactly.
  * Steps follow the pages in order:
  *
  *   1. router projection: logit[t,e] = sum_i x[t,i] * W_r[e,i]
@@ -75,6 +76,41 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
             for (int i = 0; i < 32; ++i)
                 out[b * 32 + i] = scale * (double)(int8_t)blk[2 + i];
         }
+    } else if (dt == ORACLE_Q4_K) {
+        /* Q4_K ("zonos2.cpp internals", §Recommended: F16 spine + K-quant
+         * experts, 4.50 bits per weight; the pages give no byte layout, this
+         * is the GGUF one): per row cols/256 super-blocks of 144 bytes
+         * {fp16 d, fp16 dmin, 12 bytes of six-bit sub-block scales sc[8] and
+         * mins m[8], 128 bytes of 4-bit codes}.  Sub-block j holds values
+         * 32j .. 32j+31: value = d * sc[j] * q - dmin * m[j].  Six-bit fields:
+         * for j < 4, sc[j] = low 6 bits of byte j and m[j] = low 6 bits of
+         * byte j+4; for j >= 4, sc[j] = (low nibble of byte j+4) + 16 * (top 2
+         * bits of byte j-4) and m[j] = (high nibble of byte j+4) + 16 * (top 2
+         * bits of byte j).  Codes: the 32-byte run c (c = 0..3) holds sub-block
+         * 2c in its low nibbles and sub-block 2c+1 in its high nibbles, value i
+         * of each in byte i of the run. */
+        const uint8_t *p = (const uint8_t *)base + row * (size_t)(cols / 256) * 144;
+        for (int b = 0; b < cols / 256; ++b) {
+            const uint8_t *blk = p + (size_t)b * 144;
+            const double d = f16_bits_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+            const double dmin = f16_bits_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+            const uint8_t *s = blk + 4, *qs = blk + 16;
+            for (int j = 0; j < 8; ++j) {
+                int sc, m;
+                if (j < 4) {
+                    sc = s[j] & 63;
+                    m = s[j + 4] & 63;
+                } else {
+                    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+                    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+                }
+                const uint8_t *run = qs + 32 * (j / 2);
+                for (int i = 0; i < 32; ++i) {
+                    const int q = (j % 2) ? (run[i] >> 4) : (run[i] & 15);
+                    out[b * 256 + 32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
+                }
+            }
+        }
     } else { /* ORACLE_Q4_A64 ("Zyphra-ZONOS2-4bit", §How this was quantized:
               * experts at 4 bits, groups of 64, affine; the byte layout is this
               * library's): per row cols/64 blocks of {fp16 scale, fp16 bias,
@@ -96,7 +132,8 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
 static int valid_act(int dt) { return dt == ORACLE_F32 || dt == ORACLE_BF16; }
 static int valid_w(int dt)
 {
-    return dt == ORACLE_F32 || dt == ORACLE_BF16 || dt == ORACLE_Q8_0 || dt == ORACLE_Q4_A64;
+    return dt == ORACLE_F32 || dt == ORACLE_BF16 || dt == ORACLE_Q8_0 || dt == ORACLE_Q4_A64 ||
+           dt == ORACLE_Q4_K;
 }
 
 /* ------------------------------------------------------------ thread helper */
@@ -389,6 +426,7 @@ int oracle_expert_combine(const void *x, int x_dt, int T, int d, const int32_t *
         return -1;
     if (w_dt == ORACLE_Q8_0 && (d % 32 || F % 32)) return -1;
     if (w_dt == ORACLE_Q4_A64 && (d % 64 || F % 64)) return -1;
+    if (w_dt == ORACLE_Q4_K && (d % 256 || F % 256)) return -1;
     for (size_t i = 0; i < (size_t)T * k; ++i)
         if (topk_idx[i] < 0 || topk_idx[i] >= E) return -1;
     if (T == 0) return 0;

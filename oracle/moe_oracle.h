@@ -21,7 +21,7 @@
 extern "C" {
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3, ORACLE_Q4_K = 4 };
 
 int oracle_default_threads(void);
 

@@ -42,6 +42,22 @@ def decode(a, dtype):
         return wl.bf16_bits_to_f32(a).astype(np.float64)
     blocks = np.asarray(a, np.uint8)
     scale = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    if dtype == wl.Q4_K:
+        # 256 values per 144 bytes: d, dmin, 12 bytes of 6-bit (scale, min)
+        # pairs, 4 runs of 32 code bytes (low nibbles: sub-block 2c, high: 2c+1)
+        dmin = blocks[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+        s = blocks[..., 4:16].astype(np.int64)
+        w = np.empty(blocks.shape[:-1] + (256,), np.float64)
+        for j in range(8):
+            if j < 4:
+                sc, mn = s[..., j] & 63, s[..., j + 4] & 63
+            else:
+                sc = (s[..., j + 4] & 15) + 16 * (s[..., j - 4] >> 6)
+                mn = (s[..., j + 4] >> 4) + 16 * (s[..., j] >> 6)
+            run = blocks[..., 16 + 32 * (j // 2):48 + 32 * (j // 2)].astype(np.int64)
+            q = (run >> 4) if j % 2 else (run & 15)
+            w[..., 32 * j:32 * j + 32] = scale[..., None] * sc[..., None] * q - dmin[..., None] * mn[..., None]
+        return w.reshape(w.shape[:-2] + (w.shape[-2] * w.shape[-1],))
     if dtype == wl.Q4_A64:   # {scale, bias, 32 bytes: value 2j low nibble, 2j+1 high}
         bias = blocks[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
         codes = blocks[..., 4:]
@@ -225,10 +241,12 @@ def test_k_equals_e_is_dense_softmax_gating():
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("act,wdt", [(wl.F32, wl.F32), (wl.BF16, wl.BF16), (wl.BF16, wl.Q8_0)])
+@pytest.mark.parametrize("act,wdt", [(wl.F32, wl.F32), (wl.BF16, wl.BF16), (wl.BF16, wl.Q8_0),
+                                     (wl.BF16, wl.Q4_A64), (wl.BF16, wl.Q4_K)])
 @pytest.mark.parametrize("k", [1, 2, 3])
 def test_matches_dense_brute_force(act, wdt, k):
-    layer = tiny_layer(seed=10 + k, act=act, wdt=wdt, T=5, d=64, E=6, k=k, F=96, bias_sd=0.3)
+    d, F = (256, 256) if wdt == wl.Q4_K else (64, 96) if wdt != wl.Q4_A64 else (64, 128)
+    layer = tiny_layer(seed=10 + k, act=act, wdt=wdt, T=5, d=d, E=6, k=k, F=F, bias_sd=0.3)
     out, idx, w, margin = oracle.moe_forward(layer)
     ref, sel, logits = brute_force_dense(layer)
     assert np.array_equal(idx, sel)
@@ -542,3 +560,57 @@ def test_q4_a64_layer_equals_its_exact_dequantisation():
         setattr(f, n, v.astype(np.float32))
     out_f, idx_f, _, _ = oracle.moe_forward(f)
     assert np.array_equal(idx_q, idx_f) and np.array_equal(out_q, out_f)
+
+
+# ------------------------------------------- Q4_K super-blocks (next row f3)
+def test_q4_k_super_block_worked_example():
+    """A hand-built super-block: d = 0.5, dmin = 0.25, six-bit scales and mins
+    chosen so that every bit of the 12 packed bytes is used (values >= 16 in
+    sub-blocks 4-7 put bits in the top two bits of bytes 0-7), and code
+    q = (i + 3j) mod 16 for value i of sub-block j.  The bytes are assembled
+    here field by field from the format's description; value 32j + i must be
+    0.5 * sc[j] * q - 0.25 * m[j], and the library's encoder helper must pack
+    the same 12 bytes."""
+    sc = [1, 2, 3, 63, 17, 33, 48, 5]
+    mn = [0, 1, 62, 7, 16, 40, 3, 63]
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = np.array([0.5], np.float16).view(np.uint8)
+    blk[2:4] = np.array([0.25], np.float16).view(np.uint8)
+    for j in range(4):
+        blk[4 + j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)     # sc[j]; top bits of sc[j+4]
+        blk[8 + j] = (mn[j] & 63) | ((mn[j + 4] >> 4) << 6)     # m[j];  top bits of m[j+4]
+        blk[12 + j] = (sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4)
+    q = np.array([[(i + 3 * j) % 16 for i in range(32)] for j in range(8)])
+    for c in range(4):
+        blk[16 + 32 * c:48 + 32 * c] = q[2 * c] | (q[2 * c + 1] << 4)
+    assert np.array_equal(wl.q4_k_pack_scales(np.array(sc), np.array(mn)), blk[4:16])
+    want = np.array([0.5 * sc[j] * q[j, i] - 0.25 * mn[j] for j in range(8) for i in range(32)])
+    got = decode(blk[None, None], wl.Q4_K)[0]
+    assert np.array_equal(got, want)
+    # the oracle reads the same bytes: a one-expert layer with W_g = this row
+    # against numpy on the hand values
+    T, d, F = 3, 256, 256
+    layer = tiny_layer(seed=93, act=wl.F32, wdt=wl.Q4_K, T=T, d=d, E=1, k=1, F=F)
+    layer.w_gate = np.tile(blk, (1, F, 1)).reshape(1, F, 1, 144)
+    x = decode(layer.x, wl.F32)
+    g = x @ np.tile(want, (F, 1)).T
+    u = x @ decode(layer.w_up, wl.Q4_K)[0].T
+    ref = (g / (1.0 + np.exp(-g)) * u) @ decode(layer.w_down, wl.Q4_K)[0].T
+    out, _, _, _ = oracle.moe_forward(layer)
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_q4_k_encoder_error_within_half_a_step():
+    rng = np.random.default_rng(94)
+    w = (rng.standard_normal((8, 512)) * 0.05).astype(np.float32)
+    b = wl.q4_k_quantize(w)
+    deq = decode(b, wl.Q4_K)
+    d = b[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    # the largest step of each super-block: d * 63; half of it bounds the error
+    # of values inside the sub-block's range, plus the six-bit rounding of the
+    # scales and mins (one d / dmin unit each)
+    dmin = b[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    bound = np.repeat(0.5 * 63 * d + 15 * d + dmin, 256, axis=-1)
+    assert np.all(np.abs(deq - w) <= bound)
+    assert np.sqrt(np.mean((deq - w) ** 2)) < 0.15 * np.sqrt(np.mean(w ** 2))
+

@@ -87,6 +87,17 @@ MUTANTS = {
         "scale * (double)(blk[4 + j] & 15) + bias;", "scale * ((double)(blk[4 + j] & 15) + bias);", 0),
     "q4_bias_dropped": ("double bias = f16_bits_to_double((uint16_t)(blk[2] | (blk[3] << 8)));",
                         "double bias = 0.0 * (blk[2] | blk[3]);", 0),
+    # Q4_K super-blocks ("zonos2.cpp internals", §Recommended: F16 spine + K-quant experts)
+    "q4k_high_scale_bits_from_mins": (
+        "sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);", "sc = (s[j + 4] & 15) | ((s[j] >> 6) << 4);", 0),
+    "q4k_min_nibble_low": ("m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);",
+                           "m = (s[j + 4] & 15) | ((s[j] >> 6) << 4);", 0),
+    "q4k_sub_block_nibbles_swapped": ("const int q = (j % 2) ? (run[i] >> 4) : (run[i] & 15);",
+                                      "const int q = (j % 2) ? (run[i] & 15) : (run[i] >> 4);", 0),
+    "q4k_min_added": ("d * (double)sc * (double)q - dmin * (double)m;",
+                      "d * (double)sc * (double)q + dmin * (double)m;", 0),
+    "q4k_d_dmin_swapped": ("const double dmin = f16_bits_to_double((uint16_t)(blk[2] | (blk[3] << 8)));",
+                           "const double dmin = f16_bits_to_double((uint16_t)(blk[0] | (blk[1] << 8)));", 0),
     # bf16 storage
     "bf16_low_half": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;", 0),
 }
