@@ -42,7 +42,7 @@ bool scoring_ok(int scoring)
 bool weights_ok(int act_dt, int w_dt)
 {
     if (act_dt == MOE_F32) return w_dt == MOE_F32;
-    return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64;
+    return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt);
 }
 
 // Largest d the router kernel can stage (one token of fp32 in <= 200 KB).
@@ -72,7 +72,7 @@ struct WsLayout {
 
 bool prefill_capable(int act_dt, int w_dt, int d, int F)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64) &&
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt)) &&
            d % 256 == 0 && F % 128 == 0;
 }
 
@@ -94,7 +94,7 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.tile_cnt = take(4 * (size_t)(T > 0 ? T : 1) * (size_t)E);   // <= one tile per token
     L.h = take(4 * n * (size_t)F);            // fp32 (decode); prefill uses 2 bytes/element
     // the decode_tc_capable() shape/dtype conditions, without the driver query
-    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q4_A64) && d % 128 == 0 &&
+    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt)) && d % 128 == 0 &&
             F % 128 == 0 && n <= (size_t)kDecodeTcMaxRows;
     L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
     L.pgu = L.pd = L.flags = off;
@@ -103,7 +103,7 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.y = k > 2 ? take(4 * n * (size_t)d) : off;
     // Q8_0 / 4-bit grouped GEMMs and 4-bit tensor-core decode: exponent of
     // each fp16 grouped row's scale
-    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt != MOE_BF16) || (L.dtc && w_dt == MOE_Q4_A64))
+    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt != MOE_BF16) || (L.dtc && is_q4(w_dt)))
                  ? take(4 * n) : off;
     L.n_flags = 0;
     if (L.dtc) {
@@ -135,12 +135,13 @@ moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, con
     if (st != MOE_OK) return st;
     if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
     if (!weights_ok(act_dt, w_dt)) {
-        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64)
+        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt))
                    ? MOE_ERR_UNSUPPORTED
                    : MOE_ERR_INVALID_ARG;
     }
     if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
     if (w_dt == MOE_Q4_A64 && (d % 64 || F % 64)) return MOE_ERR_INVALID_ARG;
+    if (w_dt == MOE_Q4_K && (d % 256 || F % 256)) return MOE_ERR_INVALID_ARG;   // whole super-blocks
     if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL &&
         path != MOE_PATH_DECODE_SIMT)
         return MOE_ERR_INVALID_ARG;
@@ -151,7 +152,7 @@ moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, con
     if (!w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
     if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
         return MOE_ERR_INVALID_ARG;
-    if (w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64) {
+    if (w_dt == MOE_Q8_0 || is_q4(w_dt)) {
         const uintptr_t m = 255u;
         if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
             (reinterpret_cast<uintptr_t>(w_down) & m))
@@ -280,6 +281,22 @@ moe_status moe_pack_q4_a64(const void *blocks, long long rows, int cols, void *p
     if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
         return MOE_ERR_INVALID_ARG;
     cudaError_t e = launch_pack_q4_a64(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_q4_k_packed_size(long long rows, int cols)
+{
+    if (rows < 0 || cols <= 0 || cols % 256) return 0;
+    return q4_k_packed_bytes(rows, cols);
+}
+
+moe_status moe_pack_q4_k(const void *blocks, long long rows, int cols, void *packed, moe_stream stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 256) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    cudaError_t e = launch_pack_q4_k(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -428,12 +445,12 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // the clustered router writes grouped rows only as fp16, for the 4-bit
     // tensor-core decode kernels, and only for up to 16 tokens: beyond that a
     // separate gather kernel writes them sooner than the router's owners do
-    const bool router_rows = w_dt == MOE_Q4_A64 && T <= kRouteSmallRowsMaxT;
+    const bool router_rows = is_q4(w_dt) && T <= kRouteSmallRowsMaxT;
     ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && (!fused_small || router_rows)) ? ws + L.xp
                                                                                                 : nullptr;
     // the Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels take fp16
     // rows (scaled)
-    ra.xp_fp16 = w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64;
+    ra.xp_fp16 = w_dt == MOE_Q8_0 || is_q4(w_dt);
     ra.xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     // the fused decode kernel's flags and ticket start at zero
@@ -528,7 +545,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.perm_w = perm_w;
         int32_t *xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
         a.xexp = xexp;
-        const int q4 = w_dt == MOE_Q4_A64;
+        const int q4 = is_q4(w_dt);
         if (fused_small && !q4) {
             a.x_gather = x;   // (the 4-bit kernels take fp16 token rows by TMA from xp)
         } else if (!xp_ready &&

@@ -71,7 +71,7 @@ template <> struct RawW<__nv_bfloat16> { uint4 a; };
 struct Q8Tag {};   // Q8_0 planes: int8 q plane + fp16 scale per 32 values
 template <> struct RawW<Q8Tag> { uint2 q; float s; };
 struct Q4Tag {};   // affine 4-bit planes: codes + fp16 scale and bias per 64 values
-template <> struct RawW<Q4Tag> { uint32_t q; float s, b; };
+template <> struct RawW<Q4Tag> { uint32_t q; float s, b, z; };
 
 // Weight matrix view: row-major [rows, cols] in one of the storage types.
 template <typename WT> struct WView {
@@ -134,63 +134,87 @@ template <> struct WView<Q8Tag> {
 // Affine 4-bit view: q points at the code plane [rows, cols/2] (value 2j in the
 // low nibble of byte j); fp16 scale and bias planes [cols/64, rows].  Set by
 // the host.
-// Packed affine 4-bit weights (moe_pack_q4_a64) are tiles of 128 rows x 64
-// columns (one group), 4608 bytes each, in row-tile-major order: tile (rt, g)
-// at ((rt * groups) + g) * 4608; inside, the 128 rows' 32 code bytes, then the
-// 128 fp16 scales, then the 128 fp16 biases.  A k-block of one row tile is one
-// contiguous copy.  Each 32-bit word of a row's codes holds 8 consecutive
-// values, the even ones in nibbles 0-3 and the odd ones in nibbles 4-7
-// (value i in nibble q4_nibble(i)), so that one mask of the word yields two
-// neighbouring values, one per 16-bit half.
-constexpr int kQ4TileRows = 128, kQ4TileBytes = 4608, kQ4ScaleOff = 4096, kQ4BiasOff = 4352;
+// Packed 4-bit weights are tiles of 128 rows x 64 columns in row-tile-major
+// order: tile (rt, kb) at ((rt * groups) + kb) * tile bytes, groups = cols / 64.
+// Inside: the 128 rows' 32 code bytes, then gpr x 128 fp16 scales, then gpr x
+// 128 fp16 biases ([group][row]), where a row's 64 values form gpr affine
+// groups (value = scale * q + bias): one for the affine 4-bit format
+// (moe_pack_q4_a64, 4608-byte tiles), two of 32 for Q4_K (moe_pack_q4_k,
+// 5120-byte tiles).  A k-block of one row tile is one contiguous copy.  Each
+// 32-bit word of a row's codes holds 8 consecutive values, the even ones in
+// nibbles 0-3 and the odd ones in nibbles 4-7 (value i in nibble
+// q4_nibble(i)), so that one mask of the word yields two neighbouring values,
+// one per 16-bit half.
+// the 4-bit storage types (packed tiles) and their affine groups per tile row
+__host__ __device__ __forceinline__ constexpr bool is_q4(int w_dt) { return w_dt == MOE_Q4_A64 || w_dt == MOE_Q4_K; }
+__host__ __device__ __forceinline__ constexpr int q4_gpr(int w_dt) { return w_dt == MOE_Q4_K ? 2 : 1; }
+constexpr int kQ4TileRows = 128, kQ4ScaleOff = 4096;
+constexpr int kQ4TileBytes = 4608, kQ4BiasOff = 4352;   // one group per row (affine 4-bit)
+constexpr int kQ4KTileBytes = 5120;                     // two groups per row (Q4_K)
+__host__ __device__ __forceinline__ constexpr int q4_tile_bytes(int gpr) { return 4096 + 512 * gpr; }
+__host__ __device__ __forceinline__ constexpr int q4_bias_off(int gpr) { return 4096 + 256 * gpr; }
 __host__ __device__ __forceinline__ constexpr int q4_nibble(int i) { return (i >> 1) + 4 * (i & 1); }
-__host__ __device__ __forceinline__ size_t q4_tile_offset(long long row, int g, int groups)
+// The code a tile's bias belongs to: value = scale * (q - z) + bias.  z = 0
+// for the affine 4-bit tiles (the format's own zero point); z = 8 for the
+// Q4_K tiles, whose bias is the value at code 8, the middle of the group's
+// range: its fp16 rounding error is then small, and |q - 8| <= 8 halves the
+// weight of the scale's rounding error (both roundings are systematic over a
+// group).
+__host__ __device__ __forceinline__ constexpr int q4_zero_code(int gpr) { return gpr == 2 ? 8 : 0; }
+__host__ __device__ __forceinline__ size_t q4_tile_offset(long long row, int g, int groups, int gpr = 1)
 {
-    return ((size_t)(row / kQ4TileRows) * (size_t)groups + (size_t)g) * kQ4TileBytes;
+    return ((size_t)(row / kQ4TileRows) * (size_t)groups + (size_t)g) * (size_t)q4_tile_bytes(gpr);
 }
 
 // One 32-bit word of packed codes (8 consecutive values, q4_nibble order) ->
-// 8 fp16 values scale * q + bias in K order.  Masked under the fp16 exponent
-// of 1024 (ulp 1), nibbles 0 and 4 give the pair (1024 + q_0, 1024 + q_1) and
-// nibbles 1 and 5, left in bits 4-7 of each half, (1024 + 16 q_2, 1024 + 16
-// q_3); the word shifted by 8 gives values 4-7 the same way.  One exact fma by
-// (1, 1) or (1/16, 1/16) and the matching offset leaves the codes, a second
-// one gives scale * q + bias with a single rounding.
+// 8 fp16 values scale * (q - z) + bias in K order.  Masked under the fp16
+// exponent of 1024 (ulp 1), nibbles 0 and 4 give the pair (1024 + q_0, 1024 +
+// q_1) and nibbles 1 and 5, left in bits 4-7 of each half, (1024 + 16 q_2,
+// 1024 + 16 q_3); the word shifted by 8 gives values 4-7 the same way.  One
+// exact fma by (1, 1) or (1/16, 1/16) and the matching offset (Q4Fix) leaves
+// q - z, a second one gives scale * (q - z) + bias with a single rounding.
+struct Q4Fix {
+    __half2 lo, hi;   // -(1024 + z) and -(64 + z), in both halves
+    __device__ __forceinline__ explicit Q4Fix(int z)
+        : lo(__float2half2_rn(-1024.0f - (float)z)), hi(__float2half2_rn(-64.0f - (float)z)) {}
+};
 __device__ __forceinline__ uint32_t q4_pair_fp16(uint32_t t, __half2 mul, __half2 add, __half2 sc2, __half2 bi2)
 {
     t |= 0x64006400u;
     const __half2 v = __hfma2(__hfma2(*reinterpret_cast<const __half2 *>(&t), mul, add), sc2, bi2);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
-__device__ __forceinline__ uint4 q4_word_fp16x8(uint32_t w, __half2 sc2, __half2 bi2)
+__device__ __forceinline__ uint4 q4_word_fp16x8(uint32_t w, __half2 sc2, __half2 bi2, Q4Fix fx)
 {
-    const __half2 one2 = __float2half2_rn(1.0f), m1024 = __float2half2_rn(-1024.0f);
-    const __half2 sixteenth2 = __float2half2_rn(0.0625f), m64 = __float2half2_rn(-64.0f);
+    const __half2 one2 = __float2half2_rn(1.0f), sixteenth2 = __float2half2_rn(0.0625f);
     const uint32_t w8 = w >> 8;
-    return make_uint4(q4_pair_fp16(w & 0x000F000Fu, one2, m1024, sc2, bi2),
-                      q4_pair_fp16(w & 0x00F000F0u, sixteenth2, m64, sc2, bi2),
-                      q4_pair_fp16(w8 & 0x000F000Fu, one2, m1024, sc2, bi2),
-                      q4_pair_fp16(w8 & 0x00F000F0u, sixteenth2, m64, sc2, bi2));
+    return make_uint4(q4_pair_fp16(w & 0x000F000Fu, one2, fx.lo, sc2, bi2),
+                      q4_pair_fp16(w & 0x00F000F0u, sixteenth2, fx.hi, sc2, bi2),
+                      q4_pair_fp16(w8 & 0x000F000Fu, one2, fx.lo, sc2, bi2),
+                      q4_pair_fp16(w8 & 0x00F000F0u, sixteenth2, fx.hi, sc2, bi2));
 }
 
 template <> struct WView<Q4Tag> {
     const uint8_t *q;     // packed tiles
     int groups;           // cols / 64
+    int gpr;              // affine groups per row of a tile: 1 (affine 4-bit) or 2 (Q4_K)
     __device__ __forceinline__ void load(size_t row, int col, RawW<Q4Tag> &r) const
     {
-        const uint8_t *t = q + q4_tile_offset((long long)row, col / 64, groups);
+        const uint8_t *t = q + q4_tile_offset((long long)row, col / 64, groups, gpr);
         const int rr = (int)(row % kQ4TileRows);
+        const int g = gpr == 2 ? (col % 64) / 32 : 0;
         uint32_t v;
         asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
                      : "=r"(v) : "l"(t + rr * 32 + (col % 64) / 2));
         r.q = v;
-        r.s = __half2float(reinterpret_cast<const __half *>(t + kQ4ScaleOff)[rr]);
-        r.b = __half2float(reinterpret_cast<const __half *>(t + kQ4BiasOff)[rr]);
+        r.s = __half2float(reinterpret_cast<const __half *>(t + kQ4ScaleOff)[g * kQ4TileRows + rr]);
+        r.b = __half2float(reinterpret_cast<const __half *>(t + q4_bias_off(gpr))[g * kQ4TileRows + rr]);
+        r.z = (float)q4_zero_code(gpr);
     }
     __device__ __forceinline__ static void cvt(const RawW<Q4Tag> &r, Chunk8 &c)
     {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c.v[i] = fmaf(r.s, (float)((r.q >> (4 * q4_nibble(i))) & 15u), r.b);
+        for (int i = 0; i < 8; ++i) c.v[i] = fmaf(r.s, (float)((r.q >> (4 * q4_nibble(i))) & 15u) - r.z, r.b);
     }
 };
 

@@ -354,13 +354,15 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
         WView<__nv_bfloat16> wd{static_cast<const __nv_bfloat16 *>(a.w_down), (size_t)a.F};
         return launch_t<__nv_bfloat16, __nv_bfloat16>(a, wg, wu, wd, stream);
     }
-    if (a.w_dt == MOE_Q4_A64) {
-        // affine 4-bit packed tiles of 128 rows x 64 columns
-        auto view4 = [](const void *p, long long rows, int cols) {
+    if (is_q4(a.w_dt)) {
+        // 4-bit packed tiles of 128 rows x 64 columns (affine 4-bit, Q4_K)
+        const int gpr = q4_gpr(a.w_dt);
+        auto view4 = [gpr](const void *p, long long rows, int cols) {
             (void)rows;
             WView<Q4Tag> v;
             v.q = static_cast<const uint8_t *>(p);
             v.groups = cols / 64;
+            v.gpr = gpr;
             return v;
         };
         return launch_t<__nv_bfloat16, Q4Tag>(a, view4(a.w_gate, (long long)a.E * a.F, a.d),

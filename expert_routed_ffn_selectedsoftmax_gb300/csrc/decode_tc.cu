@@ -72,7 +72,8 @@ constexpr int SLOT = A_BYTES + B_BYTES;         // 20 KB per stage, 1024-aligned
 constexpr int KBMAX = 8;                        // k-blocks per item
 constexpr int THREADS = 192;
 constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
-// Affine 4-bit weights (W4): a stage holds two parts -- k-blocks kb and kb+1 of
+// 4-bit weights (W4: affine 4-bit or Q4_K, both as packed tiles with one or
+// two affine groups per tile row, p.gpr): a stage holds two parts -- k-blocks kb and kb+1 of
 // the item's matrix, or (whole-K gate/up items) the gate and the up tile of one
 // k-block -- so the waits, commits and loop overheads of the MMA issuer and the
 // converters are paid once per two weight tiles.  Layout: two token tiles of 4 KB
@@ -89,15 +90,15 @@ constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the tok
 // fp16 rows of x scaled by 2^-xexp[r] (exact for bf16 digits), and h is kept
 // in fp16 as h * 2^-2 xexp[r], undone in the down epilogue or the combine.
 #ifndef MOE_DTC_STAGES4
-#define MOE_DTC_STAGES4 6
+#define MOE_DTC_STAGES4 5
 #endif
 #ifndef MOE_DTC_NCVT4
 #define MOE_DTC_NCVT4 2
 #endif
 constexpr int STAGES4 = MOE_DTC_STAGES4;
-constexpr int SLOT4 = 17408;                    // 2 x 4096 + 2 x 4608, 1024-aligned
-constexpr int WT_OFF4 = 2 * 4096;               // the two weight tiles
-static_assert(WT_OFF4 + 2 * kQ4TileBytes <= SLOT4 && SLOT4 % 1024 == 0, "W4 stage layout");
+constexpr int SLOT4 = 18432;                    // 2 x 4096 + 2 x 5120, 1024-aligned
+constexpr int WT_OFF4 = 2 * 4096;               // the two weight tiles (4608 or 5120 bytes each)
+static_assert(WT_OFF4 + 2 * kQ4KTileBytes <= SLOT4 && SLOT4 % 1024 == 0, "W4 stage layout");
 constexpr int NCVT4 = MOE_DTC_NCVT4;
 constexpr int THREADS_W4 = 320;                 // + 4 converter warps
 constexpr int kStagesMax = STAGES4 > STAGES ? STAGES4 : STAGES;
@@ -136,6 +137,7 @@ struct Params {
     int T;               // tokens (debug builds: range of perm_tok)
     const uint8_t *w4[2];  // W4: packed tiles of the matrix (GATEUP: gate, up; DOWN: down)
     int groups;            // W4: K / 64, tiles per row tile
+    int gpr;               // W4: affine groups per tile row (1 affine 4-bit, 2 Q4_K)
 };
 
 struct Ctl {
@@ -327,15 +329,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     const int s = it_k % STAGES;
                     if (!mbar_wait(&c.empty[s], ((it_k / STAGES) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                     const int np = w4_parts(p, it, st), ntok = p.fused ? 1 : np;
-                    mbar_expect_tx(&c.full[s], (uint32_t)(np * kQ4TileBytes + ntok * it.nt * BK * 2));
+                    const uint32_t tb = (uint32_t)q4_tile_bytes(p.gpr);
+                    mbar_expect_tx(&c.full[s], (uint32_t)(np * tb + ntok * it.nt * BK * 2));
                     uint8_t *sp = smem + s * SLOT;
                     if (p.fused) {   // gate and up tiles of k-block st
-                        bulk_load(sp + WT_OFF4, p.w4[0] + q4_tile_offset(wrow, st, p.groups), kQ4TileBytes, &c.full[s]);
-                        bulk_load(sp + WT_OFF4 + kQ4TileBytes, p.w4[1] + q4_tile_offset(wrow, st, p.groups),
-                                  kQ4TileBytes, &c.full[s]);
+                        bulk_load(sp + WT_OFF4, p.w4[0] + q4_tile_offset(wrow, st, p.groups, p.gpr), tb, &c.full[s]);
+                        bulk_load(sp + WT_OFF4 + tb, p.w4[1] + q4_tile_offset(wrow, st, p.groups, p.gpr), tb,
+                                  &c.full[s]);
                     } else {         // k-blocks kb, kb + 1: adjacent tiles
-                        bulk_load(sp + WT_OFF4, p.w4[it.m] + q4_tile_offset(wrow, it.kb0 + 2 * st, p.groups),
-                                  (uint32_t)(np * kQ4TileBytes), &c.full[s]);
+                        bulk_load(sp + WT_OFF4, p.w4[it.m] + q4_tile_offset(wrow, it.kb0 + 2 * st, p.groups, p.gpr),
+                                  np * tb, &c.full[s]);
                     }
                     for (int j = 0; j < ntok; ++j) {
                         int m, kb, tt;
@@ -440,9 +443,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         // a warp may access only the TMEM lanes of its quadrant (warp % 4): warp w
         // converts rows 32 (w % 4) .. +31 of every weight tile, lane = row:
         // 64 codes -> scale * q + bias in fp16 -> 32 columns of its TMEM lane.
-        // (q4_word_fp16x8: one packed word -> 8 fp16 weights, two exact fma steps)
+        // (q4_word_fp16x8: one packed word -> 8 fp16 weights, an exact fma and a rounded one)
         const int quad = warp & 3, row = quad * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + A_COL4;
+        const Q4Fix fx(q4_zero_code(p.gpr));
         uint32_t it_k = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -456,17 +460,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     break;
                 }
                 const int np = w4_parts(p, it, st);
+                const int tb = q4_tile_bytes(p.gpr), g1 = p.gpr - 1;   // g1: the second group's index
                 for (int j = 0; j < np; ++j) {
-                    const uint8_t *wt = smem + s * SLOT + WT_OFF4 + j * kQ4TileBytes;
+                    const uint8_t *wt = smem + s * SLOT + WT_OFF4 + j * tb;
                     const uint4 q0 = *reinterpret_cast<const uint4 *>(wt + row * 32);
                     const uint4 q1 = *reinterpret_cast<const uint4 *>(wt + row * 32 + 16);
-                    const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(wt + kQ4ScaleOff)[row]);
-                    const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(wt + kQ4BiasOff)[row]);
+                    // scale and bias of values 0-31 and of values 32-63 (the same with one group)
+                    const __half *scp = reinterpret_cast<const __half *>(wt + kQ4ScaleOff);
+                    const __half *bip = reinterpret_cast<const __half *>(wt + q4_bias_off(p.gpr));
+                    const __half2 sc2[2] = {__half2half2(scp[row]), __half2half2(scp[g1 * BM + row])};
+                    const __half2 bi2[2] = {__half2half2(bip[row]), __half2half2(bip[g1 * BM + row])};
                     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                     uint32_t o[32];   // column c: values 2c, 2c+1
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {   // values 8ch .. 8ch+7
-                        const uint4 v = q4_word_fp16x8(w[ch], sc2, bi2);
+                        const uint4 v = q4_word_fp16x8(w[ch], sc2[ch >> 2], bi2[ch >> 2], fx);
                         o[4 * ch + 0] = v.x; o[4 * ch + 1] = v.y; o[4 * ch + 2] = v.z; o[4 * ch + 3] = v.w;
                     }
                     tmem_st16(t_lane + cb * 64 + j * 32, *reinterpret_cast<const uint32_t(*)[16]>(&o[0]));
@@ -738,7 +746,7 @@ int choose_splits(int kb_total, long long units)
 
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q4_A64) && d % 128 == 0 &&
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt)) && d % 128 == 0 &&
            F % 128 == 0 && E <= kMaxExperts && tc_gemm_available();
 }
 
@@ -776,7 +784,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     int ks_gu, ks_d;
     decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
 
-    const bool w4 = a.w_dt == MOE_Q4_A64;
+    const bool w4 = is_q4(a.w_dt);
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // token rows and h: fp16 on the 4-bit path
     const CUtensorMapDataType rowt = w4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
@@ -833,6 +841,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     p.w4[0] = static_cast<const uint8_t *>(a.w_gate);
     p.w4[1] = static_cast<const uint8_t *>(a.w_up);
     p.groups = a.d / 64;
+    p.gpr = q4_gpr(a.w_dt);
     // upper bound on items: chunks <= n_exp + rows / NTMAX
     const long long chunks = n_exp + rows / NTMAX;
 

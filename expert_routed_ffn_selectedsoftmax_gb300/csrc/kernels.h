@@ -168,6 +168,9 @@ cudaError_t launch_pack_q8_0(const void *blocks, long long rows, int cols, void 
                              cudaStream_t stream);
 // q8.cu -- affine 4-bit group-64 weights repacked into tiles (codes, fp16 scales, biases)
 size_t q4_a64_packed_bytes(long long rows, int cols);   // tiles of 128 rows x 64 columns
+size_t q4_k_packed_bytes(long long rows, int cols);     // the same tiles, two groups per row
+cudaError_t launch_pack_q4_k(const void *blocks, long long rows, int cols, void *packed,
+                             cudaStream_t stream);
 cudaError_t launch_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
                                cudaStream_t stream);
 

@@ -92,6 +92,92 @@ __global__ void pack_q4_a64_kernel(const uint8_t *__restrict__ blocks, long long
     }
 }
 
+// Q4_K super-blocks ("zonos2.cpp internals", §Recommended: F16 spine + K-quant
+// experts; the GGUF layout: fp16 d, fp16 dmin, 12 bytes of six-bit sub-block
+// scales and mins, 128 bytes of codes, sub-block j = values 32j .. 32j+31
+// decoding as d * sc[j] * q - dmin * m[j]) -> tiles of 128 rows x 64 columns
+// with two affine groups per row: group g of tile column block kb is
+// sub-block j = 2 (kb % 4) + g of super-block kb / 4, scale = d * sc[j] and
+// bias = 8 d sc[j] - dmin m[j] (the value at code 8: value = scale * (q - 8)
+// + bias), each rounded to fp16.  One thread per (tile, row).
+__global__ void pack_q4_k_kernel(const uint8_t *__restrict__ blocks, long long rows, int groups,
+                                 long long n, uint8_t *__restrict__ packed)
+{
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long tile = t / kQ4TileRows;
+        const int rr = (int)(t - tile * kQ4TileRows);
+        const long long rt = tile / groups;
+        const int kb = (int)(tile - rt * groups);
+        const long long row = rt * kQ4TileRows + rr;
+        uint8_t *dst = packed + (size_t)tile * kQ4KTileBytes;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint16_t sc16[2] = {0, 0}, bi16[2] = {0, 0};
+        if (row < rows) {
+            const uint8_t *blk = blocks + ((size_t)row * (groups / 4) + kb / 4) * 144;
+            const float d = __half2float(__ushort_as_half((uint16_t)(blk[0] | (blk[1] << 8))));
+            const float dmin = __half2float(__ushort_as_half((uint16_t)(blk[2] | (blk[3] << 8))));
+            const uint8_t *s = blk + 4;
+            const uint8_t *run = blk + 16 + 32 * (kb % 4);   // sub-block 2c low, 2c+1 high nibbles
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int j = 2 * (kb % 4) + g;
+                int sc, m;
+                if (j < 4) {
+                    sc = s[j] & 63;
+                    m = s[j + 4] & 63;
+                } else {
+                    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+                    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+                }
+                // both products exact in fp32 (11-bit d or dmin times a 6-bit integer)
+                const float s32 = d * (float)sc, mb = dmin * (float)m;
+                sc16[g] = __half_as_ushort(__float2half_rn(s32));
+                bi16[g] = __half_as_ushort(__float2half_rn(8.0f * s32 - mb));   // the value at code 8
+
+            }
+            // value v of the 64: v < 32 the low nibble of run[v], else the high nibble of run[v - 32]
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {   // word i: values 8i .. 8i+7
+                uint32_t word = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int v = 8 * i + e;
+                    const uint32_t q = v < 32 ? (run[v] & 15u) : (run[v - 32] >> 4);
+                    word |= q << (4 * q4_nibble(e));
+                }
+                w[i] = word;
+            }
+        }
+        uint4 *c = reinterpret_cast<uint4 *>(dst + rr * 32);
+        c[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        c[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        uint16_t *scp = reinterpret_cast<uint16_t *>(dst + kQ4ScaleOff);
+        uint16_t *bip = reinterpret_cast<uint16_t *>(dst + q4_bias_off(2));
+        scp[rr] = sc16[0]; scp[kQ4TileRows + rr] = sc16[1];
+        bip[rr] = bi16[0]; bip[kQ4TileRows + rr] = bi16[1];
+    }
+}
+
+size_t q4_k_packed_bytes(long long rows, int cols)
+{
+    const long long tiles_r = (rows + kQ4TileRows - 1) / kQ4TileRows;
+    return (size_t)tiles_r * (size_t)(cols / 64) * kQ4KTileBytes;
+}
+
+cudaError_t launch_pack_q4_k(const void *blocks, long long rows, int cols, void *packed,
+                             cudaStream_t stream)
+{
+    const int groups = cols / 64;
+    const long long n = (rows + kQ4TileRows - 1) / kQ4TileRows * groups * kQ4TileRows;
+    if (n == 0) return cudaSuccess;
+    long long grid = (n + 255) / 256;
+    if (grid > 65535LL * 16) grid = 65535LL * 16;
+    pack_q4_k_kernel<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), rows,
+                                                         groups, n, static_cast<uint8_t *>(packed));
+    return cudaGetLastError();
+}
+
 size_t q4_a64_packed_bytes(long long rows, int cols)
 {
     const long long tiles_r = (rows + kQ4TileRows - 1) / kQ4TileRows;

@@ -123,7 +123,8 @@ template <int WQ, bool PAIR> struct Cfg {
     static constexpr int CL = PAIR ? 2 : 1;
     static constexpr int BNL = BN / CL;             // B rows held by this CTA
     static constexpr int B_BYTES = BNL * BK * 2;    // 16-bit B (this CTA's rows)
-    static constexpr int BQ_BYTES = WQ == WQ4 ? (BNL / kQ4TileRows) * kQ4TileBytes : BNL * BK;   // packed B
+    // packed B (4-bit: room for the larger, Q4_K, tiles)
+    static constexpr int BQ_BYTES = WQ == WQ4 ? (BNL / kQ4TileRows) * kQ4KTileBytes : BNL * BK;
     static constexpr int SCL_BYTES = WQ == WQ4 ? 0 : SC_BYTES / CL;   // Q8_0 scales
     static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SCL_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
@@ -157,6 +158,7 @@ struct Params {
     uint32_t *status;
     int h_fp16;               // GATEUP: write h as fp16 (else bf16)
     const uint8_t *q4[3];     // 4-bit: packed tiles of W_g, W_u, W_d
+    int gpr;                  // 4-bit: affine groups per tile row (1 affine 4-bit, 2 Q4_K)
     const int32_t *xexp;      // fp16 rows (Q8_0, 4-bit): row r of the grouped x is scaled by 2^-xexp[r];
                               // h is written scaled by 2^-2 xexp[r], undone in the down epilogue
     float *out_zero;          // GATEUP: `out` to zero for the down kernel's adds, or null
@@ -368,24 +370,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     else tma_load_2d_pair(sb, &tm_b0, bar0, kb * BK, drow);
                     continue;
                 }
-                mbar_expect_tx(&c.full[s], A_BYTES + (Q8 ? C::BQ_BYTES + C::SCL_BYTES : C::B_BYTES));
+                const uint32_t tb = (uint32_t)q4_tile_bytes(p.gpr);   // (4-bit)
+                mbar_expect_tx(&c.full[s], A_BYTES + (WQ == WQ4 ? (BNL / kQ4TileRows) * tb
+                                                      : Q8 ? C::BQ_BYTES + C::SCL_BYTES : C::B_BYTES));
                 tma_load_2d(st, &tm_a, &c.full[s], kb * BK, arow);
                 if constexpr (WQ == WQ4) {
                     // this CTA's packed 128-row tiles of k-block kb, one copy each
                     const int groups = p.K / 64;
                     if (MODE == GATEUP) {
                         if (PAIR) {
-                            bulk_load(sb, p.q4[rank] + q4_tile_offset(grow, kb, groups), kQ4TileBytes, &c.full[s]);
+                            bulk_load(sb, p.q4[rank] + q4_tile_offset(grow, kb, groups, p.gpr), tb, &c.full[s]);
                         } else {
-                            bulk_load(sb, p.q4[0] + q4_tile_offset(grow, kb, groups), kQ4TileBytes, &c.full[s]);
-                            bulk_load(sb + kQ4TileBytes, p.q4[1] + q4_tile_offset(grow, kb, groups), kQ4TileBytes,
-                                      &c.full[s]);
+                            bulk_load(sb, p.q4[0] + q4_tile_offset(grow, kb, groups, p.gpr), tb, &c.full[s]);
+                            bulk_load(sb + tb, p.q4[1] + q4_tile_offset(grow, kb, groups, p.gpr), tb, &c.full[s]);
                         }
                     } else {
 #pragma unroll
                         for (int t = 0; t < BNL / kQ4TileRows; ++t)
-                            bulk_load(sb + t * kQ4TileBytes, p.q4[2] + q4_tile_offset(drow + t * kQ4TileRows, kb, groups),
-                                      kQ4TileBytes, &c.full[s]);
+                            bulk_load(sb + t * tb, p.q4[2] + q4_tile_offset(drow + t * kQ4TileRows, kb, groups, p.gpr),
+                                      tb, &c.full[s]);
                     }
                     continue;
                 }
@@ -489,6 +492,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         // of this CTA's B rows
         const int cw = warp - 2 - kEpiWarps;
         const int rsub = lane >> 2, q = lane & 3;
+        const Q4Fix fx(q4_zero_code(p.gpr));   // (4-bit weights only)
         uint32_t it = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += nclusters) {
@@ -505,15 +509,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 #pragma unroll
                     for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
                         const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
-                        const uint8_t *t = bq + (r / kQ4TileRows) * kQ4TileBytes;
+                        const uint8_t *t = bq + (r / kQ4TileRows) * q4_tile_bytes(p.gpr);
                         const int rr = r % kQ4TileRows;
+                        // values 16q .. 16q+15 lie in group q / 2 of two (Q4_K), else in the one group
+                        const int gi = (p.gpr - 1) * (q >> 1) * kQ4TileRows + rr;
                         const uint2 v = *reinterpret_cast<const uint2 *>(t + rr * 32 + q * 8);
-                        const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(t + kQ4ScaleOff)[rr]);
-                        const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(t + kQ4BiasOff)[rr]);
+                        const __half2 sc2 = __half2half2(reinterpret_cast<const __half *>(t + kQ4ScaleOff)[gi]);
+                        const __half2 bi2 = __half2half2(reinterpret_cast<const __half *>(t + q4_bias_off(p.gpr))[gi]);
                         *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q) ^ (r & 7)) << 4)) =
-                            q4_word_fp16x8(v.x, sc2, bi2);
+                            q4_word_fp16x8(v.x, sc2, bi2, fx);
                         *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4)) =
-                            q4_word_fp16x8(v.y, sc2, bi2);
+                            q4_word_fp16x8(v.y, sc2, bi2, fx);
                     }
                     fence_proxy_async_smem();
                     warp_arrive<PAIR>(&c.cfull[cb], lane);
@@ -753,7 +759,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 }  // namespace tc
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
-bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || w_dt == MOE_Q4_A64; }
+bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt); }
 
 bool tc_gemm_prefer(int T, int d, int E, int k, int F)
 {
@@ -816,7 +822,7 @@ static int max_active_pairs()
 
 bool tc_gemm_pairs(moe_dtype w_dt)
 {
-    const bool q8 = w_dt == MOE_Q8_0, q4 = w_dt == MOE_Q4_A64;
+    const bool q8 = w_dt == MOE_Q8_0, q4 = is_q4(w_dt);
     if (MOE_GEMM_PAIR == 0 || (MOE_GEMM_PAIR == 1 && !q8 && !q4)) return false;
     if constexpr (MOE_GEMM_PAIR >= 2) {
         if (!q8 && !q4)
@@ -874,7 +880,7 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
 {
     using namespace tc;
-    const bool q8 = a.w_dt == MOE_Q8_0, q4 = a.w_dt == MOE_Q4_A64;
+    const bool q8 = a.w_dt == MOE_Q8_0, q4 = is_q4(a.w_dt);
     const bool f16 = q8 || q4;   // fp16 operands (converted weights)
     if (!f16 && a.w_dt != MOE_BF16) return cudaErrorNotSupported;
     const int rows = a.T * a.k;
@@ -935,6 +941,7 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     p.q4[0] = static_cast<const uint8_t *>(a.w_gate);
     p.q4[1] = static_cast<const uint8_t *>(a.w_up);
     p.q4[2] = static_cast<const uint8_t *>(a.w_down);
+    p.gpr = q4_gpr(a.w_dt);
     p.out_zero = a.zero_out ? a.out : nullptr;
     p.zero4 = (long long)a.T * a.d / 4;
     p.expire_ns = a.expire_ns;

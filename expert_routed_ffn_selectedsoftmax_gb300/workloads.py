@@ -109,6 +109,18 @@ WORKLOADS = {
                     "MLX build's expert format): T=4096, d=2048, E=16, top-1, "
                     "F=2816, bf16 activations and router (4 independent layers "
                     "per benchmark step)"),
+    "zonos2_decode_q4k": Workload(
+        "zonos2_decode_q4k", T=8, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q4_K, bias="normal", bias_sd=0.1, layers=28,
+        description="ZONOS2-shaped decode step with Q4_K experts (the K-quant the "
+                    "pages recommend for the expert stacks): d=2048, E=16, top-1, "
+                    "F=2816, T in {1, 8, 64}, 28-layer weight rotation"),
+    "zonos2_prefill_q4k": Workload(
+        "zonos2_prefill_q4k", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q4_K, bias="normal", bias_sd=0.1, layers=4,
+        description="ZONOS2-shaped prefill with Q4_K experts: T=4096, d=2048, E=16, "
+                    "top-1, F=2816, bf16 activations and router (4 independent "
+                    "layers per benchmark step)"),
 }
 
 
@@ -390,6 +402,39 @@ def q4_a64_quantize_torch(w):
     return out
 
 
+def q4_k_quantize_torch(w):
+    """Device twin of q4_k_quantize: float32 [..., K] -> uint8 super-blocks
+    [..., K/256, 144] (same layout and rounding rules)."""
+    import torch
+    K = w.shape[-1]
+    g = w.reshape(*w.shape[:-1], K // Q4_K_BLOCK, 8, 32).double()
+    mn = torch.clamp(-g.amin(-1), min=0.0)
+    step = (g.amax(-1) + mn) / 15.0
+    d16 = (step.amax(-1) / 63.0).to(torch.float16)
+    dmin16 = (mn.amax(-1) / 63.0).to(torch.float16)
+    d, dmin = d16.double(), dmin16.double()
+    one = torch.ones_like(d)
+    sd = torch.where(d > 0, d, one)[..., None]
+    smin = torch.where(dmin > 0, dmin, one)[..., None]
+    sc = torch.where(d[..., None] > 0, torch.clamp(torch.floor(step / sd + 0.5), 0, 63), torch.zeros_like(step))
+    m = torch.where(dmin[..., None] > 0, torch.clamp(torch.floor(mn / smin + 0.5), 0, 63), torch.zeros_like(mn))
+    a = d[..., None] * sc
+    b = dmin[..., None] * m
+    v = (g + b[..., None]) / torch.where(a > 0, a, torch.ones_like(a))[..., None]
+    q = torch.where(a[..., None] > 0, torch.clamp(torch.sign(v) * torch.floor(v.abs() + 0.5), 0, 15),
+                    torch.zeros_like(v)).to(torch.uint8)
+    sc8, m8 = sc.to(torch.uint8), m.to(torch.uint8)
+    out = torch.empty(*g.shape[:-2], Q4_K_BLOCK_BYTES, dtype=torch.uint8, device=w.device)
+    out[..., 0:2] = d16.contiguous().view(torch.uint8).reshape(*d16.shape, 2)
+    out[..., 2:4] = dmin16.contiguous().view(torch.uint8).reshape(*dmin16.shape, 2)
+    out[..., 4:8] = (sc8[..., 0:4] & 63) | ((sc8[..., 4:8] >> 4) << 6)
+    out[..., 8:12] = (m8[..., 0:4] & 63) | ((m8[..., 4:8] >> 4) << 6)
+    out[..., 12:16] = (sc8[..., 4:8] & 15) | ((m8[..., 4:8] & 15) << 4)
+    runs = q.reshape(*q.shape[:-2], 4, 2, 32)
+    out[..., 16:] = (runs[..., 0, :] | (runs[..., 1, :] << 4)).reshape(*q.shape[:-2], 128)
+    return out
+
+
 def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = None,
                       device="cuda", zipf_biases=None):
     """Draw ``layers`` independent layers directly in device memory.
@@ -403,8 +448,8 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
     layer's host-drawn x and W_r (zipf_host_inputs), which are used then.
     """
     import torch
-    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (F32, F32)):
-        raise ValueError("device stacks: bf16/bf16, bf16/Q8_0, bf16/Q4_A64 or fp32/fp32 layers")
+    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (BF16, Q4_K), (F32, F32)):
+        raise ValueError("device stacks: bf16/bf16, bf16/Q8_0, bf16/Q4_A64, bf16/Q4_K or fp32/fp32 layers")
     act = torch.float32 if w.act_dtype == F32 else torch.bfloat16
     T = w.T if T is None else T
     g = torch.Generator(device=device)
@@ -415,7 +460,8 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
         def rn(*shape, sd=1.0, q8=False):
             t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * sd
             if q8:
-                return q4_a64_quantize_torch(t) if w.w_dtype == Q4_A64 else q8_0_quantize_torch(t)
+                return {Q4_A64: q4_a64_quantize_torch, Q4_K: q4_k_quantize_torch,
+                        Q8_0: q8_0_quantize_torch}[w.w_dtype](t)
             return t.to(act)
         d, E, F = w.d, w.E, w.F
         x = rn(T, d)
@@ -430,7 +476,7 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             b = torch.from_numpy(zipf_bias(E, rng)).to(device)
         else:
             b = torch.randn(E, generator=g, device=device, dtype=torch.float32) * w.bias_sd
-        q8 = w.w_dtype in (Q8_0, Q4_A64)   # block-quantised expert weights
+        q8 = w.w_dtype in (Q8_0, Q4_A64, Q4_K)   # block-quantised expert weights
         wg = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wu = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wd = rn(E, d, F, sd=1.0 / math.sqrt(F), q8=q8)

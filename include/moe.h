@@ -28,7 +28,7 @@
  *    (1..256), k experts per token (1..min(E, 8)), F expert ffn width.
  *  - Activation storage (x, W_r): MOE_F32 or MOE_BF16; logits, routing
  *    weights and the output are fp32.  Expert weights: MOE_F32 (with F32
- *    activations), MOE_BF16, MOE_Q8_0 or MOE_Q4_A64 (with BF16 activations).
+ *    activations), MOE_BF16, MOE_Q8_0, MOE_Q4_A64 or MOE_Q4_K (with BF16 activations).
  *  - Calls on distinct workspaces and outputs are independent; there is no
  *    global mutable state.
  */
@@ -61,7 +61,7 @@ typedef enum {
     MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (see moe_check) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3, MOE_Q4_K = 4 } moe_dtype;
 
 /* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
  * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16 or
@@ -206,6 +206,39 @@ MOE_API moe_status moe_pack_q4_a64(const void *blocks, long long rows, int cols,
                                    moe_stream stream);
 
 /*
+ * Q4_K expert weights (MOE_Q4_K): the K-quant the pages recommend for the
+ * expert stacks ("zonos2.cpp internals", §Recommended: F16 spine + K-quant
+ * experts: Q4_K at 4.50 bits per weight is the usable floor; the pages give
+ * no byte layout, this is the GGUF one).  Input format: rows of `cols`
+ * values (cols % 256 == 0), stored as cols/256 super-blocks of 144 bytes
+ * {fp16 d, fp16 dmin (little endian), 12 bytes of six-bit sub-block scales
+ * sc[8] and mins m[8], 128 bytes of 4-bit codes}; sub-block j holds values
+ * 32j .. 32j+31 and decodes as d * sc[j] * q - dmin * m[j].  Six-bit fields:
+ * for j < 4, sc[j] and m[j] are the low 6 bits of bytes j and j+4; for
+ * j >= 4, sc[j] = (low nibble of byte j+4) + 16 * (top 2 bits of byte j-4)
+ * and m[j] = (high nibble of byte j+4) + 16 * (top 2 bits of byte j).
+ * Codes: the 32-byte run c (c = 0..3) holds sub-block 2c in its low nibbles
+ * and 2c+1 in its high nibbles, value i of each in byte i of the run.
+ * Used like MOE_Q4_A64 (BF16 activations; tensor-core decode kernels, grouped
+ * GEMMs, CUDA-core decode kernels) with d and F multiples of 256.
+ * moe_forward consumes them repacked by moe_pack_q4_k into the tiles of
+ * MOE_Q4_A64 (128 rows x 64 columns, same code words) with two affine groups
+ * per tile row: bytes [0, 4096) codes, [4096, 4608) fp16 scales [2][128]
+ * (group 0: values 0-31 of the tile row, group 1: values 32-63), [4608, 5120)
+ * fp16 biases [2][128]; a value decodes as scale * (q - 8) + bias with
+ * scale = fp16(d * sc[j]) and bias = fp16(8 d sc[j] - dmin m[j]), the value at
+ * code 8 (the middle of the group's range, so that the two fp16 roundings
+ * stay small; the tensor-core kernels then round each weight once more, to
+ * fp16).
+ * moe_q4_k_packed_size returns ceil(rows / 128) * (cols / 64) * 5120 (0 if
+ * cols % 256 != 0 or rows < 0); moe_pack_q4_k repacks `blocks` (device, any
+ * alignment) into `packed` (device, 256-byte aligned) on `stream`.
+ */
+MOE_API size_t moe_q4_k_packed_size(long long rows, int cols);
+MOE_API moe_status moe_pack_q4_k(const void *blocks, long long rows, int cols, void *packed,
+                                 moe_stream stream);
+
+/*
  * Bytes of device workspace moe_forward needs for these sizes (any path).
  * 0 on invalid sizes.  The workspace is scratch owned by the caller; its
  * first 256 bytes hold the device status word read by moe_check.
@@ -239,8 +272,9 @@ MOE_API moe_status moe_workspace_views(int T, int d, int E, int k, int F, moe_dt
 /*
  * moe_forward -- the whole layer, steps 1-5.
  *   x[T,d] (act_dt), w_router[E,d] (act_dt), sel_bias[E] fp32 or NULL,
- *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64: the
- *   buffers written by moe_pack_q8_0 / moe_pack_q4_a64, 256-byte aligned),
+ *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K: the
+ *   buffers written by moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k, 256-byte
+ *   aligned),
  *   out[T,d] fp32 (overwritten).
  *   workspace: device scratch of at least moe_workspace_size() bytes,
  *   256-byte aligned; it must not be shared by calls that can overlap.
@@ -295,8 +329,8 @@ MOE_API moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, in
  *   §Model architecture: dense FFN layers beside the MoE ones; "New Community
  *   Model: ZONOS3-Mini (Zyphra) - #1271", §Summary: layer 0 has a dense SwiGLU
  *   FFN).  No router: every token goes to the one expert with weight 1.
- *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64: packed by
- *   moe_pack_q8_0 / moe_pack_q4_a64 with rows = F or d); other arguments as
+ *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K: packed by
+ *   moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k with rows = F or d); other arguments as
  *   moe_forward, with a workspace of moe_workspace_size(T, d, 1, 1, F, act_dt,
  *   w_dt) bytes.
  */

@@ -107,6 +107,16 @@ def test_argument_errors_are_synchronous(lib):
     # one row tile (rows padded to 128) x 2 groups, 4608 bytes per tile
     assert lib.moe_q4_a64_packed_size(4, 128) == 2 * 4608
     assert lib.moe_q4_a64_packed_size(129, 64) == 2 * 4608
+    assert fwd(wdt=4, F=128) == I                # Q4_K needs whole 256-value super-blocks: F % 256
+    assert fwd(wdt=4, d=384, F=256) == I         #   and d % 256
+    assert fwd(act=0, wdt=4, F=256) == U         # Q4_K takes bf16 activations
+    assert lib.moe_pack_q4_k(fake, 4, 192, fake, None) == I       # cols % 256
+    assert lib.moe_pack_q4_k(fake, 4, 256, vp(0x10010), None) == I
+    assert lib.moe_q4_k_packed_size(4, 192) == 0
+    assert lib.moe_q4_k_packed_size(-1, 256) == 0
+    # one row tile x 4 tile columns, 5120 bytes per tile (two scale/bias pairs a row)
+    assert lib.moe_q4_k_packed_size(4, 256) == 4 * 5120
+    assert lib.moe_q4_k_packed_size(129, 512) == 2 * 8 * 5120
     assert fwd(path=9) == I
     assert fwd(wg=None) == I
     assert fwd(ws=vp(0x10010)) == I              # workspace not 256-byte aligned

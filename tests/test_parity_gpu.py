@@ -142,6 +142,10 @@ SMALL = [
     (wl.BF16, wl.Q4_A64, 33, 256, 16, 2, 256),
     (wl.BF16, wl.Q4_A64, 128, 1024, 64, 2, 512),
     (wl.BF16, wl.Q4_A64, 300, 512, 16, 4, 384),
+    (wl.BF16, wl.Q4_K, 5, 256, 8, 2, 256),      # Q4_K experts: two (scale, bias) pairs per
+    (wl.BF16, wl.Q4_K, 70, 512, 16, 1, 256),    #   tile row, whole 256-value super-blocks
+    (wl.BF16, wl.Q4_K, 128, 1024, 64, 2, 512),
+    (wl.BF16, wl.Q4_K, 300, 512, 16, 4, 768),
     (wl.BF16, wl.BF16, 5, 512, 64, 8, 128),     # few tokens: largest E and k of the small-batch router
     (wl.BF16, wl.BF16, 8, 2048, 33, 3, 128),    # few tokens: ragged E, longest rows
     (wl.BF16, wl.BF16, 40, 256, 256, 8, 128),   # the largest E and k the library takes
@@ -242,7 +246,8 @@ def test_device_status_ok_after_forward():
 FULL_CASES = [("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode", 1),
               ("zonos2_decode", 8), ("zonos2_decode", 64), ("zonos3_mini_prefill", None),
               ("zonos2_prefill_q8", None), ("zonos2_decode_q4", 1), ("zonos2_decode_q4", 8),
-              ("zonos2_decode_q4", 64), ("zonos2_prefill_q4", None)]
+              ("zonos2_decode_q4", 64), ("zonos2_prefill_q4", None), ("zonos2_decode_q4k", 1),
+              ("zonos2_decode_q4k", 8), ("zonos2_decode_q4k", 64), ("zonos2_prefill_q4k", None)]
 
 
 @pytest.mark.parametrize("seed", [2, 7, 13])
@@ -263,7 +268,8 @@ def test_forward_workloads_full(name, T, seed):
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8", "zonos2_prefill_q4"])
+@pytest.mark.parametrize("name", ["zonos3_mini_prefill", "zonos2_prefill_q8", "zonos2_prefill_q4",
+                                  "zonos2_prefill_q4k"])
 def test_forward_prefill_workloads_on_decode_path(name):
     """The prefill workloads at full size through the decode path (CUDA-core
     kernels at these row counts): grouping and every output row."""
@@ -275,7 +281,8 @@ def test_forward_prefill_workloads_on_decode_path(name):
 
 
 @pytest.mark.parametrize("name", ["zonos3_mini_decode", "zonos2_decode", "zonos3_mini_prefill",
-                                  "zonos2_prefill_q8", "zonos2_decode_q4", "zonos2_prefill_q4"])
+                                  "zonos2_prefill_q8", "zonos2_decode_q4", "zonos2_prefill_q4",
+                                  "zonos2_decode_q4k", "zonos2_prefill_q4k"])
 def test_graph_replay_equals_direct_launch(name):
     """The benchmark times CUDA-graph replays of the layer (warm-up launches on a
     side stream, capture on that stream, replay): at full size, a replay writes
@@ -331,6 +338,18 @@ def test_forward_prefill_small_matches_oracle(T, d, E, k, F, wdt):
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
+@pytest.mark.parametrize("T,d,E,k,F", [c for c in PREFILL_SMALL if c[1] % 256 == 0 and c[4] % 256 == 0])
+def test_forward_prefill_small_q4_k_matches_oracle(T, d, E, k, F):
+    """Q4_K experts on the grouped GEMMs (the shapes above with whole
+    256-value super-blocks along d and F)."""
+    layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
+                                 w_dtype=wl.Q4_K, bias_sd=0.5)
+    out, r = gpu_forward_views(layer, DEV, path=PREFILL)
+    check_routing_views(r, layer)
+    ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
+    check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
+
+
 def test_prefill_one_expert_many_tiles():
     """Every token to experts 3 and 5: 1100 rows per group, a ragged last tile."""
     layer = wl.make_custom_layer(22, T=1100, d=256, E=8, k=2, F=128, act_dtype=wl.BF16,
@@ -345,7 +364,7 @@ def test_prefill_one_expert_many_tiles():
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64, wl.Q4_K])
 def test_prefill_and_decode_paths_agree(wdt):
     layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
                                  w_dtype=wdt)
@@ -488,7 +507,8 @@ def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
     (DECODE, 40, wl.Q4_A64, 8, 256),      # split-K gate/up + SwiGLU reduction
     (DECODE, 128, wl.Q4_A64, 64, 512),    # whole-K gate/up writing h itself
     (DECODE, 300, wl.Q4_A64, 8, 256),     # rows grouped by the scatter kernel
-    (PREFILL, 600, wl.Q4_A64, 8, 256)])   # 4-bit grouped GEMMs
+    (PREFILL, 600, wl.Q4_A64, 8, 256),    # 4-bit grouped GEMMs
+    (DECODE, 40, wl.Q4_K, 8, 256), (PREFILL, 600, wl.Q4_K, 8, 256)])
 def test_fp16_operands_large_activations(path, T, wdt, E, F):
     """The Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels
     multiply fp16 operands.  Token rows whose magnitudes span 1e-2 .. 1e5 (h
@@ -507,9 +527,12 @@ def test_fp16_operands_large_activations(path, T, wdt, E, F):
     # logits of 1e5-magnitude rows carry the router's fp32 accumulation error
     # (~1e-7 of |logit| ~ 1e4): their weights agree to ~1e-5, not 2e-6
     check_routing_views(r, layer, w_atol=5e-5)
-    # per row: the large rows dominate any global RMS, so each row is held to
-    # the tolerance of its own magnitude
-    for rows in (mag >= 1e3, (mag >= 1) & (mag < 1e3), mag < 1):
+    # per decade of row magnitude: out grows like mag^2, so the largest rows
+    # dominate any wider bin's RMS and each row is held to the tolerance of
+    # rows of its own magnitude
+    decade = np.clip(np.floor(np.log10(mag)), -2, 4)    # mag = 1e5 joins [1e4, 1e5)
+    for lo in np.unique(decade):
+        rows = decade == lo
         if rows.any():
             sub_rows = np.where(rows)[0]
             from helpers import sub_layer
@@ -522,7 +545,9 @@ def test_fp16_operands_large_activations(path, T, wdt, E, F):
     (wl.Q8_0, PREFILL, 256, 4, 1, 128),
     (wl.Q4_A64, DECODE, 256, 4, 1, 128),     # 4-bit: SwiGLU reduction kernel
     (wl.Q4_A64, DECODE, 128, 64, 2, 512),    # 4-bit: whole-K gate/up epilogue
-    (wl.Q4_A64, PREFILL, 256, 4, 1, 128)])   # 4-bit grouped GEMMs
+    (wl.Q4_A64, PREFILL, 256, 4, 1, 128),    # 4-bit grouped GEMMs
+    (wl.Q4_K, DECODE, 256, 4, 1, 256),
+    (wl.Q4_K, PREFILL, 256, 4, 1, 256)])
 def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     """Expert weights large enough that h leaves fp16's range even for
     normalised rows: the call reports MOE_ERR_DEVICE_CHECK instead of
@@ -533,7 +558,8 @@ def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
                                  w_dtype=wl.BF16)
     rng = np.random.default_rng(6)
     big = lambda *s: (rng.standard_normal(s) * 4e3).astype(np.float32)
-    quant = wl.q8_0_quantize if wdt == wl.Q8_0 else wl.q4_a64_quantize
+    quant = {wl.Q8_0: wl.q8_0_quantize, wl.Q4_A64: wl.q4_a64_quantize,
+             wl.Q4_K: wl.q4_k_quantize}[wdt]
     layer.w_dtype = wdt
     layer.w_gate = quant(big(E, F, d))
     layer.w_up = quant(big(E, F, d))
@@ -555,13 +581,14 @@ def ctypes_check(pkg, ws):
                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
+@pytest.mark.parametrize("wdt,F", [(wl.Q4_A64, 384), (wl.Q4_K, 512)])
 @pytest.mark.parametrize("T,k", [(1, 1), (8, 1), (64, 1), (40, 2), (200, 4)])
-def test_q4_tensor_core_decode_reproducible_and_close_to_cuda_core(T, k):
-    """Affine 4-bit experts on the tensor-core decode kernels: bitwise
+def test_q4_tensor_core_decode_reproducible_and_close_to_cuda_core(T, k, wdt, F):
+    """Affine 4-bit and Q4_K experts on the tensor-core decode kernels: bitwise
     reproducible, token-permutation equivariant, within tolerance of the oracle
     and of the CUDA-core 4-bit kernels."""
-    layer = wl.make_custom_layer(29, T=T, d=512, E=16, k=k, F=384, act_dtype=wl.BF16,
-                                 w_dtype=wl.Q4_A64, bias_sd=0.5)
+    layer = wl.make_custom_layer(29, T=T, d=512, E=16, k=k, F=F, act_dtype=wl.BF16,
+                                 w_dtype=wdt, bias_sd=0.5)
     t = upload_layer(layer, DEV)
     a, r = gpu_forward_views(layer, DEV, path=DECODE, t=t)
     b, _ = gpu_forward_views(layer, DEV, path=DECODE, t=t)
@@ -606,4 +633,64 @@ def test_q4_pack_tile_layout(rows, cols):
             want[t + rr * 32:t + rr * 32 + 32] = words.astype("<u4").view(np.uint8)
             want[t + 4096 + 2 * rr:t + 4098 + 2 * rr] = blocks[r, g, 0:2]
             want[t + 4352 + 2 * rr:t + 4354 + 2 * rr] = blocks[r, g, 2:4]
+    assert got.shape == want.shape and np.array_equal(got, want)
+
+
+def q4_k_fields(blk):
+    """(d, dmin, sc[8], m[8]) of one 144-byte Q4_K super-block, decoded here
+    with numpy from the six-bit field layout moe.h states."""
+    d = float(np.frombuffer(blk[0:2].tobytes(), "<f2")[0])
+    dmin = float(np.frombuffer(blk[2:4].tobytes(), "<f2")[0])
+    s = blk[4:16].astype(np.int64)
+    sc, m = np.zeros(8, np.int64), np.zeros(8, np.int64)
+    for j in range(8):
+        if j < 4:
+            sc[j], m[j] = s[j] & 63, s[j + 4] & 63
+        else:
+            sc[j] = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4)
+            m[j] = (s[j + 4] >> 4) | ((s[j] >> 6) << 4)
+    return d, dmin, sc, m
+
+
+@pytest.mark.parametrize("rows,cols", [(130, 256), (256, 512), (1, 256)])
+def test_q4_k_pack_tile_layout(rows, cols):
+    """moe_pack_q4_k's output, byte for byte, against the tile layout its
+    header states, built here from the 144-byte super-blocks with numpy: tile
+    (row // 128, kb) at ((row // 128) * (cols / 64) + kb) * 5120 holds the 64
+    values 64 kb .. 64 kb + 63 of its 128 rows as code words (the 4-bit words
+    of the affine 4-bit tiles), then fp16 scales [2][128], then fp16 biases
+    [2][128]: group g is sub-block j = 2 (kb % 4) + g of super-block kb // 4,
+    scale = fp16(d * sc[j]), bias = fp16(8 d sc[j] - dmin m[j]) (the value at
+    code 8); rows past the last are zero."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    rng = np.random.default_rng(rows + cols + 1)
+    w = (rng.standard_normal((rows, cols)) * rng.uniform(0.1, 3.0, (rows, 1))).astype(np.float32)
+    blocks = wl.q4_k_quantize(w)                       # [rows, cols/256, 144]
+    n = pkg.moe_q4_k_packed_size(rows, cols)
+    packed = pkg.moe_pack_q4_k(torch.from_numpy(blocks.reshape(-1).copy()).to(DEV), rows, cols)
+    got = packed.cpu().numpy()[:n]
+    G, RT = cols // 64, (rows + 127) // 128
+    want = np.zeros(RT * G * 5120, dtype=np.uint8)
+    shifts_lo = np.array([0, 4, 8, 12], dtype=np.uint32)
+    shifts_hi = np.array([16, 20, 24, 28], dtype=np.uint32)
+    for r in range(rows):
+        for kb in range(G):
+            blk = blocks[r, kb // 4]
+            dd, dmin, sc, m = q4_k_fields(blk)
+            run = blk[16 + 32 * (kb % 4):48 + 32 * (kb % 4)].astype(np.uint32)
+            vals = np.concatenate([run & 15, run >> 4])        # the 64 codes in value order
+            t = ((r // 128) * G + kb) * 5120
+            rr = r % 128
+            v = vals.reshape(8, 8)                               # word i: values 8i .. 8i+7
+            words = (v[:, 0::2] << shifts_lo).sum(1) | (v[:, 1::2] << shifts_hi).sum(1)
+            want[t + rr * 32:t + rr * 32 + 32] = words.astype("<u4").view(np.uint8)
+            for g in range(2):
+                j = 2 * (kb % 4) + g
+                s32 = np.float32(dd) * np.float32(sc[j])             # exact in fp32
+                scale = np.float16(s32)
+                bias = np.float16(np.float32(8) * s32 - np.float32(dmin) * np.float32(m[j]))
+                want[t + 4096 + 256 * g + 2 * rr:t + 4098 + 256 * g + 2 * rr] = \
+                    np.array([scale]).view(np.uint8)
+                want[t + 4608 + 256 * g + 2 * rr:t + 4610 + 256 * g + 2 * rr] = \
+                    np.array([bias]).view(np.uint8)
     assert got.shape == want.shape and np.array_equal(got, want)
