@@ -427,7 +427,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // fused kernel adds into it for k = 2 and stores for k = 1; the other
     // tensor-core decode kernels add into it only when their down kernel does)
     const bool zero_out = use_fused ? k == 2
-                          : use_dtc ? k > 1 && decode_tc_down_direct(T, d, E, k, F)
+                          : use_dtc ? k > 1 && decode_tc_down_into_out(T, d, E, k, F, w_dt, num_sms)
                                     : k == 2;   // k > 2: combined from per-row outputs
     // routing, then the grouping scatter (which also writes the grouped x rows
     // that the tensor-core expert kernels read)

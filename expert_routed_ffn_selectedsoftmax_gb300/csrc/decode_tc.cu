@@ -114,6 +114,20 @@ constexpr int NACC = 4;                         // TMEM accumulators of 32 colum
 constexpr uint32_t A_COL4 = NACC * 32;          // W4: first column of the converted A buffers
 static_assert(A_COL4 + NCVT4 * 64 <= 256, "W4 accumulators and A buffers fit in 256 TMEM columns");
 constexpr int kTargetItems = MOE_DTC_TARGET_ITEMS;   // ~1 item per CTA: 2 CTAs per SM on a 152-SM GB300
+// Cluster mode (CL): the CS CTAs of a cluster take the CS K splits of one
+// unit (chunk, 128-row tile), gate/up items covering both matrices; each
+// epilogue parks its fp32 accumulators in shared memory, and CTA rank r sums
+// rows [r * 128 / CS, (r + 1) * 128 / CS) over the cluster in rank order
+// (distributed shared memory) and writes h, or w * y into out -- no partial
+// sums in global memory and no reduction kernel.  Chunks of at most 16 token
+// rows keep the reduction buffer at 16 KB.
+constexpr int NTCL = 16;
+constexpr int RED_BYTES = 2 * NTCL * BM * 4;    // [gate, up][16 token columns][128 rows] fp32
+#ifndef MOE_DTC_CLUSTER_MAX
+#define MOE_DTC_CLUSTER_MAX 8
+#endif
+constexpr int kClusterMax = 8;                  // (register arrays of the reduction)
+constexpr int kClusterUse = MOE_DTC_CLUSTER_MAX;   // largest cluster the launcher picks (0: no cluster mode)
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
@@ -138,12 +152,14 @@ struct Params {
     const uint8_t *w4[2];  // W4: packed tiles of the matrix (GATEUP: gate, up; DOWN: down)
     int groups;            // W4: K / 64, tiles per row tile
     int gpr;               // W4: affine groups per tile row (1 affine 4-bit, 2 Q4_K)
+    int cl;                // cluster mode: CTAs per cluster (= KS); 0 otherwise
 };
 
 struct Ctl {
     uint64_t full[kStagesMax], empty[kStagesMax], tfull[NACC], tempty[NACC], drain;
     uint64_t cfull[NCVT4], cempty[NCVT4];   // W4: converted buffers
     uint64_t never;      // nothing arrives here (test hook)
+    uint64_t rfull, rfree;   // cluster mode: partials of every CTA parked / read by every CTA
     uint32_t tmem_base;
     int abort_flag;
     int n_items;
@@ -151,13 +167,18 @@ struct Ctl {
     int off[kMaxExperts + 1];
 };
 
+constexpr int kCtlBytes = (int)((sizeof(Ctl) + 15) / 16 * 16);   // the reduction buffer follows
+
 struct Item {
     int e, nc, m, rt, s;
     int row0, nrows, nt, kb0, nkb;
 };
 
+// CL: cluster mode (16-row chunks; gate/up items of both matrices over a K split)
+template <bool CL>
 __device__ __forceinline__ Item decode_item(const Ctl &c, const Params &p, int item)
 {
+    constexpr int CH = CL ? NTCL : NTMAX;
     int lo = 0, hi = p.E - 1;   // largest e with unit_start[e] <= item
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -175,19 +196,23 @@ __device__ __forceinline__ Item decode_item(const Ctl &c, const Params &p, int i
     it.rt = local / p.KS;
     it.s = local - it.rt * p.KS;
     const int rows_e = c.off[lo + 1] - c.off[lo];
-    it.row0 = c.off[lo] + it.nc * NTMAX;
-    it.nrows = min(NTMAX, rows_e - it.nc * NTMAX);
+    it.row0 = c.off[lo] + it.nc * CH;
+    it.nrows = min(CH, rows_e - it.nc * CH);
     it.nt = it.nrows <= 16 ? 16 : 32;
     it.kb0 = it.s * p.kb_total / p.KS;
     it.nkb = (it.s + 1) * p.kb_total / p.KS - it.kb0;
-    if (p.fused) { it.kb0 = 0; it.nkb = 2 * p.kb_total; }   // stages alternate gate / up
+    // stages alternate gate / up tiles of each k-block (whole K outside cluster mode)
+    if (p.fused) {
+        if (CL) it.nkb *= 2;
+        else { it.kb0 = 0; it.nkb = 2 * p.kb_total; }
+    }
     return it;
 }
 
 // Weight matrix and k-block of stage `kbl` of an item.
 __device__ __forceinline__ void stage_of(const Params &p, const Item &it, int kbl, int &m, int &kb)
 {
-    if (p.fused) { m = kbl & 1; kb = kbl >> 1; }
+    if (p.fused) { m = kbl & 1; kb = it.kb0 + (kbl >> 1); }   // (kb0 = 0 outside cluster mode)
     else { m = it.m; kb = it.kb0 + kbl; }
 }
 
@@ -195,7 +220,7 @@ __device__ __forceinline__ void stage_of(const Params &p, const Item &it, int kb
 // k-block and token tile.
 __device__ __forceinline__ int w4_stages(const Params &p, const Item &it)
 {
-    return p.fused ? p.kb_total : (it.nkb + 1) / 2;
+    return p.fused ? p.kb_total : (it.nkb + 1) / 2;   // (4-bit weights: never cluster mode)
 }
 __device__ __forceinline__ int w4_parts(const Params &p, const Item &it, int st)
 {
@@ -218,6 +243,39 @@ __device__ __forceinline__ float swiglu_scaled(float g, float u, int e)
     return __fdividef(g, 1.0f + __expf(-ldexpf(g, e))) * u;
 }
 
+// Warp 0: items per expert (chunks x n_mats x row tiles x K splits), their
+// exclusive prefix sums and the item count (0 when the offsets are bad).
+template <bool CL>
+__device__ __forceinline__ void build_units(Ctl &c, const Params &p, bool offsets_ok, int lane)
+{
+    constexpr int CH = CL ? NTCL : NTMAX;
+    const int E = p.E;
+    const int units = p.n_mats * p.rtiles * p.KS;
+    int local[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane * 8 + j;
+        int n = 0;
+        if (e < E) n = (c.off[e + 1] - c.off[e] + CH - 1) / CH;
+        local[j] = n * units;
+        sum += local[j];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane * 8 + j;
+        if (e < E) c.unit_start[e] = run;
+        run += local[j];
+    }
+    if (lane == 31) { c.n_items = offsets_ok ? incl : 0; c.unit_start[E] = incl; }
+}
+
 // tm_w0/tm_w1: weight matrices (box 64 x 128 rows); tm_b16/tm_b32: the token
 // rows (grouped x for GATEUP, h for DOWN) with boxes of 16 and 32 rows.
 // GATHER: the token rows are not loaded by TMA but gathered from x through
@@ -225,7 +283,7 @@ __device__ __forceinline__ float swiglu_scaled(float g, float u, int e)
 // into the 128-byte-swizzled layout the MMA expects.
 // W4 (affine 4-bit weights): tm_w0/tm_w1 are unused; each stage's weight tile
 // is one contiguous copy from p.w4[m], converted to fp16 by warps 6-9.
-template <int MODE, bool GATHER, bool W4>
+template <int MODE, bool GATHER, bool W4, bool CL = false>
 __global__ void __launch_bounds__(GATHER || W4 ? THREADS_GATHER : THREADS, CTAS_PER_SM)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
@@ -254,6 +312,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         for (int b = 0; b < NACC; ++b) { mbar_init(&c.tfull[b], 1); mbar_init(&c.tempty[b], 128); }
         mbar_init(&c.drain, 1);
         mbar_init(&c.never, 1);
+        if (CL) { mbar_init(&c.rfull, 4 * p.cl); mbar_init(&c.rfree, 4 * p.cl); }
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -269,45 +328,44 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
     }
     if (warp == 1) tmem_alloc(&c.tmem_base, RG::TMEM_COLS);
     tc_fence_before();
-    pdl_enter();
-    if (upstream_failed(p.status)) {   // (synchronises the CTA)
-        if (warp == 1) {
-            tc_fence_after();
-            tmem_dealloc(c.tmem_base, RG::TMEM_COLS);
+    if constexpr (MODE == DOWN) {
+        // The grouping comes from the router, which completed before the
+        // kernel preceding this one passed its dependency wait and let this
+        // one start: the unit table is built now, while that kernel finishes
+        // (offsets read from L2, never a stale L1 line).  (Streaming the
+        // first weight tiles into L2 here as well measured slower: it takes
+        // bandwidth from the gate/up kernel still running.)
+        for (int e = threadIdx.x; e <= E; e += NTHREADS) c.off[e] = __ldcg(p.offsets + e);
+        __syncthreads();
+        const bool offsets_ok = debug_offsets_ok(c.off, E, p.rows_total, p.status);
+        if (threadIdx.x < 32) build_units<CL>(c, p, offsets_ok, lane);
+        pdl_enter();
+        if (upstream_failed(p.status)) {   // (synchronises the CTA)
+            if (warp == 1) {
+                tc_fence_after();
+                tmem_dealloc(c.tmem_base, RG::TMEM_COLS);
+            }
+            return;
         }
-        return;
-    }
-    for (int e = threadIdx.x; e <= E; e += NTHREADS) c.off[e] = p.offsets[e];
-    __syncthreads();
-    const bool offsets_ok = debug_offsets_ok(c.off, E, p.rows_total, p.status);
-    if (threadIdx.x < 32) {
-        const int units = p.n_mats * p.rtiles * p.KS;
-        int local[8], sum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane * 8 + j;
-            int n = 0;
-            if (e < E) n = (c.off[e + 1] - c.off[e] + NTMAX - 1) / NTMAX;
-            local[j] = n * units;
-            sum += local[j];
+    } else {
+        pdl_enter();
+        // the offsets' loads are in flight with the status read below, whose
+        // barrier also publishes them
+        for (int e = threadIdx.x; e <= E; e += NTHREADS) c.off[e] = p.offsets[e];
+        if (upstream_failed(p.status)) {   // (synchronises the CTA)
+            if (warp == 1) {
+                tc_fence_after();
+                tmem_dealloc(c.tmem_base, RG::TMEM_COLS);
+            }
+            return;
         }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - sum;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane * 8 + j;
-            if (e < E) c.unit_start[e] = run;
-            run += local[j];
-        }
-        if (lane == 31) { c.n_items = offsets_ok ? incl : 0; c.unit_start[E] = incl; }
+        const bool offsets_ok = debug_offsets_ok(c.off, E, p.rows_total, p.status);
+        if (threadIdx.x < 32) build_units<CL>(c, p, offsets_ok, lane);
     }
     tc_fence_before();
-    __syncthreads();
+    // cluster mode: peers arrive on this CTA's barriers -- all initialised first
+    if (CL) cluster_sync_all();
+    else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem = c.tmem_base;
@@ -319,7 +377,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         uint32_t it_k = 0;
         bool ok = p.expire_ns == 0 || mbar_wait(&c.never, 0, abort_flag, p.expire_ns);
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode_item(c, p, item);
+            const Item it = decode_item<CL>(c, p, item);
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
             const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
@@ -375,7 +433,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         uint32_t it_k = 0, li = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++li) {
-            const Item it = decode_item(c, p, item);
+            const Item it = decode_item<CL>(c, p, item);
             // accumulator slots: NACC of 32 columns, or (fused) NACC/2 pairs of
             // (gate, up) accumulators
             const uint32_t nslot = p.fused ? NACC / 2 : NACC;
@@ -398,7 +456,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                         w4_part(p, it, st, j, m, kb, tt);
                         const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
                         const uint64_t db = sw128_desc(sp + tt * B_BYTES);
-                        const int first = p.fused ? kb : 2 * st + j;   // first k-block of this accumulator
+                        const int first = p.fused ? kb : 2 * st + j;   // 0: first k-block of this accumulator
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
                             umma_f16_ts(d_tmem, a_tm + j * 32 + kk * 8, desc_step(db, kk * 32), idesc,
@@ -421,7 +479,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
                 const uint32_t a0 = smem_u32(smem + s * SLOT);
                 const uint32_t b0 = smem_u32(smem + s * SLOT + RG::B_OFF);
-                const int first = p.fused ? kb : kbl;   // first k-block of this accumulator
+                const int first = kb - it.kb0;   // 0: first k-block of this accumulator
                 const uint64_t da = sw128_desc(a0), db = sw128_desc(b0);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
@@ -450,7 +508,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         uint32_t it_k = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode_item(c, p, item);
+            const Item it = decode_item<CL>(c, p, item);
             const int nst = w4_stages(p, it);
             for (int st = 0; st < nst; ++st, ++it_k) {
                 const int s = it_k % STAGES, cb = it_k % NCVT4;
@@ -499,7 +557,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         uint32_t it_k = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Item it = decode_item(c, p, item);
+            const Item it = decode_item<CL>(c, p, item);
             const bool has = lane < it.nrows;
             int tok = has ? p.perm_tok[it.row0 + lane] : 0;
             if (has && !debug_index_ok(tok, p.T, p.status)) tok = 0;   // (debug builds)
@@ -536,13 +594,74 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         uint32_t li = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++li) {
-            const Item it = decode_item(c, p, item);
+            const Item it = decode_item<CL>(c, p, item);
             const uint32_t nslot = p.fused ? NACC / 2 : NACC;
             const uint32_t acc = li % nslot, aph = (li / nslot) & 1u;
             // warp-uniform outcome: tcgen05.ld below is warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait(&c.tfull[acc], aph, abort_flag))) { ok = false; break; }
             tc_fence_after();
             const int wr = it.rt * BM + quarter * 32 + lane;   // weight row = output column
+            if constexpr (CL) {
+                // park this split's accumulators (lane = row, 16 token columns;
+                // gate/up: G then U) once every CTA has read the previous ones
+                float *red = reinterpret_cast<float *>(smem + RG::CTL + kCtlBytes);
+                if (!__all_sync(0xffffffffu, mbar_wait(&c.rfree, (li & 1u) ^ 1u, abort_flag))) { ok = false; break; }
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * (MODE == GATEUP ? 64 : 32);
+                const int row = quarter * 32 + lane;
+                uint32_t v[16];
+#pragma unroll
+                for (int mt = 0; mt < (MODE == GATEUP ? 2 : 1); ++mt) {
+                    tmem_ld16(taddr + mt * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) red[(mt * NTCL + q) * BM + row] = __uint_as_float(v[q]);
+                }
+                tc_fence_before();
+                mbar_arrive(&c.tempty[acc]);
+                fence_acq_rel_cluster();
+                __syncwarp();
+                const int CS = p.cl;
+                if (lane < CS) mbar_arrive_release_cluster(peer_addr(&c.rfull, (uint32_t)lane));
+                if (!__all_sync(0xffffffffu, mbar_wait_acquire_cluster(&c.rfull, li & 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                // rows [rank * RS, +RS) of the tile: sum over the cluster in rank order
+                const int RS = BM / CS, rank = (int)cluster_rank();
+                uint32_t base[kClusterMax];
+#pragma unroll
+                for (int q = 0; q < kClusterMax; ++q) base[q] = q < CS ? peer_addr(red, (uint32_t)q) : 0u;
+                for (int idx = quarter * 32 + lane; idx < RS * it.nrows; idx += 128) {
+                    const int r = rank * RS + idx % RS, j = idx / RS;
+                    float a[kClusterMax], b[kClusterMax];
+#pragma unroll
+                    for (int q = 0; q < kClusterMax; ++q) {
+                        if (q < CS) {
+                            a[q] = ld_cluster_f32(base[q] + 4u * (uint32_t)(j * BM + r));
+                            if (MODE == GATEUP) b[q] = ld_cluster_f32(base[q] + 4u * (uint32_t)((NTCL + j) * BM + r));
+                        }
+                    }
+                    float ga = a[0], ub = MODE == GATEUP ? b[0] : 0.f;
+#pragma unroll
+                    for (int q = 1; q < kClusterMax; ++q)
+                        if (q < CS) { ga += a[q]; if (MODE == GATEUP) ub += b[q]; }
+                    const int col = it.rt * BM + r;
+                    if (MODE == GATEUP) {
+                        p.h[(size_t)(it.row0 + j) * p.R + col] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(ga) * ub));
+                    } else {
+                        int tok = p.perm_tok[it.row0 + j];
+                        float w = p.perm_w[it.row0 + j];
+                        if (!debug_index_ok(tok, p.T, p.status)) { tok = 0; w = 0.f; }   // (debug builds)
+                        float *o = p.out + (size_t)tok * p.R + col;
+                        if (p.k == 1) *o = w * ga;
+                        else atomicAdd(o, w * ga);
+                    }
+                }
+                // (the peers' partials were read: the sums above consumed them)
+                __syncwarp();
+                if (lane < CS) mbar_arrive_cluster(peer_addr(&c.rfree, (uint32_t)lane));
+                continue;
+            }
             if (MODE == GATEUP && p.fused) {
                 // lane = f; column j = token row j of the chunk; two halves of
                 // 16 token columns (the second only for 32-row chunks)
@@ -613,7 +732,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         }
     }
 
-    __syncthreads();
+    // cluster mode: no CTA leaves while a peer may still read its shared memory
+    if (CL) cluster_sync_all();
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -730,7 +851,10 @@ combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
     }
 }
 
-template <bool W4> constexpr size_t smem_bytes() { return 1024 + (size_t)Ring<W4>::CTL + sizeof(Ctl); }
+template <bool W4, bool CL = false> constexpr size_t smem_bytes()
+{
+    return 1024 + (size_t)Ring<W4>::CTL + kCtlBytes + (CL ? RED_BYTES : 0);
+}
 
 int choose_splits(int kb_total, long long units)
 {
@@ -777,6 +901,37 @@ bool decode_tc_down_direct(int T, int d, int E, int k, int F)
     return k <= 2 && n_exp * (d / dtc::BM) >= kWholeKMinUnits;
 }
 
+// Cluster mode: CS CTAs per unit (CS = 8, 4 or 2) when the kernel's units
+// (16-row chunks x 128-row tiles, an upper bound before routing) then fill at
+// most one wave of CTAs and every K split keeps at least two k-blocks; 0
+// otherwise.  bf16 weights only.
+static int cluster_size(long long units, int kb_total, int num_sms)
+{
+    const long long slots = (long long)num_sms * dtc::CTAS_PER_SM;
+    for (int cs = dtc::kClusterUse; cs >= 2; cs /= 2)
+        if (units * cs <= slots && kb_total / cs >= 2) return cs;
+    return 0;
+}
+static long long cluster_chunks(int T, int E, int k)
+{
+    const long long rows = (long long)T * k, n_exp = E < rows ? E : rows;
+    return n_exp + rows / dtc::NTCL;
+}
+int decode_tc_gateup_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
+{
+    if (w_dt != MOE_BF16 || decode_tc_gateup_fused(T, d, E, k, F, num_sms)) return 0;
+    return cluster_size(cluster_chunks(T, E, k) * (F / dtc::BM), d / dtc::BK, num_sms);
+}
+int decode_tc_down_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
+{
+    if (w_dt != MOE_BF16 || k > 2 || decode_tc_down_direct(T, d, E, k, F)) return 0;
+    return cluster_size(cluster_chunks(T, E, k) * (d / dtc::BM), F / dtc::BK, num_sms);
+}
+bool decode_tc_down_into_out(int T, int d, int E, int k, int F, int w_dt, int num_sms)
+{
+    return decode_tc_down_direct(T, d, E, k, F) || decode_tc_down_cluster(T, d, E, k, F, w_dt, num_sms) > 0;
+}
+
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
 {
     using namespace dtc;
@@ -814,7 +969,14 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     const int dev = current_device();
     if (!attr_done.done(dev)) {
         const int s16 = (int)smem_bytes<false>(), s4 = (int)smem_bytes<true>();
-        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false>,
+        const int scl = (int)smem_bytes<false, true>();
+        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, false, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
@@ -836,6 +998,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
 
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.rows_total = rows; p.status = a.status;
+    p.cl = 0;
     p.xexp = w4 ? a.xexp : nullptr;
     p.T = a.T;
     p.w4[0] = static_cast<const uint8_t *>(a.w_gate);
@@ -847,17 +1010,37 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
 
     const bool fused = decode_tc_gateup_fused(a.T, a.d, a.E, a.k, a.F, a.num_sms);
     const bool direct = decode_tc_down_direct(a.T, a.d, a.E, a.k, a.F);
+    const int cl_gu = decode_tc_gateup_cluster(a.T, a.d, a.E, a.k, a.F, a.w_dt, a.num_sms);
+    const int cl_d = decode_tc_down_cluster(a.T, a.d, a.E, a.k, a.F, a.w_dt, a.num_sms);
+    const long long chunks_cl = cluster_chunks(a.T, a.E, a.k);
+    const size_t smem_cl = smem_bytes<false, true>();
+    // grid of a cluster-mode launch: whole clusters, at most one wave
+    auto grid_cl = [&](long long units, int cs) {
+        const long long per = (long long)a.num_sms * CTAS_PER_SM / cs;
+        return dim3((unsigned)((units < per ? units : per) * cs));
+    };
 
     // gate/up: matrices W_g, W_u ([E*F, d]), K = d, token rows = grouped x
     p.K = a.d; p.R = a.F; p.kb_total = a.d / BK; p.rtiles = a.F / BM;
     if (fused) {
         p.n_mats = 1; p.KS = 1; p.fused = 1; p.h = a.h;   // an item covers both matrices
+    } else if (cl_gu) {
+        p.n_mats = 1; p.KS = cl_gu; p.fused = 1; p.h = a.h; p.cl = cl_gu;
     } else {
         p.n_mats = 2; p.KS = ks_gu; p.P = a.pgu;
     }
     const dim3 g_gu(grid_for(chunks * p.n_mats * p.rtiles * p.KS));
     p.expire_ns = a.expire_ns;   // (the gate/up kernel only)
-    if (gather) {
+    if (cl_gu) {
+        p.xg = gather ? static_cast<const uint16_t *>(a.x_gather) : nullptr;
+        p.perm_tok = a.perm_tok;
+        if (gather)
+            launch_pdl_cluster(decode_tc_kernel<GATEUP, true, false, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
+                               dim3(THREADS_GATHER), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
+        else
+            launch_pdl_cluster(decode_tc_kernel<GATEUP, false, false, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
+                               dim3(THREADS), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
+    } else if (gather) {
         p.xg = static_cast<const uint16_t *>(a.x_gather);
         p.perm_tok = a.perm_tok;
         launch_pdl(decode_tc_kernel<GATEUP, true, false>, g_gu, dim3(THREADS_GATHER), smem, stream, m_wg,
@@ -878,7 +1061,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
         if (blocks > cap) blocks = cap;
         return (int)(blocks < 1 ? 1 : blocks);
     };
-    if (!fused) {
+    if (!fused && !cl_gu) {
         launch_pdl(swiglu_reduce_kernel, dim3(reduce_grid((long long)rows * (a.F / 4), ks_gu)), reduce_block(ks_gu),
                    0, stream, a.pgu, ks_gu, rows, a.F, a.h, p.xexp, a.status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -892,19 +1075,26 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     p.fused = 0; p.h = nullptr;
     p.xg = nullptr;
     p.expire_ns = 0;
+    p.cl = 0;
     if (direct) {
         p.KS = 1; p.direct = 1; p.out = a.out; p.perm_tok = a.perm_tok; p.perm_w = a.perm_w; p.k = a.k;
+    } else if (cl_d) {
+        p.KS = cl_d; p.cl = cl_d; p.direct = 0;
+        p.out = a.out; p.perm_tok = a.perm_tok; p.perm_w = a.perm_w; p.k = a.k;
     } else {
         p.KS = ks_d; p.P = a.pd; p.perm_tok = nullptr;
     }
-    if (w4)
+    if (cl_d)
+        launch_pdl_cluster(decode_tc_kernel<DOWN, false, false, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
+                           dim3(THREADS), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
+    else if (w4)
         launch_pdl(decode_tc_kernel<DOWN, false, true>, dim3(grid_for(chunks * p.rtiles * p.KS)),
                    dim3(THREADS_W4), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
     else
         launch_pdl(decode_tc_kernel<DOWN, false, false>, dim3(grid_for(chunks * p.rtiles * p.KS)),
                    dim3(THREADS), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (direct) return cudaSuccess;
+    if (direct || cl_d) return cudaSuccess;
 
     launch_pdl(combine_kernel, dim3(reduce_grid((long long)a.T * (a.d / 4), ks_d)), reduce_block(ks_d), 0, stream,
         a.pd, ks_d, rows, a.d, a.inv, a.topk_w, p.xexp, a.T, a.k, a.out, a.status);

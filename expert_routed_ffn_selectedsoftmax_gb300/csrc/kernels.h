@@ -138,6 +138,13 @@ void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d);
 // beforehand when k > 1) -- no reduction or combine kernels
 bool decode_tc_gateup_fused(int T, int d, int E, int k, int F, int num_sms);
 bool decode_tc_down_direct(int T, int d, int E, int k, int F);
+// cluster mode (small bf16 batches): CTAs per cluster of the gate/up / down
+// kernels, 0 when not used; K splits reduced on chip, h and out written
+// directly
+int decode_tc_gateup_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms);
+int decode_tc_down_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms);
+// the down kernel adds into out (zeroed beforehand when k > 1)
+bool decode_tc_down_into_out(int T, int d, int E, int k, int F, int w_dt, int num_sms);
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream);
 
 // decode_fused.cu -- the decode expert FFN in one persistent launch (bf16,
