@@ -210,8 +210,9 @@ def expert_kernel_names(w, T, num_sms):
     tokens; beyond that a gather kernel does), then for bf16
     one persistent kernel for gate/up, SwiGLU, down and the combine when k <= 2
     and the batch has half a wave of whole-K gate/up items of at most 512 KB,
-    else the gate/up and down kernels with their split-K reductions; otherwise
-    the CUDA-core decode kernels), and how many of the library's kernels one
+    else the gate/up and down kernels, each in cluster mode for small bf16
+    batches (K splits reduced on chip) or with its split-K reduction kernel;
+    otherwise the CUDA-core decode kernels), and how many of the library's kernels one
     layer launches.  "fused": the gate/up and down GEMMs run in one kernel,
     timed as one stage."""
     rows = T * w.k
@@ -232,14 +233,27 @@ def expert_kernel_names(w, T, num_sms):
                     "launches": (1 if small else 2) + 1}
         fused = 192 <= n_exp * (w.F // 128) <= 2 * num_sms
         direct = w.k <= 2 and n_exp * (w.d // 128) >= 192
+
+        # cluster mode (bf16): CS CTAs per unit of 16-row chunks when that fills
+        # at most one wave and every K split keeps two k-blocks
+        def cluster(units, kb_total):
+            for cs in (8, 4, 2):
+                if units * cs <= 2 * num_sms and kb_total // cs >= 2:
+                    return cs
+            return 0
+        chunks_cl = n_exp + rows // 16
+        cl_gu = 0 if q4 or fused else cluster(chunks_cl * (w.F // 128), w.d // 64)
+        cl_d = 0 if q4 or w.k > 2 or direct else cluster(chunks_cl * (w.d // 128), w.F // 64)
         # 4-bit: the grouped fp16 rows come from the clustered router up to 16
         # tokens, else from a gather kernel
         launches = (1 if small else 2) + (1 if q4 and small and T > 16 else 0) + \
-            (1 if fused else 2) + (1 if direct else 2)
+            (1 if fused or cl_gu else 2) + (1 if direct or cl_d else 2)
         tag = {3: ", 4-bit", 4: ", Q4_K"}.get(w.w_dtype, "")
         gu = f"decode_tc_kernel<GATEUP{tag}> (whole K, writes h)" if fused else \
+            f"decode_tc_kernel<GATEUP> (clusters of {cl_gu}, writes h)" if cl_gu else \
             f"decode_tc_kernel<GATEUP{tag}> + swiglu_reduce_kernel"
         dn = f"decode_tc_kernel<DOWN{tag}> (whole K, adds into out)" if direct else \
+            f"decode_tc_kernel<DOWN> (clusters of {cl_d}, writes out)" if cl_d else \
             f"decode_tc_kernel<DOWN{tag}> + combine_kernel"
         return {"file": "decode_tc.cu", "gateup": gu, "down": dn, "launches": launches,
                 "fused": False}

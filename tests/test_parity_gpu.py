@@ -394,6 +394,34 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
     check_output(a, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
+@pytest.mark.parametrize("T,d,E,k,F", [
+    (2, 1024, 8, 1, 1024),   # clusters of 8 CTAs for both kernels (16 k-blocks, 16 units)
+    (3, 512, 8, 2, 512),     # clusters of 4; k = 2: two additions onto the zeroed output
+    (5, 256, 16, 2, 256),    # clusters of 2
+    (1, 2048, 16, 1, 2816),  # the ZONOS2 shape: 22 gate/up and 16 down units, clusters of 8
+    (24, 512, 4, 2, 256),    # 48 rows: chunks of 16 rows, several per expert
+])
+def test_decode_cluster_mode_deterministic_equivariant_and_matches_oracle(T, d, E, k, F):
+    """Small bf16 decode batches run the tensor-core decode kernels in cluster
+    mode: the K splits of a unit are reduced in shared memory across the
+    cluster, in rank order.  Two runs give the same bits, permuting the
+    tokens permutes the output rows bit for bit, and the result matches the
+    oracle."""
+    layer = wl.make_custom_layer(30, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16, w_dtype=wl.BF16,
+                                 bias_sd=0.5)
+    t = upload_layer(layer, DEV)
+    a, r = gpu_forward_views(layer, DEV, path=DECODE, t=t)
+    b, _ = gpu_forward_views(layer, DEV, path=DECODE, t=t)
+    assert np.array_equal(a, b)
+    perm = np.random.default_rng(8).permutation(layer.T)
+    t2 = dict(t, x=t["x"][torch.from_numpy(perm).to(DEV)].contiguous())
+    c = gpu_forward(layer, DEV, path=DECODE, t=t2).cpu().numpy()
+    assert np.array_equal(c, a[perm])
+    check_routing_views(r, layer)
+    ref, idx_ref, _, margin = oracle.moe_forward(layer)
+    check_output(a, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
+
+
 @pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64])
 @pytest.mark.parametrize("k,F", [(2, 128), (1, 1024)])   # (1, 1024): long K in the down GEMM
 def test_prefill_deterministic_and_equivariant(wdt, k, F):
