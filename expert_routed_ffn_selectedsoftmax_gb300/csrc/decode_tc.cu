@@ -907,6 +907,8 @@ bool decode_tc_down_direct(int T, int d, int E, int k, int F)
 // otherwise.  bf16 weights only.
 static int cluster_size(long long units, int kb_total, int num_sms)
 {
+    // (allowing two or more waves of clusters measured slower: ZONOS2 decode T = 8
+    // 51.3 -> 55.9 / 61.1 us per layer with two / three)
     const long long slots = (long long)num_sms * dtc::CTAS_PER_SM;
     for (int cs = dtc::kClusterUse; cs >= 2; cs /= 2)
         if (units * cs <= slots && kb_total / cs >= 2) return cs;
