@@ -234,7 +234,7 @@ def expert_kernel_names(w, T, num_sms):
         fused = 192 <= n_exp * (w.F // 128) <= 2 * num_sms
         direct = w.k <= 2 and n_exp * (w.d // 128) >= 192
 
-        # cluster mode (bf16): CS CTAs per unit of 16-row chunks when that fills
+        # cluster mode: CS CTAs per unit of 16-row chunks when that fills
         # at most one wave and every K split keeps two k-blocks
         def cluster(units, kb_total):
             for cs in (8, 4, 2):
@@ -242,18 +242,18 @@ def expert_kernel_names(w, T, num_sms):
                     return cs
             return 0
         chunks_cl = n_exp + rows // 16
-        cl_gu = 0 if q4 or fused else cluster(chunks_cl * (w.F // 128), w.d // 64)
-        cl_d = 0 if q4 or w.k > 2 or direct else cluster(chunks_cl * (w.d // 128), w.F // 64)
+        cl_gu = 0 if fused else cluster(chunks_cl * (w.F // 128), w.d // 64)
+        cl_d = 0 if w.k > 2 or direct else cluster(chunks_cl * (w.d // 128), w.F // 64)
         # 4-bit: the grouped fp16 rows come from the clustered router up to 16
         # tokens, else from a gather kernel
         launches = (1 if small else 2) + (1 if q4 and small and T > 16 else 0) + \
             (1 if fused or cl_gu else 2) + (1 if direct or cl_d else 2)
         tag = {3: ", 4-bit", 4: ", Q4_K"}.get(w.w_dtype, "")
         gu = f"decode_tc_kernel<GATEUP{tag}> (whole K, writes h)" if fused else \
-            f"decode_tc_kernel<GATEUP> (clusters of {cl_gu}, writes h)" if cl_gu else \
+            f"decode_tc_kernel<GATEUP{tag}> (clusters of {cl_gu}, writes h)" if cl_gu else \
             f"decode_tc_kernel<GATEUP{tag}> + swiglu_reduce_kernel"
         dn = f"decode_tc_kernel<DOWN{tag}> (whole K, adds into out)" if direct else \
-            f"decode_tc_kernel<DOWN> (clusters of {cl_d}, writes out)" if cl_d else \
+            f"decode_tc_kernel<DOWN{tag}> (clusters of {cl_d}, writes out)" if cl_d else \
             f"decode_tc_kernel<DOWN{tag}> + combine_kernel"
         return {"file": "decode_tc.cu", "gateup": gu, "down": dn, "launches": launches,
                 "fused": False}

@@ -218,17 +218,19 @@ __device__ __forceinline__ void stage_of(const Params &p, const Item &it, int kb
 
 // W4 stages of an item, the parts (1 or 2) of stage st, and part j's matrix,
 // k-block and token tile.
+template <bool CL>
 __device__ __forceinline__ int w4_stages(const Params &p, const Item &it)
 {
-    return p.fused ? p.kb_total : (it.nkb + 1) / 2;   // (4-bit weights: never cluster mode)
+    return p.fused ? (CL ? it.nkb / 2 : p.kb_total) : (it.nkb + 1) / 2;
 }
 __device__ __forceinline__ int w4_parts(const Params &p, const Item &it, int st)
 {
     return p.fused ? 2 : min(2, it.nkb - 2 * st);
 }
+template <bool CL>
 __device__ __forceinline__ void w4_part(const Params &p, const Item &it, int st, int j, int &m, int &kb, int &tt)
 {
-    if (p.fused) { m = j; kb = st; tt = 0; }
+    if (p.fused) { m = j; kb = CL ? it.kb0 + st : st; tt = 0; }
     else { m = it.m; kb = it.kb0 + 2 * st + j; tt = j; }
 }
 
@@ -283,14 +285,17 @@ __device__ __forceinline__ void build_units(Ctl &c, const Params &p, bool offset
 // into the 128-byte-swizzled layout the MMA expects.
 // W4 (affine 4-bit weights): tm_w0/tm_w1 are unused; each stage's weight tile
 // is one contiguous copy from p.w4[m], converted to fp16 by warps 6-9.
-template <int MODE, bool GATHER, bool W4, bool CL = false>
+// W4: 0 for bf16 weights, else the 4-bit tiles' affine groups per tile row
+// (1: affine 4-bit, 2: Q4_K), fixed at compile time.
+template <int MODE, bool GATHER, int W4, bool CL = false>
 __global__ void __launch_bounds__(GATHER || W4 ? THREADS_GATHER : THREADS, CTAS_PER_SM)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
                  const Params p)
 {
     static_assert(!(GATHER && W4), "4-bit weights take the token rows by TMA");
-    using RG = Ring<W4>;
+    using RG = Ring<(W4 != 0)>;
+    constexpr int GPR = W4 ? W4 : 1;
     constexpr int STAGES = RG::NST, SLOT = RG::SLOTB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -382,25 +387,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
             if constexpr (W4) {
-                const int nst = w4_stages(p, it);
+                const int nst = w4_stages<CL>(p, it);
                 for (int st = 0; st < nst; ++st, ++it_k) {
                     const int s = it_k % STAGES;
                     if (!mbar_wait(&c.empty[s], ((it_k / STAGES) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                     const int np = w4_parts(p, it, st), ntok = p.fused ? 1 : np;
-                    const uint32_t tb = (uint32_t)q4_tile_bytes(p.gpr);
+                    const uint32_t tb = (uint32_t)q4_tile_bytes(GPR);
                     mbar_expect_tx(&c.full[s], (uint32_t)(np * tb + ntok * it.nt * BK * 2));
                     uint8_t *sp = smem + s * SLOT;
-                    if (p.fused) {   // gate and up tiles of k-block st
-                        bulk_load(sp + WT_OFF4, p.w4[0] + q4_tile_offset(wrow, st, p.groups, p.gpr), tb, &c.full[s]);
-                        bulk_load(sp + WT_OFF4 + tb, p.w4[1] + q4_tile_offset(wrow, st, p.groups, p.gpr), tb,
+                    if (p.fused) {   // gate and up tiles of k-block kb0 + st (kb0 = 0 outside cluster mode)
+                        const int kb = CL ? it.kb0 + st : st;
+                        bulk_load(sp + WT_OFF4, p.w4[0] + q4_tile_offset(wrow, kb, p.groups, GPR), tb, &c.full[s]);
+                        bulk_load(sp + WT_OFF4 + tb, p.w4[1] + q4_tile_offset(wrow, kb, p.groups, GPR), tb,
                                   &c.full[s]);
                     } else {         // k-blocks kb, kb + 1: adjacent tiles
-                        bulk_load(sp + WT_OFF4, p.w4[it.m] + q4_tile_offset(wrow, it.kb0 + 2 * st, p.groups, p.gpr),
+                        bulk_load(sp + WT_OFF4, p.w4[it.m] + q4_tile_offset(wrow, it.kb0 + 2 * st, p.groups, GPR),
                                   np * tb, &c.full[s]);
                     }
                     for (int j = 0; j < ntok; ++j) {
                         int m, kb, tt;
-                        w4_part(p, it, st, j, m, kb, tt);
+                        w4_part<CL>(p, it, st, j, m, kb, tt);
                         tma_load_2d(sp + tt * B_BYTES, bmap, &c.full[s], kb * BK, it.row0);
                     }
                 }
@@ -442,7 +448,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             tc_fence_after();
             const uint32_t idesc = idesc_f16_mn(W4 ? 1 : 0, BM, it.nt);
             if constexpr (W4) {
-                const int nst = w4_stages(p, it);
+                const int nst = w4_stages<CL>(p, it);
                 for (int st = 0; st < nst; ++st, ++it_k) {
                     const int s = it_k % STAGES, cb = it_k % NCVT4;
                     // the converters arrive after they have seen the stage land
@@ -453,10 +459,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     const uint32_t a_tm = tmem + A_COL4 + cb * 64;   // A in TMEM: K = 16 is 8 columns
                     for (int j = 0; j < np; ++j) {
                         int m, kb, tt;
-                        w4_part(p, it, st, j, m, kb, tt);
+                        w4_part<CL>(p, it, st, j, m, kb, tt);
                         const uint32_t d_tmem = tmem + (p.fused ? (acc * 2 + m) * 32 : acc * 32);
                         const uint64_t db = sw128_desc(sp + tt * B_BYTES);
-                        const int first = p.fused ? kb : 2 * st + j;   // 0: first k-block of this accumulator
+                        const int first = p.fused ? kb - (CL ? it.kb0 : 0) : 2 * st + j;   // 0: first k-block of this accumulator
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
                             umma_f16_ts(d_tmem, a_tm + j * 32 + kk * 8, desc_step(db, kk * 32), idesc,
@@ -504,12 +510,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         // (q4_word_fp16x8: one packed word -> 8 fp16 weights, an exact fma and a rounded one)
         const int quad = warp & 3, row = quad * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + A_COL4;
-        const Q4Fix fx(q4_zero_code(p.gpr));
+        const Q4Fix fx(q4_zero_code(GPR));
         uint32_t it_k = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item it = decode_item<CL>(c, p, item);
-            const int nst = w4_stages(p, it);
+            const int nst = w4_stages<CL>(p, it);
             for (int st = 0; st < nst; ++st, ++it_k) {
                 const int s = it_k % STAGES, cb = it_k % NCVT4;
                 if (!__all_sync(0xffffffffu, mbar_wait(&c.full[s], (it_k / STAGES) & 1u, abort_flag)) ||
@@ -518,14 +524,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     break;
                 }
                 const int np = w4_parts(p, it, st);
-                const int tb = q4_tile_bytes(p.gpr), g1 = p.gpr - 1;   // g1: the second group's index
+                constexpr int tb = q4_tile_bytes(GPR), g1 = GPR - 1;   // g1: the second group's index
                 for (int j = 0; j < np; ++j) {
                     const uint8_t *wt = smem + s * SLOT + WT_OFF4 + j * tb;
                     const uint4 q0 = *reinterpret_cast<const uint4 *>(wt + row * 32);
                     const uint4 q1 = *reinterpret_cast<const uint4 *>(wt + row * 32 + 16);
                     // scale and bias of values 0-31 and of values 32-63 (the same with one group)
                     const __half *scp = reinterpret_cast<const __half *>(wt + kQ4ScaleOff);
-                    const __half *bip = reinterpret_cast<const __half *>(wt + q4_bias_off(p.gpr));
+                    const __half *bip = reinterpret_cast<const __half *>(wt + q4_bias_off(GPR));
                     const __half2 sc2[2] = {__half2half2(scp[row]), __half2half2(scp[g1 * BM + row])};
                     const __half2 bi2[2] = {__half2half2(bip[row]), __half2half2(bip[g1 * BM + row])};
                     const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -646,11 +652,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     for (int q = 1; q < kClusterMax; ++q)
                         if (q < CS) { ga += a[q]; if (MODE == GATEUP) ub += b[q]; }
                     const int col = it.rt * BM + r;
-                    if (MODE == GATEUP) {
+                    if (MODE == GATEUP && W4) {
+                        // fp16 h * 2^-2e (the scaled token rows of the 4-bit path)
+                        const float hv = swiglu_scaled(ga, ub, p.xexp[it.row0 + j]);
+                        if (!(fabsf(hv) <= 65504.f)) flag_status(p.status, kDevCheckFailed);   // h beyond fp16
+                        p.h[(size_t)(it.row0 + j) * p.R + col] = __half_as_ushort(__float2half_rn(hv));
+                    } else if (MODE == GATEUP) {
                         p.h[(size_t)(it.row0 + j) * p.R + col] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(ga) * ub));
                     } else {
                         int tok = p.perm_tok[it.row0 + j];
                         float w = p.perm_w[it.row0 + j];
+                        if (W4) w *= ldexpf(1.f, 2 * p.xexp[it.row0 + j]);   // undo h's scale
                         if (!debug_index_ok(tok, p.T, p.status)) { tok = 0; w = 0.f; }   // (debug builds)
                         float *o = p.out + (size_t)tok * p.R + col;
                         if (p.k == 1) *o = w * ga;
@@ -904,7 +916,7 @@ bool decode_tc_down_direct(int T, int d, int E, int k, int F)
 // Cluster mode: CS CTAs per unit (CS = 8, 4 or 2) when the kernel's units
 // (16-row chunks x 128-row tiles, an upper bound before routing) then fill at
 // most one wave of CTAs and every K split keeps at least two k-blocks; 0
-// otherwise.  bf16 weights only.
+// otherwise.  bf16 and 4-bit weights.
 static int cluster_size(long long units, int kb_total, int num_sms)
 {
     // (allowing two or more waves of clusters measured slower: ZONOS2 decode T = 8
@@ -921,12 +933,12 @@ static long long cluster_chunks(int T, int E, int k)
 }
 int decode_tc_gateup_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
 {
-    if (w_dt != MOE_BF16 || decode_tc_gateup_fused(T, d, E, k, F, num_sms)) return 0;
+    if (!(w_dt == MOE_BF16 || is_q4(w_dt)) || decode_tc_gateup_fused(T, d, E, k, F, num_sms)) return 0;
     return cluster_size(cluster_chunks(T, E, k) * (F / dtc::BM), d / dtc::BK, num_sms);
 }
 int decode_tc_down_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
 {
-    if (w_dt != MOE_BF16 || k > 2 || decode_tc_down_direct(T, d, E, k, F)) return 0;
+    if (!(w_dt == MOE_BF16 || is_q4(w_dt)) || k > 2 || decode_tc_down_direct(T, d, E, k, F)) return 0;
     return cluster_size(cluster_chunks(T, E, k) * (d / dtc::BM), F / dtc::BK, num_sms);
 }
 bool decode_tc_down_into_out(int T, int d, int E, int k, int F, int w_dt, int num_sms)
@@ -971,22 +983,34 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     const int dev = current_device();
     if (!attr_done.done(dev)) {
         const int s16 = (int)smem_bytes<false>(), s4 = (int)smem_bytes<true>();
-        const int scl = (int)smem_bytes<false, true>();
+        const int scl = (int)smem_bytes<false, true>(), scl4 = (int)smem_bytes<true, true>();
         if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false, true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false, true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, false, true>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 1, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 2, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 1, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 2, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
             (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, true>,
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 1>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, true>,
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 1>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 2>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 2>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess)
             return err;
         attr_done.mark(dev);
@@ -1015,7 +1039,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     const int cl_gu = decode_tc_gateup_cluster(a.T, a.d, a.E, a.k, a.F, a.w_dt, a.num_sms);
     const int cl_d = decode_tc_down_cluster(a.T, a.d, a.E, a.k, a.F, a.w_dt, a.num_sms);
     const long long chunks_cl = cluster_chunks(a.T, a.E, a.k);
-    const size_t smem_cl = smem_bytes<false, true>();
+    const size_t smem_cl = w4 ? smem_bytes<true, true>() : smem_bytes<false, true>();
     // grid of a cluster-mode launch: whole clusters, at most one wave
     auto grid_cl = [&](long long units, int cs) {
         const long long per = (long long)a.num_sms * CTAS_PER_SM / cs;
@@ -1036,7 +1060,13 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     if (cl_gu) {
         p.xg = gather ? static_cast<const uint16_t *>(a.x_gather) : nullptr;
         p.perm_tok = a.perm_tok;
-        if (gather)
+        if (w4 && p.gpr == 2)
+            launch_pdl_cluster(decode_tc_kernel<GATEUP, false, 2, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
+                               dim3(THREADS_W4), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
+        else if (w4)
+            launch_pdl_cluster(decode_tc_kernel<GATEUP, false, 1, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
+                               dim3(THREADS_W4), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
+        else if (gather)
             launch_pdl_cluster(decode_tc_kernel<GATEUP, true, false, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
                                dim3(THREADS_GATHER), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
         else
@@ -1048,8 +1078,12 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
         launch_pdl(decode_tc_kernel<GATEUP, true, false>, g_gu, dim3(THREADS_GATHER), smem, stream, m_wg,
                    m_wu, m_x16, m_x32, p);
     } else if (w4) {
-        launch_pdl(decode_tc_kernel<GATEUP, false, true>, g_gu, dim3(THREADS_W4), smem, stream, m_wg, m_wu,
-                   m_x16, m_x32, p);
+        if (p.gpr == 2)
+            launch_pdl(decode_tc_kernel<GATEUP, false, 2>, g_gu, dim3(THREADS_W4), smem, stream, m_wg, m_wu,
+                       m_x16, m_x32, p);
+        else
+            launch_pdl(decode_tc_kernel<GATEUP, false, 1>, g_gu, dim3(THREADS_W4), smem, stream, m_wg, m_wu,
+                       m_x16, m_x32, p);
     } else {
         launch_pdl(decode_tc_kernel<GATEUP, false, false>, g_gu, dim3(THREADS), smem, stream, m_wg, m_wu,
                    m_x16, m_x32, p);
@@ -1086,11 +1120,20 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     } else {
         p.KS = ks_d; p.P = a.pd; p.perm_tok = nullptr;
     }
-    if (cl_d)
+    if (cl_d && w4 && p.gpr == 2)
+        launch_pdl_cluster(decode_tc_kernel<DOWN, false, 2, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
+                           dim3(THREADS_W4), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
+    else if (cl_d && w4)
+        launch_pdl_cluster(decode_tc_kernel<DOWN, false, 1, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
+                           dim3(THREADS_W4), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
+    else if (cl_d)
         launch_pdl_cluster(decode_tc_kernel<DOWN, false, false, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
                            dim3(THREADS), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
+    else if (w4 && p.gpr == 2)
+        launch_pdl(decode_tc_kernel<DOWN, false, 2>, dim3(grid_for(chunks * p.rtiles * p.KS)),
+                   dim3(THREADS_W4), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
     else if (w4)
-        launch_pdl(decode_tc_kernel<DOWN, false, true>, dim3(grid_for(chunks * p.rtiles * p.KS)),
+        launch_pdl(decode_tc_kernel<DOWN, false, 1>, dim3(grid_for(chunks * p.rtiles * p.KS)),
                    dim3(THREADS_W4), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
     else
         launch_pdl(decode_tc_kernel<DOWN, false, false>, dim3(grid_for(chunks * p.rtiles * p.KS)),

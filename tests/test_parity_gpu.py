@@ -401,13 +401,14 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
     (1, 2048, 16, 1, 2816),  # the ZONOS2 shape: 22 gate/up and 16 down units, clusters of 8
     (24, 512, 4, 2, 256),    # 48 rows: chunks of 16 rows, several per expert
 ])
-def test_decode_cluster_mode_deterministic_equivariant_and_matches_oracle(T, d, E, k, F):
-    """Small bf16 decode batches run the tensor-core decode kernels in cluster
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q4_A64, wl.Q4_K])
+def test_decode_cluster_mode_deterministic_equivariant_and_matches_oracle(T, d, E, k, F, wdt):
+    """Small decode batches run the tensor-core decode kernels in cluster
     mode: the K splits of a unit are reduced in shared memory across the
     cluster, in rank order.  Two runs give the same bits, permuting the
     tokens permutes the output rows bit for bit, and the result matches the
-    oracle."""
-    layer = wl.make_custom_layer(30, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16, w_dtype=wl.BF16,
+    oracle (bf16, affine 4-bit and Q4_K weights)."""
+    layer = wl.make_custom_layer(30, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16, w_dtype=wdt,
                                  bias_sd=0.5)
     t = upload_layer(layer, DEV)
     a, r = gpu_forward_views(layer, DEV, path=DECODE, t=t)
