@@ -30,10 +30,12 @@ from typing import Optional
 
 import numpy as np
 
-F32, BF16, Q8_0, Q4_A64, Q4_K = 0, 1, 2, 3, 4
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64", Q4_K: "q4_k"}
+F32, BF16, Q8_0, Q4_A64, Q4_K, Q6_K = 0, 1, 2, 3, 4, 5
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64", Q4_K: "q4_k", Q6_K: "q6_k"}
 Q4_K_BLOCK = 256
 Q4_K_BLOCK_BYTES = 144
+Q6_K_BLOCK = 256
+Q6_K_BLOCK_BYTES = 210
 Q4_A64_GROUP = 64
 Q4_A64_BLOCK_BYTES = 36
 Q8_0_BLOCK = 32
@@ -115,6 +117,18 @@ WORKLOADS = {
         description="ZONOS2-shaped decode step with Q4_K experts (the K-quant the "
                     "pages recommend for the expert stacks): d=2048, E=16, top-1, "
                     "F=2816, T in {1, 8, 64}, 28-layer weight rotation"),
+    "zonos2_decode_q6k": Workload(
+        "zonos2_decode_q6k", T=8, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q6_K, bias="normal", bias_sd=0.1, layers=28,
+        description="ZONOS2-shaped decode step with Q6_K experts (the K-quant ladder's "
+                    "sweet spot): d=2048, E=16, top-1, F=2816, T in {1, 8, 64}, "
+                    "28-layer weight rotation"),
+    "zonos2_prefill_q6k": Workload(
+        "zonos2_prefill_q6k", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q6_K, bias="normal", bias_sd=0.1, layers=4,
+        description="ZONOS2-shaped prefill with Q6_K experts: T=4096, d=2048, E=16, "
+                    "top-1, F=2816, bf16 activations and router (4 independent "
+                    "layers per benchmark step)"),
     "zonos2_prefill_q4k": Workload(
         "zonos2_prefill_q4k", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
         w_dtype=Q4_K, bias="normal", bias_sd=0.1, layers=4,
@@ -266,6 +280,49 @@ def q4_k_quantize(w) -> np.ndarray:
     return out
 
 
+def q6_k_pack(q, sc, d16) -> np.ndarray:
+    """6-bit codes q[..., 256] (0..63), int8 scales sc[..., 16] and fp16 d[...]
+    -> 210-byte Q6_K super-blocks [..., 210]: ql[128] (low 4 bits), qh[64] (top
+    2 bits), int8 scales[16], fp16 d.  Value v = 128 h + 32 g + l: low bits in
+    the low (g < 2) or high (g >= 2) nibble of ql[64 h + l + 32 (g % 2)], top
+    bits in bits 2g, 2g+1 of qh[32 h + l]."""
+    q = np.asarray(q, np.uint8).reshape(np.shape(q)[:-1] + (2, 4, 32))   # [..., h, g, l]
+    lo, hi = q & 15, (q >> 4) & 3
+    ql = np.concatenate([lo[..., 0, :] | (lo[..., 2, :] << 4), lo[..., 1, :] | (lo[..., 3, :] << 4)], axis=-1)
+    qh = hi[..., 0, :] | (hi[..., 1, :] << 2) | (hi[..., 2, :] << 4) | (hi[..., 3, :] << 6)
+    lead = q.shape[:-3]
+    out = np.empty(lead + (Q6_K_BLOCK_BYTES,), np.uint8)
+    out[..., 0:128] = ql.reshape(lead + (128,))
+    out[..., 128:192] = qh.reshape(lead + (64,))
+    out[..., 192:208] = np.asarray(sc, np.int8).view(np.uint8)
+    d16 = np.ascontiguousarray(np.asarray(d16, np.float16))
+    out[..., 208:210] = d16.reshape(d16.shape + (1,)).view(np.uint8)
+    return out
+
+
+def q6_k_quantize(w) -> np.ndarray:
+    """Encode w[..., K] (K % 256 == 0) as Q6_K super-blocks: uint8 [..., K/256, 210]
+    (q6_k_pack); value v decodes as d * scales[v / 16] * (q - 32).  This
+    encoder: per 16-value group step s = max|w| / 31; d = max s / 127 rounded
+    to fp16; scale = round(s / d) clamped to [0, 127]; q - 32 =
+    round-half-away(w / (d scale)) clamped to [-32, 31] with the stored d (0
+    where d scale = 0)."""
+    w = np.asarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    if K % Q6_K_BLOCK:
+        raise ValueError("Q6_K needs the contiguous axis to be a multiple of 256")
+    g = w.reshape(w.shape[:-1] + (K // Q6_K_BLOCK, 16, 16)).astype(np.float64)
+    step = np.abs(g).max(axis=-1) / 31.0
+    d16 = (step.max(axis=-1) / 127.0).astype(np.float16)
+    d = d16.astype(np.float64)
+    safe = lambda a: np.where(a > 0, a, 1.0)
+    sc = np.where(d[..., None] > 0, np.clip(np.floor(step / safe(d)[..., None] + 0.5), 0, 127), 0)
+    a = d[..., None] * sc
+    v = g / safe(a)[..., None]
+    q = np.where(a[..., None] > 0, np.clip(np.sign(v) * np.floor(np.abs(v) + 0.5), -32, 31), 0) + 32
+    return q6_k_pack(q.reshape(q.shape[:-2] + (256,)).astype(np.uint8), sc.astype(np.int8), d16)
+
+
 def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == F32:
         return np.ascontiguousarray(a, dtype=np.float32)
@@ -277,6 +334,8 @@ def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
         return q4_a64_quantize(a)
     if dtype == Q4_K:
         return q4_k_quantize(a)
+    if dtype == Q6_K:
+        return q6_k_quantize(a)
     raise ValueError(dtype)
 
 
@@ -356,6 +415,8 @@ def weight_bytes_per_expert(d: int, F: int, w_dtype: int) -> int:
         return n // Q4_A64_GROUP * Q4_A64_BLOCK_BYTES
     if w_dtype == Q4_K:
         return n // Q4_K_BLOCK * Q4_K_BLOCK_BYTES
+    if w_dtype == Q6_K:
+        return n // Q6_K_BLOCK * Q6_K_BLOCK_BYTES
     return n // Q8_0_BLOCK * Q8_0_BLOCK_BYTES
 
 
@@ -435,6 +496,34 @@ def q4_k_quantize_torch(w):
     return out
 
 
+def q6_k_quantize_torch(w):
+    """Device twin of q6_k_quantize: float32 [..., K] -> uint8 super-blocks
+    [..., K/256, 210] (same layout and rounding rules)."""
+    import torch
+    K = w.shape[-1]
+    g = w.reshape(*w.shape[:-1], K // Q6_K_BLOCK, 16, 16).double()
+    step = g.abs().amax(-1) / 31.0
+    d16 = (step.amax(-1) / 127.0).to(torch.float16)
+    d = d16.double()
+    sd = torch.where(d > 0, d, torch.ones_like(d))[..., None]
+    sc = torch.where(d[..., None] > 0, torch.clamp(torch.floor(step / sd + 0.5), 0, 127), torch.zeros_like(step))
+    a = d[..., None] * sc
+    v = g / torch.where(a > 0, a, torch.ones_like(a))[..., None]
+    q = (torch.where(a[..., None] > 0, torch.clamp(torch.sign(v) * torch.floor(v.abs() + 0.5), -32, 31),
+                     torch.zeros_like(v)) + 32).to(torch.uint8)
+    q = q.reshape(*q.shape[:-2], 2, 4, 32)                 # [..., h, g, l]
+    lo, hi = q & 15, (q >> 4) & 3
+    ql = torch.cat([lo[..., 0, :] | (lo[..., 2, :] << 4), lo[..., 1, :] | (lo[..., 3, :] << 4)], dim=-1)
+    qh = hi[..., 0, :] | (hi[..., 1, :] << 2) | (hi[..., 2, :] << 4) | (hi[..., 3, :] << 6)
+    lead = q.shape[:-3]
+    out = torch.empty(*lead, Q6_K_BLOCK_BYTES, dtype=torch.uint8, device=w.device)
+    out[..., 0:128] = ql.reshape(*lead, 128)
+    out[..., 128:192] = qh.reshape(*lead, 64)
+    out[..., 192:208] = sc.to(torch.int8).view(torch.uint8)
+    out[..., 208:210] = d16.contiguous().view(torch.uint8).reshape(*d16.shape, 2)
+    return out
+
+
 def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = None,
                       device="cuda", zipf_biases=None):
     """Draw ``layers`` independent layers directly in device memory.
@@ -448,8 +537,9 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
     layer's host-drawn x and W_r (zipf_host_inputs), which are used then.
     """
     import torch
-    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (BF16, Q4_K), (F32, F32)):
-        raise ValueError("device stacks: bf16/bf16, bf16/Q8_0, bf16/Q4_A64, bf16/Q4_K or fp32/fp32 layers")
+    if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (BF16, Q4_K),
+                                        (BF16, Q6_K), (F32, F32)):
+        raise ValueError("device stacks: bf16/bf16, bf16 with Q8_0, Q4_A64, Q4_K or Q6_K experts, or fp32/fp32")
     act = torch.float32 if w.act_dtype == F32 else torch.bfloat16
     T = w.T if T is None else T
     g = torch.Generator(device=device)
@@ -461,7 +551,7 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * sd
             if q8:
                 return {Q4_A64: q4_a64_quantize_torch, Q4_K: q4_k_quantize_torch,
-                        Q8_0: q8_0_quantize_torch}[w.w_dtype](t)
+                        Q6_K: q6_k_quantize_torch, Q8_0: q8_0_quantize_torch}[w.w_dtype](t)
             return t.to(act)
         d, E, F = w.d, w.E, w.F
         x = rn(T, d)
@@ -476,7 +566,7 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             b = torch.from_numpy(zipf_bias(E, rng)).to(device)
         else:
             b = torch.randn(E, generator=g, device=device, dtype=torch.float32) * w.bias_sd
-        q8 = w.w_dtype in (Q8_0, Q4_A64, Q4_K)   # block-quantised expert weights
+        q8 = w.w_dtype in (Q8_0, Q4_A64, Q4_K, Q6_K)   # block-quantised expert weights
         wg = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wu = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wd = rn(E, d, F, sd=1.0 / math.sqrt(F), q8=q8)

@@ -5,8 +5,8 @@
  * no code, header or table with the CUDA library.
  *
  * Plain C, fp64 throughout.  It reads the same storage bytes as the GPU path
- * (fp32, bf16 bit patterns, 34-byte Q8_0 blocks, 36-byte affine 4-bit blocks
- * or 144-byte Q4_K super-blocks) and widens them exactly.
+ * (fp32, bf16 bit patterns, 34-byte Q8_0 blocks, 36-byte affine 4-bit blocks,
+ * 144-byte Q4_K or 210-byte Q6_K super-blocks) and widens them exactly.
  * Steps follow the pages in order:
  *
  *   1. router projection: logit[t,e] = sum_i x[t,i] * W_r[e,i]
@@ -111,6 +111,31 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
                 }
             }
         }
+    } else if (dt == ORACLE_Q6_K) {
+        /* Q6_K ("zonos2.cpp internals", §Recommended: F16 spine + K-quant
+         * experts, 6.56 bits per weight, "the sweet spot"; the pages give no
+         * byte layout, this is the GGUF one): per row cols/256 super-blocks of
+         * 210 bytes {ql[128]: low 4 bits of the codes, qh[64]: their top 2
+         * bits, int8 scales[16], fp16 d}.  Value v (0..255) lies in half
+         * h = v / 128 at u = v % 128, with g = u / 32 and l = u % 32: its low
+         * bits are the low (g < 2) or high (g >= 2) nibble of
+         * ql[64h + l + 32 (g % 2)], its top bits bits 2g, 2g+1 of qh[32h + l];
+         * the 6-bit code q decodes as d * scales[v / 16] * (q - 32). */
+        const uint8_t *p = (const uint8_t *)base + row * (size_t)(cols / 256) * 210;
+        for (int b = 0; b < cols / 256; ++b) {
+            const uint8_t *blk = p + (size_t)b * 210;
+            const uint8_t *ql = blk, *qh = blk + 128;
+            const int8_t *sc = (const int8_t *)(blk + 192);
+            const double d = f16_bits_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+            for (int v = 0; v < 256; ++v) {
+                const int h = v / 128, u = v % 128, g = u / 32, l = u % 32;
+                const uint8_t lo_byte = ql[64 * h + l + 32 * (g % 2)];
+                const int lo = g < 2 ? (lo_byte & 15) : (lo_byte >> 4);
+                const int hi = (qh[32 * h + l] >> (2 * g)) & 3;
+                const int q = lo | (hi << 4);
+                out[b * 256 + v] = d * (double)sc[v / 16] * (double)(q - 32);
+            }
+        }
     } else { /* ORACLE_Q4_A64 ("Zyphra-ZONOS2-4bit", §How this was quantized:
               * experts at 4 bits, groups of 64, affine; the byte layout is this
               * library's): per row cols/64 blocks of {fp16 scale, fp16 bias,
@@ -133,7 +158,7 @@ static int valid_act(int dt) { return dt == ORACLE_F32 || dt == ORACLE_BF16; }
 static int valid_w(int dt)
 {
     return dt == ORACLE_F32 || dt == ORACLE_BF16 || dt == ORACLE_Q8_0 || dt == ORACLE_Q4_A64 ||
-           dt == ORACLE_Q4_K;
+           dt == ORACLE_Q4_K || dt == ORACLE_Q6_K;
 }
 
 /* ------------------------------------------------------------ thread helper */
@@ -426,7 +451,7 @@ int oracle_expert_combine(const void *x, int x_dt, int T, int d, const int32_t *
         return -1;
     if (w_dt == ORACLE_Q8_0 && (d % 32 || F % 32)) return -1;
     if (w_dt == ORACLE_Q4_A64 && (d % 64 || F % 64)) return -1;
-    if (w_dt == ORACLE_Q4_K && (d % 256 || F % 256)) return -1;
+    if ((w_dt == ORACLE_Q4_K || w_dt == ORACLE_Q6_K) && (d % 256 || F % 256)) return -1;
     for (size_t i = 0; i < (size_t)T * k; ++i)
         if (topk_idx[i] < 0 || topk_idx[i] >= E) return -1;
     if (T == 0) return 0;

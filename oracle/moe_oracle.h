@@ -6,7 +6,9 @@
  * Storage dtypes: 0 = fp32, 1 = bf16 bit patterns (uint16), 2 = Q8_0 rows of
  * 34-byte blocks {fp16 scale, int8 q[32]} along the contiguous axis, 3 = affine
  * 4-bit rows of 36-byte blocks of 64 values {fp16 scale, fp16 bias, 32 bytes:
- * value 2j in the low nibble of byte j, 2j+1 in the high}, value = scale*q + bias.
+ * value 2j in the low nibble of byte j, 2j+1 in the high}, value = scale*q + bias,
+ * 4 = Q4_K rows of 144-byte super-blocks of 256 values, 5 = Q6_K rows of 210-byte
+ * super-blocks of 256 values (GGUF layouts; see moe_oracle.c).
  * Activations (x, W_r) are fp32 or bf16; expert weights may also be Q8_0.
  * Layouts (row-major): x[T,d], W_r[E,d], W_g[E,F,d], W_u[E,F,d], W_d[E,d,F].
  * All functions return 0 on success, -1 on invalid arguments.
@@ -21,7 +23,7 @@
 extern "C" {
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3, ORACLE_Q4_K = 4 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3, ORACLE_Q4_K = 4, ORACLE_Q6_K = 5 };
 
 int oracle_default_threads(void);
 

@@ -41,6 +41,20 @@ def decode(a, dtype):
     if dtype == wl.BF16:
         return wl.bf16_bits_to_f32(a).astype(np.float64)
     blocks = np.asarray(a, np.uint8)
+    if dtype == wl.Q6_K:
+        # 256 values per 210 bytes: ql[128] low 4 bits, qh[64] top 2 bits,
+        # int8 scales[16] (one per 16 values), fp16 d; code q, value d*sc*(q-32).
+        # Written per value from the layout: v = 128h + 32g + l.
+        d6 = blocks[..., 208:210].copy().view(np.float16)[..., 0].astype(np.float64)
+        sc6 = blocks[..., 192:208].copy().view(np.int8).astype(np.float64)
+        w = np.empty(blocks.shape[:-1] + (256,), np.float64)
+        for v in range(256):
+            h, g, l = v // 128, (v % 128) // 32, v % 32
+            lo_byte = blocks[..., 64 * h + l + 32 * (g % 2)].astype(np.int64)
+            lo = (lo_byte & 15) if g < 2 else (lo_byte >> 4)
+            hi = (blocks[..., 128 + 32 * h + l].astype(np.int64) >> (2 * g)) & 3
+            w[..., v] = d6 * sc6[..., v // 16] * ((lo + 16 * hi) - 32)
+        return w.reshape(w.shape[:-2] + (w.shape[-2] * w.shape[-1],))
     scale = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
     if dtype == wl.Q4_K:
         # 256 values per 144 bytes: d, dmin, 12 bytes of 6-bit (scale, min)
@@ -242,10 +256,10 @@ def test_k_equals_e_is_dense_softmax_gating():
 
 
 @pytest.mark.parametrize("act,wdt", [(wl.F32, wl.F32), (wl.BF16, wl.BF16), (wl.BF16, wl.Q8_0),
-                                     (wl.BF16, wl.Q4_A64), (wl.BF16, wl.Q4_K)])
+                                     (wl.BF16, wl.Q4_A64), (wl.BF16, wl.Q4_K), (wl.BF16, wl.Q6_K)])
 @pytest.mark.parametrize("k", [1, 2, 3])
 def test_matches_dense_brute_force(act, wdt, k):
-    d, F = (256, 256) if wdt == wl.Q4_K else (64, 96) if wdt != wl.Q4_A64 else (64, 128)
+    d, F = (256, 256) if wdt in (wl.Q4_K, wl.Q6_K) else (64, 96) if wdt != wl.Q4_A64 else (64, 128)
     layer = tiny_layer(seed=10 + k, act=act, wdt=wdt, T=5, d=d, E=6, k=k, F=F, bias_sd=0.3)
     out, idx, w, margin = oracle.moe_forward(layer)
     ref, sel, logits = brute_force_dense(layer)
@@ -614,3 +628,49 @@ def test_q4_k_encoder_error_within_half_a_step():
     assert np.all(np.abs(deq - w) <= bound)
     assert np.sqrt(np.mean((deq - w) ** 2)) < 0.15 * np.sqrt(np.mean(w ** 2))
 
+
+
+# ------------------------------------------- Q6_K super-blocks (next row f3)
+def test_q6_k_super_block_worked_example():
+    """A hand-built super-block: d = 0.25, scales[j] = 3j - 20 (negative and
+    positive int8 scales), code q = (5v + 3) mod 64 for value v, so that every
+    code and both top-bit positions occur.  The 210 bytes are assembled here
+    value by value from the format's description (ql nibble, qh bit pair,
+    scale byte, d); value v must be 0.25 * (3 (v // 16) - 20) * (q - 32), the
+    library's packer must emit the same bytes, and the oracle reads them."""
+    q = np.array([(5 * v + 3) % 64 for v in range(256)])
+    scs = np.array([3 * j - 20 for j in range(16)])
+    blk = np.zeros(210, np.uint8)
+    for v in range(256):
+        h, g, l = v // 128, (v % 128) // 32, v % 32
+        lo, hi = q[v] & 15, q[v] >> 4
+        blk[64 * h + l + 32 * (g % 2)] |= lo << (4 * (g // 2))
+        blk[128 + 32 * h + l] |= hi << (2 * g)
+    blk[192:208] = scs.astype(np.int8).view(np.uint8)
+    blk[208:210] = np.array([0.25], np.float16).view(np.uint8)
+    assert np.array_equal(wl.q6_k_pack(q.astype(np.uint8), scs.astype(np.int8), np.float16(0.25)), blk)
+    want = np.array([0.25 * scs[v // 16] * (q[v] - 32) for v in range(256)])
+    assert np.array_equal(decode(blk[None, None], wl.Q6_K)[0], want)
+    T, d, F = 3, 256, 256
+    layer = tiny_layer(seed=95, act=wl.F32, wdt=wl.Q6_K, T=T, d=d, E=1, k=1, F=F)
+    layer.w_gate = np.tile(blk, (1, F, 1)).reshape(1, F, 1, 210)
+    x = decode(layer.x, wl.F32)
+    g = x @ np.tile(want, (F, 1)).T
+    u = x @ decode(layer.w_up, wl.Q6_K)[0].T
+    ref = (g / (1.0 + np.exp(-g)) * u) @ decode(layer.w_down, wl.Q6_K)[0].T
+    out, _, _, _ = oracle.moe_forward(layer)
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_q6_k_encoder_error_within_half_a_step():
+    rng = np.random.default_rng(96)
+    w = (rng.standard_normal((8, 512)) * 0.05).astype(np.float32)
+    b = wl.q6_k_quantize(w)
+    deq = decode(b, wl.Q6_K)
+    d = b[..., 208:210].copy().view(np.float16)[..., 0].astype(np.float64)
+    sc = b[..., 192:208].copy().view(np.int8).astype(np.float64)
+    # half a step of each 16-value group, plus the scale's rounding to a
+    # multiple of d (at most d / 2 per unit of |q - 32| <= 32)
+    bound = (0.5 * d[..., None] * np.abs(sc) + 16 * d[..., None]).repeat(16, axis=-1).reshape(8, 512)
+    assert np.all(np.abs(deq - w) <= bound)
+    assert np.sqrt(np.mean((deq - w) ** 2)) < 0.03 * np.sqrt(np.mean(w ** 2))

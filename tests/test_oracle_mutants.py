@@ -98,6 +98,14 @@ MUTANTS = {
                       "d * (double)sc * (double)q + dmin * (double)m;", 0),
     "q4k_d_dmin_swapped": ("const double dmin = f16_bits_to_double((uint16_t)(blk[2] | (blk[3] << 8)));",
                            "const double dmin = f16_bits_to_double((uint16_t)(blk[0] | (blk[1] << 8)));", 0),
+    # Q6_K super-blocks ("zonos2.cpp internals", §Recommended: F16 spine + K-quant experts)
+    "q6k_top_bits_shift": ("const int hi = (qh[32 * h + l] >> (2 * g)) & 3;",
+                           "const int hi = (qh[32 * h + l] >> g) & 3;", 0),
+    "q6k_scale_per_32": ("(double)sc[v / 16]", "(double)sc[v / 32]", 0),
+    "q6k_no_offset": ("(double)(q - 32)", "(double)q", 0),
+    "q6k_nibble_halves_swapped": ("const int lo = g < 2 ? (lo_byte & 15) : (lo_byte >> 4);",
+                                  "const int lo = g < 2 ? (lo_byte >> 4) : (lo_byte & 15);", 0),
+    "q6k_ql_run_offset": ("ql[64 * h + l + 32 * (g % 2)]", "ql[64 * h + l + 32 * (g / 2)]", 0),
     # bf16 storage
     "bf16_low_half": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;", 0),
 }
