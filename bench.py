@@ -217,9 +217,10 @@ def expert_kernel_names(w, T, num_sms):
     timed as one stage."""
     rows = T * w.k
     act16 = w.act_dtype == 1
-    if (act16 and w.w_dtype in (1, 2, 3, 4) and w.d % 256 == 0 and w.F % 128 == 0
+    if (act16 and w.w_dtype in (1, 2, 3, 4, 5) and w.d % 256 == 0 and w.F % 128 == 0
             and rows >= 64 * w.E and T >= 512):
-        q = {1: "bf16", 2: "Q8_0, CTA pairs", 3: "4-bit, CTA pairs", 4: "Q4_K, CTA pairs"}[w.w_dtype]
+        q = {1: "bf16", 2: "Q8_0, CTA pairs", 3: "4-bit, CTA pairs", 4: "Q4_K, CTA pairs",
+             5: "Q6_K, CTA pairs"}[w.w_dtype]
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4, "fused": False}
     if act16 and w.w_dtype in (1, 3, 4) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
@@ -356,7 +357,7 @@ def host_layer_from_device(w, dl, T):
         if t.dtype == torch.float32:
             return t.contiguous().cpu().numpy()
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    if w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K):   # the oracle reads the blocks themselves
+    if w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K):   # the oracle reads the blocks themselves
         wts = {n: dl["blocks"][n].cpu().numpy() for n in ("w_gate", "w_up", "w_down")}
     else:
         wts = {n: bits(dl[n]) for n in ("w_gate", "w_up", "w_down")}
@@ -453,14 +454,14 @@ def scoring_mode(args):
 
 def compute_peak(w, peaks, dev_props, kernels=None):
     """The compute roofline of a workload's expert arithmetic: the measured
-    dense bf16 tensor peak for bf16 weights and for Q8_0 and affine 4-bit
-    weights on the tensor-core kernels (fp16 operands, the same dense rate);
-    for fp32 weights and 4-bit weights on the CUDA-core kernels, which run as
+    dense bf16 tensor peak for bf16 weights and for block-quantised weights on
+    the tensor-core kernels (fp16 operands, the same dense rate); for fp32
+    weights and block-quantised weights on the CUDA-core kernels, which run as
     fp32 FMAs, 128 FMA lanes x 2 flops per SM per clock at the device's
     maximum SM clock ("alu")."""
     from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
     simt = kernels is None or kernels["file"] == "decode.cu"
-    if w.w_dtype == wl.F32 or (w.w_dtype in (wl.Q4_A64, wl.Q4_K) and simt):
+    if w.w_dtype == wl.F32 or (w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K) and simt):
         mhz = float(peaks.get("sm_max_mhz") or 0) or dev_props.clock_rate / 1e3
         return dev_props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12, "alu", \
             "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock"
@@ -513,10 +514,10 @@ def setup_stack(pkg, wl, w, T, layers, seed, dev):
                                  zipf_biases=fit[0] if fit else None)
     act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
     w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0,
-            wl.Q4_A64: pkg.MOE_Q4_A64, wl.Q4_K: pkg.MOE_Q4_K}[w.w_dtype]
-    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64, pkg.MOE_Q4_K):
+            wl.Q4_A64: pkg.MOE_Q4_A64, wl.Q4_K: pkg.MOE_Q4_K, wl.Q6_K: pkg.MOE_Q6_K}[w.w_dtype]
+    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64, pkg.MOE_Q4_K, pkg.MOE_Q6_K):
         pack = {pkg.MOE_Q8_0: pkg.moe_pack_q8_0, pkg.MOE_Q4_A64: pkg.moe_pack_q4_a64,
-                pkg.MOE_Q4_K: pkg.moe_pack_q4_k}[w_dt]
+                pkg.MOE_Q4_K: pkg.moe_pack_q4_k, pkg.MOE_Q6_K: pkg.moe_pack_q6_k}[w_dt]
         for L in stack:
             L["blocks"] = {n: L[n] for n in ("w_gate", "w_up", "w_down")}
             for n, rows, cols in (("w_gate", w.E * w.F, w.d), ("w_up", w.E * w.F, w.d),
@@ -694,7 +695,9 @@ SIDE_WORKLOADS = [("tiny_fp32", None, None, 8), ("zonos2_decode", 1, None, 1),
                   ("zonos2_decode_q4", 1, None, 1), ("zonos2_decode_q4", 8, None, 8),
                   ("zonos2_decode_q4", 64, None, 64), ("zonos2_prefill_q4", None, None, 192),
                   ("zonos2_decode_q4k", 1, None, 1), ("zonos2_decode_q4k", 8, None, 8),
-                  ("zonos2_decode_q4k", 64, None, 64), ("zonos2_prefill_q4k", None, None, 192)]
+                  ("zonos2_decode_q4k", 64, None, 64), ("zonos2_prefill_q4k", None, None, 192),
+                  ("zonos2_decode_q6k", 1, None, 1), ("zonos2_decode_q6k", 8, None, 8),
+                  ("zonos2_prefill_q6k", None, None, 192)]
 
 
 def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, peak_src,
@@ -991,6 +994,8 @@ def main():
         "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands",
                   wl.Q4_A64: ("affine 4-bit weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
                               else "affine 4-bit weights, f16 tensor-core operands"),
+                  wl.Q6_K: ("q6_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
+                            else "q6_k weights, f16 tensor-core operands"),
                   wl.Q4_K: ("q4_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
                             else "q4_k weights, f16 tensor-core operands")}[w.w_dtype],
         "data": "synthetic", "config": config_dict(w, T, layers, args),

@@ -16,8 +16,8 @@ import torch
 
 from . import build as _build
 
-MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K = 0, 1, 2, 3, 4
-PACKED = (MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K)   # storage types moe_forward takes repacked
+MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K = 0, 1, 2, 3, 4, 5
+PACKED = (MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K)   # storage types moe_forward takes repacked
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_PATH_DECODE_SIMT = 0, 1, 2, 3
 MOE_SCORE_SELECTED_SOFTMAX, MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "moe_permute",
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_q4_a64_packed_size", "moe_pack_q4_a64",
-           "moe_q4_k_packed_size", "moe_pack_q4_k",
+           "moe_q4_k_packed_size", "moe_pack_q4_k", "moe_q6_k_packed_size", "moe_pack_q6_k",
            "moe_workspace_size", "moe_forward",
            "moe_forward_profiled", "moe_forward_scored", "moe_ffn_dense", "moe_forward_noalloc",
            "moe_workspace_views", "moe_forward_expire_wait", "moe_check", "moe_check_noalloc")
@@ -100,6 +100,10 @@ def _declare(L):
     L.moe_q4_k_packed_size.restype = sz
     L.moe_pack_q4_k.argtypes = [vp, ll, i, vp, vp]
     L.moe_pack_q4_k.restype = i
+    L.moe_q6_k_packed_size.argtypes = [ll, i]
+    L.moe_q6_k_packed_size.restype = sz
+    L.moe_pack_q6_k.argtypes = [vp, ll, i, vp, vp]
+    L.moe_pack_q6_k.restype = i
     L.moe_workspace_size.argtypes = [i, i, i, i, i, i, i]
     L.moe_workspace_size.restype = sz
     L.moe_forward.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz, i, vp]
@@ -233,6 +237,23 @@ def moe_pack_q4_k(blocks: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
     return packed
 
 
+def moe_q6_k_packed_size(rows: int, cols: int) -> int:
+    return int(load_library().moe_q6_k_packed_size(rows, cols))
+
+
+def moe_pack_q6_k(blocks: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
+    """Repack Q6_K super-blocks (uint8 device tensor, rows*cols/256*210 bytes)
+    into the 8-bit planes moe_forward takes."""
+    L = load_library()
+    n = moe_q6_k_packed_size(rows, cols)
+    if n == 0 and rows != 0:
+        raise MoeError(1, "moe_q6_k_packed_size")
+    packed = torch.empty(max(n, 256), dtype=torch.uint8, device=blocks.device)
+    _check(L.moe_pack_q6_k(_ptr(blocks), rows, cols, _ptr(packed), _stream(blocks)),
+           "moe_pack_q6_k")
+    return packed
+
+
 def moe_workspace_size(T: int, d: int, E: int, k: int, F: int, act_dt: int, w_dt: int) -> int:
     return int(load_library().moe_workspace_size(T, d, E, k, F, act_dt, w_dt))
 
@@ -246,8 +267,8 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
     """The whole MoE layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [E,F,d], [E,F,d], [E,d,F]; or, with
-    w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K, uint8 buffers from moe_pack_q8_0 /
-    moe_pack_q4_a64 / moe_pack_q4_k (then F is required).
+    w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K / MOE_Q6_K, uint8 buffers from moe_pack_q8_0 /
+    moe_pack_q4_a64 / moe_pack_q4_k / moe_pack_q6_k (then F is required).
     events: optional sequence of 6 torch.cuda.Event(enable_timing=True), recorded
     at the stage boundaries (moe_forward_profiled).
     scoring: a MOE_SCORE_* mode (moe_forward_scored when not SelectedSoftmax).
@@ -300,8 +321,8 @@ def moe_ffn_dense(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor,
     """A dense SwiGLU FFN layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [F,d], [F,d], [d,F] (or [1,F,d] ...); or,
-    with w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K, uint8 buffers from moe_pack_q8_0 /
-    moe_pack_q4_a64 / moe_pack_q4_k (then F is required).
+    with w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K / MOE_Q6_K, uint8 buffers from moe_pack_q8_0 /
+    moe_pack_q4_a64 / moe_pack_q4_k / moe_pack_q6_k (then F is required).
     """
     L = load_library()
     T, d = x.shape

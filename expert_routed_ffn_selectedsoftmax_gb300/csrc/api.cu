@@ -42,7 +42,7 @@ bool scoring_ok(int scoring)
 bool weights_ok(int act_dt, int w_dt)
 {
     if (act_dt == MOE_F32) return w_dt == MOE_F32;
-    return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt);
+    return w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt);
 }
 
 // Largest d the router kernel can stage (one token of fp32 in <= 200 KB).
@@ -72,7 +72,7 @@ struct WsLayout {
 
 bool prefill_capable(int act_dt, int w_dt, int d, int F)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt)) &&
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt)) &&
            d % 256 == 0 && F % 128 == 0;
 }
 
@@ -135,13 +135,14 @@ moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, con
     if (st != MOE_OK) return st;
     if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
     if (!weights_ok(act_dt, w_dt)) {
-        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt))
+        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt))
                    ? MOE_ERR_UNSUPPORTED
                    : MOE_ERR_INVALID_ARG;
     }
     if (w_dt == MOE_Q8_0 && (d % 32 || F % 32)) return MOE_ERR_INVALID_ARG;
     if (w_dt == MOE_Q4_A64 && (d % 64 || F % 64)) return MOE_ERR_INVALID_ARG;
-    if (w_dt == MOE_Q4_K && (d % 256 || F % 256)) return MOE_ERR_INVALID_ARG;   // whole super-blocks
+    if ((w_dt == MOE_Q4_K || w_dt == MOE_Q6_K) && (d % 256 || F % 256))
+        return MOE_ERR_INVALID_ARG;   // whole super-blocks
     if (path != MOE_PATH_AUTO && path != MOE_PATH_DECODE && path != MOE_PATH_PREFILL &&
         path != MOE_PATH_DECODE_SIMT)
         return MOE_ERR_INVALID_ARG;
@@ -152,7 +153,7 @@ moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, con
     if (!w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
     if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
         return MOE_ERR_INVALID_ARG;
-    if (w_dt == MOE_Q8_0 || is_q4(w_dt)) {
+    if (is_q8p(w_dt) || is_q4(w_dt)) {
         const uintptr_t m = 255u;
         if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
             (reinterpret_cast<uintptr_t>(w_down) & m))
@@ -264,6 +265,22 @@ moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *pac
     if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
         return MOE_ERR_INVALID_ARG;
     cudaError_t e = launch_pack_q8_0(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_q6_k_packed_size(long long rows, int cols)
+{
+    if (rows < 0 || cols <= 0 || cols % 256) return 0;
+    return align_up((size_t)rows * cols, 256) + (size_t)rows * (cols / 16) * 2;
+}
+
+moe_status moe_pack_q6_k(const void *blocks, long long rows, int cols, void *packed, moe_stream stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 256) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    cudaError_t e = launch_pack_q6_k(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -450,7 +467,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
                                                                                                 : nullptr;
     // the Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels take fp16
     // rows (scaled)
-    ra.xp_fp16 = w_dt == MOE_Q8_0 || is_q4(w_dt);
+    ra.xp_fp16 = is_q8p(w_dt) || is_q4(w_dt);
     ra.xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     // the fused decode kernel's flags and ticket start at zero

@@ -108,17 +108,19 @@ template <> __device__ __forceinline__ void WView<__nv_bfloat16>::cvt(const RawW
     c.v[6] = bf16lo(r.a.w); c.v[7] = bf16hi(r.a.w);
 }
 
-// Q8_0 view: p points at the q plane; the fp16 scale plane [cols/32, rows]
-// follows at align256(rows*cols) bytes.  `scales` and `rows` are set by the host.
+// 8-bit planes view (Q8_0, Q6_K): p points at the q plane; the fp16 scale
+// plane [cols/group, rows] follows at align256(rows*cols) bytes.  `scales`,
+// `rows` and `group` (32 or 16 values per scale) are set by the host.
 template <> struct WView<Q8Tag> {
     const int8_t *q;
     const __half *scales;
     size_t cols;
     size_t rows;
+    int group;
     __device__ __forceinline__ void load(size_t row, int col, RawW<Q8Tag> &r) const
     {
         r.q = ld_stream_u2(q + row * cols + col);
-        r.s = __half2float(scales[(size_t)(col / 32) * rows + row]);
+        r.s = __half2float(scales[(size_t)(col / group) * rows + row]);
     }
     __device__ __forceinline__ static void cvt(const RawW<Q8Tag> &r, Chunk8 &c)
     {
@@ -147,6 +149,10 @@ template <> struct WView<Q8Tag> {
 // one per 16-bit half.
 // the 4-bit storage types (packed tiles) and their affine groups per tile row
 __host__ __device__ __forceinline__ constexpr bool is_q4(int w_dt) { return w_dt == MOE_Q4_A64 || w_dt == MOE_Q4_K; }
+// the 8-bit planes (int8 plane + fp16 scale plane [cols / group, rows]): Q8_0
+// with a scale per 32 values, Q6_K repacked with one per 16
+__host__ __device__ __forceinline__ constexpr bool is_q8p(int w_dt) { return w_dt == MOE_Q8_0 || w_dt == MOE_Q6_K; }
+__host__ __device__ __forceinline__ constexpr int q8_group(int w_dt) { return w_dt == MOE_Q6_K ? 16 : 32; }
 __host__ __device__ __forceinline__ constexpr int q4_gpr(int w_dt) { return w_dt == MOE_Q4_K ? 2 : 1; }
 constexpr int kQ4TileRows = 128, kQ4ScaleOff = 4096;
 constexpr int kQ4TileBytes = 4608, kQ4BiasOff = 4352;   // one group per row (affine 4-bit)

@@ -369,9 +369,11 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
                                               view4(a.w_up, (long long)a.E * a.F, a.d),
                                               view4(a.w_down, (long long)a.E * a.d, a.F), stream);
     }
-    // Q8_0 packed planes: q plane, then the fp16 scales at align256(rows*cols)
-    auto view = [](const void *p, long long rows, int cols) {
+    // Q8_0 / Q6_K packed planes: q plane, then the fp16 scales at align256(rows*cols)
+    const int group = q8_group(a.w_dt);
+    auto view = [group](const void *p, long long rows, int cols) {
         WView<Q8Tag> v;
+        v.group = group;
         v.q = static_cast<const int8_t *>(p);
         v.scales = reinterpret_cast<const __half *>(static_cast<const char *>(p) +
                                                     align_up((size_t)rows * cols, 256));

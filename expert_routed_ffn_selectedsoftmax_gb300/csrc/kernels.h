@@ -180,5 +180,8 @@ cudaError_t launch_pack_q4_k(const void *blocks, long long rows, int cols, void 
                              cudaStream_t stream);
 cudaError_t launch_pack_q4_a64(const void *blocks, long long rows, int cols, void *packed,
                                cudaStream_t stream);
+// q8.cu -- Q6_K super-blocks repacked into the 8-bit planes, one scale per 16 values
+cudaError_t launch_pack_q6_k(const void *blocks, long long rows, int cols, void *packed,
+                             cudaStream_t stream);
 
 }  // namespace moe

@@ -178,6 +178,50 @@ cudaError_t launch_pack_q4_k(const void *blocks, long long rows, int cols, void 
     return cudaGetLastError();
 }
 
+// Q6_K super-blocks ("zonos2.cpp internals", §Recommended: F16 spine + K-quant
+// experts; the GGUF layout: ql[128] low 4 bits, qh[64] top 2 bits, int8
+// scales[16], fp16 d; value v = d * scales[v / 16] * (q - 32)) -> the 8-bit
+// planes with one scale per 16 values: int8 q - 32 and fp16(d * scales[j]).
+// One thread per (row, 16-value group).
+__global__ void pack_q6_k_kernel(const uint8_t *__restrict__ blocks, long long n, int groups_per_row,
+                                 long long rows, int8_t *__restrict__ q, __half *__restrict__ scales)
+{
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long row = t / groups_per_row;
+        const int j = (int)(t - row * groups_per_row);   // 16-value group of the row
+        const uint8_t *blk = blocks + ((size_t)row * (groups_per_row / 16) + j / 16) * 210;
+        const float d = __half2float(__ushort_as_half((uint16_t)(blk[208] | (blk[209] << 8))));
+        const int jb = j % 16;                          // group within the super-block
+        scales[(size_t)j * rows + row] = __float2half_rn(d * (float)(int8_t)blk[192 + jb]);
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int v = 16 * jb + i, h = v / 128, g = (v % 128) / 32, l = v % 32;
+            const uint8_t lo_byte = blk[64 * h + l + 32 * (g % 2)];
+            const int lo = g < 2 ? (lo_byte & 15) : (lo_byte >> 4);
+            const int hi = (blk[128 + 32 * h + l] >> (2 * g)) & 3;
+            const uint32_t code = (uint32_t)(uint8_t)(int8_t)((lo | (hi << 4)) - 32);
+            w[i / 4] |= code << (8 * (i % 4));
+        }
+        *reinterpret_cast<uint4 *>(q + (size_t)t * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+cudaError_t launch_pack_q6_k(const void *blocks, long long rows, int cols, void *packed,
+                             cudaStream_t stream)
+{
+    const long long n = rows * (cols / 16);
+    if (n == 0) return cudaSuccess;
+    int8_t *q = static_cast<int8_t *>(packed);
+    __half *s = reinterpret_cast<__half *>(static_cast<char *>(packed) + align_up((size_t)rows * cols, 256));
+    long long grid = (n + 255) / 256;
+    if (grid > 65535LL * 16) grid = 65535LL * 16;
+    pack_q6_k_kernel<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint8_t *>(blocks), n,
+                                                         cols / 16, rows, q, s);
+    return cudaGetLastError();
+}
+
 size_t q4_a64_packed_bytes(long long rows, int cols)
 {
     const long long tiles_r = (rows + kQ4TileRows - 1) / kQ4TileRows;

@@ -111,9 +111,10 @@ constexpr int kConvWarps = MOE_GEMM_CONV_WARPS;   // Q8_0 converter warps (4 or 
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 
-// Weight storage of a variant: 16-bit, Q8_0 or affine 4-bit (the last two
-// through converter warps).
-enum WKind { W16 = 0, WQ8 = 1, WQ4 = 2 };
+// Weight storage of a variant: 16-bit, 8-bit planes with a scale per 32 values
+// (Q8_0) or per 16 (Q6_K, repacked), or 4-bit tiles (the last three through
+// converter warps).
+enum WKind { W16 = 0, WQ8 = 1, WQ4 = 2, WQ6 = 3 };
 
 // Per-variant shared-memory layout: a ring of STAGES stages {A, this CTA's
 // part of B (16-bit), of Bq (int8) + its scales, or its packed 4-bit tiles},
@@ -125,7 +126,9 @@ template <int WQ, bool PAIR> struct Cfg {
     static constexpr int B_BYTES = BNL * BK * 2;    // 16-bit B (this CTA's rows)
     // packed B (4-bit: room for the larger, Q4_K, tiles)
     static constexpr int BQ_BYTES = WQ == WQ4 ? (BNL / kQ4TileRows) * kQ4KTileBytes : BNL * BK;
-    static constexpr int SCL_BYTES = WQ == WQ4 ? 0 : SC_BYTES / CL;   // Q8_0 scales
+    // 8-bit planes' scales: per k-block of 64 columns, NSB blocks of BN/2 rows
+    static constexpr int NSB = WQ == WQ6 ? 4 : 2;
+    static constexpr int SCL_BYTES = WQ == WQ4 ? 0 : SC_BYTES * (NSB / 2) / CL;
     static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SCL_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
     static constexpr int STAGES = Q8 ? (PAIR ? MOE_GEMM_PAIR_Q8_STAGES : MOE_GEMM_Q8_STAGES) : (PAIR ? 6 : 4);
@@ -396,21 +399,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     if (PAIR) {
                         const CUtensorMap *bm = rank ? &tm_b1 : &tm_b0;
                         tma_load_2d(sb, bm, &c.full[s], kb * BK, grow);
-                        if (Q8) tma_load_2d(sc, rank ? &tm_s1 : &tm_s0, &c.full[s], grow, kb * 2);
+                        if (Q8) tma_load_2d(sc, rank ? &tm_s1 : &tm_s0, &c.full[s], grow, kb * C::NSB);
                     } else {
                         constexpr int half_b = (Q8 ? C::BQ_BYTES : C::B_BYTES) / 2;
                         tma_load_2d(sb, &tm_b0, &c.full[s], kb * BK, grow);
                         tma_load_2d(sb + half_b, &tm_b1, &c.full[s], kb * BK, grow);
                         if (Q8) {
-                            tma_load_2d(sc, &tm_s0, &c.full[s], grow, kb * 2);
-                            tma_load_2d(sc + SC_BYTES / 2, &tm_s1, &c.full[s], grow, kb * 2);
+                            tma_load_2d(sc, &tm_s0, &c.full[s], grow, kb * C::NSB);
+                            tma_load_2d(sc + C::SCL_BYTES / 2, &tm_s1, &c.full[s], grow, kb * C::NSB);
                         }
                     }
                 } else {
                     tma_load_2d(sb, &tm_b0, &c.full[s], kb * BK, drow);   // BNL-row box
                     if (Q8) {
-                        tma_load_2d(sc, &tm_s0, &c.full[s], drow, kb * 2);
-                        if (!PAIR) tma_load_2d(sc + SC_BYTES / 2, &tm_s0, &c.full[s], drow + BN / 2, kb * 2);
+                        tma_load_2d(sc, &tm_s0, &c.full[s], drow, kb * C::NSB);
+                        if (!PAIR) tma_load_2d(sc + C::SCL_BYTES / 2, &tm_s0, &c.full[s], drow + BN / 2, kb * C::NSB);
                     }
                 }
             }
@@ -528,9 +531,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 #pragma unroll
                 for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
                     const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
-                    // scale of (row r, 32-column block q/2): boxes of [2 blocks][128 rows]
-                    const int blk = q >> 1;
-                    const __half sv = scl[(r >> 7) * 256 + blk * 128 + (r & 127)];
+                    // scale of (row r, values 16q .. 16q+15): boxes of [NSB blocks][128
+                    // rows], a block 32 columns (Q8_0) or 16 (Q6_K)
+                    const int blk = C::NSB == 4 ? q : q >> 1;
+                    const __half sv = scl[(r >> 7) * (128 * C::NSB) + blk * 128 + (r & 127)];
                     const uint4 v = *reinterpret_cast<const uint4 *>(bq + r * 64 + q * 16);
                     uint4 lo, hi;
                     dequant16(v, __half2half2(sv), lo, hi);
@@ -704,7 +708,8 @@ template <int WQ, bool PAIR> constexpr size_t smem_bytes()
 static_assert(sizeof(SmemCtl) % 16 == 0, "the staging rows after the control block take float4 stores");
 static_assert(smem_bytes<W16, true>() <= 232448 && smem_bytes<WQ8, true>() <= 232448 &&
                   smem_bytes<W16, false>() <= 232448 && smem_bytes<WQ8, false>() <= 232448 &&
-                  smem_bytes<WQ4, true>() <= 232448 && smem_bytes<WQ4, false>() <= 232448,
+                  smem_bytes<WQ4, true>() <= 232448 && smem_bytes<WQ4, false>() <= 232448 &&
+                  smem_bytes<WQ6, true>() <= 232448 && smem_bytes<WQ6, false>() <= 232448,
               "shared memory per CTA");
 
 // ------------------------------------------------------------------- host
@@ -759,7 +764,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 }  // namespace tc
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
-bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || w_dt == MOE_Q8_0 || is_q4(w_dt); }
+bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt); }
 
 bool tc_gemm_prefer(int T, int d, int E, int k, int F)
 {
@@ -822,13 +827,15 @@ static int max_active_pairs()
 
 bool tc_gemm_pairs(moe_dtype w_dt)
 {
-    const bool q8 = w_dt == MOE_Q8_0, q4 = is_q4(w_dt);
+    const bool q8 = is_q8p(w_dt), q4 = is_q4(w_dt);
     if (MOE_GEMM_PAIR == 0 || (MOE_GEMM_PAIR == 1 && !q8 && !q4)) return false;
     if constexpr (MOE_GEMM_PAIR >= 2) {
         if (!q8 && !q4)
             return max_active_pairs<tc::GATEUP, tc::W16>() > 0 && max_active_pairs<tc::DOWN, tc::W16>() > 0;
     }
     if (q4) return max_active_pairs<tc::GATEUP, tc::WQ4>() > 0 && max_active_pairs<tc::DOWN, tc::WQ4>() > 0;
+    if (w_dt == MOE_Q6_K)
+        return max_active_pairs<tc::GATEUP, tc::WQ6>() > 0 && max_active_pairs<tc::DOWN, tc::WQ6>() > 0;
     return q8 && max_active_pairs<tc::GATEUP, tc::WQ8>() > 0 && max_active_pairs<tc::DOWN, tc::WQ8>() > 0;
 }
 
@@ -880,8 +887,9 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
 {
     using namespace tc;
-    const bool q8 = a.w_dt == MOE_Q8_0, q4 = is_q4(a.w_dt);
+    const bool q8 = is_q8p(a.w_dt), q4 = is_q4(a.w_dt);
     const bool f16 = q8 || q4;   // fp16 operands (converted weights)
+    const int g8 = q8_group(a.w_dt);   // values per scale of the 8-bit planes
     if (!f16 && a.w_dt != MOE_BF16) return cudaErrorNotSupported;
     const int rows = a.T * a.k;
     cudaError_t err = cudaSuccess;
@@ -914,15 +922,15 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     }
     if (!ok) return cudaErrorInvalidValue;
 
-    // Q8_0 packed buffers: int8 plane, then the fp16 scale plane [cols/32, rows]
-    // at align256(rows * cols); maps with box {128 rows, 2 blocks}
-    auto scale_map = [](CUtensorMap *m, const void *packed, uint64_t r, uint64_t cols) {
+    // 8-bit packed buffers: int8 plane, then the fp16 scale plane [cols/g8, rows]
+    // at align256(rows * cols); maps with box {128 rows, 64/g8 blocks}
+    auto scale_map = [g8](CUtensorMap *m, const void *packed, uint64_t r, uint64_t cols) {
         auto enc = encode_fn();
         if (!enc) return false;
         const void *base = static_cast<const char *>(packed) + align_up((size_t)(r * cols), 256);
-        cuuint64_t dims[2] = {r, cols / 32};
+        cuuint64_t dims[2] = {r, cols / (uint64_t)g8};
         cuuint64_t strides[1] = {r * 2};
-        cuuint32_t box[2] = {(cuuint32_t)(BN / 2), 2};
+        cuuint32_t box[2] = {(cuuint32_t)(BN / 2), (cuuint32_t)(64 / g8)};
         cuuint32_t estr[2] = {1, 1};
         return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -948,6 +956,9 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     if (q4)
         return pair ? launch_gemms<WQ4, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
                     : launch_gemms<WQ4, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+    if (a.w_dt == MOE_Q6_K)
+        return pair ? launch_gemms<WQ6, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                    : launch_gemms<WQ6, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
     if (q8)
         return pair ? launch_gemms<WQ8, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
                     : launch_gemms<WQ8, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);

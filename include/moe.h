@@ -28,7 +28,8 @@
  *    (1..256), k experts per token (1..min(E, 8)), F expert ffn width.
  *  - Activation storage (x, W_r): MOE_F32 or MOE_BF16; logits, routing
  *    weights and the output are fp32.  Expert weights: MOE_F32 (with F32
- *    activations), MOE_BF16, MOE_Q8_0, MOE_Q4_A64 or MOE_Q4_K (with BF16 activations).
+ *    activations), MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K or MOE_Q6_K (with BF16
+ *    activations).
  *  - Calls on distinct workspaces and outputs are independent; there is no
  *    global mutable state.
  */
@@ -61,7 +62,7 @@ typedef enum {
     MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (see moe_check) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3, MOE_Q4_K = 4 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3, MOE_Q4_K = 4, MOE_Q6_K = 5 } moe_dtype;
 
 /* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
  * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16 or
@@ -239,6 +240,32 @@ MOE_API moe_status moe_pack_q4_k(const void *blocks, long long rows, int cols, v
                                  moe_stream stream);
 
 /*
+ * Q6_K expert weights (MOE_Q6_K): the K-quant the pages call the sweet spot of
+ * the expert ladder ("zonos2.cpp internals", §Recommended: F16 spine + K-quant
+ * experts: Q6_K at 6.56 bits per weight; the pages give no byte layout, this
+ * is the GGUF one).  Input format: rows of `cols` values (cols % 256 == 0),
+ * stored as cols/256 super-blocks of 210 bytes {ql[128]: low 4 bits of the
+ * 6-bit codes, qh[64]: their top 2 bits, int8 scales[16], fp16 d (little
+ * endian)}.  Value v = 128h + 32g + l of a block (h < 2, g < 4, l < 32): low
+ * bits in the low (g < 2) or high (g >= 2) nibble of ql[64h + l + 32 (g % 2)],
+ * top bits in bits 2g and 2g+1 of qh[32h + l]; it decodes as
+ * d * scales[v / 16] * (q - 32).
+ * moe_forward consumes them repacked like Q8_0 into two planes in one buffer,
+ * with one scale per 16 values:
+ *   bytes [0, rows*cols)                              int8 plane [rows, cols], q - 32
+ *   bytes [align256(rows*cols), ... + rows*cols/8)    fp16 scale plane [cols/16, rows]
+ *   (the scale of group j of row r, fp16(d * scales[j]), at index j*rows + r)
+ * and takes them where Q8_0 goes: the grouped GEMMs (fp16 operands, the same
+ * range rules) and the CUDA-core decode kernels (fp32), with d and F
+ * multiples of 256.  moe_q6_k_packed_size returns the buffer size (0 if
+ * cols % 256 != 0 or rows < 0); moe_pack_q6_k repacks `blocks` (device, any
+ * alignment) into `packed` (device, 256-byte aligned) on `stream`.
+ */
+MOE_API size_t moe_q6_k_packed_size(long long rows, int cols);
+MOE_API moe_status moe_pack_q6_k(const void *blocks, long long rows, int cols, void *packed,
+                                 moe_stream stream);
+
+/*
  * Bytes of device workspace moe_forward needs for these sizes (any path).
  * 0 on invalid sizes.  The workspace is scratch owned by the caller; its
  * first 256 bytes hold the device status word read by moe_check.
@@ -272,9 +299,9 @@ MOE_API moe_status moe_workspace_views(int T, int d, int E, int k, int F, moe_dt
 /*
  * moe_forward -- the whole layer, steps 1-5.
  *   x[T,d] (act_dt), w_router[E,d] (act_dt), sel_bias[E] fp32 or NULL,
- *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K: the
- *   buffers written by moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k, 256-byte
- *   aligned),
+ *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K / Q6_K:
+ *   the buffers written by moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k /
+ *   moe_pack_q6_k, 256-byte aligned),
  *   out[T,d] fp32 (overwritten).
  *   workspace: device scratch of at least moe_workspace_size() bytes,
  *   256-byte aligned; it must not be shared by calls that can overlap.
@@ -329,8 +356,8 @@ MOE_API moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, in
  *   §Model architecture: dense FFN layers beside the MoE ones; "New Community
  *   Model: ZONOS3-Mini (Zyphra) - #1271", §Summary: layer 0 has a dense SwiGLU
  *   FFN).  No router: every token goes to the one expert with weight 1.
- *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K: packed by
- *   moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k with rows = F or d); other arguments as
+ *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K / Q6_K: packed
+ *   by the matching moe_pack_* with rows = F or d); other arguments as
  *   moe_forward, with a workspace of moe_workspace_size(T, d, 1, 1, F, act_dt,
  *   w_dt) bytes.
  */

@@ -117,6 +117,14 @@ def test_argument_errors_are_synchronous(lib):
     # one row tile x 4 tile columns, 5120 bytes per tile (two scale/bias pairs a row)
     assert lib.moe_q4_k_packed_size(4, 256) == 4 * 5120
     assert lib.moe_q4_k_packed_size(129, 512) == 2 * 8 * 5120
+    assert fwd(wdt=5, F=128) == I                # Q6_K: whole 256-value super-blocks
+    assert fwd(act=0, wdt=5, F=256) == U         # Q6_K takes bf16 activations
+    assert lib.moe_pack_q6_k(fake, 4, 192, fake, None) == I
+    assert lib.moe_pack_q6_k(fake, 4, 256, vp(0x10010), None) == I
+    assert lib.moe_q6_k_packed_size(4, 192) == 0
+    # int8 plane (padded to 256 bytes), then fp16 scales, one per 16 values
+    assert lib.moe_q6_k_packed_size(3, 256) == 768 + 3 * 16 * 2
+    assert lib.moe_q6_k_packed_size(2, 512) == 1024 + 2 * 32 * 2
     assert fwd(path=9) == I
     assert fwd(wg=None) == I
     assert fwd(ws=vp(0x10010)) == I              # workspace not 256-byte aligned

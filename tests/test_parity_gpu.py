@@ -146,6 +146,9 @@ SMALL = [
     (wl.BF16, wl.Q4_K, 70, 512, 16, 1, 256),    #   tile row, whole 256-value super-blocks
     (wl.BF16, wl.Q4_K, 128, 1024, 64, 2, 512),
     (wl.BF16, wl.Q4_K, 300, 512, 16, 4, 768),
+    (wl.BF16, wl.Q6_K, 5, 256, 8, 2, 256),      # Q6_K experts: 8-bit planes, a scale per 16
+    (wl.BF16, wl.Q6_K, 70, 512, 16, 1, 512),    #   values (CUDA-core decode kernels)
+    (wl.BF16, wl.Q6_K, 33, 1024, 64, 2, 256),
     (wl.BF16, wl.BF16, 5, 512, 64, 8, 128),     # few tokens: largest E and k of the small-batch router
     (wl.BF16, wl.BF16, 8, 2048, 33, 3, 128),    # few tokens: ragged E, longest rows
     (wl.BF16, wl.BF16, 40, 256, 256, 8, 128),   # the largest E and k the library takes
@@ -247,7 +250,8 @@ FULL_CASES = [("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode
               ("zonos2_decode", 8), ("zonos2_decode", 64), ("zonos3_mini_prefill", None),
               ("zonos2_prefill_q8", None), ("zonos2_decode_q4", 1), ("zonos2_decode_q4", 8),
               ("zonos2_decode_q4", 64), ("zonos2_prefill_q4", None), ("zonos2_decode_q4k", 1),
-              ("zonos2_decode_q4k", 8), ("zonos2_decode_q4k", 64), ("zonos2_prefill_q4k", None)]
+              ("zonos2_decode_q4k", 8), ("zonos2_decode_q4k", 64), ("zonos2_prefill_q4k", None),
+              ("zonos2_decode_q6k", 1), ("zonos2_decode_q6k", 8), ("zonos2_prefill_q6k", None)]
 
 
 @pytest.mark.parametrize("seed", [2, 7, 13])
@@ -259,8 +263,8 @@ def test_forward_workloads_full(name, T, seed):
     the 1e-3 margin, near ties resolved validly, weights within 2e-6, counts,
     offsets, permutation and inverse bit-exact -- and every output row within
     the tolerance."""
-    if "_q4" in name and seed == 13:
-        pytest.skip("the 4-bit workloads run with two seeds")
+    if ("_q4" in name or "_q6" in name) and seed == 13:
+        pytest.skip("the 4-bit and 6-bit workloads run with two seeds")
     layer = wl.make_layer(wl.WORKLOADS[name], seed=seed, T=T)
     out, r = gpu_forward_views(layer, DEV, path=0)
     check_routing_views(r, layer)
@@ -338,12 +342,13 @@ def test_forward_prefill_small_matches_oracle(T, d, E, k, F, wdt):
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
+@pytest.mark.parametrize("wdt", [wl.Q4_K, wl.Q6_K])
 @pytest.mark.parametrize("T,d,E,k,F", [c for c in PREFILL_SMALL if c[1] % 256 == 0 and c[4] % 256 == 0])
-def test_forward_prefill_small_q4_k_matches_oracle(T, d, E, k, F):
-    """Q4_K experts on the grouped GEMMs (the shapes above with whole
+def test_forward_prefill_small_q4_k_matches_oracle(T, d, E, k, F, wdt):
+    """Q4_K and Q6_K experts on the grouped GEMMs (the shapes above with whole
     256-value super-blocks along d and F)."""
     layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
-                                 w_dtype=wl.Q4_K, bias_sd=0.5)
+                                 w_dtype=wdt, bias_sd=0.5)
     out, r = gpu_forward_views(layer, DEV, path=PREFILL)
     check_routing_views(r, layer)
     ref, idx_ref, w_ref, margin = oracle.moe_forward(layer)
@@ -364,14 +369,14 @@ def test_prefill_one_expert_many_tiles():
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64, wl.Q4_K])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K])
 def test_prefill_and_decode_paths_agree(wdt):
     layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
                                  w_dtype=wdt)
     t = upload_layer(layer, DEV)
     a = gpu_forward(layer, DEV, path=SIMT, t=t).cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(a ** 2))
-    for path in ((PREFILL,) if wdt == wl.Q8_0 else (DECODE, PREFILL)):
+    for path in ((PREFILL,) if wdt in (wl.Q8_0, wl.Q6_K) else (DECODE, PREFILL)):
         b = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy().astype(np.float64)
         assert np.abs(a - b).max() <= 2e-2 * rms
 
@@ -537,7 +542,8 @@ def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
     (DECODE, 128, wl.Q4_A64, 64, 512),    # whole-K gate/up writing h itself
     (DECODE, 300, wl.Q4_A64, 8, 256),     # rows grouped by the scatter kernel
     (PREFILL, 600, wl.Q4_A64, 8, 256),    # 4-bit grouped GEMMs
-    (DECODE, 40, wl.Q4_K, 8, 256), (PREFILL, 600, wl.Q4_K, 8, 256)])
+    (DECODE, 40, wl.Q4_K, 8, 256), (PREFILL, 600, wl.Q4_K, 8, 256),
+    (PREFILL, 600, wl.Q6_K, 8, 256)])   # Q6_K grouped GEMMs: scales per 16 values
 def test_fp16_operands_large_activations(path, T, wdt, E, F):
     """The Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels
     multiply fp16 operands.  Token rows whose magnitudes span 1e-2 .. 1e5 (h
@@ -576,7 +582,8 @@ def test_fp16_operands_large_activations(path, T, wdt, E, F):
     (wl.Q4_A64, DECODE, 128, 64, 2, 512),    # 4-bit: whole-K gate/up epilogue
     (wl.Q4_A64, PREFILL, 256, 4, 1, 128),    # 4-bit grouped GEMMs
     (wl.Q4_K, DECODE, 256, 4, 1, 256),
-    (wl.Q4_K, PREFILL, 256, 4, 1, 256)])
+    (wl.Q4_K, PREFILL, 256, 4, 1, 256),
+    (wl.Q6_K, PREFILL, 256, 4, 1, 256)])
 def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     """Expert weights large enough that h leaves fp16's range even for
     normalised rows: the call reports MOE_ERR_DEVICE_CHECK instead of
@@ -588,7 +595,7 @@ def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     rng = np.random.default_rng(6)
     big = lambda *s: (rng.standard_normal(s) * 4e3).astype(np.float32)
     quant = {wl.Q8_0: wl.q8_0_quantize, wl.Q4_A64: wl.q4_a64_quantize,
-             wl.Q4_K: wl.q4_k_quantize}[wdt]
+             wl.Q4_K: wl.q4_k_quantize, wl.Q6_K: wl.q6_k_quantize}[wdt]
     layer.w_dtype = wdt
     layer.w_gate = quant(big(E, F, d))
     layer.w_up = quant(big(E, F, d))
@@ -723,3 +730,37 @@ def test_q4_k_pack_tile_layout(rows, cols):
                 want[t + 4608 + 256 * g + 2 * rr:t + 4610 + 256 * g + 2 * rr] = \
                     np.array([bias]).view(np.uint8)
     assert got.shape == want.shape and np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("rows,cols", [(130, 256), (3, 512)])
+def test_q6_k_pack_planes(rows, cols):
+    """moe_pack_q6_k's output, byte for byte, against the planes its header
+    states, built here with numpy from the 210-byte super-blocks: the int8
+    plane [rows, cols] holds q - 32 of every value (low nibble from ql, top
+    bits from qh), and the fp16 plane [cols/16, rows] at align256(rows*cols)
+    holds fp16(d * scales[j]) of 16-value group j."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    rng = np.random.default_rng(rows * 7 + cols)
+    w = (rng.standard_normal((rows, cols)) * rng.uniform(0.1, 3.0, (rows, 1))).astype(np.float32)
+    blocks = wl.q6_k_quantize(w)                       # [rows, cols/256, 210]
+    n = pkg.moe_q6_k_packed_size(rows, cols)
+    got = pkg.moe_pack_q6_k(torch.from_numpy(blocks.reshape(-1).copy()).to(DEV), rows, cols).cpu().numpy()[:n]
+    q = np.zeros((rows, cols), np.int8)
+    scales = np.zeros((cols // 16, rows), np.float16)
+    for r in range(rows):
+        for sb in range(cols // 256):
+            blk = blocks[r, sb]
+            d = np.float32(blk[208:210].copy().view(np.float16)[0])
+            sc = blk[192:208].copy().view(np.int8)
+            for v in range(256):
+                h, g, l = v // 128, (v % 128) // 32, v % 32
+                lo_byte = int(blk[64 * h + l + 32 * (g % 2)])
+                lo = (lo_byte & 15) if g < 2 else (lo_byte >> 4)
+                hi = (int(blk[128 + 32 * h + l]) >> (2 * g)) & 3
+                q[r, 256 * sb + v] = (lo | (hi << 4)) - 32
+            for j in range(16):
+                scales[16 * sb + j, r] = np.float16(d * np.float32(sc[j]))
+    off = (rows * cols + 255) // 256 * 256
+    assert n == off + scales.size * 2
+    assert np.array_equal(got[:rows * cols], q.reshape(-1).view(np.uint8))
+    assert np.array_equal(got[off:n], scales.reshape(-1).view(np.uint8))
