@@ -223,10 +223,10 @@ def expert_kernel_names(w, T, num_sms):
              5: "Q6_K, CTA pairs"}[w.w_dtype]
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4, "fused": False}
-    if act16 and w.w_dtype in (1, 3, 4) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
+    if act16 and w.w_dtype in (1, 2, 3, 4, 5) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
         n_exp = min(w.E, rows)
         small = T <= 128 and w.d // 64 <= 64 and w.k <= w.E
-        q4 = w.w_dtype in (3, 4)
+        q4 = w.w_dtype in (2, 3, 4, 5)   # converted weights (4- or 8-bit): fp16 token rows
         if (not q4 and w.k <= 2 and n_exp * (w.F // 128) * 2 >= 2 * num_sms
                 and 2 * 128 * w.d * 2 <= 512 << 10):
             name = "decode_fused_kernel (gate/up + SwiGLU + down + combine, one launch)"
@@ -249,7 +249,7 @@ def expert_kernel_names(w, T, num_sms):
         # tokens, else from a gather kernel
         launches = (1 if small else 2) + (1 if q4 and small and T > 16 else 0) + \
             (1 if fused or cl_gu else 2) + (1 if direct or cl_d else 2)
-        tag = {3: ", 4-bit", 4: ", Q4_K"}.get(w.w_dtype, "")
+        tag = {2: ", Q8_0", 3: ", 4-bit", 4: ", Q4_K", 5: ", Q6_K"}.get(w.w_dtype, "")
         gu = f"decode_tc_kernel<GATEUP{tag}> (whole K, writes h)" if fused else \
             f"decode_tc_kernel<GATEUP{tag}> (clusters of {cl_gu}, writes h)" if cl_gu else \
             f"decode_tc_kernel<GATEUP{tag}> + swiglu_reduce_kernel"
@@ -696,8 +696,10 @@ SIDE_WORKLOADS = [("tiny_fp32", None, None, 8), ("zonos2_decode", 1, None, 1),
                   ("zonos2_decode_q4", 64, None, 64), ("zonos2_prefill_q4", None, None, 192),
                   ("zonos2_decode_q4k", 1, None, 1), ("zonos2_decode_q4k", 8, None, 8),
                   ("zonos2_decode_q4k", 64, None, 64), ("zonos2_prefill_q4k", None, None, 192),
+                  ("zonos2_decode_q8", 1, None, 1), ("zonos2_decode_q8", 8, None, 8),
+                  ("zonos2_decode_q8", 64, None, 64),
                   ("zonos2_decode_q6k", 1, None, 1), ("zonos2_decode_q6k", 8, None, 8),
-                  ("zonos2_prefill_q6k", None, None, 192)]
+                  ("zonos2_decode_q6k", 64, None, 64), ("zonos2_prefill_q6k", None, None, 192)]
 
 
 def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, peak_src,
@@ -991,7 +993,9 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {wl.F32: "f32", wl.BF16: "bf16", wl.Q8_0: "q8_0 weights, f16 tensor-core operands",
+        "dtype": {wl.F32: "f32", wl.BF16: "bf16",
+                  wl.Q8_0: ("q8_0 weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
+                            else "q8_0 weights, f16 tensor-core operands"),
                   wl.Q4_A64: ("affine 4-bit weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
                               else "affine 4-bit weights, f16 tensor-core operands"),
                   wl.Q6_K: ("q6_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"

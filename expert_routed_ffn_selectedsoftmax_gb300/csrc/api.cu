@@ -94,7 +94,7 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.tile_cnt = take(4 * (size_t)(T > 0 ? T : 1) * (size_t)E);   // <= one tile per token
     L.h = take(4 * n * (size_t)F);            // fp32 (decode); prefill uses 2 bytes/element
     // the decode_tc_capable() shape/dtype conditions, without the driver query
-    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt)) && d % 128 == 0 &&
+    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) && d % 128 == 0 &&
             F % 128 == 0 && n <= (size_t)kDecodeTcMaxRows;
     L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
     L.pgu = L.pd = L.flags = off;
@@ -103,7 +103,7 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.y = k > 2 ? take(4 * n * (size_t)d) : off;
     // Q8_0 / 4-bit grouped GEMMs and 4-bit tensor-core decode: exponent of
     // each fp16 grouped row's scale
-    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt != MOE_BF16) || (L.dtc && is_q4(w_dt)))
+    L.xexp = ((prefill_capable(act_dt, w_dt, d, F) && w_dt != MOE_BF16) || (L.dtc && w_dt != MOE_BF16))
                  ? take(4 * n) : off;
     L.n_flags = 0;
     if (L.dtc) {
@@ -462,7 +462,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // the clustered router writes grouped rows only as fp16, for the 4-bit
     // tensor-core decode kernels, and only for up to 16 tokens: beyond that a
     // separate gather kernel writes them sooner than the router's owners do
-    const bool router_rows = is_q4(w_dt) && T <= kRouteSmallRowsMaxT;
+    const bool router_rows = (is_q4(w_dt) || is_q8p(w_dt)) && T <= kRouteSmallRowsMaxT;
     ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && (!fused_small || router_rows)) ? ws + L.xp
                                                                                                 : nullptr;
     // the Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels take fp16
@@ -562,11 +562,11 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.perm_w = perm_w;
         int32_t *xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
         a.xexp = xexp;
-        const int q4 = is_q4(w_dt);
-        if (fused_small && !q4) {
-            a.x_gather = x;   // (the 4-bit kernels take fp16 token rows by TMA from xp)
+        const int conv = is_q4(w_dt) || is_q8p(w_dt);   // converted weights: fp16 token rows
+        if (fused_small && !conv) {
+            a.x_gather = x;   // (the converted-weight kernels take fp16 token rows by TMA from xp)
         } else if (!xp_ready &&
-                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, q4, xexp, T, status, num_sms, s) != cudaSuccess) {
+                   launch_gather_rows(x, d, perm_tok, T * k, xp_rows, conv, xexp, T, status, num_sms, s) != cudaSuccess) {
             return MOE_ERR_CUDA;
         }
         if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;

@@ -200,6 +200,29 @@ __device__ __forceinline__ uint4 q4_word_fp16x8(uint32_t w, __half2 sc2, __half2
                       q4_pair_fp16(w8 & 0x00F000F0u, sixteenth2, fx.hi, sc2, bi2));
 }
 
+// int8 x 16 (one uint4) -> fp16 x 16 scaled by s: (q ^ 0x80) placed in the
+// mantissa of 1024.0 gives 1024 + 128 + q exactly; subtracting 1152 leaves q,
+// and the product with s is the one rounding.  Output in value order (lo:
+// values 0-7, hi: 8-15, two per 32-bit word).
+__device__ __forceinline__ void dequant16(const uint4 q, const __half2 s, uint4 &lo, uint4 &hi)
+{
+    const uint32_t w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u,
+                           q.w ^ 0x80808080u};
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t a = __byte_perm(w[i], 0x64646464u, 0x4140);
+        uint32_t b = __byte_perm(w[i], 0x64646464u, 0x4342);
+        __half2 ha = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&a), bias), s);
+        __half2 hb = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&b), bias), s);
+        o[2 * i] = *reinterpret_cast<uint32_t *>(&ha);
+        o[2 * i + 1] = *reinterpret_cast<uint32_t *>(&hb);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 template <> struct WView<Q4Tag> {
     const uint8_t *q;     // packed tiles
     int groups;           // cols / 64

@@ -101,14 +101,33 @@ constexpr int WT_OFF4 = 2 * 4096;               // the two weight tiles (4608 or
 static_assert(WT_OFF4 + 2 * kQ4KTileBytes <= SLOT4 && SLOT4 % 1024 == 0, "W4 stage layout");
 constexpr int NCVT4 = MOE_DTC_NCVT4;
 constexpr int THREADS_W4 = 320;                 // + 4 converter warps
+// 8-bit planes (Q8_0, and Q6_K repacked: int8 q plane + fp16 scales per 32 or
+// 16 values) take the same converter path: a stage holds two parts, each an
+// int8 tile of 128 rows x 64 columns (TMA, 64-byte swizzle, so that the
+// converter lanes -- one row each -- read distinct banks) and its scales
+// ([64 / group][128] fp16, TMA), beside the fp16 token tiles; the converters
+// dequantise q * scale with one rounding to fp16 (dequant16) into the
+// A operand in tensor memory.
+#ifndef MOE_DTC_STAGES8
+#define MOE_DTC_STAGES8 3
+#endif
+constexpr int STAGES8 = MOE_DTC_STAGES8;
+constexpr int WT_OFF8 = 2 * 4096;               // two int8 tiles of 8 KB
+constexpr int Q8_TILE = 8192;
+constexpr int SC_OFF8 = WT_OFF8 + 2 * Q8_TILE;  // two scale boxes of up to 1 KB
+constexpr int SC8_MAX = 1024;
+constexpr int SLOT8 = SC_OFF8 + 2 * SC8_MAX;    // 26 KB
+static_assert(SLOT8 % 1024 == 0, "8-bit stage layout");
 constexpr int kStagesMax = STAGES4 > STAGES ? STAGES4 : STAGES;
-template <bool W4> struct Ring {
-    static constexpr int NST = W4 ? STAGES4 : STAGES;
-    static constexpr int SLOTB = W4 ? SLOT4 : SLOT;
-    static constexpr int B_OFF = W4 ? 0 : A_BYTES;      // token tile
+static_assert(STAGES8 <= kStagesMax, "barrier arrays");
+// ring of weight kind K: 0 bf16, 1 4-bit tiles, 2 8-bit planes
+template <int K> struct Ring {
+    static constexpr int NST = K == 0 ? STAGES : K == 1 ? STAGES4 : STAGES8;
+    static constexpr int SLOTB = K == 0 ? SLOT : K == 1 ? SLOT4 : SLOT8;
+    static constexpr int B_OFF = K == 0 ? A_BYTES : 0;  // token tile
     static constexpr int CTL = NST * SLOTB;
-    // TMEM: NACC accumulators of 32 columns, then (W4) NCVT4 A buffers of 32
-    static constexpr uint32_t TMEM_COLS = W4 ? 256 : 128;
+    // TMEM: NACC accumulators of 32 columns, then (converted kinds) NCVT4 A buffers of 32
+    static constexpr uint32_t TMEM_COLS = K == 0 ? 128 : 256;
 };
 constexpr int NACC = 4;                         // TMEM accumulators of 32 columns
 constexpr uint32_t A_COL4 = NACC * 32;          // W4: first column of the converted A buffers
@@ -285,17 +304,24 @@ __device__ __forceinline__ void build_units(Ctl &c, const Params &p, bool offset
 // into the 128-byte-swizzled layout the MMA expects.
 // W4 (affine 4-bit weights): tm_w0/tm_w1 are unused; each stage's weight tile
 // is one contiguous copy from p.w4[m], converted to fp16 by warps 6-9.
-// W4: 0 for bf16 weights, else the 4-bit tiles' affine groups per tile row
-// (1: affine 4-bit, 2: Q4_K), fixed at compile time.
-template <int MODE, bool GATHER, int W4, bool CL = false>
-__global__ void __launch_bounds__(GATHER || W4 ? THREADS_GATHER : THREADS, CTAS_PER_SM)
+// WQ: the weight storage, fixed at compile time: 0 bf16; 1 affine 4-bit and
+// 2 Q4_K tiles (1 or 2 affine groups per tile row); 3 Q8_0 and 4 Q6_K 8-bit
+// planes (a scale per 32 or 16 values).  tm_s0/tm_s1: the 8-bit planes' scale
+// maps (GATEUP: gate, up; DOWN: down), unused otherwise.
+template <int MODE, bool GATHER, int WQ, bool CL = false>
+__global__ void __launch_bounds__(GATHER || WQ ? THREADS_GATHER : THREADS, CTAS_PER_SM)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                  const __grid_constant__ CUtensorMap tm_b16, const __grid_constant__ CUtensorMap tm_b32,
+                 const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
                  const Params p)
 {
-    static_assert(!(GATHER && W4), "4-bit weights take the token rows by TMA");
-    using RG = Ring<(W4 != 0)>;
-    constexpr int GPR = W4 ? W4 : 1;
+    constexpr bool Q8P = WQ == 3 || WQ == 4;   // 8-bit planes
+    constexpr bool W4 = WQ != 0;               // converted weights (4- or 8-bit): fp16 A in TMEM
+    static_assert(!(GATHER && W4), "converted weights take the token rows by TMA");
+    using RG = Ring<Q8P ? 2 : (W4 ? 1 : 0)>;
+    constexpr int GPR = WQ == 2 ? 2 : 1;       // 4-bit tiles: affine groups per tile row
+    constexpr int NSB8 = WQ == 4 ? 4 : 2;      // 8-bit planes: scale blocks per k-block
+    constexpr int SCB8 = NSB8 * 128 * 2;       //   their bytes per 128-row tile
     constexpr int STAGES = RG::NST, SLOT = RG::SLOTB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -322,10 +348,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
-        if (!W4)
+        if (!W4 || Q8P)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
-        if (MODE == GATEUP && !W4)
+        if (MODE == GATEUP && (!W4 || Q8P))
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w1)) : "memory");
+        if (Q8P) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s0)) : "memory");
+            if (MODE == GATEUP)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s1)) : "memory");
+        }
         if (!GATHER) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b16)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b32)) : "memory");
@@ -386,6 +417,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
             const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
+            if constexpr (Q8P) {
+                const int nst = w4_stages<CL>(p, it);
+                for (int st = 0; st < nst; ++st, ++it_k) {
+                    const int s = it_k % STAGES;
+                    if (!mbar_wait(&c.empty[s], ((it_k / STAGES) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                    const int np = w4_parts(p, it, st), ntok = p.fused ? 1 : np;
+                    mbar_expect_tx(&c.full[s], (uint32_t)(np * (Q8_TILE + SCB8) + ntok * it.nt * BK * 2));
+                    uint8_t *sp = smem + s * SLOT;
+                    for (int j = 0; j < np; ++j) {
+                        int m, kb, tt;
+                        w4_part<CL>(p, it, st, j, m, kb, tt);
+                        const bool second = MODE == GATEUP && m == 1;
+                        tma_load_2d(sp + WT_OFF8 + j * Q8_TILE, second ? &tm_w1 : &tm_w0, &c.full[s], kb * BK, wrow);
+                        tma_load_2d(sp + SC_OFF8 + j * SC8_MAX, second ? &tm_s1 : &tm_s0, &c.full[s], wrow,
+                                    kb * NSB8);
+                    }
+                    for (int j = 0; j < ntok; ++j) {
+                        int m, kb, tt;
+                        w4_part<CL>(p, it, st, j, m, kb, tt);
+                        tma_load_2d(sp + tt * B_BYTES, bmap, &c.full[s], kb * BK, it.row0);
+                    }
+                }
+                continue;
+            }
             if constexpr (W4) {
                 const int nst = w4_stages<CL>(p, it);
                 for (int st = 0; st < nst; ++st, ++it_k) {
@@ -524,6 +579,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     break;
                 }
                 const int np = w4_parts(p, it, st);
+                if constexpr (Q8P) {
+                    // int8 row (64 values, 64-byte swizzled: 16-byte chunk c at
+                    // c ^ ((row >> 1) & 3)) -> fp16 (q * scale, one rounding)
+                    for (int j = 0; j < np; ++j) {
+                        const uint8_t *wt = smem + s * SLOT + WT_OFF8 + j * Q8_TILE + row * 64;
+                        const __half *scp = reinterpret_cast<const __half *>(smem + s * SLOT + SC_OFF8 + j * SC8_MAX);
+                        uint32_t o[32];   // column c: values 2c, 2c+1
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {   // values 16ch .. 16ch+15
+                            const uint4 v = *reinterpret_cast<const uint4 *>(wt + ((ch ^ ((row >> 1) & 3)) << 4));
+                            const __half2 sc2 = __half2half2(scp[(ch * NSB8 / 4) * 128 + row]);
+                            uint4 lo, hi;
+                            dequant16(v, sc2, lo, hi);
+                            o[8 * ch + 0] = lo.x; o[8 * ch + 1] = lo.y; o[8 * ch + 2] = lo.z; o[8 * ch + 3] = lo.w;
+                            o[8 * ch + 4] = hi.x; o[8 * ch + 5] = hi.y; o[8 * ch + 6] = hi.z; o[8 * ch + 7] = hi.w;
+                        }
+                        tmem_st16(t_lane + cb * 64 + j * 32, *reinterpret_cast<const uint32_t(*)[16]>(&o[0]));
+                        tmem_st16(t_lane + cb * 64 + j * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o[16]));
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&c.cfull[cb]);
+                    continue;
+                }
                 constexpr int tb = q4_tile_bytes(GPR), g1 = GPR - 1;   // g1: the second group's index
                 for (int j = 0; j < np; ++j) {
                     const uint8_t *wt = smem + s * SLOT + WT_OFF4 + j * tb;
@@ -863,9 +943,9 @@ combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
     }
 }
 
-template <bool W4, bool CL = false> constexpr size_t smem_bytes()
+template <int K, bool CL = false> constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)Ring<W4>::CTL + kCtlBytes + (CL ? RED_BYTES : 0);
+    return 1024 + (size_t)Ring<K>::CTL + kCtlBytes + (CL ? RED_BYTES : 0);
 }
 
 int choose_splits(int kb_total, long long units)
@@ -882,7 +962,7 @@ int choose_splits(int kb_total, long long units)
 
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt)) && d % 128 == 0 &&
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) && d % 128 == 0 &&
            F % 128 == 0 && E <= kMaxExperts && tc_gemm_available();
 }
 
@@ -933,12 +1013,14 @@ static long long cluster_chunks(int T, int E, int k)
 }
 int decode_tc_gateup_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
 {
-    if (!(w_dt == MOE_BF16 || is_q4(w_dt)) || decode_tc_gateup_fused(T, d, E, k, F, num_sms)) return 0;
+    if (!(w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) || decode_tc_gateup_fused(T, d, E, k, F, num_sms))
+        return 0;
     return cluster_size(cluster_chunks(T, E, k) * (F / dtc::BM), d / dtc::BK, num_sms);
 }
 int decode_tc_down_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
 {
-    if (!(w_dt == MOE_BF16 || is_q4(w_dt)) || k > 2 || decode_tc_down_direct(T, d, E, k, F)) return 0;
+    if (!(w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) || k > 2 || decode_tc_down_direct(T, d, E, k, F))
+        return 0;
     return cluster_size(cluster_chunks(T, E, k) * (d / dtc::BM), F / dtc::BK, num_sms);
 }
 bool decode_tc_down_into_out(int T, int d, int E, int k, int F, int w_dt, int num_sms)
@@ -946,27 +1028,72 @@ bool decode_tc_down_into_out(int T, int d, int E, int k, int F, int w_dt, int nu
     return decode_tc_down_direct(T, d, E, k, F) || decode_tc_down_cluster(T, d, E, k, F, w_dt, num_sms) > 0;
 }
 
-cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
+namespace dtc {
+
+// Dynamic shared memory of the kernels of weight storage WQ (CL: cluster mode).
+template <int WQ, bool CL> constexpr size_t smem_of()
 {
-    using namespace dtc;
+    return smem_bytes<(WQ == 3 || WQ == 4) ? 2 : (WQ ? 1 : 0), CL>();
+}
+template <int WQ> constexpr int threads_of(bool gather) { return WQ || gather ? THREADS_GATHER : THREADS; }
+
+// One launch of decode_tc_kernel<MODE, GATHER, WQ, CL>: plain, or in
+// clusters of `cluster` CTAs; the shared-memory attribute is set once per
+// device and instantiation.
+template <int MODE, bool GATHER, int WQ, bool CL>
+static cudaError_t launch_one(dim3 grid, int cluster, cudaStream_t stream, const CUtensorMap &w0,
+                              const CUtensorMap &w1, const CUtensorMap &b16, const CUtensorMap &b32,
+                              const CUtensorMap &s0, const CUtensorMap &s1, const Params &p)
+{
+    static PerDeviceFlag attr_done;
+    const int dev = current_device();
+    const size_t smem = smem_of<WQ, CL>();
+    auto kern = decode_tc_kernel<MODE, GATHER, WQ, CL>;
+    cudaError_t err;
+    if (!attr_done.done(dev)) {
+        if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return err;
+        attr_done.mark(dev);
+    }
+    const dim3 block(threads_of<WQ>(GATHER));
+    if (CL) launch_pdl_cluster(kern, grid, block, smem, stream, cluster, w0, w1, b16, b32, s0, s1, p);
+    else launch_pdl(kern, grid, block, smem, stream, w0, w1, b16, b32, s0, s1, p);
+    return cudaGetLastError();
+}
+
+template <int WQ>
+static cudaError_t launch_t(const DecodeTcArgs &a, cudaStream_t stream)
+{
+    constexpr bool conv = WQ != 0;               // converted weights (fp16 operands)
+    constexpr bool q8p = WQ == 3 || WQ == 4;     // 8-bit planes
     const int rows = a.T * a.k;
     int ks_gu, ks_d;
     decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
 
-    const bool w4 = is_q4(a.w_dt);
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    // token rows and h: fp16 on the 4-bit path
-    const CUtensorMapDataType rowt = w4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
-    const bool gather = a.x_gather != nullptr && !w4;   // token rows gathered from x in-kernel
-    CUtensorMap m_wg, m_wu, m_wd, m_x16, m_x32, m_h16, m_h32;
+    // token rows and h: fp16 when the weights are converted
+    const CUtensorMapDataType rowt = conv ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
+    const bool gather = a.x_gather != nullptr && !conv;   // token rows gathered from x in-kernel
+    CUtensorMap m_wg, m_wu, m_wd, m_x16, m_x32, m_h16, m_h32, m_sg, m_su, m_sd;
     if (!tc::make_map(&m_h16, a.h, (uint64_t)rows, a.F, 16, rowt) ||
         !tc::make_map(&m_h32, a.h, (uint64_t)rows, a.F, 32, rowt))
         return cudaErrorInvalidValue;
-    if (w4) {
+    m_sg = m_su = m_sd = m_h16;   // unused unless 8-bit planes
+    const uint64_t gu_rows = (uint64_t)a.E * a.F, d_rows = (uint64_t)a.E * a.d;
+    if (q8p) {
+        const int g8 = WQ == 4 ? 16 : 32;
+        if (!tc::make_map_u8(&m_wg, a.w_gate, gu_rows, a.d, BM, true) ||
+            !tc::make_map_u8(&m_wu, a.w_up, gu_rows, a.d, BM, true) ||
+            !tc::make_map_u8(&m_wd, a.w_down, d_rows, a.F, BM, true) ||
+            !tc::make_scale_map(&m_sg, a.w_gate, gu_rows, a.d, g8, BM) ||
+            !tc::make_scale_map(&m_su, a.w_up, gu_rows, a.d, g8, BM) ||
+            !tc::make_scale_map(&m_sd, a.w_down, d_rows, a.F, g8, BM))
+            return cudaErrorInvalidValue;
+    } else if (conv) {
         m_wg = m_wu = m_wd = m_h16;   // unused: the 4-bit tiles are contiguous copies
-    } else if (!tc::make_map(&m_wg, a.w_gate, (uint64_t)a.E * a.F, a.d, BM, bf) ||
-               !tc::make_map(&m_wu, a.w_up, (uint64_t)a.E * a.F, a.d, BM, bf) ||
-               !tc::make_map(&m_wd, a.w_down, (uint64_t)a.E * a.d, a.F, BM, bf)) {
+    } else if (!tc::make_map(&m_wg, a.w_gate, gu_rows, a.d, BM, bf) ||
+               !tc::make_map(&m_wu, a.w_up, gu_rows, a.d, BM, bf) ||
+               !tc::make_map(&m_wd, a.w_down, d_rows, a.F, BM, bf)) {
         return cudaErrorInvalidValue;
     }
     if (gather) {
@@ -978,54 +1105,17 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     }
 
     cudaError_t err;
-    const size_t smem = w4 ? smem_bytes<true>() : smem_bytes<false>();
-    static PerDeviceFlag attr_done;
-    const int dev = current_device();
-    if (!attr_done.done(dev)) {
-        const int s16 = (int)smem_bytes<false>(), s4 = (int)smem_bytes<true>();
-        const int scl = (int)smem_bytes<false, true>(), scl4 = (int)smem_bytes<true, true>();
-        if ((err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, false, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 1, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 2, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 1, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 2, true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, scl4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, true, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s16)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 1>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 1>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<GATEUP, false, 2>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(decode_tc_kernel<DOWN, false, 2>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, s4)) != cudaSuccess)
-            return err;
-        attr_done.mark(dev);
-    }
     const long long n_exp = a.E < rows ? a.E : rows;
     auto grid_for = [&](long long max_items) {
         const long long slots = (long long)a.num_sms * CTAS_PER_SM;
         long long g = max_items < slots ? max_items : slots;
-        return (int)(g < 1 ? 1 : g);
+        return dim3((unsigned)(g < 1 ? 1 : g));
     };
 
     Params p{};
     p.offsets = a.offsets; p.E = a.E; p.rows_total = rows; p.status = a.status;
     p.cl = 0;
-    p.xexp = w4 ? a.xexp : nullptr;
+    p.xexp = conv ? a.xexp : nullptr;
     p.T = a.T;
     p.w4[0] = static_cast<const uint8_t *>(a.w_gate);
     p.w4[1] = static_cast<const uint8_t *>(a.w_up);
@@ -1039,7 +1129,6 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     const int cl_gu = decode_tc_gateup_cluster(a.T, a.d, a.E, a.k, a.F, a.w_dt, a.num_sms);
     const int cl_d = decode_tc_down_cluster(a.T, a.d, a.E, a.k, a.F, a.w_dt, a.num_sms);
     const long long chunks_cl = cluster_chunks(a.T, a.E, a.k);
-    const size_t smem_cl = w4 ? smem_bytes<true, true>() : smem_bytes<false, true>();
     // grid of a cluster-mode launch: whole clusters, at most one wave
     auto grid_cl = [&](long long units, int cs) {
         const long long per = (long long)a.num_sms * CTAS_PER_SM / cs;
@@ -1055,40 +1144,24 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     } else {
         p.n_mats = 2; p.KS = ks_gu; p.P = a.pgu;
     }
-    const dim3 g_gu(grid_for(chunks * p.n_mats * p.rtiles * p.KS));
     p.expire_ns = a.expire_ns;   // (the gate/up kernel only)
-    if (cl_gu) {
-        p.xg = gather ? static_cast<const uint16_t *>(a.x_gather) : nullptr;
-        p.perm_tok = a.perm_tok;
-        if (w4 && p.gpr == 2)
-            launch_pdl_cluster(decode_tc_kernel<GATEUP, false, 2, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
-                               dim3(THREADS_W4), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
-        else if (w4)
-            launch_pdl_cluster(decode_tc_kernel<GATEUP, false, 1, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
-                               dim3(THREADS_W4), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
-        else if (gather)
-            launch_pdl_cluster(decode_tc_kernel<GATEUP, true, false, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
-                               dim3(THREADS_GATHER), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
-        else
-            launch_pdl_cluster(decode_tc_kernel<GATEUP, false, false, true>, grid_cl(chunks_cl * p.rtiles, cl_gu),
-                               dim3(THREADS), smem_cl, stream, cl_gu, m_wg, m_wu, m_x16, m_x32, p);
-    } else if (gather) {
+    if (gather) {
         p.xg = static_cast<const uint16_t *>(a.x_gather);
         p.perm_tok = a.perm_tok;
-        launch_pdl(decode_tc_kernel<GATEUP, true, false>, g_gu, dim3(THREADS_GATHER), smem, stream, m_wg,
-                   m_wu, m_x16, m_x32, p);
-    } else if (w4) {
-        if (p.gpr == 2)
-            launch_pdl(decode_tc_kernel<GATEUP, false, 2>, g_gu, dim3(THREADS_W4), smem, stream, m_wg, m_wu,
-                       m_x16, m_x32, p);
-        else
-            launch_pdl(decode_tc_kernel<GATEUP, false, 1>, g_gu, dim3(THREADS_W4), smem, stream, m_wg, m_wu,
-                       m_x16, m_x32, p);
-    } else {
-        launch_pdl(decode_tc_kernel<GATEUP, false, false>, g_gu, dim3(THREADS), smem, stream, m_wg, m_wu,
-                   m_x16, m_x32, p);
     }
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const dim3 g_gu = cl_gu ? grid_cl(chunks_cl * p.rtiles, cl_gu) : grid_for(chunks * p.n_mats * p.rtiles * p.KS);
+    err = cudaSuccess;
+    if constexpr (!conv) {   // (only bf16 weights gather token rows in-kernel)
+        if (gather && cl_gu)
+            err = launch_one<GATEUP, true, WQ, true>(g_gu, cl_gu, stream, m_wg, m_wu, m_x16, m_x32, m_sg, m_su, p);
+        else if (gather)
+            err = launch_one<GATEUP, true, WQ, false>(g_gu, 0, stream, m_wg, m_wu, m_x16, m_x32, m_sg, m_su, p);
+    }
+    if (!gather && cl_gu)
+        err = launch_one<GATEUP, false, WQ, true>(g_gu, cl_gu, stream, m_wg, m_wu, m_x16, m_x32, m_sg, m_su, p);
+    else if (!gather)
+        err = launch_one<GATEUP, false, WQ, false>(g_gu, 0, stream, m_wg, m_wu, m_x16, m_x32, m_sg, m_su, p);
+    if (err != cudaSuccess) return err;
     // split-K reductions: blocks of 32 float4 columns x min(KS, 8) split lanes
     auto reduce_block = [](int ks) { return dim3(32, ks < kSplitLanes ? (ks < 1 ? 1 : ks) : kSplitLanes); };
     auto reduce_grid = [&](long long total, int ks) {
@@ -1120,30 +1193,32 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     } else {
         p.KS = ks_d; p.P = a.pd; p.perm_tok = nullptr;
     }
-    if (cl_d && w4 && p.gpr == 2)
-        launch_pdl_cluster(decode_tc_kernel<DOWN, false, 2, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
-                           dim3(THREADS_W4), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
-    else if (cl_d && w4)
-        launch_pdl_cluster(decode_tc_kernel<DOWN, false, 1, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
-                           dim3(THREADS_W4), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
-    else if (cl_d)
-        launch_pdl_cluster(decode_tc_kernel<DOWN, false, false, true>, grid_cl(chunks_cl * p.rtiles, cl_d),
-                           dim3(THREADS), smem_cl, stream, cl_d, m_wd, m_wd, m_h16, m_h32, p);
-    else if (w4 && p.gpr == 2)
-        launch_pdl(decode_tc_kernel<DOWN, false, 2>, dim3(grid_for(chunks * p.rtiles * p.KS)),
-                   dim3(THREADS_W4), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
-    else if (w4)
-        launch_pdl(decode_tc_kernel<DOWN, false, 1>, dim3(grid_for(chunks * p.rtiles * p.KS)),
-                   dim3(THREADS_W4), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
+    if (cl_d)
+        err = launch_one<DOWN, false, WQ, true>(grid_cl(chunks_cl * p.rtiles, cl_d), cl_d, stream, m_wd, m_wd,
+                                                m_h16, m_h32, m_sd, m_sd, p);
     else
-        launch_pdl(decode_tc_kernel<DOWN, false, false>, dim3(grid_for(chunks * p.rtiles * p.KS)),
-                   dim3(THREADS), smem, stream, m_wd, m_wd, m_h16, m_h32, p);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = launch_one<DOWN, false, WQ, false>(grid_for(chunks * p.rtiles * p.KS), 0, stream, m_wd, m_wd,
+                                                 m_h16, m_h32, m_sd, m_sd, p);
+    if (err != cudaSuccess) return err;
     if (direct || cl_d) return cudaSuccess;
 
     launch_pdl(combine_kernel, dim3(reduce_grid((long long)a.T * (a.d / 4), ks_d)), reduce_block(ks_d), 0, stream,
         a.pd, ks_d, rows, a.d, a.inv, a.topk_w, p.xexp, a.T, a.k, a.out, a.status);
     return cudaGetLastError();
+}
+
+}  // namespace dtc
+
+cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
+{
+    switch (a.w_dt) {
+    case MOE_BF16: return dtc::launch_t<0>(a, stream);
+    case MOE_Q4_A64: return dtc::launch_t<1>(a, stream);
+    case MOE_Q4_K: return dtc::launch_t<2>(a, stream);
+    case MOE_Q8_0: return dtc::launch_t<3>(a, stream);
+    case MOE_Q6_K: return dtc::launch_t<4>(a, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace moe

@@ -206,27 +206,6 @@ __device__ __forceinline__ void decode_tile(const SmemCtl &c, int E, int tile, i
     mt = local - nt * m;
 }
 
-// int8 x 16 (one uint4) -> fp16 x 16 scaled by s: (q ^ 0x80) placed in the
-// mantissa of 1024.0 gives 1024 + 128 + q exactly; subtracting 1152 leaves q.
-__device__ __forceinline__ void dequant16(const uint4 q, const __half2 s, uint4 &lo, uint4 &hi)
-{
-    const uint32_t w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u,
-                           q.w ^ 0x80808080u};
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t a = __byte_perm(w[i], 0x64646464u, 0x4140);
-        uint32_t b = __byte_perm(w[i], 0x64646464u, 0x4342);
-        __half2 ha = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&a), bias), s);
-        __half2 hb = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&b), bias), s);
-        o[2 * i] = *reinterpret_cast<uint32_t *>(&ha);
-        o[2 * i + 1] = *reinterpret_cast<uint32_t *>(&hb);
-    }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
 // Bounded wait of a whole warp for a barrier phase (warp-uniform result).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
@@ -729,9 +708,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 2-D row-major [rows, cols] int8 tensor, box {64 cols, box_rows}, no swizzle
-// (the converters read it row by row).
-static bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
-                        uint32_t box_rows)
+// (the GEMM converters read it row by row) or 64-byte swizzle (the decode
+// converters: one row per lane).
+bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 bool swizzle64)
 {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -740,9 +720,28 @@ static bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The fp16 scale plane [cols/group, rows] of an 8-bit packed buffer (at
+// align256(rows * cols)), box {box_rows rows, 64/group blocks}: the scales of
+// one k-block of a weight tile.
+bool make_scale_map(CUtensorMap *m, const void *packed, uint64_t rows, uint64_t cols, int group,
+                    uint32_t box_rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const void *base = static_cast<const char *>(packed) + align_up((size_t)(rows * cols), 256);
+    cuuint64_t dims[2] = {rows, cols / (uint64_t)group};
+    cuuint64_t strides[1] = {rows * 2};
+    cuuint32_t box[2] = {box_rows, (cuuint32_t)(64 / group)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D row-major [rows, cols] 16-bit tensor, box {64 cols, box_rows}, 128B swizzle.
@@ -925,16 +924,7 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     // 8-bit packed buffers: int8 plane, then the fp16 scale plane [cols/g8, rows]
     // at align256(rows * cols); maps with box {128 rows, 64/g8 blocks}
     auto scale_map = [g8](CUtensorMap *m, const void *packed, uint64_t r, uint64_t cols) {
-        auto enc = encode_fn();
-        if (!enc) return false;
-        const void *base = static_cast<const char *>(packed) + align_up((size_t)(r * cols), 256);
-        cuuint64_t dims[2] = {r, cols / (uint64_t)g8};
-        cuuint64_t strides[1] = {r * 2};
-        cuuint32_t box[2] = {(cuuint32_t)(BN / 2), (cuuint32_t)(64 / g8)};
-        cuuint32_t estr[2] = {1, 1};
-        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        return make_scale_map(m, packed, r, cols, g8, (uint32_t)(BN / 2));
     };
     CUtensorMap m_sg = m_xp, m_su = m_xp, m_sd = m_xp;   // unused unless Q8_0
     if (q8 && !(scale_map(&m_sg, a.w_gate, gu_rows, a.d) && scale_map(&m_su, a.w_up, gu_rows, a.d) &&

@@ -37,6 +37,15 @@ namespace tc {
 // 128-byte swizzle (the K-major operand tiles of the tcgen05 kernels).
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
               CUtensorMapDataType dt);
+// 2-D row-major [rows, cols] int8 tensor map, box {64 cols, box_rows}, no
+// swizzle or (swizzle64) the 64-byte swizzle: 16-byte chunk c of row r at
+// c ^ ((r >> 1) & 3).
+bool make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 bool swizzle64 = false);
+// The fp16 scale plane [cols/group, rows] of an 8-bit packed buffer (Q8_0:
+// group 32, Q6_K: 16), box {box_rows rows, 64/group blocks}.
+bool make_scale_map(CUtensorMap *m, const void *packed, uint64_t rows, uint64_t cols, int group,
+                    uint32_t box_rows);
 }  // namespace tc
 
 // True when the tensor-core expert kernels are compiled into this library.

@@ -117,6 +117,12 @@ WORKLOADS = {
         description="ZONOS2-shaped decode step with Q4_K experts (the K-quant the "
                     "pages recommend for the expert stacks): d=2048, E=16, top-1, "
                     "F=2816, T in {1, 8, 64}, 28-layer weight rotation"),
+    "zonos2_decode_q8": Workload(
+        "zonos2_decode_q8", T=8, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=Q8_0, bias="normal", bias_sd=0.1, layers=28,
+        description="ZONOS2-shaped decode step with Q8_0 experts (the port's "
+                    "effectively lossless default): d=2048, E=16, top-1, F=2816, "
+                    "T in {1, 8, 64}, 28-layer weight rotation"),
     "zonos2_decode_q6k": Workload(
         "zonos2_decode_q6k", T=8, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
         w_dtype=Q6_K, bias="normal", bias_sd=0.1, layers=28,

@@ -65,11 +65,11 @@ typedef enum {
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3, MOE_Q4_K = 4, MOE_Q6_K = 5 } moe_dtype;
 
 /* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
- * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16 or
- *   affine 4-bit weights (4-bit tiles converted to fp16 in shared memory) with
- *   d % 128 == 0, F % 128 == 0 and T*k <= 8192, otherwise the CUDA-core
- *   kernels.  PREFILL: tcgen05 grouped GEMMs.  DECODE_SIMT: always the
- *   CUDA-core decode kernels (the decode path for fp32 and Q8_0). */
+ * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16,
+ *   4-bit (affine, Q4_K) and 8-bit-plane (Q8_0, Q6_K) weights (converted to
+ *   fp16 on chip) with d % 128 == 0, F % 128 == 0 and T*k <= 8192, otherwise
+ *   the CUDA-core kernels.  PREFILL: tcgen05 grouped GEMMs.  DECODE_SIMT:
+ *   always the CUDA-core decode kernels (the decode path for fp32). */
 typedef enum {
     MOE_PATH_AUTO = 0,
     MOE_PATH_DECODE = 1,
@@ -165,8 +165,9 @@ MOE_API moe_status moe_permute(const int32_t *topk_idx, int T, int k, int E, int
  * factor; both are undone exactly in the epilogues, so any finite bf16
  * activations are taken.  An h that still leaves fp16's range (|h| > 65504
  * after the scaling: expert weights with dot products above ~256 against a
- * unit row) makes moe_check report MOE_ERR_DEVICE_CHECK.  The CUDA-core Q8_0
- * decode kernels compute in fp32.
+ * unit row) makes moe_check report MOE_ERR_DEVICE_CHECK.  The tensor-core
+ * decode kernels (MOE_PATH_DECODE, d and F multiples of 128) take Q8_0 the
+ * same way; the CUDA-core Q8_0 decode kernels compute in fp32.
  */
 MOE_API size_t moe_q8_0_packed_size(long long rows, int cols);
 MOE_API moe_status moe_pack_q8_0(const void *blocks, long long rows, int cols, void *packed,
@@ -255,9 +256,9 @@ MOE_API moe_status moe_pack_q4_k(const void *blocks, long long rows, int cols, v
  *   bytes [0, rows*cols)                              int8 plane [rows, cols], q - 32
  *   bytes [align256(rows*cols), ... + rows*cols/8)    fp16 scale plane [cols/16, rows]
  *   (the scale of group j of row r, fp16(d * scales[j]), at index j*rows + r)
- * and takes them where Q8_0 goes: the grouped GEMMs (fp16 operands, the same
- * range rules) and the CUDA-core decode kernels (fp32), with d and F
- * multiples of 256.  moe_q6_k_packed_size returns the buffer size (0 if
+ * and takes them where Q8_0 goes: the grouped GEMMs and the tensor-core
+ * decode kernels (fp16 operands, the same range rules) and the CUDA-core
+ * decode kernels (fp32), with d and F multiples of 256.  moe_q6_k_packed_size returns the buffer size (0 if
  * cols % 256 != 0 or rows < 0); moe_pack_q6_k repacks `blocks` (device, any
  * alignment) into `packed` (device, 256-byte aligned) on `stream`.
  */

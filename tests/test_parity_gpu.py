@@ -251,7 +251,9 @@ FULL_CASES = [("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode
               ("zonos2_prefill_q8", None), ("zonos2_decode_q4", 1), ("zonos2_decode_q4", 8),
               ("zonos2_decode_q4", 64), ("zonos2_prefill_q4", None), ("zonos2_decode_q4k", 1),
               ("zonos2_decode_q4k", 8), ("zonos2_decode_q4k", 64), ("zonos2_prefill_q4k", None),
-              ("zonos2_decode_q6k", 1), ("zonos2_decode_q6k", 8), ("zonos2_prefill_q6k", None)]
+              ("zonos2_decode_q6k", 1), ("zonos2_decode_q6k", 8), ("zonos2_decode_q6k", 64),
+              ("zonos2_prefill_q6k", None), ("zonos2_decode_q8", 1), ("zonos2_decode_q8", 8),
+              ("zonos2_decode_q8", 64)]
 
 
 @pytest.mark.parametrize("seed", [2, 7, 13])
@@ -263,8 +265,8 @@ def test_forward_workloads_full(name, T, seed):
     the 1e-3 margin, near ties resolved validly, weights within 2e-6, counts,
     offsets, permutation and inverse bit-exact -- and every output row within
     the tolerance."""
-    if ("_q4" in name or "_q6" in name) and seed == 13:
-        pytest.skip("the 4-bit and 6-bit workloads run with two seeds")
+    if ("_q4" in name or "_q6" in name or "decode_q8" in name) and seed == 13:
+        pytest.skip("the 4-, 6- and 8-bit decode workloads run with two seeds")
     layer = wl.make_layer(wl.WORKLOADS[name], seed=seed, T=T)
     out, r = gpu_forward_views(layer, DEV, path=0)
     check_routing_views(r, layer)
@@ -543,6 +545,7 @@ def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
     (DECODE, 300, wl.Q4_A64, 8, 256),     # rows grouped by the scatter kernel
     (PREFILL, 600, wl.Q4_A64, 8, 256),    # 4-bit grouped GEMMs
     (DECODE, 40, wl.Q4_K, 8, 256), (PREFILL, 600, wl.Q4_K, 8, 256),
+    (DECODE, 40, wl.Q8_0, 8, 256), (DECODE, 128, wl.Q6_K, 64, 512),   # 8-bit planes, decode
     (PREFILL, 600, wl.Q6_K, 8, 256)])   # Q6_K grouped GEMMs: scales per 16 values
 def test_fp16_operands_large_activations(path, T, wdt, E, F):
     """The Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels
@@ -583,7 +586,8 @@ def test_fp16_operands_large_activations(path, T, wdt, E, F):
     (wl.Q4_A64, PREFILL, 256, 4, 1, 128),    # 4-bit grouped GEMMs
     (wl.Q4_K, DECODE, 256, 4, 1, 256),
     (wl.Q4_K, PREFILL, 256, 4, 1, 256),
-    (wl.Q6_K, PREFILL, 256, 4, 1, 256)])
+    (wl.Q6_K, PREFILL, 256, 4, 1, 256),
+    (wl.Q8_0, DECODE, 256, 4, 1, 256), (wl.Q6_K, DECODE, 128, 64, 2, 512)])
 def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     """Expert weights large enough that h leaves fp16's range even for
     normalised rows: the call reports MOE_ERR_DEVICE_CHECK instead of
@@ -617,12 +621,13 @@ def ctypes_check(pkg, ws):
                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("wdt,F", [(wl.Q4_A64, 384), (wl.Q4_K, 512)])
+@pytest.mark.parametrize("wdt,F", [(wl.Q4_A64, 384), (wl.Q4_K, 512), (wl.Q8_0, 384), (wl.Q6_K, 512)])
 @pytest.mark.parametrize("T,k", [(1, 1), (8, 1), (64, 1), (40, 2), (200, 4)])
 def test_q4_tensor_core_decode_reproducible_and_close_to_cuda_core(T, k, wdt, F):
-    """Affine 4-bit and Q4_K experts on the tensor-core decode kernels: bitwise
-    reproducible, token-permutation equivariant, within tolerance of the oracle
-    and of the CUDA-core 4-bit kernels."""
+    """Affine 4-bit, Q4_K, Q8_0 and Q6_K experts on the tensor-core decode
+    kernels (converter warps write the fp16 weights into tensor memory):
+    bitwise reproducible, token-permutation equivariant, within tolerance of
+    the oracle and of the CUDA-core kernels."""
     layer = wl.make_custom_layer(29, T=T, d=512, E=16, k=k, F=F, act_dtype=wl.BF16,
                                  w_dtype=wdt, bias_sd=0.5)
     t = upload_layer(layer, DEV)
