@@ -440,7 +440,7 @@ def run_reference(args, w, T, layers):
 def config_dict(w, T, layers, args):
     return {"workload": w.name, "T": T, "d": w.d, "E": w.E, "k": w.k, "F": w.F,
             "layers": layers, "act_dtype": "bf16" if w.act_dtype else "f32",
-            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_a64", 4: "q4_k"}[w.w_dtype],
+            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_a64", 4: "q4_k", 5: "q6_k"}[w.w_dtype],
             "bias": w.bias, "global_batch": T * max(1, args.gpus), "parallelism": "replicas",
             "l2": "inputs larger than L2: every step reads all layers' expert weights",
             "graph": not args.no_graph, "scoring": args.scoring,
