@@ -30,8 +30,10 @@ from typing import Optional
 
 import numpy as np
 
-F32, BF16, Q8_0, Q4_A64, Q4_K, Q6_K = 0, 1, 2, 3, 4, 5
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64", Q4_K: "q4_k", Q6_K: "q6_k"}
+F32, BF16, Q8_0, Q4_A64, Q4_K, Q6_K, FP8 = 0, 1, 2, 3, 4, 5, 6
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", Q8_0: "q8_0", Q4_A64: "q4_a64", Q4_K: "q4_k", Q6_K: "q6_k",
+               FP8: "fp8_e4m3"}
+FP8_MAX = 448.0          # largest finite E4M3 value
 Q4_K_BLOCK = 256
 Q4_K_BLOCK_BYTES = 144
 Q6_K_BLOCK = 256
@@ -129,6 +131,18 @@ WORKLOADS = {
         description="ZONOS2-shaped decode step with Q6_K experts (the K-quant ladder's "
                     "sweet spot): d=2048, E=16, top-1, F=2816, T in {1, 8, 64}, "
                     "28-layer weight rotation"),
+    "zonos2_decode_fp8": Workload(
+        "zonos2_decode_fp8", T=8, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=FP8, bias="normal", bias_sd=0.1, layers=28,
+        description="ZONOS2-shaped decode step with fp8 (E4M3, one scale per row) "
+                    "experts (the serving configs' fp8): d=2048, E=16, top-1, "
+                    "F=2816, T in {1, 8, 64}, 28-layer weight rotation"),
+    "zonos2_prefill_fp8": Workload(
+        "zonos2_prefill_fp8", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
+        w_dtype=FP8, bias="normal", bias_sd=0.1, layers=4,
+        description="ZONOS2-shaped prefill with fp8 (E4M3, one scale per row) "
+                    "experts: T=4096, d=2048, E=16, top-1, F=2816, bf16 "
+                    "activations and router (4 independent layers per benchmark step)"),
     "zonos2_prefill_q6k": Workload(
         "zonos2_prefill_q6k", T=4096, d=2048, E=16, k=1, F=2816, act_dtype=BF16,
         w_dtype=Q6_K, bias="normal", bias_sd=0.1, layers=4,
@@ -329,6 +343,32 @@ def q6_k_quantize(w) -> np.ndarray:
     return q6_k_pack(q.reshape(q.shape[:-2] + (256,)).astype(np.uint8), sc.astype(np.int8), d16)
 
 
+def fp8_quantize(w) -> np.ndarray:
+    """Encode w[..., K] as fp8 rows: uint8 [..., 4 + K] = {fp32 scale (little
+    endian), E4M3 codes[K]}; value = scale * E4M3(code).  This encoder: scale =
+    max|w| / 448 of the row in fp32 (1 for an all-zero row), codes = w / scale
+    (fp32, clamped to +-448) rounded to nearest-even E4M3 (torch's float8_e4m3fn
+    cast)."""
+    import torch
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float32))
+    t = torch.from_numpy(w)
+    return fp8_quantize_torch(t).numpy()
+
+
+def fp8_quantize_torch(w):
+    """fp8 rows of a float32 tensor [..., K] (fp8_quantize), on w's device."""
+    import torch
+    w = w.float()
+    K = w.shape[-1]
+    s = w.abs().amax(-1, keepdim=True) / FP8_MAX
+    s = torch.where(s > 0, s, torch.ones_like(s))
+    q = torch.clamp(w / s, -FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    out = torch.empty(*w.shape[:-1], 4 + K, dtype=torch.uint8, device=w.device)
+    out[..., 0:4] = s.contiguous().view(torch.uint8).reshape(*w.shape[:-1], 4)
+    out[..., 4:] = q
+    return out
+
+
 def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == F32:
         return np.ascontiguousarray(a, dtype=np.float32)
@@ -342,6 +382,8 @@ def _encode(a: np.ndarray, dtype: int) -> np.ndarray:
         return q4_k_quantize(a)
     if dtype == Q6_K:
         return q6_k_quantize(a)
+    if dtype == FP8:
+        return fp8_quantize(a)
     raise ValueError(dtype)
 
 
@@ -423,6 +465,8 @@ def weight_bytes_per_expert(d: int, F: int, w_dtype: int) -> int:
         return n // Q4_K_BLOCK * Q4_K_BLOCK_BYTES
     if w_dtype == Q6_K:
         return n // Q6_K_BLOCK * Q6_K_BLOCK_BYTES
+    if w_dtype == FP8:   # one byte per weight and an fp32 scale per row (2F + d rows)
+        return n + 4 * (2 * F + d)
     return n // Q8_0_BLOCK * Q8_0_BLOCK_BYTES
 
 
@@ -544,8 +588,9 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
     """
     import torch
     if (w.act_dtype, w.w_dtype) not in ((BF16, BF16), (BF16, Q8_0), (BF16, Q4_A64), (BF16, Q4_K),
-                                        (BF16, Q6_K), (F32, F32)):
-        raise ValueError("device stacks: bf16/bf16, bf16 with Q8_0, Q4_A64, Q4_K or Q6_K experts, or fp32/fp32")
+                                        (BF16, Q6_K), (BF16, FP8), (F32, F32)):
+        raise ValueError("device stacks: bf16/bf16, bf16 with Q8_0, Q4_A64, Q4_K, Q6_K or fp8 "
+                         "experts, or fp32/fp32")
     act = torch.float32 if w.act_dtype == F32 else torch.bfloat16
     T = w.T if T is None else T
     g = torch.Generator(device=device)
@@ -557,7 +602,8 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * sd
             if q8:
                 return {Q4_A64: q4_a64_quantize_torch, Q4_K: q4_k_quantize_torch,
-                        Q6_K: q6_k_quantize_torch, Q8_0: q8_0_quantize_torch}[w.w_dtype](t)
+                        Q6_K: q6_k_quantize_torch, Q8_0: q8_0_quantize_torch,
+                        FP8: fp8_quantize_torch}[w.w_dtype](t)
             return t.to(act)
         d, E, F = w.d, w.E, w.F
         x = rn(T, d)
@@ -572,7 +618,7 @@ def make_device_stack(w: Workload, seed: int, layers: int, T: Optional[int] = No
             b = torch.from_numpy(zipf_bias(E, rng)).to(device)
         else:
             b = torch.randn(E, generator=g, device=device, dtype=torch.float32) * w.bias_sd
-        q8 = w.w_dtype in (Q8_0, Q4_A64, Q4_K, Q6_K)   # block-quantised expert weights
+        q8 = w.w_dtype in (Q8_0, Q4_A64, Q4_K, Q6_K, FP8)   # quantised expert weights
         wg = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wu = rn(E, F, d, sd=1.0 / math.sqrt(d), q8=q8)
         wd = rn(E, d, F, sd=1.0 / math.sqrt(F), q8=q8)

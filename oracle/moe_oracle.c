@@ -59,6 +59,23 @@ static double f16_bits_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* OCP 8-bit floating point, E4M3 -> double, written from the format's
+ * definition: sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+ * field 0 is subnormal (0.m * 2^-6), exponent 15 with mantissa 7 is NaN, and
+ * there are no infinities (largest finite 1.75 * 2^8 = 448). */
+static double e4m3_to_double(uint8_t b)
+{
+    const int sign = b >> 7, expo = (b >> 3) & 15, mant = b & 7;
+    double v;
+    if (expo == 15 && mant == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)mant, -9);                  /* (m / 8) * 2^-6 */
+    else
+        v = ldexp((double)(8 + mant), expo - 10);     /* (1 + m / 8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
 /* Decode row `row` of a [rows, cols] matrix stored as `dt` into out[cols]. */
 static void decode_row(const void *base, int dt, size_t row, int cols, double *out)
 {
@@ -136,6 +153,16 @@ static void decode_row(const void *base, int dt, size_t row, int cols, double *o
                 out[b * 256 + v] = d * (double)sc[v / 16] * (double)(q - 32);
             }
         }
+    } else if (dt == ORACLE_FP8) {
+        /* fp8 experts ("zonos2" sglang-omni cookbook, §Benchmark Results: the
+         * served configurations run "fp8"; the pages fix neither the 8-bit
+         * variant nor the scaling, so this is a reading): E4M3 codes with one
+         * fp32 scale per row (output channel), stored per row as {fp32 scale,
+         * codes[cols]}; value = scale * E4M3(code). */
+        const uint8_t *p = (const uint8_t *)base + row * (size_t)(cols + 4);
+        float scale;
+        memcpy(&scale, p, sizeof scale);
+        for (int c = 0; c < cols; ++c) out[c] = (double)scale * e4m3_to_double(p[4 + c]);
     } else { /* ORACLE_Q4_A64 ("Zyphra-ZONOS2-4bit", §How this was quantized:
               * experts at 4 bits, groups of 64, affine; the byte layout is this
               * library's): per row cols/64 blocks of {fp16 scale, fp16 bias,
@@ -158,7 +185,7 @@ static int valid_act(int dt) { return dt == ORACLE_F32 || dt == ORACLE_BF16; }
 static int valid_w(int dt)
 {
     return dt == ORACLE_F32 || dt == ORACLE_BF16 || dt == ORACLE_Q8_0 || dt == ORACLE_Q4_A64 ||
-           dt == ORACLE_Q4_K || dt == ORACLE_Q6_K;
+           dt == ORACLE_Q4_K || dt == ORACLE_Q6_K || dt == ORACLE_FP8;
 }
 
 /* ------------------------------------------------------------ thread helper */

@@ -8,7 +8,8 @@
  * 4-bit rows of 36-byte blocks of 64 values {fp16 scale, fp16 bias, 32 bytes:
  * value 2j in the low nibble of byte j, 2j+1 in the high}, value = scale*q + bias,
  * 4 = Q4_K rows of 144-byte super-blocks of 256 values, 5 = Q6_K rows of 210-byte
- * super-blocks of 256 values (GGUF layouts; see moe_oracle.c).
+ * super-blocks of 256 values (GGUF layouts; see moe_oracle.c), 6 = fp8 rows
+ * {fp32 scale, E4M3 codes[cols]} (4 + cols bytes), value = scale * E4M3(code).
  * Activations (x, W_r) are fp32 or bf16; expert weights may also be Q8_0.
  * Layouts (row-major): x[T,d], W_r[E,d], W_g[E,F,d], W_u[E,F,d], W_d[E,d,F].
  * All functions return 0 on success, -1 on invalid arguments.
@@ -23,7 +24,8 @@
 extern "C" {
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3, ORACLE_Q4_K = 4, ORACLE_Q6_K = 5 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_Q8_0 = 2, ORACLE_Q4_A64 = 3, ORACLE_Q4_K = 4, ORACLE_Q6_K = 5,
+       ORACLE_FP8 = 6 };
 
 int oracle_default_threads(void);
 

@@ -41,6 +41,12 @@ def decode(a, dtype):
     if dtype == wl.BF16:
         return wl.bf16_bits_to_f32(a).astype(np.float64)
     blocks = np.asarray(a, np.uint8)
+    if dtype == wl.FP8:
+        # rows {fp32 scale, E4M3 codes}: the codes through torch's float8_e4m3fn
+        import torch
+        scale = blocks[..., 0:4].copy().view(np.float32)[..., 0].astype(np.float64)
+        codes = torch.from_numpy(np.ascontiguousarray(blocks[..., 4:])).view(torch.float8_e4m3fn)
+        return scale[..., None] * codes.float().numpy().astype(np.float64)
     if dtype == wl.Q6_K:
         # 256 values per 210 bytes: ql[128] low 4 bits, qh[64] top 2 bits,
         # int8 scales[16] (one per 16 values), fp16 d; code q, value d*sc*(q-32).
@@ -256,7 +262,8 @@ def test_k_equals_e_is_dense_softmax_gating():
 
 
 @pytest.mark.parametrize("act,wdt", [(wl.F32, wl.F32), (wl.BF16, wl.BF16), (wl.BF16, wl.Q8_0),
-                                     (wl.BF16, wl.Q4_A64), (wl.BF16, wl.Q4_K), (wl.BF16, wl.Q6_K)])
+                                     (wl.BF16, wl.Q4_A64), (wl.BF16, wl.Q4_K), (wl.BF16, wl.Q6_K),
+                                     (wl.BF16, wl.FP8)])
 @pytest.mark.parametrize("k", [1, 2, 3])
 def test_matches_dense_brute_force(act, wdt, k):
     d, F = (256, 256) if wdt in (wl.Q4_K, wl.Q6_K) else (64, 96) if wdt != wl.Q4_A64 else (64, 128)
@@ -674,3 +681,62 @@ def test_q6_k_encoder_error_within_half_a_step():
     bound = (0.5 * d[..., None] * np.abs(sc) + 16 * d[..., None]).repeat(16, axis=-1).reshape(8, 512)
     assert np.all(np.abs(deq - w) <= bound)
     assert np.sqrt(np.mean((deq - w) ** 2)) < 0.03 * np.sqrt(np.mean(w ** 2))
+
+
+# ------------------------------------------- fp8 (E4M3) experts (next row f3)
+# code -> value, written from the E4M3 definition (sign, 4 exponent bits with
+# bias 7, 3 mantissa bits, exponent field 0 subnormal, no infinities)
+E4M3_WORKED = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x0F: 1.875 * 2.0 ** -6,
+               0x30: 0.5, 0x38: 1.0, 0x3C: 1.5, 0x3F: 1.875, 0x40: 2.0, 0x57: 15.0, 0x7E: 448.0,
+               0x80: -0.0, 0x81: -(2.0 ** -9), 0xB8: -1.0, 0xC4: -3.0, 0xFE: -448.0}
+
+
+def test_fp8_e4m3_worked_codes_and_library_decode():
+    """Hand-derived E4M3 values agree with torch's float8_e4m3fn (the tests'
+    decoder), which then decodes every finite code."""
+    import torch
+    codes = np.array(sorted(E4M3_WORKED), np.uint8)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    assert lib.tolist() == [E4M3_WORKED[c] for c in codes.tolist()]
+    allc = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    assert np.isnan(allc[[0x7F, 0xFF]]).all() and np.isfinite(np.delete(allc, [0x7F, 0xFF])).all()
+    assert np.abs(allc[np.isfinite(allc)]).max() == 448.0
+
+
+def test_fp8_every_code_through_a_layer():
+    """One expert whose W_g rows hold every finite E4M3 code (NaN codes
+    replaced by zero) under scales of both signs' magnitudes: the oracle's
+    layer output against a numpy forward on the torch-decoded weights."""
+    T, d, F = 4, 256, 64
+    layer = tiny_layer(seed=97, act=wl.F32, wdt=wl.FP8, T=T, d=d, E=1, k=1, F=F)
+    rows = np.zeros((1, F, 4 + d), np.uint8)
+    codes = np.arange(256, dtype=np.uint8)
+    codes[[0x7F, 0xFF]] = 0
+    for f in range(F):
+        rows[0, f, 4:] = np.roll(codes, 5 * f)
+        rows[0, f, 0:4] = np.array([2.0 ** -(f % 7) * (1 + f / 64.0)], np.float32).view(np.uint8)
+    layer.w_gate = rows
+    x = decode(layer.x, wl.F32)
+    g = x @ decode(layer.w_gate, wl.FP8)[0].T
+    u = x @ decode(layer.w_up, wl.FP8)[0].T
+    ref = (g / (1.0 + np.exp(-g)) * u) @ decode(layer.w_down, wl.FP8)[0].T
+    out, _, _, _ = oracle.moe_forward(layer)
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_fp8_encoder_error_within_half_a_step():
+    rng = np.random.default_rng(98)
+    w = (rng.standard_normal((8, 512)) * 0.05).astype(np.float32)
+    w[3] = 0.0
+    b = wl.fp8_quantize(w)
+    deq = decode(b, wl.FP8)
+    s = b[..., 0:4].copy().view(np.float32)[..., 0].astype(np.float64)
+    assert s[3] == 1.0 and np.all(deq[3] == 0.0)
+    v = np.abs(w / s[:, None].astype(np.float32)).astype(np.float64)
+    # half the E4M3 spacing at |v|: 2^(floor(log2 v) - 4) for normals, 2^-10 below 2^-6
+    half = np.where(v >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(v, 2.0 ** -6))) - 4), 2.0 ** -10)
+    assert np.all(np.abs(deq - w) <= half * s[:, None] * (1 + 1e-6))
+    # each nonzero row's largest magnitude lands on 448 (to within the scale's rounding)
+    for r in range(8):
+        if r != 3:
+            assert abs(np.abs(deq[r]).max() / s[r] - 448.0) <= 448.0 * 2.0 ** -4

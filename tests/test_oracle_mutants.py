@@ -106,6 +106,14 @@ MUTANTS = {
     "q6k_nibble_halves_swapped": ("const int lo = g < 2 ? (lo_byte & 15) : (lo_byte >> 4);",
                                   "const int lo = g < 2 ? (lo_byte >> 4) : (lo_byte & 15);", 0),
     "q6k_ql_run_offset": ("ql[64 * h + l + 32 * (g % 2)]", "ql[64 * h + l + 32 * (g / 2)]", 0),
+    # fp8 (E4M3) rows ("zonos2" sglang-omni cookbook, §Benchmark Results: fp8 serving)
+    "fp8_exponent_bias_8": ("v = ldexp((double)(8 + mant), expo - 10);",
+                            "v = ldexp((double)(8 + mant), expo - 11);", 0),
+    "fp8_subnormal_as_normal": ("v = ldexp((double)mant, -9);", "v = ldexp((double)(8 + mant), -10);", 0),
+    "fp8_sign_dropped": ("    return sign ? -v : v;\n}\n\n/* Decode row", "    return v;\n}\n\n/* Decode row", 0),
+    "fp8_scale_ignored": ("out[c] = (double)scale * e4m3_to_double(p[4 + c]);",
+                          "out[c] = e4m3_to_double(p[4 + c]);", 0),
+    "fp8_two_mantissa_bits": ("mant = b & 7;", "mant = b & 3;", 0),
     # bf16 storage
     "bf16_low_half": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;", 0),
 }
