@@ -217,16 +217,16 @@ def expert_kernel_names(w, T, num_sms):
     timed as one stage."""
     rows = T * w.k
     act16 = w.act_dtype == 1
-    if (act16 and w.w_dtype in (1, 2, 3, 4, 5) and w.d % 256 == 0 and w.F % 128 == 0
+    if (act16 and w.w_dtype in (1, 2, 3, 4, 5, 6) and w.d % 256 == 0 and w.F % 128 == 0
             and rows >= 64 * w.E and T >= 512):
         q = {1: "bf16", 2: "Q8_0, CTA pairs", 3: "4-bit, CTA pairs", 4: "Q4_K, CTA pairs",
-             5: "Q6_K, CTA pairs"}[w.w_dtype]
+             5: "Q6_K, CTA pairs", 6: "fp8, CTA pairs"}[w.w_dtype]
         return {"file": "tc_gemm.cu", "gateup": f"grouped_gemm_kernel<GATEUP, {q}>",
                 "down": f"grouped_gemm_kernel<DOWN, {q}>", "launches": 4, "fused": False}
-    if act16 and w.w_dtype in (1, 2, 3, 4, 5) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
+    if act16 and w.w_dtype in (1, 2, 3, 4, 5, 6) and w.d % 128 == 0 and w.F % 128 == 0 and rows <= 8192:
         n_exp = min(w.E, rows)
         small = T <= 128 and w.d // 64 <= 64 and w.k <= w.E
-        q4 = w.w_dtype in (2, 3, 4, 5)   # converted weights (4- or 8-bit): fp16 token rows
+        q4 = w.w_dtype in (2, 3, 4, 5, 6)   # converted weights (4- or 8-bit): fp16 token rows
         if (not q4 and w.k <= 2 and n_exp * (w.F // 128) * 2 >= 2 * num_sms
                 and 2 * 128 * w.d * 2 <= 512 << 10):
             name = "decode_fused_kernel (gate/up + SwiGLU + down + combine, one launch)"
@@ -249,7 +249,7 @@ def expert_kernel_names(w, T, num_sms):
         # tokens, else from a gather kernel
         launches = (1 if small else 2) + (1 if q4 and small and T > 16 else 0) + \
             (1 if fused or cl_gu else 2) + (1 if direct or cl_d else 2)
-        tag = {2: ", Q8_0", 3: ", 4-bit", 4: ", Q4_K", 5: ", Q6_K"}.get(w.w_dtype, "")
+        tag = {2: ", Q8_0", 3: ", 4-bit", 4: ", Q4_K", 5: ", Q6_K", 6: ", fp8"}.get(w.w_dtype, "")
         gu = f"decode_tc_kernel<GATEUP{tag}> (whole K, writes h)" if fused else \
             f"decode_tc_kernel<GATEUP{tag}> (clusters of {cl_gu}, writes h)" if cl_gu else \
             f"decode_tc_kernel<GATEUP{tag}> + swiglu_reduce_kernel"
@@ -357,7 +357,7 @@ def host_layer_from_device(w, dl, T):
         if t.dtype == torch.float32:
             return t.contiguous().cpu().numpy()
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    if w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K):   # the oracle reads the blocks themselves
+    if w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K, wl.FP8):   # the oracle reads the blocks themselves
         wts = {n: dl["blocks"][n].cpu().numpy() for n in ("w_gate", "w_up", "w_down")}
     else:
         wts = {n: bits(dl[n]) for n in ("w_gate", "w_up", "w_down")}
@@ -440,7 +440,7 @@ def run_reference(args, w, T, layers):
 def config_dict(w, T, layers, args):
     return {"workload": w.name, "T": T, "d": w.d, "E": w.E, "k": w.k, "F": w.F,
             "layers": layers, "act_dtype": "bf16" if w.act_dtype else "f32",
-            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_a64", 4: "q4_k", 5: "q6_k"}[w.w_dtype],
+            "w_dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_a64", 4: "q4_k", 5: "q6_k", 6: "fp8_e4m3"}[w.w_dtype],
             "bias": w.bias, "global_batch": T * max(1, args.gpus), "parallelism": "replicas",
             "l2": "inputs larger than L2: every step reads all layers' expert weights",
             "graph": not args.no_graph, "scoring": args.scoring,
@@ -461,7 +461,7 @@ def compute_peak(w, peaks, dev_props, kernels=None):
     maximum SM clock ("alu")."""
     from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
     simt = kernels is None or kernels["file"] == "decode.cu"
-    if w.w_dtype == wl.F32 or (w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K) and simt):
+    if w.w_dtype == wl.F32 or (w.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K, wl.FP8) and simt):
         mhz = float(peaks.get("sm_max_mhz") or 0) or dev_props.clock_rate / 1e3
         return dev_props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12, "alu", \
             "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock"
@@ -514,10 +514,12 @@ def setup_stack(pkg, wl, w, T, layers, seed, dev):
                                  zipf_biases=fit[0] if fit else None)
     act_dt = pkg.MOE_F32 if w.act_dtype == wl.F32 else pkg.MOE_BF16
     w_dt = {wl.F32: pkg.MOE_F32, wl.BF16: pkg.MOE_BF16, wl.Q8_0: pkg.MOE_Q8_0,
-            wl.Q4_A64: pkg.MOE_Q4_A64, wl.Q4_K: pkg.MOE_Q4_K, wl.Q6_K: pkg.MOE_Q6_K}[w.w_dtype]
-    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64, pkg.MOE_Q4_K, pkg.MOE_Q6_K):
+            wl.Q4_A64: pkg.MOE_Q4_A64, wl.Q4_K: pkg.MOE_Q4_K, wl.Q6_K: pkg.MOE_Q6_K,
+            wl.FP8: pkg.MOE_FP8}[w.w_dtype]
+    if w_dt in (pkg.MOE_Q8_0, pkg.MOE_Q4_A64, pkg.MOE_Q4_K, pkg.MOE_Q6_K, pkg.MOE_FP8):
         pack = {pkg.MOE_Q8_0: pkg.moe_pack_q8_0, pkg.MOE_Q4_A64: pkg.moe_pack_q4_a64,
-                pkg.MOE_Q4_K: pkg.moe_pack_q4_k, pkg.MOE_Q6_K: pkg.moe_pack_q6_k}[w_dt]
+                pkg.MOE_Q4_K: pkg.moe_pack_q4_k, pkg.MOE_Q6_K: pkg.moe_pack_q6_k,
+                pkg.MOE_FP8: pkg.moe_pack_fp8}[w_dt]
         for L in stack:
             L["blocks"] = {n: L[n] for n in ("w_gate", "w_up", "w_down")}
             for n, rows, cols in (("w_gate", w.E * w.F, w.d), ("w_up", w.E * w.F, w.d),
@@ -699,7 +701,9 @@ SIDE_WORKLOADS = [("tiny_fp32", None, None, 8), ("zonos2_decode", 1, None, 1),
                   ("zonos2_decode_q8", 1, None, 1), ("zonos2_decode_q8", 8, None, 8),
                   ("zonos2_decode_q8", 64, None, 64),
                   ("zonos2_decode_q6k", 1, None, 1), ("zonos2_decode_q6k", 8, None, 8),
-                  ("zonos2_decode_q6k", 64, None, 64), ("zonos2_prefill_q6k", None, None, 192)]
+                  ("zonos2_decode_q6k", 64, None, 64), ("zonos2_prefill_q6k", None, None, 192),
+                  ("zonos2_decode_fp8", 1, None, 1), ("zonos2_decode_fp8", 8, None, 8),
+                  ("zonos2_decode_fp8", 64, None, 64), ("zonos2_prefill_fp8", None, None, 192)]
 
 
 def measure_side_workload(pkg, wl, name, T, layers, sample_rows, dev, peaks, peak_src,
@@ -1001,7 +1005,9 @@ def main():
                   wl.Q6_K: ("q6_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
                             else "q6_k weights, f16 tensor-core operands"),
                   wl.Q4_K: ("q4_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
-                            else "q4_k weights, f16 tensor-core operands")}[w.w_dtype],
+                            else "q4_k weights, f16 tensor-core operands"),
+                  wl.FP8: ("fp8 e4m3 weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
+                           else "fp8 e4m3 weights, f16 tensor-core operands")}[w.w_dtype],
         "data": "synthetic", "config": config_dict(w, T, layers, args),
         "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s", "mode": e2e_mode, **e2e_alt,
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

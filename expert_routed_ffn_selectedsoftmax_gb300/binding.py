@@ -16,8 +16,8 @@ import torch
 
 from . import build as _build
 
-MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K = 0, 1, 2, 3, 4, 5
-PACKED = (MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K)   # storage types moe_forward takes repacked
+MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K, MOE_FP8 = 0, 1, 2, 3, 4, 5, 6
+PACKED = (MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K, MOE_FP8)   # storage types moe_forward takes repacked
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_PATH_DECODE_SIMT = 0, 1, 2, 3
 MOE_SCORE_SELECTED_SOFTMAX, MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -28,6 +28,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ("moe_status_str", "moe_version", "moe_route", "moe_route_scored", "moe_permute",
            "moe_q8_0_packed_size", "moe_pack_q8_0", "moe_q4_a64_packed_size", "moe_pack_q4_a64",
            "moe_q4_k_packed_size", "moe_pack_q4_k", "moe_q6_k_packed_size", "moe_pack_q6_k",
+           "moe_fp8_packed_size", "moe_pack_fp8",
            "moe_workspace_size", "moe_forward",
            "moe_forward_profiled", "moe_forward_scored", "moe_ffn_dense", "moe_forward_noalloc",
            "moe_workspace_views", "moe_forward_expire_wait", "moe_check", "moe_check_noalloc")
@@ -104,6 +105,10 @@ def _declare(L):
     L.moe_q6_k_packed_size.restype = sz
     L.moe_pack_q6_k.argtypes = [vp, ll, i, vp, vp]
     L.moe_pack_q6_k.restype = i
+    L.moe_fp8_packed_size.argtypes = [ll, i]
+    L.moe_fp8_packed_size.restype = sz
+    L.moe_pack_fp8.argtypes = [vp, ll, i, vp, vp]
+    L.moe_pack_fp8.restype = i
     L.moe_workspace_size.argtypes = [i, i, i, i, i, i, i]
     L.moe_workspace_size.restype = sz
     L.moe_forward.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, i, i, vp, vp, sz, i, vp]
@@ -254,6 +259,23 @@ def moe_pack_q6_k(blocks: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
     return packed
 
 
+def moe_fp8_packed_size(rows: int, cols: int) -> int:
+    return int(load_library().moe_fp8_packed_size(rows, cols))
+
+
+def moe_pack_fp8(rows_in: torch.Tensor, rows: int, cols: int) -> torch.Tensor:
+    """Repack fp8 rows {fp32 scale, E4M3 codes} (uint8 device tensor,
+    rows*(4+cols) bytes) into the E4M3 plane and row scales moe_forward takes."""
+    L = load_library()
+    n = moe_fp8_packed_size(rows, cols)
+    if n == 0 and rows != 0:
+        raise MoeError(1, "moe_fp8_packed_size")
+    packed = torch.empty(max(n, 256), dtype=torch.uint8, device=rows_in.device)
+    _check(L.moe_pack_fp8(_ptr(rows_in), rows, cols, _ptr(packed), _stream(rows_in)),
+           "moe_pack_fp8")
+    return packed
+
+
 def moe_workspace_size(T: int, d: int, E: int, k: int, F: int, act_dt: int, w_dt: int) -> int:
     return int(load_library().moe_workspace_size(T, d, E, k, F, act_dt, w_dt))
 
@@ -267,8 +289,9 @@ def moe_forward(x: torch.Tensor, w_router: torch.Tensor, sel_bias: Optional[torc
     """The whole MoE layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [E,F,d], [E,F,d], [E,d,F]; or, with
-    w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K / MOE_Q6_K, uint8 buffers from moe_pack_q8_0 /
-    moe_pack_q4_a64 / moe_pack_q4_k / moe_pack_q6_k (then F is required).
+    w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K / MOE_Q6_K / MOE_FP8, uint8 buffers from
+    moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k / moe_pack_q6_k / moe_pack_fp8 (then F is
+    required).
     events: optional sequence of 6 torch.cuda.Event(enable_timing=True), recorded
     at the stage boundaries (moe_forward_profiled).
     scoring: a MOE_SCORE_* mode (moe_forward_scored when not SelectedSoftmax).
@@ -321,8 +344,9 @@ def moe_ffn_dense(x: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor,
     """A dense SwiGLU FFN layer -> out fp32 [T, d].
 
     Weights: float32/bfloat16 tensors [F,d], [F,d], [d,F] (or [1,F,d] ...); or,
-    with w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K / MOE_Q6_K, uint8 buffers from moe_pack_q8_0 /
-    moe_pack_q4_a64 / moe_pack_q4_k / moe_pack_q6_k (then F is required).
+    with w_dtype=MOE_Q8_0 / MOE_Q4_A64 / MOE_Q4_K / MOE_Q6_K / MOE_FP8, uint8 buffers from
+    moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k / moe_pack_q6_k / moe_pack_fp8 (then F is
+    required).
     """
     L = load_library()
     T, d = x.shape

@@ -42,7 +42,7 @@ bool scoring_ok(int scoring)
 bool weights_ok(int act_dt, int w_dt)
 {
     if (act_dt == MOE_F32) return w_dt == MOE_F32;
-    return w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt);
+    return w_dt == MOE_BF16 || is_conv(w_dt);
 }
 
 // Largest d the router kernel can stage (one token of fp32 in <= 200 KB).
@@ -72,7 +72,7 @@ struct WsLayout {
 
 bool prefill_capable(int act_dt, int w_dt, int d, int F)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt)) &&
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_conv(w_dt)) &&
            d % 256 == 0 && F % 128 == 0;
 }
 
@@ -94,7 +94,7 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.tile_cnt = take(4 * (size_t)(T > 0 ? T : 1) * (size_t)E);   // <= one tile per token
     L.h = take(4 * n * (size_t)F);            // fp32 (decode); prefill uses 2 bytes/element
     // the decode_tc_capable() shape/dtype conditions, without the driver query
-    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) && d % 128 == 0 &&
+    L.dtc = act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_conv(w_dt)) && d % 128 == 0 &&
             F % 128 == 0 && n <= (size_t)kDecodeTcMaxRows;
     L.xp = (prefill_capable(act_dt, w_dt, d, F) || L.dtc) ? take(2 * n * (size_t)d) : off;
     L.pgu = L.pd = L.flags = off;
@@ -135,7 +135,7 @@ moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, con
     if (st != MOE_OK) return st;
     if (F <= 0 || F % 8) return MOE_ERR_INVALID_ARG;
     if (!weights_ok(act_dt, w_dt)) {
-        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt))
+        return (w_dt == MOE_F32 || w_dt == MOE_BF16 || is_conv(w_dt))
                    ? MOE_ERR_UNSUPPORTED
                    : MOE_ERR_INVALID_ARG;
     }
@@ -153,7 +153,7 @@ moe_status forward_args_check(const void *x, moe_dtype act_dt, int T, int d, con
     if (!w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
     if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
         return MOE_ERR_INVALID_ARG;
-    if (is_q8p(w_dt) || is_q4(w_dt)) {
+    if (is_conv(w_dt)) {
         const uintptr_t m = 255u;
         if ((reinterpret_cast<uintptr_t>(w_gate) & m) || (reinterpret_cast<uintptr_t>(w_up) & m) ||
             (reinterpret_cast<uintptr_t>(w_down) & m))
@@ -281,6 +281,22 @@ moe_status moe_pack_q6_k(const void *blocks, long long rows, int cols, void *pac
     if (!blocks || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
         return MOE_ERR_INVALID_ARG;
     cudaError_t e = launch_pack_q6_k(blocks, rows, cols, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_fp8_packed_size(long long rows, int cols)
+{
+    if (rows < 0 || cols <= 0) return 0;
+    return align_up((size_t)rows * cols, 256) + (size_t)rows * 4;
+}
+
+moe_status moe_pack_fp8(const void *rows_in, long long rows, int cols, void *packed, moe_stream stream)
+{
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!rows_in || !packed || (reinterpret_cast<uintptr_t>(packed) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    cudaError_t e = launch_pack_fp8(rows_in, rows, cols, packed, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -462,12 +478,12 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
     // the clustered router writes grouped rows only as fp16, for the 4-bit
     // tensor-core decode kernels, and only for up to 16 tokens: beyond that a
     // separate gather kernel writes them sooner than the router's owners do
-    const bool router_rows = (is_q4(w_dt) || is_q8p(w_dt)) && T <= kRouteSmallRowsMaxT;
+    const bool router_rows = is_conv(w_dt) && T <= kRouteSmallRowsMaxT;
     ra.xp = ((use_prefill || (use_dtc && !use_fused)) && act16 && (!fused_small || router_rows)) ? ws + L.xp
                                                                                                 : nullptr;
     // the Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels take fp16
     // rows (scaled)
-    ra.xp_fp16 = is_q8p(w_dt) || is_q4(w_dt);
+    ra.xp_fp16 = is_conv(w_dt);
     ra.xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
     ra.out_zero = (zero_out && !use_prefill) ? out : nullptr;   // the GEMM path zeroes its own
     // the fused decode kernel's flags and ticket start at zero
@@ -562,7 +578,7 @@ moe_status forward_impl(const void *x, moe_dtype act_dt, int T, int d, const voi
         a.perm_w = perm_w;
         int32_t *xexp = reinterpret_cast<int32_t *>(ws + L.xexp);
         a.xexp = xexp;
-        const int conv = is_q4(w_dt) || is_q8p(w_dt);   // converted weights: fp16 token rows
+        const int conv = is_conv(w_dt);   // converted weights: fp16 token rows
         if (fused_small && !conv) {
             a.x_gather = x;   // (the converted-weight kernels take fp16 token rows by TMA from xp)
         } else if (!xp_ready &&

@@ -71,6 +71,8 @@ template <> struct RawW<__nv_bfloat16> { uint4 a; };
 struct Q8Tag {};   // Q8_0 planes: int8 q plane + fp16 scale per 32 values
 template <> struct RawW<Q8Tag> { uint2 q; float s; };
 struct Q4Tag {};   // affine 4-bit planes: codes + fp16 scale and bias per 64 values
+struct F8Tag {};   // fp8 planes: E4M3 codes + fp32 scale per row
+template <> struct RawW<F8Tag> { uint2 q; float s; };
 template <> struct RawW<Q4Tag> { uint32_t q; float s, b, z; };
 
 // Weight matrix view: row-major [rows, cols] in one of the storage types.
@@ -153,6 +155,43 @@ __host__ __device__ __forceinline__ constexpr bool is_q4(int w_dt) { return w_dt
 // with a scale per 32 values, Q6_K repacked with one per 16
 __host__ __device__ __forceinline__ constexpr bool is_q8p(int w_dt) { return w_dt == MOE_Q8_0 || w_dt == MOE_Q6_K; }
 __host__ __device__ __forceinline__ constexpr int q8_group(int w_dt) { return w_dt == MOE_Q6_K ? 16 : 32; }
+// fp8 (E4M3) planes: code plane [rows, cols], then one fp32 scale per row at
+// align256(rows * cols)
+__host__ __device__ __forceinline__ constexpr bool is_fp8(int w_dt) { return w_dt == MOE_FP8; }
+// converted weights (fp16 operands on the tensor cores): 4-bit tiles, 8-bit planes
+__host__ __device__ __forceinline__ constexpr bool is_conv(int w_dt) { return is_q4(w_dt) || is_q8p(w_dt) || is_fp8(w_dt); }
+
+// two E4M3 codes (low byte: the first) -> fp16x2 (low half: the first), exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two)
+{
+    uint32_t out;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(two));
+    return out;
+}
+
+// fp8 view: q points at the E4M3 plane [rows, cols]; `scales` (fp32 [rows])
+// follow at align256(rows * cols).  Set by the host.
+template <> struct WView<F8Tag> {
+    const uint8_t *q;
+    const float *scales;
+    size_t cols;
+    __device__ __forceinline__ void load(size_t row, int col, RawW<F8Tag> &r) const
+    {
+        r.q = ld_stream_u2(q + row * cols + col);
+        r.s = scales[row];
+    }
+    __device__ __forceinline__ static void cvt(const RawW<F8Tag> &r, Chunk8 &c)
+    {
+        const uint32_t w[2] = {r.q.x, r.q.y};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+            c.v[2 * i] = f.x * r.s;
+            c.v[2 * i + 1] = f.y * r.s;
+        }
+    }
+};
 __host__ __device__ __forceinline__ constexpr int q4_gpr(int w_dt) { return w_dt == MOE_Q4_K ? 2 : 1; }
 constexpr int kQ4TileRows = 128, kQ4ScaleOff = 4096;
 constexpr int kQ4TileBytes = 4608, kQ4BiasOff = 4352;   // one group per row (affine 4-bit)

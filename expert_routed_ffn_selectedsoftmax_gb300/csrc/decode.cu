@@ -369,6 +369,20 @@ cudaError_t launch_decode_experts(const DecodeArgs &a, cudaStream_t stream)
                                               view4(a.w_up, (long long)a.E * a.F, a.d),
                                               view4(a.w_down, (long long)a.E * a.d, a.F), stream);
     }
+    if (is_fp8(a.w_dt)) {
+        // fp8 planes: E4M3 plane, then the fp32 row scales at align256(rows*cols)
+        auto view8 = [](const void *p, long long rows, int cols) {
+            WView<F8Tag> v;
+            v.q = static_cast<const uint8_t *>(p);
+            v.scales = reinterpret_cast<const float *>(static_cast<const char *>(p) +
+                                                       align_up((size_t)rows * cols, 256));
+            v.cols = (size_t)cols;
+            return v;
+        };
+        return launch_t<__nv_bfloat16, F8Tag>(a, view8(a.w_gate, (long long)a.E * a.F, a.d),
+                                              view8(a.w_up, (long long)a.E * a.F, a.d),
+                                              view8(a.w_down, (long long)a.E * a.d, a.F), stream);
+    }
     // Q8_0 / Q6_K packed planes: q plane, then the fp16 scales at align256(rows*cols)
     const int group = q8_group(a.w_dt);
     auto view = [group](const void *p, long long rows, int cols) {

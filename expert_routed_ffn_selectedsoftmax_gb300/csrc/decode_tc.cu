@@ -172,6 +172,7 @@ struct Params {
     int groups;            // W4: K / 64, tiles per row tile
     int gpr;               // W4: affine groups per tile row (1 affine 4-bit, 2 Q4_K)
     int cl;                // cluster mode: CTAs per cluster (= KS); 0 otherwise
+    const float *wsc[2];   // fp8: fp32 row scales of the matrices (GATEUP: gate, up; DOWN: down)
 };
 
 struct Ctl {
@@ -306,8 +307,10 @@ __device__ __forceinline__ void build_units(Ctl &c, const Params &p, bool offset
 // is one contiguous copy from p.w4[m], converted to fp16 by warps 6-9.
 // WQ: the weight storage, fixed at compile time: 0 bf16; 1 affine 4-bit and
 // 2 Q4_K tiles (1 or 2 affine groups per tile row); 3 Q8_0 and 4 Q6_K 8-bit
-// planes (a scale per 32 or 16 values).  tm_s0/tm_s1: the 8-bit planes' scale
-// maps (GATEUP: gate, up; DOWN: down), unused otherwise.
+// planes (a scale per 32 or 16 values); 5 fp8 planes (E4M3 codes widened to
+// fp16 exactly; each row's fp32 scale, p.wsc, multiplies its sums in the
+// epilogue).  tm_s0/tm_s1: the 8-bit planes' scale maps (GATEUP: gate, up;
+// DOWN: down), unused otherwise.
 template <int MODE, bool GATHER, int WQ, bool CL = false>
 __global__ void __launch_bounds__(GATHER || WQ ? THREADS_GATHER : THREADS, CTAS_PER_SM)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
@@ -315,10 +318,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                  const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
                  const Params p)
 {
-    constexpr bool Q8P = WQ == 3 || WQ == 4;   // 8-bit planes
+    constexpr bool Q8P = WQ == 3 || WQ == 4;   // 8-bit planes with fp16 scale planes
+    constexpr bool FP8 = WQ == 5;              // fp8 planes: row scales applied to the sums
+    constexpr bool P8 = Q8P || FP8;            // 8-bit tiles by TMA
     constexpr bool W4 = WQ != 0;               // converted weights (4- or 8-bit): fp16 A in TMEM
     static_assert(!(GATHER && W4), "converted weights take the token rows by TMA");
-    using RG = Ring<Q8P ? 2 : (W4 ? 1 : 0)>;
+    using RG = Ring<P8 ? 2 : (W4 ? 1 : 0)>;
     constexpr int GPR = WQ == 2 ? 2 : 1;       // 4-bit tiles: affine groups per tile row
     constexpr int NSB8 = WQ == 4 ? 4 : 2;      // 8-bit planes: scale blocks per k-block
     constexpr int SCB8 = NSB8 * 128 * 2;       //   their bytes per 128-row tile
@@ -348,9 +353,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
-        if (!W4 || Q8P)
+        if (!W4 || P8)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w0)) : "memory");
-        if (MODE == GATEUP && (!W4 || Q8P))
+        if (MODE == GATEUP && (!W4 || P8))
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w1)) : "memory");
         if (Q8P) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s0)) : "memory");
@@ -417,21 +422,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             const CUtensorMap *bmap = it.nt == 16 ? &tm_b16 : &tm_b32;
             const uint32_t bytes = A_BYTES + (GATHER ? 0 : it.nt * BK * 2);
             const int wrow = it.e * p.R + it.rt * BM;
-            if constexpr (Q8P) {
+            if constexpr (P8) {
                 const int nst = w4_stages<CL>(p, it);
                 for (int st = 0; st < nst; ++st, ++it_k) {
                     const int s = it_k % STAGES;
                     if (!mbar_wait(&c.empty[s], ((it_k / STAGES) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                     const int np = w4_parts(p, it, st), ntok = p.fused ? 1 : np;
-                    mbar_expect_tx(&c.full[s], (uint32_t)(np * (Q8_TILE + SCB8) + ntok * it.nt * BK * 2));
+                    mbar_expect_tx(&c.full[s], (uint32_t)(np * (Q8_TILE + (Q8P ? SCB8 : 0)) + ntok * it.nt * BK * 2));
                     uint8_t *sp = smem + s * SLOT;
                     for (int j = 0; j < np; ++j) {
                         int m, kb, tt;
                         w4_part<CL>(p, it, st, j, m, kb, tt);
                         const bool second = MODE == GATEUP && m == 1;
                         tma_load_2d(sp + WT_OFF8 + j * Q8_TILE, second ? &tm_w1 : &tm_w0, &c.full[s], kb * BK, wrow);
-                        tma_load_2d(sp + SC_OFF8 + j * SC8_MAX, second ? &tm_s1 : &tm_s0, &c.full[s], wrow,
-                                    kb * NSB8);
+                        if (Q8P)
+                            tma_load_2d(sp + SC_OFF8 + j * SC8_MAX, second ? &tm_s1 : &tm_s0, &c.full[s], wrow,
+                                        kb * NSB8);
                     }
                     for (int j = 0; j < ntok; ++j) {
                         int m, kb, tt;
@@ -579,9 +585,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                     break;
                 }
                 const int np = w4_parts(p, it, st);
-                if constexpr (Q8P) {
-                    // int8 row (64 values, 64-byte swizzled: 16-byte chunk c at
-                    // c ^ ((row >> 1) & 3)) -> fp16 (q * scale, one rounding)
+                if constexpr (P8) {
+                    // 8-bit row (64 values, 64-byte swizzled: 16-byte chunk c at
+                    // c ^ ((row >> 1) & 3)) -> fp16: int8 q * scale, one
+                    // rounding (Q8_0, Q6_K), or E4M3 widened exactly (fp8)
                     for (int j = 0; j < np; ++j) {
                         const uint8_t *wt = smem + s * SLOT + WT_OFF8 + j * Q8_TILE + row * 64;
                         const __half *scp = reinterpret_cast<const __half *>(smem + s * SLOT + SC_OFF8 + j * SC8_MAX);
@@ -589,11 +596,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
 #pragma unroll
                         for (int ch = 0; ch < 4; ++ch) {   // values 16ch .. 16ch+15
                             const uint4 v = *reinterpret_cast<const uint4 *>(wt + ((ch ^ ((row >> 1) & 3)) << 4));
-                            const __half2 sc2 = __half2half2(scp[(ch * NSB8 / 4) * 128 + row]);
-                            uint4 lo, hi;
-                            dequant16(v, sc2, lo, hi);
-                            o[8 * ch + 0] = lo.x; o[8 * ch + 1] = lo.y; o[8 * ch + 2] = lo.z; o[8 * ch + 3] = lo.w;
-                            o[8 * ch + 4] = hi.x; o[8 * ch + 5] = hi.y; o[8 * ch + 6] = hi.z; o[8 * ch + 7] = hi.w;
+                            if constexpr (FP8) {
+                                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    o[8 * ch + i] = e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
+                            } else {
+                                const __half2 sc2 = __half2half2(scp[(ch * NSB8 / 4) * 128 + row]);
+                                uint4 lo, hi;
+                                dequant16(v, sc2, lo, hi);
+                                o[8 * ch + 0] = lo.x; o[8 * ch + 1] = lo.y; o[8 * ch + 2] = lo.z; o[8 * ch + 3] = lo.w;
+                                o[8 * ch + 4] = hi.x; o[8 * ch + 5] = hi.y; o[8 * ch + 6] = hi.z; o[8 * ch + 7] = hi.w;
+                            }
                         }
                         tmem_st16(t_lane + cb * 64 + j * 32, *reinterpret_cast<const uint32_t(*)[16]>(&o[0]));
                         tmem_st16(t_lane + cb * 64 + j * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o[16]));
@@ -697,10 +711,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 uint32_t v[16];
 #pragma unroll
                 for (int mt = 0; mt < (MODE == GATEUP ? 2 : 1); ++mt) {
+                    // fp8: this row's scale multiplies its partial sums
+                    const float rs = FP8 ? p.wsc[mt][(size_t)it.e * p.R + it.rt * BM + row] : 1.f;
                     tmem_ld16(taddr + mt * 32, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) red[(mt * NTCL + q) * BM + row] = __uint_as_float(v[q]);
+                    for (int q = 0; q < 16; ++q) red[(mt * NTCL + q) * BM + row] = __uint_as_float(v[q]) * rs;
                 }
                 tc_fence_before();
                 mbar_arrive(&c.tempty[acc]);
@@ -761,6 +777,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                 uint16_t *dst = p.h + (size_t)it.row0 * p.R + wr;
                 // W4: lane j holds the scale exponent of token row j (fp16 h, scaled)
                 const int e_l = (W4 && lane < it.nrows) ? p.xexp[it.row0 + lane] : 0;
+                // fp8: this row's gate and up scales multiply its sums
+                const float gs = FP8 ? p.wsc[0][(size_t)it.e * p.R + wr] : 1.f;
+                const float us = FP8 ? p.wsc[1][(size_t)it.e * p.R + wr] : 1.f;
                 bool out_of_range = false;
                 for (int half = 0; half < it.nt / 16; ++half) {
                     uint32_t g[16], u[16];
@@ -773,7 +792,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
                         if (W4) {
                             const int ej = __shfl_sync(0xffffffffu, e_l, j);
                             if (j < it.nrows) {
-                                const float hv = swiglu_scaled(__uint_as_float(g[q]), __uint_as_float(u[q]), ej);
+                                const float hv = swiglu_scaled(__uint_as_float(g[q]) * gs, __uint_as_float(u[q]) * us, ej);
                                 out_of_range |= !(fabsf(hv) <= 65504.f);
                                 dst[(size_t)j * p.R] = __half_as_ushort(__float2half_rn(hv));
                             }
@@ -795,6 +814,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&c.tempty[acc]);          // accumulator is in registers now
+            if constexpr (FP8) {                  // this row's scale multiplies its sums
+                const float rs = p.wsc[MODE == GATEUP ? it.m : 0][(size_t)it.e * p.R + wr];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * rs);
+            }
             if (MODE == DOWN && p.direct) {
                 // token and routing weight of row j, held by lane j
                 int tok_l = lane < it.nrows ? p.perm_tok[it.row0 + lane] : 0;
@@ -962,7 +986,7 @@ int choose_splits(int kb_total, long long units)
 
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E)
 {
-    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) && d % 128 == 0 &&
+    return act_dt == MOE_BF16 && (w_dt == MOE_BF16 || is_conv(w_dt)) && d % 128 == 0 &&
            F % 128 == 0 && E <= kMaxExperts && tc_gemm_available();
 }
 
@@ -1013,13 +1037,13 @@ static long long cluster_chunks(int T, int E, int k)
 }
 int decode_tc_gateup_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
 {
-    if (!(w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) || decode_tc_gateup_fused(T, d, E, k, F, num_sms))
+    if (!(w_dt == MOE_BF16 || is_conv(w_dt)) || decode_tc_gateup_fused(T, d, E, k, F, num_sms))
         return 0;
     return cluster_size(cluster_chunks(T, E, k) * (F / dtc::BM), d / dtc::BK, num_sms);
 }
 int decode_tc_down_cluster(int T, int d, int E, int k, int F, int w_dt, int num_sms)
 {
-    if (!(w_dt == MOE_BF16 || is_q4(w_dt) || is_q8p(w_dt)) || k > 2 || decode_tc_down_direct(T, d, E, k, F))
+    if (!(w_dt == MOE_BF16 || is_conv(w_dt)) || k > 2 || decode_tc_down_direct(T, d, E, k, F))
         return 0;
     return cluster_size(cluster_chunks(T, E, k) * (d / dtc::BM), F / dtc::BK, num_sms);
 }
@@ -1033,7 +1057,7 @@ namespace dtc {
 // Dynamic shared memory of the kernels of weight storage WQ (CL: cluster mode).
 template <int WQ, bool CL> constexpr size_t smem_of()
 {
-    return smem_bytes<(WQ == 3 || WQ == 4) ? 2 : (WQ ? 1 : 0), CL>();
+    return smem_bytes<WQ >= 3 ? 2 : (WQ ? 1 : 0), CL>();
 }
 template <int WQ> constexpr int threads_of(bool gather) { return WQ || gather ? THREADS_GATHER : THREADS; }
 
@@ -1065,7 +1089,8 @@ template <int WQ>
 static cudaError_t launch_t(const DecodeTcArgs &a, cudaStream_t stream)
 {
     constexpr bool conv = WQ != 0;               // converted weights (fp16 operands)
-    constexpr bool q8p = WQ == 3 || WQ == 4;     // 8-bit planes
+    constexpr bool q8p = WQ == 3 || WQ == 4;     // 8-bit planes with fp16 scale planes
+    constexpr bool p8 = q8p || WQ == 5;          // 8-bit tiles (Q8_0, Q6_K, fp8)
     const int rows = a.T * a.k;
     int ks_gu, ks_d;
     decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
@@ -1080,14 +1105,15 @@ static cudaError_t launch_t(const DecodeTcArgs &a, cudaStream_t stream)
         return cudaErrorInvalidValue;
     m_sg = m_su = m_sd = m_h16;   // unused unless 8-bit planes
     const uint64_t gu_rows = (uint64_t)a.E * a.F, d_rows = (uint64_t)a.E * a.d;
-    if (q8p) {
+    if (p8) {
         const int g8 = WQ == 4 ? 16 : 32;
         if (!tc::make_map_u8(&m_wg, a.w_gate, gu_rows, a.d, BM, true) ||
             !tc::make_map_u8(&m_wu, a.w_up, gu_rows, a.d, BM, true) ||
-            !tc::make_map_u8(&m_wd, a.w_down, d_rows, a.F, BM, true) ||
-            !tc::make_scale_map(&m_sg, a.w_gate, gu_rows, a.d, g8, BM) ||
-            !tc::make_scale_map(&m_su, a.w_up, gu_rows, a.d, g8, BM) ||
-            !tc::make_scale_map(&m_sd, a.w_down, d_rows, a.F, g8, BM))
+            !tc::make_map_u8(&m_wd, a.w_down, d_rows, a.F, BM, true))
+            return cudaErrorInvalidValue;
+        if (q8p && (!tc::make_scale_map(&m_sg, a.w_gate, gu_rows, a.d, g8, BM) ||
+                    !tc::make_scale_map(&m_su, a.w_up, gu_rows, a.d, g8, BM) ||
+                    !tc::make_scale_map(&m_sd, a.w_down, d_rows, a.F, g8, BM)))
             return cudaErrorInvalidValue;
     } else if (conv) {
         m_wg = m_wu = m_wd = m_h16;   // unused: the 4-bit tiles are contiguous copies
@@ -1121,6 +1147,14 @@ static cudaError_t launch_t(const DecodeTcArgs &a, cudaStream_t stream)
     p.w4[1] = static_cast<const uint8_t *>(a.w_up);
     p.groups = a.d / 64;
     p.gpr = q4_gpr(a.w_dt);
+    // fp8: the row scales follow each E4M3 plane at align256(rows * cols)
+    auto row_scales = [](const void *w, uint64_t r, int cols) {
+        return reinterpret_cast<const float *>(static_cast<const char *>(w) + align_up((size_t)r * cols, 256));
+    };
+    if (WQ == 5) {
+        p.wsc[0] = row_scales(a.w_gate, gu_rows, a.d);
+        p.wsc[1] = row_scales(a.w_up, gu_rows, a.d);
+    }
     // upper bound on items: chunks <= n_exp + rows / NTMAX
     const long long chunks = n_exp + rows / NTMAX;
 
@@ -1181,6 +1215,7 @@ static cudaError_t launch_t(const DecodeTcArgs &a, cudaStream_t stream)
     p.K = a.F; p.R = a.d; p.n_mats = 1; p.kb_total = a.F / BK; p.rtiles = a.d / BM;
     p.w4[0] = p.w4[1] = static_cast<const uint8_t *>(a.w_down);
     p.groups = a.F / 64;
+    if (WQ == 5) p.wsc[0] = p.wsc[1] = row_scales(a.w_down, d_rows, a.F);
     p.fused = 0; p.h = nullptr;
     p.xg = nullptr;
     p.expire_ns = 0;
@@ -1217,6 +1252,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t stream)
     case MOE_Q4_K: return dtc::launch_t<2>(a, stream);
     case MOE_Q8_0: return dtc::launch_t<3>(a, stream);
     case MOE_Q6_K: return dtc::launch_t<4>(a, stream);
+    case MOE_FP8: return dtc::launch_t<5>(a, stream);
     default: return cudaErrorInvalidValue;
     }
 }

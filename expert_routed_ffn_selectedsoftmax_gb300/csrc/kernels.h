@@ -183,5 +183,8 @@ cudaError_t launch_pack_q4_a64(const void *blocks, long long rows, int cols, voi
 // q8.cu -- Q6_K super-blocks repacked into the 8-bit planes, one scale per 16 values
 cudaError_t launch_pack_q6_k(const void *blocks, long long rows, int cols, void *packed,
                              cudaStream_t stream);
+// q8.cu -- fp8 rows {fp32 scale, E4M3 codes} into the E4M3 plane and fp32 row scales
+cudaError_t launch_pack_fp8(const void *rows_in, long long rows, int cols, void *packed,
+                            cudaStream_t stream);
 
 }  // namespace moe

@@ -222,6 +222,37 @@ cudaError_t launch_pack_q6_k(const void *blocks, long long rows, int cols, void 
     return cudaGetLastError();
 }
 
+// fp8 rows {fp32 scale, E4M3 codes[cols]} (4 + cols bytes each, any
+// alignment) -> the E4M3 plane [rows, cols] and the fp32 row scales at
+// align256(rows * cols).  One thread per byte of the plane; the first byte's
+// thread of each row also moves its scale.
+__global__ void pack_fp8_kernel(const uint8_t *__restrict__ src, long long n, int cols,
+                                uint8_t *__restrict__ q, float *__restrict__ scales)
+{
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+         t += (long long)gridDim.x * blockDim.x) {
+        const long long row = t / cols;
+        const int c = (int)(t - row * cols);
+        const uint8_t *r = src + (size_t)row * (size_t)(cols + 4);
+        q[t] = r[4 + c];
+        if (c == 0)
+            scales[row] = __uint_as_float((uint32_t)r[0] | ((uint32_t)r[1] << 8) | ((uint32_t)r[2] << 16) |
+                                          ((uint32_t)r[3] << 24));
+    }
+}
+
+cudaError_t launch_pack_fp8(const void *rows_in, long long rows, int cols, void *packed, cudaStream_t stream)
+{
+    const long long n = rows * cols;
+    if (n == 0) return cudaSuccess;
+    uint8_t *q = static_cast<uint8_t *>(packed);
+    float *s = reinterpret_cast<float *>(static_cast<char *>(packed) + align_up((size_t)rows * cols, 256));
+    long long grid = (n + 255) / 256;
+    if (grid > 65535LL * 16) grid = 65535LL * 16;
+    pack_fp8_kernel<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint8_t *>(rows_in), n, cols, q, s);
+    return cudaGetLastError();
+}
+
 size_t q4_a64_packed_bytes(long long rows, int cols)
 {
     const long long tiles_r = (rows + kQ4TileRows - 1) / kQ4TileRows;

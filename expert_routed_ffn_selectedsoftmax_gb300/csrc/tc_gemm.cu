@@ -112,9 +112,10 @@ constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 
 // Weight storage of a variant: 16-bit, 8-bit planes with a scale per 32 values
-// (Q8_0) or per 16 (Q6_K, repacked), or 4-bit tiles (the last three through
-// converter warps).
-enum WKind { W16 = 0, WQ8 = 1, WQ4 = 2, WQ6 = 3 };
+// (Q8_0) or per 16 (Q6_K, repacked), 4-bit tiles, or fp8 planes (E4M3 codes;
+// each row's fp32 scale multiplies its sums in the epilogue) -- all but the
+// first through converter warps.
+enum WKind { W16 = 0, WQ8 = 1, WQ4 = 2, WQ6 = 3, WF8 = 4 };
 
 // Per-variant shared-memory layout: a ring of STAGES stages {A, this CTA's
 // part of B (16-bit), of Bq (int8) + its scales, or its packed 4-bit tiles},
@@ -128,7 +129,8 @@ template <int WQ, bool PAIR> struct Cfg {
     static constexpr int BQ_BYTES = WQ == WQ4 ? (BNL / kQ4TileRows) * kQ4KTileBytes : BNL * BK;
     // 8-bit planes' scales: per k-block of 64 columns, NSB blocks of BN/2 rows
     static constexpr int NSB = WQ == WQ6 ? 4 : 2;
-    static constexpr int SCL_BYTES = WQ == WQ4 ? 0 : SC_BYTES * (NSB / 2) / CL;
+    // (only the kinds with fp16 scale planes, Q8_0 and Q6_K, load scales)
+    static constexpr int SCL_BYTES = (WQ == WQ8 || WQ == WQ6) ? SC_BYTES * (NSB / 2) / CL : 0;
     static constexpr int STAGE = Q8 ? (A_BYTES + BQ_BYTES + SCL_BYTES + 1023) / 1024 * 1024
                                     : A_BYTES + B_BYTES;
     static constexpr int STAGES = Q8 ? (PAIR ? MOE_GEMM_PAIR_Q8_STAGES : MOE_GEMM_Q8_STAGES) : (PAIR ? 6 : 4);
@@ -167,6 +169,7 @@ struct Params {
     float *out_zero;          // GATEUP: `out` to zero for the down kernel's adds, or null
     long long zero4;          // float4 elements of out_zero
     uint32_t expire_ns;       // > 0: the producer's first wait gives up after this long (test hook)
+    const float *wsc[3];      // fp8: fp32 row scales of W_g, W_u, W_d
 };
 
 // (16-byte aligned size: the down epilogue's float4 staging rows follow it)
@@ -378,19 +381,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     if (PAIR) {
                         const CUtensorMap *bm = rank ? &tm_b1 : &tm_b0;
                         tma_load_2d(sb, bm, &c.full[s], kb * BK, grow);
-                        if (Q8) tma_load_2d(sc, rank ? &tm_s1 : &tm_s0, &c.full[s], grow, kb * C::NSB);
+                        if (C::SCL_BYTES > 0) tma_load_2d(sc, rank ? &tm_s1 : &tm_s0, &c.full[s], grow, kb * C::NSB);
                     } else {
                         constexpr int half_b = (Q8 ? C::BQ_BYTES : C::B_BYTES) / 2;
                         tma_load_2d(sb, &tm_b0, &c.full[s], kb * BK, grow);
                         tma_load_2d(sb + half_b, &tm_b1, &c.full[s], kb * BK, grow);
-                        if (Q8) {
+                        if (C::SCL_BYTES > 0) {
                             tma_load_2d(sc, &tm_s0, &c.full[s], grow, kb * C::NSB);
                             tma_load_2d(sc + C::SCL_BYTES / 2, &tm_s1, &c.full[s], grow, kb * C::NSB);
                         }
                     }
                 } else {
                     tma_load_2d(sb, &tm_b0, &c.full[s], kb * BK, drow);   // BNL-row box
-                    if (Q8) {
+                    if (C::SCL_BYTES > 0) {
                         tma_load_2d(sc, &tm_s0, &c.full[s], drow, kb * C::NSB);
                         if (!PAIR) tma_load_2d(sc + C::SCL_BYTES / 2, &tm_s0, &c.full[s], drow + BN / 2, kb * C::NSB);
                     }
@@ -507,6 +510,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     warp_arrive<PAIR>(&c.cfull[cb], lane);
                     continue;
                 }
+                if constexpr (WQ == WF8) {
+                    // E4M3 codes widened to fp16 exactly (the row scales act in the epilogue)
+#pragma unroll
+                    for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
+                        const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(bq + r * 64 + q * 16);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) o[i] = e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
+                        *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q) ^ (r & 7)) << 4)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(bo + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4)) =
+                            make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    fence_proxy_async_smem();
+                    warp_arrive<PAIR>(&c.cfull[cb], lane);
+                    continue;
+                }
 #pragma unroll
                 for (int pass = 0; pass < BNL / 8 / kConvWarps; ++pass) {
                     const int r = cw * (BNL / kConvWarps) + pass * 8 + rsub;
@@ -570,6 +592,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 // row's scale s; h / s^2 = (G/s) * sigmoid(G) * (U/s) is what fp16
                 // holds (its magnitude is bounded by the weights, whatever x is)
                 const float sx = (p.xexp && valid) ? ldexpf(1.f, p.xexp[grow]) : 1.f;
+                // fp8: the row scales of this thread's gate and up columns
+                const float *gsc = nullptr, *usc = nullptr;
+                if constexpr (WQ == WF8) {
+                    const size_t r0 = (size_t)e * p.F + nt * (BN / 2) + chalf * HC;
+                    gsc = p.wsc[0] + r0;
+                    usc = p.wsc[1] + r0;
+                }
                 bool out_of_range = false;
 #pragma unroll 1
                 for (int cc = 0; cc < HC; cc += 32) {
@@ -583,8 +612,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int hi = j >> 3, i0 = (2 * j) & 15;
-                        const float g0 = __uint_as_float(g[hi][i0]), g1 = __uint_as_float(g[hi][i0 + 1]);
-                        const float u0 = __uint_as_float(u[hi][i0]), u1 = __uint_as_float(u[hi][i0 + 1]);
+                        float g0 = __uint_as_float(g[hi][i0]), g1 = __uint_as_float(g[hi][i0 + 1]);
+                        float u0 = __uint_as_float(u[hi][i0]), u1 = __uint_as_float(u[hi][i0 + 1]);
+                        if constexpr (WQ == WF8) {
+                            const int cj = cc + 2 * j;
+                            g0 *= __ldg(gsc + cj); g1 *= __ldg(gsc + cj + 1);
+                            u0 *= __ldg(usc + cj); u1 *= __ldg(usc + cj + 1);
+                        }
                         if (p.h_fp16) {
                             const float h0 = __fdividef(g0 * u0, 1.0f + __expf(-sx * g0));
                             const float h1 = __fdividef(g1 * u1, 1.0f + __expf(-sx * g1));
@@ -626,11 +660,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 float *stg = reinterpret_cast<float *>(smem + C::CTL + sizeof(SmemCtl)) +
                              (warp - 2) * 32 * kStgRow;
                 const uint32_t tv = tbase + chalf * (BN / 2);
+                // fp8: the row scales of this warp's output columns
+                const float *dsc = WQ == WF8 ? p.wsc[2] + (size_t)e * p.d + nt * BN + chalf * (BN / 2) : nullptr;
 #pragma unroll 1
                 for (int cc = 0; cc < BN / 2; cc += 16) {
                     uint32_t v[16];
                     tmem_ld16(tv + cc, v);
                     tmem_ld_wait();
+                    if constexpr (WQ == WF8) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * __ldg(dsc + cc + i));
+                    }
                     float4 *srow = reinterpret_cast<float4 *>(stg + lane * kStgRow);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -688,7 +728,8 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "the staging rows after the control blo
 static_assert(smem_bytes<W16, true>() <= 232448 && smem_bytes<WQ8, true>() <= 232448 &&
                   smem_bytes<W16, false>() <= 232448 && smem_bytes<WQ8, false>() <= 232448 &&
                   smem_bytes<WQ4, true>() <= 232448 && smem_bytes<WQ4, false>() <= 232448 &&
-                  smem_bytes<WQ6, true>() <= 232448 && smem_bytes<WQ6, false>() <= 232448,
+                  smem_bytes<WQ6, true>() <= 232448 && smem_bytes<WQ6, false>() <= 232448 &&
+                  smem_bytes<WF8, true>() <= 232448 && smem_bytes<WF8, false>() <= 232448,
               "shared memory per CTA");
 
 // ------------------------------------------------------------------- host
@@ -763,7 +804,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 }  // namespace tc
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
-bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || is_q8p(w_dt) || is_q4(w_dt); }
+bool tc_gemm_supports(moe_dtype w_dt) { return w_dt == MOE_BF16 || is_conv(w_dt); }
 
 bool tc_gemm_prefer(int T, int d, int E, int k, int F)
 {
@@ -826,7 +867,7 @@ static int max_active_pairs()
 
 bool tc_gemm_pairs(moe_dtype w_dt)
 {
-    const bool q8 = is_q8p(w_dt), q4 = is_q4(w_dt);
+    const bool q8 = is_q8p(w_dt) || is_fp8(w_dt), q4 = is_q4(w_dt);
     if (MOE_GEMM_PAIR == 0 || (MOE_GEMM_PAIR == 1 && !q8 && !q4)) return false;
     if constexpr (MOE_GEMM_PAIR >= 2) {
         if (!q8 && !q4)
@@ -835,6 +876,8 @@ bool tc_gemm_pairs(moe_dtype w_dt)
     if (q4) return max_active_pairs<tc::GATEUP, tc::WQ4>() > 0 && max_active_pairs<tc::DOWN, tc::WQ4>() > 0;
     if (w_dt == MOE_Q6_K)
         return max_active_pairs<tc::GATEUP, tc::WQ6>() > 0 && max_active_pairs<tc::DOWN, tc::WQ6>() > 0;
+    if (is_fp8(w_dt))
+        return max_active_pairs<tc::GATEUP, tc::WF8>() > 0 && max_active_pairs<tc::DOWN, tc::WF8>() > 0;
     return q8 && max_active_pairs<tc::GATEUP, tc::WQ8>() > 0 && max_active_pairs<tc::DOWN, tc::WQ8>() > 0;
 }
 
@@ -886,8 +929,8 @@ static cudaError_t launch_gemms(const TcArgs &a, tc::Params p, const CUtensorMap
 cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
 {
     using namespace tc;
-    const bool q8 = is_q8p(a.w_dt), q4 = is_q4(a.w_dt);
-    const bool f16 = q8 || q4;   // fp16 operands (converted weights)
+    const bool q8 = is_q8p(a.w_dt), q4 = is_q4(a.w_dt), f8 = is_fp8(a.w_dt);
+    const bool f16 = q8 || q4 || f8;   // fp16 operands (converted weights)
     const int g8 = q8_group(a.w_dt);   // values per scale of the 8-bit planes
     if (!f16 && a.w_dt != MOE_BF16) return cudaErrorNotSupported;
     const int rows = a.T * a.k;
@@ -910,7 +953,7 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     bool ok = make_map(&m_xp, a.xp, rows, a.d, BM, act) && make_map(&m_h, a.h, rows, a.F, BM, act);
     if (q4) {
         m_wg = m_wu = m_wd = m_xp;   // unused: the 4-bit tiles are contiguous copies
-    } else if (q8) {
+    } else if (q8 || f8) {
         ok = ok && make_map_u8(&m_wg, a.w_gate, gu_rows, a.d, BN / 2) &&
              make_map_u8(&m_wu, a.w_up, gu_rows, a.d, BN / 2) &&
              make_map_u8(&m_wd, a.w_down, d_rows, a.F, wd_box);
@@ -943,6 +986,16 @@ cudaError_t launch_tc_experts(const TcArgs &a, cudaStream_t stream)
     p.out_zero = a.zero_out ? a.out : nullptr;
     p.zero4 = (long long)a.T * a.d / 4;
     p.expire_ns = a.expire_ns;
+    if (f8) {   // the fp32 row scales follow each E4M3 plane at align256(rows * cols)
+        auto rs = [](const void *w, uint64_t r, int cols) {
+            return reinterpret_cast<const float *>(static_cast<const char *>(w) + align_up((size_t)r * cols, 256));
+        };
+        p.wsc[0] = rs(a.w_gate, gu_rows, a.d);
+        p.wsc[1] = rs(a.w_up, gu_rows, a.d);
+        p.wsc[2] = rs(a.w_down, d_rows, a.F);
+        return pair ? launch_gemms<WF8, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
+                    : launch_gemms<WF8, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);
+    }
     if (q4)
         return pair ? launch_gemms<WQ4, true>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream)
                     : launch_gemms<WQ4, false>(a, p, m_xp, m_wg, m_wu, m_h, m_wd, m_sg, m_su, m_sd, stream);

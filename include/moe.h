@@ -28,8 +28,8 @@
  *    (1..256), k experts per token (1..min(E, 8)), F expert ffn width.
  *  - Activation storage (x, W_r): MOE_F32 or MOE_BF16; logits, routing
  *    weights and the output are fp32.  Expert weights: MOE_F32 (with F32
- *    activations), MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K or MOE_Q6_K (with BF16
- *    activations).
+ *    activations), MOE_BF16, MOE_Q8_0, MOE_Q4_A64, MOE_Q4_K, MOE_Q6_K or MOE_FP8
+ *    (with BF16 activations).
  *  - Calls on distinct workspaces and outputs are independent; there is no
  *    global mutable state.
  */
@@ -62,11 +62,12 @@ typedef enum {
     MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (see moe_check) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3, MOE_Q4_K = 4, MOE_Q6_K = 5 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_A64 = 3, MOE_Q4_K = 4, MOE_Q6_K = 5,
+               MOE_FP8 = 6 } moe_dtype;
 
 /* Which expert-compute kernels moe_forward uses.  AUTO picks by shape.
  * DECODE: few rows per expert -- tcgen05 weight-streaming kernels for bf16,
- *   4-bit (affine, Q4_K) and 8-bit-plane (Q8_0, Q6_K) weights (converted to
+ *   4-bit (affine, Q4_K) and 8-bit-plane (Q8_0, Q6_K, fp8) weights (converted to
  *   fp16 on chip) with d % 128 == 0, F % 128 == 0 and T*k <= 8192, otherwise
  *   the CUDA-core kernels.  PREFILL: tcgen05 grouped GEMMs.  DECODE_SIMT:
  *   always the CUDA-core decode kernels (the decode path for fp32). */
@@ -267,6 +268,30 @@ MOE_API moe_status moe_pack_q6_k(const void *blocks, long long rows, int cols, v
                                  moe_stream stream);
 
 /*
+ * fp8 expert weights (MOE_FP8): the serving configurations run "fp8" ("zonos2"
+ * sglang-omni cookbook, §Benchmark Results); the pages fix neither the 8-bit
+ * variant nor the scaling, and this library reads it as OCP E4M3 codes (sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, no infinities, NaN codes 0x7F
+ * and 0xFF, largest finite 448) with one fp32 scale per row (output channel;
+ * a per-tensor scale is the case of equal rows).  Input format: per row
+ * {fp32 scale (little endian), cols E4M3 codes}, 4 + cols bytes; value =
+ * scale * E4M3(code).
+ * moe_forward consumes them repacked into one buffer:
+ *   bytes [0, rows*cols)                            E4M3 plane [rows, cols]
+ *   bytes [align256(rows*cols), ... + 4*rows)       fp32 scale per row
+ * The tensor-core kernels (grouped GEMMs, decode) widen the codes to fp16
+ * exactly, multiply by fp16 token rows with fp32 accumulation (the same range
+ * rules as Q8_0) and apply each row's scale to its fp32 sums; the CUDA-core
+ * decode kernels compute scale * code in fp32.  d and F multiples of 8 (the
+ * tensor-core kernels: as for bf16).  moe_fp8_packed_size returns the buffer
+ * size (0 if rows < 0 or cols <= 0); moe_pack_fp8 repacks `rows_in` (device,
+ * any alignment) into `packed` (device, 256-byte aligned) on `stream`.
+ */
+MOE_API size_t moe_fp8_packed_size(long long rows, int cols);
+MOE_API moe_status moe_pack_fp8(const void *rows_in, long long rows, int cols, void *packed,
+                                moe_stream stream);
+
+/*
  * Bytes of device workspace moe_forward needs for these sizes (any path).
  * 0 on invalid sizes.  The workspace is scratch owned by the caller; its
  * first 256 bytes hold the device status word read by moe_check.
@@ -300,9 +325,9 @@ MOE_API moe_status moe_workspace_views(int T, int d, int E, int k, int F, moe_dt
 /*
  * moe_forward -- the whole layer, steps 1-5.
  *   x[T,d] (act_dt), w_router[E,d] (act_dt), sel_bias[E] fp32 or NULL,
- *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K / Q6_K:
- *   the buffers written by moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k /
- *   moe_pack_q6_k, 256-byte aligned),
+ *   w_gate[E,F,d], w_up[E,F,d], w_down[E,d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K / Q6_K /
+ *   fp8: the buffers written by moe_pack_q8_0 / moe_pack_q4_a64 / moe_pack_q4_k /
+ *   moe_pack_q6_k / moe_pack_fp8, 256-byte aligned),
  *   out[T,d] fp32 (overwritten).
  *   workspace: device scratch of at least moe_workspace_size() bytes,
  *   256-byte aligned; it must not be shared by calls that can overlap.
@@ -357,7 +382,7 @@ MOE_API moe_status moe_forward_scored(const void *x, moe_dtype act_dt, int T, in
  *   §Model architecture: dense FFN layers beside the MoE ones; "New Community
  *   Model: ZONOS3-Mini (Zyphra) - #1271", §Summary: layer 0 has a dense SwiGLU
  *   FFN).  No router: every token goes to the one expert with weight 1.
- *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K / Q6_K: packed
+ *   w_gate[F,d], w_up[F,d], w_down[d,F] in w_dt (Q8_0 / Q4_A64 / Q4_K / Q6_K / fp8: packed
  *   by the matching moe_pack_* with rows = F or d); other arguments as
  *   moe_forward, with a workspace of moe_workspace_size(T, d, 1, 1, F, act_dt,
  *   w_dt) bytes.

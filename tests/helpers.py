@@ -4,7 +4,8 @@ import numpy as np
 from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
 
 # Output tolerances: max|gpu - oracle| <= TOL * RMS(oracle output).
-TOL = {wl.F32: 1e-4, wl.BF16: 2e-2, wl.Q8_0: 2e-2, wl.Q4_A64: 2e-2, wl.Q4_K: 2e-2, wl.Q6_K: 2e-2}
+TOL = {wl.F32: 1e-4, wl.BF16: 2e-2, wl.Q8_0: 2e-2, wl.Q4_A64: 2e-2, wl.Q4_K: 2e-2, wl.Q6_K: 2e-2,
+       wl.FP8: 2e-2}
 # Routing indices must match exactly where the oracle's k-th vs (k+1)-th
 # ranking-score margin is at least this.
 MARGIN = 1e-3
@@ -23,10 +24,11 @@ def upload_layer(layer, dev):
     import expert_routed_ffn_selectedsoftmax_gb300 as pkg
     t = dict(x=to_dev(layer.x, dev), w_router=to_dev(layer.w_router, dev),
              bias=to_dev(layer.bias, dev))
-    if layer.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K):
+    if layer.w_dtype in (wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K, wl.FP8):
         E, F, d = layer.E, layer.F, layer.d
         pack = {wl.Q8_0: pkg.moe_pack_q8_0, wl.Q4_A64: pkg.moe_pack_q4_a64,
-                wl.Q4_K: pkg.moe_pack_q4_k, wl.Q6_K: pkg.moe_pack_q6_k}[layer.w_dtype]
+                wl.Q4_K: pkg.moe_pack_q4_k, wl.Q6_K: pkg.moe_pack_q6_k,
+                wl.FP8: pkg.moe_pack_fp8}[layer.w_dtype]
         t["w_gate"] = pack(to_dev(layer.w_gate.reshape(-1), dev), E * F, d)
         t["w_up"] = pack(to_dev(layer.w_up.reshape(-1), dev), E * F, d)
         t["w_down"] = pack(to_dev(layer.w_down.reshape(-1), dev), E * d, F)

@@ -125,6 +125,17 @@ def test_argument_errors_are_synchronous(lib):
     # int8 plane (padded to 256 bytes), then fp16 scales, one per 16 values
     assert lib.moe_q6_k_packed_size(3, 256) == 768 + 3 * 16 * 2
     assert lib.moe_q6_k_packed_size(2, 512) == 1024 + 2 * 32 * 2
+    assert fwd(act=0, wdt=6) == U                # fp8 takes bf16 activations
+    assert fwd(wdt=6, wg=vp(0x10010)) == I       # fp8 packed buffers are 256-byte aligned
+    assert fwd(wdt=7) == I                       # unknown weight storage
+    assert lib.moe_pack_fp8(fake, 4, 0, fake, None) == I
+    assert lib.moe_pack_fp8(fake, 4, 64, vp(0x10010), None) == I
+    assert lib.moe_pack_fp8(fake, 0, 64, fake, None) == 0   # no rows: nothing to do
+    assert lib.moe_fp8_packed_size(3, 0) == 0
+    assert lib.moe_fp8_packed_size(-1, 64) == 0
+    # E4M3 plane (padded to 256 bytes), then one fp32 scale per row
+    assert lib.moe_fp8_packed_size(3, 64) == 256 + 3 * 4
+    assert lib.moe_fp8_packed_size(130, 128) == 16640 + 130 * 4
     assert fwd(path=9) == I
     assert fwd(wg=None) == I
     assert fwd(ws=vp(0x10010)) == I              # workspace not 256-byte aligned

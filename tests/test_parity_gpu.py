@@ -149,6 +149,10 @@ SMALL = [
     (wl.BF16, wl.Q6_K, 5, 256, 8, 2, 256),      # Q6_K experts: 8-bit planes, a scale per 16
     (wl.BF16, wl.Q6_K, 70, 512, 16, 1, 512),    #   values (CUDA-core decode kernels)
     (wl.BF16, wl.Q6_K, 33, 1024, 64, 2, 256),
+    (wl.BF16, wl.FP8, 5, 256, 8, 2, 128),       # fp8 experts: E4M3 planes, a scale per row
+    (wl.BF16, wl.FP8, 70, 512, 16, 1, 192),     #   (F = 192: CUDA-core decode kernels)
+    (wl.BF16, wl.FP8, 33, 1024, 64, 2, 256),
+    (wl.BF16, wl.FP8, 300, 512, 16, 4, 384),
     (wl.BF16, wl.BF16, 5, 512, 64, 8, 128),     # few tokens: largest E and k of the small-batch router
     (wl.BF16, wl.BF16, 8, 2048, 33, 3, 128),    # few tokens: ragged E, longest rows
     (wl.BF16, wl.BF16, 40, 256, 256, 8, 128),   # the largest E and k the library takes
@@ -253,7 +257,8 @@ FULL_CASES = [("tiny_fp32", None), ("zonos3_mini_decode", None), ("zonos2_decode
               ("zonos2_decode_q4k", 8), ("zonos2_decode_q4k", 64), ("zonos2_prefill_q4k", None),
               ("zonos2_decode_q6k", 1), ("zonos2_decode_q6k", 8), ("zonos2_decode_q6k", 64),
               ("zonos2_prefill_q6k", None), ("zonos2_decode_q8", 1), ("zonos2_decode_q8", 8),
-              ("zonos2_decode_q8", 64)]
+              ("zonos2_decode_q8", 64), ("zonos2_decode_fp8", 1), ("zonos2_decode_fp8", 8),
+              ("zonos2_decode_fp8", 64), ("zonos2_prefill_fp8", None)]
 
 
 @pytest.mark.parametrize("seed", [2, 7, 13])
@@ -265,8 +270,8 @@ def test_forward_workloads_full(name, T, seed):
     the 1e-3 margin, near ties resolved validly, weights within 2e-6, counts,
     offsets, permutation and inverse bit-exact -- and every output row within
     the tolerance."""
-    if ("_q4" in name or "_q6" in name or "decode_q8" in name) and seed == 13:
-        pytest.skip("the 4-, 6- and 8-bit decode workloads run with two seeds")
+    if ("_q4" in name or "_q6" in name or "decode_q8" in name or "_fp8" in name) and seed == 13:
+        pytest.skip("the 4-, 6- and 8-bit workloads run with two seeds")
     layer = wl.make_layer(wl.WORKLOADS[name], seed=seed, T=T)
     out, r = gpu_forward_views(layer, DEV, path=0)
     check_routing_views(r, layer)
@@ -288,7 +293,8 @@ def test_forward_prefill_workloads_on_decode_path(name):
 
 @pytest.mark.parametrize("name", ["zonos3_mini_decode", "zonos2_decode", "zonos3_mini_prefill",
                                   "zonos2_prefill_q8", "zonos2_decode_q4", "zonos2_prefill_q4",
-                                  "zonos2_decode_q4k", "zonos2_prefill_q4k"])
+                                  "zonos2_decode_q4k", "zonos2_prefill_q4k", "zonos2_decode_fp8",
+                                  "zonos2_prefill_fp8"])
 def test_graph_replay_equals_direct_launch(name):
     """The benchmark times CUDA-graph replays of the layer (warm-up launches on a
     side stream, capture on that stream, replay): at full size, a replay writes
@@ -344,11 +350,11 @@ def test_forward_prefill_small_matches_oracle(T, d, E, k, F, wdt):
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.Q4_K, wl.Q6_K])
+@pytest.mark.parametrize("wdt", [wl.Q4_K, wl.Q6_K, wl.FP8])
 @pytest.mark.parametrize("T,d,E,k,F", [c for c in PREFILL_SMALL if c[1] % 256 == 0 and c[4] % 256 == 0])
 def test_forward_prefill_small_q4_k_matches_oracle(T, d, E, k, F, wdt):
-    """Q4_K and Q6_K experts on the grouped GEMMs (the shapes above with whole
-    256-value super-blocks along d and F)."""
+    """Q4_K, Q6_K and fp8 experts on the grouped GEMMs (the shapes above with
+    whole 256-value super-blocks along d and F)."""
     layer = wl.make_custom_layer(21, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16,
                                  w_dtype=wdt, bias_sd=0.5)
     out, r = gpu_forward_views(layer, DEV, path=PREFILL)
@@ -371,14 +377,14 @@ def test_prefill_one_expert_many_tiles():
     check_output(out, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64, wl.Q4_K, wl.Q6_K, wl.FP8])
 def test_prefill_and_decode_paths_agree(wdt):
     layer = wl.make_custom_layer(23, T=640, d=512, E=8, k=2, F=256, act_dtype=wl.BF16,
                                  w_dtype=wdt)
     t = upload_layer(layer, DEV)
     a = gpu_forward(layer, DEV, path=SIMT, t=t).cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(a ** 2))
-    for path in ((PREFILL,) if wdt in (wl.Q8_0, wl.Q6_K) else (DECODE, PREFILL)):
+    for path in ((PREFILL,) if wdt in (wl.Q8_0, wl.Q6_K) else (DECODE, PREFILL)):   # (fp8: both)
         b = gpu_forward(layer, DEV, path=path, t=t).cpu().numpy().astype(np.float64)
         assert np.abs(a - b).max() <= 2e-2 * rms
 
@@ -408,13 +414,14 @@ def test_decode_tc_deterministic_and_equivariant(T, k):
     (1, 2048, 16, 1, 2816),  # the ZONOS2 shape: 22 gate/up and 16 down units, clusters of 8
     (24, 512, 4, 2, 256),    # 48 rows: chunks of 16 rows, several per expert
 ])
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q4_A64, wl.Q4_K])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q4_A64, wl.Q4_K, wl.FP8])
 def test_decode_cluster_mode_deterministic_equivariant_and_matches_oracle(T, d, E, k, F, wdt):
     """Small decode batches run the tensor-core decode kernels in cluster
     mode: the K splits of a unit are reduced in shared memory across the
     cluster, in rank order.  Two runs give the same bits, permuting the
     tokens permutes the output rows bit for bit, and the result matches the
-    oracle (bf16, affine 4-bit and Q4_K weights)."""
+    oracle (bf16, affine 4-bit, Q4_K and fp8 weights: fp8 row scales act on
+    each split's sums before the reduction)."""
     layer = wl.make_custom_layer(30, T=T, d=d, E=E, k=k, F=F, act_dtype=wl.BF16, w_dtype=wdt,
                                  bias_sd=0.5)
     t = upload_layer(layer, DEV)
@@ -430,7 +437,7 @@ def test_decode_cluster_mode_deterministic_equivariant_and_matches_oracle(T, d, 
     check_output(a, layer, ref, idx_ref, margin, idx_gpu=r["topk_idx"])
 
 
-@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64])
+@pytest.mark.parametrize("wdt", [wl.BF16, wl.Q8_0, wl.Q4_A64, wl.FP8])
 @pytest.mark.parametrize("k,F", [(2, 128), (1, 1024)])   # (1, 1024): long K in the down GEMM
 def test_prefill_deterministic_and_equivariant(wdt, k, F):
     layer = wl.make_custom_layer(24, T=512, d=256, E=8, k=k, F=F, act_dtype=wl.BF16,
@@ -546,7 +553,9 @@ def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
     (PREFILL, 600, wl.Q4_A64, 8, 256),    # 4-bit grouped GEMMs
     (DECODE, 40, wl.Q4_K, 8, 256), (PREFILL, 600, wl.Q4_K, 8, 256),
     (DECODE, 40, wl.Q8_0, 8, 256), (DECODE, 128, wl.Q6_K, 64, 512),   # 8-bit planes, decode
-    (PREFILL, 600, wl.Q6_K, 8, 256)])   # Q6_K grouped GEMMs: scales per 16 values
+    (PREFILL, 600, wl.Q6_K, 8, 256),    # Q6_K grouped GEMMs: scales per 16 values
+    (DECODE, 40, wl.FP8, 8, 256), (DECODE, 128, wl.FP8, 64, 512),   # fp8: row scales on the sums
+    (PREFILL, 600, wl.FP8, 8, 256)])
 def test_fp16_operands_large_activations(path, T, wdt, E, F):
     """The Q8_0 grouped GEMMs and the 4-bit tensor-core decode kernels
     multiply fp16 operands.  Token rows whose magnitudes span 1e-2 .. 1e5 (h
@@ -587,7 +596,8 @@ def test_fp16_operands_large_activations(path, T, wdt, E, F):
     (wl.Q4_K, DECODE, 256, 4, 1, 256),
     (wl.Q4_K, PREFILL, 256, 4, 1, 256),
     (wl.Q6_K, PREFILL, 256, 4, 1, 256),
-    (wl.Q8_0, DECODE, 256, 4, 1, 256), (wl.Q6_K, DECODE, 128, 64, 2, 512)])
+    (wl.Q8_0, DECODE, 256, 4, 1, 256), (wl.Q6_K, DECODE, 128, 64, 2, 512),
+    (wl.FP8, DECODE, 256, 4, 1, 128), (wl.FP8, PREFILL, 256, 4, 1, 128)])
 def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     """Expert weights large enough that h leaves fp16's range even for
     normalised rows: the call reports MOE_ERR_DEVICE_CHECK instead of
@@ -599,7 +609,7 @@ def test_fp16_h_beyond_range_is_reported(wdt, path, T, E, k, F):
     rng = np.random.default_rng(6)
     big = lambda *s: (rng.standard_normal(s) * 4e3).astype(np.float32)
     quant = {wl.Q8_0: wl.q8_0_quantize, wl.Q4_A64: wl.q4_a64_quantize,
-             wl.Q4_K: wl.q4_k_quantize, wl.Q6_K: wl.q6_k_quantize}[wdt]
+             wl.Q4_K: wl.q4_k_quantize, wl.Q6_K: wl.q6_k_quantize, wl.FP8: wl.fp8_quantize}[wdt]
     layer.w_dtype = wdt
     layer.w_gate = quant(big(E, F, d))
     layer.w_up = quant(big(E, F, d))
@@ -621,10 +631,11 @@ def ctypes_check(pkg, ws):
                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("wdt,F", [(wl.Q4_A64, 384), (wl.Q4_K, 512), (wl.Q8_0, 384), (wl.Q6_K, 512)])
+@pytest.mark.parametrize("wdt,F", [(wl.Q4_A64, 384), (wl.Q4_K, 512), (wl.Q8_0, 384), (wl.Q6_K, 512),
+                                   (wl.FP8, 384)])
 @pytest.mark.parametrize("T,k", [(1, 1), (8, 1), (64, 1), (40, 2), (200, 4)])
 def test_q4_tensor_core_decode_reproducible_and_close_to_cuda_core(T, k, wdt, F):
-    """Affine 4-bit, Q4_K, Q8_0 and Q6_K experts on the tensor-core decode
+    """Affine 4-bit, Q4_K, Q8_0, Q6_K and fp8 experts on the tensor-core decode
     kernels (converter warps write the fp16 weights into tensor memory):
     bitwise reproducible, token-permutation equivariant, within tolerance of
     the oracle and of the CUDA-core kernels."""
@@ -769,3 +780,21 @@ def test_q6_k_pack_planes(rows, cols):
     assert n == off + scales.size * 2
     assert np.array_equal(got[:rows * cols], q.reshape(-1).view(np.uint8))
     assert np.array_equal(got[off:n], scales.reshape(-1).view(np.uint8))
+
+
+@pytest.mark.parametrize("rows,cols", [(130, 128), (3, 2048), (1, 8)])
+def test_fp8_pack_planes(rows, cols):
+    """moe_pack_fp8's output, byte for byte, against the layout its header
+    states, built here with numpy from the rows {fp32 scale, E4M3 codes}: the
+    E4M3 plane [rows, cols], then at align256(rows*cols) the fp32 scales."""
+    import expert_routed_ffn_selectedsoftmax_gb300 as pkg
+    rng = np.random.default_rng(rows + cols)
+    w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    src = wl.fp8_quantize(w)                       # [rows, 4 + cols]
+    n = pkg.moe_fp8_packed_size(rows, cols)
+    plane_end = (rows * cols + 255) // 256 * 256
+    assert n == plane_end + 4 * rows
+    got = pkg.moe_pack_fp8(torch.from_numpy(src.reshape(-1).copy()).to(DEV), rows, cols).cpu().numpy()[:n]
+    assert np.array_equal(got[:rows * cols], src[:, 4:].reshape(-1))
+    assert np.array_equal(got[plane_end:plane_end + 4 * rows].view(np.float32),
+                          src[:, 0:4].copy().view(np.float32)[:, 0])

@@ -56,9 +56,11 @@ CASES = [
     (DECODE_SPLIT, DECODE, (32, 256, 8, 4, 128), wl.BF16),     # k > 2
     (DECODE_SPLIT, DECODE, (8, 256, 8, 1, 128), wl.Q4_A64),    # 4-bit converter warps
     (DECODE_SPLIT, DECODE, (8, 256, 8, 1, 256), wl.Q8_0),      # 8-bit converter warps
+    (DECODE_SPLIT, DECODE, (8, 256, 8, 1, 256), wl.FP8),       # fp8 converter warps
     (DECODE_FUSED, DECODE, (128, 256, 64, 2, 512), wl.BF16),
     (GEMM, PREFILL, (600, 256, 4, 2, 128), wl.BF16),
     (GEMM, PREFILL, (600, 256, 4, 2, 128), wl.Q8_0),   # CTA pairs (clusters of two)
+    (GEMM, PREFILL, (600, 256, 4, 2, 128), wl.FP8),
 ]
 
 
