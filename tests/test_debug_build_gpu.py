@@ -25,8 +25,8 @@ DECODE, PREFILL, SIMT = 1, 2, 3
 DEVICE_CHECK = 6   # MOE_ERR_DEVICE_CHECK
 
 # (act, w, T, d, E, k, F, path): the one-launch decode kernel, the split-K
-# tensor-core decode kernels (bf16 and 4-bit, k = 4 through the combine), the
-# CUDA-core kernels, and the grouped GEMMs (bf16, Q8_0, 4-bit)
+# tensor-core decode kernels (bf16, 4-bit and fp8, k = 4 through the combine), the
+# CUDA-core kernels, and the grouped GEMMs (bf16, Q8_0, 4-bit, fp8)
 CASES = [
     (wl.BF16, wl.BF16, 128, 1024, 64, 2, 512, 0),
     (wl.BF16, wl.BF16, 40, 512, 16, 2, 384, DECODE),
@@ -37,6 +37,8 @@ CASES = [
     (wl.BF16, wl.BF16, 600, 256, 8, 2, 256, PREFILL),
     (wl.BF16, wl.Q8_0, 600, 256, 8, 2, 256, PREFILL),
     (wl.BF16, wl.Q4_A64, 600, 256, 8, 2, 256, PREFILL),
+    (wl.BF16, wl.FP8, 64, 512, 16, 1, 384, DECODE),
+    (wl.BF16, wl.FP8, 600, 256, 8, 2, 256, PREFILL),
 ]
 
 

@@ -524,6 +524,9 @@ def test_ffn_dense_matches_oracle(act, wdt, T, path):
     (SIMT, 40, wl.BF16, wl.Q8_0),
     (PREFILL, 600, wl.BF16, wl.BF16),   # grouped GEMMs
     (PREFILL, 600, wl.BF16, wl.Q8_0),
+    (DECODE, 64, wl.BF16, wl.FP8),      # fp8: row scales before the slot-order combine
+    (SIMT, 40, wl.BF16, wl.FP8),
+    (PREFILL, 600, wl.BF16, wl.FP8),
 ])
 def test_k_above_two_reproducible_and_equivariant(path, T, act, wdt, k):
     """With k > 2 every path adds a token's k expert outputs in slot order (no
