@@ -108,21 +108,35 @@ constexpr int THREADS_W4 = 320;                 // + 4 converter warps
 // ([64 / group][128] fp16, TMA), beside the fp16 token tiles; the converters
 // dequantise q * scale with one rounding to fp16 (dequant16) into the
 // A operand in tensor memory.
+// Ring depths of the converted kinds: in cluster mode the CTA also holds the
+// 16 KB reduction buffer, so its ring is one stage shorter than outside it (a
+// deeper 8-bit ring there would leave one CTA per SM).  The extra stage
+// outside cluster mode lets the producer run a stage further ahead of the
+// converters, whose stage is freed only once the MMAs have read its token
+// rows.
 #ifndef MOE_DTC_STAGES8
 #define MOE_DTC_STAGES8 3
 #endif
-constexpr int STAGES8 = MOE_DTC_STAGES8;
+#ifndef MOE_DTC_STAGES8_WIDE
+#define MOE_DTC_STAGES8_WIDE 4
+#endif
+#ifndef MOE_DTC_STAGES4_WIDE
+#define MOE_DTC_STAGES4_WIDE 5
+#endif
+constexpr int STAGES8 = MOE_DTC_STAGES8;            // cluster mode
+constexpr int STAGES8W = MOE_DTC_STAGES8_WIDE;      // outside cluster mode
+constexpr int STAGES4W = MOE_DTC_STAGES4_WIDE;
 constexpr int WT_OFF8 = 2 * 4096;               // two int8 tiles of 8 KB
 constexpr int Q8_TILE = 8192;
 constexpr int SC_OFF8 = WT_OFF8 + 2 * Q8_TILE;  // two scale boxes of up to 1 KB
 constexpr int SC8_MAX = 1024;
 constexpr int SLOT8 = SC_OFF8 + 2 * SC8_MAX;    // 26 KB
 static_assert(SLOT8 % 1024 == 0, "8-bit stage layout");
-constexpr int kStagesMax = STAGES4 > STAGES ? STAGES4 : STAGES;
-static_assert(STAGES8 <= kStagesMax, "barrier arrays");
-// ring of weight kind K: 0 bf16, 1 4-bit tiles, 2 8-bit planes
-template <int K> struct Ring {
-    static constexpr int NST = K == 0 ? STAGES : K == 1 ? STAGES4 : STAGES8;
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+constexpr int kStagesMax = cmax(cmax(STAGES, STAGES4), cmax(STAGES4W, cmax(STAGES8, STAGES8W)));
+// ring of weight kind K: 0 bf16, 1 4-bit tiles, 2 8-bit planes (CL: cluster mode)
+template <int K, bool CL = false> struct Ring {
+    static constexpr int NST = K == 0 ? STAGES : K == 1 ? (CL ? STAGES4 : STAGES4W) : (CL ? STAGES8 : STAGES8W);
     static constexpr int SLOTB = K == 0 ? SLOT : K == 1 ? SLOT4 : SLOT8;
     static constexpr int B_OFF = K == 0 ? A_BYTES : 0;  // token tile
     static constexpr int CTL = NST * SLOTB;
@@ -323,7 +337,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constan
     constexpr bool P8 = Q8P || FP8;            // 8-bit tiles by TMA
     constexpr bool W4 = WQ != 0;               // converted weights (4- or 8-bit): fp16 A in TMEM
     static_assert(!(GATHER && W4), "converted weights take the token rows by TMA");
-    using RG = Ring<P8 ? 2 : (W4 ? 1 : 0)>;
+    using RG = Ring<P8 ? 2 : (W4 ? 1 : 0), CL>;
     constexpr int GPR = WQ == 2 ? 2 : 1;       // 4-bit tiles: affine groups per tile row
     constexpr int NSB8 = WQ == 4 ? 4 : 2;      // 8-bit planes: scale blocks per k-block
     constexpr int SCB8 = NSB8 * 128 * 2;       //   their bytes per 128-row tile
@@ -969,8 +983,12 @@ combine_kernel(const float *__restrict__ pd, int KS, int rows_total, int d,
 
 template <int K, bool CL = false> constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)Ring<K>::CTL + kCtlBytes + (CL ? RED_BYTES : 0);
+    return 1024 + (size_t)Ring<K, CL>::CTL + kCtlBytes + (CL ? RED_BYTES : 0);
 }
+// two CTAs per SM (228 KB of shared memory, 1 KB reserved per CTA)
+static_assert(2 * (smem_bytes<1, false>() + 1024) <= 233472 && 2 * (smem_bytes<1, true>() + 1024) <= 233472 &&
+              2 * (smem_bytes<2, false>() + 1024) <= 233472 && 2 * (smem_bytes<2, true>() + 1024) <= 233472,
+              "two CTAs per SM");
 
 int choose_splits(int kb_total, long long units)
 {
