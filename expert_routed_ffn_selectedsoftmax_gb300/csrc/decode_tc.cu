@@ -123,9 +123,13 @@ constexpr int THREADS_W4 = 320;                 // + 4 converter warps
 #ifndef MOE_DTC_STAGES4_WIDE
 #define MOE_DTC_STAGES4_WIDE 5
 #endif
+#ifndef MOE_DTC_STAGES_WIDE
+#define MOE_DTC_STAGES_WIDE 4
+#endif
 constexpr int STAGES8 = MOE_DTC_STAGES8;            // cluster mode
 constexpr int STAGES8W = MOE_DTC_STAGES8_WIDE;      // outside cluster mode
 constexpr int STAGES4W = MOE_DTC_STAGES4_WIDE;
+constexpr int STAGESW = MOE_DTC_STAGES_WIDE;        // bf16 outside cluster mode
 constexpr int WT_OFF8 = 2 * 4096;               // two int8 tiles of 8 KB
 constexpr int Q8_TILE = 8192;
 constexpr int SC_OFF8 = WT_OFF8 + 2 * Q8_TILE;  // two scale boxes of up to 1 KB
@@ -133,10 +137,11 @@ constexpr int SC8_MAX = 1024;
 constexpr int SLOT8 = SC_OFF8 + 2 * SC8_MAX;    // 26 KB
 static_assert(SLOT8 % 1024 == 0, "8-bit stage layout");
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
-constexpr int kStagesMax = cmax(cmax(STAGES, STAGES4), cmax(STAGES4W, cmax(STAGES8, STAGES8W)));
+constexpr int kStagesMax = cmax(cmax(cmax(STAGES, STAGESW), STAGES4), cmax(STAGES4W, cmax(STAGES8, STAGES8W)));
 // ring of weight kind K: 0 bf16, 1 4-bit tiles, 2 8-bit planes (CL: cluster mode)
 template <int K, bool CL = false> struct Ring {
-    static constexpr int NST = K == 0 ? STAGES : K == 1 ? (CL ? STAGES4 : STAGES4W) : (CL ? STAGES8 : STAGES8W);
+    static constexpr int NST = K == 0 ? (CL ? STAGES : STAGESW) : K == 1 ? (CL ? STAGES4 : STAGES4W)
+                                                                : (CL ? STAGES8 : STAGES8W);
     static constexpr int SLOTB = K == 0 ? SLOT : K == 1 ? SLOT4 : SLOT8;
     static constexpr int B_OFF = K == 0 ? A_BYTES : 0;  // token tile
     static constexpr int CTL = NST * SLOTB;
@@ -986,7 +991,8 @@ template <int K, bool CL = false> constexpr size_t smem_bytes()
     return 1024 + (size_t)Ring<K, CL>::CTL + kCtlBytes + (CL ? RED_BYTES : 0);
 }
 // two CTAs per SM (228 KB of shared memory, 1 KB reserved per CTA)
-static_assert(2 * (smem_bytes<1, false>() + 1024) <= 233472 && 2 * (smem_bytes<1, true>() + 1024) <= 233472 &&
+static_assert(2 * (smem_bytes<0, false>() + 1024) <= 233472 && 2 * (smem_bytes<0, true>() + 1024) <= 233472 &&
+              2 * (smem_bytes<1, false>() + 1024) <= 233472 && 2 * (smem_bytes<1, true>() + 1024) <= 233472 &&
               2 * (smem_bytes<2, false>() + 1024) <= 233472 && 2 * (smem_bytes<2, true>() + 1024) <= 233472,
               "two CTAs per SM");
 
