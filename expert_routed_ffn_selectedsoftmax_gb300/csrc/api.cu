@@ -108,7 +108,7 @@ WsLayout ws_layout(int T, int d, int E, int k, int F, int act_dt, int w_dt)
     L.n_flags = 0;
     if (L.dtc) {
         int ks_gu = 1, ks_d = 1;
-        decode_tc_splits(T, d, E, k, F, &ks_gu, &ks_d);
+        decode_tc_splits(T, d, E, k, F, w_dt, &ks_gu, &ks_d);
         L.pgu = take(4 * (size_t)ks_gu * 2 * n * (size_t)F);
         L.pd = take(4 * (size_t)ks_d * n * (size_t)d);
         // the fused decode kernel's flags (whichever decode kernels run)

@@ -69,7 +69,7 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB weight tile
 constexpr int NTMAX = 32;                       // token rows per item
 constexpr int B_BYTES = NTMAX * BK * 2;         // 4 KB token tile (16 or 32 rows used)
 constexpr int SLOT = A_BYTES + B_BYTES;         // 20 KB per stage, 1024-aligned
-constexpr int KBMAX = 8;                        // k-blocks per item
+constexpr int KBMAX = 8;                        // k-blocks per item (bf16; kbmax_of)
 constexpr int THREADS = 192;
 constexpr int THREADS_GATHER = 320;             // + 4 warps that gather the token rows
 // 4-bit weights (W4: affine 4-bit or Q4_K, both as packed tiles with one or
@@ -996,10 +996,18 @@ static_assert(2 * (smem_bytes<0, false>() + 1024) <= 233472 && 2 * (smem_bytes<0
               2 * (smem_bytes<2, false>() + 1024) <= 233472 && 2 * (smem_bytes<2, true>() + 1024) <= 233472,
               "two CTAs per SM");
 
-int choose_splits(int kb_total, long long units)
+// Longest split-K item, in k-blocks, by weight storage: a converted kind's item
+// pays more to start (its first loads, then the first conversion before any
+// MMA), so its items are twice as long as bf16's (ZONOS2 decode T = 64: fp8
+// 71.6 -> 69.4, Q8_0 77.7 -> 75.5, affine 4-bit 77.4 -> 74.3 us per layer; at
+// T = 8, two waves of items instead of four, the 4-bit and Q8_0 layers are
+// ~1 % slower; bf16 was 2 % slower at T = 8 with longer items).
+int kbmax_of(int w_dt) { return w_dt == MOE_BF16 ? KBMAX : 2 * KBMAX; }
+
+int choose_splits(int kb_total, long long units, int kbmax)
 {
     long long ks = (kTargetItems + units - 1) / (units > 0 ? units : 1);
-    const int min_ks = (kb_total + KBMAX - 1) / KBMAX;   // keep each split <= KBMAX k-blocks
+    const int min_ks = (kb_total + kbmax - 1) / kbmax;   // keep each split <= kbmax k-blocks
     if (ks < min_ks) ks = min_ks;
     if (ks > kb_total) ks = kb_total;
     if (ks < 1) ks = 1;
@@ -1014,11 +1022,12 @@ bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E)
            F % 128 == 0 && E <= kMaxExperts && tc_gemm_available();
 }
 
-void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d)
+void decode_tc_splits(int T, int d, int E, int k, int F, int w_dt, int *ks_gu, int *ks_d)
 {
     const long long n_exp = (long long)(E < T * k ? E : T * k);
-    *ks_gu = dtc::choose_splits(d / dtc::BK, n_exp * 2 * (F / dtc::BM));
-    *ks_d = dtc::choose_splits(F / dtc::BK, n_exp * (d / dtc::BM));
+    const int kbmax = dtc::kbmax_of(w_dt);
+    *ks_gu = dtc::choose_splits(d / dtc::BK, n_exp * 2 * (F / dtc::BM), kbmax);
+    *ks_d = dtc::choose_splits(F / dtc::BK, n_exp * (d / dtc::BM), kbmax);
 }
 
 // Whole-K items stream at a few tens of GB/s per CTA: about 200 of them keep
@@ -1117,7 +1126,7 @@ static cudaError_t launch_t(const DecodeTcArgs &a, cudaStream_t stream)
     constexpr bool p8 = q8p || WQ == 5;          // 8-bit tiles (Q8_0, Q6_K, fp8)
     const int rows = a.T * a.k;
     int ks_gu, ks_d;
-    decode_tc_splits(a.T, a.d, a.E, a.k, a.F, &ks_gu, &ks_d);
+    decode_tc_splits(a.T, a.d, a.E, a.k, a.F, a.w_dt, &ks_gu, &ks_d);
 
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // token rows and h: fp16 when the weights are converted

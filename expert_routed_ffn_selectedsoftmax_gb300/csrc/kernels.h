@@ -133,7 +133,7 @@ struct DecodeTcArgs {
 };
 constexpr int kDecodeTcMaxRows = 8192;   // T*k above this uses the CUDA-core kernels
 bool decode_tc_capable(int act_dt, int w_dt, int d, int F, int E);
-void decode_tc_splits(int T, int d, int E, int k, int F, int *ks_gu, int *ks_d);
+void decode_tc_splits(int T, int d, int E, int k, int F, int w_dt, int *ks_gu, int *ks_d);
 // whole-K schedules: gate/up writes h itself; down adds into out (zeroed
 // beforehand when k > 1) -- no reduction or combine kernels
 bool decode_tc_gateup_fused(int T, int d, int E, int k, int F, int num_sms);
