@@ -447,6 +447,19 @@ def config_dict(w, T, layers, args):
             "dense": bool(args.dense)}
 
 
+def dtype_label(w, names):
+    """The arithmetic the path runs in: the storage of the expert weights and,
+    for quantised weights, whether the CUDA-core kernels (fp32) or the
+    tensor-core kernels (fp16 operands) run them."""
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    if w.w_dtype in (wl.F32, wl.BF16):
+        return {wl.F32: "f32", wl.BF16: "bf16"}[w.w_dtype]
+    fmt = {wl.Q8_0: "q8_0", wl.Q4_A64: "affine 4-bit", wl.Q4_K: "q4_k", wl.Q6_K: "q6_k",
+           wl.FP8: "fp8 e4m3"}[w.w_dtype]
+    how = "f32 CUDA-core arithmetic" if names["file"] == "decode.cu" else "f16 tensor-core operands"
+    return f"{fmt} weights, {how}"
+
+
 def scoring_mode(args):
     """moe_forward scoring argument (and the oracle's mode) for --scoring."""
     return {"selected_softmax": 0, "softmax": 1, "sigmoid": 2}[args.scoring]
@@ -997,17 +1010,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {wl.F32: "f32", wl.BF16: "bf16",
-                  wl.Q8_0: ("q8_0 weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
-                            else "q8_0 weights, f16 tensor-core operands"),
-                  wl.Q4_A64: ("affine 4-bit weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
-                              else "affine 4-bit weights, f16 tensor-core operands"),
-                  wl.Q6_K: ("q6_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
-                            else "q6_k weights, f16 tensor-core operands"),
-                  wl.Q4_K: ("q4_k weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
-                            else "q4_k weights, f16 tensor-core operands"),
-                  wl.FP8: ("fp8 e4m3 weights, f32 CUDA-core arithmetic" if names["file"] == "decode.cu"
-                           else "fp8 e4m3 weights, f16 tensor-core operands")}[w.w_dtype],
+        "dtype": dtype_label(w, names),
         "data": "synthetic", "config": config_dict(w, T, layers, args),
         "clocks": clk, "e2e": {"value": e2e_value, "unit": "tokens/s", "mode": e2e_mode, **e2e_alt,
                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -107,3 +107,31 @@ def test_reference_arm_prints_the_contract_line_on_rank_zero_only():
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
     assert j["config"]["workload"] == "tiny_fp32"
     assert _reference({"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_every_workload_has_its_labels_and_peaks():
+    """Every workload the benchmark can run (its side configurations and every
+    named workload at its own T) gets a config, a kernel selection, a dtype
+    label, a compute peak and nonzero expert bytes on the host, so that a new
+    weight storage cannot reach the GPU run without them."""
+    import argparse
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    from expert_routed_ffn_selectedsoftmax_gb300 import workloads as wl
+    args = argparse.Namespace(gpus=1, no_graph=False, scoring="selected_softmax", dense=False)
+    props = types.SimpleNamespace(multi_processor_count=152, clock_rate=2070000)
+    peaks = {"hbm_gbs": 6670.9, "bf16_tflops": 1943.5, "sm_max_mhz": 2070}
+    cases = [(name, T) for name, T, _, _ in bench.SIDE_WORKLOADS] + [(n, None) for n in wl.WORKLOADS]
+    for name, T in cases:
+        w = wl.WORKLOADS[name]
+        T = w.T if T is None else T
+        cfg = bench.config_dict(w, T, w.layers, args)
+        assert cfg["workload"] == name and cfg["w_dtype"] == wl.DTYPE_NAMES[w.w_dtype]
+        names = bench.expert_kernel_names(w, T, 152)
+        assert names["launches"] >= 1 and names["file"] in ("decode.cu", "decode_tc.cu", "decode_fused.cu",
+                                                            "tc_gemm.cu")
+        assert bench.dtype_label(w, names)
+        peak = bench.compute_peak(w, peaks, props, names)
+        assert peak[0] > 0
+        assert wl.weight_bytes_per_expert(w.d, w.F, w.w_dtype) > 0
