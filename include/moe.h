@@ -283,7 +283,8 @@ MOE_API moe_status moe_pack_q6_k(const void *blocks, long long rows, int cols, v
  * exactly, multiply by fp16 token rows with fp32 accumulation (the same range
  * rules as Q8_0) and apply each row's scale to its fp32 sums; the CUDA-core
  * decode kernels compute scale * code in fp32.  NaN codes (0x7F, 0xFF) are not
- * checked: they propagate into the outputs as NaN.  d and F multiples of 8 (the
+ * validated: they propagate into the outputs as NaN (some paths' range check on h
+ * may also report MOE_ERR_DEVICE_CHECK).  d and F multiples of 8 (the
  * tensor-core kernels: as for bf16).  moe_fp8_packed_size returns the buffer
  * size (0 if rows < 0 or cols <= 0); moe_pack_fp8 repacks `rows_in` (device,
  * any alignment) into `packed` (device, 256-byte aligned) on `stream`.
